@@ -1,0 +1,179 @@
+"""fp64 CPU oracle for the autoregressive KV-cache append + causal attention step.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package. The product path
+(``kv_cache_append_gb300``) never imports it and shares no code with it.
+
+The arithmetic lives in ``kvc_oracle.c`` (plain C loops in double precision,
+written from the page "Autoregressive KV-cache append and causal attention",
+Required behavior). This module only compiles that file with gcc, marshals
+arrays with ctypes and shapes the results.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "kvc_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libkvc_oracle.so")
+
+DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+FLAG_OVERFLOW = 1
+FLAG_MASK = 2
+
+
+def compile_library(src: str, out: str) -> str:
+    """gcc -O2 -fopenmp: one C file to one shared library."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-shared", "-fPIC", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile ``kvc_oracle.c`` into ``libkvc_oracle.so`` next to it."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(SOURCE)):
+        return _LIB_PATH
+    return compile_library(SOURCE, _LIB_PATH)
+
+
+def _host(t: torch.Tensor) -> torch.Tensor:
+    return t.detach().to("cpu").contiguous()
+
+
+def _ptr(t: torch.Tensor):
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else ctypes.c_void_p(0)
+
+
+def default_scale(D: int) -> float:
+    """Positive default scale 1/sqrt(D), D the query/key width."""
+    return 1.0 / math.sqrt(D)
+
+
+def _dims(query, key_cache, value_cache):
+    B, Hq, Q, D = query.shape
+    _, Hk, M, _ = key_cache.shape
+    Dv = value_cache.shape[-1]
+    return B, Hq, Hk, Q, D, Dv, M
+
+
+def _scale(options, D):
+    options = dict(options or {})
+    scale = float(options.pop("scale", default_scale(D)))
+    if options:
+        raise ValueError(f"unknown option keys: {sorted(options)}")
+    return scale
+
+
+class Oracle:
+    """One loaded build of ``kvc_oracle.c``."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        i64, vp, dbl = ctypes.c_int64, ctypes.c_void_p, ctypes.c_double
+        lib.kvo_step.restype = ctypes.c_int
+        lib.kvo_step.argtypes = [ctypes.c_int] + [i64] * 7 + [vp] * 7 + [dbl] + [vp] * 7
+        lib.kvo_rows.restype = ctypes.c_int
+        lib.kvo_rows.argtypes = [ctypes.c_int] + [i64] * 7 + [vp] * 7 + [dbl, vp, i64] + [vp] * 3
+        lib.kvo_widen_n.restype = None
+        lib.kvo_widen_n.argtypes = [ctypes.c_int, vp, i64, vp]
+        lib.kvo_threads.restype = ctypes.c_int
+        lib.kvo_threads.argtypes = []
+        self.lib = lib
+
+    def threads(self) -> int:
+        """OpenMP threads the oracle uses."""
+        return int(self.lib.kvo_threads())
+
+    def widen(self, t: torch.Tensor) -> np.ndarray:
+        """Exact widening of an fp32/bf16/fp16 tensor to float64 by the oracle's decoder."""
+        h = _host(t)
+        out = np.empty(h.numel(), dtype=np.float64)
+        self.lib.kvo_widen_n(DTYPE_CODES[h.dtype], _ptr(h), h.numel(), out.ctypes.data)
+        return out.reshape(tuple(h.shape))
+
+    def step(self, query, new_key, new_value, key_cache, value_cache, lengths, append_mask,
+             options: dict | None = None) -> dict:
+        """The whole step on the CPU in fp64.
+
+        Returns key_cache / value_cache (input dtype, the bytes the step
+        leaves), lengths (int64), attention [B,Hq,Q,M] and context
+        [B,Hq,Q,Dv] as float64 numpy arrays, and flags [B] (1 = overflow,
+        2 = non-prefix mask; a flagged row appends nothing).
+        """
+        q, nk, nv, kc, vc = (_host(x) for x in (query, new_key, new_value, key_cache,
+                                                 value_cache))
+        B, Hq, Hk, Q, D, Dv, M = _dims(q, kc, vc)
+        scale = _scale(options, D)
+        ln = _host(lengths).to(torch.int64)
+        mk = _host(append_mask).to(torch.uint8)
+        out_k = torch.empty_like(kc)
+        out_v = torch.empty_like(vc)
+        out_len = torch.empty(B, dtype=torch.int64)
+        att = np.zeros((B, Hq, Q, M), dtype=np.float64)
+        ctx = np.zeros((B, Hq, Q, Dv), dtype=np.float64)
+        flags = np.zeros(B, dtype=np.int32)
+        work = np.empty(max(1, self.threads()) * max(1, M), dtype=np.float64)
+        self.lib.kvo_step(DTYPE_CODES[q.dtype], B, Hq, Hk, Q, D, Dv, M, _ptr(q), _ptr(nk),
+                          _ptr(nv), _ptr(kc), _ptr(vc), _ptr(ln), _ptr(mk), scale, _ptr(out_k),
+                          _ptr(out_v), _ptr(out_len), att.ctypes.data, ctx.ctypes.data,
+                          flags.ctypes.data, work.ctypes.data)
+        return {"key_cache": out_k, "value_cache": out_v, "lengths": out_len,
+                "attention": att, "context": ctx, "flags": flags}
+
+    def rows(self, query, new_key, new_value, key_cache, value_cache, lengths, append_mask,
+             rows_bht, options: dict | None = None):
+        """Attention rows [n, M] and context rows [n, Dv] (float64) for the listed (b, h, t)."""
+        q, nk, nv, kc, vc = (_host(x) for x in (query, new_key, new_value, key_cache,
+                                                 value_cache))
+        B, Hq, Hk, Q, D, Dv, M = _dims(q, kc, vc)
+        scale = _scale(options, D)
+        ln = _host(lengths).to(torch.int64)
+        mk = _host(append_mask).to(torch.uint8)
+        idx = np.ascontiguousarray(np.asarray(rows_bht, dtype=np.int64).reshape(-1, 3))
+        n = idx.shape[0]
+        att = np.zeros((n, M), dtype=np.float64)
+        ctx = np.zeros((n, Dv), dtype=np.float64)
+        work = np.empty(max(1, self.threads()) * max(1, M), dtype=np.float64)
+        self.lib.kvo_rows(DTYPE_CODES[q.dtype], B, Hq, Hk, Q, D, Dv, M, _ptr(q), _ptr(nk),
+                          _ptr(nv), _ptr(kc), _ptr(vc), _ptr(ln), _ptr(mk), scale,
+                          idx.ctypes.data, n, att.ctypes.data, ctx.ctypes.data,
+                          work.ctypes.data)
+        return att, ctx
+
+
+_lock = threading.Lock()
+_default: Oracle | None = None
+
+
+def default() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def threads() -> int:
+    return default().threads()
+
+
+def widen(t):
+    return default().widen(t)
+
+
+def step(*args, **kw):
+    return default().step(*args, **kw)
+
+
+def rows(*args, **kw):
+    return default().rows(*args, **kw)

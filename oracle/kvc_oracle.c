@@ -1,0 +1,265 @@
+/*
+ * kvc_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, fp64 CPU statement of the autoregressive KV-cache append and
+ * causal attention step, written from the page "Autoregressive KV-cache append
+ * and causal attention" (biotorch, problems/kv_cache_attention_step), section
+ * "Required behavior". Only tests/, the package smoke check and bench.py's CPU
+ * baseline may load this library. It shares no code, header or constant with
+ * the CUDA implementation.
+ *
+ * What each function follows:
+ *   kvo_widen          exact widening of fp32 / bf16 / fp16 storage to double
+ *                      (IEEE 754 binary16 and the bfloat16 truncated-binary32
+ *                      formats, from their definitions).
+ *   kvo_append_count   "append_mask[B,Q] is bool and each row must be a prefix
+ *                      of True values followed by False. Its count n must
+ *                      satisfy length+n <= M" (Required behavior, bullet 3).
+ *                      A row outside that contract (non-prefix mask, length
+ *                      outside [0, M], length+n > M) is treated as n = 0 and
+ *                      flagged: this follows "Fixed-capacity KV cache"
+ *                      (aiengineeringfromscratch), Task: when append raises,
+ *                      the cache does not change.
+ *   kvo_step           the whole step: copy caches byte-wise, write new rows at
+ *                      slots length+t for the True slots (bullet 3), return the
+ *                      updated lengths (bullet 4), then for every query row the
+ *                      scaled scores, stable softmax over the allowed slots
+ *                      j <= old_length+t and j < new_length, attention and
+ *                      context = attention . updated_values (bullets 4-5);
+ *                      invalid rows (mask False) are all zero (bullet 4).
+ *   kvo_rows           the same attention/context for a list of (b,h,t) rows
+ *                      only, reading the updated cache through its definition
+ *                      (new row if length <= j < length+n, else old cache row).
+ *
+ * Precision: every element is widened exactly to double, dot products, max,
+ * exp, sums and the weighted value sum are taken in double, in slot order.
+ * Nothing is blocked, fused or reordered.
+ *
+ * Parity pins live in tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { KVO_F32 = 0, KVO_BF16 = 1, KVO_F16 = 2 };
+
+/* Per-batch-row flags written by kvo_step / kvo_append_count. */
+enum {
+    KVO_FLAG_OVERFLOW = 1, /* length < 0, length > M, or length + n > M */
+    KVO_FLAG_MASK = 2      /* append_mask row is not a True-prefix */
+};
+
+static int64_t elem_size(int dtype) { return dtype == KVO_F32 ? 4 : 2; }
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double half_bits_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24); /* subnormal: f * 2^-14 * 2^-10 */
+    } else if (e == 31) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + f), e - 25); /* (1 + f/1024) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32. */
+static double bf16_bits_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+double kvo_widen(int dtype, const void *base, int64_t i) {
+    if (dtype == KVO_F32) {
+        float f;
+        memcpy(&f, (const char *)base + 4 * i, 4);
+        return (double)f;
+    }
+    uint16_t u;
+    memcpy(&u, (const char *)base + 2 * i, 2);
+    return dtype == KVO_BF16 ? bf16_bits_to_double(u) : half_bits_to_double(u);
+}
+
+/* Decode n elements into out (used by the pins on the widening itself). */
+void kvo_widen_n(int dtype, const void *base, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = kvo_widen(dtype, base, i);
+}
+
+int64_t kvo_append_count(const uint8_t *mask_row, int64_t Q, int64_t length, int64_t M,
+                         int32_t *flags) {
+    int64_t n = 0;
+    while (n < Q && mask_row[n]) ++n;
+    int32_t f = 0;
+    for (int64_t t = n; t < Q; ++t)
+        if (mask_row[t]) f |= KVO_FLAG_MASK;
+    if (length < 0 || length > M || length + n > M) f |= KVO_FLAG_OVERFLOW;
+    if (flags) *flags = f;
+    return f ? 0 : n;
+}
+
+int kvo_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Element (b, head, row, d) of a dense [B, H, R, W] tensor. */
+static int64_t at4(int64_t H, int64_t R, int64_t W, int64_t b, int64_t h, int64_t r, int64_t d) {
+    return ((b * H + h) * R + r) * W + d;
+}
+
+/*
+ * Attention for query row (b, h, t).
+ * valid: t < n (the row's append slot is True); an invalid row is all zero.
+ * The cache row at slot j is new_key[b, kv, j - length] when
+ * length <= j < length + n_src, else key_cache[b, kv, j] (same for values).
+ * kvo_step passes the already-updated cache with n_src = 0; kvo_rows passes
+ * the input cache with n_src = n, which is the same row by definition.
+ * Allowed slots: j <= length + t, which is < length + n = new_length.
+ */
+static void attend_row(int dtype, int64_t Hq, int64_t Hk, int64_t Q, int64_t D, int64_t Dv,
+                       int64_t M, const void *query, const void *new_key, const void *new_value,
+                       const void *key_cache, const void *value_cache, int64_t length,
+                       int64_t n_src, int valid, double scale, int64_t b, int64_t h, int64_t t,
+                       double *att_row /* M */, double *ctx_row /* Dv */, double *scratch /* M */) {
+    for (int64_t j = 0; j < M; ++j) att_row[j] = 0.0;
+    for (int64_t e = 0; e < Dv; ++e) ctx_row[e] = 0.0;
+    if (!valid) return; /* invalid query row: zero attention and context */
+
+    const int64_t group = Hq / Hk;
+    const int64_t kv = h / group; /* query head h uses KV head floor(h/(Hq/Hk)) */
+    const int64_t last = length + t; /* allowed: j <= old_length + t (< new_length) */
+    const int64_t n = n_src;
+
+    double m = -INFINITY;
+    for (int64_t j = 0; j <= last; ++j) {
+        double s = 0.0;
+        for (int64_t d = 0; d < D; ++d) {
+            double qd = kvo_widen(dtype, query, at4(Hq, Q, D, b, h, t, d));
+            double kd = (j >= length && j < length + n)
+                            ? kvo_widen(dtype, new_key, at4(Hk, Q, D, b, kv, j - length, d))
+                            : kvo_widen(dtype, key_cache, at4(Hk, M, D, b, kv, j, d));
+            s += qd * kd;
+        }
+        s *= scale;
+        scratch[j] = s;
+        if (s > m) m = s;
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j <= last; ++j) {
+        scratch[j] = exp(scratch[j] - m);
+        l += scratch[j];
+    }
+    for (int64_t j = 0; j <= last; ++j) att_row[j] = scratch[j] / l;
+    for (int64_t j = 0; j <= last; ++j) {
+        for (int64_t e = 0; e < Dv; ++e) {
+            double ve = (j >= length && j < length + n)
+                            ? kvo_widen(dtype, new_value, at4(Hk, Q, Dv, b, kv, j - length, e))
+                            : kvo_widen(dtype, value_cache, at4(Hk, M, Dv, b, kv, j, e));
+            ctx_row[e] += att_row[j] * ve;
+        }
+    }
+}
+
+/*
+ * The whole step. Layouts are dense row-major:
+ *   query [B,Hq,Q,D], new_key [B,Hk,Q,D], new_value [B,Hk,Q,Dv],
+ *   key_cache [B,Hk,M,D], value_cache [B,Hk,M,Dv] in `dtype`;
+ *   lengths [B] int64; append_mask [B,Q] bytes (0 = False);
+ *   out caches in `dtype`, out_lengths [B] int64,
+ *   out_attention [B,Hq,Q,M] and out_context [B,Hq,Q,Dv] in double,
+ *   flags [B] (nullable). Returns the OR of all flags.
+ * work: caller scratch of M doubles per OpenMP thread (kvo_threads()).
+ */
+int kvo_step(int dtype, int64_t B, int64_t Hq, int64_t Hk, int64_t Q, int64_t D, int64_t Dv,
+             int64_t M, const void *query, const void *new_key, const void *new_value,
+             const void *key_cache, const void *value_cache, const int64_t *lengths,
+             const uint8_t *append_mask, double scale, void *out_key_cache,
+             void *out_value_cache, int64_t *out_lengths, double *out_attention,
+             double *out_context, int32_t *flags, double *work) {
+    const int64_t es = elem_size(dtype);
+    int any = 0;
+    /* 1. copy both caches byte for byte (every unwritten entry preserved). */
+    memcpy(out_key_cache, key_cache, (size_t)(B * Hk * M * D * es));
+    memcpy(out_value_cache, value_cache, (size_t)(B * Hk * M * Dv * es));
+    for (int64_t b = 0; b < B; ++b) {
+        int32_t f = 0;
+        const int64_t L = lengths[b];
+        const int64_t n = kvo_append_count(append_mask + b * Q, Q, L, M, &f);
+        if (flags) flags[b] = f;
+        any |= f;
+        /* 2. write new rows t < n at slot L + t, per KV head. */
+        for (int64_t k = 0; k < Hk; ++k) {
+            for (int64_t t = 0; t < n; ++t) {
+                memcpy((char *)out_key_cache + at4(Hk, M, D, b, k, L + t, 0) * es,
+                       (const char *)new_key + at4(Hk, Q, D, b, k, t, 0) * es, (size_t)(D * es));
+                memcpy((char *)out_value_cache + at4(Hk, M, Dv, b, k, L + t, 0) * es,
+                       (const char *)new_value + at4(Hk, Q, Dv, b, k, t, 0) * es,
+                       (size_t)(Dv * es));
+            }
+        }
+        out_lengths[b] = L + n;
+    }
+    /* 3. attention over the updated cache for every (b, h, t). */
+    const int64_t rows = B * Hq;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < rows; ++bh) {
+        const int64_t b = bh / Hq, h = bh % Hq;
+        const int64_t L = lengths[b];
+        const int64_t n = kvo_append_count(append_mask + b * Q, Q, L, M, NULL);
+        int tid = 0;
+#ifdef _OPENMP
+        tid = omp_get_thread_num();
+#endif
+        double *scratch = work + (int64_t)tid * M;
+        for (int64_t t = 0; t < Q; ++t) {
+            /* Read the updated cache itself: the rows written above. */
+            attend_row(dtype, Hq, Hk, Q, D, Dv, M, query, new_key, new_value, out_key_cache,
+                       out_value_cache, L, 0, t < n, scale, b, h, t,
+                       out_attention + at4(Hq, Q, M, b, h, t, 0),
+                       out_context + at4(Hq, Q, Dv, b, h, t, 0), scratch);
+        }
+    }
+    return any;
+}
+
+/*
+ * Attention and context for selected rows only, without building the updated
+ * cache: rows_bht holds n_rows triples (b, h, t). Outputs are
+ * att [n_rows, M] and ctx [n_rows, Dv] in double. work: M doubles per thread.
+ */
+int kvo_rows(int dtype, int64_t B, int64_t Hq, int64_t Hk, int64_t Q, int64_t D, int64_t Dv,
+             int64_t M, const void *query, const void *new_key, const void *new_value,
+             const void *key_cache, const void *value_cache, const int64_t *lengths,
+             const uint8_t *append_mask, double scale, const int64_t *rows_bht, int64_t n_rows,
+             double *att, double *ctx, double *work) {
+    (void)B;
+    int any = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : any)
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const int64_t b = rows_bht[3 * i], h = rows_bht[3 * i + 1], t = rows_bht[3 * i + 2];
+        int32_t f = 0;
+        const int64_t L = lengths[b];
+        const int64_t n = kvo_append_count(append_mask + b * Q, Q, L, M, &f);
+        any |= f;
+        int tid = 0;
+#ifdef _OPENMP
+        tid = omp_get_thread_num();
+#endif
+        attend_row(dtype, Hq, Hk, Q, D, Dv, M, query, new_key, new_value, key_cache,
+                   value_cache, L, n, t < n, scale, b, h, t, att + i * M, ctx + i * Dv,
+                   work + (int64_t)tid * M);
+    }
+    return any;
+}
