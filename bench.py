@@ -1,0 +1,416 @@
+"""Benchmark of the KV-cache append + causal attention step on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload gqa_decode|ragged_specdec|long_mqa|chunked_append|tiny_fp32]
+
+One step = one kvc_step over one batch of the workload: copy + scatter of
+both caches, attention partials, split combine, attention rows and context.
+Inputs are seeded synthetic tensors (workloads.py) resident in HBM before the
+timed region; the caches alone are far larger than the 129 MB L2, so no L2
+flush is needed between steps. Prints one JSON line (rank 0).
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on the host cores, each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "effective HBM GB/s (and % of 8 TB/s) + kv steps/s per config, 1 GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+FUSED_SOURCES = ["kv_cache_append_gb300/csrc/kvc_fused.cu",
+                 "kv_cache_append_gb300/csrc/kvc_internal.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_step_traffic.json")
+
+
+# ----------------------------------------------------------------- bytes model
+def algorithmic_bytes(spec: workloads.Spec, batch_rows: int | None = None) -> dict:
+    """Bytes the step must move at minimum: full cache read + write, the
+    attention and context writes, the query / new key / new value reads,
+    lengths and mask (read) and lengths (write)."""
+    B = spec.B if batch_rows is None else batch_rows
+    es = 4 if spec.dtype == "f32" else 2
+    cache = B * spec.Hk * spec.M * (spec.D + spec.Dv) * es
+    qkv = (B * spec.Hq * spec.Q * spec.D + B * spec.Hk * spec.Q * (spec.D + spec.Dv)) * es
+    small = B * 8 * 2 + B * spec.Q
+    att = B * spec.Hq * spec.Q * spec.M * es
+    ctx = B * spec.Hq * spec.Q * spec.Dv * es
+    fused = 2 * cache + qkv + small
+    return {"total": fused + att + ctx, "fused_kernel": fused, "finalize_kernel": att + ctx}
+
+
+def source_digest(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def fused_traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu
+    summary, if it was taken on the current kernel source and this workload."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_sha256") != source_digest(FUSED_SOURCES):
+        return None
+    entry = rec.get("workloads", {}).get(workload)
+    return None if entry is None else float(entry["dram_bytes_per_launch"])
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.t:
+            self.t.join(timeout=5)
+
+    def summary(self, t0, t1):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = [s for (ts, s) in self.samples if len(s) >= 9]
+        window = [s for (ts, s) in self.samples if t0 - 0.25 <= ts <= t1 + 0.25 and len(s) >= 9]
+        busy = [s for s in rows if _num(s[4]) and _num(s[4]) >= 50]
+        use = window if window else busy
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [_num(s[1]) for s in use if _num(s[1])]
+        reasons = sorted({names[i] for s in use for i in range(4) if s[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": _num(use[0][2]), "reasons": reasons, "samples": len(use),
+                "window": "timed region" if window else "busy samples (timed region < 200 ms)",
+                "power_w_max": max((_num(s[3]) or 0.0) for s in use)}
+
+
+def _num(x):
+    try:
+        return float(x)
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- CPU oracle leg
+def oracle_sample(spec: workloads.Spec, x_cpu: workloads.StepInputs, budget_s: float):
+    """Time the fp64 oracle on the first k batch rows, k grown until the run
+    takes about budget_s. Returns (seconds, rows, threads)."""
+    import oracle
+    oracle.build()
+    k = 1
+    while True:
+        sub = [t[:k] for t in x_cpu.args()]
+        t0 = time.perf_counter()
+        oracle.step(*sub, x_cpu.options)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or k >= spec.B:
+            return dt, k, oracle.threads()
+        grow = max(2, int(math.ceil(budget_s / max(dt, 1e-3) * k)))
+        k = min(spec.B, grow)
+
+
+def cpu_inputs(spec, seed):
+    """Seeded inputs on the host for the oracle legs (independent of any GPU)."""
+    return workloads.generate(spec, seed, device="cpu")
+
+
+def run_reference(args, spec, world, rank):
+    if rank != 0:
+        return
+    x = cpu_inputs(spec, seed=1)
+    per_step_budget = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    # size the sample once, then time W + K steps of that sample
+    _, rows, threads = oracle_sample(spec, x, per_step_budget)
+    sub = [t[:rows] for t in x.args()]
+    import oracle
+    for _ in range(args.warmup):
+        oracle.step(*sub, x.options)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.step(*sub, x.options)
+    dt = (time.perf_counter() - t0) / args.steps
+    nbytes = algorithmic_bytes(spec, rows)["total"]
+    value = nbytes / dt / 1e9
+    sample = f"first {rows} of {spec.B} batch rows of {args.workload} per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(args.workload, spec),
+        "steps_per_s": round(1.0 / dt * rows / spec.B, 6),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(name, spec):
+    return {"workload": name, "B": spec.B, "Hq": spec.Hq, "Hk": spec.Hk, "Q": spec.Q,
+            "D": spec.D, "Dv": spec.Dv, "M": spec.M, "dtype": spec.dtype,
+            "lengths": list(spec.lengths), "append_counts": list(spec.counts),
+            "scale": spec.scale if spec.scale is not None else "1/sqrt(D)",
+            "l2": "inputs (caches) larger than the 129 MB L2; no flush between steps"}
+
+
+# ----------------------------------------------------------------- GPU leg
+def run_ours(args, spec, world, rank, local):
+    import kv_cache_append_gb300 as kvc
+    from kv_cache_append_gb300 import build as kbuild
+    if not os.path.exists(kbuild.LIB):
+        kbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = workloads.generate(spec, seed=1 + rank, device=dev)
+    q, nk, nv, kc, vc, ln, mk = x.args()
+    mk = mk.view(torch.uint8)
+    scale = x.options.get("scale", kvc.default_scale(spec.D))
+    dims = kvc.dims_of(q, kc, vc)
+    out = kvc.allocate_outputs(q, kc, vc)
+    nws = kvc.workspace_bytes(dims)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
+    nkern, path = kvc.plan_info(dims, kc, vc, nk, nv, out["key_cache"], out["value_cache"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        kvc.step_into(dims, q, nk, nv, kc, vc, ln, mk, scale, out, ws, None,
+                      stream.cuda_stream, events)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    nev = nkern + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    for e in [ev for row in evs for ev in row] + [start, end]:
+        e.record(stream)  # torch creates the CUDA event on its first record
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(world)
+    ms_total = start.elapsed_time(end)
+    time.sleep(0.25)
+    clocks.stop()
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+    kern_ms = [statistics.mean(e[k].elapsed_time(e[k + 1]) for e in evs) for k in range(nkern)]
+
+    nbytes = algorithmic_bytes(spec)
+    value = world * nbytes["total"] / (ms_step * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    fused_ms = kern_ms[0]
+    achieved = nbytes["fused_kernel"] / (fused_ms * 1e-3) / 1e9
+    traffic = fused_traffic(args.workload) if path == "fused" else None
+
+    # ---- end to end through the public API: pinned host in, pinned host out
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(kvc, x, dev, spec, max(3, min(args.steps, 10)), nbytes["total"], world)
+
+    # ---- CPU oracle baseline, rank 0 at N = 1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        xc = cpu_inputs(spec, seed=1)
+        dt, rows, threads = oracle_sample(spec, xc, args.cpu_budget)
+        cpu = {"value": round(algorithmic_bytes(spec, rows)["total"] / dt / 1e9, 4),
+               "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"first {rows} of {spec.B} batch rows of {args.workload}, one step"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": spec.dtype, "data": "synthetic",
+        "config": config_of(args.workload, spec),
+        "pct_of_8TBs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
+        "steps_per_s": round(world * 1e3 / ms_step, 2),
+        "bytes_per_step": nbytes["total"],
+        "path": path,
+        "kernels": {"fused_step_kernel": {"ms": round(kern_ms[0], 4),
+                                          "algorithmic_GBps": round(achieved, 1)}},
+        "roofline": {"bound": "hbm", "kernel": "fused_step_kernel",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "traffic": traffic},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": nkern * args.steps,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+    }
+    if nkern > 1:
+        fin_ms = kern_ms[-1]
+        line["kernels"]["finalize_kernel"] = {
+            "ms": round(fin_ms, 4),
+            "algorithmic_GBps": round(nbytes["finalize_kernel"] / (fin_ms * 1e-3) / 1e9, 1)}
+    print(json.dumps(line), flush=True)
+
+
+def measure_e2e(kvc, x, dev, spec, steps, nbytes, world):
+    """The public call with host buffers: every step copies the inputs from
+    pinned host memory, runs kv_cache_attention_step, copies every output back."""
+    host_in = [t.to("cpu").pin_memory() for t in x.args()]
+    out0 = kvc.kv_cache_attention_step(*x.args(), x.options)
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out0.items()}
+    del out0
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        args = [t.to(dev, non_blocking=True) for t in host_in]
+        out = kvc.kv_cache_attention_step(*args, x.options)
+        for k, v in out.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(s.elapsed_time(e) / steps, world)
+    return {"value": round(world * nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
+            "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa_decode", choices=sorted(workloads.SPECS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size B (profiling captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    spec = workloads.SPECS[args.workload]
+    if args.batch:
+        spec = spec.replace(B=args.batch)
+    if args.impl == "reference":
+        run_reference(args, spec, world, rank)
+    else:
+        run_ours(args, spec, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

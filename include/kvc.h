@@ -1,0 +1,158 @@
+/*
+ * kvc.h -- C ABI of libkvc: the autoregressive KV-cache append + causal
+ * attention step on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one defined on the page "Autoregressive KV-cache
+ * append and causal attention" (biotorch, problems/kv_cache_attention_step),
+ * section "Required behavior":
+ *
+ *   - query [B,Hq,Q,D], new_key [B,Hk,Q,D], new_value [B,Hk,Q,Dv],
+ *     key_cache [B,Hk,M,D], value_cache [B,Hk,M,Dv], all of one floating
+ *     dtype; B,Hq,Hk,D,Dv,M >= 1, Q >= 0, Hk divides Hq.
+ *   - Query head h reads KV head floor(h / (Hq/Hk)).
+ *   - append_mask[b,:] is n_b True values followed by False; new rows
+ *     t < n_b are written at cache slot lengths[b] + t.
+ *   - The whole updated cache is returned (every other slot bit-identical,
+ *     tail included), inputs are never modified, lengths become length + n.
+ *   - A valid query t (t < n_b) attends to slots j <= lengths[b] + t with
+ *     scores scale * dot(q, k) and a max-subtracted softmax; attention
+ *     [B,Hq,Q,M] is zero on every other slot; context [B,Hq,Q,Dv] =
+ *     attention . updated values; rows t >= n_b are all zero.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are dense, row-major, contiguous, in DEVICE memory of the
+ *     current CUDA device, owned by the caller. The library allocates nothing.
+ *   - Inputs are read only. Outputs and the workspace must not overlap any
+ *     input or each other (KVC_E_ALIAS).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). No call synchronizes; results are ready when the stream is.
+ *   - A negative return means nothing was launched (except KVC_E_CUDA,
+ *     which reports a failed launch).
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVC_API __attribute__((visibility("default")))
+#else
+#define KVC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of query, new_key, new_value, both caches and both outputs
+ * ("finite floating with matching dtype", Required behavior, bullet 1). */
+typedef enum { KVC_F32 = 0, KVC_BF16 = 1, KVC_F16 = 2 } kvc_dtype;
+
+/* Problem sizes (Required behavior, bullet 1). dtype is a kvc_dtype. */
+typedef struct {
+    int64_t B, Hq, Hk, Q, D, Dv, M;
+    int32_t dtype;
+} kvc_dims;
+
+/* Return codes. */
+#define KVC_OK 0
+#define KVC_E_NULL (-1)      /* a required pointer is NULL */
+#define KVC_E_SHAPE (-2)     /* a size < 1 (Q < 0), Hq % Hk != 0, or sizes overflow */
+#define KVC_E_DTYPE (-3)     /* dtype is not a kvc_dtype */
+#define KVC_E_SCALE (-4)     /* scale <= 0, NaN or infinite */
+#define KVC_E_WORKSPACE (-5) /* workspace NULL, too small, or not 16-byte aligned */
+#define KVC_E_ALIAS (-6)     /* an output overlaps an input, another output or the workspace */
+#define KVC_E_DEVICE (-7)    /* current device is not an sm_103 GPU */
+#define KVC_E_CUDA (-8)      /* a CUDA call or kernel launch failed */
+
+/* Bits OR-ed into *dev_status by the kernels (never cleared by the library). */
+#define KVC_DEV_OVERFLOW 1 /* some row had length < 0, length > M or length + n > M */
+#define KVC_DEV_MASK 2     /* some append_mask row was not a True-prefix */
+#define KVC_DEV_TIMEOUT 4  /* an internal pipeline wait gave up (outputs invalid) */
+
+/*
+ * Bytes of device workspace kvc_step needs for these sizes (0 when Q == 0).
+ * Pure host arithmetic; valid for any GPU with at most 1024 SMs.
+ * Returns 0 and sets nothing for invalid dims (kvc_step then reports why).
+ * Holds the per-split softmax partials (max, sum, weighted values, fp32) and
+ * one fp32 score per (b, h, t, slot).
+ */
+KVC_API size_t kvc_workspace_bytes(const kvc_dims *dims);
+
+/*
+ * One step: append + attention ("Required behavior", bullets 1-7).
+ *
+ *   dims            sizes and dtype (host pointer).
+ *   query           [B,Hq,Q,D]    device, dtype.        May be NULL iff Q == 0.
+ *   new_key         [B,Hk,Q,D]    device, dtype.        May be NULL iff Q == 0.
+ *   new_value       [B,Hk,Q,Dv]   device, dtype.        May be NULL iff Q == 0.
+ *   key_cache       [B,Hk,M,D]    device, dtype.
+ *   value_cache     [B,Hk,M,Dv]   device, dtype.
+ *   lengths         [B]           device, int64, old valid prefix per row.
+ *   append_mask     [B,Q]         device, one byte per entry (0 = False).
+ *                                 May be NULL iff Q == 0.
+ *   scale           > 0, finite. Scores are scale * dot(q, k); the caller
+ *                   passes 1/sqrt(D) for the default.
+ *   out_key_cache   [B,Hk,M,D]    device, dtype: the updated key cache.
+ *   out_value_cache [B,Hk,M,Dv]   device, dtype: the updated value cache.
+ *   out_lengths     [B]           device, int64: length + n.
+ *   out_attention   [B,Hq,Q,M]    device, dtype. May be NULL iff Q == 0.
+ *   out_context     [B,Hq,Q,Dv]   device, dtype. May be NULL iff Q == 0.
+ *   workspace       device scratch of workspace_bytes >= kvc_workspace_bytes(dims),
+ *                   16-byte aligned; contents on entry do not matter.
+ *                   May be NULL iff kvc_workspace_bytes(dims) == 0.
+ *   dev_status      device int32, nullable. The kernels OR KVC_DEV_* bits into it.
+ *   stream          cudaStream_t to enqueue on.
+ *
+ * Rows outside the contract (non-prefix mask, length outside [0, M], or
+ * length + n > M; "capacity overflow and non-prefix append masks are
+ * outside this contract", bullet 7) never touch memory out of bounds: the
+ * row appends nothing (its cache rows and length are returned unchanged, as
+ * a failed append leaves a fixed-capacity cache unchanged), its query rows
+ * are zero, and KVC_DEV_OVERFLOW / KVC_DEV_MASK is set in *dev_status.
+ *
+ * Returns KVC_OK once the work is enqueued, else a KVC_E_* code.
+ */
+KVC_API int kvc_step(const kvc_dims *dims, const void *query, const void *new_key, const void *new_value,
+             const void *key_cache, const void *value_cache, const int64_t *lengths,
+             const uint8_t *append_mask, double scale, void *out_key_cache,
+             void *out_value_cache, int64_t *out_lengths, void *out_attention,
+             void *out_context, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+             void *stream);
+
+/*
+ * kvc_step with timing: events[0] is recorded on `stream` before the first
+ * kernel and events[i] after the i-th kernel, for i < n_events (each a
+ * cudaEvent_t created by the caller; entries beyond the kernel count are
+ * recorded at the end). Same arguments and results as kvc_step otherwise.
+ */
+KVC_API int kvc_step_timed(const kvc_dims *dims, const void *query, const void *new_key,
+                   const void *new_value, const void *key_cache, const void *value_cache,
+                   const int64_t *lengths, const uint8_t *append_mask, double scale,
+                   void *out_key_cache, void *out_value_cache, int64_t *out_lengths,
+                   void *out_attention, void *out_context, void *workspace,
+                   size_t workspace_bytes, int32_t *dev_status, void *stream,
+                   void *const *events, int n_events);
+
+/*
+ * Number of kernels kvc_step launches for these sizes and pointers, and the
+ * name of the path it takes ("fused" or "generic") through *path_name
+ * (nullable). Pure host logic except for a cached device-attribute query.
+ * Returns a negative KVC_E_* code on invalid arguments.
+ */
+KVC_API int kvc_plan_info(const kvc_dims *dims, const void *key_cache, const void *value_cache,
+                  const void *new_key, const void *new_value, const void *out_key_cache,
+                  const void *out_value_cache, const char **path_name);
+
+/* Static text for a KVC_OK / KVC_E_* code. */
+KVC_API const char *kvc_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+KVC_API int kvc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

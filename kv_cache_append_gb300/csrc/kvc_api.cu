@@ -1,0 +1,381 @@
+// kvc_api.cu -- the C ABI of libkvc (include/kvc.h): argument checks, the
+// work decomposition and kernel launches of one step.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "kvc.h"
+#include "kvc_internal.cuh"
+#include "kvc_launch.h"
+
+namespace kvc {
+namespace {
+
+constexpr int64_t kSizingCtas = 1024;      // workspace sizing holds for up to this many SMs
+constexpr int64_t kStageTargetBytes = 16384;
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool init = false;
+    int sms = 0, smem_optin = 0, major = 0, minor = 0;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+cudaError_t device_info(DeviceInfo* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.init) {
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                        dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+                cudaSuccess)
+            return e;
+        d.init = true;
+    }
+    *out = d;
+    return cudaSuccess;
+}
+
+int elem_size(int32_t dtype) { return dtype == KVC_F32 ? 4 : 2; }
+
+int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+// Sizes valid and every tensor's byte count representable.
+int check_dims(const kvc_dims* d) {
+    if (!d) return KVC_E_NULL;
+    if (d->dtype != KVC_F32 && d->dtype != KVC_BF16 && d->dtype != KVC_F16) return KVC_E_DTYPE;
+    if (d->B < 1 || d->Hq < 1 || d->Hk < 1 || d->D < 1 || d->Dv < 1 || d->M < 1 || d->Q < 0)
+        return KVC_E_SHAPE;
+    if (d->Hq % d->Hk != 0) return KVC_E_SHAPE;
+    const double lim = 4.0e18;  // keep every byte offset well inside int64
+    const double es = elem_size(d->dtype);
+    const double B = d->B, Hq = d->Hq, Hk = d->Hk, Q = d->Q, D = d->D, Dv = d->Dv, M = d->M;
+    if (B * Hk * M * (D + Dv) * es > lim || B * Hq * Q * M * 8.0 > lim ||
+        B * Hq * Q * (D + Dv) * es > lim || B * Q > lim)
+        return KVC_E_SHAPE;
+    if (M > (int64_t(1) << 40) || Q > (int64_t(1) << 31)) return KVC_E_SHAPE;
+    return KVC_OK;
+}
+
+// The decomposition and shared-memory layout of one step.
+struct Plan {
+    bool fused = false;
+    int T = 0;
+    int64_t TPU = 0, TT = 0, P = 0, KP = 0;
+    int RPW = 4, WR = 1, WS = 8, NRG = 1, SW = 0, NS = 0, LAG = 0, DVC = 1;
+    int stage_bytes = 0, off_stages = 0, off_q = 0, off_p = 0, off_state = 0, off_state_acc = 0,
+        off_flag = 0;
+    size_t smem = 0;
+    size_t off_ml = 0, off_acc = 0, off_scores = 0, ws_bytes = 0;
+};
+
+// Whether the fused kernel's row shapes apply (16-byte rows, widths it holds).
+bool fused_shapes(const kvc_dims& d) {
+    const int64_t es = elem_size(d.dtype);
+    return (d.D * es) % 16 == 0 && (d.Dv * es) % 16 == 0 && d.D * es <= 512 && d.Dv <= 256;
+}
+
+int64_t pieces_bound(int64_t TPU, int64_t TT, int64_t P) {
+    const int64_t shortest = TT / P;  // >= 1 since P <= TT
+    return std::min<int64_t>(P, (TPU - 1) / shortest + 2);
+}
+
+void workspace_layout(const kvc_dims& d, int64_t KP, Plan* pl) {
+    const int64_t U = d.B * d.Hk, R = (d.Hq / d.Hk) * d.Q;
+    if (d.Q == 0) {
+        pl->off_ml = pl->off_acc = pl->off_scores = pl->ws_bytes = 0;
+        return;
+    }
+    int64_t off = 0;
+    pl->off_ml = static_cast<size_t>(off);
+    off = align_up(off + U * KP * R * 2 * 4, 256);
+    pl->off_acc = static_cast<size_t>(off);
+    off = align_up(off + U * KP * R * d.Dv * 4, 256);
+    pl->off_scores = static_cast<size_t>(off);
+    off = align_up(off + d.B * d.Hq * d.Q * d.M * 4, 256);
+    pl->ws_bytes = static_cast<size_t>(off);
+}
+
+// Tiling of the fused kernel that depends only on the sizes.
+void fused_tiling(const kvc_dims& d, Plan* pl) {
+    const int64_t es = elem_size(d.dtype);
+    const int64_t row = (d.D + d.Dv) * es;
+    int64_t T = kStageTargetBytes / row / 32 * 32;
+    T = std::max<int64_t>(32, std::min<int64_t>(128, T));
+    if (d.M < T) T = align_up(d.M, 32);
+    pl->T = static_cast<int>(T);
+    pl->TPU = (d.M + T - 1) / T;
+    pl->TT = d.B * d.Hk * pl->TPU;
+    const int64_t R = (d.Hq / d.Hk) * d.Q;
+    pl->RPW = R <= 4 ? 4 : 8;
+    const int64_t RG = (R + pl->RPW - 1) / pl->RPW;
+    int WR = 1;
+    while (WR < RG && WR < kConsumerWarps) WR *= 2;
+    pl->WR = WR;
+    pl->WS = kConsumerWarps / WR;
+    pl->NRG = static_cast<int>(std::max<int64_t>(1, (RG + WR - 1) / WR));
+    pl->SW = pl->T / pl->WS;
+    pl->DVC = d.Dv <= 128 ? 1 : 2;
+}
+
+// Full fused plan for a device with `sms` SMs and `smem_cap` bytes of
+// opt-in shared memory per block. False if it does not fit.
+bool fused_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
+    if (!fused_shapes(d)) return false;
+    fused_tiling(d, pl);
+    const int64_t es = elem_size(d.dtype);
+    const int64_t R = (d.Hq / d.Hk) * d.Q;
+    const int64_t RGpad = (R + pl->RPW - 1) / pl->RPW * pl->RPW;
+    int64_t off = 2 * kMaxStages * 8;
+    pl->off_flag = static_cast<int>(off);
+    off = 512;
+    pl->off_q = static_cast<int>(off);
+    off = align_up(off + RGpad * d.D * 4, 128);
+    pl->off_p = static_cast<int>(off);
+    off = align_up(off + int64_t(kConsumerWarps) * pl->SW * pl->RPW * 4, 128);
+    pl->off_state = static_cast<int>(off);
+    off = align_up(off + int64_t(pl->WS) * R * 2 * 4, 128);
+    pl->off_state_acc = static_cast<int>(off);
+    off = align_up(off + int64_t(pl->WS) * R * d.Dv * 4, 1024);
+    pl->off_stages = static_cast<int>(off);
+    const int64_t stage = align_up(int64_t(pl->T) * (d.D + d.Dv) * es, 128);
+    pl->stage_bytes = static_cast<int>(stage);
+    if (off + 2 * stage > smem_cap) return false;
+    pl->NS = static_cast<int>(std::min<int64_t>(kMaxStages, (smem_cap - off) / stage));
+    pl->LAG = std::min(4, pl->NS - 1);
+    pl->smem = static_cast<size_t>(off + int64_t(pl->NS) * stage);
+    pl->P = std::min<int64_t>(sms, pl->TT);
+    pl->KP = pieces_bound(pl->TPU, pl->TT, pl->P);
+    pl->fused = true;
+    workspace_layout(d, pl->KP, pl);
+    return true;
+}
+
+void generic_plan(const kvc_dims& d, Plan* pl) {
+    *pl = Plan();
+    pl->fused = false;
+    pl->T = static_cast<int>(std::min<int64_t>(d.M, int64_t(1) << 30));
+    pl->TPU = 1;
+    pl->TT = d.B * d.Hk;
+    pl->P = pl->TT;
+    pl->KP = 1;
+    workspace_layout(d, 1, pl);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range range_of(const void* p, int64_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Range{a, a + static_cast<uintptr_t>(bytes > 0 && p ? bytes : 0)};
+}
+
+bool overlaps(Range a, Range b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
+
+int step_impl(const kvc_dims* dims, const void* query, const void* new_key, const void* new_value,
+              const void* key_cache, const void* value_cache, const int64_t* lengths,
+              const uint8_t* append_mask, double scale, void* out_key_cache,
+              void* out_value_cache, int64_t* out_lengths, void* out_attention,
+              void* out_context, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+              void* stream_ptr, void* const* events, int n_events) {
+    int rc = check_dims(dims);
+    if (rc != KVC_OK) return rc;
+    const kvc_dims d = *dims;
+    const bool hasq = d.Q > 0;
+    if (!key_cache || !value_cache || !lengths || !out_key_cache || !out_value_cache ||
+        !out_lengths)
+        return KVC_E_NULL;
+    if (hasq && (!query || !new_key || !new_value || !append_mask || !out_attention || !out_context))
+        return KVC_E_NULL;
+    if (!(scale > 0.0) || !std::isfinite(scale)) return KVC_E_SCALE;
+    if (events && n_events < 0) return KVC_E_NULL;
+
+    DeviceInfo dev;
+    if (device_info(&dev) != cudaSuccess) return KVC_E_CUDA;
+    if (dev.major != 10 || dev.minor != 3) return KVC_E_DEVICE;
+
+    const int64_t es = elem_size(d.dtype);
+    const bool ptrs_aligned = aligned16(key_cache) && aligned16(value_cache) &&
+                              aligned16(out_key_cache) && aligned16(out_value_cache) &&
+                              (!hasq || (aligned16(new_key) && aligned16(new_value)));
+    Plan pl;
+    if (!(ptrs_aligned && fused_plan(d, dev.sms, dev.smem_optin, &pl))) generic_plan(d, &pl);
+
+    if (pl.ws_bytes > 0) {
+        if (!workspace || workspace_bytes < pl.ws_bytes || !aligned16(workspace))
+            return KVC_E_WORKSPACE;
+    }
+
+    // Outputs and workspace must not overlap inputs or each other.
+    const Range in[] = {
+        range_of(query, d.B * d.Hq * d.Q * d.D * es),
+        range_of(new_key, d.B * d.Hk * d.Q * d.D * es),
+        range_of(new_value, d.B * d.Hk * d.Q * d.Dv * es),
+        range_of(key_cache, d.B * d.Hk * d.M * d.D * es),
+        range_of(value_cache, d.B * d.Hk * d.M * d.Dv * es),
+        range_of(lengths, d.B * 8),
+        range_of(append_mask, d.B * d.Q),
+    };
+    const Range out[] = {
+        range_of(out_key_cache, d.B * d.Hk * d.M * d.D * es),
+        range_of(out_value_cache, d.B * d.Hk * d.M * d.Dv * es),
+        range_of(out_lengths, d.B * 8),
+        range_of(out_attention, d.B * d.Hq * d.Q * d.M * es),
+        range_of(out_context, d.B * d.Hq * d.Q * d.Dv * es),
+        range_of(workspace, static_cast<int64_t>(pl.ws_bytes)),
+    };
+    for (const Range& o : out)
+        for (const Range& i : in)
+            if (overlaps(o, i)) return KVC_E_ALIAS;
+    for (size_t a = 0; a < sizeof(out) / sizeof(out[0]); ++a)
+        for (size_t b = a + 1; b < sizeof(out) / sizeof(out[0]); ++b)
+            if (overlaps(out[a], out[b])) return KVC_E_ALIAS;
+
+    StepParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.B = d.B; p.Hq = d.Hq; p.Hk = d.Hk; p.Q = d.Q; p.D = d.D; p.Dv = d.Dv; p.M = d.M;
+    p.G = d.Hq / d.Hk;
+    p.R = p.G * d.Q;
+    p.es = static_cast<int>(es);
+    p.qscale = static_cast<float>(scale * 1.4426950408889634);
+    p.T = pl.T; p.TPU = pl.TPU; p.TT = pl.TT; p.P = pl.P; p.KP = pl.KP;
+    p.RPW = pl.RPW; p.WR = pl.WR; p.WS = pl.WS; p.NRG = pl.NRG; p.SW = pl.SW;
+    p.NS = pl.NS; p.LAG = pl.LAG;
+    p.stage_bytes = pl.stage_bytes; p.off_stages = pl.off_stages; p.off_q = pl.off_q;
+    p.off_p = pl.off_p; p.off_state = pl.off_state; p.off_state_acc = pl.off_state_acc;
+    p.off_flag = pl.off_flag;
+    p.query = query; p.new_key = new_key; p.new_value = new_value;
+    p.key_cache = key_cache; p.value_cache = value_cache;
+    p.lengths = lengths; p.mask = append_mask;
+    p.out_key_cache = out_key_cache; p.out_value_cache = out_value_cache;
+    p.out_lengths = out_lengths; p.out_attention = out_attention; p.out_context = out_context;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    if (pl.ws_bytes > 0) {
+        p.part_ml = reinterpret_cast<float*>(ws + pl.off_ml);
+        p.part_acc = reinterpret_cast<float*>(ws + pl.off_acc);
+        p.scores = reinterpret_cast<float*>(ws + pl.off_scores);
+    }
+    p.dev_status = dev_status;
+    p.vec_attention = (d.M % 8 == 0) && aligned16(out_attention);
+
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    int recorded = 0;
+    auto record = [&]() -> cudaError_t {
+        if (events && recorded < n_events)
+            return cudaEventRecord(static_cast<cudaEvent_t>(events[recorded++]), stream);
+        return cudaSuccess;
+    };
+    cudaError_t e = record();
+    if (e == cudaSuccess) {
+        if (pl.fused) {
+            e = launch_fused(p, d.dtype, pl.DVC, pl.smem, stream);
+            if (e == cudaSuccess) e = record();
+        } else {
+            e = launch_generic_copy(p, d.dtype, stream);
+            if (e == cudaSuccess) e = record();
+            if (e == cudaSuccess && hasq) {
+                e = launch_generic_attend(p, d.dtype, stream);
+                if (e == cudaSuccess) e = record();
+            }
+        }
+        if (e == cudaSuccess && hasq) {
+            e = launch_finalize(p, d.dtype, stream);
+            if (e == cudaSuccess) e = record();
+        }
+        while (e == cudaSuccess && events && recorded < n_events) e = record();
+    }
+    return e == cudaSuccess ? KVC_OK : KVC_E_CUDA;
+}
+
+}  // namespace
+}  // namespace kvc
+
+extern "C" {
+
+size_t kvc_workspace_bytes(const kvc_dims* dims) {
+    using namespace kvc;
+    if (check_dims(dims) != KVC_OK || dims->Q == 0) return 0;
+    Plan pl;
+    if (fused_shapes(*dims)) {
+        fused_tiling(*dims, &pl);
+        const int64_t P = std::min<int64_t>(kSizingCtas, pl.TT);
+        workspace_layout(*dims, pieces_bound(pl.TPU, pl.TT, P), &pl);
+    } else {
+        generic_plan(*dims, &pl);
+    }
+    return pl.ws_bytes;
+}
+
+int kvc_step(const kvc_dims* dims, const void* query, const void* new_key, const void* new_value,
+             const void* key_cache, const void* value_cache, const int64_t* lengths,
+             const uint8_t* append_mask, double scale, void* out_key_cache,
+             void* out_value_cache, int64_t* out_lengths, void* out_attention,
+             void* out_context, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+             void* stream) {
+    return kvc::step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
+                          append_mask, scale, out_key_cache, out_value_cache, out_lengths,
+                          out_attention, out_context, workspace, workspace_bytes, dev_status,
+                          stream, nullptr, 0);
+}
+
+int kvc_step_timed(const kvc_dims* dims, const void* query, const void* new_key,
+                   const void* new_value, const void* key_cache, const void* value_cache,
+                   const int64_t* lengths, const uint8_t* append_mask, double scale,
+                   void* out_key_cache, void* out_value_cache, int64_t* out_lengths,
+                   void* out_attention, void* out_context, void* workspace,
+                   size_t workspace_bytes, int32_t* dev_status, void* stream,
+                   void* const* events, int n_events) {
+    return kvc::step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
+                          append_mask, scale, out_key_cache, out_value_cache, out_lengths,
+                          out_attention, out_context, workspace, workspace_bytes, dev_status,
+                          stream, events, n_events);
+}
+
+int kvc_plan_info(const kvc_dims* dims, const void* key_cache, const void* value_cache,
+                  const void* new_key, const void* new_value, const void* out_key_cache,
+                  const void* out_value_cache, const char** path_name) {
+    using namespace kvc;
+    const int rc = check_dims(dims);
+    if (rc != KVC_OK) return rc;
+    DeviceInfo dev;
+    if (device_info(&dev) != cudaSuccess) return KVC_E_CUDA;
+    const bool hasq = dims->Q > 0;
+    const bool ptrs_aligned = aligned16(key_cache) && aligned16(value_cache) &&
+                              aligned16(out_key_cache) && aligned16(out_value_cache) &&
+                              (!hasq || (aligned16(new_key) && aligned16(new_value)));
+    Plan pl;
+    const bool fused = ptrs_aligned && fused_plan(*dims, dev.sms, dev.smem_optin, &pl);
+    if (path_name) *path_name = fused ? "fused" : "generic";
+    return fused ? (hasq ? 2 : 1) : (hasq ? 3 : 1);
+}
+
+const char* kvc_status_string(int status) {
+    switch (status) {
+        case KVC_OK: return "ok";
+        case KVC_E_NULL: return "a required pointer is NULL";
+        case KVC_E_SHAPE: return "invalid sizes (need B,Hq,Hk,D,Dv,M >= 1, Q >= 0, Hk | Hq)";
+        case KVC_E_DTYPE: return "unknown dtype";
+        case KVC_E_SCALE: return "scale must be positive and finite";
+        case KVC_E_WORKSPACE: return "workspace missing, too small or not 16-byte aligned";
+        case KVC_E_ALIAS: return "an output overlaps an input, another output or the workspace";
+        case KVC_E_DEVICE: return "the current CUDA device is not an sm_103 (GB300) GPU";
+        case KVC_E_CUDA: return "a CUDA call or kernel launch failed";
+        default: return "unknown status";
+    }
+}
+
+int kvc_version(void) { return 100; }
+
+}  // extern "C"

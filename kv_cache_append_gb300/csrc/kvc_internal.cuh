@@ -1,0 +1,271 @@
+// kvc_internal.cuh -- device helpers shared by the kernels of libkvc.
+//
+// Inline PTX for the sm_90+/sm_100+ asynchronous copy engine (TMA bulk
+// copies with mbarrier completion, bulk-group stores), bounded mbarrier
+// waits, storage-type conversions, and the per-row append rule of the step
+// ("Autoregressive KV-cache append and causal attention", Required behavior,
+// bullet 3).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvc.h"
+
+namespace kvc {
+
+// ----------------------------------------------------------------- constants
+constexpr int kConsumerWarps = 8;                        // attention warps per CTA
+constexpr int kFusedThreads = (kConsumerWarps + 2) * 32;  // + producer warp + storer warp
+constexpr int kMaxStages = 16;
+constexpr int kFinalizeThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;            // log2(e): scores kept in base 2
+// A pipeline wait gives up after this long (the kernel then sets
+// KVC_DEV_TIMEOUT and winds down instead of spinning forever).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// --------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete. Gives up
+// (returns false) when *abort is set by another role of the CTA, or after
+// kWaitLimitNs; in the latter case it sets *abort itself.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0 = 0;
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            const unsigned long long now = global_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitNs) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// TMA bulk copy global -> shared, completion counted on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// TMA bulk copy shared -> global in the current bulk async-group.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most N bulk groups still read shared memory.
+__device__ __forceinline__ void bulk_wait_read(int n) {
+    switch (n) {
+        case 0: asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
+        default: asm volatile("cp.async.bulk.wait_group.read 4;" ::: "memory"); break;
+    }
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Named barrier 1 among the consumer warps only.
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// 2^x on the MUFU unit; exp2(-inf) = +0.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ------------------------------------------------------------ storage types
+template <typename T>
+struct Storage;
+
+template <>
+struct Storage<float> {
+    static constexpr int kVec16 = 4;  // elements per 16 bytes
+    __device__ static void widen16(const uint4& v, float* f) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    // four consecutive elements at p (16-byte aligned)
+    __device__ static void load4(const unsigned char* p, float* f) {
+        const float4 v = *reinterpret_cast<const float4*>(p);
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    }
+    __device__ static float to_float(float x) { return x; }
+    __device__ static float from_float(float x) { return x; }
+};
+
+template <>
+struct Storage<__nv_bfloat16> {
+    static constexpr int kVec16 = 8;
+    __device__ static void two(uint32_t w, float* f) {
+        f[0] = __uint_as_float(w << 16);          // low half = first element
+        f[1] = __uint_as_float(w & 0xffff0000u);
+    }
+    __device__ static void widen16(const uint4& v, float* f) {
+        two(v.x, f); two(v.y, f + 2); two(v.z, f + 4); two(v.w, f + 6);
+    }
+    __device__ static void load4(const unsigned char* p, float* f) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        two(v.x, f); two(v.y, f + 2);
+    }
+    __device__ static float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+    __device__ static __nv_bfloat16 from_float(float x) { return __float2bfloat16_rn(x); }
+};
+
+template <>
+struct Storage<__half> {
+    static constexpr int kVec16 = 8;
+    __device__ static void two(uint32_t w, float* f) {
+        __half2 h;
+        *reinterpret_cast<uint32_t*>(&h) = w;
+        const float2 x = __half22float2(h);
+        f[0] = x.x; f[1] = x.y;
+    }
+    __device__ static void widen16(const uint4& v, float* f) {
+        two(v.x, f); two(v.y, f + 2); two(v.z, f + 4); two(v.w, f + 6);
+    }
+    __device__ static void load4(const unsigned char* p, float* f) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        two(v.x, f); two(v.y, f + 2);
+    }
+    __device__ static float to_float(__half x) { return __half2float(x); }
+    __device__ static __half from_float(float x) { return __float2half_rn(x); }
+};
+
+// ------------------------------------------------------------ per-row rule
+// The append of one batch row: n leading True entries of its mask row; a row
+// outside the contract (non-prefix mask, length outside [0, M], length + n > M)
+// appends nothing and reports a KVC_DEV_* flag.
+struct RowAppend {
+    int64_t L;   // old length
+    int64_t n;   // rows appended (0 for a flagged row)
+    int flags;   // KVC_DEV_OVERFLOW | KVC_DEV_MASK
+};
+
+__device__ __forceinline__ RowAppend row_append(const int64_t* lengths, const uint8_t* mask,
+                                                int64_t b, int64_t Q, int64_t M) {
+    RowAppend r;
+    r.L = lengths[b];
+    int64_t n = 0;
+    const uint8_t* row = mask + b * Q;
+    while (n < Q && row[n]) ++n;
+    int f = 0;
+    for (int64_t t = n; t < Q; ++t)
+        if (row[t]) f |= KVC_DEV_MASK;
+    if (r.L < 0 || r.L > M || r.L + n > M) f |= KVC_DEV_OVERFLOW;
+    r.flags = f;
+    r.n = f ? 0 : n;
+    return r;
+}
+
+// ------------------------------------------------------ work decomposition
+// Tiles of T cache slots; unit u = (b, kv head) owns tiles [u*TPU, (u+1)*TPU).
+// CTA c of P owns global tiles [floor(c*TT/P), floor((c+1)*TT/P)).
+__host__ __device__ __forceinline__ int64_t cta_first_tile(int64_t c, int64_t TT, int64_t P) {
+    return c * TT / P;
+}
+// The CTA whose range holds global tile g.
+__host__ __device__ __forceinline__ int64_t cta_of_tile(int64_t g, int64_t TT, int64_t P) {
+    return ((g + 1) * P - 1) / TT;
+}
+
+// Everything the kernels need, passed by value.
+struct StepParams {
+    // sizes
+    int64_t B, Hq, Hk, Q, D, Dv, M, G, R;  // G = Hq/Hk, R = G*Q rows per unit
+    int es;                                 // element size in bytes
+    float qscale;                           // scale * log2(e)
+    // decomposition
+    int T;        // slots per tile
+    int64_t TPU;  // tiles per unit
+    int64_t TT;   // total tiles
+    int64_t P;    // CTAs of the attention/copy kernel
+    int64_t KP;   // partial slots per unit
+    // fused-kernel layout
+    int RPW, WR, WS, NRG, SW, NS, LAG;
+    int stage_bytes, off_stages, off_q, off_p, off_state, off_state_acc, off_flag;
+    // tensors
+    const void* query;
+    const void* new_key;
+    const void* new_value;
+    const void* key_cache;
+    const void* value_cache;
+    const int64_t* lengths;
+    const uint8_t* mask;
+    void* out_key_cache;
+    void* out_value_cache;
+    int64_t* out_lengths;
+    void* out_attention;
+    void* out_context;
+    float* part_ml;   // [U][KP][R][2]  (max in base 2, sum)
+    float* part_acc;  // [U][KP][R][Dv] (unnormalised weighted values)
+    float* scores;    // [B][Hq][Q][M]  (scale*log2e*dot, allowed slots only)
+    int32_t* dev_status;
+    int vec_attention;  // 1: attention rows may be written 8 elements at a time
+};
+
+}  // namespace kvc

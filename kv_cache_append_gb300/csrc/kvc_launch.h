@@ -1,0 +1,22 @@
+// kvc_launch.h -- host-side launchers of libkvc's kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+// Fused copy + scatter + attention partials (kvc_fused.cu).
+cudaError_t launch_fused(const StepParams& p, int dtype, int dvc, size_t smem,
+                         cudaStream_t stream);
+
+// Merge of the partials, context rows and attention rows (kvc_finalize.cu).
+cudaError_t launch_finalize(const StepParams& p, int dtype, cudaStream_t stream);
+
+// Generic path for shapes or alignments the fused kernel does not take
+// (kvc_generic.cu): copy + scatter, then attention partials.
+cudaError_t launch_generic_copy(const StepParams& p, int dtype, cudaStream_t stream);
+cudaError_t launch_generic_attend(const StepParams& p, int dtype, cudaStream_t stream);
+
+}  // namespace kvc

@@ -1,0 +1,246 @@
+"""ctypes binding of libkvc (include/kvc.h).
+
+Argument marshalling only: every step of the operation runs in libkvc's CUDA
+kernels. PyTorch supplies device memory and the current stream. There is no
+CPU fallback: if libkvc.so is missing or the tensors are not on a CUDA
+device, the call raises.
+
+Python face of the step, as on the page "Autoregressive KV-cache append and
+causal attention" (Function signature / Return):
+
+    kv_cache_attention_step(query, new_key, new_value, key_cache, value_cache,
+                            lengths, append_mask, options)
+        -> {"key_cache", "value_cache", "lengths", "attention", "context"}
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvc.so")
+
+DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+
+KVC_OK = 0
+STATUS_NAMES = {0: "KVC_OK", -1: "KVC_E_NULL", -2: "KVC_E_SHAPE", -3: "KVC_E_DTYPE",
+                -4: "KVC_E_SCALE", -5: "KVC_E_WORKSPACE", -6: "KVC_E_ALIAS",
+                -7: "KVC_E_DEVICE", -8: "KVC_E_CUDA"}
+DEV_OVERFLOW, DEV_MASK, DEV_TIMEOUT = 1, 2, 4
+
+
+class KvcError(ValueError):
+    """A libkvc call returned a KVC_E_* status."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("Hq", ctypes.c_int64), ("Hk", ctypes.c_int64),
+                ("Q", ctypes.c_int64), ("D", ctypes.c_int64), ("Dv", ctypes.c_int64),
+                ("M", ctypes.c_int64), ("dtype", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libkvc.so (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with `python -m kv_cache_append_gb300.build` "
+                    "(needs nvcc); there is no CPU fallback")
+            lib = ctypes.CDLL(path)
+            vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+            dp = ctypes.POINTER(Dims)
+            lib.kvc_workspace_bytes.restype = sz
+            lib.kvc_workspace_bytes.argtypes = [dp]
+            step_args = [dp] + [vp] * 7 + [ctypes.c_double] + [vp] * 6 + [sz, vp, vp]
+            lib.kvc_step.restype = i32
+            lib.kvc_step.argtypes = step_args
+            lib.kvc_step_timed.restype = i32
+            lib.kvc_step_timed.argtypes = step_args + [ctypes.POINTER(vp), i32]
+            lib.kvc_plan_info.restype = i32
+            lib.kvc_plan_info.argtypes = [dp] + [vp] * 6 + [ctypes.POINTER(ctypes.c_char_p)]
+            lib.kvc_status_string.restype = ctypes.c_char_p
+            lib.kvc_status_string.argtypes = [i32]
+            lib.kvc_version.restype = i32
+            lib.kvc_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return library().kvc_status_string(status).decode()
+
+
+def make_dims(B, Hq, Hk, Q, D, Dv, M, dtype) -> Dims:
+    code = DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return Dims(B, Hq, Hk, Q, D, Dv, M, code)
+
+
+def dims_of(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor) -> Dims:
+    B, Hq, Q, D = query.shape
+    _, Hk, M, _ = key_cache.shape
+    return make_dims(B, Hq, Hk, Q, D, value_cache.shape[-1], M, key_cache.dtype)
+
+
+def workspace_bytes(dims: Dims) -> int:
+    return int(library().kvc_workspace_bytes(ctypes.byref(dims)))
+
+
+def plan_info(dims: Dims, key_cache, value_cache, new_key, new_value, out_key_cache,
+              out_value_cache):
+    """(kernel count, path name) kvc_step takes for these tensors."""
+    name = ctypes.c_char_p()
+    n = library().kvc_plan_info(ctypes.byref(dims), *(_p(t) for t in (
+        key_cache, value_cache, new_key, new_value, out_key_cache, out_value_cache)),
+        ctypes.byref(name))
+    if n < 0:
+        raise KvcError(n, status_string(n))
+    return n, name.value.decode()
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None or t.numel() == 0:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def default_scale(D: int) -> float:
+    """The page's default scale 1/sqrt(D)."""
+    return 1.0 / math.sqrt(D)
+
+
+def _scale_from(options: Optional[dict], D: int) -> float:
+    options = dict(options or {})
+    scale = options.pop("scale", None)
+    if options:
+        raise ValueError(f"unknown option keys {sorted(options)}: 'scale' is the only key")
+    if scale is None:
+        return default_scale(D)
+    scale = float(scale)
+    if not (scale > 0.0 and math.isfinite(scale)):
+        raise ValueError("scale must be positive and finite")
+    return scale
+
+
+def check_inputs(query, new_key, new_value, key_cache, value_cache, lengths, append_mask):
+    """Shape/dtype/device contract of the step (Required behavior, bullet 1)."""
+    for name, t in (("query", query), ("new_key", new_key), ("new_value", new_value),
+                    ("key_cache", key_cache), ("value_cache", value_cache)):
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D, got {tuple(t.shape)}")
+        if t.dtype not in DTYPES:
+            raise ValueError(f"{name}: dtype {t.dtype} not in float32/bfloat16/float16")
+        if t.dtype != query.dtype:
+            raise ValueError("query, new_key, new_value and the caches need one dtype")
+        if t.device != query.device:
+            raise ValueError("all tensors must be on one device")
+    if query.device.type != "cuda":
+        raise ValueError("kv_cache_attention_step runs on a CUDA device only (no CPU path)")
+    B, Hq, Q, D = query.shape
+    _, Hk, M, _ = key_cache.shape
+    Dv = value_cache.shape[-1]
+    if tuple(key_cache.shape) != (B, Hk, M, D):
+        raise ValueError(f"key_cache shape {tuple(key_cache.shape)} != {(B, Hk, M, D)}")
+    if tuple(value_cache.shape) != (B, Hk, M, Dv):
+        raise ValueError(f"value_cache shape {tuple(value_cache.shape)} != {(B, Hk, M, Dv)}")
+    if tuple(new_key.shape) != (B, Hk, Q, D):
+        raise ValueError(f"new_key shape {tuple(new_key.shape)} != {(B, Hk, Q, D)}")
+    if tuple(new_value.shape) != (B, Hk, Q, Dv):
+        raise ValueError(f"new_value shape {tuple(new_value.shape)} != {(B, Hk, Q, Dv)}")
+    if min(B, Hq, Hk, D, Dv, M) < 1 or Hq % Hk:
+        raise ValueError("need B,Hq,Hk,D,Dv,M >= 1 and Hq a multiple of Hk")
+    if tuple(lengths.shape) != (B,) or lengths.device != query.device:
+        raise ValueError("lengths must be [B] on the same device")
+    if lengths.dtype.is_floating_point or lengths.dtype == torch.bool:
+        raise ValueError("lengths must be integers")
+    if tuple(append_mask.shape) != (B, Q) or append_mask.device != query.device:
+        raise ValueError("append_mask must be [B, Q] on the same device")
+    if append_mask.dtype not in (torch.bool, torch.uint8):
+        raise ValueError("append_mask must be bool")
+    return B, Hq, Hk, Q, D, Dv, M
+
+
+def allocate_outputs(query, key_cache, value_cache) -> dict:
+    B, Hq, Q, _ = query.shape
+    M, Dv = key_cache.shape[2], value_cache.shape[-1]
+    dev, dt = query.device, query.dtype
+    return {
+        "key_cache": torch.empty_like(key_cache, memory_format=torch.contiguous_format),
+        "value_cache": torch.empty_like(value_cache, memory_format=torch.contiguous_format),
+        "lengths": torch.empty(B, dtype=torch.int64, device=dev),
+        "attention": torch.empty(B, Hq, Q, M, dtype=dt, device=dev),
+        "context": torch.empty(B, Hq, Q, Dv, dtype=dt, device=dev),
+    }
+
+
+def step_into(dims: Dims, query, new_key, new_value, key_cache, value_cache, lengths,
+              append_mask, scale: float, out: dict, workspace: Optional[torch.Tensor],
+              status: Optional[torch.Tensor] = None, stream: Optional[int] = None,
+              events: Optional[Sequence] = None) -> None:
+    """Enqueue one kvc_step into preallocated outputs (no checks beyond libkvc's).
+
+    All tensors must be contiguous CUDA tensors; lengths int64, append_mask
+    one byte per entry. ``events`` (torch.cuda.Event, enable_timing) are
+    recorded before the first kernel and after each kernel."""
+    lib = library()
+    if stream is None:
+        stream = torch.cuda.current_stream(query.device).cuda_stream
+    ws_ptr = _p(workspace)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    args = [ctypes.byref(dims), _p(query), _p(new_key), _p(new_value), _p(key_cache),
+            _p(value_cache), _p(lengths), _p(append_mask), ctypes.c_double(scale),
+            _p(out["key_cache"]), _p(out["value_cache"]), _p(out["lengths"]),
+            _p(out["attention"]), _p(out["context"]), ws_ptr, ws_len, _p(status),
+            ctypes.c_void_p(stream)]
+    if events:
+        handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+        rc = lib.kvc_step_timed(*args, handles, len(events))
+    else:
+        rc = lib.kvc_step(*args)
+    if rc != KVC_OK:
+        raise KvcError(rc, status_string(rc))
+
+
+def kv_cache_attention_step(query: torch.Tensor, new_key: torch.Tensor, new_value: torch.Tensor,
+                            key_cache: torch.Tensor, value_cache: torch.Tensor,
+                            lengths: torch.Tensor, append_mask: torch.Tensor,
+                            options: Optional[dict] = None,
+                            status: Optional[torch.Tensor] = None) -> dict:
+    """One autoregressive KV-cache step on the GPU.
+
+    Returns {"key_cache", "value_cache", "lengths", "attention", "context"}:
+    the whole updated caches (new rows at slots length + t for the True-prefix
+    of append_mask), lengths + n, attention [B,Hq,Q,M] and context
+    [B,Hq,Q,Dv] under the lower-right causal rule. ``options`` may hold
+    "scale" only (default 1/sqrt(D)). ``status`` is an optional int32 CUDA
+    tensor of one element into which the kernels OR contract-violation bits
+    (1 = capacity overflow, 2 = non-prefix mask); it is not synchronized.
+    """
+    check_inputs(query, new_key, new_value, key_cache, value_cache, lengths, append_mask)
+    scale = _scale_from(options, query.shape[-1])
+    q, nk, nv, kc, vc = (t.contiguous() for t in (query, new_key, new_value, key_cache,
+                                                   value_cache))
+    ln = lengths.to(torch.int64).contiguous()
+    mk = append_mask.contiguous()
+    mk = mk.view(torch.uint8) if mk.dtype == torch.bool else mk
+    dims = dims_of(q, kc, vc)
+    out = allocate_outputs(q, kc, vc)
+    nbytes = workspace_bytes(dims)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
+    with torch.cuda.device(q.device):
+        step_into(dims, q, nk, nv, kc, vc, ln, mk, scale, out, ws, status)
+    return out
