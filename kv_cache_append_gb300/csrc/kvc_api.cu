@@ -12,7 +12,6 @@ namespace kvc {
 namespace {
 
 constexpr int64_t kSizingCtas = 1024;      // workspace sizing holds for up to this many SMs
-constexpr int64_t kStageTargetBytes = 16384;
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
@@ -62,7 +61,10 @@ int check_dims(const kvc_dims* d) {
     if (B * Hk * M * (D + Dv) * es > lim || B * Hq * Q * M * 8.0 > lim ||
         B * Hq * Q * (D + Dv) * es > lim || B * Q > lim)
         return KVC_E_SHAPE;
-    if (M > (int64_t(1) << 40) || Q > (int64_t(1) << 31)) return KVC_E_SHAPE;
+    // slot, row and width indices inside the kernels are 32-bit
+    if (d->M >= (int64_t(1) << 31) || d->Q >= (int64_t(1) << 20) || d->D >= (int64_t(1) << 20) ||
+        d->Dv >= (int64_t(1) << 20) || (d->Hq / d->Hk) * d->Q >= (int64_t(1) << 20))
+        return KVC_E_SHAPE;
     return KVC_OK;
 }
 
@@ -71,9 +73,9 @@ struct Plan {
     bool fused = false;
     int T = 0;
     int64_t TPU = 0, TT = 0, P = 0, KP = 0;
-    int RPW = 4, WR = 1, WS = 8, NRG = 1, SW = 0, NS = 0, LAG = 0, DVC = 1;
+    int RPW = 4, WR = 1, WS = 8, NRG = 1, SW = 0, NS = 0, LAG = 0, DVC = 1, NCHL = 0;
     int stage_bytes = 0, off_stages = 0, off_q = 0, off_p = 0, off_state = 0, off_state_acc = 0,
-        off_flag = 0;
+        off_row_lim = 0, off_row_off = 0, off_flag = 0;
     size_t smem = 0;
     size_t off_ml = 0, off_acc = 0, off_scores = 0, ws_bytes = 0;
 };
@@ -116,7 +118,9 @@ void fused_tiling(const kvc_dims& d, Plan* pl) {
     pl->TPU = (d.M + T - 1) / T;
     pl->TT = d.B * d.Hk * pl->TPU;
     const int64_t R = (d.Hq / d.Hk) * d.Q;
-    pl->RPW = R <= 4 ? 4 : 8;
+    // Up to 32 rows per unit: 4 rows per warp, one row group each, query rows
+    // in registers. More rows: 8 rows per warp from shared memory.
+    pl->RPW = R <= 32 ? 4 : 8;
     const int64_t RG = (R + pl->RPW - 1) / pl->RPW;
     int WR = 1;
     while (WR < RG && WR < kConsumerWarps) WR *= 2;
@@ -125,6 +129,8 @@ void fused_tiling(const kvc_dims& d, Plan* pl) {
     pl->NRG = static_cast<int>(std::max<int64_t>(1, (RG + WR - 1) / WR));
     pl->SW = pl->T / pl->WS;
     pl->DVC = d.Dv <= 128 ? 1 : 2;
+    const int64_t nck = d.D * elem_size(d.dtype) / 16;  // 16-byte chunks per key row
+    pl->NCHL = pl->RPW == 4 ? static_cast<int>((nck + 7) / 8) : 0;
 }
 
 // Full fused plan for a device with `sms` SMs and `smem_cap` bytes of
@@ -145,13 +151,17 @@ bool fused_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
     pl->off_state = static_cast<int>(off);
     off = align_up(off + int64_t(pl->WS) * R * 2 * 4, 128);
     pl->off_state_acc = static_cast<int>(off);
-    off = align_up(off + int64_t(pl->WS) * R * d.Dv * 4, 1024);
+    off = align_up(off + int64_t(pl->WS) * R * d.Dv * 4, 128);
+    pl->off_row_lim = static_cast<int>(off);
+    off = align_up(off + R * 4, 16);
+    pl->off_row_off = static_cast<int>(off);
+    off = align_up(off + R * 8, 1024);
     pl->off_stages = static_cast<int>(off);
     const int64_t stage = align_up(int64_t(pl->T) * (d.D + d.Dv) * es, 128);
     pl->stage_bytes = static_cast<int>(stage);
     if (off + 2 * stage > smem_cap) return false;
     pl->NS = static_cast<int>(std::min<int64_t>(kMaxStages, (smem_cap - off) / stage));
-    pl->LAG = std::min(4, pl->NS - 1);
+    pl->LAG = std::min(std::min(kStoreLag, 7), pl->NS - 1);
     pl->smem = static_cast<size_t>(off + int64_t(pl->NS) * stage);
     pl->P = std::min<int64_t>(sms, pl->TT);
     pl->KP = pieces_bound(pl->TPU, pl->TT, pl->P);
@@ -255,6 +265,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     p.NS = pl.NS; p.LAG = pl.LAG;
     p.stage_bytes = pl.stage_bytes; p.off_stages = pl.off_stages; p.off_q = pl.off_q;
     p.off_p = pl.off_p; p.off_state = pl.off_state; p.off_state_acc = pl.off_state_acc;
+    p.off_row_lim = pl.off_row_lim; p.off_row_off = pl.off_row_off;
     p.off_flag = pl.off_flag;
     p.query = query; p.new_key = new_key; p.new_value = new_value;
     p.key_cache = key_cache; p.value_cache = value_cache;
@@ -280,7 +291,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     cudaError_t e = record();
     if (e == cudaSuccess) {
         if (pl.fused) {
-            e = launch_fused(p, d.dtype, pl.DVC, pl.smem, stream);
+            e = launch_fused(p, d.dtype, pl.DVC, pl.NCHL, pl.smem, stream);
             if (e == cudaSuccess) e = record();
         } else {
             e = launch_generic_copy(p, d.dtype, stream);

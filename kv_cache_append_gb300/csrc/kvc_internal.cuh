@@ -19,7 +19,18 @@ namespace kvc {
 // ----------------------------------------------------------------- constants
 constexpr int kConsumerWarps = 8;                        // attention warps per CTA
 constexpr int kFusedThreads = (kConsumerWarps + 2) * 32;  // + producer warp + storer warp
-constexpr int kMaxStages = 16;
+#ifndef KVC_MAX_STAGES
+#define KVC_MAX_STAGES 16
+#endif
+#ifndef KVC_STAGE_BYTES
+#define KVC_STAGE_BYTES 32768
+#endif
+#ifndef KVC_STORE_LAG
+#define KVC_STORE_LAG 4
+#endif
+constexpr int kMaxStages = KVC_MAX_STAGES;        // ring stages at most
+constexpr int kStageTargetBytes = KVC_STAGE_BYTES;  // cache bytes (K + V) per tile
+constexpr int kStoreLag = KVC_STORE_LAG;          // bulk-store groups in flight per CTA
 constexpr int kFinalizeThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;            // log2(e): scores kept in base 2
 // A pipeline wait gives up after this long (the kernel then sets
@@ -116,7 +127,10 @@ __device__ __forceinline__ void bulk_wait_read(int n) {
         case 1: asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); break;
         case 2: asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); break;
         case 3: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
-        default: asm volatile("cp.async.bulk.wait_group.read 4;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.bulk.wait_group.read 4;" ::: "memory"); break;
+        case 5: asm volatile("cp.async.bulk.wait_group.read 5;" ::: "memory"); break;
+        case 6: asm volatile("cp.async.bulk.wait_group.read 6;" ::: "memory"); break;
+        default: asm volatile("cp.async.bulk.wait_group.read 7;" ::: "memory"); break;
     }
 }
 
@@ -154,6 +168,16 @@ struct Storage<float> {
         const float4 v = *reinterpret_cast<const float4*>(p);
         f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
     }
+    // 16 bytes as two (even, odd) element pairs
+    __device__ static void widen16_2(const uint4& v, float2* f) {
+        f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+        f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+    }
+    __device__ static void load4_2(const unsigned char* p, float2* f) {
+        const float4 v = *reinterpret_cast<const float4*>(p);
+        f[0] = make_float2(v.x, v.y);
+        f[1] = make_float2(v.z, v.w);
+    }
     __device__ static float to_float(float x) { return x; }
     __device__ static float from_float(float x) { return x; }
 };
@@ -171,6 +195,16 @@ struct Storage<__nv_bfloat16> {
     __device__ static void load4(const unsigned char* p, float* f) {
         const uint2 v = *reinterpret_cast<const uint2*>(p);
         two(v.x, f); two(v.y, f + 2);
+    }
+    __device__ static float2 pair(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    __device__ static void widen16_2(const uint4& v, float2* f) {
+        f[0] = pair(v.x); f[1] = pair(v.y); f[2] = pair(v.z); f[3] = pair(v.w);
+    }
+    __device__ static void load4_2(const unsigned char* p, float2* f) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        f[0] = pair(v.x); f[1] = pair(v.y);
     }
     __device__ static float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
     __device__ static __nv_bfloat16 from_float(float x) { return __float2bfloat16_rn(x); }
@@ -191,6 +225,18 @@ struct Storage<__half> {
     __device__ static void load4(const unsigned char* p, float* f) {
         const uint2 v = *reinterpret_cast<const uint2*>(p);
         two(v.x, f); two(v.y, f + 2);
+    }
+    __device__ static float2 pair(uint32_t w) {
+        __half2 h;
+        *reinterpret_cast<uint32_t*>(&h) = w;
+        return __half22float2(h);
+    }
+    __device__ static void widen16_2(const uint4& v, float2* f) {
+        f[0] = pair(v.x); f[1] = pair(v.y); f[2] = pair(v.z); f[3] = pair(v.w);
+    }
+    __device__ static void load4_2(const unsigned char* p, float2* f) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        f[0] = pair(v.x); f[1] = pair(v.y);
     }
     __device__ static float to_float(__half x) { return __half2float(x); }
     __device__ static __half from_float(float x) { return __float2half_rn(x); }
@@ -247,7 +293,8 @@ struct StepParams {
     int64_t KP;   // partial slots per unit
     // fused-kernel layout
     int RPW, WR, WS, NRG, SW, NS, LAG;
-    int stage_bytes, off_stages, off_q, off_p, off_state, off_state_acc, off_flag;
+    int stage_bytes, off_stages, off_q, off_p, off_state, off_state_acc, off_row_lim, off_row_off,
+        off_flag;
     // tensors
     const void* query;
     const void* new_key;

@@ -8,7 +8,9 @@
 namespace kvc {
 
 // Fused copy + scatter + attention partials (kvc_fused.cu).
-cudaError_t launch_fused(const StepParams& p, int dtype, int dvc, size_t smem,
+// nchl > 0: 4 query rows per warp held in registers as nchl 16-byte chunks
+// per lane; nchl == 0: 8 rows per warp read from shared memory.
+cudaError_t launch_fused(const StepParams& p, int dtype, int dvc, int nchl, size_t smem,
                          cudaStream_t stream);
 
 // Merge of the partials, context rows and attention rows (kvc_finalize.cu).
