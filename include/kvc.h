@@ -65,6 +65,8 @@ typedef struct {
 #define KVC_E_ALIAS (-6)     /* an output overlaps an input, another output or the workspace */
 #define KVC_E_DEVICE (-7)    /* current device is not an sm_103 GPU */
 #define KVC_E_CUDA (-8)      /* a CUDA call or kernel launch failed */
+#define KVC_E_STATIC_LIMIT (-9) /* kvc_step_static: the sizes need more than
+                                   KVC_STATIC_SCRATCH_BYTES of scratch */
 
 /* Bits OR-ed into *dev_status by the kernels (never cleared by the library). */
 #define KVC_DEV_OVERFLOW 1 /* some row had length < 0, length > M or length + n > M */
@@ -144,6 +146,37 @@ KVC_API int kvc_step_timed(const kvc_dims *dims, const void *query, const void *
 KVC_API int kvc_plan_info(const kvc_dims *dims, const void *key_cache, const void *value_cache,
                   const void *new_key, const void *new_value, const void *out_key_cache,
                   const void *out_value_cache, const char **path_name);
+
+/*
+ * kvc_step_static -- kvc_step for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a deployment variant of kvc_step.
+ *
+ * Some callers cannot call cudaMalloc (or any allocator) when they run the
+ * step: serving loops that reserve all device memory up front, plugins whose
+ * host framework owns the device allocator, or code that cannot accept the
+ * device-wide synchronisation of cudaMalloc/cudaFree. They still pass inputs
+ * and outputs exactly as for kvc_step, but no workspace: the scratch is one
+ * library-owned __device__ array of KVC_STATIC_SCRATCH_BYTES (96 MiB), held
+ * by every GPU that loads the library until the process exits.
+ *
+ * Arguments and results are those of kvc_step without workspace and
+ * workspace_bytes. Sizes whose kvc_workspace_bytes() exceeds
+ * KVC_STATIC_SCRATCH_BYTES are rejected with KVC_E_STATIC_LIMIT before any
+ * launch (the gqa_decode shape, B=64 Hq=32 Hk=8 Q=1 M=8192, needs about
+ * 70 MB). The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture. Every call shares the one array: calls whose
+ * kernels may overlap on the GPU (unordered streams) race and must not be
+ * issued; calls ordered on one stream are fine. Nothing in the array needs
+ * clearing between calls. Never allocates device memory.
+ */
+#define KVC_STATIC_SCRATCH_BYTES (96ull << 20)
+KVC_API int kvc_step_static(const kvc_dims *dims, const void *query, const void *new_key,
+                            const void *new_value, const void *key_cache,
+                            const void *value_cache, const int64_t *lengths,
+                            const uint8_t *append_mask, double scale, void *out_key_cache,
+                            void *out_value_cache, int64_t *out_lengths, void *out_attention,
+                            void *out_context, int32_t *dev_status, void *stream);
 
 /* Static text for a KVC_OK / KVC_E_* code. */
 KVC_API const char *kvc_status_string(int status);

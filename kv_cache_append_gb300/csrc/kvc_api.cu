@@ -383,6 +383,8 @@ const char* kvc_status_string(int status) {
         case KVC_E_ALIAS: return "an output overlaps an input, another output or the workspace";
         case KVC_E_DEVICE: return "the current CUDA device is not an sm_103 (GB300) GPU";
         case KVC_E_CUDA: return "a CUDA call or kernel launch failed";
+        case KVC_E_STATIC_LIMIT:
+            return "kvc_step_static: these sizes need more scratch than KVC_STATIC_SCRATCH_BYTES";
         default: return "unknown status";
     }
 }

@@ -30,7 +30,7 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 KVC_OK = 0
 STATUS_NAMES = {0: "KVC_OK", -1: "KVC_E_NULL", -2: "KVC_E_SHAPE", -3: "KVC_E_DTYPE",
                 -4: "KVC_E_SCALE", -5: "KVC_E_WORKSPACE", -6: "KVC_E_ALIAS",
-                -7: "KVC_E_DEVICE", -8: "KVC_E_CUDA"}
+                -7: "KVC_E_DEVICE", -8: "KVC_E_CUDA", -9: "KVC_E_STATIC_LIMIT"}
 DEV_OVERFLOW, DEV_MASK, DEV_TIMEOUT = 1, 2, 4
 
 
@@ -71,6 +71,8 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kvc_step.argtypes = step_args
             lib.kvc_step_timed.restype = i32
             lib.kvc_step_timed.argtypes = step_args + [ctypes.POINTER(vp), i32]
+            lib.kvc_step_static.restype = i32
+            lib.kvc_step_static.argtypes = [dp] + [vp] * 7 + [ctypes.c_double] + [vp] * 7
             lib.kvc_plan_info.restype = i32
             lib.kvc_plan_info.argtypes = [dp] + [vp] * 6 + [ctypes.POINTER(ctypes.c_char_p)]
             lib.kvc_status_string.restype = ctypes.c_char_p
