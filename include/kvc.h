@@ -74,11 +74,11 @@ typedef struct {
 #define KVC_DEV_TIMEOUT 4  /* an internal pipeline wait gave up (outputs invalid) */
 
 /*
- * Bytes of device workspace kvc_step needs for these sizes (0 when Q == 0).
- * Pure host arithmetic; valid for any GPU with at most 1024 SMs.
- * Returns 0 and sets nothing for invalid dims (kvc_step then reports why).
- * Holds the per-split softmax partials (max, sum, weighted values, fp32) and
- * one fp32 score per (b, h, t, slot).
+ * Bytes of device workspace kvc_step needs for these sizes (at least 256,
+ * also when Q == 0). Pure host arithmetic; valid for any GPU with at most
+ * 256 SMs. Returns 0 for invalid dims (kvc_step then reports why).
+ * Holds the work counter of the fused kernel, the per-chunk softmax partials
+ * (max, sum, weighted values, fp32) and one fp32 score per (b, h, t, slot).
  */
 KVC_API size_t kvc_workspace_bytes(const kvc_dims *dims);
 
@@ -103,7 +103,6 @@ KVC_API size_t kvc_workspace_bytes(const kvc_dims *dims);
  *   out_context     [B,Hq,Q,Dv]   device, dtype. May be NULL iff Q == 0.
  *   workspace       device scratch of workspace_bytes >= kvc_workspace_bytes(dims),
  *                   16-byte aligned; contents on entry do not matter.
- *                   May be NULL iff kvc_workspace_bytes(dims) == 0.
  *   dev_status      device int32, nullable. The kernels OR KVC_DEV_* bits into it.
  *   stream          cudaStream_t to enqueue on.
  *

@@ -11,7 +11,7 @@
 namespace kvc {
 namespace {
 
-constexpr int64_t kSizingCtas = 1024;      // workspace sizing holds for up to this many SMs
+constexpr int64_t kSizingCtas = 256;       // workspace sizing holds for up to this many SMs
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
@@ -72,13 +72,23 @@ int check_dims(const kvc_dims* d) {
 struct Plan {
     bool fused = false;
     int T = 0;
-    int64_t TPU = 0, TT = 0, P = 0, KP = 0;
+    int64_t TPU = 0, CH = 1, KP = 1, NQ = 0, P = 0;
     int RPW = 4, WR = 1, WS = 8, NRG = 1, SW = 0, NS = 0, LAG = 0, DVC = 1, NCHL = 0;
     int stage_bytes = 0, off_stages = 0, off_q = 0, off_p = 0, off_state = 0, off_state_acc = 0,
-        off_row_lim = 0, off_row_off = 0, off_flag = 0;
+        off_row_lim = 0, off_row_off = 0, off_flag = 0, off_meta = 0;
+    bool q_staged = false;
+    int q_stage_bytes = 0, off_stage_q = 0;
     size_t smem = 0;
-    size_t off_ml = 0, off_acc = 0, off_scores = 0, ws_bytes = 0;
+    size_t off_counter = 0, off_ml = 0, off_acc = 0, off_scores = 0, ws_bytes = 0;
 };
+
+#ifndef KVC_CHUNKS_PER_CTA
+#define KVC_CHUNKS_PER_CTA 32
+#endif
+constexpr int64_t kChunksPerCta = KVC_CHUNKS_PER_CTA;  // aim: this many chunks per CTA
+constexpr int64_t kMinChunksPerCta = 8;   // never fewer (every CTA busy, tail short)
+constexpr int64_t kPartialRatio = 16;     // a chunk moves >= 16x its partials' bytes
+constexpr int64_t kMaxStagedQuery = 16384;
 
 // Whether the fused kernel's row shapes apply (16-byte rows, widths it holds).
 bool fused_shapes(const kvc_dims& d) {
@@ -86,18 +96,11 @@ bool fused_shapes(const kvc_dims& d) {
     return (d.D * es) % 16 == 0 && (d.Dv * es) % 16 == 0 && d.D * es <= 512 && d.Dv <= 256;
 }
 
-int64_t pieces_bound(int64_t TPU, int64_t TT, int64_t P) {
-    const int64_t shortest = TT / P;  // >= 1 since P <= TT
-    return std::min<int64_t>(P, (TPU - 1) / shortest + 2);
-}
-
 void workspace_layout(const kvc_dims& d, int64_t KP, Plan* pl) {
     const int64_t U = d.B * d.Hk, R = (d.Hq / d.Hk) * d.Q;
-    if (d.Q == 0) {
-        pl->off_ml = pl->off_acc = pl->off_scores = pl->ws_bytes = 0;
-        return;
-    }
     int64_t off = 0;
+    pl->off_counter = static_cast<size_t>(off);
+    off = 256;
     pl->off_ml = static_cast<size_t>(off);
     off = align_up(off + U * KP * R * 2 * 4, 256);
     pl->off_acc = static_cast<size_t>(off);
@@ -116,7 +119,6 @@ void fused_tiling(const kvc_dims& d, Plan* pl) {
     if (d.M < T) T = align_up(d.M, 32);
     pl->T = static_cast<int>(T);
     pl->TPU = (d.M + T - 1) / T;
-    pl->TT = d.B * d.Hk * pl->TPU;
     const int64_t R = (d.Hq / d.Hk) * d.Q;
     // Up to 32 rows per unit: 4 rows per warp, one row group each, query rows
     // in registers. More rows: 8 rows per warp from shared memory.
@@ -129,23 +131,44 @@ void fused_tiling(const kvc_dims& d, Plan* pl) {
     pl->NRG = static_cast<int>(std::max<int64_t>(1, (RG + WR - 1) / WR));
     pl->SW = pl->T / pl->WS;
     pl->DVC = d.Dv <= 128 ? 1 : 2;
-    const int64_t nck = d.D * elem_size(d.dtype) / 16;  // 16-byte chunks per key row
+    const int64_t nck = d.D * es / 16;  // 16-byte chunks per key row
     pl->NCHL = pl->RPW == 4 ? static_cast<int>((nck + 7) / 8) : 0;
+}
+
+// Chunks for `ctas` CTAs: about kChunksPerCta chunks per CTA, bigger when a
+// chunk's partials would be more than 1/kPartialRatio of the bytes it moves,
+// but never so big that a CTA gets fewer than kMinChunksPerCta.
+void chunking(const kvc_dims& d, int64_t ctas, Plan* pl) {
+    const int64_t es = elem_size(d.dtype);
+    const int64_t U = d.B * d.Hk, R = (d.Hq / d.Hk) * d.Q;
+    const int64_t TT = U * pl->TPU;
+    const int64_t tile_bytes = int64_t(pl->T) * (d.D + d.Dv) * es;
+    const int64_t ch_part = (kPartialRatio * R * (d.Dv + 2) * 4 + tile_bytes - 1) / tile_bytes;
+    int64_t ch = std::max<int64_t>(TT / (ctas * kChunksPerCta), ch_part);
+    ch = std::min<int64_t>(ch, TT / (ctas * kMinChunksPerCta));
+    ch = std::max<int64_t>(1, std::min<int64_t>(ch, pl->TPU));
+    pl->CH = ch;
+    pl->KP = (pl->TPU + ch - 1) / ch;
+    pl->NQ = U * pl->KP;
 }
 
 // Full fused plan for a device with `sms` SMs and `smem_cap` bytes of
 // opt-in shared memory per block. False if it does not fit.
-bool fused_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
+bool fused_plan(const kvc_dims& d, int sms, int smem_cap, bool query_aligned, Plan* pl) {
     if (!fused_shapes(d)) return false;
     fused_tiling(d, pl);
     const int64_t es = elem_size(d.dtype);
     const int64_t R = (d.Hq / d.Hk) * d.Q;
+    const int64_t qbytes = R * d.D * es;
+    pl->q_staged = d.Q > 0 && query_aligned && qbytes <= kMaxStagedQuery;
+    if (pl->RPW == 4 && d.Q > 0 && !pl->q_staged) return false;  // register path reads staged rows
+    pl->q_stage_bytes = pl->q_staged ? static_cast<int>(qbytes) : 0;
     const int64_t RGpad = (R + pl->RPW - 1) / pl->RPW * pl->RPW;
-    int64_t off = 2 * kMaxStages * 8;
-    pl->off_flag = static_cast<int>(off);
-    off = 512;
+    pl->off_flag = 512;
+    pl->off_meta = 1024;  // kMaxStages metadata records of 32 bytes
+    int64_t off = 1024 + kMaxStages * 32;
     pl->off_q = static_cast<int>(off);
-    off = align_up(off + RGpad * d.D * 4, 128);
+    off = align_up(off + (pl->RPW == 4 ? 0 : RGpad * d.D * 4), 128);
     pl->off_p = static_cast<int>(off);
     off = align_up(off + int64_t(kConsumerWarps) * pl->SW * pl->RPW * 4, 128);
     pl->off_state = static_cast<int>(off);
@@ -157,14 +180,16 @@ bool fused_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
     pl->off_row_off = static_cast<int>(off);
     off = align_up(off + R * 8, 1024);
     pl->off_stages = static_cast<int>(off);
-    const int64_t stage = align_up(int64_t(pl->T) * (d.D + d.Dv) * es, 128);
+    const int64_t kv_bytes = int64_t(pl->T) * (d.D + d.Dv) * es;
+    pl->off_stage_q = static_cast<int>(align_up(kv_bytes, 16));
+    const int64_t stage = align_up(pl->off_stage_q + pl->q_stage_bytes, 128);
     pl->stage_bytes = static_cast<int>(stage);
     if (off + 2 * stage > smem_cap) return false;
     pl->NS = static_cast<int>(std::min<int64_t>(kMaxStages, (smem_cap - off) / stage));
     pl->LAG = std::min(std::min(kStoreLag, 7), pl->NS - 1);
     pl->smem = static_cast<size_t>(off + int64_t(pl->NS) * stage);
-    pl->P = std::min<int64_t>(sms, pl->TT);
-    pl->KP = pieces_bound(pl->TPU, pl->TT, pl->P);
+    chunking(d, sms, pl);
+    pl->P = std::min<int64_t>(sms, pl->NQ);
     pl->fused = true;
     workspace_layout(d, pl->KP, pl);
     return true;
@@ -175,9 +200,10 @@ void generic_plan(const kvc_dims& d, Plan* pl) {
     pl->fused = false;
     pl->T = static_cast<int>(std::min<int64_t>(d.M, int64_t(1) << 30));
     pl->TPU = 1;
-    pl->TT = d.B * d.Hk;
-    pl->P = pl->TT;
+    pl->CH = 1;
     pl->KP = 1;
+    pl->NQ = d.B * d.Hk;
+    pl->P = pl->NQ;
     workspace_layout(d, 1, pl);
 }
 
@@ -221,7 +247,8 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
                               aligned16(out_key_cache) && aligned16(out_value_cache) &&
                               (!hasq || (aligned16(new_key) && aligned16(new_value)));
     Plan pl;
-    if (!(ptrs_aligned && fused_plan(d, dev.sms, dev.smem_optin, &pl))) generic_plan(d, &pl);
+    if (!(ptrs_aligned && fused_plan(d, dev.sms, dev.smem_optin, aligned16(query), &pl)))
+        generic_plan(d, &pl);
 
     if (pl.ws_bytes > 0) {
         if (!workspace || workspace_bytes < pl.ws_bytes || !aligned16(workspace))
@@ -260,12 +287,14 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     p.R = p.G * d.Q;
     p.es = static_cast<int>(es);
     p.qscale = static_cast<float>(scale * 1.4426950408889634);
-    p.T = pl.T; p.TPU = pl.TPU; p.TT = pl.TT; p.P = pl.P; p.KP = pl.KP;
+    p.T = pl.T; p.TPU = pl.TPU; p.CH = pl.CH; p.KP = pl.KP; p.NQ = pl.NQ; p.P = pl.P;
     p.RPW = pl.RPW; p.WR = pl.WR; p.WS = pl.WS; p.NRG = pl.NRG; p.SW = pl.SW;
     p.NS = pl.NS; p.LAG = pl.LAG;
     p.stage_bytes = pl.stage_bytes; p.off_stages = pl.off_stages; p.off_q = pl.off_q;
     p.off_p = pl.off_p; p.off_state = pl.off_state; p.off_state_acc = pl.off_state_acc;
-    p.off_row_lim = pl.off_row_lim; p.off_row_off = pl.off_row_off;
+    p.off_row_lim = pl.off_row_lim; p.off_row_off = pl.off_row_off; p.off_meta = pl.off_meta;
+    p.q_staged = pl.q_staged ? 1 : 0; p.q_stage_bytes = pl.q_stage_bytes;
+    p.off_stage_q = pl.off_stage_q;
     p.off_flag = pl.off_flag;
     p.query = query; p.new_key = new_key; p.new_value = new_value;
     p.key_cache = key_cache; p.value_cache = value_cache;
@@ -277,6 +306,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
         p.part_ml = reinterpret_cast<float*>(ws + pl.off_ml);
         p.part_acc = reinterpret_cast<float*>(ws + pl.off_acc);
         p.scores = reinterpret_cast<float*>(ws + pl.off_scores);
+        p.counter = reinterpret_cast<unsigned int*>(ws + pl.off_counter);
     }
     p.dev_status = dev_status;
     p.vec_attention = (d.M % 8 == 0) && aligned16(out_attention);
@@ -291,7 +321,9 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     cudaError_t e = record();
     if (e == cudaSuccess) {
         if (pl.fused) {
-            e = launch_fused(p, d.dtype, pl.DVC, pl.NCHL, pl.smem, stream);
+            // chunks are handed out from a counter that starts at zero
+            if (p.counter) e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream);
+            if (e == cudaSuccess) e = launch_fused(p, d.dtype, pl.DVC, pl.NCHL, pl.smem, stream);
             if (e == cudaSuccess) e = record();
         } else {
             e = launch_generic_copy(p, d.dtype, stream);
@@ -317,12 +349,13 @@ extern "C" {
 
 size_t kvc_workspace_bytes(const kvc_dims* dims) {
     using namespace kvc;
-    if (check_dims(dims) != KVC_OK || dims->Q == 0) return 0;
+    if (check_dims(dims) != KVC_OK) return 0;
     Plan pl;
     if (fused_shapes(*dims)) {
+        // more CTAs make smaller chunks, hence more partial slots: size for the most
         fused_tiling(*dims, &pl);
-        const int64_t P = std::min<int64_t>(kSizingCtas, pl.TT);
-        workspace_layout(*dims, pieces_bound(pl.TPU, pl.TT, P), &pl);
+        chunking(*dims, kSizingCtas, &pl);
+        workspace_layout(*dims, pl.KP, &pl);
     } else {
         generic_plan(*dims, &pl);
     }
@@ -367,7 +400,7 @@ int kvc_plan_info(const kvc_dims* dims, const void* key_cache, const void* value
                               aligned16(out_key_cache) && aligned16(out_value_cache) &&
                               (!hasq || (aligned16(new_key) && aligned16(new_value)));
     Plan pl;
-    const bool fused = ptrs_aligned && fused_plan(*dims, dev.sms, dev.smem_optin, &pl);
+    const bool fused = ptrs_aligned && fused_plan(*dims, dev.sms, dev.smem_optin, true, &pl);
     if (path_name) *path_name = fused ? "fused" : "generic";
     return fused ? (hasq ? 2 : 1) : (hasq ? 3 : 1);
 }

@@ -1,7 +1,7 @@
 // kvc_finalize.cu -- split combine and attention-row writer of libkvc.
 //
 // One CTA per query row (b, h, t). For a valid row (t < n_b) it merges the
-// per-piece partials (m_k, l_k, acc_k) of the row's unit with the
+// per-chunk partials (m_k, l_k, acc_k) of the row's unit with the
 // log-sum-exp rescale  m = max m_k,  l = sum l_k 2^(m_k - m),
 // context = sum acc_k 2^(m_k - m) / l  ("context = attention . updated_values",
 // "stable softmax on allowed keys", Required behavior, bullet 5), then writes
@@ -64,18 +64,10 @@ __global__ void __launch_bounds__(kFinalizeThreads)
     int64_t lim = -1;  // last allowed slot
     if (valid) {
         lim = ra.L + t;
-        const int64_t first = u * p.TPU;
-        const int64_t cf = cta_of_tile(first, p.TT, p.P);
-        const int64_t np = cta_of_tile(first + p.TPU - 1, p.TT, p.P) - cf + 1;
-        // pieces whose first slot is allowed for this row
-        int64_t kmax = 0;
+        // chunks whose first slot is allowed for this row wrote a partial
+        const int64_t kmax = min(p.KP, lim / (p.CH * p.T) + 1);
         mx = -INFINITY;
-        for (int64_t k = 0; k < np; ++k) {
-            const int64_t g = max(cta_first_tile(cf + k, p.TT, p.P), first);
-            if ((g - first) * p.T > lim) break;
-            kmax = k + 1;
-            mx = fmaxf(mx, p.part_ml[2 * ((u * p.KP + k) * p.R + r)]);
-        }
+        for (int64_t k = 0; k < kmax; ++k) mx = fmaxf(mx, p.part_ml[2 * ((u * p.KP + k) * p.R + r)]);
         float l = 0.f;
         for (int64_t k = 0; k < kmax; ++k) {
             const int64_t pr = (u * p.KP + k) * p.R + r;

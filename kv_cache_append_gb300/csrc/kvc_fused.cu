@@ -1,15 +1,20 @@
 // kvc_fused.cu -- the fused append + attention kernel of libkvc.
 //
-// One persistent CTA per SM streams an equal share of all cache tiles
-// (T slots of one (b, kv-head) unit; K rows then V rows) through a ring of
-// shared-memory stages:
+// One persistent CTA per SM. Work comes in chunks of CH consecutive tiles of
+// one (b, kv-head) unit (a tile is T cache slots, K rows then V rows); the
+// CTA's producer takes the next chunk from a global counter, so CTAs that
+// draw attention-heavy chunks simply take fewer of them. Chunks are handed
+// out chunk-index-major (chunk 0 of every unit first), which puts the tiles
+// that hold the valid prefix early and the pure-copy tails last. Each tile
+// goes through a ring of shared-memory stages:
 //
-//   producer warp  TMA bulk-loads the UPDATED cache rows of a tile: old rows
-//                  from key_cache/value_cache, rows [length, length+n) straight
-//                  from new_key/new_value ("Write new_key/value at positions
-//                  length+t only for True append slots t", Required behavior,
-//                  bullet 3). So the tile in shared memory is exactly the
-//                  returned cache tile.
+//   producer warp  takes chunks, writes each tile's metadata into its stage
+//                  and TMA bulk-loads the UPDATED cache rows of the tile: old
+//                  rows from key_cache/value_cache, rows [length, length+n)
+//                  straight from new_key/new_value ("Write new_key/value at
+//                  positions length+t only for True append slots t", Required
+//                  behavior, bullet 3), plus the unit's query rows with the
+//                  first tile of a chunk that attends.
 //   storer warp    TMA bulk-stores every tile to out_key_cache/out_value_cache
 //                  ("Return the entire updated cache, preserving every
 //                  unwritten entry exactly", bullet 4): a bit copy, never
@@ -20,8 +25,8 @@
 //                  keep an online max / sum-exp / weighted-value state per row
 //                  under the lower-right causal limit j <= length + t (bullet
 //                  4), and store each score for the attention rows. At the
-//                  end of the CTA's piece of a unit they write one partial
-//                  (max, sum, weighted values) per row.
+//                  end of a chunk they write one partial (max, sum, weighted
+//                  values) per row into the chunk's slot.
 //
 // So the valid prefix of the cache is read from HBM once and serves both the
 // copy and the attention. kvc_finalize.cu merges the partials.
@@ -51,8 +56,24 @@ __device__ __forceinline__ Unit load_unit(const StepParams& p, int64_t u) {
 struct Bars {
     uint32_t base;
     __device__ uint32_t full(int s) const { return base + 8u * s; }
-    __device__ uint32_t empty(int s) const { return base + 8u * (kMaxStages + s); }
+    __device__ uint32_t empty(int s) const { return base + 128u + 8u * s; }
+    __device__ uint32_t consumers() const { return base + 256u; }  // consumer-warp rendezvous
 };
+
+// What the producer tells the other roles about the tile in a stage.
+struct TileMeta {
+    int64_t L;     // old length of the unit's batch row
+    int64_t u;     // unit = b * Hk + kv
+    int32_t n;     // rows appended (0 for a flagged row)
+    int32_t i;     // tile index within the unit
+    int32_t k;     // chunk index within the unit
+    int32_t flags;
+};
+static_assert(sizeof(TileMeta) == 32, "TileMeta is 32 bytes");
+constexpr int kFirst = 1;    // first tile of its chunk
+constexpr int kLast = 2;     // last tile of its chunk
+constexpr int kDone = 4;     // no more tiles: the roles stop
+constexpr int kQStaged = 8;  // the stage also holds the unit's query rows
 
 // Position in the stage ring: stage index and the parity of its current lap.
 struct Ring {
@@ -100,87 +121,110 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
     mbar_wait(bar, parity, &never);
 }
 
-// Tiles of unit u inside the CTA's global range [g0, g1): local [i_lo, i_hi).
-struct Piece {
-    int64_t i_lo, i_hi;
-};
-
-__device__ __forceinline__ Piece piece_of(const StepParams& p, int64_t u, int64_t g0, int64_t g1) {
-    const int64_t first = u * p.TPU;
-    return Piece{max(g0, first) - first, min(g1, first + p.TPU) - first};
-}
-
 __device__ void run_producer(const StepParams& p, unsigned char* smem, Bars bars,
-                             volatile int* abort, int64_t g0, int64_t g1) {
+                             volatile int* abort) {
     const int64_t rowK = p.D * p.es, rowV = p.Dv * p.es;
     const uint32_t stage0 = smem_addr(smem + p.off_stages);
     const uint32_t vofs = static_cast<uint32_t>(p.T * rowK);
+    TileMeta* meta = reinterpret_cast<TileMeta*>(smem + p.off_meta);
     const unsigned char* kc = static_cast<const unsigned char*>(p.key_cache);
     const unsigned char* vc = static_cast<const unsigned char*>(p.value_cache);
     const unsigned char* nk = static_cast<const unsigned char*>(p.new_key);
     const unsigned char* nv = static_cast<const unsigned char*>(p.new_value);
+    const unsigned char* qry = static_cast<const unsigned char*>(p.query);
+    const int64_t U = p.B * p.Hk;
     int64_t issued = 0;
     Ring ring;
     bool ok = true;
-    for (int64_t u = g0 / p.TPU; ok && u * p.TPU < g1; ++u) {
+    while (ok) {
+        const int64_t q = atomicAdd(p.counter, 1u);
+        if (q >= p.NQ) break;
+#if KVC_CHUNK_ORDER == 1
+        // alternate the two ends of the chunk-index-major list: attention-heavy
+        // first chunks and pure-copy last chunks are in flight together, and the
+        // list runs out in its middle
+        const int64_t idx = (q & 1) ? p.NQ - 1 - (q >> 1) : (q >> 1);
+#else
+        const int64_t idx = q;
+#endif
+        const int64_t k = idx / U, u = idx - k * U;  // chunk-index-major list
         const Unit x = load_unit(p, u);
-        const Piece pc = piece_of(p, u, g0, g1);
+        const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, p.TPU);
+        const bool attend = x.n > 0 && i0 * p.T < x.N;
         const unsigned char* kcu = kc + u * p.M * rowK;
         const unsigned char* vcu = vc + u * p.M * rowV;
         const unsigned char* nku = nk + u * p.Q * rowK;
         const unsigned char* nvu = nv + u * p.Q * rowV;
-        for (int64_t i = pc.i_lo; i < pc.i_hi; ++i) {
+        for (int64_t i = i0; i < i1; ++i) {
             if (issued >= p.NS && !mbar_wait(bars.empty(ring.s), ring.ph ^ 1u, abort)) {
                 ok = false;
                 break;
             }
             const int64_t j0 = i * p.T, j1 = min(j0 + p.T, p.M);
+            const bool stage_q = attend && p.q_staged && i == i0;
+            TileMeta& mt = meta[ring.s];
+            mt.L = x.L;
+            mt.u = u;
+            mt.n = static_cast<int32_t>(x.n);
+            mt.i = static_cast<int32_t>(i);
+            mt.k = static_cast<int32_t>(k);
+            mt.flags = (i == i0 ? kFirst : 0) | (i == i1 - 1 ? kLast : 0) | (stage_q ? kQStaged : 0);
             const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
-            mbar_arrive_expect_tx(bars.full(ring.s),
-                                  static_cast<uint32_t>((j1 - j0) * (rowK + rowV)));
+            uint32_t bytes = static_cast<uint32_t>((j1 - j0) * (rowK + rowV));
+            if (stage_q) bytes += static_cast<uint32_t>(p.q_stage_bytes);
+            mbar_arrive_expect_tx(bars.full(ring.s), bytes);  // publishes the metadata too
             load_rows(sK, kcu, nku, rowK, j0, j1, x.L, x.N, bars.full(ring.s));
             load_rows(sK + vofs, vcu, nvu, rowV, j0, j1, x.L, x.N, bars.full(ring.s));
+            if (stage_q)  // the G*Q query rows of the unit are contiguous in query
+                bulk_g2s(sK + static_cast<uint32_t>(p.off_stage_q),
+                         qry + (x.b * p.Hq + x.kv * p.G) * p.Q * rowK,
+                         static_cast<uint32_t>(p.q_stage_bytes), bars.full(ring.s));
             ++issued;
             ring.next(p.NS);
         }
     }
-    // Do not leave while issued copies may still write shared memory.
+    if (ok) {  // sentinel tile: tells the storer and the consumers to stop
+        if (issued < p.NS || mbar_wait(bars.empty(ring.s), ring.ph ^ 1u, abort)) {
+            meta[ring.s].flags = kDone;
+            mbar_arrive_expect_tx(bars.full(ring.s), 0u);
+            return;
+        }
+    }
+    // Gave up: do not leave while issued copies may still write shared memory.
     for (int64_t q = issued > p.NS ? issued - p.NS : 0; q < issued; ++q)
         mbar_drain(bars.full(static_cast<int>(q % p.NS)), static_cast<uint32_t>((q / p.NS) & 1));
 }
 
 __device__ void run_storer(const StepParams& p, unsigned char* smem, Bars bars,
-                           volatile int* abort, int64_t g0, int64_t g1) {
+                           volatile int* abort) {
     const int64_t rowK = p.D * p.es, rowV = p.Dv * p.es;
     const uint32_t stage0 = smem_addr(smem + p.off_stages);
     const uint32_t vofs = static_cast<uint32_t>(p.T * rowK);
+    const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
     unsigned char* okc = static_cast<unsigned char*>(p.out_key_cache);
     unsigned char* ovc = static_cast<unsigned char*>(p.out_value_cache);
     int64_t stored = 0, released = 0;
     Ring ring, rel;
     bool ok = true;
-    for (int64_t u = g0 / p.TPU; ok && u * p.TPU < g1; ++u) {
-        const Piece pc = piece_of(p, u, g0, g1);
-        unsigned char* oku = okc + u * p.M * rowK;
-        unsigned char* ovu = ovc + u * p.M * rowV;
-        for (int64_t i = pc.i_lo; i < pc.i_hi; ++i) {
-            if (!mbar_wait(bars.full(ring.s), ring.ph, abort)) {
-                ok = false;
-                break;
-            }
-            const int64_t j0 = i * p.T, j1 = min(j0 + p.T, p.M);
-            const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
-            bulk_s2g(oku + j0 * rowK, sK, static_cast<uint32_t>((j1 - j0) * rowK));
-            bulk_s2g(ovu + j0 * rowV, sK + vofs, static_cast<uint32_t>((j1 - j0) * rowV));
-            bulk_commit();
-            ++stored;
-            ring.next(p.NS);
-            if (stored - released > p.LAG) {
-                bulk_wait_read(p.LAG);  // groups older than the newest LAG have read smem
-                for (; released < stored - p.LAG; ++released) {
-                    mbar_arrive(bars.empty(rel.s), 1u);
-                    rel.next(p.NS);
-                }
+    for (;;) {
+        if (!mbar_wait(bars.full(ring.s), ring.ph, abort)) {
+            ok = false;
+            break;
+        }
+        const TileMeta mt = meta[ring.s];
+        if (mt.flags & kDone) break;
+        const int64_t j0 = static_cast<int64_t>(mt.i) * p.T, j1 = min(j0 + p.T, p.M);
+        const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
+        bulk_s2g(okc + (mt.u * p.M + j0) * rowK, sK, static_cast<uint32_t>((j1 - j0) * rowK));
+        bulk_s2g(ovc + (mt.u * p.M + j0) * rowV, sK + vofs, static_cast<uint32_t>((j1 - j0) * rowV));
+        bulk_commit();
+        ++stored;
+        ring.next(p.NS);
+        if (stored - released > p.LAG) {
+            bulk_wait_read(p.LAG);  // groups older than the newest LAG have read smem
+            for (; released < stored - p.LAG; ++released) {
+                mbar_arrive(bars.empty(rel.s), 1u);
+                rel.next(p.NS);
             }
         }
     }
@@ -192,6 +236,17 @@ __device__ void run_storer(const StepParams& p, unsigned char* smem, Bars bars,
         }
     }
     bulk_wait_all();
+}
+
+// Rendezvous of the 8 consumer warps on an mbarrier (bounded, unlike bar.sync,
+// so a warp that gave up can never strand the others).
+__device__ __forceinline__ bool consumer_rendezvous(Bars bars, uint32_t& phase,
+                                                    volatile int* abort) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bars.consumers(), 1u);
+    const bool ok = warp_wait(bars.consumers(), phase, abort);
+    phase ^= 1u;
+    return ok;
 }
 
 // One warp, one row group of RPW query rows, the warp's SW slots of a tile.
@@ -503,180 +558,203 @@ __device__ __forceinline__ void store_state(const StepParams& p, float* st_ml, f
 
 template <typename T, int RPW, int DVC, int NCHL>
 __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bars,
-                              volatile int* abort, int64_t c, int64_t g0, int64_t g1) {
+                              volatile int* abort) {
     using S = Storage<T>;
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int VEC = S::kVec16;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane & 7;
     const int wr = w / p.WS, ws = w % p.WS;
     const int R = static_cast<int>(p.R), D = static_cast<int>(p.D), Dv = static_cast<int>(p.Dv);
     const int Q = static_cast<int>(p.Q);
+    const int nck = (D * p.es) >> 4;  // 16-byte chunks per key / query row
     float* qs = reinterpret_cast<float*>(smem + p.off_q);
     float* pb = reinterpret_cast<float*>(smem + p.off_p) + w * p.SW * RPW;
     float* st_ml = reinterpret_cast<float*>(smem + p.off_state);
     float* st_acc = reinterpret_cast<float*>(smem + p.off_state_acc);
     int* row_lim = reinterpret_cast<int*>(smem + p.off_row_lim);
     int64_t* row_off = reinterpret_cast<int64_t*>(smem + p.off_row_off);
+    const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
     const unsigned char* stages = smem + p.off_stages;
     const int vofs = p.T * D * p.es;
     const T* query = static_cast<const T*>(p.query);
     constexpr int nthr = kConsumerWarps * 32;
     Ring ring;
+    uint32_t cphase = 0;
 
-    // Every consumer warp waits on and releases EVERY tile of the range, in
-    // order, so no role ever runs more than one ring lap ahead of another and
-    // each parity wait refers to exactly one phase.
-    for (int64_t u = g0 / p.TPU; u * p.TPU < g1; ++u) {
-        const Unit x = load_unit(p, u);
-        const Piece pc = piece_of(p, u, g0, g1);
-        const int64_t i_end = min(pc.i_hi, (x.N + p.T - 1) / p.T);
-        const bool attend = x.n > 0 && pc.i_lo < i_end;  // this piece holds allowed slots
-        if (!attend) {
-            for (int64_t i = pc.i_lo; i < pc.i_hi; ++i) {
-                const bool ok = warp_wait(bars.full(ring.s), ring.ph, abort);
-                if (ok && lane == 0) mbar_arrive(bars.empty(ring.s), 1u);
-                ring.next(p.NS);
+    // current chunk
+    bool attend = false;
+    int64_t L = 0, n = 0, N = 0, u = 0, k = 0, b = 0, kv = 0;
+    // register path (NCHL > 0): 4 rows per warp, whole chunk
+    constexpr int V2 = VEC / 2;
+    constexpr int NQR = NCHL > 0 ? NCHL : 1;
+    float2 qr[4][NQR][V2];
+    int lim4[4] = {-1, -1, -1, -1};
+    int maxlim = -1, mylim = -1;
+    int64_t myoff = 0;
+    float m4[4], lp[4];
+    float2 acc2[4][DVC][2];
+    // shared-memory path (NCHL == 0)
+    float m[RPW], l[RPW], acc[RPW][DVC][4];
+
+    for (;;) {
+        const int s = ring.s;
+        const uint32_t ph = ring.ph;
+        ring.next(p.NS);
+        if (!warp_wait(bars.full(s), ph, abort)) break;
+        const TileMeta mt = meta[s];
+        if (mt.flags & kDone) break;
+        const unsigned char* sK = stages + s * p.stage_bytes;
+
+        if (mt.flags & kFirst) {  // a new chunk
+            u = mt.u;
+            k = mt.k;
+            L = mt.L;
+            n = mt.n;
+            N = L + n;
+            b = u / p.Hk;
+            kv = u - b * p.Hk;
+            attend = n > 0 && static_cast<int64_t>(mt.i) * p.T < N;
+            if (k == 0 && kv == 0 && w == 0 && lane == 0) {
+                // returned length and contract flags: once per batch row
+                const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
+                p.out_lengths[b] = ra.L + ra.n;
+                if (ra.flags && p.dev_status) atomicOr(p.dev_status, ra.flags);
             }
-            continue;
-        }
-        const int64_t k = c - cta_of_tile(u * p.TPU, p.TT, p.P);  // this piece's partial slot
-        const int64_t s_k = pc.i_lo * p.T;                         // its first slot
-
-        consumer_sync();  // the previous piece is done with q / state / row tables
-        for (int idx = threadIdx.x; idx < R * D; idx += nthr) {
-            const int r = idx / D, d = idx - r * D;
-            const int64_t h = x.kv * p.G + r / Q, t = r % Q;
-            qs[idx] = S::to_float(query[((x.b * p.Hq + h) * Q + t) * D + d]) * p.qscale;
-        }
-        for (int r = threadIdx.x; r < R; r += nthr) {
-            const int t = r % Q;
-            const int64_t h = x.kv * p.G + r / Q;
-            row_lim[r] = t < x.n ? static_cast<int>(x.L + t) : -1;
-            row_off[r] = ((x.b * p.Hq + h) * Q + t) * p.M;
-        }
-        if (p.NRG > 1) {
-            for (int idx = threadIdx.x; idx < R; idx += nthr) {
-                st_ml[2 * idx] = -INFINITY;
-                st_ml[2 * idx + 1] = 0.f;
-            }
-            for (int idx = threadIdx.x; idx < R * Dv; idx += nthr) st_acc[idx] = 0.f;
-        }
-        consumer_sync();
-
-        if constexpr (NCHL > 0) {
-            // 4 rows per warp, one row group per warp (NRG == 1), q in registers
-            constexpr int V2 = S::kVec16 / 2;
-            const int r0 = wr * 4;
-            float2 qr[4][NCHL][V2];
-            int lim[4];
-            int maxlim = -1, mylim = -1;
-            int64_t myoff = 0;
-            const int sub = lane & 7, nck = (D * p.es) >> 4;
+            if (attend) {
+                if constexpr (NCHL > 0) {
+                    // the warp's 4 rows straight from the staged query rows
+                    const unsigned char* qst = sK + p.off_stage_q;
+                    const int r0 = wr * 4;
 #pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-                const int r = r0 + ii;
-                lim[ii] = r < R ? row_lim[r] : -1;
-                maxlim = max(maxlim, lim[ii]);
-                if (sub == ii) {
-                    mylim = lim[ii];
-                    myoff = r < R ? row_off[r] : 0;
-                }
+                    for (int ii = 0; ii < 4; ++ii) {
+                        const int r = r0 + ii;
+                        const int t = r % Q;
+                        lim4[ii] = (r < R && t < n) ? static_cast<int>(L + t) : -1;
 #pragma unroll
-                for (int cc = 0; cc < NCHL; ++cc) {
-                    const int ck = sub + 8 * cc;
+                        for (int cc = 0; cc < NCHL; ++cc) {
+                            const int ck = sub + 8 * cc;
+                            if (r < R && ck < nck) {
+                                const uint4 raw =
+                                    *reinterpret_cast<const uint4*>(qst + (r * nck + ck) * 16);
+                                S::widen16_2(raw, qr[ii][cc]);
 #pragma unroll
-                    for (int e = 0; e < V2; ++e) {
-                        const int d = ck * S::kVec16 + 2 * e;
-                        qr[ii][cc][e] = (r < R && ck < nck)
-                                            ? make_float2(qs[r * D + d], qs[r * D + d + 1])
-                                            : make_float2(0.f, 0.f);
+                                for (int e = 0; e < V2; ++e) {
+                                    qr[ii][cc][e].x *= p.qscale;
+                                    qr[ii][cc][e].y *= p.qscale;
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < V2; ++e) qr[ii][cc][e] = make_float2(0.f, 0.f);
+                            }
+                        }
+                        m4[ii] = -INFINITY;
+                        lp[ii] = 0.f;
+#pragma unroll
+                        for (int cc = 0; cc < DVC; ++cc)
+                            acc2[ii][cc][0] = acc2[ii][cc][1] = make_float2(0.f, 0.f);
                     }
+                    maxlim = max(max(lim4[0], lim4[1]), max(lim4[2], lim4[3]));
+                    mylim = -1;
+                    myoff = 0;
+#pragma unroll
+                    for (int ii = 0; ii < 4; ++ii) {
+                        if (sub == ii) {
+                            const int r = r0 + ii;
+                            mylim = lim4[ii];
+                            myoff = ((b * p.Hq + kv * p.G + r / Q) * p.Q + r % Q) * p.M;
+                        }
+                    }
+                } else {
+                    // query rows into shared memory (fp32, pre-scaled), row tables
+                    for (int idx = threadIdx.x; idx < R * D; idx += nthr) {
+                        T v;
+                        if (mt.flags & kQStaged) {
+                            v = reinterpret_cast<const T*>(sK + p.off_stage_q)[idx];
+                        } else {
+                            const int r = idx / D, d = idx - r * D;
+                            v = query[((b * p.Hq + kv * p.G + r / Q) * Q + r % Q) * D + d];
+                        }
+                        qs[idx] = S::to_float(v) * p.qscale;
+                    }
+                    for (int r = threadIdx.x; r < R; r += nthr) {
+                        const int t = r % Q;
+                        row_lim[r] = t < n ? static_cast<int>(L + t) : -1;
+                        row_off[r] = ((b * p.Hq + kv * p.G + r / Q) * Q + t) * p.M;
+                    }
+                    if (p.NRG > 1) {
+                        for (int idx = threadIdx.x; idx < R; idx += nthr) {
+                            st_ml[2 * idx] = -INFINITY;
+                            st_ml[2 * idx + 1] = 0.f;
+                        }
+                        for (int idx = threadIdx.x; idx < R * Dv; idx += nthr) st_acc[idx] = 0.f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < RPW; ++i) {
+                        m[i] = -INFINITY;
+                        l[i] = 0.f;
+#pragma unroll
+                        for (int cc = 0; cc < DVC; ++cc)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) acc[i][cc][e] = 0.f;
+                    }
+                    if (!consumer_rendezvous(bars, cphase, abort)) break;
                 }
             }
-            float m4[4], lp[4];
-            float2 acc2[4][DVC][2];
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-                m4[ii] = -INFINITY;
-                lp[ii] = 0.f;
-#pragma unroll
-                for (int cc = 0; cc < DVC; ++cc)
-                    acc2[ii][cc][0] = acc2[ii][cc][1] = make_float2(0.f, 0.f);
-            }
-            for (int64_t i = pc.i_lo; i < pc.i_hi; ++i) {
-                const int s = ring.s;
-                const uint32_t ph = ring.ph;
-                ring.next(p.NS);
-                if (!warp_wait(bars.full(s), ph, abort)) continue;
-                if (i < i_end && r0 < R) {
-                    const unsigned char* sK = stages + s * p.stage_bytes;
-                    tile_rows_qr<T, NCHL, DVC>(p, ws, static_cast<int>(i * p.T), sK, sK + vofs,
-                                               qr, pb, lim, maxlim, mylim, myoff, m4, lp, acc2);
+        }
+
+        if (attend && static_cast<int64_t>(mt.i) * p.T < N) {
+            const int j0 = mt.i * p.T;
+            if constexpr (NCHL > 0) {
+                if (wr * 4 < R)
+                    tile_rows_qr<T, NCHL, DVC>(p, ws, j0, sK, sK + vofs, qr, pb, lim4, maxlim,
+                                               mylim, myoff, m4, lp, acc2);
+            } else {
+                for (int rgi = 0; rgi < p.NRG; ++rgi) {
+                    const int rg = wr + rgi * p.WR;
+                    if (rg * RPW >= R) break;
+                    if (p.NRG > 1) load_state<T, RPW, DVC>(p, st_ml, st_acc, rg * RPW, m, l, acc);
+                    tile_rows<T, RPW, DVC>(p, rg, ws, j0, sK, sK + vofs, qs, pb, row_lim,
+                                           row_off, m, l, acc);
+                    if (p.NRG > 1)
+                        store_state<T, RPW, DVC>(p, st_ml, st_acc, rg * RPW, m, l, acc);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars.empty(s), 1u);
             }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.empty(s), 1u);
+
+        if (!((mt.flags & kLast) && attend)) continue;
+        // ---- end of an attending chunk: merge the WS slot-split warps per row
+        if constexpr (NCHL > 0) {
+            const int r0 = wr * 4;
             if (r0 < R) {
-                float m[RPW], l[RPW], acc[RPW][DVC][4];
+                float mm[4], ll[4], aa[4][DVC][4];
 #pragma unroll
                 for (int ii = 0; ii < 4; ++ii) {
                     float t = lp[ii];
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                    m[ii] = m4[ii];
-                    l[ii] = t;
+                    mm[ii] = m4[ii];
+                    ll[ii] = t;
 #pragma unroll
                     for (int cc = 0; cc < DVC; ++cc) {
-                        acc[ii][cc][0] = acc2[ii][cc][0].x;
-                        acc[ii][cc][1] = acc2[ii][cc][0].y;
-                        acc[ii][cc][2] = acc2[ii][cc][1].x;
-                        acc[ii][cc][3] = acc2[ii][cc][1].y;
+                        aa[ii][cc][0] = acc2[ii][cc][0].x;
+                        aa[ii][cc][1] = acc2[ii][cc][0].y;
+                        aa[ii][cc][2] = acc2[ii][cc][1].x;
+                        aa[ii][cc][3] = acc2[ii][cc][1].y;
                     }
                 }
-                store_state<T, RPW, DVC>(p, st_ml + 2 * ws * R, st_acc + ws * R * Dv, r0, m, l,
-                                         acc);
+                store_state<T, 4, DVC>(p, st_ml + 2 * ws * R, st_acc + ws * R * Dv, r0, mm, ll, aa);
             }
         } else {
-        float m[RPW], l[RPW], acc[RPW][DVC][4];
-#pragma unroll
-        for (int i = 0; i < RPW; ++i) {
-            m[i] = -INFINITY;
-            l[i] = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < DVC; ++cc)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[i][cc][e] = 0.f;
+            if (p.NRG == 1 && wr * RPW < R)
+                store_state<T, RPW, DVC>(p, st_ml + 2 * ws * R, st_acc + ws * R * Dv, wr * RPW, m,
+                                         l, acc);
         }
-        for (int64_t i = pc.i_lo; i < pc.i_hi; ++i) {
-            const int s = ring.s;
-            const uint32_t ph = ring.ph;
-            ring.next(p.NS);
-            if (!warp_wait(bars.full(s), ph, abort)) continue;
-            if (i >= i_end) {  // past the new length: copy only
-                if (lane == 0) mbar_arrive(bars.empty(s), 1u);
-                continue;
-            }
-            const unsigned char* sK = stages + s * p.stage_bytes;
-            const int j0 = static_cast<int>(i * p.T);
-            for (int rgi = 0; rgi < p.NRG; ++rgi) {
-                const int rg = wr + rgi * p.WR;
-                if (rg * RPW >= R) break;
-                if (p.NRG > 1) load_state<T, RPW, DVC>(p, st_ml, st_acc, rg * RPW, m, l, acc);
-                tile_rows<T, RPW, DVC>(p, rg, ws, j0, sK, sK + vofs, qs, pb, row_lim, row_off,
-                                       m, l, acc);
-                if (p.NRG > 1) store_state<T, RPW, DVC>(p, st_ml, st_acc, rg * RPW, m, l, acc);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.empty(s), 1u);
-        }
-
-        // ---- this piece's partial per row: merge the WS slot-split warps
-        if (p.NRG == 1 && wr * RPW < R)
-            store_state<T, RPW, DVC>(p, st_ml + 2 * ws * R, st_acc + ws * R * Dv, wr * RPW, m, l,
-                                     acc);
-        }
-        consumer_sync();
+        if (!consumer_rendezvous(bars, cphase, abort)) break;
+        const int64_t s_k = k * p.CH * p.T;  // the chunk's first slot
         for (int r = w; r < R; r += kConsumerWarps) {
             const int t = r % Q;
-            if (t >= x.n || s_k > x.L + t) continue;  // no allowed slot of this row here
+            if (t >= n || s_k > L + t) continue;  // no allowed slot of this row here
             float mx = -INFINITY;
             for (int q = 0; q < p.WS; ++q) mx = fmaxf(mx, st_ml[2 * (q * R + r)]);
             float lsum = 0.f;
@@ -695,15 +773,17 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
                     const float mq = st_ml[2 * (q * R + r)];
                     if (mq == -INFINITY) continue;
                     const float wq = fast_exp2(mq - mx);
-                    const float4 b = *reinterpret_cast<const float4*>(st_acc + (q * R + r) * Dv + e0);
-                    a.x = fmaf(b.x, wq, a.x);
-                    a.y = fmaf(b.y, wq, a.y);
-                    a.z = fmaf(b.z, wq, a.z);
-                    a.w = fmaf(b.w, wq, a.w);
+                    const float4 bq =
+                        *reinterpret_cast<const float4*>(st_acc + (q * R + r) * Dv + e0);
+                    a.x = fmaf(bq.x, wq, a.x);
+                    a.y = fmaf(bq.y, wq, a.y);
+                    a.z = fmaf(bq.z, wq, a.z);
+                    a.w = fmaf(bq.w, wq, a.w);
                 }
                 *reinterpret_cast<float4*>(p.part_acc + prow * p.Dv + e0) = a;
             }
         }
+        if (!consumer_rendezvous(bars, cphase, abort)) break;  // state slots free again
     }
 }
 
@@ -718,33 +798,21 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             mbar_init(bars.full(s), 1u);
             mbar_init(bars.empty(s), 1u + kConsumerWarps);
         }
+        mbar_init(bars.consumers(), kConsumerWarps);
         *abort = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
-    const int64_t c = blockIdx.x;
-    const int64_t g0 = cta_first_tile(c, p.TT, p.P), g1 = cta_first_tile(c + 1, p.TT, p.P);
     const int warp = threadIdx.x >> 5;
-
     if (warp < kConsumerWarps) {
-        // Returned lengths and contract flags: written once per batch row, by
-        // the CTA holding the first tile of unit (b, kv head 0).
-        for (int64_t u = (g0 + p.TPU - 1) / p.TPU + threadIdx.x; u * p.TPU < g1;
-             u += kConsumerWarps * 32) {
-            if (u % p.Hk != 0) continue;
-            const int64_t b = u / p.Hk;
-            const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
-            p.out_lengths[b] = ra.L + ra.n;
-            if (ra.flags && p.dev_status) atomicOr(p.dev_status, ra.flags);
-        }
-        run_consumers<T, RPW, DVC, NCHL>(p, smem, bars, abort, c, g0, g1);
+        run_consumers<T, RPW, DVC, NCHL>(p, smem, bars, abort);
     } else if (warp == kConsumerWarps) {
-        if ((threadIdx.x & 31) == 0) run_producer(p, smem, bars, abort, g0, g1);
+        if ((threadIdx.x & 31) == 0) run_producer(p, smem, bars, abort);
     } else {
-        if ((threadIdx.x & 31) == 0) run_storer(p, smem, bars, abort, g0, g1);
+        if ((threadIdx.x & 31) == 0) run_storer(p, smem, bars, abort);
     }
-    __syncthreads();  // every thread reaches this exactly once: all loops are bounded
+    __syncthreads();  // every thread reaches this exactly once: all waits are bounded
     if (threadIdx.x == 0 && *abort && p.dev_status) atomicOr(p.dev_status, KVC_DEV_TIMEOUT);
 }
 

@@ -25,6 +25,9 @@ constexpr int kFusedThreads = (kConsumerWarps + 2) * 32;  // + producer warp + s
 #ifndef KVC_STAGE_BYTES
 #define KVC_STAGE_BYTES 32768
 #endif
+#ifndef KVC_CHUNK_ORDER
+#define KVC_CHUNK_ORDER 1
+#endif
 #ifndef KVC_STORE_LAG
 #define KVC_STORE_LAG 4
 #endif
@@ -136,6 +139,137 @@ __device__ __forceinline__ void bulk_wait_read(int n) {
 
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ---------------------------------------------- TMA tensor copies (tiled)
+// 3-D tile load global -> shared (box given by the tensor map), counted on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// 3-D tile store shared -> global in the current bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, int x, int y, int z, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::
+                     "l"(reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA stores, tensor-core operand reads).
+__device__ __forceinline__ void fence_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------- tensor memory / tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16/fp16 operands, fp32 accumulate).
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// The mbarrier receives one arrival once every tcgen05.mma this thread issued so far is complete.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this warp's 32 lanes (one lane per thread).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a tcgen05 operand laid out with the
+// 128-byte swizzle (rows of 128 bytes, 8-row atoms of 1024 bytes, the 16-byte
+// chunk index XOR-ed with the row index within the atom). lbo / sbo in bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of a kind::f16 tcgen05.mma with fp32 accumulation.
+// bf16: operands are bf16 (else fp16). b_mn_major: B is stored N-contiguous.
+__host__ __device__ constexpr uint32_t mma_idesc_f16(int M, int N, bool bf16, bool b_mn_major) {
+    return (1u << 4)                                   // D: fp32
+           | ((bf16 ? 1u : 0u) << 7)                   // A type
+           | ((bf16 ? 1u : 0u) << 10)                  // B type
+           | (0u << 15)                                // A: K-major
+           | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
 // Named barrier 1 among the consumer warps only.
@@ -269,15 +403,9 @@ __device__ __forceinline__ RowAppend row_append(const int64_t* lengths, const ui
 }
 
 // ------------------------------------------------------ work decomposition
-// Tiles of T cache slots; unit u = (b, kv head) owns tiles [u*TPU, (u+1)*TPU).
-// CTA c of P owns global tiles [floor(c*TT/P), floor((c+1)*TT/P)).
-__host__ __device__ __forceinline__ int64_t cta_first_tile(int64_t c, int64_t TT, int64_t P) {
-    return c * TT / P;
-}
-// The CTA whose range holds global tile g.
-__host__ __device__ __forceinline__ int64_t cta_of_tile(int64_t g, int64_t TT, int64_t P) {
-    return ((g + 1) * P - 1) / TT;
-}
+// Tiles of T cache slots; unit u = (b, kv head) owns tiles [0, TPU). Chunk k of
+// unit u is its tiles [k*CH, min((k+1)*CH, TPU)); every chunk that holds an
+// allowed slot writes one partial per query row into slot (u, k).
 
 // Everything the kernels need, passed by value.
 struct StepParams {
@@ -288,13 +416,17 @@ struct StepParams {
     // decomposition
     int T;        // slots per tile
     int64_t TPU;  // tiles per unit
-    int64_t TT;   // total tiles
-    int64_t P;    // CTAs of the attention/copy kernel
-    int64_t KP;   // partial slots per unit
+    int64_t CH;   // tiles per chunk
+    int64_t KP;   // chunks (= partial slots) per unit
+    int64_t NQ;   // chunks in all
+    int64_t P;    // CTAs of the fused kernel
     // fused-kernel layout
     int RPW, WR, WS, NRG, SW, NS, LAG;
     int stage_bytes, off_stages, off_q, off_p, off_state, off_state_acc, off_row_lim, off_row_off,
-        off_flag;
+        off_flag, off_meta;
+    int q_staged;       // 1: the G*Q query rows ride in the stage of a chunk's first tile
+    int q_stage_bytes;  // their size (G*Q*D*es)
+    int off_stage_q;    // their offset inside a stage
     // tensors
     const void* query;
     const void* new_key;
@@ -311,6 +443,7 @@ struct StepParams {
     float* part_ml;   // [U][KP][R][2]  (max in base 2, sum)
     float* part_acc;  // [U][KP][R][Dv] (unnormalised weighted values)
     float* scores;    // [B][Hq][Q][M]  (scale*log2e*dot, allowed slots only)
+    unsigned int* counter;  // next chunk to hand out (zeroed before each launch)
     int32_t* dev_status;
     int vec_attention;  // 1: attention rows may be written 8 elements at a time
 };

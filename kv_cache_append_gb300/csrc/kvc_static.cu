@@ -62,7 +62,7 @@ extern "C" KVC_API int kvc_step_static(const kvc_dims* dims, const void* query,
                                        void* out_value_cache, int64_t* out_lengths,
                                        void* out_attention, void* out_context,
                                        int32_t* dev_status, void* stream) {
-    const size_t need = kvc_workspace_bytes(dims);  // 0 for Q == 0 and for invalid dims
+    const size_t need = kvc_workspace_bytes(dims);  // 0 only for invalid dims
     if (need > static_cast<size_t>(KVC_STATIC_SCRATCH_BYTES)) return KVC_E_STATIC_LIMIT;
     void* scratch = nullptr;
     if (need > 0) {

@@ -55,7 +55,7 @@ def test_workspace_bytes_host_only(lib):
     # one fp32 score per (b, h, t, slot) at least, plus the partials
     assert ws >= 2 * 4 * 3 * 32 * 4 + 2 * 2 * 6 * (16 + 2) * 4
     assert ws % 256 == 0
-    assert kvc.workspace_bytes(_dims(Q=0)) == 0
+    assert kvc.workspace_bytes(_dims(Q=0)) == 256           # the fused kernel's work counter
     assert kvc.workspace_bytes(_dims(Hq=3)) == 0          # invalid: Hk does not divide Hq
     big = _dims(B=64, Hq=32, Hk=8, Q=1, D=128, Dv=128, M=8192, dtype=1)
     assert kvc.workspace_bytes(big) >= 64 * 32 * 8192 * 4
