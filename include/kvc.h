@@ -138,9 +138,10 @@ KVC_API int kvc_step_timed(const kvc_dims *dims, const void *query, const void *
 
 /*
  * Number of kernels kvc_step launches for these sizes and pointers, and the
- * name of the path it takes ("fused" or "generic") through *path_name
- * (nullable). Pure host logic except for a cached device-attribute query.
- * Returns a negative KVC_E_* code on invalid arguments.
+ * name of the path it takes ("tensor", "fused" or "generic") through
+ * *path_name (nullable), for a 16-byte aligned query. Pure host logic except
+ * for a cached device-attribute query. Returns a negative KVC_E_* code on
+ * invalid arguments.
  */
 KVC_API int kvc_plan_info(const kvc_dims *dims, const void *key_cache, const void *value_cache,
                   const void *new_key, const void *new_value, const void *out_key_cache,

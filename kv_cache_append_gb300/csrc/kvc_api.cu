@@ -71,6 +71,9 @@ int check_dims(const kvc_dims* d) {
 // The decomposition and shared-memory layout of one step.
 struct Plan {
     bool fused = false;
+    bool tensor = false;  // the tensor-core fused kernel (kvc_fused_tc.cu)
+    int tc_off_qbuf = 0, tc_off_pbuf = 0, tc_tmem_cols = 0;
+    size_t off_tile_max = 0;
     int T = 0;
     int64_t TPU = 0, CH = 1, KP = 1, NQ = 0, P = 0;
     int RPW = 4, WR = 1, WS = 8, NRG = 1, SW = 0, NS = 0, LAG = 0, DVC = 1, NCHL = 0;
@@ -96,8 +99,12 @@ bool fused_shapes(const kvc_dims& d) {
     return (d.D * es) % 16 == 0 && (d.Dv * es) % 16 == 0 && d.D * es <= 512 && d.Dv <= 256;
 }
 
+// Workspace: chunk counter | partial (max, sum) | partial weighted values |
+// attention-row inputs, either fp32 scores or fp16 2^(score - tile max) plus
+// one fp32 tile maximum per (row, 64 slots); the region fits both.
 void workspace_layout(const kvc_dims& d, int64_t KP, Plan* pl) {
     const int64_t U = d.B * d.Hk, R = (d.Hq / d.Hk) * d.Q;
+    const int64_t rows = d.B * d.Hq * d.Q;
     int64_t off = 0;
     pl->off_counter = static_cast<size_t>(off);
     off = 256;
@@ -106,7 +113,10 @@ void workspace_layout(const kvc_dims& d, int64_t KP, Plan* pl) {
     pl->off_acc = static_cast<size_t>(off);
     off = align_up(off + U * KP * R * d.Dv * 4, 256);
     pl->off_scores = static_cast<size_t>(off);
-    off = align_up(off + d.B * d.Hq * d.Q * d.M * 4, 256);
+    const int64_t fp16_part = align_up(rows * d.M * 2, 256);
+    pl->off_tile_max = static_cast<size_t>(off + fp16_part);
+    const int64_t fmt1 = fp16_part + rows * ((d.M + 63) / 64) * 4;
+    off = align_up(off + std::max<int64_t>(rows * d.M * 4, fmt1), 256);
     pl->ws_bytes = static_cast<size_t>(off);
 }
 
@@ -207,6 +217,91 @@ void generic_plan(const kvc_dims& d, Plan* pl) {
     workspace_layout(d, 1, pl);
 }
 
+#ifndef KVC_TC_MIN_ROWS
+#define KVC_TC_MIN_ROWS 64
+#endif
+constexpr int kTcT = 64;        // slots per tile of the tensor-core kernel
+constexpr int kTcBox = 64 * 128;  // one 64-element-wide box of a tile
+
+// Shapes the tensor-core kernel takes: 16-bit caches, key and value widths
+// multiples of 64 (at most 256), KVC_TC_MIN_ROWS..128 query rows per unit.
+bool tc_shapes(const kvc_dims& d) {
+    const int64_t R = (d.Hq / d.Hk) * d.Q;
+    return d.dtype != KVC_F32 && d.D % 64 == 0 && d.D <= 256 && d.Dv % 64 == 0 && d.Dv <= 256 &&
+           d.Q >= 1 && R >= KVC_TC_MIN_ROWS && R <= 128 && d.B * d.Hk < (int64_t(1) << 31);
+}
+
+void tc_tiling(const kvc_dims& d, Plan* pl) {
+    pl->T = kTcT;
+    pl->TPU = (d.M + kTcT - 1) / kTcT;
+}
+
+bool tc_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
+    if (!tc_shapes(d)) return false;
+    *pl = Plan();
+    tc_tiling(d, pl);
+    const int64_t nkb = d.D / 64, nvb = d.Dv / 64;
+    pl->off_flag = 512;
+    pl->off_meta = 1024;
+    int64_t off = 2048;
+    pl->tc_off_qbuf = static_cast<int>(off);
+    off += nkb * 128 * 128;
+    pl->tc_off_pbuf = static_cast<int>(off);
+    off += 128 * 128;
+    off = align_up(off, 1024);
+    pl->off_stages = static_cast<int>(off);
+    const int64_t stage = (nkb + nvb) * kTcBox;
+    pl->stage_bytes = static_cast<int>(stage);
+    if (off + 2 * stage > smem_cap) return false;
+    pl->NS = static_cast<int>(std::min<int64_t>(kMaxStages, (smem_cap - off) / stage));
+    pl->LAG = std::min(std::min(kStoreLag, 7), pl->NS - 1);
+    pl->smem = static_cast<size_t>(off + int64_t(pl->NS) * stage);
+    pl->tc_tmem_cols = 2 * kTcT + d.Dv <= 256 ? 256 : 512;
+    chunking(d, sms, pl);
+    pl->P = std::min<int64_t>(sms, pl->NQ);
+    pl->tensor = true;
+    workspace_layout(d, pl->KP, pl);
+    return true;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// [U][M][width] 16-bit cache as boxes of 64 elements x 64 slots, 128-byte swizzle.
+bool cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t width, int64_t M,
+               int64_t U) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(M),
+                                static_cast<cuuint64_t>(U)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(width * 2),
+                                   static_cast<cuuint64_t>(M * width * 2)};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTcT), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map,
+              dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+              3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Range {
@@ -247,7 +342,8 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
                               aligned16(out_key_cache) && aligned16(out_value_cache) &&
                               (!hasq || (aligned16(new_key) && aligned16(new_value)));
     Plan pl;
-    if (!(ptrs_aligned && fused_plan(d, dev.sms, dev.smem_optin, aligned16(query), &pl)))
+    if (!(ptrs_aligned && aligned16(query) && tc_plan(d, dev.sms, dev.smem_optin, &pl)) &&
+        !(ptrs_aligned && fused_plan(d, dev.sms, dev.smem_optin, aligned16(query), &pl)))
         generic_plan(d, &pl);
 
     if (pl.ws_bytes > 0) {
@@ -307,7 +403,14 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
         p.part_acc = reinterpret_cast<float*>(ws + pl.off_acc);
         p.scores = reinterpret_cast<float*>(ws + pl.off_scores);
         p.counter = reinterpret_cast<unsigned int*>(ws + pl.off_counter);
+        p.pvals = reinterpret_cast<__half*>(ws + pl.off_scores);
+        p.tile_max = reinterpret_cast<float*>(ws + pl.off_tile_max);
     }
+    p.score_fmt = pl.tensor ? 1 : 0;
+    p.tiles64 = (d.M + 63) / 64;
+    p.tc_off_qbuf = pl.tc_off_qbuf;
+    p.tc_off_pbuf = pl.tc_off_pbuf;
+    p.tc_tmem_cols = pl.tc_tmem_cols;
     p.dev_status = dev_status;
     p.vec_attention = (d.M % 8 == 0) && aligned16(out_attention);
 
@@ -320,7 +423,19 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     };
     cudaError_t e = record();
     if (e == cudaSuccess) {
-        if (pl.fused) {
+        if (pl.tensor) {
+            TcParams tp;
+            std::memset(&tp, 0, sizeof(tp));
+            tp.p = p;
+            if (!cache_map(&tp.tm_k, key_cache, d.dtype, d.D, d.M, d.B * d.Hk) ||
+                !cache_map(&tp.tm_v, value_cache, d.dtype, d.Dv, d.M, d.B * d.Hk) ||
+                !cache_map(&tp.tm_ok, out_key_cache, d.dtype, d.D, d.M, d.B * d.Hk) ||
+                !cache_map(&tp.tm_ov, out_value_cache, d.dtype, d.Dv, d.M, d.B * d.Hk))
+                return KVC_E_CUDA;
+            e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream);
+            if (e == cudaSuccess) e = launch_fused_tc(tp, d.dtype, pl.smem, stream);
+            if (e == cudaSuccess) e = record();
+        } else if (pl.fused) {
             // chunks are handed out from a counter that starts at zero
             if (p.counter) e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream);
             if (e == cudaSuccess) e = launch_fused(p, d.dtype, pl.DVC, pl.NCHL, pl.smem, stream);
@@ -351,15 +466,24 @@ size_t kvc_workspace_bytes(const kvc_dims* dims) {
     using namespace kvc;
     if (check_dims(dims) != KVC_OK) return 0;
     Plan pl;
+    generic_plan(*dims, &pl);
+    size_t bytes = pl.ws_bytes;
+    // more CTAs make smaller chunks, hence more partial slots: size for the most
     if (fused_shapes(*dims)) {
-        // more CTAs make smaller chunks, hence more partial slots: size for the most
-        fused_tiling(*dims, &pl);
-        chunking(*dims, kSizingCtas, &pl);
-        workspace_layout(*dims, pl.KP, &pl);
-    } else {
-        generic_plan(*dims, &pl);
+        Plan f;
+        fused_tiling(*dims, &f);
+        chunking(*dims, kSizingCtas, &f);
+        workspace_layout(*dims, f.KP, &f);
+        bytes = std::max(bytes, f.ws_bytes);
     }
-    return pl.ws_bytes;
+    if (tc_shapes(*dims)) {
+        Plan t;
+        tc_tiling(*dims, &t);
+        chunking(*dims, kSizingCtas, &t);
+        workspace_layout(*dims, t.KP, &t);
+        bytes = std::max(bytes, t.ws_bytes);
+    }
+    return bytes;
 }
 
 int kvc_step(const kvc_dims* dims, const void* query, const void* new_key, const void* new_value,
@@ -400,6 +524,10 @@ int kvc_plan_info(const kvc_dims* dims, const void* key_cache, const void* value
                               aligned16(out_key_cache) && aligned16(out_value_cache) &&
                               (!hasq || (aligned16(new_key) && aligned16(new_value)));
     Plan pl;
+    if (ptrs_aligned && tc_plan(*dims, dev.sms, dev.smem_optin, &pl)) {
+        if (path_name) *path_name = "tensor";
+        return 2;
+    }
     const bool fused = ptrs_aligned && fused_plan(*dims, dev.sms, dev.smem_optin, true, &pl);
     if (path_name) *path_name = fused ? "fused" : "generic";
     return fused ? (hasq ? 2 : 1) : (hasq ? 3 : 1);

@@ -8,6 +8,8 @@
 // the full attention row: 2^(s_j - m) / l on the allowed slots j <= length + t
 // and +0 on every other slot (bullet 4: "Invalid query rows return zero
 // attention/context"; "attention[B,H_q,Q,M]"). Invalid rows are all +0.
+// The tensor-core kernel leaves 2^(s_j - ref) in fp16 with one reference
+// maximum per 64-slot tile instead of s_j; then a_j = p_j 2^(ref - m) / l.
 #include "kvc_internal.cuh"
 #include "kvc_launch.h"
 
@@ -86,6 +88,36 @@ __global__ void __launch_bounds__(kFinalizeThreads)
         for (int64_t e = threadIdx.x; e < p.Dv; e += blockDim.x) ctx[e] = S::from_float(0.f);
     }
 
+    if (p.score_fmt == 1) {
+        // fp16 2^(s - tile max) per slot and one maximum per 64-slot tile
+        const __half* pv = p.pvals + row * p.M;
+        const float* tmx = p.tile_max + row * p.tiles64;
+        if (p.vec_attention) {
+            for (int64_t j0 = static_cast<int64_t>(threadIdx.x) * 8; j0 < p.M;
+                 j0 += static_cast<int64_t>(blockDim.x) * 8) {
+                float v[8];
+                if (j0 <= lim) {
+                    const float c = fast_exp2(tmx[j0 >> 6] - mx) * inv_l;
+                    const uint4 raw = *reinterpret_cast<const uint4*>(pv + j0);
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const __half h = __ushort_as_half(static_cast<unsigned short>(w[i >> 1] >> ((i & 1) * 16)));
+                        v[i] = (j0 + i <= lim) ? __half2float(h) * c : 0.f;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+                }
+                store8<T>(att + j0, v);
+            }
+        } else {
+            for (int64_t j = threadIdx.x; j < p.M; j += blockDim.x)
+                att[j] = S::from_float(
+                    j <= lim ? __half2float(pv[j]) * fast_exp2(tmx[j >> 6] - mx) * inv_l : 0.f);
+        }
+        return;
+    }
     const float* sc = p.scores + row * p.M;
     if (p.vec_attention) {
         for (int64_t j0 = static_cast<int64_t>(threadIdx.x) * 8; j0 < p.M;

@@ -1,0 +1,546 @@
+// kvc_fused_tc.cu -- the fused append + attention kernel on the tensor cores.
+//
+// Same work as kvc_fused.cu (one persistent CTA per SM, chunks of tiles from a
+// global counter, every tile of the updated cache copied to the output and
+// the tiles that hold allowed slots attended), with the two products of the
+// attention on the 5th-generation tensor cores (tcgen05, accumulators in
+// tensor memory). For 16-bit caches whose key and value widths are multiples
+// of 64 and units of at most 128 query rows (G = Hq/Hk heads x Q new tokens).
+//
+// A tile is 64 cache slots. Tiles move by TMA tensor copies in 64-element-wide
+// boxes with the 128-byte swizzle, the layout the tensor cores read:
+//
+//   producer warp  takes chunks, writes each tile's metadata, TMA-loads the
+//                  tile's K and V boxes from the input caches.
+//   storer warp    overwrites the rows [length, length+n) of the tile in
+//                  shared memory with new_key/new_value ("Write new_key/value
+//                  at positions length+t only for True append slots t",
+//                  Required behavior, bullet 3), then TMA-stores the tile to
+//                  the output caches ("Return the entire updated cache", bullet
+//                  4). The tile in shared memory is then exactly the updated
+//                  cache tile, and the tensor cores read it from there.
+//   MMA warp       one thread: S = Q K^T (M = 128 query rows, N = 64 slots,
+//                  K = D) into one of two tensor-memory S buffers, then
+//                  O += P V (N = Dv, K = 64 slots) into the tensor-memory O.
+//   4 softmax      one query row per thread: reads its S row, applies
+//   warps          scale*log2(e) and the lower-right causal limit j <= length +
+//                  t (bullet 4), keeps a reference maximum (raised, and O
+//                  rescaled, only when a score exceeds it by more than 2^8),
+//                  writes P = 2^(s - ref) for the next product and, in fp16,
+//                  for the attention rows; at the end of a chunk it writes the
+//                  row's partial (reference max, sum, O row).
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "kvc_internal.cuh"
+#include "kvc_launch.h"
+#include "kvc_pipeline.cuh"
+
+namespace kvc {
+
+namespace {
+
+constexpr int kTcT = 64;                  // slots per tile
+constexpr int kBox = kTcT * 128;          // bytes of one 64-element-wide box of a tile
+constexpr int kQBox = 128 * 128;          // bytes of one 64-element-wide box of the query rows
+constexpr int kSoftWarps = 4;
+constexpr int kMmaWarp = 4, kProdWarp = 5, kStoreWarp = 6;
+constexpr int kTcThreads = 7 * 32;
+constexpr float kRescale = 8.f;           // raise the reference max when exceeded by 2^8
+
+struct TcBars {
+    uint32_t base;
+    __device__ uint32_t full(int s) const { return base + 8u * s; }
+    __device__ uint32_t empty(int s) const { return base + 128u + 8u * s; }
+    __device__ uint32_t patched(int s) const { return base + 256u + 8u * s; }
+    __device__ uint32_t s_ready(int b) const { return base + 384u + 8u * b; }
+    __device__ uint32_t s_free(int b) const { return base + 400u + 8u * b; }
+    __device__ uint32_t p_ready() const { return base + 416u; }
+    __device__ uint32_t o_done() const { return base + 424u; }
+    __device__ uint32_t q_ready() const { return base + 432u; }
+    __device__ uint32_t drained() const { return base + 440u; }
+};
+constexpr int kTmemSlot = 448;  // tensor-memory base address written by tcgen05.alloc
+
+// Rows [a, c) of the tile starting at slot j0 must come from the new rows.
+struct PatchRange {
+    int64_t a, c;
+};
+__device__ __forceinline__ PatchRange patch_range(const TileMeta& mt, int64_t M) {
+    const int64_t j0 = static_cast<int64_t>(mt.i) * kTcT, j1 = min(j0 + kTcT, M);
+    const int64_t N = mt.L + mt.n;
+    return PatchRange{max(mt.L, j0), min(N, j1)};
+}
+
+__device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars,
+                            volatile int* abort) {
+    const StepParams& p = tp.p;
+    const uint32_t stage0 = smem_addr(smem + p.off_stages);
+    TileMeta* meta = reinterpret_cast<TileMeta*>(smem + p.off_meta);
+    const int nkb = static_cast<int>(p.D / 64), nvb = static_cast<int>(p.Dv / 64);
+    const uint32_t tile_bytes = static_cast<uint32_t>((nkb + nvb) * kBox);
+    const int64_t U = p.B * p.Hk;
+    int64_t issued = 0;
+    Ring ring;
+    bool ok = true;
+    while (ok) {
+        const int64_t q = atomicAdd(p.counter, 1u);
+        if (q >= p.NQ) break;
+        const int64_t idx = chunk_of(q, p.NQ);
+        const int64_t k = idx / U, u = idx - k * U;
+        const Unit x = load_unit(p, u);
+        const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, p.TPU);
+        for (int64_t i = i0; i < i1; ++i) {
+            if (issued >= p.NS && !mbar_wait(bars.empty(ring.s), ring.ph ^ 1u, abort)) {
+                ok = false;
+                break;
+            }
+            TileMeta& mt = meta[ring.s];
+            mt.L = x.L;
+            mt.u = u;
+            mt.n = static_cast<int32_t>(x.n);
+            mt.i = static_cast<int32_t>(i);
+            mt.k = static_cast<int32_t>(k);
+            mt.flags = (i == i0 ? kFirst : 0) | (i == i1 - 1 ? kLast : 0);
+            const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
+            const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBox);
+            mbar_arrive_expect_tx(bars.full(ring.s), tile_bytes);  // publishes the metadata too
+            const int y = static_cast<int>(i * kTcT), z = static_cast<int>(u);
+            for (int b = 0; b < nkb; ++b)
+                tma_load_3d(sK + b * kBox, &tp.tm_k, 64 * b, y, z, bars.full(ring.s));
+            for (int b = 0; b < nvb; ++b)
+                tma_load_3d(sV + b * kBox, &tp.tm_v, 64 * b, y, z, bars.full(ring.s));
+            ++issued;
+            ring.next(p.NS);
+        }
+    }
+    if (ok) {  // sentinel tile: tells the other roles to stop
+        if (issued < p.NS || mbar_wait(bars.empty(ring.s), ring.ph ^ 1u, abort)) {
+            meta[ring.s].flags = kDone;
+            mbar_arrive_expect_tx(bars.full(ring.s), 0u);
+            return;
+        }
+    }
+    for (int64_t q = issued > p.NS ? issued - p.NS : 0; q < issued; ++q)
+        mbar_drain(bars.full(static_cast<int>(q % p.NS)), static_cast<uint32_t>((q / p.NS) & 1));
+}
+
+// Whole warp: patch the new rows into the swizzled tile, then (lane 0) store it.
+__device__ void tc_storer(const TcParams& tp, unsigned char* smem, TcBars bars,
+                          volatile int* abort) {
+    const StepParams& p = tp.p;
+    const int lane = threadIdx.x & 31;
+    const uint32_t stage0 = smem_addr(smem + p.off_stages);
+    const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
+    const int nkb = static_cast<int>(p.D / 64), nvb = static_cast<int>(p.Dv / 64);
+    const int64_t rowK = p.D * p.es, rowV = p.Dv * p.es;
+    const int ckK = static_cast<int>(rowK / 16), ckV = static_cast<int>(rowV / 16);
+    const unsigned char* nk = static_cast<const unsigned char*>(p.new_key);
+    const unsigned char* nv = static_cast<const unsigned char*>(p.new_value);
+    int64_t stored = 0, released = 0;
+    Ring ring, rel;
+    bool ok = true;
+    for (;;) {
+        if (!warp_wait(bars.full(ring.s), ring.ph, abort)) {
+            ok = false;
+            break;
+        }
+        const TileMeta mt = meta[ring.s];
+        if (mt.flags & kDone) break;
+        unsigned char* tK = smem + p.off_stages + static_cast<int64_t>(ring.s) * p.stage_bytes;
+        unsigned char* tV = tK + nkb * kBox;
+        const int64_t j0 = static_cast<int64_t>(mt.i) * kTcT;
+        const PatchRange pr = patch_range(mt, p.M);
+        if (pr.c > pr.a) {
+            const int rows = static_cast<int>(pr.c - pr.a);
+            const unsigned char* nku = nk + (mt.u * p.Q + (pr.a - mt.L)) * rowK;
+            const unsigned char* nvu = nv + (mt.u * p.Q + (pr.a - mt.L)) * rowV;
+            for (int e = lane; e < rows * ckK; e += 32) {
+                const int rr = e / ckK, ch = e - rr * ckK;
+                const int r = static_cast<int>(pr.a - j0) + rr;
+                *reinterpret_cast<uint4*>(tK + (ch >> 3) * kBox + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
+                    *reinterpret_cast<const uint4*>(nku + rr * rowK + ch * 16);
+            }
+            for (int e = lane; e < rows * ckV; e += 32) {
+                const int rr = e / ckV, ch = e - rr * ckV;
+                const int r = static_cast<int>(pr.a - j0) + rr;
+                *reinterpret_cast<uint4*>(tV + (ch >> 3) * kBox + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
+                    *reinterpret_cast<const uint4*>(nvu + rr * rowV + ch * 16);
+            }
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.patched(ring.s), 1u);
+        }
+        if (lane == 0) {
+            const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
+            const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBox);
+            const int y = static_cast<int>(j0), z = static_cast<int>(mt.u);
+            for (int b = 0; b < nkb; ++b) tma_store_3d(&tp.tm_ok, 64 * b, y, z, sK + b * kBox);
+            for (int b = 0; b < nvb; ++b) tma_store_3d(&tp.tm_ov, 64 * b, y, z, sV + b * kBox);
+            bulk_commit();
+            ++stored;
+            if (stored - released > p.LAG) {
+                bulk_wait_read(p.LAG);
+                for (; released < stored - p.LAG; ++released) {
+                    mbar_arrive(bars.empty(rel.s), 1u);
+                    rel.next(p.NS);
+                }
+            }
+        }
+        ring.next(p.NS);
+    }
+    if (lane == 0) {
+        bulk_wait_read(0);
+        if (ok) {
+            for (; released < stored; ++released) {
+                mbar_arrive(bars.empty(rel.s), 1u);
+                rel.next(p.NS);
+            }
+        }
+        bulk_wait_all();
+    }
+    __syncwarp();
+}
+
+// One thread issues every tensor-core instruction of the CTA.
+__device__ void tc_mma_issuer(const TcParams& tp, unsigned char* smem, TcBars bars,
+                              volatile int* abort, uint32_t tmem, bool bf16) {
+    const StepParams& p = tp.p;
+    const uint32_t stage0 = smem_addr(smem + p.off_stages);
+    const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
+    const uint32_t qbuf = smem_addr(smem + p.tc_off_qbuf);
+    const uint32_t pbuf = smem_addr(smem + p.tc_off_pbuf);
+    const int nkb = static_cast<int>(p.D / 64);
+    const int Dv = static_cast<int>(p.Dv);
+    const uint32_t idesc_s = mma_idesc_f16(128, kTcT, bf16, false);
+    const uint32_t idesc_o = mma_idesc_f16(128, Dv, bf16, true);
+    const uint32_t tmem_o = tmem + 2 * kTcT;
+    Ring ring;
+    uint32_t pbits = 0;          // parity of each stage's patched barrier
+    uint32_t q_ph = 0, p_ph = 0;
+    int sbuf = 0;
+    int s_uses[2] = {0, 0};
+    bool attend = false, has_pending = false, pend_first = false;
+    int pend_stage = 0;
+    int64_t N = 0;
+
+    auto issue_pv = [&](int stage, bool first) -> bool {
+        if (!mbar_wait(bars.p_ready(), p_ph, abort)) return false;
+        p_ph ^= 1u;
+        tc_fence_after();
+        const uint32_t sV = stage0 + static_cast<uint32_t>(stage) * p.stage_bytes +
+                            static_cast<uint32_t>(nkb * kBox);
+#pragma unroll
+        for (int kk = 0; kk < kTcT / 16; ++kk)
+            tc_mma(tmem_o, smem_desc_sw128(pbuf + kk * 32, 16, 1024),
+                   smem_desc_sw128(sV + kk * 16 * 128, kBox, 1024), idesc_o, !(first && kk == 0));
+        tc_commit(bars.o_done());
+        tc_commit(bars.empty(stage));
+        return true;
+    };
+
+    for (;;) {
+        const int s = ring.s;
+        const uint32_t ph = ring.ph;
+        ring.next(p.NS);
+        if (!mbar_wait(bars.full(s), ph, abort)) break;
+        const TileMeta mt = meta[s];
+        if (mt.flags & kDone) break;
+        if (mt.flags & kFirst) {
+            N = mt.L + mt.n;
+            attend = mt.n > 0 && static_cast<int64_t>(mt.i) * kTcT < N;
+        }
+        const bool comp = attend && static_cast<int64_t>(mt.i) * kTcT < N;
+        // consume every patched phase the storer produces on this stage
+        const PatchRange pr = patch_range(mt, p.M);
+        if (pr.c > pr.a) {
+            if (!mbar_wait(bars.patched(s), (pbits >> s) & 1u, abort)) break;
+            pbits ^= 1u << s;
+        }
+        if (comp) {
+            if (mt.flags & kFirst) {
+                if (!mbar_wait(bars.q_ready(), q_ph, abort)) break;
+                q_ph ^= 1u;
+            }
+            if (s_uses[sbuf] > 0 &&
+                !mbar_wait(bars.s_free(sbuf), static_cast<uint32_t>((s_uses[sbuf] - 1) & 1), abort))
+                break;
+            tc_fence_after();
+            const uint32_t sK = stage0 + static_cast<uint32_t>(s) * p.stage_bytes;
+            const uint32_t tmem_s = tmem + sbuf * kTcT;
+            for (int kb = 0; kb < nkb; ++kb) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma(tmem_s, smem_desc_sw128(qbuf + kb * kQBox + kk * 32, 16, 1024),
+                           smem_desc_sw128(sK + kb * kBox + kk * 32, 16, 1024), idesc_s,
+                           (kb | kk) != 0);
+            }
+            tc_commit(bars.s_ready(sbuf));
+            ++s_uses[sbuf];
+            sbuf ^= 1;
+            if (has_pending && !issue_pv(pend_stage, pend_first)) break;
+            has_pending = true;
+            pend_stage = s;
+            pend_first = (mt.flags & kFirst) != 0;
+        } else {
+            // A product may wait for the next tile only if that tile attends:
+            // a pending stage is not released, and the ring must keep moving.
+            if (has_pending) {
+                if (!issue_pv(pend_stage, pend_first)) break;
+                has_pending = false;
+            }
+            mbar_arrive(bars.empty(s), 1u);
+        }
+        if ((mt.flags & kLast) && attend && has_pending) {
+            if (!issue_pv(pend_stage, pend_first)) break;
+            has_pending = false;
+        }
+    }
+    // every issued tensor-core instruction has finished before the CTA frees
+    // tensor memory (also when a wait gave up)
+    tc_commit(bars.drained());
+    volatile int never = 0;
+    mbar_wait(bars.drained(), 0u, &never);
+}
+
+template <typename T>
+__device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
+                           volatile int* abort, uint32_t tmem) {
+    const StepParams& p = tp.p;
+    const int r = threadIdx.x;  // query row of the unit (tensor-memory lane)
+    const int w = r >> 5, lane = r & 31;
+    const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
+    unsigned char* qbuf = smem + p.tc_off_qbuf;
+    unsigned char* pbuf = smem + p.tc_off_pbuf;
+    const int R = static_cast<int>(p.R), Q = static_cast<int>(p.Q), D = static_cast<int>(p.D);
+    const int Dv = static_cast<int>(p.Dv);
+    const int ckQ = D * p.es / 16;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(w * 32) << 16);  // this warp's lanes
+    const unsigned char* query = static_cast<const unsigned char*>(p.query);
+    Ring ring;
+    int sbuf = 0;
+    int s_uses[2] = {0, 0};
+    uint32_t o_ph = 0;
+    bool attend = false, first_tile = false;
+    int64_t L = 0, n = 0, N = 0, u = 0, k = 0, rowg = 0;
+    int lim = -1;
+    bool valid = false;
+    float m_ref = -INFINITY, l = 0.f;
+
+    for (;;) {
+        const int s = ring.s;
+        const uint32_t ph = ring.ph;
+        ring.next(p.NS);
+        if (!warp_wait(bars.full(s), ph, abort)) break;
+        const TileMeta mt = meta[s];
+        if (mt.flags & kDone) break;
+        if (lane == 0) mbar_arrive(bars.empty(s), 1u);  // this role reads only the metadata
+        if (mt.flags & kFirst) {
+            u = mt.u;
+            k = mt.k;
+            L = mt.L;
+            n = mt.n;
+            N = L + n;
+            attend = n > 0 && static_cast<int64_t>(mt.i) * kTcT < N;
+            const int64_t b = u / p.Hk, kv = u - b * p.Hk;
+            if (k == 0 && kv == 0 && r == 0) {
+                const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
+                p.out_lengths[b] = ra.L + ra.n;
+                if (ra.flags && p.dev_status) atomicOr(p.dev_status, ra.flags);
+            }
+            if (attend) {
+                // every tensor-core instruction of the previous chunk has finished
+                const int t = Q > 0 ? r % Q : 0;
+                valid = r < R && t < n;
+                lim = valid ? static_cast<int>(L + t) : -1;
+                rowg = ((b * p.Hq + kv * p.G + r / max(Q, 1)) * p.Q + t);
+                const unsigned char* src = query + rowg * D * p.es;
+                for (int ch = 0; ch < ckQ; ++ch) {
+                    const uint4 v = r < R ? *reinterpret_cast<const uint4*>(src + ch * 16)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(qbuf + (ch >> 3) * kQBox + r * 128 +
+                                              (((ch & 7) ^ (r & 7)) << 4)) = v;
+                }
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.q_ready(), 1u);
+                m_ref = -INFINITY;
+                l = 0.f;
+                first_tile = true;
+            }
+        }
+        const bool comp = attend && static_cast<int64_t>(mt.i) * kTcT < N;
+        if (comp) {
+            if (!warp_wait(bars.s_ready(sbuf), static_cast<uint32_t>(s_uses[sbuf] & 1), abort)) break;
+            ++s_uses[sbuf];
+            tc_fence_after();
+            float sv[kTcT];
+            tmem_ld32(trow + sbuf * kTcT, sv);
+            tmem_ld32(trow + sbuf * kTcT + 32, sv + 32);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.s_free(sbuf), 1u);
+            sbuf ^= 1;
+            const int j0 = mt.i * kTcT;
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kTcT; ++c) {
+                sv[c] = (j0 + c <= lim) ? sv[c] * p.qscale : -INFINITY;
+                tmax = fmaxf(tmax, sv[c]);
+            }
+            if (!first_tile) {  // P buffer free and O quiescent: the previous product is done
+                if (!warp_wait(bars.o_done(), o_ph, abort)) break;
+                o_ph ^= 1u;
+            }
+            const bool raise = tmax > m_ref + kRescale || (m_ref == -INFINITY && tmax != -INFINITY);
+            const float corr = (raise && m_ref != -INFINITY) ? fast_exp2(m_ref - tmax) : 1.f;
+            if (__any_sync(0xffffffffu, raise && m_ref != -INFINITY && !first_tile)) {
+                tc_fence_after();
+                for (int cb = 0; cb < Dv; cb += 32) {
+                    float ov[32];
+                    tmem_ld32(trow + 2 * kTcT + cb, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] *= corr;
+                    tmem_st32(trow + 2 * kTcT + cb, ov);
+                }
+                tmem_wait_st();
+            }
+            if (raise) {
+                l *= corr;
+                m_ref = tmax;
+            }
+            // P row: 2^(s - ref), as the operand type for O += P V and as fp16 for the rows
+            float lsum = 0.f;
+            uint32_t pk[kTcT / 2];   // operand type, two per word
+            uint32_t phb[kTcT / 2];  // fp16, two per word
+#pragma unroll
+            for (int c = 0; c < kTcT; c += 2) {
+                const float e0 = (sv[c] == -INFINITY) ? 0.f : fast_exp2(sv[c] - m_ref);
+                const float e1 = (sv[c + 1] == -INFINITY) ? 0.f : fast_exp2(sv[c + 1] - m_ref);
+                lsum += e0 + e1;
+                const T a = Storage<T>::from_float(e0), bb = Storage<T>::from_float(e1);
+                pk[c / 2] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&a)) |
+                            (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&bb)) << 16);
+                const __half h0 = __float2half_rn(e0), h1 = __float2half_rn(e1);
+                phb[c / 2] = static_cast<uint32_t>(__half_as_ushort(h0)) |
+                             (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+            }
+            l += lsum;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(pbuf + r * 128 + ((ch ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            if (valid && j0 <= lim) {
+                __half* dst = p.pvals + rowg * p.M + j0;
+                if (j0 + kTcT <= p.M && (p.M & 7) == 0) {
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        *reinterpret_cast<uint4*>(dst + 8 * ch) =
+                            make_uint4(phb[4 * ch], phb[4 * ch + 1], phb[4 * ch + 2], phb[4 * ch + 3]);
+                } else {
+                    for (int c = 0; c < kTcT && j0 + c < p.M; ++c)
+                        dst[c] = __ushort_as_half(static_cast<unsigned short>(phb[c / 2] >> ((c & 1) * 16)));
+                }
+                p.tile_max[rowg * p.tiles64 + mt.i] = m_ref;
+            }
+            fence_async_shared();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_ready(), 1u);
+            first_tile = false;
+        }
+        if ((mt.flags & kLast) && attend) {
+            // the chunk's last product: read O and write the row's partial
+            if (!warp_wait(bars.o_done(), o_ph, abort)) break;
+            o_ph ^= 1u;
+            tc_fence_after();
+            const int64_t s_k = k * p.CH * kTcT;
+            const bool write = valid && s_k <= lim;
+            const int64_t prow = (u * p.KP + k) * p.R + r;
+            for (int cb = 0; cb < Dv; cb += 32) {
+                float ov[32];
+                tmem_ld32(trow + 2 * kTcT + cb, ov);
+                tmem_wait_ld();
+                if (write) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(p.part_acc + prow * Dv + cb + e) =
+                            make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
+                }
+            }
+            if (write) {
+                p.part_ml[2 * prow] = m_ref;
+                p.part_ml[2 * prow + 1] = l;
+            }
+            tc_fence_before();
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_step_kernel(const __grid_constant__ TcParams tp) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const StepParams& p = tp.p;
+    const TcBars bars{smem_addr(smem)};
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + p.off_flag);
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.NS; ++s) {
+            mbar_init(bars.full(s), 1u);
+            mbar_init(bars.empty(s), 2u + kSoftWarps);  // storer, MMA issuer, softmax warps
+            mbar_init(bars.patched(s), 1u);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bars.s_ready(b), 1u);
+            mbar_init(bars.s_free(b), kSoftWarps);
+        }
+        mbar_init(bars.p_ready(), kSoftWarps);
+        mbar_init(bars.o_done(), 1u);
+        mbar_init(bars.q_ready(), kSoftWarps);
+        mbar_init(bars.drained(), 1u);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(smem + kTmemSlot), static_cast<uint32_t>(p.tc_tmem_cols));
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
+
+    if (warp < kSoftWarps) {
+        tc_softmax<T>(tp, smem, bars, abort, tmem);
+    } else if (warp == kMmaWarp) {
+        if ((threadIdx.x & 31) == 0)
+            tc_mma_issuer(tp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value);
+    } else if (warp == kProdWarp) {
+        if ((threadIdx.x & 31) == 0) tc_producer(tp, smem, bars, abort);
+    } else if (warp == kStoreWarp) {
+        tc_storer(tp, smem, bars, abort);
+    }
+    tc_fence_before();
+    __syncthreads();  // every thread reaches this exactly once: all waits are bounded
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, static_cast<uint32_t>(p.tc_tmem_cols));
+    }
+    if (threadIdx.x == 0 && *abort && p.dev_status) atomicOr(p.dev_status, KVC_DEV_TIMEOUT);
+}
+
+}  // namespace
+
+cudaError_t launch_fused_tc(const TcParams& tp, int dtype, size_t smem, cudaStream_t stream) {
+    auto kern = dtype == KVC_BF16 ? tc_step_kernel<__nv_bfloat16> : tc_step_kernel<__half>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(tp.p.P), kTcThreads, smem, stream>>>(tp);
+    return cudaGetLastError();
+}
+
+}  // namespace kvc

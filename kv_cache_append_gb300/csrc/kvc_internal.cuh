@@ -204,13 +204,16 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
         : "memory");
 }
 
-// 32 consecutive 32-bit TMEM columns of this warp's 32 lanes (one lane per thread).
+// 32 consecutive 32-bit TMEM columns of this warp's 32 lanes (one lane per
+// thread). The wait is in the same statement, so the outputs are complete
+// when the statement ends.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
           "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
@@ -222,11 +225,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// The store's source registers are free again when the statement ends.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
         "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
         "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
         "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
         "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
@@ -444,6 +449,17 @@ struct StepParams {
     float* part_acc;  // [U][KP][R][Dv] (unnormalised weighted values)
     float* scores;    // [B][Hq][Q][M]  (scale*log2e*dot, allowed slots only)
     unsigned int* counter;  // next chunk to hand out (zeroed before each launch)
+    // How the attention rows' inputs are kept between the kernels:
+    //   score_fmt 0: scores = scale*log2e*dot, fp32, [B][Hq][Q][M];
+    //   score_fmt 1: pvals = 2^(score - tile_max) as fp16 [B][Hq][Q][M], with
+    //                tile_max the reference maximum per (row, 64-slot tile),
+    //                fp32 [B][Hq][Q][ceil(M/64)].
+    int score_fmt;
+    __half* pvals;
+    float* tile_max;
+    int64_t tiles64;  // ceil(M / 64)
+    // tensor-core kernel layout
+    int tc_off_qbuf, tc_off_pbuf, tc_tmem_cols;
     int32_t* dev_status;
     int vec_attention;  // 1: attention rows may be written 8 elements at a time
 };

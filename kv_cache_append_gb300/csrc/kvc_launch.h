@@ -1,6 +1,7 @@
 // kvc_launch.h -- host-side launchers of libkvc's kernels (internal).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "kvc_internal.cuh"
@@ -12,6 +13,20 @@ namespace kvc {
 // per lane; nchl == 0: 8 rows per warp read from shared memory.
 cudaError_t launch_fused(const StepParams& p, int dtype, int dvc, int nchl, size_t smem,
                          cudaStream_t stream);
+
+// Kernel parameters of the tensor-core fused kernel: the four caches as TMA
+// tensor maps ([U][M][width], boxes of 64 elements x 64 slots, 128-byte
+// swizzle) and the common parameters.
+struct TcParams {
+    CUtensorMap tm_k;   // key_cache
+    CUtensorMap tm_v;   // value_cache
+    CUtensorMap tm_ok;  // out_key_cache
+    CUtensorMap tm_ov;  // out_value_cache
+    StepParams p;
+};
+
+// Fused copy + scatter + attention partials on the tensor cores (kvc_fused_tc.cu).
+cudaError_t launch_fused_tc(const TcParams& tp, int dtype, size_t smem, cudaStream_t stream);
 
 // Merge of the partials, context rows and attention rows (kvc_finalize.cu).
 cudaError_t launch_finalize(const StepParams& p, int dtype, cudaStream_t stream);

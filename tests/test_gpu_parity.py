@@ -265,3 +265,62 @@ def test_full_size_workload(name):
     compare_batch_rows(x, out, bsel)
     del out, x
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ tensor-core path
+TC = {
+    "r128_fp16_D192_Dv128": Spec(B=2, Hq=16, Hk=1, Q=8, D=192, Dv=128, M=3000, dtype="f16",
+                                 lengths=("uniform", 2000, 2992), std=0.5, scale=0.05),
+    "r64_bf16_ragged": Spec(B=3, Hq=16, Hk=2, Q=8, D=128, Dv=128, M=700, dtype="bf16",
+                            lengths=("uniform", 0, 692), counts=("uniform", 0, 8)),
+    "r64_bf16_D64_Dv256": Spec(B=2, Hq=8, Hk=1, Q=8, D=64, Dv=256, M=333, dtype="bf16",
+                               lengths=("uniform", 100, 325)),
+    "r64_fp16_D256_Dv64": Spec(B=2, Hq=4, Hk=1, Q=16, D=256, Dv=64, M=512, dtype="f16",
+                               lengths=("uniform", 0, 496), counts=("uniform", 1, 16)),
+    "r96_bf16_hot": Spec(B=2, Hq=12, Hk=1, Q=8, D=128, Dv=128, M=1024, dtype="bf16",
+                         hot_frac=0.2, hot_scale=50.0),
+}
+
+
+def _path(x):
+    return kvc.plan_info(kvc.dims_of(x.query, x.key_cache, x.value_cache), x.key_cache,
+                         x.value_cache, x.new_key, x.new_value, x.key_cache, x.value_cache)[1]
+
+
+@pytest.mark.parametrize("name", sorted(TC))
+@pytest.mark.parametrize("seed", [0, 1])
+def test_tensor_core_path(name, seed):
+    x = workloads.generate(TC[name], seed)
+    xg = x.to(DEV)
+    assert _path(xg) == "tensor"
+    out, status = run_gpu(xg)
+    compare_full(x, out, status)
+
+
+def test_tensor_core_path_growing_scores():
+    """Scores that grow along the slots raise the reference maximum on many
+    tiles, so the context accumulator is rescaled again and again."""
+    spec = Spec(B=2, Hq=16, Hk=2, Q=8, D=128, Dv=128, M=640, dtype="bf16",
+                lengths=("fixed", 600))
+    x = workloads.generate(spec, 9)
+    ramp = (1.0 + torch.arange(spec.M, dtype=torch.float32) / 24.0)[None, None, :, None]
+    x.key_cache = (x.key_cache.float() * ramp).to(torch.bfloat16)
+    x.query = (x.query.float() * 4.0).to(torch.bfloat16)
+    xg = x.to(DEV)
+    assert _path(xg) == "tensor"
+    out, status = run_gpu(xg)
+    compare_full(x, out, status)
+
+
+def test_tensor_core_path_contract_violations():
+    spec = Spec(B=4, Hq=16, Hk=2, Q=8, D=64, Dv=64, M=256, dtype="f16")
+    x = workloads.generate(spec, 11)
+    x.lengths = torch.tensor([10, 250, 300, 100])
+    m = workloads.prefix_mask([8, 8, 3, 8], 8)
+    m[3, 6] = False
+    m[3, 7] = True   # not a prefix
+    x.append_mask = m
+    xg = x.to(DEV)
+    assert _path(xg) == "tensor"
+    out, status = run_gpu(xg)
+    compare_full(x, out, status, expect_flags=kvc.DEV_MASK | kvc.DEV_OVERFLOW)
