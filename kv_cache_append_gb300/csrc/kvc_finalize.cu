@@ -49,10 +49,104 @@ __device__ __forceinline__ void store8<__half>(__half* dst, const float* v) {
     store8_16(dst, v);
 }
 
+constexpr int kWeightCap = 1024;  // chunk weights kept in shared memory
+
+// Block-wide max / sum of one float per thread.
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    float r = lane < nw ? red[lane] : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, o));
+    return r;
+}
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    float r = lane < nw ? red[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    return r;
+}
+
+// Eight attention values starting at slot j0 of a row (vectorised path).
+template <int FMT>
+__device__ __forceinline__ void row8(const StepParams& p, const float* sc, const __half* pv,
+                                     const float* tmx, int64_t j0, int64_t lim, float mx,
+                                     float inv_l, float* v) {
+    if (j0 > lim) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        return;
+    }
+    if constexpr (FMT == 1) {
+        const float c = fast_exp2(tmx[j0 >> 6] - mx) * inv_l;
+        const uint4 raw = *reinterpret_cast<const uint4*>(pv + j0);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const __half h =
+                __ushort_as_half(static_cast<unsigned short>(w[i >> 1] >> ((i & 1) * 16)));
+            v[i] = (j0 + i <= lim) ? __half2float(h) * c : 0.f;
+        }
+    } else {
+        const float4 a = *reinterpret_cast<const float4*>(sc + j0);
+        const float4 b = *reinterpret_cast<const float4*>(sc + j0 + 4);
+        const float s8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = (j0 + i <= lim) ? fast_exp2(s8[i] - mx) * inv_l : 0.f;
+    }
+}
+
+template <typename T, int FMT>
+__device__ __forceinline__ void write_row(const StepParams& p, T* att, int64_t row, int64_t lim,
+                                          float mx, float inv_l) {
+    using S = Storage<T>;
+    const float* sc = p.scores + row * p.M;
+    const __half* pv = p.pvals + row * p.M;
+    const float* tmx = p.tile_max + row * p.tiles64;
+    if (p.vec_attention) {
+        constexpr int U4 = 4;  // vectors in flight per thread
+        const int64_t step = static_cast<int64_t>(blockDim.x) * 8;
+        int64_t j0 = static_cast<int64_t>(threadIdx.x) * 8;
+        for (; j0 + (U4 - 1) * step < p.M; j0 += U4 * step) {
+            float v[U4][8];
+#pragma unroll
+            for (int q = 0; q < U4; ++q) row8<FMT>(p, sc, pv, tmx, j0 + q * step, lim, mx, inv_l, v[q]);
+#pragma unroll
+            for (int q = 0; q < U4; ++q) store8<T>(att + j0 + q * step, v[q]);
+        }
+        for (; j0 < p.M; j0 += step) {
+            float v[8];
+            row8<FMT>(p, sc, pv, tmx, j0, lim, mx, inv_l, v);
+            store8<T>(att + j0, v);
+        }
+    } else {
+        for (int64_t j = threadIdx.x; j < p.M; j += blockDim.x) {
+            float a = 0.f;
+            if (j <= lim)
+                a = FMT == 1 ? __half2float(pv[j]) * fast_exp2(tmx[j >> 6] - mx) * inv_l
+                             : fast_exp2(sc[j] - mx) * inv_l;
+            att[j] = S::from_float(a);
+        }
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kFinalizeThreads)
     finalize_kernel(const __grid_constant__ StepParams p) {
     using S = Storage<T>;
+    __shared__ float wts[kWeightCap];
+    __shared__ float red[32];
+    __shared__ float part[kFinalizeThreads];
     const int64_t row = blockIdx.x;  // (b * Hq + h) * Q + t
     const int64_t t = row % p.Q, bh = row / p.Q;
     const int64_t h = bh % p.Hq, b = bh / p.Hq;
@@ -61,6 +155,7 @@ __global__ void __launch_bounds__(kFinalizeThreads)
     T* att = static_cast<T*>(p.out_attention) + row * p.M;
     T* ctx = static_cast<T*>(p.out_context) + row * p.Dv;
     const bool valid = t < ra.n;
+    const int nthr = blockDim.x;
 
     float mx = 0.f, inv_l = 0.f;
     int64_t lim = -1;  // last allowed slot
@@ -68,78 +163,59 @@ __global__ void __launch_bounds__(kFinalizeThreads)
         lim = ra.L + t;
         // chunks whose first slot is allowed for this row wrote a partial
         const int64_t kmax = min(p.KP, lim / (p.CH * p.T) + 1);
-        mx = -INFINITY;
-        for (int64_t k = 0; k < kmax; ++k) mx = fmaxf(mx, p.part_ml[2 * ((u * p.KP + k) * p.R + r)]);
-        float l = 0.f;
-        for (int64_t k = 0; k < kmax; ++k) {
-            const int64_t pr = (u * p.KP + k) * p.R + r;
-            l += p.part_ml[2 * pr + 1] * fast_exp2(p.part_ml[2 * pr] - mx);
+        const float* ml = p.part_ml + 2 * (u * p.KP * p.R + r);  // chunk k at ml[2 * k * R]
+        const int64_t kstride = 2 * p.R;
+        float lm = -INFINITY;
+        for (int64_t k = threadIdx.x; k < kmax; k += nthr) lm = fmaxf(lm, ml[k * kstride]);
+        mx = block_max(lm, red);
+        float ls = 0.f;
+        for (int64_t k = threadIdx.x; k < kmax; k += nthr) {
+            const float w = fast_exp2(ml[k * kstride] - mx);
+            if (k < kWeightCap) wts[k] = w;
+            ls = fmaf(ml[k * kstride + 1], w, ls);
         }
-        inv_l = 1.f / l;
-        for (int64_t e = threadIdx.x; e < p.Dv; e += blockDim.x) {
-            float a = 0.f;
-            for (int64_t k = 0; k < kmax; ++k) {
-                const int64_t pr = (u * p.KP + k) * p.R + r;
-                a = fmaf(p.part_acc[pr * p.Dv + e], fast_exp2(p.part_ml[2 * pr] - mx), a);
+        inv_l = 1.f / block_sum(ls, red);  // block_sum's barriers also publish wts
+        // context: thread groups split the chunks, threads of a group split Dv
+        const int Dv = static_cast<int>(p.Dv);
+        const int ng = max(1, nthr / Dv);
+        const int g = threadIdx.x / Dv, e = threadIdx.x - g * Dv;
+        const float* acc = p.part_acc + (u * p.KP * p.R + r) * p.Dv;  // chunk k at acc[k * R * Dv]
+        const int64_t astride = p.R * p.Dv;
+        for (int e0 = (ng > 1 ? e : threadIdx.x); e0 < Dv; e0 += (ng > 1 ? Dv : nthr)) {
+            if (g >= ng) break;
+            float a0 = 0.f, a1 = 0.f;
+            int64_t k = g;
+            for (; k + ng < kmax; k += 2 * ng) {
+                const float w0 = k < kWeightCap ? wts[k] : fast_exp2(ml[k * kstride] - mx);
+                const float w1 = k + ng < kWeightCap ? wts[k + ng] : fast_exp2(ml[(k + ng) * kstride] - mx);
+                a0 = fmaf(acc[k * astride + e0], w0, a0);
+                a1 = fmaf(acc[(k + ng) * astride + e0], w1, a1);
             }
-            ctx[e] = S::from_float(a * inv_l);
-        }
-    } else {
-        for (int64_t e = threadIdx.x; e < p.Dv; e += blockDim.x) ctx[e] = S::from_float(0.f);
-    }
-
-    if (p.score_fmt == 1) {
-        // fp16 2^(s - tile max) per slot and one maximum per 64-slot tile
-        const __half* pv = p.pvals + row * p.M;
-        const float* tmx = p.tile_max + row * p.tiles64;
-        if (p.vec_attention) {
-            for (int64_t j0 = static_cast<int64_t>(threadIdx.x) * 8; j0 < p.M;
-                 j0 += static_cast<int64_t>(blockDim.x) * 8) {
-                float v[8];
-                if (j0 <= lim) {
-                    const float c = fast_exp2(tmx[j0 >> 6] - mx) * inv_l;
-                    const uint4 raw = *reinterpret_cast<const uint4*>(pv + j0);
-                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const __half h = __ushort_as_half(static_cast<unsigned short>(w[i >> 1] >> ((i & 1) * 16)));
-                        v[i] = (j0 + i <= lim) ? __half2float(h) * c : 0.f;
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) v[i] = 0.f;
-                }
-                store8<T>(att + j0, v);
+            if (k < kmax) {
+                const float w0 = k < kWeightCap ? wts[k] : fast_exp2(ml[k * kstride] - mx);
+                a0 = fmaf(acc[k * astride + e0], w0, a0);
             }
-        } else {
-            for (int64_t j = threadIdx.x; j < p.M; j += blockDim.x)
-                att[j] = S::from_float(
-                    j <= lim ? __half2float(pv[j]) * fast_exp2(tmx[j >> 6] - mx) * inv_l : 0.f);
-        }
-        return;
-    }
-    const float* sc = p.scores + row * p.M;
-    if (p.vec_attention) {
-        for (int64_t j0 = static_cast<int64_t>(threadIdx.x) * 8; j0 < p.M;
-             j0 += static_cast<int64_t>(blockDim.x) * 8) {
-            float v[8];
-            if (j0 <= lim) {
-                const float4 a = *reinterpret_cast<const float4*>(sc + j0);
-                const float4 c = *reinterpret_cast<const float4*>(sc + j0 + 4);
-                const float s[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    v[i] = (j0 + i <= lim) ? fast_exp2(s[i] - mx) * inv_l : 0.f;
+            if (ng > 1) {
+                part[threadIdx.x] = a0 + a1;
             } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = 0.f;
+                ctx[e0] = S::from_float((a0 + a1) * inv_l);
             }
-            store8<T>(att + j0, v);
+        }
+        if (ng > 1) {
+            __syncthreads();
+            for (int e0 = threadIdx.x; e0 < Dv; e0 += nthr) {
+                float a = 0.f;
+                for (int q = 0; q < ng; ++q) a += part[q * Dv + e0];
+                ctx[e0] = S::from_float(a * inv_l);
+            }
         }
     } else {
-        for (int64_t j = threadIdx.x; j < p.M; j += blockDim.x)
-            att[j] = S::from_float(j <= lim ? fast_exp2(sc[j] - mx) * inv_l : 0.f);
+        for (int64_t e = threadIdx.x; e < p.Dv; e += nthr) ctx[e] = S::from_float(0.f);
     }
+    if (p.score_fmt == 1)
+        write_row<T, 1>(p, att, row, lim, mx, inv_l);
+    else
+        write_row<T, 0>(p, att, row, lim, mx, inv_l);
 }
 
 }  // namespace

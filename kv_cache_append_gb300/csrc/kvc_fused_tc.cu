@@ -324,6 +324,7 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
     uint32_t o_ph = 0;
     bool attend = false, first_tile = false;
     int64_t L = 0, n = 0, N = 0, u = 0, k = 0, rowg = 0;
+    int64_t q_unit = -1;  // unit whose query rows the query block holds
     int lim = -1;
     bool valid = false;
     float m_ref = -INFINITY, l = 0.f;
@@ -355,12 +356,17 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
                 valid = r < R && t < n;
                 lim = valid ? static_cast<int>(L + t) : -1;
                 rowg = ((b * p.Hq + kv * p.G + r / max(Q, 1)) * p.Q + t);
-                const unsigned char* src = query + rowg * D * p.es;
-                for (int ch = 0; ch < ckQ; ++ch) {
-                    const uint4 v = r < R ? *reinterpret_cast<const uint4*>(src + ch * 16)
-                                          : make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(qbuf + (ch >> 3) * kQBox + r * 128 +
-                                              (((ch & 7) ^ (r & 7)) << 4)) = v;
+                if (u != q_unit) {  // the query block of another unit: reload it
+                    const unsigned char* src = query + rowg * D * p.es;
+                    for (int ch = 0; ch < ckQ; ++ch) {
+                        unsigned char* dst = qbuf + (ch >> 3) * kQBox + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+                        if (r < R)
+                            cp_async16(dst, src + ch * 16);
+                        else
+                            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    cp_async_wait_all();
+                    q_unit = u;
                 }
                 fence_async_shared();
                 __syncwarp();

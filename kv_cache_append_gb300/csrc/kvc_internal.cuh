@@ -160,6 +160,15 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, int x, int y, int
                  : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (no registers in between).
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA stores, tensor-core operand reads).
 __device__ __forceinline__ void fence_async_shared() {
