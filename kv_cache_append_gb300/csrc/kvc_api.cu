@@ -89,7 +89,6 @@ struct Plan {
 #define KVC_CHUNKS_PER_CTA 32
 #endif
 constexpr int64_t kChunksPerCta = KVC_CHUNKS_PER_CTA;  // aim: this many chunks per CTA
-constexpr int64_t kMinChunksPerCta = 8;   // never fewer (every CTA busy, tail short)
 constexpr int64_t kPartialRatio = 16;     // a chunk moves >= 16x its partials' bytes
 constexpr int64_t kMaxStagedQuery = 16384;
 
@@ -145,21 +144,38 @@ void fused_tiling(const kvc_dims& d, Plan* pl) {
     pl->NCHL = pl->RPW == 4 ? static_cast<int>((nck + 7) / 8) : 0;
 }
 
-// Chunks for `ctas` CTAs: about kChunksPerCta chunks per CTA, bigger when a
-// chunk's partials would be more than 1/kPartialRatio of the bytes it moves,
-// but never so big that a CTA gets fewer than kMinChunksPerCta.
-void chunking(const kvc_dims& d, int64_t ctas, Plan* pl) {
+// Chunks for `ctas` CTAs. Many chunks per CTA balance uneven rows (a CTA
+// that draws attention-heavy chunks takes fewer of them); but every chunk
+// that attends writes one partial per query row, which for wide units (many
+// query rows, long values) can outweigh the tile data itself. So start at
+// kChunksPerCta chunks per CTA and halve that until a chunk moves at least
+// kPartialRatio times its partials' bytes, then size chunks to split the
+// tiles into about ctas * m equal parts.
+int64_t chunk_tiles(const kvc_dims& d, int64_t ctas, int64_t T, int64_t TPU) {
     const int64_t es = elem_size(d.dtype);
     const int64_t U = d.B * d.Hk, R = (d.Hq / d.Hk) * d.Q;
-    const int64_t TT = U * pl->TPU;
-    const int64_t tile_bytes = int64_t(pl->T) * (d.D + d.Dv) * es;
-    const int64_t ch_part = (kPartialRatio * R * (d.Dv + 2) * 4 + tile_bytes - 1) / tile_bytes;
-    int64_t ch = std::max<int64_t>(TT / (ctas * kChunksPerCta), ch_part);
-    ch = std::min<int64_t>(ch, TT / (ctas * kMinChunksPerCta));
-    ch = std::max<int64_t>(1, std::min<int64_t>(ch, pl->TPU));
-    pl->CH = ch;
-    pl->KP = (pl->TPU + ch - 1) / ch;
-    pl->NQ = U * pl->KP;
+    const int64_t TT = U * TPU;
+    const int64_t tile_bytes = T * (d.D + d.Dv) * es;
+    const int64_t part_bytes = R * (d.Dv + 2) * 4;
+    int64_t m = kChunksPerCta, ch = 1;
+    for (;; m /= 2) {
+        ch = std::max<int64_t>(1, (TT + ctas * m - 1) / (ctas * m));
+        if (m == 1 || ch * tile_bytes >= kPartialRatio * part_bytes) break;
+    }
+    return std::min<int64_t>(ch, TPU);
+}
+
+void chunking(const kvc_dims& d, int64_t ctas, Plan* pl) {
+    pl->CH = chunk_tiles(d, ctas, pl->T, pl->TPU);
+    pl->KP = (pl->TPU + pl->CH - 1) / pl->CH;
+    pl->NQ = d.B * d.Hk * pl->KP;
+}
+
+// Largest chunk count per unit any GPU with up to kSizingCtas SMs may use.
+int64_t sizing_kp(const kvc_dims& d, int64_t T, int64_t TPU) {
+    int64_t ch = TPU;
+    for (int64_t c = 1; c <= kSizingCtas; ++c) ch = std::min(ch, chunk_tiles(d, c, T, TPU));
+    return (TPU + ch - 1) / ch;
 }
 
 // Full fused plan for a device with `sms` SMs and `smem_cap` bytes of
@@ -472,15 +488,13 @@ size_t kvc_workspace_bytes(const kvc_dims* dims) {
     if (fused_shapes(*dims)) {
         Plan f;
         fused_tiling(*dims, &f);
-        chunking(*dims, kSizingCtas, &f);
-        workspace_layout(*dims, f.KP, &f);
+        workspace_layout(*dims, sizing_kp(*dims, f.T, f.TPU), &f);
         bytes = std::max(bytes, f.ws_bytes);
     }
     if (tc_shapes(*dims)) {
         Plan t;
         tc_tiling(*dims, &t);
-        chunking(*dims, kSizingCtas, &t);
-        workspace_layout(*dims, t.KP, &t);
+        workspace_layout(*dims, sizing_kp(*dims, t.T, t.TPU), &t);
         bytes = std::max(bytes, t.ws_bytes);
     }
     return bytes;
