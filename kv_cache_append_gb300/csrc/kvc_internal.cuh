@@ -29,7 +29,7 @@ constexpr int kFusedThreads = (kConsumerWarps + 2) * 32;  // + producer warp + s
 #define KVC_CHUNK_ORDER 1
 #endif
 #ifndef KVC_STORE_LAG
-#define KVC_STORE_LAG 4
+#define KVC_STORE_LAG 1
 #endif
 constexpr int kMaxStages = KVC_MAX_STAGES;        // ring stages at most
 constexpr int kStageTargetBytes = KVC_STAGE_BYTES;  // cache bytes (K + V) per tile
