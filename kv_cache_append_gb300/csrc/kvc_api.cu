@@ -241,10 +241,13 @@ constexpr int kTcBox = 64 * 128;  // one 64-element-wide box of a tile
 
 // Shapes the tensor-core kernel takes: 16-bit caches, key and value widths
 // multiples of 64 (at most 256), KVC_TC_MIN_ROWS..128 query rows per unit.
+// Tensor memory holds S twice (2 x 64 columns), O (Dv), Q (D/2) and P twice
+// (2 x 32): Dv + D/2 <= 320.
 bool tc_shapes(const kvc_dims& d) {
     const int64_t R = (d.Hq / d.Hk) * d.Q;
     return d.dtype != KVC_F32 && d.D % 64 == 0 && d.D <= 256 && d.Dv % 64 == 0 && d.Dv <= 256 &&
-           d.Q >= 1 && R >= KVC_TC_MIN_ROWS && R <= 128 && d.B * d.Hk < (int64_t(1) << 31);
+           d.Dv + d.D / 2 <= 320 && d.Q >= 1 && R >= KVC_TC_MIN_ROWS && R <= 128 &&
+           d.B * d.Hk < (int64_t(1) << 31);
 }
 
 void tc_tiling(const kvc_dims& d, Plan* pl) {
@@ -260,11 +263,6 @@ bool tc_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
     pl->off_flag = 512;
     pl->off_meta = 1024;
     int64_t off = 2048;
-    pl->tc_off_qbuf = static_cast<int>(off);
-    off += nkb * 128 * 128;
-    pl->tc_off_pbuf = static_cast<int>(off);
-    off += 128 * 128;
-    off = align_up(off, 1024);
     pl->off_stages = static_cast<int>(off);
     const int64_t stage = (nkb + nvb) * kTcBox;
     pl->stage_bytes = static_cast<int>(stage);
@@ -272,7 +270,7 @@ bool tc_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
     pl->NS = static_cast<int>(std::min<int64_t>(kMaxStages, (smem_cap - off) / stage));
     pl->LAG = std::min(std::min(kStoreLag, 7), pl->NS - 1);
     pl->smem = static_cast<size_t>(off + int64_t(pl->NS) * stage);
-    pl->tc_tmem_cols = 2 * kTcT + d.Dv <= 256 ? 256 : 512;
+    pl->tc_tmem_cols = 512;  // S0, S1, O, Q, P0, P1
     chunking(d, sms, pl);
     pl->P = std::min<int64_t>(sms, pl->NQ);
     pl->tensor = true;

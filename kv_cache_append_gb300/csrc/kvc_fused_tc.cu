@@ -20,15 +20,23 @@
 //                  4). The tile in shared memory is then exactly the updated
 //                  cache tile, and the tensor cores read it from there.
 //   MMA warp       one thread: S = Q K^T (M = 128 query rows, N = 64 slots,
-//                  K = D) into one of two tensor-memory S buffers, then
-//                  O += P V (N = Dv, K = 64 slots) into the tensor-memory O.
-//   4 softmax      one query row per thread: reads its S row, applies
-//   warps          scale*log2(e) and the lower-right causal limit j <= length +
-//                  t (bullet 4), keeps a reference maximum (raised, and O
-//                  rescaled, only when a score exceeds it by more than 2^8),
-//                  writes P = 2^(s - ref) for the next product and, in fp16,
-//                  for the attention rows; at the end of a chunk it writes the
-//                  row's partial (reference max, sum, O row).
+//                  K = D; Q read from tensor memory) into one of two
+//                  tensor-memory S buffers, then O += P V (N = Dv, K = 64
+//                  slots; P read from one of two tensor-memory P buffers) into
+//                  the tensor-memory O.
+//   4 softmax      one query row per thread (= tensor-memory lane): writes the
+//   warps          unit's query row into tensor memory, reads its S row,
+//                  applies scale*log2(e) and the lower-right causal limit j <=
+//                  length + t (bullet 4), keeps a reference maximum (raised,
+//                  and O rescaled, only when a score exceeds it by more than
+//                  2^8), writes P = 2^(s - ref) into tensor memory for the
+//                  next product and, in fp16, to the workspace for the
+//                  attention rows; at the end of a chunk it writes the row's
+//                  partial (reference max, sum, O row).
+//
+// Tensor memory (512 columns x 128 lanes, fp32 words): S0 [0, 64), S1 [64,
+// 128), O [128, 128 + Dv), Q [128 + Dv, + D/2) as packed 16-bit pairs, P0 and
+// P1 32 columns each after Q.
 #include <cuda.h>
 
 #include <type_traits>
@@ -36,6 +44,7 @@
 #include "kvc_internal.cuh"
 #include "kvc_launch.h"
 #include "kvc_pipeline.cuh"
+#include "kvc_tcgen05.cuh"
 
 namespace kvc {
 
@@ -43,7 +52,6 @@ namespace {
 
 constexpr int kTcT = 64;                  // slots per tile
 constexpr int kBox = kTcT * 128;          // bytes of one 64-element-wide box of a tile
-constexpr int kQBox = 128 * 128;          // bytes of one 64-element-wide box of the query rows
 constexpr int kSoftWarps = 4;
 constexpr int kMmaWarp = 4, kProdWarp = 5, kStoreWarp = 6;
 constexpr int kTcThreads = 7 * 32;
@@ -56,12 +64,22 @@ struct TcBars {
     __device__ uint32_t patched(int s) const { return base + 256u + 8u * s; }
     __device__ uint32_t s_ready(int b) const { return base + 384u + 8u * b; }
     __device__ uint32_t s_free(int b) const { return base + 400u + 8u * b; }
-    __device__ uint32_t p_ready() const { return base + 416u; }
-    __device__ uint32_t o_done() const { return base + 424u; }
-    __device__ uint32_t q_ready() const { return base + 432u; }
-    __device__ uint32_t drained() const { return base + 440u; }
+    // One pair per P buffer: a buffer is written again only after the product
+    // that read it has finished, so neither barrier runs two phases ahead of
+    // its waiter.
+    __device__ uint32_t p_ready(int b) const { return base + 416u + 8u * b; }
+    __device__ uint32_t o_done(int b) const { return base + 432u + 8u * b; }
+    __device__ uint32_t q_ready() const { return base + 448u; }
+    __device__ uint32_t drained() const { return base + 456u; }
 };
-constexpr int kTmemSlot = 448;  // tensor-memory base address written by tcgen05.alloc
+constexpr int kTmemSlot = 464;  // tensor-memory base address written by tcgen05.alloc
+
+// Tensor-memory column of each region.
+struct TmemCols {
+    uint32_t o, q, p0;
+    __device__ TmemCols(int D, int Dv)
+        : o(2 * kTcT), q(2 * kTcT + Dv), p0(2 * kTcT + Dv + D / 2) {}
+};
 
 // Rows [a, c) of the tile starting at slot j0 must come from the new rows.
 struct PatchRange {
@@ -209,34 +227,36 @@ __device__ void tc_mma_issuer(const TcParams& tp, unsigned char* smem, TcBars ba
     const StepParams& p = tp.p;
     const uint32_t stage0 = smem_addr(smem + p.off_stages);
     const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
-    const uint32_t qbuf = smem_addr(smem + p.tc_off_qbuf);
-    const uint32_t pbuf = smem_addr(smem + p.tc_off_pbuf);
     const int nkb = static_cast<int>(p.D / 64);
     const int Dv = static_cast<int>(p.Dv);
+    const TmemCols cols(static_cast<int>(p.D), Dv);
     const uint32_t idesc_s = mma_idesc_f16(128, kTcT, bf16, false);
     const uint32_t idesc_o = mma_idesc_f16(128, Dv, bf16, true);
-    const uint32_t tmem_o = tmem + 2 * kTcT;
     Ring ring;
-    uint32_t pbits = 0;          // parity of each stage's patched barrier
-    uint32_t q_ph = 0, p_ph = 0;
+    uint32_t pbits = 0;  // parity of each stage's patched barrier
+    uint32_t q_ph = 0;
     int sbuf = 0;
     int s_uses[2] = {0, 0};
+    int64_t pv_count = 0;  // products O += P V issued; the c-th reads P[c % 2]
     bool attend = false, has_pending = false, pend_first = false;
     int pend_stage = 0;
     int64_t N = 0;
 
     auto issue_pv = [&](int stage, bool first) -> bool {
-        if (!mbar_wait(bars.p_ready(), p_ph, abort)) return false;
-        p_ph ^= 1u;
+        const int pb = static_cast<int>(pv_count & 1);
+        if (!mbar_wait(bars.p_ready(pb), static_cast<uint32_t>((pv_count >> 1) & 1), abort))
+            return false;
         tc_fence_after();
         const uint32_t sV = stage0 + static_cast<uint32_t>(stage) * p.stage_bytes +
                             static_cast<uint32_t>(nkb * kBox);
 #pragma unroll
         for (int kk = 0; kk < kTcT / 16; ++kk)
-            tc_mma(tmem_o, smem_desc_sw128(pbuf + kk * 32, 16, 1024),
-                   smem_desc_sw128(sV + kk * 16 * 128, kBox, 1024), idesc_o, !(first && kk == 0));
-        tc_commit(bars.o_done());
+            tc_mma_ts(tmem + cols.o, tmem + cols.p0 + 32 * pb + 8 * kk,
+                      smem_desc_sw128(sV + kk * 16 * 128, kBox, 1024), idesc_o,
+                      !(first && kk == 0));
+        tc_commit(bars.o_done(pb));
         tc_commit(bars.empty(stage));
+        ++pv_count;
         return true;
     };
 
@@ -272,9 +292,9 @@ __device__ void tc_mma_issuer(const TcParams& tp, unsigned char* smem, TcBars ba
             for (int kb = 0; kb < nkb; ++kb) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc_mma(tmem_s, smem_desc_sw128(qbuf + kb * kQBox + kk * 32, 16, 1024),
-                           smem_desc_sw128(sK + kb * kBox + kk * 32, 16, 1024), idesc_s,
-                           (kb | kk) != 0);
+                    tc_mma_ts(tmem_s, tmem + cols.q + 32 * kb + 8 * kk,
+                              smem_desc_sw128(sK + kb * kBox + kk * 32, 16, 1024), idesc_s,
+                              (kb | kk) != 0);
             }
             tc_commit(bars.s_ready(sbuf));
             ++s_uses[sbuf];
@@ -311,25 +331,37 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
     const int r = threadIdx.x;  // query row of the unit (tensor-memory lane)
     const int w = r >> 5, lane = r & 31;
     const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
-    unsigned char* qbuf = smem + p.tc_off_qbuf;
-    unsigned char* pbuf = smem + p.tc_off_pbuf;
     const int R = static_cast<int>(p.R), Q = static_cast<int>(p.Q), D = static_cast<int>(p.D);
     const int Dv = static_cast<int>(p.Dv);
-    const int ckQ = D * p.es / 16;
+    const TmemCols cols(D, Dv);
     const uint32_t trow = tmem + (static_cast<uint32_t>(w * 32) << 16);  // this warp's lanes
     const unsigned char* query = static_cast<const unsigned char*>(p.query);
     Ring ring;
     int sbuf = 0;
     int s_uses[2] = {0, 0};
-    uint32_t o_ph = 0;
+    int64_t comp = 0;                  // attending tiles done so far = products issued for them
+    int64_t pv_seen[2] = {0, 0};       // completions consumed on o_done[b]
     bool attend = false, first_tile = false;
     int64_t L = 0, n = 0, N = 0, u = 0, k = 0, rowg = 0;
-    int64_t q_unit = -1;  // unit whose query rows the query block holds
+    int64_t q_unit = -1;  // unit whose query rows tensor memory holds
     int lim = -1;
     bool valid = false;
     float m_ref = -INFINITY, l = 0.f;
 
-    for (;;) {
+    // Wait until product c (which read P[c % 2]) has completed, consuming the
+    // completions of that barrier strictly in order.
+    auto wait_pv = [&](int64_t c) -> bool {
+        const int b = static_cast<int>(c & 1);
+        const int64_t kth = c >> 1;
+        while (pv_seen[b] <= kth) {
+            if (!warp_wait(bars.o_done(b), static_cast<uint32_t>(pv_seen[b] & 1), abort)) return false;
+            ++pv_seen[b];
+        }
+        return true;
+    };
+
+    bool ok = true;
+    while (ok) {
         const int s = ring.s;
         const uint32_t ph = ring.ph;
         ring.next(p.NS);
@@ -351,24 +383,25 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
                 if (ra.flags && p.dev_status) atomicOr(p.dev_status, ra.flags);
             }
             if (attend) {
-                // every tensor-core instruction of the previous chunk has finished
-                const int t = Q > 0 ? r % Q : 0;
+                // every tensor-core instruction of earlier chunks has finished
+                const int t = r % Q;
                 valid = r < R && t < n;
                 lim = valid ? static_cast<int>(L + t) : -1;
-                rowg = ((b * p.Hq + kv * p.G + r / max(Q, 1)) * p.Q + t);
-                if (u != q_unit) {  // the query block of another unit: reload it
-                    const unsigned char* src = query + rowg * D * p.es;
-                    for (int ch = 0; ch < ckQ; ++ch) {
-                        unsigned char* dst = qbuf + (ch >> 3) * kQBox + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-                        if (r < R)
-                            cp_async16(dst, src + ch * 16);
-                        else
-                            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                rowg = ((b * p.Hq + kv * p.G + r / Q) * p.Q + t);
+                if (u != q_unit) {  // this row's query into tensor memory, 64 elements at a time
+                    const uint4* src = reinterpret_cast<const uint4*>(query + rowg * D * p.es);
+                    for (int g = 0; g < D / 64; ++g) {
+                        uint32_t wq[32];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 v = r < R ? src[8 * g + c] : make_uint4(0u, 0u, 0u, 0u);
+                            wq[4 * c] = v.x; wq[4 * c + 1] = v.y; wq[4 * c + 2] = v.z; wq[4 * c + 3] = v.w;
+                        }
+                        tmem_st32u(trow + cols.q + 32 * g, wq);
                     }
-                    cp_async_wait_all();
                     q_unit = u;
                 }
-                fence_async_shared();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars.q_ready(), 1u);
                 m_ref = -INFINITY;
@@ -376,15 +409,14 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
                 first_tile = true;
             }
         }
-        const bool comp = attend && static_cast<int64_t>(mt.i) * kTcT < N;
-        if (comp) {
+        const bool is_comp = attend && static_cast<int64_t>(mt.i) * kTcT < N;
+        if (is_comp) {
             if (!warp_wait(bars.s_ready(sbuf), static_cast<uint32_t>(s_uses[sbuf] & 1), abort)) break;
             ++s_uses[sbuf];
             tc_fence_after();
             float sv[kTcT];
             tmem_ld32(trow + sbuf * kTcT, sv);
             tmem_ld32(trow + sbuf * kTcT + 32, sv + 32);
-            tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.s_free(sbuf), 1u);
@@ -396,23 +428,22 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
                 sv[c] = (j0 + c <= lim) ? sv[c] * p.qscale : -INFINITY;
                 tmax = fmaxf(tmax, sv[c]);
             }
-            if (!first_tile) {  // P buffer free and O quiescent: the previous product is done
-                if (!warp_wait(bars.o_done(), o_ph, abort)) break;
-                o_ph ^= 1u;
-            }
+            // P[comp % 2] is free once the product two tiles back has finished
+            if (comp >= 2 && !wait_pv(comp - 2)) break;
             const bool raise = tmax > m_ref + kRescale || (m_ref == -INFINITY && tmax != -INFINITY);
             const float corr = (raise && m_ref != -INFINITY) ? fast_exp2(m_ref - tmax) : 1.f;
             if (__any_sync(0xffffffffu, raise && m_ref != -INFINITY && !first_tile)) {
+                // O must be quiescent: the previous product has finished, this
+                // tile's is not issued before p_ready
+                if (!wait_pv(comp - 1)) break;
                 tc_fence_after();
                 for (int cb = 0; cb < Dv; cb += 32) {
                     float ov[32];
-                    tmem_ld32(trow + 2 * kTcT + cb, ov);
-                    tmem_wait_ld();
+                    tmem_ld32(trow + cols.o + cb, ov);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ov[e] *= corr;
-                    tmem_st32(trow + 2 * kTcT + cb, ov);
+                    tmem_st32(trow + cols.o + cb, ov);
                 }
-                tmem_wait_st();
             }
             if (raise) {
                 l *= corr;
@@ -435,10 +466,7 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
                              (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
             }
             l += lsum;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(pbuf + r * 128 + ((ch ^ (r & 7)) << 4)) =
-                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            tmem_st32u(trow + cols.p0 + 32 * static_cast<uint32_t>(comp & 1), pk);
             if (valid && j0 <= lim) {
                 __half* dst = p.pvals + rowg * p.M + j0;
                 if (j0 + kTcT <= p.M && (p.M & 7) == 0) {
@@ -452,24 +480,22 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
                 }
                 p.tile_max[rowg * p.tiles64 + mt.i] = m_ref;
             }
-            fence_async_shared();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.p_ready(), 1u);
+            if (lane == 0) mbar_arrive(bars.p_ready(static_cast<int>(comp & 1)), 1u);
+            ++comp;
             first_tile = false;
         }
         if ((mt.flags & kLast) && attend) {
             // the chunk's last product: read O and write the row's partial
-            if (!warp_wait(bars.o_done(), o_ph, abort)) break;
-            o_ph ^= 1u;
+            if (!wait_pv(comp - 1)) break;
             tc_fence_after();
             const int64_t s_k = k * p.CH * kTcT;
             const bool write = valid && s_k <= lim;
             const int64_t prow = (u * p.KP + k) * p.R + r;
             for (int cb = 0; cb < Dv; cb += 32) {
                 float ov[32];
-                tmem_ld32(trow + 2 * kTcT + cb, ov);
-                tmem_wait_ld();
+                tmem_ld32(trow + cols.o + cb, ov);
                 if (write) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
@@ -503,8 +529,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_step_kernel(const __grid_con
             mbar_init(bars.s_ready(b), 1u);
             mbar_init(bars.s_free(b), kSoftWarps);
         }
-        mbar_init(bars.p_ready(), kSoftWarps);
-        mbar_init(bars.o_done(), 1u);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bars.p_ready(b), kSoftWarps);
+            mbar_init(bars.o_done(b), 1u);
+        }
         mbar_init(bars.q_ready(), kSoftWarps);
         mbar_init(bars.drained(), 1u);
         *abort = 0;
