@@ -35,9 +35,17 @@ import workloads  # noqa: E402
 METRIC = "effective HBM GB/s (and % of 8 TB/s) + kv steps/s per config, 1 GB300"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-FUSED_SOURCES = ["kv_cache_append_gb300/csrc/kvc_fused.cu",
-                 "kv_cache_append_gb300/csrc/kvc_internal.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_step_traffic.json")
+_CSRC = "kv_cache_append_gb300/csrc/"
+# The first kernel of each path and the sources that define it.
+STEP_KERNEL = {"fused": "fused_step_kernel", "tensor": "tc_step_kernel",
+               "generic": "generic_copy_kernel"}
+KERNEL_SOURCES = {
+    "fused_step_kernel": [_CSRC + f for f in ("kvc_fused.cu", "kvc_internal.cuh",
+                                              "kvc_pipeline.cuh")],
+    "tc_step_kernel": [_CSRC + f for f in ("kvc_fused_tc.cu", "kvc_internal.cuh",
+                                           "kvc_pipeline.cuh", "kvc_tcgen05.cuh")],
+}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
 
 
 # ----------------------------------------------------------------- bytes model
@@ -72,18 +80,20 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def fused_traffic(workload: str):
-    """DRAM bytes per launch of the fused kernel from the committed ncu
-    summary, if it was taken on the current kernel source and this workload."""
+def kernel_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, if it was taken on the kernel's current source; else None."""
+    if kernel not in KERNEL_SOURCES:
+        return None
     try:
         with open(TRAFFIC_FILE) as f:
-            rec = json.load(f)
+            entry = json.load(f)["workloads"][workload]
     except Exception:
         return None
-    if rec.get("kernel_source_sha256") != source_digest(FUSED_SOURCES):
+    if entry.get("kernel") != kernel or \
+            entry.get("kernel_source_sha256") != source_digest(KERNEL_SOURCES[kernel]):
         return None
-    entry = rec.get("workloads", {}).get(workload)
-    return None if entry is None else float(entry["dram_bytes_per_launch"])
+    return float(entry["dram_bytes_per_launch"])
 
 
 # ----------------------------------------------------------------- clocks
@@ -304,7 +314,8 @@ def run_ours(args, spec, world, rank, local):
     peak, peak_src = measured_peak()
     fused_ms = kern_ms[0]
     achieved = nbytes["fused_kernel"] / (fused_ms * 1e-3) / 1e9
-    traffic = fused_traffic(args.workload) if path == "fused" else None
+    kname = STEP_KERNEL[path]
+    traffic = kernel_traffic(args.workload, kname)
 
     # ---- end to end through the public API: pinned host in, pinned host out
     e2e = None
@@ -332,9 +343,9 @@ def run_ours(args, spec, world, rank, local):
         "steps_per_s": round(world * 1e3 / ms_step, 2),
         "bytes_per_step": nbytes["total"],
         "path": path,
-        "kernels": {"fused_step_kernel": {"ms": round(kern_ms[0], 4),
-                                          "algorithmic_GBps": round(achieved, 1)}},
-        "roofline": {"bound": "hbm", "kernel": "fused_step_kernel",
+        "kernels": {kname: {"ms": round(kern_ms[0], 4),
+                            "algorithmic_GBps": round(achieved, 1)}},
+        "roofline": {"bound": "hbm", "kernel": kname,
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": traffic},
