@@ -72,7 +72,7 @@ int check_dims(const kvc_dims* d) {
 struct Plan {
     bool fused = false;
     bool tensor = false;  // the tensor-core fused kernel (kvc_fused_tc.cu)
-    int tc_off_qbuf = 0, tc_off_pbuf = 0, tc_tmem_cols = 0;
+    int tc_off_stg = 0, tc_stg_bytes = 0, tc_tmem_cols = 0;
     size_t off_tile_max = 0;
     int T = 0;
     int64_t TPU = 0, CH = 1, KP = 1, NQ = 0, P = 0;
@@ -112,7 +112,7 @@ void workspace_layout(const kvc_dims& d, int64_t KP, Plan* pl) {
     pl->off_acc = static_cast<size_t>(off);
     off = align_up(off + U * KP * R * d.Dv * 4, 256);
     pl->off_scores = static_cast<size_t>(off);
-    const int64_t fp16_part = align_up(rows * d.M * 2, 256);
+    const int64_t fp16_part = align_up(rows * align_up(d.M, 8) * 2, 256);
     pl->off_tile_max = static_cast<size_t>(off + fp16_part);
     const int64_t fmt1 = fp16_part + rows * ((d.M + 63) / 64) * 4;
     off = align_up(off + std::max<int64_t>(rows * d.M * 4, fmt1), 256);
@@ -260,9 +260,13 @@ bool tc_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
     *pl = Plan();
     tc_tiling(d, pl);
     const int64_t nkb = d.D / 64, nvb = d.Dv / 64;
+    const int64_t R = (d.Hq / d.Hk) * d.Q;
     pl->off_flag = 512;
     pl->off_meta = 1024;
     int64_t off = 2048;
+    pl->tc_off_stg = static_cast<int>(off);  // two staging buffers: R rows of 128 bytes
+    pl->tc_stg_bytes = static_cast<int>(align_up(R * 128, 1024));
+    off += 2 * pl->tc_stg_bytes;
     pl->off_stages = static_cast<int>(off);
     const int64_t stage = (nkb + nvb) * kTcBox;
     pl->stage_bytes = static_cast<int>(stage);
@@ -312,6 +316,23 @@ bool cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t width,
     return fn(map,
               dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
               3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [planes][rows][ld] array of `es`-byte elements (only the first `width` of
+// each row in the map) as boxes of box_x elements x box_y rows, 128-byte swizzle.
+bool rows_map(CUtensorMap* map, void* base, CUtensorMapDataType type, int64_t es, int64_t width,
+              int64_t ld, int64_t rows, int64_t planes, int box_x, int box_y) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(planes)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * es),
+                                   static_cast<cuuint64_t>(rows * ld * es)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_x), static_cast<cuuint32_t>(box_y), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, type, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -422,8 +443,9 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     }
     p.score_fmt = pl.tensor ? 1 : 0;
     p.tiles64 = (d.M + 63) / 64;
-    p.tc_off_qbuf = pl.tc_off_qbuf;
-    p.tc_off_pbuf = pl.tc_off_pbuf;
+    p.pv_ld = align_up(d.M, 8);
+    p.tc_off_stg = pl.tc_off_stg;
+    p.tc_stg_bytes = pl.tc_stg_bytes;
     p.tc_tmem_cols = pl.tc_tmem_cols;
     p.dev_status = dev_status;
     p.vec_attention = (d.M % 8 == 0) && aligned16(out_attention);
@@ -444,7 +466,11 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
             if (!cache_map(&tp.tm_k, key_cache, d.dtype, d.D, d.M, d.B * d.Hk) ||
                 !cache_map(&tp.tm_v, value_cache, d.dtype, d.Dv, d.M, d.B * d.Hk) ||
                 !cache_map(&tp.tm_ok, out_key_cache, d.dtype, d.D, d.M, d.B * d.Hk) ||
-                !cache_map(&tp.tm_ov, out_value_cache, d.dtype, d.Dv, d.M, d.B * d.Hk))
+                !cache_map(&tp.tm_ov, out_value_cache, d.dtype, d.Dv, d.M, d.B * d.Hk) ||
+                !rows_map(&tp.tm_pv, p.pvals, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, d.M, p.pv_ld,
+                          p.R, d.B * d.Hk, 64, static_cast<int>(p.R)) ||
+                !rows_map(&tp.tm_acc, p.part_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d.Dv, d.Dv,
+                          p.R, d.B * d.Hk * p.KP, 32, static_cast<int>(p.R)))
                 return KVC_E_CUDA;
             e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream);
             if (e == cudaSuccess) e = launch_fused_tc(tp, d.dtype, pl.smem, stream);

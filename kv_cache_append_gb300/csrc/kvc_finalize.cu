@@ -111,7 +111,7 @@ __device__ __forceinline__ void write_row(const StepParams& p, T* att, int64_t r
                                           float mx, float inv_l) {
     using S = Storage<T>;
     const float* sc = p.scores + row * p.M;
-    const __half* pv = p.pvals + row * p.M;
+    const __half* pv = p.pvals + row * p.pv_ld;
     const float* tmx = p.tile_max + row * p.tiles64;
     if (p.vec_attention) {
         constexpr int U4 = 4;  // vectors in flight per thread

@@ -11,7 +11,8 @@
 // boxes with the 128-byte swizzle, the layout the tensor cores read:
 //
 //   producer warp  takes chunks, writes each tile's metadata, TMA-loads the
-//                  tile's K and V boxes from the input caches.
+//                  tile's K and V boxes from the input caches; starts an L2
+//                  prefetch of the unit's query rows for each attending chunk.
 //   storer warp    overwrites the rows [length, length+n) of the tile in
 //                  shared memory with new_key/new_value ("Write new_key/value
 //                  at positions length+t only for True append slots t",
@@ -32,7 +33,10 @@
 //                  2^8), writes P = 2^(s - ref) into tensor memory for the
 //                  next product and, in fp16, to the workspace for the
 //                  attention rows; at the end of a chunk it writes the row's
-//                  partial (reference max, sum, O row).
+//                  partial (reference max, sum, O row). P rows and O rows go
+//                  to the workspace through two swizzled shared-memory
+//                  staging buffers and TMA tensor stores (one box of R rows
+//                  per round) instead of one scattered store per row.
 //
 // Tensor memory (512 columns x 128 lanes, fp32 words): S0 [0, 64), S1 [64,
 // 128), O [128, 128 + Dv), Q [128 + Dv, + D/2) as packed 16-bit pairs, P0 and
@@ -71,8 +75,11 @@ struct TcBars {
     __device__ uint32_t o_done(int b) const { return base + 432u + 8u * b; }
     __device__ uint32_t q_ready() const { return base + 448u; }
     __device__ uint32_t drained() const { return base + 456u; }
+    // staging buffer b: rows written (softmax warps) / read by its TMA store
+    __device__ uint32_t stg_full(int b) const { return base + 464u + 8u * b; }
+    __device__ uint32_t stg_free(int b) const { return base + 480u + 8u * b; }
 };
-constexpr int kTmemSlot = 464;  // tensor-memory base address written by tcgen05.alloc
+constexpr int kTmemSlot = 496;  // tensor-memory base address written by tcgen05.alloc
 
 // Tensor-memory column of each region.
 struct TmemCols {
@@ -109,6 +116,9 @@ __device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars
         const int64_t k = idx / U, u = idx - k * U;
         const Unit x = load_unit(p, u);
         const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, p.TPU);
+        if (x.n > 0 && i0 * kTcT < x.L + x.n)  // the softmax warps load these rows at the chunk start
+            bulk_prefetch_l2(static_cast<const unsigned char*>(p.query) + u * p.R * p.D * p.es,
+                             static_cast<uint32_t>(p.R * p.D * p.es));
         for (int64_t i = i0; i < i1; ++i) {
             if (issued >= p.NS && !mbar_wait(bars.empty(ring.s), ring.ph ^ 1u, abort)) {
                 ok = false;
@@ -333,14 +343,17 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
     const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
     const int R = static_cast<int>(p.R), Q = static_cast<int>(p.Q), D = static_cast<int>(p.D);
     const int Dv = static_cast<int>(p.Dv);
+    const float qs = p.qscale;
     const TmemCols cols(D, Dv);
     const uint32_t trow = tmem + (static_cast<uint32_t>(w * 32) << 16);  // this warp's lanes
     const unsigned char* query = static_cast<const unsigned char*>(p.query);
+    unsigned char* stg = smem + p.tc_off_stg;
+    const uint32_t stg_addr = smem_addr(stg);
     Ring ring;
-    int sbuf = 0;
-    int s_uses[2] = {0, 0};
+    int sbuf = 0, su0 = 0, su1 = 0;    // S buffer in use; completions consumed per S buffer
     int64_t comp = 0;                  // attending tiles done so far = products issued for them
-    int64_t pv_seen[2] = {0, 0};       // completions consumed on o_done[b]
+    int64_t pv0 = 0, pv1 = 0;          // completions consumed on o_done[0], o_done[1]
+    int64_t use = 0;                   // staging rounds so far (round u uses buffer u % 2)
     bool attend = false, first_tile = false;
     int64_t L = 0, n = 0, N = 0, u = 0, k = 0, rowg = 0;
     int64_t q_unit = -1;  // unit whose query rows tensor memory holds
@@ -348,16 +361,51 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
     bool valid = false;
     float m_ref = -INFINITY, l = 0.f;
 
-    // Wait until product c (which read P[c % 2]) has completed, consuming the
-    // completions of that barrier strictly in order.
+    // Wait until product c (which read P[c % 2]) has finished, consuming the
+    // completions of that buffer's barrier strictly in order.
     auto wait_pv = [&](int64_t c) -> bool {
-        const int b = static_cast<int>(c & 1);
         const int64_t kth = c >> 1;
-        while (pv_seen[b] <= kth) {
-            if (!warp_wait(bars.o_done(b), static_cast<uint32_t>(pv_seen[b] & 1), abort)) return false;
-            ++pv_seen[b];
+        if (c & 1) {
+            for (; pv1 <= kth; ++pv1)
+                if (!warp_wait(bars.o_done(1), static_cast<uint32_t>(pv1 & 1), abort)) return false;
+        } else {
+            for (; pv0 <= kth; ++pv0)
+                if (!warp_wait(bars.o_done(0), static_cast<uint32_t>(pv0 & 1), abort)) return false;
         }
         return true;
+    };
+    // One staging round: every row of the unit writes its 128 bytes into the
+    // buffer (128-byte swizzle, the TMA layout), then thread 0 stores the box.
+    // The buffer is free once the store two rounds back has read it.
+    auto stage = [&](const uint32_t* words, const CUtensorMap* map, int x, int z) -> bool {
+        const int b = static_cast<int>(use & 1);
+        if (use >= 2 &&
+            !warp_wait(bars.stg_free(b), static_cast<uint32_t>(((use >> 1) - 1) & 1), abort))
+            return false;
+        if (r < R) {
+            unsigned char* row = stg + b * p.tc_stg_bytes + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
+                    make_uint4(words[4 * c], words[4 * c + 1], words[4 * c + 2], words[4 * c + 3]);
+        }
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.stg_full(b), 1u);
+        bool ok = true;
+        if (r == 0) {
+            ok = mbar_wait(bars.stg_full(b), static_cast<uint32_t>((use >> 1) & 1), abort);
+            if (ok) {
+                tma_store_3d(map, x, 0, z, stg_addr + static_cast<uint32_t>(b * p.tc_stg_bytes));
+                bulk_commit();
+                if (use >= 1) {  // the previous round's store has read its buffer
+                    bulk_wait_read(1);
+                    mbar_arrive(bars.stg_free(b ^ 1), 1u);
+                }
+            }
+        }
+        ++use;
+        return w != 0 || __shfl_sync(0xffffffffu, ok, 0);
     };
 
     bool ok = true;
@@ -388,16 +436,18 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
                 valid = r < R && t < n;
                 lim = valid ? static_cast<int>(L + t) : -1;
                 rowg = ((b * p.Hq + kv * p.G + r / Q) * p.Q + t);
-                if (u != q_unit) {  // this row's query into tensor memory, 64 elements at a time
+                if (u != q_unit) {  // this row's query into tensor memory, 128 elements at a time
                     const uint4* src = reinterpret_cast<const uint4*>(query + rowg * D * p.es);
-                    for (int g = 0; g < D / 64; ++g) {
-                        uint32_t wq[32];
+                    for (int g0 = 0; g0 < D / 64; g0 += 2) {
+                        const int ng = min(2, D / 64 - g0);
+                        uint4 v[16];
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint4 v = r < R ? src[8 * g + c] : make_uint4(0u, 0u, 0u, 0u);
-                            wq[4 * c] = v.x; wq[4 * c + 1] = v.y; wq[4 * c + 2] = v.z; wq[4 * c + 3] = v.w;
-                        }
-                        tmem_st32u(trow + cols.q + 32 * g, wq);
+                        for (int c = 0; c < 16; ++c)
+                            v[c] = (r < R && c < 8 * ng) ? src[8 * g0 + c] : make_uint4(0u, 0u, 0u, 0u);
+                        tmem_st32u(trow + cols.q + 32 * g0, reinterpret_cast<const uint32_t*>(v));
+                        if (ng > 1)
+                            tmem_st32u(trow + cols.q + 32 * (g0 + 1),
+                                       reinterpret_cast<const uint32_t*>(v + 8));
                     }
                     q_unit = u;
                 }
@@ -411,8 +461,9 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
         }
         const bool is_comp = attend && static_cast<int64_t>(mt.i) * kTcT < N;
         if (is_comp) {
-            if (!warp_wait(bars.s_ready(sbuf), static_cast<uint32_t>(s_uses[sbuf] & 1), abort)) break;
-            ++s_uses[sbuf];
+            if (!warp_wait(bars.s_ready(sbuf), static_cast<uint32_t>((sbuf ? su1 : su0) & 1), abort))
+                break;
+            if (sbuf) ++su1; else ++su0;
             tc_fence_after();
             float sv[kTcT];
             tmem_ld32(trow + sbuf * kTcT, sv);
@@ -421,16 +472,21 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.s_free(sbuf), 1u);
             sbuf ^= 1;
+            // causal limit: slots j <= lim count; the scale is applied through qs > 0
             const int j0 = mt.i * kTcT;
-            float tmax = -INFINITY;
+            const bool none = j0 > lim;
+            if (!__all_sync(0xffffffffu, j0 + kTcT - 1 <= lim || none)) {
 #pragma unroll
-            for (int c = 0; c < kTcT; ++c) {
-                sv[c] = (j0 + c <= lim) ? sv[c] * p.qscale : -INFINITY;
-                tmax = fmaxf(tmax, sv[c]);
+                for (int c = 0; c < kTcT; ++c)
+                    if (j0 + c > lim) sv[c] = -INFINITY;
             }
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < kTcT; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+            const float tmax = none ? -INFINITY : fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * qs;
             // P[comp % 2] is free once the product two tiles back has finished
             if (comp >= 2 && !wait_pv(comp - 2)) break;
-            const bool raise = tmax > m_ref + kRescale || (m_ref == -INFINITY && tmax != -INFINITY);
+            const bool raise = tmax > m_ref + kRescale;
             const float corr = (raise && m_ref != -INFINITY) ? fast_exp2(m_ref - tmax) : 1.f;
             if (__any_sync(0xffffffffu, raise && m_ref != -INFINITY && !first_tile)) {
                 // O must be quiescent: the previous product has finished, this
@@ -449,67 +505,50 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
                 l *= corr;
                 m_ref = tmax;
             }
-            // P row: 2^(s - ref), as the operand type for O += P V and as fp16 for the rows
-            float lsum = 0.f;
-            uint32_t pk[kTcT / 2];   // operand type, two per word
-            uint32_t phb[kTcT / 2];  // fp16, two per word
+            // P row: 2^(s qs - ref); rows with no allowed slot in the tile give 0
+            const float negm = (none || m_ref == -INFINITY) ? -INFINITY : -m_ref;
+            float ls0 = 0.f, ls1 = 0.f;
+            uint32_t pk[kTcT / 2];  // operand type, two per word
+            uint32_t ph[kTcT / 2];  // fp16, two per word (the attention rows' inputs)
 #pragma unroll
             for (int c = 0; c < kTcT; c += 2) {
-                const float e0 = (sv[c] == -INFINITY) ? 0.f : fast_exp2(sv[c] - m_ref);
-                const float e1 = (sv[c + 1] == -INFINITY) ? 0.f : fast_exp2(sv[c + 1] - m_ref);
-                lsum += e0 + e1;
-                const T a = Storage<T>::from_float(e0), bb = Storage<T>::from_float(e1);
-                pk[c / 2] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&a)) |
-                            (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&bb)) << 16);
-                const __half h0 = __float2half_rn(e0), h1 = __float2half_rn(e1);
-                phb[c / 2] = static_cast<uint32_t>(__half_as_ushort(h0)) |
-                             (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+                const float e0 = fast_exp2(fmaf(sv[c], qs, negm));
+                const float e1 = fast_exp2(fmaf(sv[c + 1], qs, negm));
+                if (c & 2) ls1 += e0 + e1; else ls0 += e0 + e1;
+                pk[c / 2] = pack2<T>(e0, e1);
+                if constexpr (!std::is_same<T, __half>::value) ph[c / 2] = pack2<__half>(e0, e1);
             }
-            l += lsum;
+            l += ls0 + ls1;
             tmem_st32u(trow + cols.p0 + 32 * static_cast<uint32_t>(comp & 1), pk);
-            if (valid && j0 <= lim) {
-                __half* dst = p.pvals + rowg * p.M + j0;
-                if (j0 + kTcT <= p.M && (p.M & 7) == 0) {
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        *reinterpret_cast<uint4*>(dst + 8 * ch) =
-                            make_uint4(phb[4 * ch], phb[4 * ch + 1], phb[4 * ch + 2], phb[4 * ch + 3]);
-                } else {
-                    for (int c = 0; c < kTcT && j0 + c < p.M; ++c)
-                        dst[c] = __ushort_as_half(static_cast<unsigned short>(phb[c / 2] >> ((c & 1) * 16)));
-                }
-                p.tile_max[rowg * p.tiles64 + mt.i] = m_ref;
-            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.p_ready(static_cast<int>(comp & 1)), 1u);
+            if (valid && !none) p.tile_max[rowg * p.tiles64 + mt.i] = m_ref;
+            if (!stage(std::is_same<T, __half>::value ? pk : ph, &tp.tm_pv, j0, static_cast<int>(u)))
+                break;
             ++comp;
             first_tile = false;
         }
         if ((mt.flags & kLast) && attend) {
-            // the chunk's last product: read O and write the row's partial
+            // the chunk's last product: read O and store the row's partial
             if (!wait_pv(comp - 1)) break;
             tc_fence_after();
             const int64_t s_k = k * p.CH * kTcT;
-            const bool write = valid && s_k <= lim;
-            const int64_t prow = (u * p.KP + k) * p.R + r;
-            for (int cb = 0; cb < Dv; cb += 32) {
+            const int z = static_cast<int>(u * p.KP + k);
+            for (int cb = 0; cb < Dv && ok; cb += 32) {
                 float ov[32];
                 tmem_ld32(trow + cols.o + cb, ov);
-                if (write) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(p.part_acc + prow * Dv + cb + e) =
-                            make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
-                }
+                ok = stage(reinterpret_cast<const uint32_t*>(ov), &tp.tm_acc, cb, z);
             }
-            if (write) {
+            if (valid && s_k <= lim) {
+                const int64_t prow = (u * p.KP + k) * p.R + r;
                 p.part_ml[2 * prow] = m_ref;
                 p.part_ml[2 * prow + 1] = l;
             }
             tc_fence_before();
         }
     }
+    if (r == 0) bulk_wait_all();  // the staged stores have finished
 }
 
 template <typename T>
@@ -532,6 +571,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_step_kernel(const __grid_con
         for (int b = 0; b < 2; ++b) {
             mbar_init(bars.p_ready(b), kSoftWarps);
             mbar_init(bars.o_done(b), 1u);
+            mbar_init(bars.stg_full(b), kSoftWarps);
+            mbar_init(bars.stg_free(b), 1u);
         }
         mbar_init(bars.q_ready(), kSoftWarps);
         mbar_init(bars.drained(), 1u);

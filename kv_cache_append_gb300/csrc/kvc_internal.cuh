@@ -460,15 +460,17 @@ struct StepParams {
     unsigned int* counter;  // next chunk to hand out (zeroed before each launch)
     // How the attention rows' inputs are kept between the kernels:
     //   score_fmt 0: scores = scale*log2e*dot, fp32, [B][Hq][Q][M];
-    //   score_fmt 1: pvals = 2^(score - tile_max) as fp16 [B][Hq][Q][M], with
-    //                tile_max the reference maximum per (row, 64-slot tile),
-    //                fp32 [B][Hq][Q][ceil(M/64)].
+    //   score_fmt 1: pvals = 2^(score - tile_max) as fp16 [B][Hq][Q][pv_ld]
+    //                (pv_ld = M rounded up to 8), with tile_max the reference
+    //                maximum per (row, 64-slot tile), fp32 [B][Hq][Q][ceil(M/64)].
     int score_fmt;
     __half* pvals;
+    int64_t pv_ld;
     float* tile_max;
     int64_t tiles64;  // ceil(M / 64)
-    // tensor-core kernel layout
-    int tc_off_qbuf, tc_off_pbuf, tc_tmem_cols;
+    // tensor-core kernel layout: two staging buffers of tc_stg_bytes each at
+    // tc_off_stg (rows of 128 bytes for TMA stores), tensor-memory columns
+    int tc_off_stg, tc_stg_bytes, tc_tmem_cols;
     int32_t* dev_status;
     int vec_attention;  // 1: attention rows may be written 8 elements at a time
 };

@@ -16,12 +16,15 @@ cudaError_t launch_fused(const StepParams& p, int dtype, int dvc, int nchl, size
 
 // Kernel parameters of the tensor-core fused kernel: the four caches as TMA
 // tensor maps ([U][M][width], boxes of 64 elements x 64 slots, 128-byte
-// swizzle) and the common parameters.
+// swizzle), the two workspace arrays it stores by TMA, and the common
+// parameters.
 struct TcParams {
-    CUtensorMap tm_k;   // key_cache
-    CUtensorMap tm_v;   // value_cache
-    CUtensorMap tm_ok;  // out_key_cache
-    CUtensorMap tm_ov;  // out_value_cache
+    CUtensorMap tm_k;    // key_cache
+    CUtensorMap tm_v;    // value_cache
+    CUtensorMap tm_ok;   // out_key_cache
+    CUtensorMap tm_ov;   // out_value_cache
+    CUtensorMap tm_pv;   // pvals as [U][R][pv_ld] fp16, boxes of 64 slots x R rows
+    CUtensorMap tm_acc;  // part_acc as [U * KP][R][Dv] fp32, boxes of 32 values x R rows
     StepParams p;
 };
 
