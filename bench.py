@@ -39,6 +39,11 @@ _CSRC = "kv_cache_append_gb300/csrc/"
 # The first kernel of each path and the sources that define it.
 STEP_KERNEL = {"fused": "fused_step_kernel", "tensor": "tc_step_kernel",
                "generic": "generic_copy_kernel"}
+# Every kernel of a step with query rows, in launch order.
+PATH_KERNELS = {"fused": ["fused_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
+                "tensor": ["tc_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
+                "generic": ["generic_copy_kernel", "generic_attend_kernel",
+                            "finalize_merge_kernel", "finalize_rows_kernel"]}
 KERNEL_SOURCES = {
     "fused_step_kernel": [_CSRC + f for f in ("kvc_fused.cu", "kvc_internal.cuh",
                                               "kvc_pipeline.cuh")],
@@ -354,9 +359,12 @@ def run_ours(args, spec, world, rank, local):
         "gpu_launches": nkern * args.steps,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
+    names = PATH_KERNELS[path]
+    for k in range(1, nkern):
+        line["kernels"][names[k]] = {"ms": round(kern_ms[k], 4)}
     if nkern > 1:
-        fin_ms = kern_ms[-1]
-        line["kernels"]["finalize_kernel"] = {
+        fin_ms = kern_ms[-1] + kern_ms[-2]
+        line["kernels"]["finalize (merge + rows)"] = {
             "ms": round(fin_ms, 4),
             "algorithmic_GBps": round(nbytes["finalize_kernel"] / (fin_ms * 1e-3) / 1e9, 1)}
     print(json.dumps(line), flush=True)

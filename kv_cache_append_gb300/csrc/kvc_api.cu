@@ -49,6 +49,8 @@ int elem_size(int32_t dtype) { return dtype == KVC_F32 ? 4 : 2; }
 int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
 // Sizes valid and every tensor's byte count representable.
+constexpr int64_t kFinalizeSeg = 8192;  // attention slots per finalize block (multiple of 8)
+
 int check_dims(const kvc_dims* d) {
     if (!d) return KVC_E_NULL;
     if (d->dtype != KVC_F32 && d->dtype != KVC_BF16 && d->dtype != KVC_F16) return KVC_E_DTYPE;
@@ -65,6 +67,8 @@ int check_dims(const kvc_dims* d) {
     if (d->M >= (int64_t(1) << 31) || d->Q >= (int64_t(1) << 20) || d->D >= (int64_t(1) << 20) ||
         d->Dv >= (int64_t(1) << 20) || (d->Hq / d->Hk) * d->Q >= (int64_t(1) << 20))
         return KVC_E_SHAPE;
+    // one finalize block per (query row, segment of kFinalizeSeg slots)
+    if (B * Hq * Q * std::ceil(M / kFinalizeSeg) >= 2147483647.0) return KVC_E_SHAPE;
     return KVC_OK;
 }
 
@@ -82,7 +86,7 @@ struct Plan {
     bool q_staged = false;
     int q_stage_bytes = 0, off_stage_q = 0;
     size_t smem = 0;
-    size_t off_counter = 0, off_ml = 0, off_acc = 0, off_scores = 0, ws_bytes = 0;
+    size_t off_counter = 0, off_ml = 0, off_acc = 0, off_rowstat = 0, off_scores = 0, ws_bytes = 0;
 };
 
 #ifndef KVC_CHUNKS_PER_CTA
@@ -111,6 +115,8 @@ void workspace_layout(const kvc_dims& d, int64_t KP, Plan* pl) {
     off = align_up(off + U * KP * R * 2 * 4, 256);
     pl->off_acc = static_cast<size_t>(off);
     off = align_up(off + U * KP * R * d.Dv * 4, 256);
+    pl->off_rowstat = static_cast<size_t>(off);
+    off = align_up(off + rows * static_cast<int64_t>(sizeof(RowStat)), 256);
     pl->off_scores = static_cast<size_t>(off);
     const int64_t fp16_part = align_up(rows * align_up(d.M, 8) * 2, 256);
     pl->off_tile_max = static_cast<size_t>(off + fp16_part);
@@ -440,6 +446,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
         p.counter = reinterpret_cast<unsigned int*>(ws + pl.off_counter);
         p.pvals = reinterpret_cast<__half*>(ws + pl.off_scores);
         p.tile_max = reinterpret_cast<float*>(ws + pl.off_tile_max);
+        p.rowstat = reinterpret_cast<RowStat*>(ws + pl.off_rowstat);
     }
     p.score_fmt = pl.tensor ? 1 : 0;
     p.tiles64 = (d.M + 63) / 64;
@@ -449,6 +456,10 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     p.tc_tmem_cols = pl.tc_tmem_cols;
     p.dev_status = dev_status;
     p.vec_attention = (d.M % 8 == 0) && aligned16(out_attention);
+    // finalize blocks: rows longer than kFinalizeSeg slots are split so that
+    // long-context steps with few query rows still fill the GPU
+    p.fin_seg = d.M <= kFinalizeSeg ? align_up(d.M, 8) : kFinalizeSeg;
+    p.fin_nseg = (d.M + p.fin_seg - 1) / p.fin_seg;
 
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     int recorded = 0;
@@ -489,7 +500,9 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
             }
         }
         if (e == cudaSuccess && hasq) {
-            e = launch_finalize(p, d.dtype, stream);
+            e = launch_finalize_merge(p, d.dtype, stream);
+            if (e == cudaSuccess) e = record();
+            if (e == cudaSuccess) e = launch_finalize_rows(p, d.dtype, stream);
             if (e == cudaSuccess) e = record();
         }
         while (e == cudaSuccess && events && recorded < n_events) e = record();
@@ -562,13 +575,14 @@ int kvc_plan_info(const kvc_dims* dims, const void* key_cache, const void* value
                               aligned16(out_key_cache) && aligned16(out_value_cache) &&
                               (!hasq || (aligned16(new_key) && aligned16(new_value)));
     Plan pl;
+    // the step kernel(s), then (with query rows) the merge and the row writer
     if (ptrs_aligned && tc_plan(*dims, dev.sms, dev.smem_optin, &pl)) {
         if (path_name) *path_name = "tensor";
-        return 2;
+        return 3;
     }
     const bool fused = ptrs_aligned && fused_plan(*dims, dev.sms, dev.smem_optin, true, &pl);
     if (path_name) *path_name = fused ? "fused" : "generic";
-    return fused ? (hasq ? 2 : 1) : (hasq ? 3 : 1);
+    return fused ? (hasq ? 3 : 1) : (hasq ? 4 : 1);
 }
 
 const char* kvc_status_string(int status) {

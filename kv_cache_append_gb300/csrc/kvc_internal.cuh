@@ -422,6 +422,15 @@ __device__ __forceinline__ RowAppend row_append(const int64_t* lengths, const ui
 // allowed slot writes one partial per query row into slot (u, k).
 
 // Everything the kernels need, passed by value.
+// One query row's softmax normaliser after the merge of its chunk partials:
+// attention_j = 2^(s_j - mx) * inv_l for slots j <= lim (lim = -1: none).
+struct RowStat {
+    float mx;
+    float inv_l;
+    int32_t lim;
+    int32_t pad;
+};
+
 struct StepParams {
     // sizes
     int64_t B, Hq, Hk, Q, D, Dv, M, G, R;  // G = Hq/Hk, R = G*Q rows per unit
@@ -473,6 +482,9 @@ struct StepParams {
     int tc_off_stg, tc_stg_bytes, tc_tmem_cols;
     int32_t* dev_status;
     int vec_attention;  // 1: attention rows may be written 8 elements at a time
+    int64_t fin_seg;    // attention slots per row-writer block (a multiple of 8)
+    int64_t fin_nseg;   // row-writer blocks per query row: ceil(M / fin_seg)
+    RowStat* rowstat;   // [B][Hq][Q]: the merged maximum, 1 / sum and last allowed slot
 };
 
 }  // namespace kvc

@@ -31,8 +31,10 @@ struct TcParams {
 // Fused copy + scatter + attention partials on the tensor cores (kvc_fused_tc.cu).
 cudaError_t launch_fused_tc(const TcParams& tp, int dtype, size_t smem, cudaStream_t stream);
 
-// Merge of the partials, context rows and attention rows (kvc_finalize.cu).
-cudaError_t launch_finalize(const StepParams& p, int dtype, cudaStream_t stream);
+// Merge of the partials: context rows and one RowStat per query row (kvc_finalize.cu).
+cudaError_t launch_finalize_merge(const StepParams& p, int dtype, cudaStream_t stream);
+// Attention rows from the kept scores (or P values) and the RowStats (kvc_finalize.cu).
+cudaError_t launch_finalize_rows(const StepParams& p, int dtype, cudaStream_t stream);
 
 // Generic path for shapes or alignments the fused kernel does not take
 // (kvc_generic.cu): copy + scatter, then attention partials.

@@ -120,6 +120,9 @@ SMALL = {
                                 counts=("uniform", 0, 2)),
     "bf16_D8_M1": Spec(B=3, Hq=2, Hk=1, Q=1, D=8, Dv=8, M=1, dtype="bf16",
                        lengths=("fixed", 0)),
+    # rows longer than one finalize segment (8192 slots), M not a multiple of 8
+    "fp32_three_segments": Spec(B=1, Hq=2, Hk=1, Q=2, D=16, Dv=16, M=2 * 8192 + 13,
+                                dtype="f32", lengths=("uniform", 9000, 16395)),
 }
 
 
@@ -201,7 +204,7 @@ def test_generic_path_shapes(D, Dv, dtype):
     n, path = kvc.plan_info(kvc.dims_of(xg.query, xg.key_cache, xg.value_cache), xg.key_cache,
                             xg.value_cache, xg.new_key, xg.new_value, xg.key_cache,
                             xg.value_cache)
-    assert path == "generic" and n == 3
+    assert path == "generic" and n == 4  # copy, attend, merge, row writer
     out, status = run_gpu(xg)
     compare_full(x, out, status)
 
@@ -279,6 +282,11 @@ TC = {
                                lengths=("uniform", 0, 496), counts=("uniform", 1, 16)),
     "r96_bf16_hot": Spec(B=2, Hq=12, Hk=1, Q=8, D=128, Dv=128, M=1024, dtype="bf16",
                          hot_frac=0.2, hot_scale=50.0),
+    # several finalize segments per row; padded fp16 P rows (M % 8 != 0)
+    "r64_fp16_segments": Spec(B=1, Hq=8, Hk=1, Q=8, D=64, Dv=64, M=20000, dtype="f16",
+                              lengths=("uniform", 17000, 19990)),
+    "r64_bf16_segments_M9005": Spec(B=1, Hq=8, Hk=1, Q=8, D=64, Dv=64, M=9005, dtype="bf16",
+                                    lengths=("uniform", 8000, 8995)),
 }
 
 
