@@ -93,7 +93,10 @@ struct Plan {
 #define KVC_CHUNKS_PER_CTA 32
 #endif
 constexpr int64_t kChunksPerCta = KVC_CHUNKS_PER_CTA;  // aim: this many chunks per CTA
-constexpr int64_t kPartialRatio = 16;     // a chunk moves >= 16x its partials' bytes
+#ifndef KVC_PARTIAL_RATIO
+#define KVC_PARTIAL_RATIO 16
+#endif
+constexpr int64_t kPartialRatio = KVC_PARTIAL_RATIO;  // a chunk moves >= this x its partials' bytes
 constexpr int64_t kMaxStagedQuery = 16384;
 
 // Whether the fused kernel's row shapes apply (16-byte rows, widths it holds).
