@@ -415,6 +415,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size B (profiling captures)")
+    ap.add_argument("--q", type=int, default=None,
+                    help="override the tokens per step Q (the 32- and 24-token chunked appends)")
+    ap.add_argument("--dtype", choices=["f32", "bf16", "f16"], default=None,
+                    help="override the workload's dtype (the fp32 chunked append)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -422,6 +426,10 @@ def main():
     spec = workloads.SPECS[args.workload]
     if args.batch:
         spec = spec.replace(B=args.batch)
+    if args.q is not None:
+        spec = spec.replace(Q=args.q)
+    if args.dtype:
+        spec = spec.replace(dtype=args.dtype)
     if args.impl == "reference":
         run_reference(args, spec, world, rank)
     else:

@@ -77,6 +77,7 @@ struct Plan {
     bool fused = false;
     bool tensor = false;  // the tensor-core fused kernel (kvc_fused_tc.cu)
     int tc_off_stg = 0, tc_stg_bytes = 0, tc_tmem_cols = 0;
+    int64_t tc_nrg = 1;
     size_t off_tile_max = 0;
     int T = 0;
     int64_t TPU = 0, CH = 1, KP = 1, NQ = 0, P = 0;
@@ -249,13 +250,14 @@ constexpr int kTcT = 64;        // slots per tile of the tensor-core kernel
 constexpr int kTcBox = 64 * 128;  // one 64-element-wide box of a tile
 
 // Shapes the tensor-core kernel takes: 16-bit caches, key and value widths
-// multiples of 64 (at most 256), KVC_TC_MIN_ROWS..128 query rows per unit.
+// multiples of 64 (at most 256), KVC_TC_MIN_ROWS..256 query rows per unit
+// (more than 128: two row groups).
 // Tensor memory holds S twice (2 x 64 columns), O (Dv), Q (D/2) and P twice
 // (2 x 32): Dv + D/2 <= 320.
 bool tc_shapes(const kvc_dims& d) {
     const int64_t R = (d.Hq / d.Hk) * d.Q;
     return d.dtype != KVC_F32 && d.D % 64 == 0 && d.D <= 256 && d.Dv % 64 == 0 && d.Dv <= 256 &&
-           d.Dv + d.D / 2 <= 320 && d.Q >= 1 && R >= KVC_TC_MIN_ROWS && R <= 128 &&
+           d.Dv + d.D / 2 <= 320 && d.Q >= 1 && R >= KVC_TC_MIN_ROWS && R <= 256 &&
            d.B * d.Hk < (int64_t(1) << 31);
 }
 
@@ -273,8 +275,9 @@ bool tc_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
     pl->off_flag = 512;
     pl->off_meta = 1024;
     int64_t off = 2048;
-    pl->tc_off_stg = static_cast<int>(off);  // two staging buffers: R rows of 128 bytes
-    pl->tc_stg_bytes = static_cast<int>(align_up(R * 128, 1024));
+    pl->tc_nrg = (R + 127) / 128;
+    pl->tc_off_stg = static_cast<int>(off);  // two staging buffers: up to 128 rows of 128 bytes
+    pl->tc_stg_bytes = static_cast<int>(align_up(std::min<int64_t>(R, 128) * 128, 1024));
     off += 2 * pl->tc_stg_bytes;
     pl->off_stages = static_cast<int>(off);
     const int64_t stage = (nkb + nvb) * kTcBox;
@@ -285,6 +288,7 @@ bool tc_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
     pl->smem = static_cast<size_t>(off + int64_t(pl->NS) * stage);
     pl->tc_tmem_cols = 512;  // S0, S1, O, Q, P0, P1
     chunking(d, sms, pl);
+    pl->NQ *= pl->tc_nrg;  // every chunk once per row group
     pl->P = std::min<int64_t>(sms, pl->NQ);
     pl->tensor = true;
     workspace_layout(d, pl->KP, pl);
@@ -455,6 +459,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     p.tiles64 = (d.M + 63) / 64;
     p.pv_ld = align_up(d.M, 8);
     p.tc_off_stg = pl.tc_off_stg;
+    p.tc_nrg = pl.tc_nrg;
     p.tc_stg_bytes = pl.tc_stg_bytes;
     p.tc_tmem_cols = pl.tc_tmem_cols;
     p.dev_status = dev_status;
@@ -482,9 +487,9 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
                 !cache_map(&tp.tm_ok, out_key_cache, d.dtype, d.D, d.M, d.B * d.Hk) ||
                 !cache_map(&tp.tm_ov, out_value_cache, d.dtype, d.Dv, d.M, d.B * d.Hk) ||
                 !rows_map(&tp.tm_pv, p.pvals, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, d.M, p.pv_ld,
-                          p.R, d.B * d.Hk, 64, static_cast<int>(p.R)) ||
+                          p.R, d.B * d.Hk, 64, static_cast<int>(std::min<int64_t>(p.R, 128))) ||
                 !rows_map(&tp.tm_acc, p.part_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d.Dv, d.Dv,
-                          p.R, d.B * d.Hk * p.KP, 32, static_cast<int>(p.R)))
+                          p.R, d.B * d.Hk * p.KP, 32, static_cast<int>(std::min<int64_t>(p.R, 128))))
                 return KVC_E_CUDA;
             e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream);
             if (e == cudaSuccess) e = launch_fused_tc(tp, d.dtype, pl.smem, stream);

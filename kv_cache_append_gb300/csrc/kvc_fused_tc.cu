@@ -5,7 +5,9 @@
 // the tiles that hold allowed slots attended), with the two products of the
 // attention on the 5th-generation tensor cores (tcgen05, accumulators in
 // tensor memory). For 16-bit caches whose key and value widths are multiples
-// of 64 and units of at most 128 query rows (G = Hq/Hk heads x Q new tokens).
+// of 64 and units of at most 256 query rows (G = Hq/Hk heads x Q new tokens).
+// A unit with more than 128 rows is worked as two row groups of up to 128
+// rows (one product row each); both read every tile, the first also stores it.
 //
 // A tile is 64 cache slots. Tiles move by TMA tensor copies in 64-element-wide
 // boxes with the 128-byte swizzle, the layout the tensor cores read:
@@ -60,6 +62,8 @@ constexpr int kSoftWarps = 4;
 constexpr int kMmaWarp = 4, kProdWarp = 5, kStoreWarp = 6;
 constexpr int kTcThreads = 7 * 32;
 constexpr float kRescale = 8.f;           // raise the reference max when exceeded by 2^8
+constexpr int kRgShift = 8;               // TileMeta flags bits 8..: the tile's row group
+constexpr int kRgRows = 128;              // query rows per row group (one product row each)
 
 struct TcBars {
     uint32_t base;
@@ -112,13 +116,17 @@ __device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars
     while (ok) {
         const int64_t q = atomicAdd(p.counter, 1u);
         if (q >= p.NQ) break;
-        const int64_t idx = chunk_of(q, p.NQ);
-        const int64_t k = idx / U, u = idx - k * U;
+        const int64_t idx = chunk_of(q, p.NQ);  // chunk k of (unit u, row group rg)
+        const int64_t UG = U * p.tc_nrg;
+        const int64_t k = idx / UG, ug = idx - k * UG;
+        const int64_t u = ug / p.tc_nrg, rg = ug - u * p.tc_nrg;
         const Unit x = load_unit(p, u);
         const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, p.TPU);
-        if (x.n > 0 && i0 * kTcT < x.L + x.n)  // the softmax warps load these rows at the chunk start
-            bulk_prefetch_l2(static_cast<const unsigned char*>(p.query) + u * p.R * p.D * p.es,
-                             static_cast<uint32_t>(p.R * p.D * p.es));
+        if (x.n > 0 && i0 * kTcT < x.L + x.n) {  // the softmax warps load these rows at the chunk start
+            const int64_t r0 = rg * kRgRows, nr = min(static_cast<int64_t>(kRgRows), p.R - r0);
+            bulk_prefetch_l2(static_cast<const unsigned char*>(p.query) + (u * p.R + r0) * p.D * p.es,
+                             static_cast<uint32_t>(nr * p.D * p.es));
+        }
         for (int64_t i = i0; i < i1; ++i) {
             if (issued >= p.NS && !mbar_wait(bars.empty(ring.s), ring.ph ^ 1u, abort)) {
                 ok = false;
@@ -130,7 +138,8 @@ __device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars
             mt.n = static_cast<int32_t>(x.n);
             mt.i = static_cast<int32_t>(i);
             mt.k = static_cast<int32_t>(k);
-            mt.flags = (i == i0 ? kFirst : 0) | (i == i1 - 1 ? kLast : 0);
+            mt.flags = (i == i0 ? kFirst : 0) | (i == i1 - 1 ? kLast : 0) |
+                       static_cast<int32_t>(rg << kRgShift);
             const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
             const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBox);
             mbar_arrive_expect_tx(bars.full(ring.s), tile_bytes);  // publishes the metadata too
@@ -201,12 +210,14 @@ __device__ void tc_storer(const TcParams& tp, unsigned char* smem, TcBars bars,
             if (lane == 0) mbar_arrive(bars.patched(ring.s), 1u);
         }
         if (lane == 0) {
-            const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
-            const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBox);
-            const int y = static_cast<int>(j0), z = static_cast<int>(mt.u);
-            for (int b = 0; b < nkb; ++b) tma_store_3d(&tp.tm_ok, 64 * b, y, z, sK + b * kBox);
-            for (int b = 0; b < nvb; ++b) tma_store_3d(&tp.tm_ov, 64 * b, y, z, sV + b * kBox);
-            bulk_commit();
+            if ((mt.flags >> kRgShift) == 0) {  // other row groups read the same tile
+                const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
+                const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBox);
+                const int y = static_cast<int>(j0), z = static_cast<int>(mt.u);
+                for (int b = 0; b < nkb; ++b) tma_store_3d(&tp.tm_ok, 64 * b, y, z, sK + b * kBox);
+                for (int b = 0; b < nvb; ++b) tma_store_3d(&tp.tm_ov, 64 * b, y, z, sV + b * kBox);
+            }
+            bulk_commit();  // (an empty group for a tile it does not store)
             ++stored;
             if (stored - released > p.LAG) {
                 bulk_wait_read(p.LAG);
@@ -356,7 +367,8 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
     int64_t use = 0;                   // staging rounds so far (round u uses buffer u % 2)
     bool attend = false, first_tile = false;
     int64_t L = 0, n = 0, N = 0, u = 0, k = 0, rowg = 0;
-    int64_t q_unit = -1;  // unit whose query rows tensor memory holds
+    int64_t q_unit = -1;  // unit * row groups + row group whose query rows tensor memory holds
+    int rbase = 0, Rg = 0;  // first row and rows of the current row group
     int lim = -1;
     bool valid = false;
     float m_ref = -INFINITY, l = 0.f;
@@ -382,7 +394,7 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
         if (use >= 2 &&
             !warp_wait(bars.stg_free(b), static_cast<uint32_t>(((use >> 1) - 1) & 1), abort))
             return false;
-        if (r < R) {
+        if (r < Rg) {
             unsigned char* row = stg + b * p.tc_stg_bytes + r * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
@@ -396,7 +408,7 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
         if (r == 0) {
             ok = mbar_wait(bars.stg_full(b), static_cast<uint32_t>((use >> 1) & 1), abort);
             if (ok) {
-                tma_store_3d(map, x, 0, z, stg_addr + static_cast<uint32_t>(b * p.tc_stg_bytes));
+                tma_store_3d(map, x, rbase, z, stg_addr + static_cast<uint32_t>(b * p.tc_stg_bytes));
                 bulk_commit();
                 if (use >= 1) {  // the previous round's store has read its buffer
                     bulk_wait_read(1);
@@ -424,32 +436,36 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
             n = mt.n;
             N = L + n;
             attend = n > 0 && static_cast<int64_t>(mt.i) * kTcT < N;
+            const int rg = mt.flags >> kRgShift;
+            rbase = rg * kRgRows;
+            Rg = min(kRgRows, R - rbase);
             const int64_t b = u / p.Hk, kv = u - b * p.Hk;
-            if (k == 0 && kv == 0 && r == 0) {
+            if (k == 0 && kv == 0 && rg == 0 && r == 0) {
                 const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
                 p.out_lengths[b] = ra.L + ra.n;
                 if (ra.flags && p.dev_status) atomicOr(p.dev_status, ra.flags);
             }
             if (attend) {
                 // every tensor-core instruction of earlier chunks has finished
-                const int t = r % Q;
-                valid = r < R && t < n;
+                const int rr = rbase + r;  // row of the unit
+                const int t = rr % Q;
+                valid = r < Rg && t < n;
                 lim = valid ? static_cast<int>(L + t) : -1;
-                rowg = ((b * p.Hq + kv * p.G + r / Q) * p.Q + t);
-                if (u != q_unit) {  // this row's query into tensor memory, 128 elements at a time
+                rowg = ((b * p.Hq + kv * p.G + rr / Q) * p.Q + t);
+                if (u * p.tc_nrg + rg != q_unit) {  // the row's query into tensor memory, 128 elements at a time
                     const uint4* src = reinterpret_cast<const uint4*>(query + rowg * D * p.es);
                     for (int g0 = 0; g0 < D / 64; g0 += 2) {
                         const int ng = min(2, D / 64 - g0);
                         uint4 v[16];
 #pragma unroll
                         for (int c = 0; c < 16; ++c)
-                            v[c] = (r < R && c < 8 * ng) ? src[8 * g0 + c] : make_uint4(0u, 0u, 0u, 0u);
+                            v[c] = (r < Rg && c < 8 * ng) ? src[8 * g0 + c] : make_uint4(0u, 0u, 0u, 0u);
                         tmem_st32u(trow + cols.q + 32 * g0, reinterpret_cast<const uint32_t*>(v));
                         if (ng > 1)
                             tmem_st32u(trow + cols.q + 32 * (g0 + 1),
                                        reinterpret_cast<const uint32_t*>(v + 8));
                     }
-                    q_unit = u;
+                    q_unit = u * p.tc_nrg + rg;
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -541,7 +557,7 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
                 ok = stage(reinterpret_cast<const uint32_t*>(ov), &tp.tm_acc, cb, z);
             }
             if (valid && s_k <= lim) {
-                const int64_t prow = (u * p.KP + k) * p.R + r;
+                const int64_t prow = (u * p.KP + k) * p.R + rbase + r;
                 p.part_ml[2 * prow] = m_ref;
                 p.part_ml[2 * prow + 1] = l;
             }

@@ -480,6 +480,7 @@ struct StepParams {
     // tensor-core kernel layout: two staging buffers of tc_stg_bytes each at
     // tc_off_stg (rows of 128 bytes for TMA stores), tensor-memory columns
     int tc_off_stg, tc_stg_bytes, tc_tmem_cols;
+    int64_t tc_nrg;  // row groups of up to 128 query rows per unit (1 or 2)
     int32_t* dev_status;
     int vec_attention;  // 1: attention rows may be written 8 elements at a time
     int64_t fin_seg;    // attention slots per row-writer block (a multiple of 8)

@@ -287,6 +287,13 @@ TC = {
                               lengths=("uniform", 17000, 19990)),
     "r64_bf16_segments_M9005": Spec(B=1, Hq=8, Hk=1, Q=8, D=64, Dv=64, M=9005, dtype="bf16",
                                     lengths=("uniform", 8000, 8995)),
+    # more than 128 query rows per unit: two row groups
+    "r160_bf16_chunk40": Spec(B=2, Hq=8, Hk=2, Q=40, D=64, Dv=64, M=600, dtype="bf16",
+                              lengths=("uniform", 100, 500)),
+    "r200_fp16_ragged": Spec(B=3, Hq=8, Hk=1, Q=25, D=128, Dv=128, M=777, dtype="f16",
+                             lengths=("uniform", 0, 752), counts=("uniform", 0, 25)),
+    "r256_bf16_D192": Spec(B=1, Hq=16, Hk=1, Q=16, D=192, Dv=128, M=1000, dtype="bf16",
+                           lengths=("uniform", 500, 984), counts=("uniform", 1, 16)),
 }
 
 
