@@ -39,7 +39,15 @@ _CSRC = "kv_cache_append_gb300/csrc/"
 # The first kernel of each path and the sources that define it.
 STEP_KERNEL = {"fused": "fused_step_kernel", "tensor": "tc_step_kernel",
                "generic": "generic_copy_kernel"}
-# Every kernel of a step with query rows, in launch order.
+# Every kernel of a step with query rows, in launch order (in place: the
+# cache write comes first and the generic path has no copy kernel).
+PATH_KERNELS_INPLACE = {
+    "fused": ["inplace_rows_kernel", "fused_step_kernel", "finalize_merge_kernel",
+              "finalize_rows_kernel"],
+    "tensor": ["inplace_rows_kernel", "tc_step_kernel", "finalize_merge_kernel",
+               "finalize_rows_kernel"],
+    "generic": ["inplace_rows_kernel", "generic_attend_kernel", "finalize_merge_kernel",
+                "finalize_rows_kernel"]}
 PATH_KERNELS = {"fused": ["fused_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "tensor": ["tc_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "generic": ["generic_copy_kernel", "generic_attend_kernel",
@@ -67,6 +75,26 @@ def algorithmic_bytes(spec: workloads.Spec, batch_rows: int | None = None) -> di
     ctx = B * spec.Hq * spec.Q * spec.Dv * es
     fused = 2 * cache + qkv + small
     return {"total": fused + att + ctx, "fused_kernel": fused, "finalize_kernel": att + ctx}
+
+
+def algorithmic_bytes_inplace(spec: workloads.Spec, lengths, counts) -> dict:
+    """Bytes the in-place step must move at minimum: the valid prefix of both
+    caches read (new length N_b = L_b + n_b slots per KV head), the appended
+    rows written, query / new rows / lengths / mask read, attention and
+    context written. ``lengths``/``counts`` are the batch rows' L_b and n_b."""
+    es = 4 if spec.dtype == "f32" else 2
+    B = len(lengths)
+    row = spec.Hk * (spec.D + spec.Dv) * es
+    N = int(sum(lengths)) + int(sum(counts))
+    prefix = N * row
+    appended = int(sum(counts)) * row
+    qkv = (B * spec.Hq * spec.Q * spec.D + B * spec.Hk * spec.Q * (spec.D + spec.Dv)) * es
+    small = B * 8 * 2 + B * spec.Q
+    att = B * spec.Hq * spec.Q * spec.M * es
+    ctx = B * spec.Hq * spec.Q * spec.Dv * es
+    step = prefix + qkv + small
+    return {"total": step + appended + att + ctx, "fused_kernel": step,
+            "finalize_kernel": att + ctx}
 
 
 def source_digest(paths) -> str:
@@ -234,7 +262,11 @@ def run_reference(args, spec, world, rank):
     for _ in range(args.steps):
         oracle.step(*sub, x.options)
     dt = (time.perf_counter() - t0) / args.steps
-    nbytes = algorithmic_bytes(spec, rows)["total"]
+    if args.inplace:  # the same step, counted with the in-place method's bytes
+        nbytes = algorithmic_bytes_inplace(spec, x.lengths[:rows].tolist(),
+                                           x.append_mask[:rows].to(torch.int64).sum(1).tolist())["total"]
+    else:
+        nbytes = algorithmic_bytes(spec, rows)["total"]
     value = nbytes / dt / 1e9
     sample = f"first {rows} of {spec.B} batch rows of {args.workload} per step"
     line = {
@@ -276,12 +308,23 @@ def run_ours(args, spec, world, rank, local):
     out = kvc.allocate_outputs(q, kc, vc)
     nws = kvc.workspace_bytes(dims)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
-    nkern, path = kvc.plan_info(dims, kc, vc, nk, nv, out["key_cache"], out["value_cache"])
     stream = torch.cuda.current_stream(dev)
+    if args.inplace:
+        # donated caches: every step appends the same rows at the same slots,
+        # so repeated steps leave the caches as the first one did
+        nkern, path = kvc.plan_info_inplace(dims, kc, vc, nk, nv)
+        del out["key_cache"], out["value_cache"]
+        torch.cuda.empty_cache()
 
-    def step(events=None):
-        kvc.step_into(dims, q, nk, nv, kc, vc, ln, mk, scale, out, ws, None,
-                      stream.cuda_stream, events)
+        def step(events=None):
+            kvc.step_inplace_into(dims, q, nk, nv, kc, vc, ln, mk, scale, out, ws, None,
+                                  stream.cuda_stream, events)
+    else:
+        nkern, path = kvc.plan_info(dims, kc, vc, nk, nv, out["key_cache"], out["value_cache"])
+
+        def step(events=None):
+            kvc.step_into(dims, q, nk, nv, kc, vc, ln, mk, scale, out, ws, None,
+                          stream.cuda_stream, events)
 
     for _ in range(args.warmup):
         step()
@@ -314,25 +357,33 @@ def run_ours(args, spec, world, rank, local):
     ms_step = ms_total / args.steps
     kern_ms = [statistics.mean(e[k].elapsed_time(e[k + 1]) for e in evs) for k in range(nkern)]
 
-    nbytes = algorithmic_bytes(spec)
+    lengths_h = x.lengths.cpu().tolist()
+    counts_h = x.append_mask.to(torch.int64).sum(1).cpu().tolist()
+    nbytes = (algorithmic_bytes_inplace(spec, lengths_h, counts_h) if args.inplace
+              else algorithmic_bytes(spec))
     value = world * nbytes["total"] / (ms_step * 1e-3) / 1e9
     peak, peak_src = measured_peak()
-    fused_ms = kern_ms[0]
+    ks = 1 if args.inplace and nkern > 1 else 0  # index of the step kernel
+    fused_ms = kern_ms[ks]
     achieved = nbytes["fused_kernel"] / (fused_ms * 1e-3) / 1e9
     kname = STEP_KERNEL[path]
-    traffic = kernel_traffic(args.workload, kname)
+    traffic = None if args.inplace else kernel_traffic(args.workload, kname)
 
     # ---- end to end through the public API: pinned host in, pinned host out
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(kvc, x, dev, spec, max(3, min(args.steps, 10)), nbytes["total"], world)
+        e2e = (measure_e2e_inplace(kvc, x, dev, max(3, min(args.steps, 10)), nbytes["total"],
+                                   world) if args.inplace else
+               measure_e2e(kvc, x, dev, spec, max(3, min(args.steps, 10)), nbytes["total"], world))
 
     # ---- CPU oracle baseline, rank 0 at N = 1 only
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xc = cpu_inputs(spec, seed=1)
         dt, rows, threads = oracle_sample(spec, xc, args.cpu_budget)
-        cpu = {"value": round(algorithmic_bytes(spec, rows)["total"] / dt / 1e9, 4),
+        sample_bytes = (algorithmic_bytes_inplace(spec, lengths_h[:rows], counts_h[:rows])
+                        if args.inplace else algorithmic_bytes(spec, rows))
+        cpu = {"value": round(sample_bytes["total"] / dt / 1e9, 4),
                "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"first {rows} of {spec.B} batch rows of {args.workload}, one step"}
 
@@ -348,7 +399,7 @@ def run_ours(args, spec, world, rank, local):
         "steps_per_s": round(world * 1e3 / ms_step, 2),
         "bytes_per_step": nbytes["total"],
         "path": path,
-        "kernels": {kname: {"ms": round(kern_ms[0], 4),
+        "kernels": {kname: {"ms": round(kern_ms[ks], 4),
                             "algorithmic_GBps": round(achieved, 1)}},
         "roofline": {"bound": "hbm", "kernel": kname,
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -359,10 +410,14 @@ def run_ours(args, spec, world, rank, local):
         "gpu_launches": nkern * args.steps,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
-    names = PATH_KERNELS[path]
-    for k in range(1, nkern):
-        line["kernels"][names[k]] = {"ms": round(kern_ms[k], 4)}
-    if nkern > 1:
+    names = (PATH_KERNELS_INPLACE if args.inplace else PATH_KERNELS)[path]
+    for k in range(nkern):
+        if k != ks:
+            line["kernels"][names[k]] = {"ms": round(kern_ms[k], 4)}
+    if args.inplace:
+        line["config"]["mode"] = ("in place: donated caches, only the appended rows written, "
+                                  "the attention reads the valid prefix")
+    if nkern > 2:
         fin_ms = kern_ms[-1] + kern_ms[-2]
         line["kernels"]["finalize (merge + rows)"] = {
             "ms": round(fin_ms, 4),
@@ -402,6 +457,44 @@ def measure_e2e(kvc, x, dev, spec, steps, nbytes, world):
             "steps": steps}
 
 
+def measure_e2e_inplace(kvc, x, dev, steps, nbytes, world):
+    """The in-place public call with host buffers for everything but the
+    donated caches, which stay resident on the device as a serving loop keeps
+    them: every step copies query, new rows, lengths and mask in from pinned
+    host memory and copies lengths, attention and context back."""
+    kc, vc = x.key_cache, x.value_cache
+    host_in = [t.to("cpu").pin_memory() for t in (x.query, x.new_key, x.new_value, x.lengths,
+                                                  x.append_mask)]
+    out0 = kvc.kv_cache_attention_step_inplace(x.query, x.new_key, x.new_value, kc, vc,
+                                               x.lengths, x.append_mask, x.options)
+    keys = ("lengths", "attention", "context")
+    host_out = {k: torch.empty(out0[k].shape, dtype=out0[k].dtype, pin_memory=True) for k in keys}
+    del out0
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        q, nk, nv, ln, mk = (t.to(dev, non_blocking=True) for t in host_in)
+        out = kvc.kv_cache_attention_step_inplace(q, nk, nv, kc, vc, ln, mk, x.options)
+        for k in keys:
+            host_out[k].copy_(out[k], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(s.elapsed_time(e) / steps, world)
+    return {"value": round(world * nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
+            "steps": steps, "resident": "key_cache, value_cache (donated, updated in place)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -419,6 +512,8 @@ def main():
                     help="override the tokens per step Q (the 32- and 24-token chunked appends)")
     ap.add_argument("--dtype", choices=["f32", "bf16", "f16"], default=None,
                     help="override the workload's dtype (the fp32 chunked append)")
+    ap.add_argument("--inplace", action="store_true",
+                    help="time kvc_step_inplace (donated caches updated in place)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

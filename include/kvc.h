@@ -148,6 +148,54 @@ KVC_API int kvc_plan_info(const kvc_dims *dims, const void *key_cache, const voi
                   const void *out_value_cache, const char **path_name);
 
 /*
+ * kvc_step_inplace -- the step on caches the caller donates for update in
+ * place, as a serving stack keeps them: one buffer of full capacity per
+ * layer per request, appended into ("KV-Cache for Incremental Decoding",
+ * Key Functions & Tricks: a pre-allocated fixed-size buffer; "Fixed-capacity
+ * KV cache", Task: append adds the new steps after the stored ones).
+ *
+ * Same operation and results as kvc_step, except that the updated caches
+ * are key_cache/value_cache themselves: only the rows [length, length + n)
+ * of each batch row are written (from new_key/new_value, "Write new_key/value
+ * at positions length+t only for True append slots t", Required behavior,
+ * bullet 3), every other slot keeps its contents, and the attention reads
+ * only the slots below each row's new length. The full-cache copy of
+ * kvc_step is not made.
+ *
+ *   key_cache       [B,Hk,M,D]  device, dtype, read and written in place.
+ *   value_cache     [B,Hk,M,Dv] device, dtype, read and written in place.
+ *   other arguments as for kvc_step (there are no out_key_cache /
+ *   out_value_cache); the workspace size is kvc_workspace_bytes(dims).
+ *
+ * The caches may not overlap any other argument or each other
+ * (KVC_E_ALIAS). Rows outside the contract append nothing and are flagged
+ * exactly as in kvc_step, so their cache rows are not written. Work is
+ * enqueued on `stream`; a call whose kernels overlap another call on the
+ * same caches (unordered streams) races with it.
+ */
+KVC_API int kvc_step_inplace(const kvc_dims *dims, const void *query, const void *new_key,
+                     const void *new_value, void *key_cache, void *value_cache,
+                     const int64_t *lengths, const uint8_t *append_mask, double scale,
+                     int64_t *out_lengths, void *out_attention, void *out_context,
+                     void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* kvc_step_inplace with events around its kernels, as kvc_step_timed. */
+KVC_API int kvc_step_inplace_timed(const kvc_dims *dims, const void *query, const void *new_key,
+                           const void *new_value, void *key_cache, void *value_cache,
+                           const int64_t *lengths, const uint8_t *append_mask, double scale,
+                           int64_t *out_lengths, void *out_attention, void *out_context,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                           void *stream, void *const *events, int n_events);
+
+/*
+ * Kernel count and path name (as kvc_plan_info) of kvc_step_inplace for
+ * these sizes and pointers.
+ */
+KVC_API int kvc_plan_info_inplace(const kvc_dims *dims, const void *key_cache,
+                          const void *value_cache, const void *new_key, const void *new_value,
+                          const char **path_name);
+
+/*
  * kvc_step_static -- kvc_step for callers that cannot allocate device memory.
  * The pages have no counterpart: this is a deployment variant of kvc_step.
  *

@@ -368,7 +368,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
               const uint8_t* append_mask, double scale, void* out_key_cache,
               void* out_value_cache, int64_t* out_lengths, void* out_attention,
               void* out_context, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-              void* stream_ptr, void* const* events, int n_events) {
+              void* stream_ptr, void* const* events, int n_events, bool inplace) {
     int rc = check_dims(dims);
     if (rc != KVC_OK) return rc;
     const kvc_dims d = *dims;
@@ -409,9 +409,15 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
         range_of(lengths, d.B * 8),
         range_of(append_mask, d.B * d.Q),
     };
+    // In place the caches are both: they may not overlap the other inputs,
+    // each other, or any output.
+    if (inplace)
+        for (int c = 3; c < 5; ++c)
+            for (int i = 0; i < 7; ++i)
+                if (i != c && overlaps(in[c], in[i])) return KVC_E_ALIAS;
     const Range out[] = {
-        range_of(out_key_cache, d.B * d.Hk * d.M * d.D * es),
-        range_of(out_value_cache, d.B * d.Hk * d.M * d.Dv * es),
+        range_of(inplace ? nullptr : out_key_cache, d.B * d.Hk * d.M * d.D * es),
+        range_of(inplace ? nullptr : out_value_cache, d.B * d.Hk * d.M * d.Dv * es),
         range_of(out_lengths, d.B * 8),
         range_of(out_attention, d.B * d.Hq * d.Q * d.M * es),
         range_of(out_context, d.B * d.Hq * d.Q * d.Dv * es),
@@ -464,6 +470,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     p.tc_tmem_cols = pl.tc_tmem_cols;
     p.dev_status = dev_status;
     p.vec_attention = (d.M % 8 == 0) && aligned16(out_attention);
+    p.inplace = inplace ? 1 : 0;
     // finalize blocks: rows longer than kFinalizeSeg slots are split so that
     // long-context steps with few query rows still fill the GPU
     p.fin_seg = d.M <= kFinalizeSeg ? align_up(d.M, 8) : kFinalizeSeg;
@@ -477,7 +484,12 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
         return cudaSuccess;
     };
     cudaError_t e = record();
-    if (e == cudaSuccess) {
+    if (e == cudaSuccess && inplace) {  // the appended rows and the lengths, before any reader
+        const bool words16 = (d.D * es) % 16 == 0 && (d.Dv * es) % 16 == 0 && ptrs_aligned;
+        e = launch_inplace_rows(p, words16, stream);
+        if (e == cudaSuccess) e = record();
+    }
+    if (e == cudaSuccess && (hasq || !inplace)) {
         if (pl.tensor) {
             TcParams tp;
             std::memset(&tp, 0, sizeof(tp));
@@ -500,8 +512,10 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
             if (e == cudaSuccess) e = launch_fused(p, d.dtype, pl.DVC, pl.NCHL, pl.smem, stream);
             if (e == cudaSuccess) e = record();
         } else {
-            e = launch_generic_copy(p, d.dtype, stream);
-            if (e == cudaSuccess) e = record();
+            if (!inplace) {
+                e = launch_generic_copy(p, d.dtype, stream);
+                if (e == cudaSuccess) e = record();
+            }
             if (e == cudaSuccess && hasq) {
                 e = launch_generic_attend(p, d.dtype, stream);
                 if (e == cudaSuccess) e = record();
@@ -513,8 +527,8 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
             if (e == cudaSuccess) e = launch_finalize_rows(p, d.dtype, stream);
             if (e == cudaSuccess) e = record();
         }
-        while (e == cudaSuccess && events && recorded < n_events) e = record();
     }
+    while (e == cudaSuccess && events && recorded < n_events) e = record();
     return e == cudaSuccess ? KVC_OK : KVC_E_CUDA;
 }
 
@@ -554,7 +568,7 @@ int kvc_step(const kvc_dims* dims, const void* query, const void* new_key, const
     return kvc::step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
                           append_mask, scale, out_key_cache, out_value_cache, out_lengths,
                           out_attention, out_context, workspace, workspace_bytes, dev_status,
-                          stream, nullptr, 0);
+                          stream, nullptr, 0, false);
 }
 
 int kvc_step_timed(const kvc_dims* dims, const void* query, const void* new_key,
@@ -567,7 +581,30 @@ int kvc_step_timed(const kvc_dims* dims, const void* query, const void* new_key,
     return kvc::step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
                           append_mask, scale, out_key_cache, out_value_cache, out_lengths,
                           out_attention, out_context, workspace, workspace_bytes, dev_status,
-                          stream, events, n_events);
+                          stream, events, n_events, false);
+}
+
+int kvc_step_inplace(const kvc_dims* dims, const void* query, const void* new_key,
+                     const void* new_value, void* key_cache, void* value_cache,
+                     const int64_t* lengths, const uint8_t* append_mask, double scale,
+                     int64_t* out_lengths, void* out_attention, void* out_context,
+                     void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    return kvc::step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
+                          append_mask, scale, key_cache, value_cache, out_lengths, out_attention,
+                          out_context, workspace, workspace_bytes, dev_status, stream, nullptr, 0,
+                          true);
+}
+
+int kvc_step_inplace_timed(const kvc_dims* dims, const void* query, const void* new_key,
+                           const void* new_value, void* key_cache, void* value_cache,
+                           const int64_t* lengths, const uint8_t* append_mask, double scale,
+                           int64_t* out_lengths, void* out_attention, void* out_context,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream, void* const* events, int n_events) {
+    return kvc::step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
+                          append_mask, scale, key_cache, value_cache, out_lengths, out_attention,
+                          out_context, workspace, workspace_bytes, dev_status, stream, events,
+                          n_events, true);
 }
 
 int kvc_plan_info(const kvc_dims* dims, const void* key_cache, const void* value_cache,
@@ -591,6 +628,15 @@ int kvc_plan_info(const kvc_dims* dims, const void* key_cache, const void* value
     const bool fused = ptrs_aligned && fused_plan(*dims, dev.sms, dev.smem_optin, true, &pl);
     if (path_name) *path_name = fused ? "fused" : "generic";
     return fused ? (hasq ? 3 : 1) : (hasq ? 4 : 1);
+}
+
+int kvc_plan_info_inplace(const kvc_dims* dims, const void* key_cache, const void* value_cache,
+                          const void* new_key, const void* new_value, const char** path_name) {
+    const int rc = kvc_plan_info(dims, key_cache, value_cache, new_key, new_value, key_cache,
+                                 value_cache, path_name);
+    if (rc < 0) return rc;
+    // the cache write, then with query rows the step kernel, the merge and the row writer
+    return dims->Q > 0 ? 4 : 1;
 }
 
 const char* kvc_status_string(int status) {

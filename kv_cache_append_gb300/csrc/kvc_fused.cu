@@ -65,7 +65,10 @@ __device__ void run_producer(const StepParams& p, unsigned char* smem, Bars bars
         const int64_t idx = chunk_of(q, p.NQ);
         const int64_t k = idx / U, u = idx - k * U;  // chunk-index-major list
         const Unit x = load_unit(p, u);
-        const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, p.TPU);
+        // in place, tiles from the new length on are neither read nor written
+        const int64_t iend = !p.inplace ? p.TPU : x.n > 0 ? min(p.TPU, (x.N + p.T - 1) / p.T) : 0;
+        const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, iend);
+        if (i0 >= i1) continue;
         const bool attend = x.n > 0 && i0 * p.T < x.N;
         const unsigned char* kcu = kc + u * p.M * rowK;
         const unsigned char* vcu = vc + u * p.M * rowV;
@@ -131,9 +134,12 @@ __device__ void run_storer(const StepParams& p, unsigned char* smem, Bars bars,
         if (mt.flags & kDone) break;
         const int64_t j0 = static_cast<int64_t>(mt.i) * p.T, j1 = min(j0 + p.T, p.M);
         const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
-        bulk_s2g(okc + (mt.u * p.M + j0) * rowK, sK, static_cast<uint32_t>((j1 - j0) * rowK));
-        bulk_s2g(ovc + (mt.u * p.M + j0) * rowV, sK + vofs, static_cast<uint32_t>((j1 - j0) * rowV));
-        bulk_commit();
+        if (!p.inplace) {
+            bulk_s2g(okc + (mt.u * p.M + j0) * rowK, sK, static_cast<uint32_t>((j1 - j0) * rowK));
+            bulk_s2g(ovc + (mt.u * p.M + j0) * rowV, sK + vofs,
+                     static_cast<uint32_t>((j1 - j0) * rowV));
+        }
+        bulk_commit();  // (an empty group in place)
         ++stored;
         ring.next(p.NS);
         if (stored - released > p.LAG) {
@@ -529,7 +535,7 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
             b = u / p.Hk;
             kv = u - b * p.Hk;
             attend = n > 0 && static_cast<int64_t>(mt.i) * p.T < N;
-            if (k == 0 && kv == 0 && w == 0 && lane == 0) {
+            if (k == 0 && kv == 0 && w == 0 && lane == 0 && !p.inplace) {
                 // returned length and contract flags: once per batch row
                 const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
                 p.out_lengths[b] = ra.L + ra.n;

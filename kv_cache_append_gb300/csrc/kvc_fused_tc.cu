@@ -121,7 +121,10 @@ __device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars
         const int64_t k = idx / UG, ug = idx - k * UG;
         const int64_t u = ug / p.tc_nrg, rg = ug - u * p.tc_nrg;
         const Unit x = load_unit(p, u);
-        const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, p.TPU);
+        // in place, tiles from the new length on are neither read nor written
+        const int64_t iend = !p.inplace ? p.TPU : x.n > 0 ? min(p.TPU, (x.N + kTcT - 1) / kTcT) : 0;
+        const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, iend);
+        if (i0 >= i1) continue;
         if (x.n > 0 && i0 * kTcT < x.L + x.n) {  // the softmax warps load these rows at the chunk start
             const int64_t r0 = rg * kRgRows, nr = min(static_cast<int64_t>(kRgRows), p.R - r0);
             bulk_prefetch_l2(static_cast<const unsigned char*>(p.query) + (u * p.R + r0) * p.D * p.es,
@@ -210,7 +213,7 @@ __device__ void tc_storer(const TcParams& tp, unsigned char* smem, TcBars bars,
             if (lane == 0) mbar_arrive(bars.patched(ring.s), 1u);
         }
         if (lane == 0) {
-            if ((mt.flags >> kRgShift) == 0) {  // other row groups read the same tile
+            if ((mt.flags >> kRgShift) == 0 && !p.inplace) {  // other row groups read the same tile
                 const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
                 const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBox);
                 const int y = static_cast<int>(j0), z = static_cast<int>(mt.u);
@@ -440,7 +443,7 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
             rbase = rg * kRgRows;
             Rg = min(kRgRows, R - rbase);
             const int64_t b = u / p.Hk, kv = u - b * p.Hk;
-            if (k == 0 && kv == 0 && rg == 0 && r == 0) {
+            if (k == 0 && kv == 0 && rg == 0 && r == 0 && !p.inplace) {
                 const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
                 p.out_lengths[b] = ra.L + ra.n;
                 if (ra.flags && p.dev_status) atomicOr(p.dev_status, ra.flags);

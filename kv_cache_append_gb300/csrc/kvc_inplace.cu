@@ -1,0 +1,56 @@
+// kvc_inplace.cu -- the cache write of the in-place step.
+//
+// A serving stack keeps the cache in a buffer allocated once at its full
+// capacity and appends into it ("KV-Cache for Incremental Decoding", Key
+// Functions & Tricks: a pre-allocated fixed-size buffer per layer per
+// request; "Fixed-capacity KV cache", Task: append adds the new steps after
+// the stored ones). In that mode only the n_b appended rows of each batch row
+// change: this kernel writes new_key/new_value rows t < n_b at slots
+// length_b + t of the caller's caches ("Write new_key/value at positions
+// length+t only for True append slots t", Required behavior, bullet 3), and
+// the returned lengths length_b + n_b with the contract flags. Every other
+// slot is left as it is; the attention kernels then read only the slots below
+// each row's new length.
+#include "kvc_internal.cuh"
+#include "kvc_launch.h"
+
+namespace kvc {
+namespace {
+
+constexpr int kRowThreads = 128;
+
+// One CTA per (batch row, KV head); Word is the unit each thread moves
+// (16 bytes when every row is a whole number of aligned 16-byte words,
+// else one element).
+template <typename Word>
+__global__ void __launch_bounds__(kRowThreads) inplace_rows_kernel(const __grid_constant__ StepParams p) {
+    const int64_t u = blockIdx.x;
+    const int64_t b = u / p.Hk, kv = u - b * p.Hk;
+    const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
+    if (kv == 0 && threadIdx.x == 0) {
+        p.out_lengths[b] = ra.L + ra.n;
+        if (ra.flags && p.dev_status) atomicOr(p.dev_status, ra.flags);
+    }
+    for (int which = 0; which < 2; ++which) {
+        const int64_t row = (which ? p.Dv : p.D) * p.es / static_cast<int64_t>(sizeof(Word));
+        const Word* src = static_cast<const Word*>(which ? p.new_value : p.new_key) + u * p.Q * row;
+        Word* dst = static_cast<Word*>(which ? p.out_value_cache : p.out_key_cache) +
+                    (u * p.M + ra.L) * row;
+        for (int64_t i = threadIdx.x; i < ra.n * row; i += kRowThreads) dst[i] = src[i];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_inplace_rows(const StepParams& p, bool words16, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>(p.B * p.Hk));
+    if (words16)
+        inplace_rows_kernel<uint4><<<grid, kRowThreads, 0, stream>>>(p);
+    else if (p.es == 2)
+        inplace_rows_kernel<uint16_t><<<grid, kRowThreads, 0, stream>>>(p);
+    else
+        inplace_rows_kernel<uint32_t><<<grid, kRowThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kvc

@@ -483,6 +483,10 @@ struct StepParams {
     int64_t tc_nrg;  // row groups of up to 128 query rows per unit (1 or 2)
     int32_t* dev_status;
     int vec_attention;  // 1: attention rows may be written 8 elements at a time
+    // 1: the caches are updated in place (out_key_cache == key_cache): the
+    // step kernels read only the tiles below each unit's new length and store
+    // nothing; inplace_rows_kernel writes the appended rows and the lengths.
+    int inplace;
     int64_t fin_seg;    // attention slots per row-writer block (a multiple of 8)
     int64_t fin_nseg;   // row-writer blocks per query row: ceil(M / fin_seg)
     RowStat* rowstat;   // [B][Hq][Q]: the merged maximum, 1 / sum and last allowed slot

@@ -36,6 +36,11 @@ cudaError_t launch_finalize_merge(const StepParams& p, int dtype, cudaStream_t s
 // Attention rows from the kept scores (or P values) and the RowStats (kvc_finalize.cu).
 cudaError_t launch_finalize_rows(const StepParams& p, int dtype, cudaStream_t stream);
 
+// The in-place step's cache write: appended rows and returned lengths
+// (kvc_inplace.cu). words16: every row is a whole number of 16-byte words and
+// the caches and new rows are 16-byte aligned.
+cudaError_t launch_inplace_rows(const StepParams& p, bool words16, cudaStream_t stream);
+
 // Generic path for shapes or alignments the fused kernel does not take
 // (kvc_generic.cu): copy + scatter, then attention partials.
 cudaError_t launch_generic_copy(const StepParams& p, int dtype, cudaStream_t stream);

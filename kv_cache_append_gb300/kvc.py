@@ -75,6 +75,13 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kvc_step_static.argtypes = [dp] + [vp] * 7 + [ctypes.c_double] + [vp] * 7
             lib.kvc_plan_info.restype = i32
             lib.kvc_plan_info.argtypes = [dp] + [vp] * 6 + [ctypes.POINTER(ctypes.c_char_p)]
+            inplace_args = [dp] + [vp] * 7 + [ctypes.c_double] + [vp] * 4 + [sz, vp, vp]
+            lib.kvc_step_inplace.restype = i32
+            lib.kvc_step_inplace.argtypes = inplace_args
+            lib.kvc_step_inplace_timed.restype = i32
+            lib.kvc_step_inplace_timed.argtypes = inplace_args + [ctypes.POINTER(vp), i32]
+            lib.kvc_plan_info_inplace.restype = i32
+            lib.kvc_plan_info_inplace.argtypes = [dp] + [vp] * 4 + [ctypes.POINTER(ctypes.c_char_p)]
             lib.kvc_status_string.restype = ctypes.c_char_p
             lib.kvc_status_string.argtypes = [i32]
             lib.kvc_version.restype = i32
@@ -109,6 +116,16 @@ def plan_info(dims: Dims, key_cache, value_cache, new_key, new_value, out_key_ca
     n = library().kvc_plan_info(ctypes.byref(dims), *(_p(t) for t in (
         key_cache, value_cache, new_key, new_value, out_key_cache, out_value_cache)),
         ctypes.byref(name))
+    if n < 0:
+        raise KvcError(n, status_string(n))
+    return n, name.value.decode()
+
+
+def plan_info_inplace(dims: Dims, key_cache, value_cache, new_key, new_value):
+    """(kernel count, path name) kvc_step_inplace takes for these tensors."""
+    name = ctypes.c_char_p()
+    n = library().kvc_plan_info_inplace(ctypes.byref(dims), *(_p(t) for t in (
+        key_cache, value_cache, new_key, new_value)), ctypes.byref(name))
     if n < 0:
         raise KvcError(n, status_string(n))
     return n, name.value.decode()
@@ -245,4 +262,64 @@ def kv_cache_attention_step(query: torch.Tensor, new_key: torch.Tensor, new_valu
     ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
     with torch.cuda.device(q.device):
         step_into(dims, q, nk, nv, kc, vc, ln, mk, scale, out, ws, status)
+    return out
+
+
+def step_inplace_into(dims: Dims, query, new_key, new_value, key_cache, value_cache, lengths,
+                      append_mask, scale: float, out: dict, workspace: Optional[torch.Tensor],
+                      status: Optional[torch.Tensor] = None, stream: Optional[int] = None,
+                      events: Optional[Sequence] = None) -> None:
+    """Enqueue one kvc_step_inplace: key_cache/value_cache are updated in
+    place; out holds "lengths", "attention" and "context" (no checks beyond
+    libkvc's)."""
+    lib = library()
+    if stream is None:
+        stream = torch.cuda.current_stream(query.device).cuda_stream
+    ws_ptr = _p(workspace)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    args = [ctypes.byref(dims), _p(query), _p(new_key), _p(new_value), _p(key_cache),
+            _p(value_cache), _p(lengths), _p(append_mask), ctypes.c_double(scale),
+            _p(out["lengths"]), _p(out["attention"]), _p(out["context"]), ws_ptr, ws_len,
+            _p(status), ctypes.c_void_p(stream)]
+    if events:
+        handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+        rc = lib.kvc_step_inplace_timed(*args, handles, len(events))
+    else:
+        rc = lib.kvc_step_inplace(*args)
+    if rc != KVC_OK:
+        raise KvcError(rc, status_string(rc))
+
+
+def kv_cache_attention_step_inplace(query: torch.Tensor, new_key: torch.Tensor,
+                                    new_value: torch.Tensor, key_cache: torch.Tensor,
+                                    value_cache: torch.Tensor, lengths: torch.Tensor,
+                                    append_mask: torch.Tensor, options: Optional[dict] = None,
+                                    status: Optional[torch.Tensor] = None) -> dict:
+    """The step on donated caches, as a serving stack keeps them: key_cache
+    and value_cache (contiguous CUDA tensors) are updated in place, only the
+    appended rows [length, length + n) being written. Returns the same dict
+    as kv_cache_attention_step, whose "key_cache"/"value_cache" are the
+    arguments themselves."""
+    check_inputs(query, new_key, new_value, key_cache, value_cache, lengths, append_mask)
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()):
+        raise ValueError("the caches are updated in place and must be contiguous")
+    scale = _scale_from(options, query.shape[-1])
+    q, nk, nv = (t.contiguous() for t in (query, new_key, new_value))
+    ln = lengths.to(torch.int64).contiguous()
+    mk = append_mask.contiguous()
+    mk = mk.view(torch.uint8) if mk.dtype == torch.bool else mk
+    dims = dims_of(q, key_cache, value_cache)
+    B, Hq, Q, _ = q.shape
+    M, Dv = key_cache.shape[2], value_cache.shape[-1]
+    out = {
+        "key_cache": key_cache,
+        "value_cache": value_cache,
+        "lengths": torch.empty(B, dtype=torch.int64, device=q.device),
+        "attention": torch.empty(B, Hq, Q, M, dtype=q.dtype, device=q.device),
+        "context": torch.empty(B, Hq, Q, Dv, dtype=q.dtype, device=q.device),
+    }
+    nbytes = workspace_bytes(dims)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
+    with torch.cuda.device(q.device):
+        step_inplace_into(dims, q, nk, nv, key_cache, value_cache, ln, mk, scale, out, ws, status)
     return out

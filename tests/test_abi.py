@@ -103,3 +103,25 @@ def test_binding_rejects_unknown_option():
     with pytest.raises(ValueError, match="only key"):
         kvc.kvc._scale_from({"scale": 0.5, "dropout": 0.1}, 16)
     assert kvc.kvc._scale_from({}, 16) == 0.25
+
+
+def _call_inplace(lib, dims, scale=0.25, null=()):
+    ptrs = {n: ctypes.c_void_p(4096 * (i + 1)) for i, n in enumerate(
+        ["q", "nk", "nv", "kc", "vc", "len", "mask", "ol", "oa", "oc", "ws"])}
+    for n in null:
+        ptrs[n] = None
+    return lib.kvc_step_inplace(ctypes.byref(dims) if dims is not None else None,
+                                ptrs["q"], ptrs["nk"], ptrs["nv"], ptrs["kc"], ptrs["vc"],
+                                ptrs["len"], ptrs["mask"], ctypes.c_double(scale), ptrs["ol"],
+                                ptrs["oa"], ptrs["oc"], ptrs["ws"], 1 << 30, None, None)
+
+
+def test_inplace_argument_errors_return_before_any_launch(lib):
+    assert _call_inplace(lib, None) == -1                   # KVC_E_NULL
+    assert _call_inplace(lib, _dims(dtype=7)) == -3         # KVC_E_DTYPE
+    assert _call_inplace(lib, _dims(Hq=3)) == -2            # KVC_E_SHAPE
+    assert _call_inplace(lib, _dims(), null=("kc",)) == -1  # the donated caches are required
+    assert _call_inplace(lib, _dims(), null=("vc",)) == -1
+    assert _call_inplace(lib, _dims(), null=("ol",)) == -1
+    assert _call_inplace(lib, _dims(), null=("q",)) == -1
+    assert _call_inplace(lib, _dims(), scale=0.0) == -4     # KVC_E_SCALE
