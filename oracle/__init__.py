@@ -88,6 +88,8 @@ class Oracle:
         lib.kvo_widen_n.argtypes = [ctypes.c_int, vp, i64, vp]
         lib.kvo_threads.restype = ctypes.c_int
         lib.kvo_threads.argtypes = []
+        lib.kvo_attend_cache.restype = ctypes.c_int
+        lib.kvo_attend_cache.argtypes = [ctypes.c_int] + [i64] * 7 + [vp] * 6 + [dbl] + [vp] * 3
         self.lib = lib
 
     def threads(self) -> int:
@@ -151,6 +153,32 @@ class Oracle:
         return att, ctx
 
 
+    def attend_cache(self, q, cache_key, cache_value, cu_seqlens_q, seqlens_k, slot_ids=None,
+                     scale: float | None = None):
+        """Read-only re-attention of packed queries q [total_q, Hq, D] over the
+        cache rows slot_ids[b] (default b) of cache_key [num_slots, Hk, M, D] /
+        cache_value [num_slots, Hk, M, Dv]: out [total_q, Hq, Dv] float64 and
+        flags [B] (1 = sequence outside the contract, zero rows)."""
+        qh, kc, vc = (_host(x) for x in (q, cache_key, cache_value))
+        total_q, Hq, D = qh.shape
+        num_slots, Hk, M, _ = kc.shape
+        Dv = vc.shape[-1]
+        cu = _host(cu_seqlens_q).to(torch.int32)
+        B = cu.numel() - 1
+        kl = _host(seqlens_k).to(torch.int32)
+        sl = None if slot_ids is None else _host(slot_ids).to(torch.int32)
+        if scale is None:
+            scale = default_scale(D)
+        out = np.zeros((total_q, Hq, Dv), dtype=np.float64)
+        flags = np.zeros(B, dtype=np.int32)
+        work = np.empty(max(1, self.threads()) * max(1, M), dtype=np.float64)
+        self.lib.kvo_attend_cache(DTYPE_CODES[qh.dtype], B, Hq, Hk, D, Dv, M, num_slots,
+                                  _ptr(qh), _ptr(kc), _ptr(vc), _ptr(cu), _ptr(kl),
+                                  None if sl is None else _ptr(sl), float(scale),
+                                  out.ctypes.data, flags.ctypes.data, work.ctypes.data)
+        return out, flags
+
+
 _lock = threading.Lock()
 _default: Oracle | None = None
 
@@ -173,6 +201,10 @@ def widen(t):
 
 def step(*args, **kw):
     return default().step(*args, **kw)
+
+
+def attend_cache(*args, **kw):
+    return default().attend_cache(*args, **kw)
 
 
 def rows(*args, **kw):

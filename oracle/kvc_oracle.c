@@ -30,6 +30,11 @@
  *   kvo_rows           the same attention/context for a list of (b,h,t) rows
  *                      only, reading the updated cache through its definition
  *                      (new row if length <= j < length+n, else old cache row).
+ *   kvo_attend_cache   the read-only re-attention of "ClikaRT::ops::
+ *                      attention_over_cache" (docs.clika.io): packed queries
+ *                      attend a cache another call already appended, through
+ *                      a per-sequence cache row (slot_ids) and total cached
+ *                      length (cu_seqlens_k); the cache is never written.
  *
  * Precision: every element is widened exactly to double, dot products, max,
  * exp, sums and the weighted value sum are taken in double, in slot order.
@@ -260,6 +265,79 @@ int kvo_rows(int dtype, int64_t B, int64_t Hq, int64_t Hk, int64_t Q, int64_t D,
         attend_row(dtype, Hq, Hk, Q, D, Dv, M, query, new_key, new_value, key_cache,
                    value_cache, L, n, t < n, scale, b, h, t, att + i * M, ctx + i * Dv,
                    work + (int64_t)tid * M);
+    }
+    return any;
+}
+
+/*
+ * Read-only re-attention ("ClikaRT::ops::attention_over_cache", the
+ * function's description). Sequence b owns the packed query rows
+ * cu_q[b] .. cu_q[b+1]-1 of q [total_q, Hq, D] (S_b rows) and reads cache row
+ * slot_b = slot_ids[b] (b when slot_ids is NULL) of cache_key
+ * [num_slots, Hk, M, D] / cache_value [num_slots, Hk, M, Dv], which holds its
+ * K_b = seqlens_k[b] cached positions (the total, q's own positions
+ * included). "q's position derives from cu_seqlens_k": the S_b queries are
+ * the sequence's last S_b positions, so query t sits at K_b - S_b + t and
+ * attends the slots j <= K_b - S_b + t (the lower-right causal rule of the
+ * append step). Query head h reads KV head floor(h / (Hq/Hk)).
+ * out [total_q, Hq, Dv] in double. A sequence outside the contract
+ * (S_b < 0, S_b > K_b, K_b > M, slot_b outside [0, num_slots)) gets zero
+ * rows and flag KVO_FLAG_OVERFLOW in flags[b] (nullable). Returns the OR of
+ * all flags.
+ */
+int kvo_attend_cache(int dtype, int64_t B, int64_t Hq, int64_t Hk, int64_t D, int64_t Dv,
+                     int64_t M, int64_t num_slots, const void *q, const void *cache_key,
+                     const void *cache_value, const int32_t *cu_q, const int32_t *seqlens_k,
+                     const int32_t *slot_ids, double scale, double *out, int32_t *flags,
+                     double *work) {
+    const int64_t total_q = cu_q[B];
+    for (int64_t i = 0; i < total_q * Hq * Dv; ++i) out[i] = 0.0;
+    const int64_t group = Hq / Hk;
+    int any = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : any)
+    for (int64_t b = 0; b < B; ++b) {
+        const int64_t S = (int64_t)cu_q[b + 1] - cu_q[b];
+        const int64_t K = seqlens_k[b];
+        const int64_t slot = slot_ids ? slot_ids[b] : b;
+        const int bad = S < 0 || S > K || K > M || slot < 0 || slot >= num_slots;
+        if (flags) flags[b] = bad ? KVO_FLAG_OVERFLOW : 0;
+        if (bad) {
+            any |= KVO_FLAG_OVERFLOW;
+            continue;
+        }
+        int tid = 0;
+#ifdef _OPENMP
+        tid = omp_get_thread_num();
+#endif
+        double *sc = work + (int64_t)tid * M;
+        for (int64_t t = 0; t < S; ++t) {
+            const int64_t row = cu_q[b] + t;
+            const int64_t last = K - S + t; /* allowed: j <= K - S + t */
+            for (int64_t h = 0; h < Hq; ++h) {
+                const int64_t kv = h / group;
+                double m = -INFINITY;
+                for (int64_t j = 0; j <= last; ++j) {
+                    double s = 0.0;
+                    for (int64_t d = 0; d < D; ++d)
+                        s += kvo_widen(dtype, q, (row * Hq + h) * D + d) *
+                             kvo_widen(dtype, cache_key, ((slot * Hk + kv) * M + j) * D + d);
+                    s *= scale;
+                    sc[j] = s;
+                    if (s > m) m = s;
+                }
+                double l = 0.0;
+                for (int64_t j = 0; j <= last; ++j) {
+                    sc[j] = exp(sc[j] - m);
+                    l += sc[j];
+                }
+                double *o = out + (row * Hq + h) * Dv;
+                for (int64_t j = 0; j <= last; ++j) {
+                    const double a = sc[j] / l;
+                    for (int64_t e = 0; e < Dv; ++e)
+                        o[e] += a * kvo_widen(dtype, cache_value, ((slot * Hk + kv) * M + j) * Dv + e);
+                }
+            }
+        }
     }
     return any;
 }

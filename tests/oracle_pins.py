@@ -14,6 +14,9 @@ Sources:
               problems), Step-by-Step Approach, step 6.
   [lowright]  KempnerForge pull request 542, Summary and Testing: multi-token
               appends to a filled cache with a lower-right causal mask.
+  [readonly]  "ClikaRT::ops::attention_over_cache" (docs.clika.io): packed
+              queries re-attend an already appended cache through slot_ids
+              and cu_seqlens_k, without writing it.
 """
 from __future__ import annotations
 
@@ -448,6 +451,99 @@ def pin_low_precision_inputs_vs_sdpa(o):
         np.testing.assert_allclose(out["context"][valid], ref_ctx[valid], rtol=0, atol=1e-12)
 
 
+# ---------------------------------------------------------------- [readonly]
+def _pack_step_queries(x, counts):
+    """The step's valid query rows (t < n_b) as packed [total_q, Hq, D] rows."""
+    rows, cu = [], [0]
+    for b in range(x.query.shape[0]):
+        n = int(counts[b])
+        rows.append(x.query[b, :, :n].permute(1, 0, 2))  # [n, Hq, D]
+        cu.append(cu[-1] + n)
+    return torch.cat(rows, 0).contiguous(), torch.tensor(cu, dtype=torch.int32)
+
+
+def pin_attend_cache_equals_step_context(o):
+    """[readonly] + [contract]: appending n rows and attending with the step
+    gives the context that re-attending the updated cache with those n
+    queries (total length L + n) gives."""
+    from workloads import Spec
+    for dtype, seed in (("f32", 0), ("bf16", 1), ("f16", 2)):
+        spec = Spec(B=3, Hq=4, Hk=2, Q=4, D=16, Dv=8, M=40, dtype=dtype,
+                    counts=("uniform", 0, 4))
+        x = workloads.generate(spec, seed)
+        ref = o.step(*x.args(), x.options)
+        counts = x.append_mask.to(torch.int64).sum(1)
+        q, cu = _pack_step_queries(x, counts)
+        kl = (x.lengths + counts).to(torch.int32)
+        out, flags = o.attend_cache(q, ref["key_cache"], ref["value_cache"], cu, kl)
+        assert not flags.any()
+        for b in range(spec.B):
+            for t in range(int(counts[b])):
+                np.testing.assert_allclose(out[int(cu[b]) + t], ref["context"][b, :, t],
+                                           rtol=0, atol=1e-12)
+
+
+def pin_attend_cache_vs_sdpa(o):
+    """[readonly]: torch's fp64 scaled_dot_product_attention with an explicit
+    lower-right boolean mask, per sequence, through the slot map."""
+    g = torch.Generator().manual_seed(5)
+    Hq, Hk, D, Dv, M, slots = 6, 2, 8, 5, 24, 4
+    kc = torch.randn(slots, Hk, M, D, generator=g, dtype=torch.float64).float()
+    vc = torch.randn(slots, Hk, M, Dv, generator=g, dtype=torch.float64).float()
+    S, K = [3, 1, 0, 5], [10, 1, 7, 24]
+    slot = torch.tensor([2, 0, 3, 1], dtype=torch.int32)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(S)]), dtype=torch.int32)
+    q = torch.randn(int(cu[-1]), Hq, D, generator=g, dtype=torch.float64).float()
+    scale = 0.3
+    out, flags = o.attend_cache(q, kc, vc, cu, torch.tensor(K, dtype=torch.int32), slot,
+                                scale=scale)
+    assert not flags.any()
+    q, kc, vc = q.double(), kc.double(), vc.double()
+    for b in range(len(S)):
+        if S[b] == 0:
+            continue
+        s = int(slot[b])
+        keys = kc[s, :, :K[b]].repeat_interleave(Hq // Hk, 0)      # [Hq, K, D]
+        vals = vc[s, :, :K[b]].repeat_interleave(Hq // Hk, 0)
+        qb = q[int(cu[b]):int(cu[b + 1])].permute(1, 0, 2)          # [Hq, S, D]
+        pos = torch.arange(S[b])[:, None] + (K[b] - S[b])
+        allowed = torch.arange(K[b])[None, :] <= pos                # lower-right causal
+        want = F.scaled_dot_product_attention(qb, keys, vals, attn_mask=allowed, scale=scale)
+        np.testing.assert_allclose(out[int(cu[b]):int(cu[b + 1])],
+                                   want.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def pin_attend_cache_slot_permutation(o):
+    """[readonly]: permuting the cache rows together with slot_ids changes nothing."""
+    g = torch.Generator().manual_seed(8)
+    kc = torch.randn(5, 1, 12, 4, generator=g).to(torch.bfloat16)
+    vc = torch.randn(5, 1, 12, 3, generator=g).to(torch.bfloat16)
+    q = torch.randn(6, 2, 4, generator=g).to(torch.bfloat16)
+    cu = torch.tensor([0, 2, 3, 6], dtype=torch.int32)
+    kl = torch.tensor([5, 12, 3], dtype=torch.int32)
+    slot = torch.tensor([4, 0, 2], dtype=torch.int32)
+    a, _ = o.attend_cache(q, kc, vc, cu, kl, slot)
+    perm = torch.tensor([3, 1, 4, 0, 2])  # new row i holds old row perm[i]
+    inv = torch.argsort(perm)
+    b, _ = o.attend_cache(q, kc[perm], vc[perm], cu, kl, inv[slot.long()].to(torch.int32))
+    np.testing.assert_array_equal(a, b)
+
+
+def pin_attend_cache_outside_contract(o):
+    """[readonly]: a sequence with S > K, K > M or its slot out of range gets
+    zero rows and a flag; the others are untouched by it."""
+    kc = torch.ones(2, 1, 8, 4)
+    vc = torch.ones(2, 1, 8, 4)
+    q = torch.ones(7, 1, 4)
+    cu = torch.tensor([0, 3, 4, 5, 7], dtype=torch.int32)
+    kl = torch.tensor([2, 9, 4, 5], dtype=torch.int32)
+    slot = torch.tensor([0, 1, 5, 1], dtype=torch.int32)
+    out, flags = o.attend_cache(q, kc, vc, cu, kl, slot)
+    assert flags.tolist() == [1, 1, 1, 0]
+    assert np.all(out[:5] == 0.0)
+    np.testing.assert_allclose(out[5:], 1.0, rtol=0, atol=1e-15)
+
+
 ALL_PINS = [
     pin_fixed_capacity_example,
     pin_fixed_capacity_closed_form,
@@ -465,4 +561,8 @@ ALL_PINS = [
     pin_widen_fp16_all_patterns,
     pin_widen_bf16_all_patterns,
     pin_low_precision_inputs_vs_sdpa,
+    pin_attend_cache_equals_step_context,
+    pin_attend_cache_vs_sdpa,
+    pin_attend_cache_slot_permutation,
+    pin_attend_cache_outside_contract,
 ]

@@ -20,6 +20,11 @@ MUTANTS = {
     "bf16_shift": ("(uint32_t)b << 16", "(uint32_t)b << 15"),
     "non_prefix_accepted": ("if (mask_row[t]) f |= KVO_FLAG_MASK;", ";"),
     "softmax_epsilon": ("att_row[j] = scratch[j] / l;", "att_row[j] = scratch[j] / (l + 1e-9);"),
+    # read-only re-attention
+    "attend_self_slot_excluded": ("const int64_t last = K - S + t;", "const int64_t last = K - S + t - 1;"),
+    "attend_slot_ignored": ("const int64_t slot = slot_ids ? slot_ids[b] : b;", "const int64_t slot = b;"),
+    "attend_query_row_fixed": ("const int64_t row = cu_q[b] + t;", "const int64_t row = cu_q[b];"),
+    "attend_s_gt_k_accepted": ("const int bad = S < 0 || S > K ||", "const int bad = S < 0 ||"),
 }
 
 
