@@ -196,6 +196,62 @@ KVC_API int kvc_plan_info_inplace(const kvc_dims *dims, const void *key_cache,
                           const char **path_name);
 
 /*
+ * kvc_attend_cache -- read-only re-attention over a cache that earlier steps
+ * appended ("ClikaRT::ops::attention_over_cache": attend a KV cache without
+ * appending to it; q packed varlen, a continuous head-major cache, slot_ids
+ * naming each batch row's cache row, cu_seqlens_k each sequence's total
+ * cached length; the cache is never written). The RoPE, qk-norm, softcap,
+ * sliding-window, sink and quantised-scale options of that function are not
+ * part of this operation.
+ *
+ *   dims            B sequences, Hq, Hk, Q = the largest query count of a
+ *                   sequence (max_seqlen_q), D, Dv, M = slots per cache row,
+ *                   dtype (host pointer).
+ *   num_slots       cache rows: the caches are [num_slots, Hk, M, D] and
+ *                   [num_slots, Hk, M, Dv] (device, dtype, read only).
+ *   total_q         packed query rows.
+ *   q               [total_q, Hq, D] device, dtype; sequence b owns rows
+ *                   cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 (S_b rows).
+ *   cu_seqlens_q    [B + 1] device int32, non-decreasing, ending at total_q.
+ *   seqlens_k       device int32: [B] totals K_b (k_cumulative = 0) or
+ *                   [B + 1] cumulative offsets, K_b = [b+1] - [b]
+ *                   (k_cumulative = 1). K_b counts the sequence's own S_b
+ *                   query positions.
+ *   slot_ids        [B] device int32 cache row per sequence, or NULL for
+ *                   row b (then num_slots >= B).
+ *   scale           > 0, finite.
+ *   out             [total_q, Hq, Dv] device, dtype.
+ *   workspace       >= kvc_attend_cache_workspace_bytes(dims), 16-byte
+ *                   aligned.
+ *   dev_status      device int32, nullable.
+ *
+ * The S_b queries are the sequence's last S_b positions: query t attends
+ * slots j <= K_b - S_b + t of its cache row (the append step's lower-right
+ * causal rule), query head h the KV head floor(h / (Hq/Hk)). A sequence with
+ * S_b > Q, S_b > K_b, K_b > M or its slot outside [0, num_slots) gets zero
+ * output rows and KVC_DEV_OVERFLOW. Returns KVC_OK once enqueued, else a
+ * KVC_E_* code (nothing launched).
+ */
+KVC_API size_t kvc_attend_cache_workspace_bytes(const kvc_dims *dims);
+
+KVC_API int kvc_attend_cache(const kvc_dims *dims, int64_t num_slots, int64_t total_q,
+                     const void *q, const void *key_cache, const void *value_cache,
+                     const int32_t *cu_seqlens_q, const int32_t *seqlens_k, int k_cumulative,
+                     const int32_t *slot_ids, double scale, void *out, void *workspace,
+                     size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * kvc_attend_cache with events: events[0] before the first kernel, then one
+ * after each kernel (query packing, attention, merge, context unpacking).
+ */
+KVC_API int kvc_attend_cache_timed(const kvc_dims *dims, int64_t num_slots, int64_t total_q,
+                           const void *q, const void *key_cache, const void *value_cache,
+                           const int32_t *cu_seqlens_q, const int32_t *seqlens_k,
+                           int k_cumulative, const int32_t *slot_ids, double scale, void *out,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                           void *stream, void *const *events, int n_events);
+
+/*
  * kvc_step_static -- kvc_step for callers that cannot allocate device memory.
  * The pages have no counterpart: this is a deployment variant of kvc_step.
  *

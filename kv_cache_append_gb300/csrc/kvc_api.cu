@@ -363,20 +363,34 @@ Range range_of(const void* p, int64_t bytes) {
 
 bool overlaps(Range a, Range b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
 
+// How a step runs: out of place (the default), in place on donated caches,
+// or as read-only re-attention (in place, nothing written to the caches, the
+// cache row of batch row b given by slot_ids, no attention rows).
+struct StepMode {
+    bool inplace = false;
+    bool readonly = false;
+    bool rows = true;                  // write the attention rows
+    const int32_t* slot_ids = nullptr;  // device [B]; NULL: row b
+    int64_t cache_units = -1;          // units the caches hold (default B * Hk)
+};
+
 int step_impl(const kvc_dims* dims, const void* query, const void* new_key, const void* new_value,
               const void* key_cache, const void* value_cache, const int64_t* lengths,
               const uint8_t* append_mask, double scale, void* out_key_cache,
               void* out_value_cache, int64_t* out_lengths, void* out_attention,
               void* out_context, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-              void* stream_ptr, void* const* events, int n_events, bool inplace) {
+              void* stream_ptr, void* const* events, int n_events, const StepMode& mode) {
     int rc = check_dims(dims);
     if (rc != KVC_OK) return rc;
     const kvc_dims d = *dims;
     const bool hasq = d.Q > 0;
+    const bool inplace = mode.inplace;
+    const int64_t CU = mode.cache_units >= 0 ? mode.cache_units : d.B * d.Hk;
     if (!key_cache || !value_cache || !lengths || !out_key_cache || !out_value_cache ||
         !out_lengths)
         return KVC_E_NULL;
-    if (hasq && (!query || !new_key || !new_value || !append_mask || !out_attention || !out_context))
+    if (hasq && (!query || !new_key || !new_value || !append_mask || !out_context ||
+                 (mode.rows && !out_attention)))
         return KVC_E_NULL;
     if (!(scale > 0.0) || !std::isfinite(scale)) return KVC_E_SCALE;
     if (events && n_events < 0) return KVC_E_NULL;
@@ -402,10 +416,10 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     // Outputs and workspace must not overlap inputs or each other.
     const Range in[] = {
         range_of(query, d.B * d.Hq * d.Q * d.D * es),
-        range_of(new_key, d.B * d.Hk * d.Q * d.D * es),
-        range_of(new_value, d.B * d.Hk * d.Q * d.Dv * es),
-        range_of(key_cache, d.B * d.Hk * d.M * d.D * es),
-        range_of(value_cache, d.B * d.Hk * d.M * d.Dv * es),
+        range_of(mode.readonly ? nullptr : new_key, d.B * d.Hk * d.Q * d.D * es),
+        range_of(mode.readonly ? nullptr : new_value, d.B * d.Hk * d.Q * d.Dv * es),
+        range_of(key_cache, CU * d.M * d.D * es),
+        range_of(value_cache, CU * d.M * d.Dv * es),
         range_of(lengths, d.B * 8),
         range_of(append_mask, d.B * d.Q),
     };
@@ -419,7 +433,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
         range_of(inplace ? nullptr : out_key_cache, d.B * d.Hk * d.M * d.D * es),
         range_of(inplace ? nullptr : out_value_cache, d.B * d.Hk * d.M * d.Dv * es),
         range_of(out_lengths, d.B * 8),
-        range_of(out_attention, d.B * d.Hq * d.Q * d.M * es),
+        range_of(mode.rows ? out_attention : nullptr, d.B * d.Hq * d.Q * d.M * es),
         range_of(out_context, d.B * d.Hq * d.Q * d.Dv * es),
         range_of(workspace, static_cast<int64_t>(pl.ws_bytes)),
     };
@@ -471,6 +485,8 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     p.dev_status = dev_status;
     p.vec_attention = (d.M % 8 == 0) && aligned16(out_attention);
     p.inplace = inplace ? 1 : 0;
+    p.readonly = mode.readonly ? 1 : 0;
+    p.slot_ids = mode.slot_ids;
     // finalize blocks: rows longer than kFinalizeSeg slots are split so that
     // long-context steps with few query rows still fill the GPU
     p.fin_seg = d.M <= kFinalizeSeg ? align_up(d.M, 8) : kFinalizeSeg;
@@ -484,7 +500,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
         return cudaSuccess;
     };
     cudaError_t e = record();
-    if (e == cudaSuccess && inplace) {  // the appended rows and the lengths, before any reader
+    if (e == cudaSuccess && inplace && !mode.readonly) {  // appended rows and lengths, before any reader
         const bool words16 = (d.D * es) % 16 == 0 && (d.Dv * es) % 16 == 0 && ptrs_aligned;
         e = launch_inplace_rows(p, words16, stream);
         if (e == cudaSuccess) e = record();
@@ -494,8 +510,8 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
             TcParams tp;
             std::memset(&tp, 0, sizeof(tp));
             tp.p = p;
-            if (!cache_map(&tp.tm_k, key_cache, d.dtype, d.D, d.M, d.B * d.Hk) ||
-                !cache_map(&tp.tm_v, value_cache, d.dtype, d.Dv, d.M, d.B * d.Hk) ||
+            if (!cache_map(&tp.tm_k, key_cache, d.dtype, d.D, d.M, CU) ||
+                !cache_map(&tp.tm_v, value_cache, d.dtype, d.Dv, d.M, CU) ||
                 !cache_map(&tp.tm_ok, out_key_cache, d.dtype, d.D, d.M, d.B * d.Hk) ||
                 !cache_map(&tp.tm_ov, out_value_cache, d.dtype, d.Dv, d.M, d.B * d.Hk) ||
                 !rows_map(&tp.tm_pv, p.pvals, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, d.M, p.pv_ld,
@@ -524,14 +540,142 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
         if (e == cudaSuccess && hasq) {
             e = launch_finalize_merge(p, d.dtype, stream);
             if (e == cudaSuccess) e = record();
-            if (e == cudaSuccess) e = launch_finalize_rows(p, d.dtype, stream);
-            if (e == cudaSuccess) e = record();
+            if (e == cudaSuccess && mode.rows) {
+                e = launch_finalize_rows(p, d.dtype, stream);
+                if (e == cudaSuccess) e = record();
+            }
         }
     }
     while (e == cudaSuccess && events && recorded < n_events) e = record();
     return e == cudaSuccess ? KVC_OK : KVC_E_CUDA;
 }
 
+}  // namespace
+}  // namespace kvc
+
+namespace kvc {
+namespace {
+StepMode inplace_mode() {
+    StepMode m;
+    m.inplace = true;
+    return m;
+}
+
+// Workspace of the read-only re-attention: the dense step's workspace, then
+// the dense query and context rows, lengths, mask, slots and a lengths
+// scratch the step needs as an argument.
+struct AttendLayout {
+    size_t step = 0, q_dense = 0, ctx_dense = 0, lengths = 0, mask = 0, slots = 0, out_len = 0,
+           total = 0;
+};
+
+bool attend_layout(const kvc_dims& d, AttendLayout* L) {
+    const size_t step = kvc_workspace_bytes(&d);
+    if (step == 0) return false;
+    const size_t es = static_cast<size_t>(elem_size(d.dtype));
+    const size_t B = static_cast<size_t>(d.B), rows = B * d.Hq * d.Q;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    size_t off = up(step);
+    L->step = step;
+    L->q_dense = off; off = up(off + rows * d.D * es);
+    L->ctx_dense = off; off = up(off + rows * d.Dv * es);
+    L->lengths = off; off = up(off + B * 8);
+    L->mask = off; off = up(off + B * d.Q);
+    L->slots = off; off = up(off + B * 4);
+    L->out_len = off; off = up(off + B * 8);
+    L->total = off;
+    return true;
+}
+
+int attend_impl(const kvc_dims* dims, int64_t num_slots, int64_t total_q, const void* q,
+                const void* key_cache, const void* value_cache, const int32_t* cu_seqlens_q,
+                const int32_t* seqlens_k, int k_cumulative, const int32_t* slot_ids,
+                double scale, void* out, void* workspace, size_t workspace_bytes,
+                int32_t* dev_status, void* stream_ptr, void* const* events, int n_events) {
+    int rc = check_dims(dims);
+    if (rc != KVC_OK) return rc;
+    const kvc_dims d = *dims;
+    if (num_slots < 1 || total_q < 0 || (k_cumulative != 0 && k_cumulative != 1) ||
+        (!slot_ids && num_slots < d.B) || (total_q > 0 && d.Q < 1))
+        return KVC_E_SHAPE;
+    const int64_t es = elem_size(d.dtype);
+    if (static_cast<double>(num_slots) * d.Hk * d.M * (d.D + d.Dv) * es > 4.0e18 ||
+        static_cast<double>(total_q) * d.Hq * (d.D + d.Dv) * es > 4.0e18 ||
+        total_q >= (int64_t(1) << 31) || num_slots >= (int64_t(1) << 31))
+        return KVC_E_SHAPE;
+    if (!key_cache || !value_cache || !cu_seqlens_q || !seqlens_k ||
+        (total_q > 0 && (!q || !out)))
+        return KVC_E_NULL;
+    if (!(scale > 0.0) || !std::isfinite(scale)) return KVC_E_SCALE;
+    if (events && n_events < 0) return KVC_E_NULL;
+    AttendLayout L;
+    if (!attend_layout(d, &L)) return KVC_E_SHAPE;
+    if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return KVC_E_WORKSPACE;
+    const Range ins[] = {
+        range_of(q, total_q * d.Hq * d.D * es),
+        range_of(key_cache, num_slots * d.Hk * d.M * d.D * es),
+        range_of(value_cache, num_slots * d.Hk * d.M * d.Dv * es),
+        range_of(cu_seqlens_q, (d.B + 1) * 4),
+        range_of(seqlens_k, (d.B + k_cumulative) * 4),
+        range_of(slot_ids, d.B * 4),
+        range_of(workspace, static_cast<int64_t>(L.total)),
+    };
+    const Range o = range_of(out, total_q * d.Hq * d.Dv * es);
+    for (const Range& i : ins)
+        if (overlaps(o, i)) return KVC_E_ALIAS;
+    for (int i = 0; i < 6; ++i)
+        if (overlaps(ins[i], ins[6])) return KVC_E_ALIAS;
+
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    AttendParams a;
+    std::memset(&a, 0, sizeof(a));
+    a.B = d.B; a.Hq = d.Hq; a.Hk = d.Hk; a.Q = d.Q; a.D = d.D; a.Dv = d.Dv; a.M = d.M;
+    a.num_slots = num_slots; a.total_q = total_q;
+    a.es = static_cast<int>(es); a.k_cumulative = k_cumulative;
+    a.q = q; a.cu_q = cu_seqlens_q; a.seqlens_k = seqlens_k; a.slot_ids = slot_ids;
+    a.q_dense = ws + L.q_dense;
+    a.lengths = reinterpret_cast<int64_t*>(ws + L.lengths);
+    a.mask = ws + L.mask;
+    a.slots = reinterpret_cast<int32_t*>(ws + L.slots);
+    a.ctx_dense = ws + L.ctx_dense;
+    a.out = out;
+    a.dev_status = dev_status;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    int recorded = 0;
+    auto record = [&]() -> cudaError_t {
+        if (events && recorded < n_events)
+            return cudaEventRecord(static_cast<cudaEvent_t>(events[recorded++]), stream);
+        return cudaSuccess;
+    };
+    cudaError_t e = record();
+    if (e == cudaSuccess && d.Q > 0) {
+        e = launch_attend_prep(a, stream);
+        if (e == cudaSuccess) e = record();
+    }
+    if (e != cudaSuccess) return KVC_E_CUDA;
+    if (d.Q > 0) {
+        // the dense step, read-only: its events continue from the last one
+        StepMode mode;
+        mode.inplace = true;
+        mode.readonly = true;
+        mode.rows = false;
+        mode.slot_ids = a.slots;
+        mode.cache_units = num_slots * d.Hk;
+        const int n_step = events ? std::max(0, std::min(n_events - (recorded - 1), 3)) : 0;
+        void* const* ev_step = events && recorded > 0 ? events + (recorded - 1) : nullptr;
+        rc = step_impl(&d, a.q_dense, key_cache, value_cache, key_cache, value_cache, a.lengths,
+                       a.mask, scale, const_cast<void*>(key_cache), const_cast<void*>(value_cache),
+                       reinterpret_cast<int64_t*>(ws + L.out_len), nullptr, ws + L.ctx_dense,
+                       workspace, L.step, dev_status, stream_ptr, ev_step, n_step, mode);
+        if (rc != KVC_OK) return rc;
+        recorded += std::max(0, n_step - 1);
+        e = launch_attend_unpack(a, stream);
+        if (e == cudaSuccess) e = record();
+    }
+    while (e == cudaSuccess && events && recorded < n_events) e = record();
+    return e == cudaSuccess ? KVC_OK : KVC_E_CUDA;
+}
 }  // namespace
 }  // namespace kvc
 
@@ -568,7 +712,7 @@ int kvc_step(const kvc_dims* dims, const void* query, const void* new_key, const
     return kvc::step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
                           append_mask, scale, out_key_cache, out_value_cache, out_lengths,
                           out_attention, out_context, workspace, workspace_bytes, dev_status,
-                          stream, nullptr, 0, false);
+                          stream, nullptr, 0, kvc::StepMode());
 }
 
 int kvc_step_timed(const kvc_dims* dims, const void* query, const void* new_key,
@@ -581,7 +725,7 @@ int kvc_step_timed(const kvc_dims* dims, const void* query, const void* new_key,
     return kvc::step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
                           append_mask, scale, out_key_cache, out_value_cache, out_lengths,
                           out_attention, out_context, workspace, workspace_bytes, dev_status,
-                          stream, events, n_events, false);
+                          stream, events, n_events, kvc::StepMode());
 }
 
 int kvc_step_inplace(const kvc_dims* dims, const void* query, const void* new_key,
@@ -592,7 +736,7 @@ int kvc_step_inplace(const kvc_dims* dims, const void* query, const void* new_ke
     return kvc::step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
                           append_mask, scale, key_cache, value_cache, out_lengths, out_attention,
                           out_context, workspace, workspace_bytes, dev_status, stream, nullptr, 0,
-                          true);
+                          kvc::inplace_mode());
 }
 
 int kvc_step_inplace_timed(const kvc_dims* dims, const void* query, const void* new_key,
@@ -604,7 +748,7 @@ int kvc_step_inplace_timed(const kvc_dims* dims, const void* query, const void* 
     return kvc::step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
                           append_mask, scale, key_cache, value_cache, out_lengths, out_attention,
                           out_context, workspace, workspace_bytes, dev_status, stream, events,
-                          n_events, true);
+                          n_events, kvc::inplace_mode());
 }
 
 int kvc_plan_info(const kvc_dims* dims, const void* key_cache, const void* value_cache,
@@ -637,6 +781,33 @@ int kvc_plan_info_inplace(const kvc_dims* dims, const void* key_cache, const voi
     if (rc < 0) return rc;
     // the cache write, then with query rows the step kernel, the merge and the row writer
     return dims->Q > 0 ? 4 : 1;
+}
+
+size_t kvc_attend_cache_workspace_bytes(const kvc_dims* dims) {
+    kvc::AttendLayout L;
+    if (!dims || kvc::check_dims(dims) != KVC_OK || !kvc::attend_layout(*dims, &L)) return 0;
+    return L.total;
+}
+
+int kvc_attend_cache(const kvc_dims* dims, int64_t num_slots, int64_t total_q, const void* q,
+                     const void* key_cache, const void* value_cache, const int32_t* cu_seqlens_q,
+                     const int32_t* seqlens_k, int k_cumulative, const int32_t* slot_ids,
+                     double scale, void* out, void* workspace, size_t workspace_bytes,
+                     int32_t* dev_status, void* stream) {
+    return kvc::attend_impl(dims, num_slots, total_q, q, key_cache, value_cache, cu_seqlens_q,
+                            seqlens_k, k_cumulative, slot_ids, scale, out, workspace,
+                            workspace_bytes, dev_status, stream, nullptr, 0);
+}
+
+int kvc_attend_cache_timed(const kvc_dims* dims, int64_t num_slots, int64_t total_q,
+                           const void* q, const void* key_cache, const void* value_cache,
+                           const int32_t* cu_seqlens_q, const int32_t* seqlens_k,
+                           int k_cumulative, const int32_t* slot_ids, double scale, void* out,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream, void* const* events, int n_events) {
+    return kvc::attend_impl(dims, num_slots, total_q, q, key_cache, value_cache, cu_seqlens_q,
+                            seqlens_k, k_cumulative, slot_ids, scale, out, workspace,
+                            workspace_bytes, dev_status, stream, events, n_events);
 }
 
 const char* kvc_status_string(int status) {

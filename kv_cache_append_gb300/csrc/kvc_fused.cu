@@ -70,8 +70,10 @@ __device__ void run_producer(const StepParams& p, unsigned char* smem, Bars bars
         const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, iend);
         if (i0 >= i1) continue;
         const bool attend = x.n > 0 && i0 * p.T < x.N;
-        const unsigned char* kcu = kc + u * p.M * rowK;
-        const unsigned char* vcu = vc + u * p.M * rowV;
+        const int64_t cu = cache_unit(p, u);
+        const unsigned char* kcu = kc + cu * p.M * rowK;
+        const unsigned char* vcu = vc + cu * p.M * rowV;
+        const int64_t Ls = p.readonly ? x.N : x.L;  // first slot sourced from the new rows
         const unsigned char* nku = nk + u * p.Q * rowK;
         const unsigned char* nvu = nv + u * p.Q * rowV;
         for (int64_t i = i0; i < i1; ++i) {
@@ -92,8 +94,8 @@ __device__ void run_producer(const StepParams& p, unsigned char* smem, Bars bars
             uint32_t bytes = static_cast<uint32_t>((j1 - j0) * (rowK + rowV));
             if (stage_q) bytes += static_cast<uint32_t>(p.q_stage_bytes);
             mbar_arrive_expect_tx(bars.full(ring.s), bytes);  // publishes the metadata too
-            load_rows(sK, kcu, nku, rowK, j0, j1, x.L, x.N, bars.full(ring.s));
-            load_rows(sK + vofs, vcu, nvu, rowV, j0, j1, x.L, x.N, bars.full(ring.s));
+            load_rows(sK, kcu, nku, rowK, j0, j1, Ls, x.N, bars.full(ring.s));
+            load_rows(sK + vofs, vcu, nvu, rowV, j0, j1, Ls, x.N, bars.full(ring.s));
             if (stage_q)  // the G*Q query rows of the unit are contiguous in query
                 bulk_g2s(sK + static_cast<uint32_t>(p.off_stage_q),
                          qry + (x.b * p.Hq + x.kv * p.G) * p.Q * rowK,

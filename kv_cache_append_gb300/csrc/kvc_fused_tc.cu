@@ -92,12 +92,14 @@ struct TmemCols {
         : o(2 * kTcT), q(2 * kTcT + Dv), p0(2 * kTcT + Dv + D / 2) {}
 };
 
-// Rows [a, c) of the tile starting at slot j0 must come from the new rows.
+// Rows [a, c) of the tile starting at slot j0 must come from the new rows
+// (none in read-only re-attention: the cache already holds them).
 struct PatchRange {
     int64_t a, c;
 };
-__device__ __forceinline__ PatchRange patch_range(const TileMeta& mt, int64_t M) {
-    const int64_t j0 = static_cast<int64_t>(mt.i) * kTcT, j1 = min(j0 + kTcT, M);
+__device__ __forceinline__ PatchRange patch_range(const TileMeta& mt, const StepParams& p) {
+    if (p.readonly) return PatchRange{0, 0};
+    const int64_t j0 = static_cast<int64_t>(mt.i) * kTcT, j1 = min(j0 + kTcT, p.M);
     const int64_t N = mt.L + mt.n;
     return PatchRange{max(mt.L, j0), min(N, j1)};
 }
@@ -146,7 +148,7 @@ __device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars
             const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
             const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBox);
             mbar_arrive_expect_tx(bars.full(ring.s), tile_bytes);  // publishes the metadata too
-            const int y = static_cast<int>(i * kTcT), z = static_cast<int>(u);
+            const int y = static_cast<int>(i * kTcT), z = static_cast<int>(cache_unit(p, u));
             for (int b = 0; b < nkb; ++b)
                 tma_load_3d(sK + b * kBox, &tp.tm_k, 64 * b, y, z, bars.full(ring.s));
             for (int b = 0; b < nvb; ++b)
@@ -191,7 +193,7 @@ __device__ void tc_storer(const TcParams& tp, unsigned char* smem, TcBars bars,
         unsigned char* tK = smem + p.off_stages + static_cast<int64_t>(ring.s) * p.stage_bytes;
         unsigned char* tV = tK + nkb * kBox;
         const int64_t j0 = static_cast<int64_t>(mt.i) * kTcT;
-        const PatchRange pr = patch_range(mt, p.M);
+        const PatchRange pr = patch_range(mt, p);
         if (pr.c > pr.a) {
             const int rows = static_cast<int>(pr.c - pr.a);
             const unsigned char* nku = nk + (mt.u * p.Q + (pr.a - mt.L)) * rowK;
@@ -297,7 +299,7 @@ __device__ void tc_mma_issuer(const TcParams& tp, unsigned char* smem, TcBars ba
         }
         const bool comp = attend && static_cast<int64_t>(mt.i) * kTcT < N;
         // consume every patched phase the storer produces on this stage
-        const PatchRange pr = patch_range(mt, p.M);
+        const PatchRange pr = patch_range(mt, p);
         if (pr.c > pr.a) {
             if (!mbar_wait(bars.patched(s), (pbits >> s) & 1u, abort)) break;
             pbits ^= 1u << s;

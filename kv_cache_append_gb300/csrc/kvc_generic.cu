@@ -58,11 +58,14 @@ __global__ void __launch_bounds__(kAttendWarps * 32)
     const int64_t kv = h / p.G, u = b * p.Hk + kv, r = (h % p.G) * p.Q + t;
     const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
     if (t >= ra.n) return;  // invalid row: kvc_finalize.cu writes zeros
-    const int64_t L = ra.L, N = ra.L + ra.n, lim = L + t;
+    const int64_t lim = ra.L + t;
+    // slots [L, N) come from the new rows (none in read-only re-attention)
+    const int64_t L = p.readonly ? ra.L + ra.n : ra.L, N = ra.L + ra.n;
+    const int64_t cu = cache_unit(p, u);
     const T* q = static_cast<const T*>(p.query) + row * p.D;
-    const T* kc = static_cast<const T*>(p.key_cache) + u * p.M * p.D;
+    const T* kc = static_cast<const T*>(p.key_cache) + cu * p.M * p.D;
     const T* nk = static_cast<const T*>(p.new_key) + u * p.Q * p.D;
-    const T* vc = static_cast<const T*>(p.value_cache) + u * p.M * p.Dv;
+    const T* vc = static_cast<const T*>(p.value_cache) + cu * p.M * p.Dv;
     const T* nv = static_cast<const T*>(p.new_value) + u * p.Q * p.Dv;
     float* sc = p.scores + row * p.M;
 

@@ -487,9 +487,22 @@ struct StepParams {
     // step kernels read only the tiles below each unit's new length and store
     // nothing; inplace_rows_kernel writes the appended rows and the lengths.
     int inplace;
+    // 1 (with inplace): read-only re-attention. Every slot below the new
+    // length comes from the cache (no new rows are sourced or patched), and
+    // unit (b, kv) reads cache unit slot_ids[b] * Hk + kv.
+    int readonly;
+    const int32_t* slot_ids;  // [B] cache row per batch row; NULL: row b
     int64_t fin_seg;    // attention slots per row-writer block (a multiple of 8)
     int64_t fin_nseg;   // row-writer blocks per query row: ceil(M / fin_seg)
     RowStat* rowstat;   // [B][Hq][Q]: the merged maximum, 1 / sum and last allowed slot
 };
+
+// The cache unit that unit u = b * Hk + kv reads.
+__device__ __forceinline__ int64_t cache_unit(const StepParams& p, int64_t u) {
+    if (!p.slot_ids) return u;
+    const int64_t b = u / p.Hk;
+    return static_cast<int64_t>(p.slot_ids[b]) * p.Hk + (u - b * p.Hk);
+}
+
 
 }  // namespace kvc

@@ -41,6 +41,26 @@ cudaError_t launch_finalize_rows(const StepParams& p, int dtype, cudaStream_t st
 // the caches and new rows are 16-byte aligned.
 cudaError_t launch_inplace_rows(const StepParams& p, bool words16, cudaStream_t stream);
 
+// Read-only re-attention: packed queries to the dense step view and the
+// context back (kvc_attend.cu). Q is the largest query count per sequence.
+struct AttendParams {
+    int64_t B, Hq, Hk, Q, D, Dv, M, num_slots, total_q;
+    int es, k_cumulative;
+    const void* q;              // [total_q, Hq, D]
+    const int32_t* cu_q;        // [B + 1]
+    const int32_t* seqlens_k;   // [B], or [B + 1] cumulative
+    const int32_t* slot_ids;    // [B] or NULL
+    void* q_dense;              // [B, Hq, Q, D]
+    int64_t* lengths;           // [B]  K_b - S_b
+    uint8_t* mask;              // [B, Q]
+    int32_t* slots;             // [B]
+    const void* ctx_dense;      // [B, Hq, Q, Dv]
+    void* out;                  // [total_q, Hq, Dv]
+    int32_t* dev_status;
+};
+cudaError_t launch_attend_prep(const AttendParams& a, cudaStream_t stream);
+cudaError_t launch_attend_unpack(const AttendParams& a, cudaStream_t stream);
+
 // Generic path for shapes or alignments the fused kernel does not take
 // (kvc_generic.cu): copy + scatter, then attention partials.
 cudaError_t launch_generic_copy(const StepParams& p, int dtype, cudaStream_t stream);

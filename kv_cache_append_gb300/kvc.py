@@ -82,6 +82,15 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kvc_step_inplace_timed.argtypes = inplace_args + [ctypes.POINTER(vp), i32]
             lib.kvc_plan_info_inplace.restype = i32
             lib.kvc_plan_info_inplace.argtypes = [dp] + [vp] * 4 + [ctypes.POINTER(ctypes.c_char_p)]
+            i64 = ctypes.c_int64
+            attend_args = ([dp, i64, i64] + [vp] * 5 + [i32, vp, ctypes.c_double, vp, vp, sz, vp,
+                                                         vp])
+            lib.kvc_attend_cache_workspace_bytes.restype = sz
+            lib.kvc_attend_cache_workspace_bytes.argtypes = [dp]
+            lib.kvc_attend_cache.restype = i32
+            lib.kvc_attend_cache.argtypes = attend_args
+            lib.kvc_attend_cache_timed.restype = i32
+            lib.kvc_attend_cache_timed.argtypes = attend_args + [ctypes.POINTER(vp), i32]
             lib.kvc_status_string.restype = ctypes.c_char_p
             lib.kvc_status_string.argtypes = [i32]
             lib.kvc_version.restype = i32
@@ -322,4 +331,80 @@ def kv_cache_attention_step_inplace(query: torch.Tensor, new_key: torch.Tensor,
     ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
     with torch.cuda.device(q.device):
         step_inplace_into(dims, q, nk, nv, key_cache, value_cache, ln, mk, scale, out, ws, status)
+    return out
+
+
+def attend_cache_workspace_bytes(dims: Dims) -> int:
+    return int(library().kvc_attend_cache_workspace_bytes(ctypes.byref(dims)))
+
+
+def attend_cache_into(dims: Dims, num_slots: int, q, key_cache, value_cache, cu_seqlens_q,
+                      seqlens_k, k_cumulative: bool, slot_ids, scale: float, out,
+                      workspace: torch.Tensor, status: Optional[torch.Tensor] = None,
+                      stream: Optional[int] = None, events: Optional[Sequence] = None) -> None:
+    """Enqueue one kvc_attend_cache (no checks beyond libkvc's)."""
+    lib = library()
+    if stream is None:
+        stream = torch.cuda.current_stream(key_cache.device).cuda_stream
+    ws_len = workspace.numel() * workspace.element_size()
+    args = [ctypes.byref(dims), int(num_slots), int(q.shape[0]), _p(q), _p(key_cache),
+            _p(value_cache), _p(cu_seqlens_q), _p(seqlens_k), int(bool(k_cumulative)),
+            _p(slot_ids), ctypes.c_double(scale), _p(out), _p(workspace), ws_len, _p(status),
+            ctypes.c_void_p(stream)]
+    if events:
+        handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+        rc = lib.kvc_attend_cache_timed(*args, handles, len(events))
+    else:
+        rc = lib.kvc_attend_cache(*args)
+    if rc != KVC_OK:
+        raise KvcError(rc, status_string(rc))
+
+
+def attention_over_cache(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                         cu_seqlens_q: torch.Tensor, seqlens_k: torch.Tensor,
+                         slot_ids: Optional[torch.Tensor] = None,
+                         max_seqlen_q: Optional[int] = None, scale: Optional[float] = None,
+                         status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Read-only re-attention of packed queries over an appended cache.
+
+    q [total_q, Hq, D]; key_cache [num_slots, Hk, M, D] and value_cache
+    [num_slots, Hk, M, Dv] (never written); cu_seqlens_q [B + 1] packing
+    offsets; seqlens_k each sequence's total cached length, [B] or cumulative
+    [B + 1]; slot_ids [B] cache row per sequence (default row b). Query t of a
+    sequence with S queries and K cached positions attends slots
+    j <= K - S + t. Returns out [total_q, Hq, Dv]. ``max_seqlen_q`` (the
+    largest S) is read from cu_seqlens_q when not given (a device sync).
+    """
+    for name, t in (("q", q), ("key_cache", key_cache), ("value_cache", value_cache)):
+        if t.dtype not in DTYPES or t.dtype != q.dtype:
+            raise ValueError(f"{name}: one dtype among float32/bfloat16/float16 is needed")
+        if t.device.type != "cuda" or t.device != q.device:
+            raise ValueError("attention_over_cache runs on one CUDA device only (no CPU path)")
+    if q.dim() != 3 or key_cache.dim() != 4 or value_cache.dim() != 4:
+        raise ValueError("q is [total_q, Hq, D]; the caches are [num_slots, Hk, M, D|Dv]")
+    total_q, Hq, D = q.shape
+    num_slots, Hk, M, Dk = key_cache.shape
+    if Dk != D or tuple(value_cache.shape[:3]) != (num_slots, Hk, M):
+        raise ValueError("cache shapes do not match q")
+    B = cu_seqlens_q.numel() - 1
+    if B < 1 or seqlens_k.numel() not in (B, B + 1):
+        raise ValueError("cu_seqlens_q is [B + 1]; seqlens_k is [B] or cumulative [B + 1]")
+    if Hq % Hk:
+        raise ValueError("Hq must be a multiple of Hk")
+    if scale is None:
+        scale = default_scale(D)
+    if max_seqlen_q is None:
+        max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B else 0
+    Dv = value_cache.shape[-1]
+    dims = make_dims(B, Hq, Hk, max(1, int(max_seqlen_q)), D, Dv, M, q.dtype)
+    cu = cu_seqlens_q.to(device=q.device, dtype=torch.int32).contiguous()
+    kl = seqlens_k.to(device=q.device, dtype=torch.int32).contiguous()
+    sl = None if slot_ids is None else slot_ids.to(device=q.device,
+                                                   dtype=torch.int32).contiguous()
+    out = torch.empty(total_q, Hq, Dv, dtype=q.dtype, device=q.device)
+    ws = torch.empty(attend_cache_workspace_bytes(dims), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        attend_cache_into(dims, num_slots, q.contiguous(), key_cache.contiguous(),
+                          value_cache.contiguous(), cu, kl, seqlens_k.numel() == B + 1, sl,
+                          float(scale), out, ws, status)
     return out

@@ -125,3 +125,31 @@ def test_inplace_argument_errors_return_before_any_launch(lib):
     assert _call_inplace(lib, _dims(), null=("ol",)) == -1
     assert _call_inplace(lib, _dims(), null=("q",)) == -1
     assert _call_inplace(lib, _dims(), scale=0.0) == -4     # KVC_E_SCALE
+
+
+def test_attend_cache_workspace_and_argument_errors(lib):
+    d = _dims(Q=4)
+    ws = lib.kvc_attend_cache_workspace_bytes(ctypes.byref(d))
+    assert ws >= kvc.workspace_bytes(d) + 2 * 4 * 4 * (16 + 16) * 4
+    assert lib.kvc_attend_cache_workspace_bytes(ctypes.byref(_dims(Hq=3))) == 0
+    p = [ctypes.c_void_p(4096 * (i + 1)) for i in range(8)]
+
+    def call(dims, num_slots=4, total_q=5, scale=0.5, null=(), k_cum=0):
+        a = list(p)
+        for i in null:
+            a[i] = None
+        # q, key_cache, value_cache, cu_q, seqlens_k, slot_ids, out, workspace
+        return lib.kvc_attend_cache(ctypes.byref(dims) if dims is not None else None,
+                                    num_slots, total_q, a[0], a[1], a[2], a[3], a[4], k_cum,
+                                    a[5], ctypes.c_double(scale), a[6], a[7], 1 << 30, None,
+                                    None)
+    assert call(None) == -1                       # KVC_E_NULL
+    assert call(_dims(Hq=3)) == -2                # KVC_E_SHAPE
+    assert call(d, num_slots=0) == -2
+    assert call(d, total_q=-1) == -2
+    assert call(d, k_cum=2) == -2
+    assert call(d, num_slots=1, null=(5,)) == -2  # identity slots need num_slots >= B
+    assert call(d, null=(1,)) == -1               # key_cache
+    assert call(d, null=(0,)) == -1               # q
+    assert call(d, null=(6,)) == -1               # out
+    assert call(d, scale=-2.0) == -4              # KVC_E_SCALE
