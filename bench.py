@@ -48,6 +48,10 @@ PATH_KERNELS_INPLACE = {
                "finalize_rows_kernel"],
     "generic": ["inplace_rows_kernel", "generic_attend_kernel", "finalize_merge_kernel",
                 "finalize_rows_kernel"]}
+PATH_KERNELS_READONLY = {
+    path: ["attend_prep_kernel", STEP_KERNEL[path] if path != "generic" else "generic_attend_kernel",
+           "finalize_merge_kernel", "attend_unpack_kernel"]
+    for path in ("fused", "tensor", "generic")}
 PATH_KERNELS = {"fused": ["fused_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "tensor": ["tc_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "generic": ["generic_copy_kernel", "generic_attend_kernel",
@@ -95,6 +99,22 @@ def algorithmic_bytes_inplace(spec: workloads.Spec, lengths, counts) -> dict:
     step = prefix + qkv + small
     return {"total": step + appended + att + ctx, "fused_kernel": step,
             "finalize_kernel": att + ctx}
+
+
+def algorithmic_bytes_readonly(spec: workloads.Spec, lengths, counts) -> dict:
+    """Bytes the read-only re-attention must move at minimum: each sequence's
+    cached prefix (K_b = L_b + n_b slots per KV head) read, its n_b packed
+    query rows read and output rows written, and the per-sequence offsets,
+    lengths and slots."""
+    es = 4 if spec.dtype == "f32" else 2
+    B = len(lengths)
+    K = int(sum(lengths)) + int(sum(counts))
+    tq = int(sum(counts))
+    prefix = K * spec.Hk * (spec.D + spec.Dv) * es
+    step = prefix + tq * spec.Hq * spec.D * es + (B + 1) * 4 + B * 8
+    out = tq * spec.Hq * spec.Dv * es
+    return {"total": step + out, "fused_kernel": prefix + tq * spec.Hq * spec.D * es,
+            "finalize_kernel": out}
 
 
 def source_digest(paths) -> str:
@@ -262,9 +282,10 @@ def run_reference(args, spec, world, rank):
     for _ in range(args.steps):
         oracle.step(*sub, x.options)
     dt = (time.perf_counter() - t0) / args.steps
-    if args.inplace:  # the same step, counted with the in-place method's bytes
-        nbytes = algorithmic_bytes_inplace(spec, x.lengths[:rows].tolist(),
-                                           x.append_mask[:rows].to(torch.int64).sum(1).tolist())["total"]
+    if args.inplace or args.readonly:  # the same attention, counted with that face's bytes
+        f = algorithmic_bytes_readonly if args.readonly else algorithmic_bytes_inplace
+        nbytes = f(spec, x.lengths[:rows].tolist(),
+                   x.append_mask[:rows].to(torch.int64).sum(1).tolist())["total"]
     else:
         nbytes = algorithmic_bytes(spec, rows)["total"]
     value = nbytes / dt / 1e9
@@ -309,7 +330,31 @@ def run_ours(args, spec, world, rank, local):
     nws = kvc.workspace_bytes(dims)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
     stream = torch.cuda.current_stream(dev)
-    if args.inplace:
+    if args.readonly:
+        # packed queries = the step's valid query rows; each sequence's cached
+        # length = its new length; cache rows visited through a permutation
+        counts_d = x.append_mask.to(torch.int64).sum(1)
+        Bn = spec.B
+        rows_q = [q[b, :, :int(counts_d[b])].permute(1, 0, 2) for b in range(Bn)]
+        q_packed = torch.cat(rows_q, 0).contiguous()
+        cu = torch.zeros(Bn + 1, dtype=torch.int32, device=dev)
+        cu[1:] = torch.cumsum(counts_d, 0).to(torch.int32)
+        kl = (x.lengths + counts_d).to(torch.int32)
+        g = torch.Generator().manual_seed(11 + rank)
+        perm = torch.randperm(Bn, generator=g)
+        kc_p, vc_p = kc[perm].contiguous(), vc[perm].contiguous()   # sequence b in row inv[b]
+        slots = torch.argsort(perm).to(torch.int32).to(dev)
+        del out
+        out_ro = torch.empty(q_packed.shape[0], spec.Hq, spec.Dv, dtype=q.dtype, device=dev)
+        ws = torch.empty(kvc.attend_cache_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+        torch.cuda.empty_cache()
+        nkern = 4
+        path = kvc.plan_info(dims, kc_p, vc_p, nk, nv, kc_p, vc_p)[1]
+
+        def step(events=None):
+            kvc.attend_cache_into(dims, Bn, q_packed, kc_p, vc_p, cu, kl, False, slots, scale,
+                                  out_ro, ws, None, stream.cuda_stream, events)
+    elif args.inplace:
         # donated caches: every step appends the same rows at the same slots,
         # so repeated steps leave the caches as the first one did
         nkern, path = kvc.plan_info_inplace(dims, kc, vc, nk, nv)
@@ -359,19 +404,24 @@ def run_ours(args, spec, world, rank, local):
 
     lengths_h = x.lengths.cpu().tolist()
     counts_h = x.append_mask.to(torch.int64).sum(1).cpu().tolist()
-    nbytes = (algorithmic_bytes_inplace(spec, lengths_h, counts_h) if args.inplace
+    nbytes = (algorithmic_bytes_readonly(spec, lengths_h, counts_h) if args.readonly else
+              algorithmic_bytes_inplace(spec, lengths_h, counts_h) if args.inplace
               else algorithmic_bytes(spec))
     value = world * nbytes["total"] / (ms_step * 1e-3) / 1e9
     peak, peak_src = measured_peak()
-    ks = 1 if args.inplace and nkern > 1 else 0  # index of the step kernel
+    ks = 1 if (args.inplace or args.readonly) and nkern > 1 else 0  # index of the step kernel
     fused_ms = kern_ms[ks]
     achieved = nbytes["fused_kernel"] / (fused_ms * 1e-3) / 1e9
     kname = STEP_KERNEL[path]
-    traffic = None if args.inplace else kernel_traffic(args.workload, kname)
+    if args.readonly and path == "generic":
+        kname = "generic_attend_kernel"
+    traffic = None if (args.inplace or args.readonly) else kernel_traffic(args.workload, kname)
 
     # ---- end to end through the public API: pinned host in, pinned host out
     e2e = None
-    if not args.no_e2e:
+    if args.readonly:
+        e2e = None  # the read-only face has no host-buffer leg here
+    elif not args.no_e2e:
         e2e = (measure_e2e_inplace(kvc, x, dev, max(3, min(args.steps, 10)), nbytes["total"],
                                    world) if args.inplace else
                measure_e2e(kvc, x, dev, spec, max(3, min(args.steps, 10)), nbytes["total"], world))
@@ -381,11 +431,15 @@ def run_ours(args, spec, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xc = cpu_inputs(spec, seed=1)
         dt, rows, threads = oracle_sample(spec, xc, args.cpu_budget)
-        sample_bytes = (algorithmic_bytes_inplace(spec, lengths_h[:rows], counts_h[:rows])
+        sample_bytes = (algorithmic_bytes_readonly(spec, lengths_h[:rows], counts_h[:rows])
+                        if args.readonly else
+                        algorithmic_bytes_inplace(spec, lengths_h[:rows], counts_h[:rows])
                         if args.inplace else algorithmic_bytes(spec, rows))
         cpu = {"value": round(sample_bytes["total"] / dt / 1e9, 4),
                "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"first {rows} of {spec.B} batch rows of {args.workload}, one step"}
+               "sample": f"first {rows} of {spec.B} batch rows of {args.workload}, one step"
+                         + (" (the oracle's step: the same attention plus the cache copy)"
+                            if args.readonly else "")}
 
     if rank != 0:
         return
@@ -410,16 +464,21 @@ def run_ours(args, spec, world, rank, local):
         "gpu_launches": nkern * args.steps,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
-    names = (PATH_KERNELS_INPLACE if args.inplace else PATH_KERNELS)[path]
+    names = (PATH_KERNELS_READONLY if args.readonly else
+             PATH_KERNELS_INPLACE if args.inplace else PATH_KERNELS)[path]
     for k in range(nkern):
         if k != ks:
             line["kernels"][names[k]] = {"ms": round(kern_ms[k], 4)}
     if args.inplace:
         line["config"]["mode"] = ("in place: donated caches, only the appended rows written, "
                                   "the attention reads the valid prefix")
+    if args.readonly:
+        line["config"]["mode"] = ("read-only re-attention: packed queries (the step's valid "
+                                  "rows) over the cached prefix through a slot permutation; "
+                                  "context only, no attention rows, cache not written")
     if nkern > 2:
         fin_ms = kern_ms[-1] + kern_ms[-2]
-        line["kernels"]["finalize (merge + rows)"] = {
+        line["kernels"]["merge + unpack" if args.readonly else "finalize (merge + rows)"] = {
             "ms": round(fin_ms, 4),
             "algorithmic_GBps": round(nbytes["finalize_kernel"] / (fin_ms * 1e-3) / 1e9, 1)}
     print(json.dumps(line), flush=True)
@@ -514,6 +573,8 @@ def main():
                     help="override the workload's dtype (the fp32 chunked append)")
     ap.add_argument("--inplace", action="store_true",
                     help="time kvc_step_inplace (donated caches updated in place)")
+    ap.add_argument("--readonly", action="store_true",
+                    help="time kvc_attend_cache (read-only re-attention over the cache)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

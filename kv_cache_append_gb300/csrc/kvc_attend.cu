@@ -8,7 +8,7 @@
 // j <= K_b - S_b + t: exactly the attention of the append step with old
 // length K_b - S_b and S_b appended rows, the cache already holding them.
 // These kernels map the packed face onto that dense step view and back:
-//   attend_prep_kernel    per sequence: the contract check (S_b <= Qmax,
+//   attend_prep_kernel    per (sequence, query head): the contract check (S_b <= Qmax,
 //                         S_b <= K_b <= M, slot in range), lengths K_b - S_b,
 //                         a mask of S_b leading True, the slot, and the query
 //                         rows gathered into [B, Hq, Qmax, D] (zeros past S_b);
@@ -43,51 +43,63 @@ __device__ __forceinline__ SeqInfo seq_info(const AttendParams& a, int64_t b) {
     return s;
 }
 
+// One CTA per (sequence b, query head h); Word is the unit each thread
+// moves (16 bytes when rows and pointers allow, else 2 bytes).
+template <typename Word>
 __global__ void __launch_bounds__(kPackThreads) attend_prep_kernel(const __grid_constant__ AttendParams a) {
-    const int64_t b = blockIdx.x;
+    const int64_t b = blockIdx.x / a.Hq, h = blockIdx.x - b * a.Hq;
     const SeqInfo s = seq_info(a, b);
-    if (threadIdx.x == 0) {
-        a.lengths[b] = s.bad ? 0 : s.K - s.S;
-        a.slots[b] = s.bad ? 0 : static_cast<int32_t>(s.slot);
-        if (s.bad && a.dev_status) atomicOr(a.dev_status, KVC_DEV_OVERFLOW);
+    if (h == 0) {
+        if (threadIdx.x == 0) {
+            a.lengths[b] = s.bad ? 0 : s.K - s.S;
+            a.slots[b] = s.bad ? 0 : static_cast<int32_t>(s.slot);
+            if (s.bad && a.dev_status) atomicOr(a.dev_status, KVC_DEV_OVERFLOW);
+        }
+        for (int64_t t = threadIdx.x; t < a.Q; t += kPackThreads)
+            a.mask[b * a.Q + t] = (!s.bad && t < s.S) ? 1 : 0;
     }
-    for (int64_t t = threadIdx.x; t < a.Q; t += kPackThreads)
-        a.mask[b * a.Q + t] = (!s.bad && t < s.S) ? 1 : 0;
-    const int64_t w = a.D * a.es / 2;  // 16-bit words per query row
-    const uint16_t* src = static_cast<const uint16_t*>(a.q);
-    uint16_t* dst = static_cast<uint16_t*>(a.q_dense);
-    for (int64_t i = threadIdx.x; i < a.Hq * a.Q * w; i += kPackThreads) {
-        const int64_t h = i / (a.Q * w), rem = i - h * a.Q * w;
-        const int64_t t = rem / w, c = rem - t * w;
-        dst[((b * a.Hq + h) * a.Q + t) * w + c] =
-            (!s.bad && t < s.S) ? src[((s.q0 + t) * a.Hq + h) * w + c] : uint16_t(0);
+    const int64_t w = a.D * a.es / static_cast<int64_t>(sizeof(Word));  // words per query row
+    const Word* src = static_cast<const Word*>(a.q);
+    Word* dst = static_cast<Word*>(a.q_dense) + (b * a.Hq + h) * a.Q * w;
+    for (int64_t i = threadIdx.x; i < a.Q * w; i += kPackThreads) {
+        const int64_t t = i / w, c = i - t * w;
+        dst[i] = (!s.bad && t < s.S) ? src[((s.q0 + t) * a.Hq + h) * w + c] : Word{};
     }
 }
 
+template <typename Word>
 __global__ void __launch_bounds__(kPackThreads) attend_unpack_kernel(const __grid_constant__ AttendParams a) {
-    const int64_t b = blockIdx.x;
+    const int64_t b = blockIdx.x / a.Hq, h = blockIdx.x - b * a.Hq;
     const SeqInfo s = seq_info(a, b);
     if (!s.rows_ok) return;  // its rows cannot be located in out
-    const int64_t w = a.Dv * a.es / 2;  // 16-bit words per context row
-    const uint16_t* src = static_cast<const uint16_t*>(a.ctx_dense);
-    uint16_t* dst = static_cast<uint16_t*>(a.out);
-    for (int64_t i = threadIdx.x; i < s.S * a.Hq * w; i += kPackThreads) {
-        const int64_t t = i / (a.Hq * w), rem = i - t * a.Hq * w;
-        const int64_t h = rem / w, c = rem - h * w;
-        dst[((s.q0 + t) * a.Hq + h) * w + c] =
-            s.bad ? uint16_t(0) : src[((b * a.Hq + h) * a.Q + t) * w + c];
+    const int64_t w = a.Dv * a.es / static_cast<int64_t>(sizeof(Word));  // words per context row
+    const Word* src = static_cast<const Word*>(a.ctx_dense) + (b * a.Hq + h) * a.Q * w;
+    Word* dst = static_cast<Word*>(a.out);
+    for (int64_t i = threadIdx.x; i < s.S * w; i += kPackThreads) {
+        const int64_t t = i / w, c = i - t * w;
+        dst[((s.q0 + t) * a.Hq + h) * w + c] = s.bad ? Word{} : src[i];
     }
 }
+
+bool aligned16p(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
 cudaError_t launch_attend_prep(const AttendParams& a, cudaStream_t stream) {
-    attend_prep_kernel<<<static_cast<unsigned>(a.B), kPackThreads, 0, stream>>>(a);
+    const dim3 grid(static_cast<unsigned>(a.B * a.Hq));
+    if ((a.D * a.es) % 16 == 0 && aligned16p(a.q) && aligned16p(a.q_dense))
+        attend_prep_kernel<uint4><<<grid, kPackThreads, 0, stream>>>(a);
+    else
+        attend_prep_kernel<uint16_t><<<grid, kPackThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_attend_unpack(const AttendParams& a, cudaStream_t stream) {
-    attend_unpack_kernel<<<static_cast<unsigned>(a.B), kPackThreads, 0, stream>>>(a);
+    const dim3 grid(static_cast<unsigned>(a.B * a.Hq));
+    if ((a.Dv * a.es) % 16 == 0 && aligned16p(a.out) && aligned16p(a.ctx_dense))
+        attend_unpack_kernel<uint4><<<grid, kPackThreads, 0, stream>>>(a);
+    else
+        attend_unpack_kernel<uint16_t><<<grid, kPackThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
