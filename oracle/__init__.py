@@ -179,6 +179,72 @@ class Oracle:
         return out, flags
 
 
+    def step_paged(self, query, new_key, new_value, key_pool, value_pool, block_table,
+                   lengths, append_mask, options: dict | None = None) -> dict:
+        """The step on a paged block pool ("ClikaRT::ops::attention_over_cache":
+        a paged block pool [num_blocks, H_kv, block_size, D] with a rank-2
+        [B, max_blocks] block table). Batch row b's logical cache slot j lives in
+        block block_table[b, j // block_size], row j % block_size; its capacity
+        is M = max_blocks * block_size. By definition the step on the pool is the
+        step (kvo_step) on each row's logical cache, gathered through the table,
+        with the updated rows written back through it: the gather and scatter are
+        plain indexing, the step is the pinned one. A row whose table entries for
+        the blocks it would touch (slots [0, length + n)) fall outside
+        [0, num_blocks) appends nothing, gets zero query rows and flag 1, like a
+        capacity overflow. Blocks not written keep their bytes.
+
+        Returns the pool after the step (key_pool, value_pool), lengths,
+        attention [B,Hq,Q,M], context [B,Hq,Q,Dv] (float64) and flags [B].
+        """
+        kp, vp = _host(key_pool), _host(value_pool)
+        table = _host(block_table).to(torch.int64)
+        num_blocks, Hk, bs, D = kp.shape
+        Dv = vp.shape[-1]
+        B, max_blocks = table.shape
+        M = max_blocks * bs
+        ln = _host(lengths).to(torch.int64)
+        mk = _host(append_mask).to(torch.bool)
+        Q = mk.shape[1]
+        # rows whose needed blocks are outside the pool: append nothing (n = 0)
+        n_pref = torch.zeros(B, dtype=torch.int64)
+        for b in range(B):
+            n = 0
+            while n < Q and bool(mk[b, n]):
+                n += 1
+            n_pref[b] = n
+        bad = torch.zeros(B, dtype=torch.bool)
+        for b in range(B):
+            L, n = int(ln[b]), int(n_pref[b])
+            if L < 0 or L + n > M or bool(mk[b, n:].any()):
+                continue  # outside the step's contract: the step flags them and appends nothing
+            last = (L + n + bs - 1) // bs if n > 0 else 0
+            if last and bool(((table[b, :last] < 0) | (table[b, :last] >= num_blocks)).any()):
+                bad[b] = True
+        mk_eff = mk.clone()
+        mk_eff[bad] = False
+        # gather each row's logical cache (blocks outside the pool read as zeros; never used)
+        safe = table.clamp(0, num_blocks - 1)
+        kc = kp[safe].permute(0, 2, 1, 3, 4).reshape(B, Hk, M, D)
+        vc = vp[safe].permute(0, 2, 1, 3, 4).reshape(B, Hk, M, Dv)
+        ref = self.step(query, new_key, new_value, kc, vc, ln, mk_eff, options)
+        ref["flags"] = ref["flags"] | np.where(bad.numpy(), 1, 0).astype(np.int32)
+        # write back only the appended rows, through the table
+        out_k, out_v = kp.clone(), vp.clone()
+        nk_, nv_ = _host(new_key), _host(new_value)
+        counts = mk_eff.to(torch.int64).cumprod(1).sum(1)
+        for b in range(B):
+            L, n = int(ln[b]), int(counts[b])
+            if ref["flags"][b] or n == 0:
+                continue
+            for t in range(n):
+                j = L + t
+                blk, row = int(table[b, j // bs]), j % bs
+                out_k[blk, :, row] = nk_[b, :, t]
+                out_v[blk, :, row] = nv_[b, :, t]
+        ref["key_cache"], ref["value_cache"] = out_k, out_v
+        return ref
+
+
 _lock = threading.Lock()
 _default: Oracle | None = None
 
@@ -205,6 +271,10 @@ def step(*args, **kw):
 
 def attend_cache(*args, **kw):
     return default().attend_cache(*args, **kw)
+
+
+def step_paged(*args, **kw):
+    return default().step_paged(*args, **kw)
 
 
 def rows(*args, **kw):

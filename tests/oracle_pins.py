@@ -544,6 +544,77 @@ def pin_attend_cache_outside_contract(o):
     np.testing.assert_allclose(out[5:], 1.0, rtol=0, atol=1e-15)
 
 
+# ---------------------------------------------------------------- [paged]
+def _to_pool(cache, perm, max_blocks, bs):
+    """[B, Hk, M, W] logical caches as a pool whose block perm[b*max_blocks + i]
+    holds block i of row b; returns (pool, table)."""
+    B, Hk, M, W = cache.shape
+    blocks = cache.reshape(B, Hk, max_blocks, bs, W).permute(0, 2, 1, 3, 4).reshape(
+        B * max_blocks, Hk, bs, W)
+    pool = torch.empty_like(blocks)
+    pool[perm] = blocks
+    table = perm.reshape(B, max_blocks).to(torch.int32)
+    return pool, table
+
+
+def _from_pool(pool, table):
+    B, max_blocks = table.shape
+    nb, Hk, bs, W = pool.shape
+    return pool[table.long()].permute(0, 2, 1, 3, 4).reshape(B, Hk, max_blocks * bs, W)
+
+
+def pin_paged_equals_contiguous_step(o):
+    """[paged] + [contract]: on any block placement, the paged step gives the
+    contiguous step's attention, context and lengths, and the pool read back
+    through the table is the contiguous step's updated cache."""
+    from workloads import Spec
+    for dtype, seed, bs in (("f32", 0, 4), ("bf16", 1, 8), ("f16", 2, 16)):
+        spec = Spec(B=3, Hq=4, Hk=2, Q=3, D=8, Dv=4, M=48, dtype=dtype,
+                    counts=("uniform", 0, 3))
+        x = workloads.generate(spec, seed)
+        ref = o.step(*x.args(), x.options)
+        mb = spec.M // bs
+        perm = torch.randperm(spec.B * mb, generator=torch.Generator().manual_seed(seed))
+        kp, table = _to_pool(x.key_cache, perm, mb, bs)
+        vp, _ = _to_pool(x.value_cache, perm, mb, bs)
+        got = o.step_paged(x.query, x.new_key, x.new_value, kp, vp, table,
+                                     x.lengths, x.append_mask, x.options)
+        np.testing.assert_array_equal(got["attention"], ref["attention"])
+        np.testing.assert_array_equal(got["context"], ref["context"])
+        assert torch.equal(got["lengths"], ref["lengths"])
+        assert torch.equal(_from_pool(got["key_cache"], table), ref["key_cache"])
+        assert torch.equal(_from_pool(got["value_cache"], table), ref["value_cache"])
+
+
+def pin_paged_bad_block_ids_append_nothing(o):
+    """[paged]: a row whose needed table entries fall outside the pool appends
+    nothing, has zero query rows and is flagged; blocks outside every row's
+    table keep their bytes; the other rows are unaffected."""
+    from workloads import Spec
+    spec = Spec(B=3, Hq=2, Hk=1, Q=2, D=4, Dv=4, M=16, dtype="f32", counts=("fixed", 2),
+                lengths=("fixed", 5))
+    x = workloads.generate(spec, 3)
+    bs, mb = 4, 4
+    perm = torch.arange(spec.B * mb) + 2            # blocks 0 and 1 belong to nobody
+    kp, table = _to_pool(x.key_cache, perm - 2, mb, bs)
+    kp = torch.cat([torch.full((2, 1, bs, 4), 7.0), kp]).contiguous()
+    vp, _ = _to_pool(x.value_cache, perm - 2, mb, bs)
+    vp = torch.cat([torch.full((2, 1, bs, 4), 7.0), vp]).contiguous()
+    table = perm.reshape(spec.B, mb).to(torch.int32)
+    table[1, 1] = 99                               # row 1 needs blocks 0, 1 (slots 0..6)
+    got = o.step_paged(x.query, x.new_key, x.new_value, kp, vp, table, x.lengths,
+                                 x.append_mask, x.options)
+    assert got["flags"].tolist() == [0, 1, 0]
+    assert int(got["lengths"][1]) == 5 and np.all(got["attention"][1] == 0)
+    assert torch.equal(got["key_cache"][:2], kp[:2])
+    ok = table.clone()
+    ok[1, 1] = 0
+    ref = o.step(x.query, x.new_key, x.new_value, _from_pool(kp, ok), _from_pool(vp, ok),
+                 x.lengths, x.append_mask, x.options)
+    for b in (0, 2):
+        np.testing.assert_array_equal(got["context"][b], ref["context"][b])
+
+
 ALL_PINS = [
     pin_fixed_capacity_example,
     pin_fixed_capacity_closed_form,
@@ -565,4 +636,6 @@ ALL_PINS = [
     pin_attend_cache_vs_sdpa,
     pin_attend_cache_slot_permutation,
     pin_attend_cache_outside_contract,
+    pin_paged_equals_contiguous_step,
+    pin_paged_bad_block_ids_append_nothing,
 ]
