@@ -92,16 +92,29 @@ struct TmemCols {
         : o(2 * kTcT), q(2 * kTcT + Dv), p0(2 * kTcT + Dv + D / 2) {}
 };
 
-// Rows [a, c) of the tile starting at slot j0 must come from the new rows
-// (none in read-only re-attention: the cache already holds them).
+// What the storer does to a tile in shared memory before the products read
+// it: rows [a, c) come from the new rows (none in read-only re-attention: the
+// cache already holds them), and the value rows [za, zc) from the new length
+// on are set to zero in the tile that holds the last allowed slot, so that
+// whatever the cache holds past its valid prefix (Inf or NaN included)
+// cannot reach O += P V through a zero weight.
 struct PatchRange {
-    int64_t a, c;
+    int64_t a, c, za, zc;
+    __device__ bool any() const { return c > a || zc > za; }
 };
 __device__ __forceinline__ PatchRange patch_range(const TileMeta& mt, const StepParams& p) {
-    if (p.readonly) return PatchRange{0, 0};
     const int64_t j0 = static_cast<int64_t>(mt.i) * kTcT, j1 = min(j0 + kTcT, p.M);
     const int64_t N = mt.L + mt.n;
-    return PatchRange{max(mt.L, j0), min(N, j1)};
+    PatchRange r{0, 0, 0, 0};
+    if (!p.readonly) {
+        r.a = max(mt.L, j0);
+        r.c = min(N, j1);
+    }
+    if (mt.n > 0 && j0 < N && N < j1) {
+        r.za = N;
+        r.zc = j1;
+    }
+    return r;
 }
 
 __device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars,
@@ -194,6 +207,8 @@ __device__ void tc_storer(const TcParams& tp, unsigned char* smem, TcBars bars,
         unsigned char* tV = tK + nkb * kBox;
         const int64_t j0 = static_cast<int64_t>(mt.i) * kTcT;
         const PatchRange pr = patch_range(mt, p);
+        const bool store = (mt.flags >> kRgShift) == 0 && !p.inplace;  // other row groups read it too
+        bool committed = false;
         if (pr.c > pr.a) {
             const int rows = static_cast<int>(pr.c - pr.a);
             const unsigned char* nku = nk + (mt.u * p.Q + (pr.a - mt.L)) * rowK;
@@ -210,19 +225,42 @@ __device__ void tc_storer(const TcParams& tp, unsigned char* smem, TcBars bars,
                 *reinterpret_cast<uint4*>(tV + (ch >> 3) * kBox + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
                     *reinterpret_cast<const uint4*>(nvu + rr * rowV + ch * 16);
             }
-            fence_async_shared();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.patched(ring.s), 1u);
         }
-        if (lane == 0) {
-            if ((mt.flags >> kRgShift) == 0 && !p.inplace) {  // other row groups read the same tile
-                const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
-                const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBox);
+        const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
+        const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBox);
+        auto store_tile = [&]() {  // lane 0: the tile to the output caches, one bulk group
+            if (store) {
                 const int y = static_cast<int>(j0), z = static_cast<int>(mt.u);
                 for (int b = 0; b < nkb; ++b) tma_store_3d(&tp.tm_ok, 64 * b, y, z, sK + b * kBox);
                 for (int b = 0; b < nvb; ++b) tma_store_3d(&tp.tm_ov, 64 * b, y, z, sV + b * kBox);
             }
             bulk_commit();  // (an empty group for a tile it does not store)
+        };
+        if (pr.zc > pr.za) {
+            if (store) {  // the output cache keeps the tail: store the tile before zeroing it
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    store_tile();
+                    bulk_wait_read(0);
+                }
+                __syncwarp();
+                committed = true;
+            }
+            const int z0 = static_cast<int>(pr.za - j0), nz = static_cast<int>(pr.zc - pr.za);
+            for (int e = lane; e < nz * nvb * 8; e += 32) {
+                const int rr = e / (nvb * 8), ch = e - rr * (nvb * 8);
+                *reinterpret_cast<uint4*>(tV + (ch >> 3) * kBox + (z0 + rr) * 128 + ((ch & 7) << 4)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        if (pr.any()) {
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.patched(ring.s), 1u);
+        }
+        if (lane == 0) {
+            if (!committed) store_tile();
             ++stored;
             if (stored - released > p.LAG) {
                 bulk_wait_read(p.LAG);
@@ -300,7 +338,7 @@ __device__ void tc_mma_issuer(const TcParams& tp, unsigned char* smem, TcBars ba
         const bool comp = attend && static_cast<int64_t>(mt.i) * kTcT < N;
         // consume every patched phase the storer produces on this stage
         const PatchRange pr = patch_range(mt, p);
-        if (pr.c > pr.a) {
+        if (pr.any()) {
             if (!mbar_wait(bars.patched(s), (pbits >> s) & 1u, abort)) break;
             pbits ^= 1u << s;
         }

@@ -131,3 +131,13 @@ def test_decode_scale_against_the_oracle():
     q, kc, vc, cu, K, slot = make_case(64, 32, 8, 128, 128, 8192, "bf16", 9, 1, s_min=1,
                                        k_lo=1024, num_slots=64)
     check(q, kc, vc, cu, K, slot)
+
+
+@pytest.mark.parametrize("name", ["specdec_bf16", "mqa_f16_D192"])
+def test_poisoned_slots_past_the_cached_length(name):
+    B, Hq, Hk, D, Dv, M, dtype, smax = CASES[name]
+    q, kc, vc, cu, K, slot = make_case(B, Hq, Hk, D, Dv, M, dtype, 13, smax, s_min=1)
+    for b in range(B):
+        kc[int(slot[b]), :, int(K[b]):] = float("inf")
+        vc[int(slot[b]), :, int(K[b]):] = float("nan")
+    check(q, kc, vc, cu, K, slot)

@@ -339,3 +339,43 @@ def test_tensor_core_path_contract_violations():
     assert _path(xg) == "tensor"
     out, status = run_gpu(xg)
     compare_full(x, out, status, expect_flags=kvc.DEV_MASK | kvc.DEV_OVERFLOW)
+
+
+# ------------------------------------------------------------------ poisoned tails
+def _poison_tails(x):
+    """Slots from each row's new length on hold +Inf keys and NaN values: the
+    step must neither read them into any result nor change them."""
+    counts = x.append_mask.to(torch.int64).sum(1)
+    for b in range(x.key_cache.shape[0]):
+        N = int(x.lengths[b]) + int(counts[b])
+        x.key_cache[b, :, N:] = float("inf")
+        x.value_cache[b, :, N:] = float("nan")
+    return x
+
+
+POISON = {
+    "fused_bf16": Spec(B=4, Hq=8, Hk=2, Q=3, D=128, Dv=128, M=500, dtype="bf16",
+                       lengths=("uniform", 10, 400), counts=("uniform", 1, 3)),
+    "tensor_f16": Spec(B=3, Hq=16, Hk=1, Q=8, D=192, Dv=128, M=700, dtype="f16",
+                       lengths=("uniform", 10, 600), counts=("uniform", 1, 8)),
+    "tensor_bf16_rg2": Spec(B=2, Hq=8, Hk=2, Q=40, D=64, Dv=64, M=600, dtype="bf16",
+                            lengths=("uniform", 100, 500)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(POISON))
+@pytest.mark.parametrize("inplace", [False, True])
+def test_poisoned_tail_slots(name, inplace):
+    x = _poison_tails(workloads.generate(POISON[name], 12))
+    xg = x.to(DEV)
+    if inplace:
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        kc, vc = xg.key_cache.clone(), xg.value_cache.clone()
+        out = kvc.kv_cache_attention_step_inplace(xg.query, xg.new_key, xg.new_value, kc, vc,
+                                                  xg.lengths, xg.append_mask, xg.options,
+                                                  status=status)
+        torch.cuda.synchronize()
+        status = int(status.item())
+    else:
+        out, status = run_gpu(xg)
+    compare_full(x, out, status)
