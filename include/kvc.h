@@ -196,6 +196,48 @@ KVC_API int kvc_plan_info_inplace(const kvc_dims *dims, const void *key_cache,
                           const char **path_name);
 
 /*
+ * kvc_step_paged -- the in-place step on a paged block pool
+ * ("ClikaRT::ops::attention_over_cache": a paged block pool
+ * [num_blocks, H_kv, block_size, D] with a rank-2 [B, max_blocks] block
+ * table). Batch row b's cache slot j lives in block
+ * block_table[b * max_blocks + j / block_size], row j % block_size; the
+ * capacity is M = max_blocks * block_size (dims->M, a multiple of
+ * block_size). Same operation and results as kvc_step_inplace on each row's
+ * logical cache: the appended rows are written into their blocks, the
+ * attention reads the blocks below each row's new length, nothing else in
+ * the pools is written.
+ *
+ *   key_pool        [num_blocks, Hk, block_size, D]  device, dtype, in place.
+ *   value_pool      [num_blocks, Hk, block_size, Dv] device, dtype, in place.
+ *   block_table     [B, M / block_size] device int32.
+ *   other arguments as for kvc_step_inplace; workspace >=
+ *   kvc_paged_workspace_bytes(dims).
+ *
+ * A row that appends and has a table entry outside [0, num_blocks) for one
+ * of the blocks of its slots [0, length + n) appends nothing, gets zero
+ * query rows and KVC_DEV_OVERFLOW (no kernel reads a bad block id). The
+ * blocks different rows write must be distinct, and no row may read a block
+ * another row writes in the same call (as with one owner per block).
+ */
+KVC_API size_t kvc_paged_workspace_bytes(const kvc_dims *dims);
+
+KVC_API int kvc_step_paged(const kvc_dims *dims, int64_t num_blocks, int64_t block_size,
+                   const int32_t *block_table, const void *query, const void *new_key,
+                   const void *new_value, void *key_pool, void *value_pool,
+                   const int64_t *lengths, const uint8_t *append_mask, double scale,
+                   int64_t *out_lengths, void *out_attention, void *out_context, void *workspace,
+                   size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* kvc_step_paged with events around its kernels (the block-id check first). */
+KVC_API int kvc_step_paged_timed(const kvc_dims *dims, int64_t num_blocks, int64_t block_size,
+                         const int32_t *block_table, const void *query, const void *new_key,
+                         const void *new_value, void *key_pool, void *value_pool,
+                         const int64_t *lengths, const uint8_t *append_mask, double scale,
+                         int64_t *out_lengths, void *out_attention, void *out_context,
+                         void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                         void *stream, void *const *events, int n_events);
+
+/*
  * kvc_attend_cache -- read-only re-attention over a cache that earlier steps
  * appended ("ClikaRT::ops::attention_over_cache": attend a KV cache without
  * appending to it; q packed varlen, a continuous head-major cache, slot_ids

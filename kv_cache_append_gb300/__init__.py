@@ -7,10 +7,12 @@ of libkvc.so (include/kvc.h); this package is its thin Python binding.
 from .kvc import (DEV_MASK, DEV_OVERFLOW, DEV_TIMEOUT, DTYPES, Dims, KvcError,  # noqa: F401
                   allocate_outputs, attend_cache_into, attend_cache_workspace_bytes,
                   attention_over_cache, check_inputs, default_scale, dims_of,
-                  kv_cache_attention_step, kv_cache_attention_step_inplace, library,
+                  kv_cache_attention_step, kv_cache_attention_step_inplace,
+                  kv_cache_attention_step_paged, library, paged_workspace_bytes, step_paged_into,
                   make_dims, plan_info, plan_info_inplace, status_string, step_inplace_into,
                   step_into, workspace_bytes)
 
 __all__ = ["kv_cache_attention_step", "kv_cache_attention_step_inplace",
+           "kv_cache_attention_step_paged",
            "attention_over_cache", "KvcError",
            "workspace_bytes", "step_into", "step_inplace_into", "library"]

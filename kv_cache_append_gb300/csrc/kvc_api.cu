@@ -316,15 +316,16 @@ EncodeTiledFn encode_tiled() {
 }
 
 // [U][M][width] 16-bit cache as boxes of 64 elements x 64 slots, 128-byte swizzle.
+// (box_rows: 64, or a paged pool's block size when that is smaller)
 bool cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t width, int64_t M,
-               int64_t U) {
+               int64_t U, int64_t box_rows = kTcT) {
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(M),
                                 static_cast<cuuint64_t>(U)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(width * 2),
                                    static_cast<cuuint64_t>(M * width * 2)};
-    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTcT), 1};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(map,
               dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -372,6 +373,9 @@ struct StepMode {
     bool rows = true;                  // write the attention rows
     const int32_t* slot_ids = nullptr;  // device [B]; NULL: row b
     int64_t cache_units = -1;          // units the caches hold (default B * Hk)
+    // paged pools (in place only): [num_blocks, Hk, block_size, width]
+    const int32_t* block_table = nullptr;  // device [B, M / block_size]
+    int64_t block_size = 0, num_blocks = 0;
 };
 
 int step_impl(const kvc_dims* dims, const void* query, const void* new_key, const void* new_value,
@@ -385,7 +389,10 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     const kvc_dims d = *dims;
     const bool hasq = d.Q > 0;
     const bool inplace = mode.inplace;
+    const bool paged = mode.block_table != nullptr;
+    // rows the caches hold per tensor: units x slots, or pool blocks x block rows
     const int64_t CU = mode.cache_units >= 0 ? mode.cache_units : d.B * d.Hk;
+    const int64_t cache_rows = paged ? mode.num_blocks * d.Hk * mode.block_size : CU * d.M;
     if (!key_cache || !value_cache || !lengths || !out_key_cache || !out_value_cache ||
         !out_lengths)
         return KVC_E_NULL;
@@ -403,8 +410,13 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     const bool ptrs_aligned = aligned16(key_cache) && aligned16(value_cache) &&
                               aligned16(out_key_cache) && aligned16(out_value_cache) &&
                               (!hasq || (aligned16(new_key) && aligned16(new_value)));
+    // the tensor-core kernel's paged boxes: whole 64-row tiles of one block, or
+    // 8/16/32-row blocks stacked in a tile
+    const bool tc_pages = !paged || mode.block_size % kTcT == 0 ||
+                          (kTcT % mode.block_size == 0 && mode.block_size >= 8);
     Plan pl;
-    if (!(ptrs_aligned && aligned16(query) && tc_plan(d, dev.sms, dev.smem_optin, &pl)) &&
+    if (!(ptrs_aligned && aligned16(query) && tc_pages &&
+          tc_plan(d, dev.sms, dev.smem_optin, &pl)) &&
         !(ptrs_aligned && fused_plan(d, dev.sms, dev.smem_optin, aligned16(query), &pl)))
         generic_plan(d, &pl);
 
@@ -418,8 +430,8 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
         range_of(query, d.B * d.Hq * d.Q * d.D * es),
         range_of(mode.readonly ? nullptr : new_key, d.B * d.Hk * d.Q * d.D * es),
         range_of(mode.readonly ? nullptr : new_value, d.B * d.Hk * d.Q * d.Dv * es),
-        range_of(key_cache, CU * d.M * d.D * es),
-        range_of(value_cache, CU * d.M * d.Dv * es),
+        range_of(key_cache, cache_rows * d.D * es),
+        range_of(value_cache, cache_rows * d.Dv * es),
         range_of(lengths, d.B * 8),
         range_of(append_mask, d.B * d.Q),
     };
@@ -487,6 +499,9 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     p.inplace = inplace ? 1 : 0;
     p.readonly = mode.readonly ? 1 : 0;
     p.slot_ids = mode.slot_ids;
+    p.block_table = mode.block_table;
+    p.block_size = mode.block_size;
+    p.max_blocks = paged ? d.M / mode.block_size : 0;
     // finalize blocks: rows longer than kFinalizeSeg slots are split so that
     // long-context steps with few query rows still fill the GPU
     p.fin_seg = d.M <= kFinalizeSeg ? align_up(d.M, 8) : kFinalizeSeg;
@@ -510,8 +525,14 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
             TcParams tp;
             std::memset(&tp, 0, sizeof(tp));
             tp.p = p;
-            if (!cache_map(&tp.tm_k, key_cache, d.dtype, d.D, d.M, CU) ||
-                !cache_map(&tp.tm_v, value_cache, d.dtype, d.Dv, d.M, CU) ||
+            const bool ok_maps =
+                paged ? cache_map(&tp.tm_k, key_cache, d.dtype, d.D, mode.block_size,
+                                  mode.num_blocks * d.Hk, std::min<int64_t>(kTcT, mode.block_size)) &&
+                            cache_map(&tp.tm_v, value_cache, d.dtype, d.Dv, mode.block_size,
+                                      mode.num_blocks * d.Hk, std::min<int64_t>(kTcT, mode.block_size))
+                      : cache_map(&tp.tm_k, key_cache, d.dtype, d.D, d.M, CU) &&
+                            cache_map(&tp.tm_v, value_cache, d.dtype, d.Dv, d.M, CU);
+            if (!ok_maps ||
                 !cache_map(&tp.tm_ok, out_key_cache, d.dtype, d.D, d.M, d.B * d.Hk) ||
                 !cache_map(&tp.tm_ov, out_value_cache, d.dtype, d.Dv, d.M, d.B * d.Hk) ||
                 !rows_map(&tp.tm_pv, p.pvals, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, d.M, p.pv_ld,
@@ -676,6 +697,78 @@ int attend_impl(const kvc_dims* dims, int64_t num_slots, int64_t total_q, const 
     while (e == cudaSuccess && events && recorded < n_events) e = record();
     return e == cudaSuccess ? KVC_OK : KVC_E_CUDA;
 }
+// Workspace of the paged step: the step's own, then the checked mask.
+size_t paged_mask_offset(const kvc_dims& d) {
+    return (kvc_workspace_bytes(&d) + 255) & ~size_t(255);
+}
+
+int paged_impl(const kvc_dims* dims, int64_t num_blocks, int64_t block_size,
+               const int32_t* block_table, const void* query, const void* new_key,
+               const void* new_value, void* key_pool, void* value_pool, const int64_t* lengths,
+               const uint8_t* append_mask, double scale, int64_t* out_lengths, void* out_attention,
+               void* out_context, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+               void* stream_ptr, void* const* events, int n_events) {
+    int rc = check_dims(dims);
+    if (rc != KVC_OK) return rc;
+    const kvc_dims d = *dims;
+    if (block_size < 1 || num_blocks < 1 || d.M % block_size != 0 ||
+        static_cast<double>(num_blocks) * d.Hk * block_size * (d.D + d.Dv) *
+                elem_size(d.dtype) > 4.0e18 ||
+        num_blocks >= (int64_t(1) << 31) / std::max<int64_t>(1, d.Hk))
+        return KVC_E_SHAPE;
+    if (!block_table || !lengths || !out_lengths) return KVC_E_NULL;
+    if (d.Q > 0 && !append_mask) return KVC_E_NULL;
+    if (events && n_events < 0) return KVC_E_NULL;
+    const size_t moff = paged_mask_offset(d);
+    const size_t need = moff + static_cast<size_t>(d.B * d.Q);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KVC_E_WORKSPACE;
+    // the table and the checked mask must not overlap an output or the pools
+    const int64_t es = elem_size(d.dtype);
+    const Range tbl = range_of(block_table, d.B * (d.M / block_size) * 4);
+    const Range pools[] = {range_of(key_pool, num_blocks * d.Hk * block_size * d.D * es),
+                           range_of(value_pool, num_blocks * d.Hk * block_size * d.Dv * es)};
+    const Range outs[] = {range_of(out_lengths, d.B * 8),
+                          range_of(out_attention, d.B * d.Hq * d.Q * d.M * es),
+                          range_of(out_context, d.B * d.Hq * d.Q * d.Dv * es),
+                          range_of(workspace, static_cast<int64_t>(need))};
+    for (const Range& o : outs)
+        if (overlaps(o, tbl)) return KVC_E_ALIAS;
+    for (const Range& pl : pools)
+        if (overlaps(pl, tbl)) return KVC_E_ALIAS;
+
+    uint8_t* mask_eff = static_cast<unsigned char*>(workspace) + moff;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    int recorded = 0;
+    auto record = [&]() -> cudaError_t {
+        if (events && recorded < n_events)
+            return cudaEventRecord(static_cast<cudaEvent_t>(events[recorded++]), stream);
+        return cudaSuccess;
+    };
+    cudaError_t e = record();
+    if (e == cudaSuccess && d.Q > 0) {
+        StepParams p0;
+        std::memset(&p0, 0, sizeof(p0));
+        p0.B = d.B; p0.Hk = d.Hk; p0.Q = d.Q; p0.M = d.M;
+        p0.lengths = lengths; p0.mask = append_mask; p0.dev_status = dev_status;
+        p0.block_table = block_table; p0.block_size = block_size;
+        p0.max_blocks = d.M / block_size;
+        e = launch_paged_prep(p0, num_blocks, mask_eff, stream);
+        if (e == cudaSuccess) e = record();
+    }
+    if (e != cudaSuccess) return KVC_E_CUDA;
+    StepMode mode;
+    mode.inplace = true;
+    mode.block_table = block_table;
+    mode.block_size = block_size;
+    mode.num_blocks = num_blocks;
+    void* const* ev = events && recorded > 0 ? events + (recorded - 1) : nullptr;
+    const int nev = events ? std::max(0, n_events - (recorded - 1)) : 0;
+    return step_impl(dims, query, new_key, new_value, key_pool, value_pool, lengths,
+                     d.Q > 0 ? mask_eff : append_mask, scale, key_pool, value_pool, out_lengths,
+                     out_attention, out_context, workspace, moff, dev_status, stream_ptr, ev, nev,
+                     mode);
+}
+
 }  // namespace
 }  // namespace kvc
 
@@ -781,6 +874,36 @@ int kvc_plan_info_inplace(const kvc_dims* dims, const void* key_cache, const voi
     if (rc < 0) return rc;
     // the cache write, then with query rows the step kernel, the merge and the row writer
     return dims->Q > 0 ? 4 : 1;
+}
+
+size_t kvc_paged_workspace_bytes(const kvc_dims* dims) {
+    if (!dims || kvc::check_dims(dims) != KVC_OK) return 0;
+    return kvc::paged_mask_offset(*dims) + static_cast<size_t>(dims->B * dims->Q);
+}
+
+int kvc_step_paged(const kvc_dims* dims, int64_t num_blocks, int64_t block_size,
+                   const int32_t* block_table, const void* query, const void* new_key,
+                   const void* new_value, void* key_pool, void* value_pool,
+                   const int64_t* lengths, const uint8_t* append_mask, double scale,
+                   int64_t* out_lengths, void* out_attention, void* out_context, void* workspace,
+                   size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    return kvc::paged_impl(dims, num_blocks, block_size, block_table, query, new_key, new_value,
+                           key_pool, value_pool, lengths, append_mask, scale, out_lengths,
+                           out_attention, out_context, workspace, workspace_bytes, dev_status,
+                           stream, nullptr, 0);
+}
+
+int kvc_step_paged_timed(const kvc_dims* dims, int64_t num_blocks, int64_t block_size,
+                         const int32_t* block_table, const void* query, const void* new_key,
+                         const void* new_value, void* key_pool, void* value_pool,
+                         const int64_t* lengths, const uint8_t* append_mask, double scale,
+                         int64_t* out_lengths, void* out_attention, void* out_context,
+                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                         void* stream, void* const* events, int n_events) {
+    return kvc::paged_impl(dims, num_blocks, block_size, block_table, query, new_key, new_value,
+                           key_pool, value_pool, lengths, append_mask, scale, out_lengths,
+                           out_attention, out_context, workspace, workspace_bytes, dev_status,
+                           stream, events, n_events);
 }
 
 size_t kvc_attend_cache_workspace_bytes(const kvc_dims* dims) {

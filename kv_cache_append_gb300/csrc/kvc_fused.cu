@@ -81,7 +81,9 @@ __device__ void run_producer(const StepParams& p, unsigned char* smem, Bars bars
                 ok = false;
                 break;
             }
-            const int64_t j0 = i * p.T, j1 = min(j0 + p.T, p.M);
+            const int64_t j0 = i * p.T;
+            // paged: only rows below the new length (the block ids checked)
+            const int64_t j1 = p.block_table ? min(j0 + p.T, x.N) : min(j0 + p.T, p.M);
             const bool stage_q = attend && p.q_staged && i == i0;
             TileMeta& mt = meta[ring.s];
             mt.L = x.L;
@@ -94,8 +96,13 @@ __device__ void run_producer(const StepParams& p, unsigned char* smem, Bars bars
             uint32_t bytes = static_cast<uint32_t>((j1 - j0) * (rowK + rowV));
             if (stage_q) bytes += static_cast<uint32_t>(p.q_stage_bytes);
             mbar_arrive_expect_tx(bars.full(ring.s), bytes);  // publishes the metadata too
-            load_rows(sK, kcu, nku, rowK, j0, j1, Ls, x.N, bars.full(ring.s));
-            load_rows(sK + vofs, vcu, nvu, rowV, j0, j1, Ls, x.N, bars.full(ring.s));
+            if (p.block_table) {
+                load_rows_paged(sK, p, kc, u, nku, rowK, j0, j1, Ls, x.N, bars.full(ring.s));
+                load_rows_paged(sK + vofs, p, vc, u, nvu, rowV, j0, j1, Ls, x.N, bars.full(ring.s));
+            } else {
+                load_rows(sK, kcu, nku, rowK, j0, j1, Ls, x.N, bars.full(ring.s));
+                load_rows(sK + vofs, vcu, nvu, rowV, j0, j1, Ls, x.N, bars.full(ring.s));
+            }
             if (stage_q)  // the G*Q query rows of the unit are contiguous in query
                 bulk_g2s(sK + static_cast<uint32_t>(p.off_stage_q),
                          qry + (x.b * p.Hq + x.kv * p.G) * p.Q * rowK,

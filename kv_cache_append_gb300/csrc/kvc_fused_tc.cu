@@ -160,12 +160,33 @@ __device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars
                        static_cast<int32_t>(rg << kRgShift);
             const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
             const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBox);
-            mbar_arrive_expect_tx(bars.full(ring.s), tile_bytes);  // publishes the metadata too
-            const int y = static_cast<int>(i * kTcT), z = static_cast<int>(cache_unit(p, u));
-            for (int b = 0; b < nkb; ++b)
-                tma_load_3d(sK + b * kBox, &tp.tm_k, 64 * b, y, z, bars.full(ring.s));
-            for (int b = 0; b < nvb; ++b)
-                tma_load_3d(sV + b * kBox, &tp.tm_v, 64 * b, y, z, bars.full(ring.s));
+            if (!p.block_table) {
+                mbar_arrive_expect_tx(bars.full(ring.s), tile_bytes);  // publishes the metadata too
+                const int y = static_cast<int>(i * kTcT), z = static_cast<int>(cache_unit(p, u));
+                for (int b = 0; b < nkb; ++b)
+                    tma_load_3d(sK + b * kBox, &tp.tm_k, 64 * b, y, z, bars.full(ring.s));
+                for (int b = 0; b < nvb; ++b)
+                    tma_load_3d(sV + b * kBox, &tp.tm_v, 64 * b, y, z, bars.full(ring.s));
+            } else {
+                // paged: one box of min(64, block_size) rows per block piece of
+                // the tile, for the blocks below the new length only (their
+                // ids were checked); the pool maps are [blocks * Hk][bs][width]
+                const int64_t j0 = i * kTcT;
+                const int64_t h = min(static_cast<int64_t>(kTcT), p.block_size);
+                const int64_t npc = min((x.N - j0 + h - 1) / h, kTcT / h);
+                mbar_arrive_expect_tx(bars.full(ring.s),
+                                      static_cast<uint32_t>(npc * h * 128 * (nkb + nvb)));
+                for (int64_t c = 0; c < npc; ++c) {
+                    const int64_t j = j0 + c * h;
+                    const int y = static_cast<int>(j % p.block_size);
+                    const int z = static_cast<int>(paged_unit(p, u, j));
+                    const uint32_t o = static_cast<uint32_t>(c * h * 128);
+                    for (int b = 0; b < nkb; ++b)
+                        tma_load_3d(sK + b * kBox + o, &tp.tm_k, 64 * b, y, z, bars.full(ring.s));
+                    for (int b = 0; b < nvb; ++b)
+                        tma_load_3d(sV + b * kBox + o, &tp.tm_v, 64 * b, y, z, bars.full(ring.s));
+                }
+            }
             ++issued;
             ring.next(p.NS);
         }

@@ -61,17 +61,16 @@ __global__ void __launch_bounds__(kAttendWarps * 32)
     const int64_t lim = ra.L + t;
     // slots [L, N) come from the new rows (none in read-only re-attention)
     const int64_t L = p.readonly ? ra.L + ra.n : ra.L, N = ra.L + ra.n;
-    const int64_t cu = cache_unit(p, u);
     const T* q = static_cast<const T*>(p.query) + row * p.D;
-    const T* kc = static_cast<const T*>(p.key_cache) + cu * p.M * p.D;
     const T* nk = static_cast<const T*>(p.new_key) + u * p.Q * p.D;
-    const T* vc = static_cast<const T*>(p.value_cache) + cu * p.M * p.Dv;
     const T* nv = static_cast<const T*>(p.new_value) + u * p.Q * p.Dv;
+    const int64_t rk = p.D * p.es, rv = p.Dv * p.es;
     float* sc = p.scores + row * p.M;
 
     float mloc = -INFINITY;
     for (int64_t j = lane; j <= lim; j += 32) {
-        const T* krow = (j >= L && j < N) ? nk + (j - L) * p.D : kc + j * p.D;
+        const T* krow = (j >= L && j < N) ? nk + (j - L) * p.D
+                                          : reinterpret_cast<const T*>(cache_row(p, p.key_cache, u, j, rk));
         float dot = 0.f;
         for (int64_t d = 0; d < p.D; ++d)
             dot = fmaf(S::to_float(q[d]) * p.qscale, S::to_float(krow[d]), dot);
@@ -89,7 +88,8 @@ __global__ void __launch_bounds__(kAttendWarps * 32)
     for (int64_t e = lane; e < p.Dv; e += 32) {
         float a = 0.f;
         for (int64_t j = 0; j <= lim; ++j) {
-            const T* vrow = (j >= L && j < N) ? nv + (j - L) * p.Dv : vc + j * p.Dv;
+            const T* vrow = (j >= L && j < N) ? nv + (j - L) * p.Dv
+                                              : reinterpret_cast<const T*>(cache_row(p, p.value_cache, u, j, rv));
             a = fmaf(fast_exp2(sc[j] - mloc), S::to_float(vrow[e]), a);
         }
         p.part_acc[prow * p.Dv + e] = a;

@@ -492,6 +492,12 @@ struct StepParams {
     // unit (b, kv) reads cache unit slot_ids[b] * Hk + kv.
     int readonly;
     const int32_t* slot_ids;  // [B] cache row per batch row; NULL: row b
+    // Paged caches (block_table != NULL): pools [num_blocks, Hk, block_size,
+    // width]; slot j of batch row b lives in block block_table[b * max_blocks
+    // + j / block_size], row j % block_size. Only the in-place step uses it,
+    // after the host-side plan checked that every block id it reads is valid.
+    const int32_t* block_table;
+    int64_t block_size, max_blocks;
     int64_t fin_seg;    // attention slots per row-writer block (a multiple of 8)
     int64_t fin_nseg;   // row-writer blocks per query row: ceil(M / fin_seg)
     RowStat* rowstat;   // [B][Hq][Q]: the merged maximum, 1 / sum and last allowed slot
@@ -502,6 +508,23 @@ __device__ __forceinline__ int64_t cache_unit(const StepParams& p, int64_t u) {
     if (!p.slot_ids) return u;
     const int64_t b = u / p.Hk;
     return static_cast<int64_t>(p.slot_ids[b]) * p.Hk + (u - b * p.Hk);
+}
+
+// Pool unit (block * Hk + kv) and row of slot j of unit u in a paged cache.
+__device__ __forceinline__ int64_t paged_unit(const StepParams& p, int64_t u, int64_t j) {
+    const int64_t b = u / p.Hk;
+    return static_cast<int64_t>(p.block_table[b * p.max_blocks + j / p.block_size]) * p.Hk +
+           (u - b * p.Hk);
+}
+
+// Address of cache row (unit u, slot j) for rows of `row` bytes, contiguous
+// ([units][M] rows, through the slot map) or paged.
+__device__ __forceinline__ unsigned char* cache_row(const StepParams& p, const void* base,
+                                                    int64_t u, int64_t j, int64_t row) {
+    unsigned char* c = static_cast<unsigned char*>(const_cast<void*>(base));
+    if (p.block_table)
+        return c + (paged_unit(p, u, j) * p.block_size + j % p.block_size) * row;
+    return c + (cache_unit(p, u) * p.M + j) * row;
 }
 
 

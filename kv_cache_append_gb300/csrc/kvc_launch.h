@@ -41,6 +41,11 @@ cudaError_t launch_finalize_rows(const StepParams& p, int dtype, cudaStream_t st
 // the caches and new rows are 16-byte aligned.
 cudaError_t launch_inplace_rows(const StepParams& p, bool words16, cudaStream_t stream);
 
+// The paged step's block-id check (kvc_inplace.cu): the mask the step then
+// uses, with every row whose needed block ids are out of range cleared.
+cudaError_t launch_paged_prep(const StepParams& p, int64_t num_blocks, uint8_t* mask_out,
+                              cudaStream_t stream);
+
 // Read-only re-attention: packed queries to the dense step view and the
 // context back (kvc_attend.cu). Q is the largest query count per sequence.
 struct AttendParams {

@@ -72,6 +72,29 @@ __device__ __forceinline__ void load_rows(uint32_t dst, const unsigned char* cac
                  static_cast<uint32_t>((j1 - c) * row_bytes), bar);
 }
 
+// Paged form of load_rows: rows [j0, j1) of unit u split at block boundaries;
+// within a block, old rows from the pool and rows [L, N) from the new rows.
+__device__ __forceinline__ void load_rows_paged(uint32_t dst, const StepParams& p,
+                                                const void* pool, int64_t u,
+                                                const unsigned char* new_unit, int64_t row_bytes,
+                                                int64_t j0, int64_t j1, int64_t L, int64_t N,
+                                                uint32_t bar) {
+    for (int64_t a = j0; a < j1;) {
+        const int64_t e = min(j1, (a / p.block_size + 1) * p.block_size);
+        const int64_t na = clamp64(L, a, e), nc = clamp64(N, a, e);
+        if (na > a)
+            bulk_g2s(dst + static_cast<uint32_t>((a - j0) * row_bytes), cache_row(p, pool, u, a, row_bytes),
+                     static_cast<uint32_t>((na - a) * row_bytes), bar);
+        if (nc > na)
+            bulk_g2s(dst + static_cast<uint32_t>((na - j0) * row_bytes), new_unit + (na - L) * row_bytes,
+                     static_cast<uint32_t>((nc - na) * row_bytes), bar);
+        if (e > nc)
+            bulk_g2s(dst + static_cast<uint32_t>((nc - j0) * row_bytes), cache_row(p, pool, u, nc, row_bytes),
+                     static_cast<uint32_t>((e - nc) * row_bytes), bar);
+        a = e;
+    }
+}
+
 // All 32 lanes wait; the result is made warp-uniform so the warp never
 // diverges on it.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {

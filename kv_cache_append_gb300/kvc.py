@@ -91,6 +91,14 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kvc_attend_cache.argtypes = attend_args
             lib.kvc_attend_cache_timed.restype = i32
             lib.kvc_attend_cache_timed.argtypes = attend_args + [ctypes.POINTER(vp), i32]
+            paged_args = ([dp, i64, i64] + [vp] * 8 + [ctypes.c_double] + [vp] * 4 +
+                          [sz, vp, vp])
+            lib.kvc_paged_workspace_bytes.restype = sz
+            lib.kvc_paged_workspace_bytes.argtypes = [dp]
+            lib.kvc_step_paged.restype = i32
+            lib.kvc_step_paged.argtypes = paged_args
+            lib.kvc_step_paged_timed.restype = i32
+            lib.kvc_step_paged_timed.argtypes = paged_args + [ctypes.POINTER(vp), i32]
             lib.kvc_status_string.restype = ctypes.c_char_p
             lib.kvc_status_string.argtypes = [i32]
             lib.kvc_version.restype = i32
@@ -407,4 +415,79 @@ def attention_over_cache(q: torch.Tensor, key_cache: torch.Tensor, value_cache: 
         attend_cache_into(dims, num_slots, q.contiguous(), key_cache.contiguous(),
                           value_cache.contiguous(), cu, kl, seqlens_k.numel() == B + 1, sl,
                           float(scale), out, ws, status)
+    return out
+
+
+def paged_workspace_bytes(dims: Dims) -> int:
+    return int(library().kvc_paged_workspace_bytes(ctypes.byref(dims)))
+
+
+def step_paged_into(dims: Dims, block_table, query, new_key, new_value, key_pool, value_pool,
+                    lengths, append_mask, scale: float, out: dict, workspace: torch.Tensor,
+                    status: Optional[torch.Tensor] = None, stream: Optional[int] = None,
+                    events: Optional[Sequence] = None) -> None:
+    """Enqueue one kvc_step_paged (no checks beyond libkvc's); out holds
+    "lengths", "attention" and "context"."""
+    lib = library()
+    if stream is None:
+        stream = torch.cuda.current_stream(key_pool.device).cuda_stream
+    ws_len = workspace.numel() * workspace.element_size()
+    args = [ctypes.byref(dims), int(key_pool.shape[0]), int(key_pool.shape[2]), _p(block_table),
+            _p(query), _p(new_key), _p(new_value), _p(key_pool), _p(value_pool), _p(lengths),
+            _p(append_mask), ctypes.c_double(scale), _p(out["lengths"]), _p(out["attention"]),
+            _p(out["context"]), _p(workspace), ws_len, _p(status), ctypes.c_void_p(stream)]
+    if events:
+        handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+        rc = lib.kvc_step_paged_timed(*args, handles, len(events))
+    else:
+        rc = lib.kvc_step_paged(*args)
+    if rc != KVC_OK:
+        raise KvcError(rc, status_string(rc))
+
+
+def kv_cache_attention_step_paged(query: torch.Tensor, new_key: torch.Tensor,
+                                  new_value: torch.Tensor, key_pool: torch.Tensor,
+                                  value_pool: torch.Tensor, block_table: torch.Tensor,
+                                  lengths: torch.Tensor, append_mask: torch.Tensor,
+                                  options: Optional[dict] = None,
+                                  status: Optional[torch.Tensor] = None) -> dict:
+    """The in-place step on a paged block pool: key_pool [num_blocks, Hk,
+    block_size, D] / value_pool [..., Dv] are updated in place, batch row b's
+    slot j living in block block_table[b, j // block_size] (capacity
+    M = block_table.shape[1] * block_size). Returns {"key_cache": key_pool,
+    "value_cache": value_pool, "lengths", "attention", "context"}."""
+    if query.dim() != 4 or key_pool.dim() != 4 or value_pool.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("query [B,Hq,Q,D], pools [num_blocks,Hk,block_size,D|Dv], table [B,max_blocks]")
+    for name, t in (("query", query), ("new_key", new_key), ("new_value", new_value),
+                    ("key_pool", key_pool), ("value_pool", value_pool)):
+        if t.dtype not in DTYPES or t.dtype != query.dtype:
+            raise ValueError(f"{name}: one dtype among float32/bfloat16/float16 is needed")
+        if t.device.type != "cuda" or t.device != query.device:
+            raise ValueError("the paged step runs on one CUDA device only (no CPU path)")
+    if not (key_pool.is_contiguous() and value_pool.is_contiguous()):
+        raise ValueError("the pools are updated in place and must be contiguous")
+    B, Hq, Q, D = query.shape
+    num_blocks, Hk, bs, Dk = key_pool.shape
+    Dv = value_pool.shape[-1]
+    if Dk != D or tuple(value_pool.shape[:3]) != (num_blocks, Hk, bs) or block_table.shape[0] != B:
+        raise ValueError("pool / table shapes do not match the query")
+    if tuple(new_key.shape) != (B, Hk, Q, D) or tuple(new_value.shape) != (B, Hk, Q, Dv):
+        raise ValueError("new_key / new_value shapes do not match")
+    if tuple(append_mask.shape) != (B, Q) or tuple(lengths.shape) != (B,):
+        raise ValueError("append_mask is [B, Q] and lengths [B]")
+    scale = _scale_from(options, D)
+    M = block_table.shape[1] * bs
+    dims = make_dims(B, Hq, Hk, Q, D, Dv, M, query.dtype)
+    q, nk, nv = (t.contiguous() for t in (query, new_key, new_value))
+    tb = block_table.to(device=query.device, dtype=torch.int32).contiguous()
+    ln = lengths.to(torch.int64).contiguous()
+    mk = append_mask.contiguous()
+    mk = mk.view(torch.uint8) if mk.dtype == torch.bool else mk
+    out = {"key_cache": key_pool, "value_cache": value_pool,
+           "lengths": torch.empty(B, dtype=torch.int64, device=q.device),
+           "attention": torch.empty(B, Hq, Q, M, dtype=q.dtype, device=q.device),
+           "context": torch.empty(B, Hq, Q, Dv, dtype=q.dtype, device=q.device)}
+    ws = torch.empty(max(16, paged_workspace_bytes(dims)), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        step_paged_into(dims, tb, q, nk, nv, key_pool, value_pool, ln, mk, scale, out, ws, status)
     return out
