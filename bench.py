@@ -48,6 +48,8 @@ PATH_KERNELS_INPLACE = {
                "finalize_rows_kernel"],
     "generic": ["inplace_rows_kernel", "generic_attend_kernel", "finalize_merge_kernel",
                 "finalize_rows_kernel"]}
+PATH_KERNELS_PAGED = {
+    path: ["paged_prep_kernel"] + PATH_KERNELS_INPLACE[path] for path in PATH_KERNELS_INPLACE}
 PATH_KERNELS_READONLY = {
     path: ["attend_prep_kernel", STEP_KERNEL[path] if path != "generic" else "generic_attend_kernel",
            "finalize_merge_kernel", "attend_unpack_kernel"]
@@ -330,7 +332,36 @@ def run_ours(args, spec, world, rank, local):
     nws = kvc.workspace_bytes(dims)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
     stream = torch.cuda.current_stream(dev)
-    if args.readonly:
+    if args.paged:
+        # the caches as a pool of block_size-slot blocks in a shuffled order
+        bs = args.paged
+        Bn, Hk_, M_ = kc.shape[:3]
+        mb = M_ // bs
+        g = torch.Generator().manual_seed(17 + rank)
+        perm = torch.randperm(Bn * mb, generator=g).to(dev)
+        table = perm.reshape(Bn, mb).to(torch.int32)
+
+        def to_pool(c):
+            W = c.shape[-1]
+            blocks = c.reshape(Bn, Hk_, mb, bs, W).permute(0, 2, 1, 3, 4).reshape(Bn * mb, Hk_, bs, W)
+            pool = torch.empty_like(blocks)
+            pool[perm] = blocks
+            return pool
+        kc_p, vc_p = to_pool(kc), to_pool(vc)
+        del out["key_cache"], out["value_cache"]
+        x.key_cache = x.value_cache = None
+        kc = vc = None
+        torch.cuda.empty_cache()
+        ws = torch.empty(kvc.paged_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+        nkern = 5 if spec.Q > 0 else 2
+        path = kvc.plan_info_inplace(dims, kc_p, vc_p, nk, nv)[1]
+        if path == "tensor" and not (bs % 64 == 0 or (64 % bs == 0 and bs >= 8)):
+            path = "fused"
+
+        def step(events=None):
+            kvc.step_paged_into(dims, table, q, nk, nv, kc_p, vc_p, ln, mk, scale, out, ws, None,
+                                stream.cuda_stream, events)
+    elif args.readonly:
         # packed queries = the step's valid query rows; each sequence's cached
         # length = its new length; cache rows visited through a permutation
         counts_d = x.append_mask.to(torch.int64).sum(1)
@@ -405,22 +436,24 @@ def run_ours(args, spec, world, rank, local):
     lengths_h = x.lengths.cpu().tolist()
     counts_h = x.append_mask.to(torch.int64).sum(1).cpu().tolist()
     nbytes = (algorithmic_bytes_readonly(spec, lengths_h, counts_h) if args.readonly else
-              algorithmic_bytes_inplace(spec, lengths_h, counts_h) if args.inplace
+              algorithmic_bytes_inplace(spec, lengths_h, counts_h) if (args.inplace or args.paged)
               else algorithmic_bytes(spec))
     value = world * nbytes["total"] / (ms_step * 1e-3) / 1e9
     peak, peak_src = measured_peak()
-    ks = 1 if (args.inplace or args.readonly) and nkern > 1 else 0  # index of the step kernel
+    ks = (2 if args.paged and nkern > 2 else
+          1 if (args.inplace or args.readonly) and nkern > 1 else 0)  # index of the step kernel
     fused_ms = kern_ms[ks]
     achieved = nbytes["fused_kernel"] / (fused_ms * 1e-3) / 1e9
     kname = STEP_KERNEL[path]
     if args.readonly and path == "generic":
         kname = "generic_attend_kernel"
-    traffic = None if (args.inplace or args.readonly) else kernel_traffic(args.workload, kname)
+    traffic = (None if (args.inplace or args.readonly or args.paged)
+               else kernel_traffic(args.workload, kname))
 
     # ---- end to end through the public API: pinned host in, pinned host out
     e2e = None
-    if args.readonly:
-        e2e = None  # the read-only face has no host-buffer leg here
+    if args.readonly or args.paged:
+        e2e = None  # these faces have no host-buffer leg here
     elif not args.no_e2e:
         e2e = (measure_e2e_inplace(kvc, x, dev, max(3, min(args.steps, 10)), nbytes["total"],
                                    world) if args.inplace else
@@ -434,7 +467,7 @@ def run_ours(args, spec, world, rank, local):
         sample_bytes = (algorithmic_bytes_readonly(spec, lengths_h[:rows], counts_h[:rows])
                         if args.readonly else
                         algorithmic_bytes_inplace(spec, lengths_h[:rows], counts_h[:rows])
-                        if args.inplace else algorithmic_bytes(spec, rows))
+                        if (args.inplace or args.paged) else algorithmic_bytes(spec, rows))
         cpu = {"value": round(sample_bytes["total"] / dt / 1e9, 4),
                "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"first {rows} of {spec.B} batch rows of {args.workload}, one step"
@@ -464,7 +497,7 @@ def run_ours(args, spec, world, rank, local):
         "gpu_launches": nkern * args.steps,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
-    names = (PATH_KERNELS_READONLY if args.readonly else
+    names = (PATH_KERNELS_READONLY if args.readonly else PATH_KERNELS_PAGED if args.paged else
              PATH_KERNELS_INPLACE if args.inplace else PATH_KERNELS)[path]
     for k in range(nkern):
         if k != ks:
@@ -472,6 +505,9 @@ def run_ours(args, spec, world, rank, local):
     if args.inplace:
         line["config"]["mode"] = ("in place: donated caches, only the appended rows written, "
                                   "the attention reads the valid prefix")
+    if args.paged:
+        line["config"]["mode"] = (f"paged: pools of {args.paged}-slot blocks in a shuffled "
+                                  "order, updated in place through the block table")
     if args.readonly:
         line["config"]["mode"] = ("read-only re-attention: packed queries (the step's valid "
                                   "rows) over the cached prefix through a slot permutation; "
@@ -573,6 +609,8 @@ def main():
                     help="override the workload's dtype (the fp32 chunked append)")
     ap.add_argument("--inplace", action="store_true",
                     help="time kvc_step_inplace (donated caches updated in place)")
+    ap.add_argument("--paged", type=int, default=0, metavar="BLOCK_SIZE",
+                    help="time kvc_step_paged on pools of BLOCK_SIZE-slot blocks")
     ap.add_argument("--readonly", action="store_true",
                     help="time kvc_attend_cache (read-only re-attention over the cache)")
     args = ap.parse_args()

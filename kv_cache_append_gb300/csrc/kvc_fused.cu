@@ -69,6 +69,8 @@ __device__ void run_producer(const StepParams& p, unsigned char* smem, Bars bars
         const int64_t iend = !p.inplace ? p.TPU : x.n > 0 ? min(p.TPU, (x.N + p.T - 1) / p.T) : 0;
         const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, iend);
         if (i0 >= i1) continue;
+        TileIds ids;  // paged: the block ids of the next tile to load
+        if (p.block_table) fetch_tile_ids(p, u, i0 * p.T, min(i0 * p.T + p.T, x.N), ids);
         const bool attend = x.n > 0 && i0 * p.T < x.N;
         const int64_t cu = cache_unit(p, u);
         const unsigned char* kcu = kc + cu * p.M * rowK;
@@ -97,8 +99,10 @@ __device__ void run_producer(const StepParams& p, unsigned char* smem, Bars bars
             if (stage_q) bytes += static_cast<uint32_t>(p.q_stage_bytes);
             mbar_arrive_expect_tx(bars.full(ring.s), bytes);  // publishes the metadata too
             if (p.block_table) {
-                load_rows_paged(sK, p, kc, u, nku, rowK, j0, j1, Ls, x.N, bars.full(ring.s));
-                load_rows_paged(sK + vofs, p, vc, u, nvu, rowV, j0, j1, Ls, x.N, bars.full(ring.s));
+                load_rows_paged(sK, sK + vofs, p, ids, u, nku, nvu, rowK, rowV, j0, j1, Ls, x.N,
+                                bars.full(ring.s));
+                if (i + 1 < i1)  // the next tile's ids arrive while its stage frees up
+                    fetch_tile_ids(p, u, j0 + p.T, min(j0 + 2 * p.T, x.N), ids);
             } else {
                 load_rows(sK, kcu, nku, rowK, j0, j1, Ls, x.N, bars.full(ring.s));
                 load_rows(sK + vofs, vcu, nvu, rowV, j0, j1, Ls, x.N, bars.full(ring.s));

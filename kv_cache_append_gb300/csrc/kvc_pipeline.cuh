@@ -72,25 +72,77 @@ __device__ __forceinline__ void load_rows(uint32_t dst, const unsigned char* cac
                  static_cast<uint32_t>((j1 - c) * row_bytes), bar);
 }
 
-// Paged form of load_rows: rows [j0, j1) of unit u split at block boundaries;
-// within a block, old rows from the pool and rows [L, N) from the new rows.
-__device__ __forceinline__ void load_rows_paged(uint32_t dst, const StepParams& p,
-                                                const void* pool, int64_t u,
-                                                const unsigned char* new_unit, int64_t row_bytes,
-                                                int64_t j0, int64_t j1, int64_t L, int64_t N,
-                                                uint32_t bar) {
+// Block ids of the blocks holding slots [j0, j1) of unit u, loaded together
+// (up to kTileIds; a tile's producer loads the next tile's ids while it
+// waits for a free stage, so no lookup stalls a copy).
+constexpr int kTileIds = 8;
+struct TileIds {
+    int64_t first = -1;  // block index of id[0]
+    int n = 0;
+    int32_t id[kTileIds];
+};
+
+__device__ __forceinline__ void fetch_tile_ids(const StepParams& p, int64_t u, int64_t j0,
+                                               int64_t j1, TileIds& t) {
+    const int32_t* row = p.block_table + (u / p.Hk) * p.max_blocks;
+    t.first = j0 / p.block_size;
+    t.n = j1 > j0 ? static_cast<int>(min(static_cast<int64_t>(kTileIds),
+                                         (j1 - 1) / p.block_size - t.first + 1))
+                  : 0;
+#pragma unroll
+    for (int k = 0; k < kTileIds; ++k)
+        if (k < t.n) t.id[k] = row[t.first + k];
+}
+
+// Pool unit (block * Hk + kv) of slot j of unit u, from t when it holds it.
+__device__ __forceinline__ int64_t tile_pool_unit(const StepParams& p, const TileIds& t,
+                                                  int64_t u, int64_t j) {
+    const int64_t e = j / p.block_size - t.first;
+    int32_t id = 0;
+    bool have = false;
+#pragma unroll
+    for (int k = 0; k < kTileIds; ++k)
+        if (k == e && k < t.n) {
+            id = t.id[k];
+            have = true;
+        }
+    if (!have) return paged_unit(p, u, j);
+    return static_cast<int64_t>(id) * p.Hk + (u % p.Hk);
+}
+
+// Paged form of load_rows, for the keys and the values of one tile: rows
+// [j0, j1) of unit u split at block boundaries; within a block, old rows from
+// the pools and rows [L, N) from the new rows.
+__device__ __forceinline__ void load_rows_paged(uint32_t dstK, uint32_t dstV, const StepParams& p,
+                                                const TileIds& ids, int64_t u,
+                                                const unsigned char* newK, const unsigned char* newV,
+                                                int64_t rowK, int64_t rowV, int64_t j0, int64_t j1,
+                                                int64_t L, int64_t N, uint32_t bar) {
+    const unsigned char* kp = static_cast<const unsigned char*>(p.key_cache);
+    const unsigned char* vp = static_cast<const unsigned char*>(p.value_cache);
     for (int64_t a = j0; a < j1;) {
         const int64_t e = min(j1, (a / p.block_size + 1) * p.block_size);
         const int64_t na = clamp64(L, a, e), nc = clamp64(N, a, e);
-        if (na > a)
-            bulk_g2s(dst + static_cast<uint32_t>((a - j0) * row_bytes), cache_row(p, pool, u, a, row_bytes),
-                     static_cast<uint32_t>((na - a) * row_bytes), bar);
-        if (nc > na)
-            bulk_g2s(dst + static_cast<uint32_t>((na - j0) * row_bytes), new_unit + (na - L) * row_bytes,
-                     static_cast<uint32_t>((nc - na) * row_bytes), bar);
-        if (e > nc)
-            bulk_g2s(dst + static_cast<uint32_t>((nc - j0) * row_bytes), cache_row(p, pool, u, nc, row_bytes),
-                     static_cast<uint32_t>((e - nc) * row_bytes), bar);
+        const int64_t base = tile_pool_unit(p, ids, u, a) * p.block_size - (a / p.block_size) * p.block_size;
+        // pool row of slot j in this block: base + j
+        if (na > a) {
+            bulk_g2s(dstK + static_cast<uint32_t>((a - j0) * rowK), kp + (base + a) * rowK,
+                     static_cast<uint32_t>((na - a) * rowK), bar);
+            bulk_g2s(dstV + static_cast<uint32_t>((a - j0) * rowV), vp + (base + a) * rowV,
+                     static_cast<uint32_t>((na - a) * rowV), bar);
+        }
+        if (nc > na) {
+            bulk_g2s(dstK + static_cast<uint32_t>((na - j0) * rowK), newK + (na - L) * rowK,
+                     static_cast<uint32_t>((nc - na) * rowK), bar);
+            bulk_g2s(dstV + static_cast<uint32_t>((na - j0) * rowV), newV + (na - L) * rowV,
+                     static_cast<uint32_t>((nc - na) * rowV), bar);
+        }
+        if (e > nc) {
+            bulk_g2s(dstK + static_cast<uint32_t>((nc - j0) * rowK), kp + (base + nc) * rowK,
+                     static_cast<uint32_t>((e - nc) * rowK), bar);
+            bulk_g2s(dstV + static_cast<uint32_t>((nc - j0) * rowV), vp + (base + nc) * rowV,
+                     static_cast<uint32_t>((e - nc) * rowV), bar);
+        }
         a = e;
     }
 }
