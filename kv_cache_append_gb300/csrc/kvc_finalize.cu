@@ -69,6 +69,7 @@ template <typename T>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     finalize_merge_kernel(const __grid_constant__ StepParams p) {
     using S = Storage<T>;
+    launch_dependents();  // the row writer's blocks may take their places now; they wait for this grid
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
     if (row >= p.B * p.Hq * p.Q) return;  // whole warps leave together
@@ -176,6 +177,9 @@ __global__ void __launch_bounds__(kFinalizeThreads)
     const int64_t row = blockIdx.x / p.fin_nseg;
     const int64_t seg = blockIdx.x - row * p.fin_nseg;
     const int64_t j_begin = seg * p.fin_seg, j_end = min(p.M, j_begin + p.fin_seg);
+    // Launched as a dependent of the merge, this block may be resident before
+    // the merge ends: it waits for the merge before reading the row record.
+    grid_dependency_wait();
     const RowStat st = p.rowstat[row];
     const int64_t lim = st.lim;
     T* att = static_cast<T*>(p.out_attention) + row * p.M;
@@ -218,13 +222,23 @@ __global__ void __launch_bounds__(kFinalizeThreads)
     }
 }
 
+// The row writer is launched as a programmatic dependent of the merge: its
+// blocks may become resident while the merge runs (no launch gap between the
+// two) and wait for it before reading the merged row records.
 template <typename T>
 cudaError_t rows_t(const StepParams& p, dim3 grid, cudaStream_t stream) {
-    if (p.score_fmt == 1)
-        finalize_rows_kernel<T, 1><<<grid, kFinalizeThreads, 0, stream>>>(p);
-    else
-        finalize_rows_kernel<T, 0><<<grid, kFinalizeThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kFinalizeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.score_fmt == 1) return cudaLaunchKernelEx(&cfg, finalize_rows_kernel<T, 1>, p);
+    return cudaLaunchKernelEx(&cfg, finalize_rows_kernel<T, 0>, p);
 }
 
 }  // namespace

@@ -292,6 +292,16 @@ __device__ __forceinline__ void consumer_sync() {
 }
 
 // 2^x on the MUFU unit; exp2(-inf) = +0.
+// Programmatic dependent launch: a grid lets the grid launched after it on
+// its stream start early; that grid waits here until this one has finished
+// and its writes are visible (a no-op when it was launched normally).
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
