@@ -129,11 +129,18 @@ void workspace_layout(const kvc_dims& d, int64_t KP, Plan* pl) {
     pl->ws_bytes = static_cast<size_t>(off);
 }
 
+// Cache bytes per tile of the fused kernel. A step that copies the caches
+// keeps tiles of 32 KB: more ring stages keep more copies in flight, which
+// copy-heavy steps (short rows) need. Without the copy (in place, read-only,
+// paged) the consumers bound the step and 64 KB tiles halve their per-tile
+// overhead per slot (decode in place: 0.536 -> 0.466 ms per step).
+constexpr int64_t kStageTargetInplace = 2 * kStageTargetBytes;
+
 // Tiling of the fused kernel that depends only on the sizes.
-void fused_tiling(const kvc_dims& d, Plan* pl) {
+void fused_tiling(const kvc_dims& d, Plan* pl, int64_t stage_target = kStageTargetBytes) {
     const int64_t es = elem_size(d.dtype);
     const int64_t row = (d.D + d.Dv) * es;
-    int64_t T = kStageTargetBytes / row / 32 * 32;
+    int64_t T = stage_target / row / 32 * 32;
     T = std::max<int64_t>(32, std::min<int64_t>(128, T));
     if (d.M < T) T = align_up(d.M, 32);
     pl->T = static_cast<int>(T);
@@ -190,9 +197,10 @@ int64_t sizing_kp(const kvc_dims& d, int64_t T, int64_t TPU) {
 
 // Full fused plan for a device with `sms` SMs and `smem_cap` bytes of
 // opt-in shared memory per block. False if it does not fit.
-bool fused_plan(const kvc_dims& d, int sms, int smem_cap, bool query_aligned, Plan* pl) {
+bool fused_plan(const kvc_dims& d, int sms, int smem_cap, bool query_aligned, Plan* pl,
+                int64_t stage_target = kStageTargetBytes) {
     if (!fused_shapes(d)) return false;
-    fused_tiling(d, pl);
+    fused_tiling(d, pl, stage_target);
     const int64_t es = elem_size(d.dtype);
     const int64_t R = (d.Hq / d.Hk) * d.Q;
     const int64_t qbytes = R * d.D * es;
@@ -417,7 +425,10 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     Plan pl;
     if (!(ptrs_aligned && aligned16(query) && tc_pages &&
           tc_plan(d, dev.sms, dev.smem_optin, &pl)) &&
-        !(ptrs_aligned && fused_plan(d, dev.sms, dev.smem_optin, aligned16(query), &pl)))
+        !(ptrs_aligned &&
+          ((inplace && fused_plan(d, dev.sms, dev.smem_optin, aligned16(query), &pl,
+                                  kStageTargetInplace)) ||
+           fused_plan(d, dev.sms, dev.smem_optin, aligned16(query), &pl, kStageTargetBytes))))
         generic_plan(d, &pl);
 
     if (pl.ws_bytes > 0) {
@@ -781,11 +792,14 @@ size_t kvc_workspace_bytes(const kvc_dims* dims) {
     generic_plan(*dims, &pl);
     size_t bytes = pl.ws_bytes;
     // more CTAs make smaller chunks, hence more partial slots: size for the most
-    if (fused_shapes(*dims)) {
-        Plan f;
-        fused_tiling(*dims, &f);
-        workspace_layout(*dims, sizing_kp(*dims, f.T, f.TPU), &f);
-        bytes = std::max(bytes, f.ws_bytes);
+    if (fused_shapes(*dims)) {  // both tile sizes (copying and in-place steps)
+        const int64_t targets[2] = {kStageTargetBytes, kStageTargetInplace};
+        for (const int64_t target : targets) {
+            Plan f;
+            fused_tiling(*dims, &f, target);
+            workspace_layout(*dims, sizing_kp(*dims, f.T, f.TPU), &f);
+            bytes = std::max(bytes, f.ws_bytes);
+        }
     }
     if (tc_shapes(*dims)) {
         Plan t;

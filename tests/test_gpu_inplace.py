@@ -2,9 +2,12 @@
 
 The caches are donated and updated in place: afterwards they must equal the
 oracle's updated caches bit for bit, the lengths must be exact, attention and
-context must meet the same tolerances as the out-of-place step, and — the
-kernels being the same — attention, context and lengths must equal the
-out-of-place step's bit for bit. Inputs other than the caches stay untouched.
+context must meet the same tolerances as the out-of-place step, and caches and
+lengths must equal the out-of-place step's bit for bit. Attention and context
+are compared with the out-of-place step within the step's tolerance only: the
+in-place step may cut the cache into larger tiles (it copies nothing), so its
+partial sums can round differently. Inputs other than the caches stay
+untouched.
 """
 import numpy as np
 import pytest
@@ -12,7 +15,7 @@ import torch
 
 import kv_cache_append_gb300 as kvc
 import workloads
-from test_gpu_parity import (DEV, SMALL, TC, _bits, _built, check_append_property,  # noqa: F401
+from test_gpu_parity import (DEV, SMALL, TC, TOL, _bits, _built, check_append_property,  # noqa: F401
                              compare_batch_rows, compare_full, run_gpu)
 from workloads import Spec
 
@@ -33,9 +36,13 @@ def run_inplace(x: workloads.StepInputs):
 
 def same_as_out_of_place(xg, out):
     ref, _ = run_gpu(xg)
-    for k in ("key_cache", "value_cache", "attention", "context"):
+    for k in ("key_cache", "value_cache"):
         assert torch.equal(_bits(out[k]), _bits(ref[k])), k
     assert torch.equal(out["lengths"], ref["lengths"])
+    atol_a, atol_c = TOL[xg.query.dtype]
+    for k, atol in (("attention", atol_a), ("context", atol_c)):
+        np.testing.assert_allclose(out[k].double().cpu().numpy(), ref[k].double().cpu().numpy(),
+                                   rtol=0, atol=atol, err_msg=k)
 
 
 CASES = {
