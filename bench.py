@@ -135,20 +135,30 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
-    summary, if it was taken on the kernel's current source; else None."""
+def mode_key(args) -> str:
+    """Key of a workload and step face in the traffic record, e.g.
+    "gqa_decode", "inplace:gqa_decode", "paged64:gqa_decode"."""
+    mode = ("readonly" if args.readonly else f"paged{args.paged}" if args.paged else
+            "inplace" if args.inplace else "")
+    return f"{mode}:{args.workload}" if mode else args.workload
+
+
+def kernel_traffic(key: str, kernel: str, algorithmic: int):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary for
+    `key`, scaled from the captured launch to this one by their algorithmic
+    bytes, if the capture was taken on the kernel's current source; else None."""
     if kernel not in KERNEL_SOURCES:
         return None
     try:
         with open(TRAFFIC_FILE) as f:
-            entry = json.load(f)["workloads"][workload]
+            entry = json.load(f)["workloads"][key]
+        cap = entry["captured"]
     except Exception:
         return None
     if entry.get("kernel") != kernel or \
             entry.get("kernel_source_sha256") != source_digest(KERNEL_SOURCES[kernel]):
         return None
-    return float(entry["dram_bytes_per_launch"])
+    return round(float(cap["dram_bytes"]) * algorithmic / float(cap["algorithmic_bytes"]))
 
 
 # ----------------------------------------------------------------- clocks
@@ -454,8 +464,7 @@ def run_ours(args, spec, world, rank, local):
     kname = STEP_KERNEL[path]
     if args.readonly and path == "generic":
         kname = "generic_attend_kernel"
-    traffic = (None if (args.inplace or args.readonly or args.paged)
-               else kernel_traffic(args.workload, kname))
+    traffic = kernel_traffic(mode_key(args), kname, nbytes["fused_kernel"])
 
     # ---- end to end through the public API: pinned host in, pinned host out
     e2e = None
@@ -494,6 +503,7 @@ def run_ours(args, spec, world, rank, local):
         "bytes_per_step": nbytes["total"],
         "path": path,
         "kernels": {kname: {"ms": round(kern_ms[ks], 4),
+                            "algorithmic_bytes": nbytes["fused_kernel"],
                             "algorithmic_GBps": round(achieved, 1)}},
         "roofline": {"bound": "hbm", "kernel": kname,
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
