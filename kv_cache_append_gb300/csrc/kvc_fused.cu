@@ -328,13 +328,15 @@ __device__ __forceinline__ void tile_rows(const StepParams& p, int rg, int ws, i
 
 // Decode-shaped variant: 4 query rows per warp held in registers for the
 // whole piece (NCHL 16-byte chunks of each row per lane), packed fp32 FMAs,
-// a per-lane running sum reduced only at the end of the piece, and passes and
-// slots clipped to the rows' last allowed slot.
+// scores reduced by a reduce-scatter butterfly (4 shuffles per 4 slots and 4
+// rows), two passes in flight, a per-lane running sum reduced only at the end
+// of the piece, and passes and slots clipped to the rows' last allowed slot.
+// mylim / myoff belong to row sub/2, the row whose scores this lane ends with.
 template <typename T, int NCHL, int DVC>
 __device__ __forceinline__ void tile_rows_qr(
     const StepParams& p, int ws, int j0, const unsigned char* sK, const unsigned char* sV,
-    const float2 (&qr)[4][NCHL][Storage<T>::kVec16 / 2], float* pb, const int (&lim)[4],
-    int maxlim, int mylim, int64_t myoff, float (&m)[4], float (&lp)[4],
+    const float2 (&qr)[4][NCHL][Storage<T>::kVec16 / 2], float* pb, int maxlim, int mylim,
+    int64_t myoff, float (&m)[4], float (&lp)[4],
     float2 (&acc)[4][DVC][2]) {
     using S = Storage<T>;
     constexpr int V2 = S::kVec16 / 2;
@@ -349,50 +351,67 @@ __device__ __forceinline__ void tile_rows_qr(
     const int npass = (nslot + 3) >> 2;
     __syncwarp();
 
-    float tmax[4];
+    // Each pass scores 4 slots (one per group of 8 lanes) for the 4 rows; the
+    // 8 lanes of a group reduce their partial dots with a reduce-scatter
+    // butterfly, after which lanes 2r and 2r+1 hold row r's score.
+    constexpr int UNR = 2;  // passes scored together (the second one clamped to the last)
+    const bool h4 = (sub & 4) != 0, h2 = (sub & 2) != 0;
+    const int ri = sub >> 1;
+    float tm = -INFINITY;
+    for (int pp = 0; pp < npass; pp += UNR) {
+        float kd[UNR];
+        int sls[UNR];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) tmax[i] = -INFINITY;
-    for (int pp = 0; pp < npass; ++pp) {
-        const int sl = ws * SW + pp * 4 + gi;
-        const int j = j0 + sl;
-        float2 d2[4];
+        for (int uu = 0; uu < UNR; ++uu) {
+            sls[uu] = ws * SW + min(pp + uu, npass - 1) * 4 + gi;
+            float2 d2[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d2[i] = make_float2(0.f, 0.f);
-        const unsigned char* krow = sK + sl * rowK;
+            for (int i = 0; i < 4; ++i) d2[i] = make_float2(0.f, 0.f);
+            const unsigned char* krow = sK + sls[uu] * rowK;
 #pragma unroll
-        for (int c = 0; c < NCHL; ++c) {
-            const int ck = sub + 8 * c;
-            if (ck < nck) {
-                const uint4 raw = *reinterpret_cast<const uint4*>(krow + ck * 16);
-                float2 k2[V2];
-                S::widen16_2(raw, k2);
+            for (int c = 0; c < NCHL; ++c) {
+                const int ck = sub + 8 * c;
+                if (ck < nck) {
+                    const uint4 raw = *reinterpret_cast<const uint4*>(krow + ck * 16);
+                    float2 k2[V2];
+                    S::widen16_2(raw, k2);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                    for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int e = 0; e < V2; ++e) d2[i] = __ffma2_rn(qr[i][c][e], k2[e], d2[i]);
+                        for (int e = 0; e < V2; ++e) d2[i] = __ffma2_rn(qr[i][c][e], k2[e], d2[i]);
+                }
+            }
+            const float a0 = d2[0].x + d2[0].y, a1 = d2[1].x + d2[1].y;
+            const float a2 = d2[2].x + d2[2].y, a3 = d2[3].x + d2[3].y;
+            float k0 = h4 ? a2 : a0, k1 = h4 ? a3 : a1;
+            k0 += __shfl_xor_sync(0xffffffffu, h4 ? a0 : a2, 4);
+            k1 += __shfl_xor_sync(0xffffffffu, h4 ? a1 : a3, 4);
+            float kk = h2 ? k1 : k0;
+            kk += __shfl_xor_sync(0xffffffffu, h2 ? k0 : k1, 2);
+            kk += __shfl_xor_sync(0xffffffffu, kk, 1);
+            kd[uu] = kk;
+        }
+#pragma unroll
+        for (int uu = 0; uu < UNR; ++uu) {
+            if (pp + uu < npass) {
+                const int j = j0 + sls[uu];
+                const float sc = (j <= mylim) ? kd[uu] : -INFINITY;
+                tm = fmaxf(tm, sc);
+                if (!(sub & 1)) {
+                    pb[(sls[uu] - ws * SW) * 4 + ri] = sc;
+                    if (j <= mylim) p.scores[myoff + j] = sc;
+                }
             }
         }
-        float mine = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float d = d2[i].x + d2[i].y;
-            d += __shfl_xor_sync(0xffffffffu, d, 1);
-            d += __shfl_xor_sync(0xffffffffu, d, 2);
-            d += __shfl_xor_sync(0xffffffffu, d, 4);
-            const float sc = (j <= lim[i]) ? d : -INFINITY;
-            tmax[i] = fmaxf(tmax[i], sc);
-            if (sub == i) mine = sc;
-        }
-        if (sub < 4) {
-            pb[(pp * 4 + gi) * 4 + sub] = mine;
-            if (j <= mylim) p.scores[myoff + j] = mine;
-        }
     }
+    tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+    tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+    float tmax[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tmax[i] = __shfl_sync(0xffffffffu, tm, 2 * i);
     float corr[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 8));
-        tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 16));
         const float mn = fmaxf(m[i], tmax[i]);
         corr[i] = (mn == -INFINITY) ? 1.f : fast_exp2(m[i] - mn);
         m[i] = mn;
@@ -421,6 +440,7 @@ __device__ __forceinline__ void tile_rows_qr(
     }
     __syncwarp();
     const unsigned char* v0 = sV + ws * SW * rowV;
+#pragma unroll 4
     for (int sl = 0; sl < nslot; ++sl) {
         const float4 pv = *reinterpret_cast<const float4*>(pb + sl * 4);
         const float2 p2[4] = {make_float2(pv.x, pv.x), make_float2(pv.y, pv.y),
@@ -592,7 +612,7 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
                     myoff = 0;
 #pragma unroll
                     for (int ii = 0; ii < 4; ++ii) {
-                        if (sub == ii) {
+                        if ((sub >> 1) == ii) {  // the row this lane's scores end in
                             const int r = r0 + ii;
                             mylim = lim4[ii];
                             myoff = ((b * p.Hq + kv * p.G + r / Q) * p.Q + r % Q) * p.M;
@@ -640,8 +660,8 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
             const int j0 = mt.i * p.T;
             if constexpr (NCHL > 0) {
                 if (wr * 4 < R)
-                    tile_rows_qr<T, NCHL, DVC>(p, ws, j0, sK, sK + vofs, qr, pb, lim4, maxlim,
-                                               mylim, myoff, m4, lp, acc2);
+                    tile_rows_qr<T, NCHL, DVC>(p, ws, j0, sK, sK + vofs, qr, pb, maxlim, mylim,
+                                               myoff, m4, lp, acc2);
             } else {
                 for (int rgi = 0; rgi < p.NRG; ++rgi) {
                     const int rg = wr + rgi * p.WR;

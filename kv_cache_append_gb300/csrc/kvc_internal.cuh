@@ -63,14 +63,20 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar, uint32_t count) {
                  : "memory");
 }
 
+// Suspend-time hint of mbarrier.try_wait (ns): a waiting thread sleeps in
+// hardware until the phase completes or the hint runs out, instead of
+// spinning on the issue slots the consumer warps need.
+#ifndef KVC_WAIT_HINT_NS
+#define KVC_WAIT_HINT_NS 20000
+#endif
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(static_cast<uint32_t>(KVC_WAIT_HINT_NS))
         : "memory");
     return ok != 0;
 }
