@@ -38,7 +38,7 @@ FALLBACK_HBM_GBS = 6800.0
 _CSRC = "kv_cache_append_gb300/csrc/"
 # The first kernel of each path and the sources that define it.
 STEP_KERNEL = {"fused": "fused_step_kernel", "tensor": "tc_step_kernel",
-               "generic": "generic_copy_kernel"}
+               "decode_tc": "decode_tc_kernel", "generic": "generic_copy_kernel"}
 # Every kernel of a step with query rows, in launch order (in place: the
 # cache write comes first and the generic path has no copy kernel).
 PATH_KERNELS_INPLACE = {
@@ -46,6 +46,8 @@ PATH_KERNELS_INPLACE = {
               "finalize_rows_kernel"],
     "tensor": ["inplace_rows_kernel", "tc_step_kernel", "finalize_merge_kernel",
                "finalize_rows_kernel"],
+    "decode_tc": ["inplace_rows_kernel", "decode_tc_kernel", "finalize_merge_kernel",
+                  "finalize_rows_kernel"],
     "generic": ["inplace_rows_kernel", "generic_attend_kernel", "finalize_merge_kernel",
                 "finalize_rows_kernel"]}
 PATH_KERNELS_PAGED = {
@@ -53,7 +55,7 @@ PATH_KERNELS_PAGED = {
 PATH_KERNELS_READONLY = {
     path: ["attend_prep_kernel", STEP_KERNEL[path] if path != "generic" else "generic_attend_kernel",
            "finalize_merge_kernel", "attend_unpack_kernel"]
-    for path in ("fused", "tensor", "generic")}
+    for path in ("fused", "tensor", "decode_tc", "generic")}
 PATH_KERNELS = {"fused": ["fused_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "tensor": ["tc_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "generic": ["generic_copy_kernel", "generic_attend_kernel",
@@ -63,6 +65,8 @@ KERNEL_SOURCES = {
                                               "kvc_pipeline.cuh")],
     "tc_step_kernel": [_CSRC + f for f in ("kvc_fused_tc.cu", "kvc_internal.cuh",
                                            "kvc_pipeline.cuh", "kvc_tcgen05.cuh")],
+    "decode_tc_kernel": [_CSRC + f for f in ("kvc_decode_tc.cu", "kvc_internal.cuh",
+                                             "kvc_pipeline.cuh", "kvc_tcgen05.cuh")],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
 
@@ -365,7 +369,7 @@ def run_ours(args, spec, world, rank, local):
         ws = torch.empty(kvc.paged_workspace_bytes(dims), dtype=torch.uint8, device=dev)
         nkern = 5 if spec.Q > 0 else 2
         path = kvc.plan_info_inplace(dims, kc_p, vc_p, nk, nv)[1]
-        if path == "tensor" and not (bs % 64 == 0 or (64 % bs == 0 and bs >= 8)):
+        if path in ("tensor", "decode_tc") and not (bs % 64 == 0 or (64 % bs == 0 and bs >= 8)):
             path = "fused"
 
         def step(events=None):
@@ -390,7 +394,7 @@ def run_ours(args, spec, world, rank, local):
         ws = torch.empty(kvc.attend_cache_workspace_bytes(dims), dtype=torch.uint8, device=dev)
         torch.cuda.empty_cache()
         nkern = 4
-        path = kvc.plan_info(dims, kc_p, vc_p, nk, nv, kc_p, vc_p)[1]
+        path = kvc.plan_info_inplace(dims, kc_p, vc_p, nk, nv)[1]
 
         def step(events=None):
             kvc.attend_cache_into(dims, Bn, q_packed, kc_p, vc_p, cu, kl, False, slots, scale,

@@ -188,8 +188,12 @@ KVC_API int kvc_step_inplace_timed(const kvc_dims *dims, const void *query, cons
                            void *stream, void *const *events, int n_events);
 
 /*
- * Kernel count and path name (as kvc_plan_info) of kvc_step_inplace for
- * these sizes and pointers.
+ * Kernel count and path name of kvc_step_inplace for these sizes and
+ * pointers: as kvc_plan_info, or "decode_tc" where the step that copies no
+ * cache runs its attention on the decode tensor-core kernel (16-bit caches,
+ * D a multiple of 64 up to 256, Dv = 128, at most 16 query rows per KV head).
+ * The read-only re-attention and the paged step (block sizes that are a
+ * multiple of 64, or 8, 16 or 32) take the same path.
  */
 KVC_API int kvc_plan_info_inplace(const kvc_dims *dims, const void *key_cache,
                           const void *value_cache, const void *new_key, const void *new_value,

@@ -76,6 +76,8 @@ int check_dims(const kvc_dims* d) {
 struct Plan {
     bool fused = false;
     bool tensor = false;  // the tensor-core fused kernel (kvc_fused_tc.cu)
+    bool dec = false;     // the decode tensor-core kernel (kvc_decode_tc.cu)
+    int dec_off_red = 0, dec_off_pt = 0, dec_nr = 16;
     int tc_off_stg = 0, tc_stg_bytes = 0, tc_tmem_cols = 0;
     int64_t tc_nrg = 1;
     size_t off_tile_max = 0;
@@ -303,6 +305,56 @@ bool tc_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
     return true;
 }
 
+#ifndef KVC_DECODE_TC
+#define KVC_DECODE_TC 1
+#endif
+constexpr int kDecT = 128;  // slots per tile of the decode tensor-core kernel
+
+// Shapes the decode tensor-core kernel takes (steps that copy no cache):
+// 16-bit caches, key width a multiple of 64 (at most 256), value width 128,
+// 1..16 query rows per unit.
+bool dec_shapes(const kvc_dims& d) {
+    const int64_t R = (d.Hq / d.Hk) * d.Q;
+    return KVC_DECODE_TC && d.dtype != KVC_F32 && d.D % 64 == 0 && d.D <= 256 && d.Dv == 128 &&
+           d.Q >= 1 && R <= 16 && d.B * d.Hk * R < (int64_t(1) << 31) &&
+           d.M < (int64_t(1) << 30);
+}
+
+void dec_tiling(const kvc_dims& d, Plan* pl) {
+    pl->T = kDecT;
+    pl->TPU = (d.M + kDecT - 1) / kDecT;
+}
+
+// Shared memory: barriers | abort flag | tile metadata | exchange buffers |
+// two P^T buffers (16 rows x 128 slots) | stages of K (128 x D), V (128 x Dv)
+// and the unit's 16 query rows, all in 64-element column blocks.
+bool dec_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
+    if (!dec_shapes(d)) return false;
+    *pl = Plan();
+    dec_tiling(d, pl);
+    const int64_t nkb = d.D / 64, nvb = d.Dv / 64;
+    const int64_t R = (d.Hq / d.Hk) * d.Q;
+    pl->off_flag = 512;
+    pl->off_meta = 1024;  // kMaxStages records of 32 bytes
+    int64_t off = 1024 + int64_t(kMaxStages) * 32;
+    pl->dec_off_red = static_cast<int>(off);  // [2][16][4] values, [2][4] flags
+    off = align_up(off + 2 * 16 * 4 * 4 + 2 * 4 * 4, 1024);
+    pl->dec_off_pt = static_cast<int>(off);
+    off += 2 * 2 * 16 * 128;
+    pl->off_stages = static_cast<int>(off);
+    const int64_t stage = (nkb + nvb) * kDecT * 128 + nkb * 16 * 128;
+    pl->stage_bytes = static_cast<int>(stage);
+    if (off + 2 * stage > smem_cap) return false;
+    pl->NS = static_cast<int>(std::min<int64_t>(kMaxStages, (smem_cap - off) / stage));
+    pl->smem = static_cast<size_t>(off + int64_t(pl->NS) * stage);
+    pl->dec_nr = R <= 4 ? 4 : R <= 8 ? 8 : 16;
+    chunking(d, sms, pl);
+    pl->P = std::min<int64_t>(sms, pl->NQ);
+    pl->dec = true;
+    workspace_layout(d, pl->KP, pl);
+    return true;
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -425,6 +477,8 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     Plan pl;
     if (!(ptrs_aligned && aligned16(query) && tc_pages &&
           tc_plan(d, dev.sms, dev.smem_optin, &pl)) &&
+        !(inplace && ptrs_aligned && aligned16(query) && tc_pages &&
+          dec_plan(d, dev.sms, dev.smem_optin, &pl)) &&
         !(ptrs_aligned &&
           ((inplace && fused_plan(d, dev.sms, dev.smem_optin, aligned16(query), &pl,
                                   kStageTargetInplace)) ||
@@ -505,6 +559,8 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     p.tc_nrg = pl.tc_nrg;
     p.tc_stg_bytes = pl.tc_stg_bytes;
     p.tc_tmem_cols = pl.tc_tmem_cols;
+    p.dec_off_red = pl.dec_off_red;
+    p.dec_off_pt = pl.dec_off_pt;
     p.dev_status = dev_status;
     p.vec_attention = (d.M % 8 == 0) && aligned16(out_attention);
     p.inplace = inplace ? 1 : 0;
@@ -553,6 +609,26 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
                 return KVC_E_CUDA;
             e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream);
             if (e == cudaSuccess) e = launch_fused_tc(tp, d.dtype, pl.smem, stream);
+            if (e == cudaSuccess) e = record();
+        } else if (pl.dec) {
+            DecParams dp;
+            std::memset(&dp, 0, sizeof(dp));
+            dp.p = p;
+            const int64_t bh = paged ? std::min<int64_t>(kDecT / 2, mode.block_size) : kDecT / 2;
+            const bool ok_maps =
+                (paged ? cache_map(&dp.tm_k, key_cache, d.dtype, d.D, mode.block_size,
+                                   mode.num_blocks * d.Hk, bh) &&
+                             cache_map(&dp.tm_v, value_cache, d.dtype, d.Dv, mode.block_size,
+                                       mode.num_blocks * d.Hk, bh)
+                       : cache_map(&dp.tm_k, key_cache, d.dtype, d.D, d.M, CU, bh) &&
+                             cache_map(&dp.tm_v, value_cache, d.dtype, d.Dv, d.M, CU, bh)) &&
+                rows_map(&dp.tm_q, const_cast<void*>(query),
+                         d.dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                         2, d.D, d.D, d.B * d.Hk * p.R, 1, 64, 16);
+            if (!ok_maps) return KVC_E_CUDA;
+            e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream);
+            if (e == cudaSuccess) e = launch_decode_tc(dp, d.dtype, pl.dec_nr, pl.smem, stream);
             if (e == cudaSuccess) e = record();
         } else if (pl.fused) {
             // chunks are handed out from a counter that starts at zero
@@ -807,6 +883,12 @@ size_t kvc_workspace_bytes(const kvc_dims* dims) {
         workspace_layout(*dims, sizing_kp(*dims, t.T, t.TPU), &t);
         bytes = std::max(bytes, t.ws_bytes);
     }
+    if (dec_shapes(*dims)) {
+        Plan t;
+        dec_tiling(*dims, &t);
+        workspace_layout(*dims, sizing_kp(*dims, t.T, t.TPU), &t);
+        bytes = std::max(bytes, t.ws_bytes);
+    }
     return bytes;
 }
 
@@ -883,9 +965,17 @@ int kvc_plan_info(const kvc_dims* dims, const void* key_cache, const void* value
 
 int kvc_plan_info_inplace(const kvc_dims* dims, const void* key_cache, const void* value_cache,
                           const void* new_key, const void* new_value, const char** path_name) {
+    using namespace kvc;
     const int rc = kvc_plan_info(dims, key_cache, value_cache, new_key, new_value, key_cache,
                                  value_cache, path_name);
     if (rc < 0) return rc;
+    DeviceInfo dev;
+    Plan pl;
+    if (path_name && std::strcmp(*path_name, "tensor") != 0 && device_info(&dev) == cudaSuccess &&
+        aligned16(key_cache) && aligned16(value_cache) &&
+        (dims->Q == 0 || (aligned16(new_key) && aligned16(new_value))) &&
+        dec_plan(*dims, dev.sms, dev.smem_optin, &pl))
+        *path_name = "decode_tc";
     // the cache write, then with query rows the step kernel, the merge and the row writer
     return dims->Q > 0 ? 4 : 1;
 }

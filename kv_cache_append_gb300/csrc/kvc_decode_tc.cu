@@ -1,0 +1,584 @@
+// kvc_decode_tc.cu -- attention of the steps that copy no cache (in place,
+// read-only re-attention, paged) on the tensor cores, for units of at most 16
+// query rows (G = Hq/Hk heads x Q new tokens): decode and short speculative
+// steps.
+//
+// Without the cache copy such a step reads each valid cache row once and
+// does 2 * R * (D + Dv) flops on it; on the CUDA cores the few rows per unit
+// cost tens of instructions per slot and warp, and the instruction issue, not
+// HBM, bounds the step. Here the cache slots are the M dimension of both
+// tcgen05 products of a 128-slot tile, with the unit's query rows as N = 16
+// (padded):
+//
+//   S^T  = K Q^T      M = 128 slots, N = 16 rows, K = D    (A = K tile, B = Q)
+//   O^T += V^T P^T    M = Dv = 128,  N = 16 rows, K = 128 slots
+//                                               (A = V tile read M-major, B = P^T)
+//
+// so per tile the tensor cores take the dot products and the weighted sum,
+// and each softmax thread handles one slot for the R rows.
+//
+//   producer warp   takes chunks of tiles of one unit from the global counter
+//                   (the fused kernel's chunking and hand-out order), TMA-loads
+//                   each tile's K and V rows below the new length (64-element
+//                   boxes, 128-byte swizzle, the layout the tensor cores read)
+//                   and the unit's query rows (16 rows, 4 KB from L2) with it.
+//   MMA warp        one thread: S^T into one of two tensor-memory buffers,
+//                   then O^T += V^T P^T into the tensor-memory O^T.
+//   4 softmax warps one slot per thread (= the tensor-memory lane of S^T):
+//                   applies scale*log2(e) and the lower-right causal limit
+//                   j <= length + t ("Required behavior", bullet 4), keeps the
+//                   fp32 scores for the attention rows, writes P^T =
+//                   2^(s - ref) into shared memory (the second product's B
+//                   operand) and sets the value rows from the new length on to
+//                   zero in the tile, so that whatever the cache holds there
+//                   (Inf, NaN) cannot reach O^T through a zero weight. Each row
+//                   keeps one reference maximum, raised (and O^T rescaled) only
+//                   when a score exceeds it by more than 2^8; at the end of a
+//                   chunk each thread (= the value column of O^T) writes the
+//                   row partials (reference, sum, weighted values).
+//
+// The scores and partials have the fused kernel's layout, so the same merge
+// and row writer (kvc_finalize.cu) finish the step ("stable softmax on
+// allowed keys", bullet 5).
+//
+// Tensor memory (64 columns x 128 lanes, fp32): S^T buffers at columns 0 and
+// 16, O^T at 32 (lane = value column, column = query row).
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "kvc_internal.cuh"
+#include "kvc_launch.h"
+#include "kvc_pipeline.cuh"
+#include "kvc_tcgen05.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int kDT = 128;             // slots per tile (M of S^T = K Q^T)
+constexpr int kDN = 16;              // query rows of a unit, padded (N of both products)
+constexpr int kBlk = kDT * 128;      // one 64-element-wide column block of a K or V tile
+constexpr int kNBlk = kDN * 128;     // one 64-element-wide column block of Q or P^T
+constexpr int kHalf = 64;            // slots per TMA box of a contiguous cache
+constexpr int kSoftWarps = 4;
+constexpr int kMmaWarp = 4, kProdWarp = 5;
+constexpr int kDecThreads = 6 * 32;
+constexpr float kRescale = 8.f;      // raise a row's reference maximum when exceeded by 2^8
+constexpr uint32_t kTmemCols = 64;
+constexpr uint32_t kColO = 32;
+
+struct DecBars {
+    uint32_t base;
+    __device__ uint32_t full(int s) const { return base + 8u * s; }
+    __device__ uint32_t empty(int s) const { return base + 128u + 8u * s; }
+    __device__ uint32_t s_ready(int b) const { return base + 256u + 8u * b; }
+    __device__ uint32_t s_free(int b) const { return base + 272u + 8u * b; }
+    // one pair per P^T buffer, as in the tensor-core step kernel
+    __device__ uint32_t p_ready(int b) const { return base + 288u + 8u * b; }
+    __device__ uint32_t o_done(int b) const { return base + 304u + 8u * b; }
+    __device__ uint32_t rendezvous() const { return base + 320u; }  // the 4 softmax warps
+    __device__ uint32_t drained() const { return base + 328u; }
+};
+constexpr int kTmemSlot = 336;  // tensor-memory base address written by tcgen05.alloc
+
+// Reduce v[0..NR) over the 32 lanes of a warp (maximum or sum) by a
+// reduce-scatter butterfly: NR - 1 + 5 - log2(NR) shuffles instead of 5 NR.
+// Returns row (lane >> (5 - log2 NR))'s result, held by every lane of that
+// row's group of 32 / NR lanes.
+template <int NR, bool MAX>
+__device__ __forceinline__ float warp_reduce_rows(const float (&v)[NR]) {
+    const int lane = threadIdx.x & 31;
+    float a[NR];
+#pragma unroll
+    for (int i = 0; i < NR; ++i) a[i] = v[i];
+    int o = 16;
+#pragma unroll
+    for (int h = NR / 2; h >= 1; h /= 2, o /= 2) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float keep = up ? a[i + h] : a[i];
+            const float send = up ? a[i] : a[i + h];
+            const float got = __shfl_xor_sync(0xffffffffu, send, o);
+            a[i] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+    }
+#pragma unroll
+    for (; o >= 1; o /= 2) {
+        const float got = __shfl_xor_sync(0xffffffffu, a[0], o);
+        a[0] = MAX ? fmaxf(a[0], got) : a[0] + got;
+    }
+    return a[0];
+}
+
+template <int NR>
+struct RowsLog2;
+template <>
+struct RowsLog2<4> { static constexpr int v = 2; };
+template <>
+struct RowsLog2<8> { static constexpr int v = 3; };
+template <>
+struct RowsLog2<16> { static constexpr int v = 4; };
+
+__device__ void dec_producer(const DecParams& dp, unsigned char* smem, DecBars bars,
+                             volatile int* abort) {
+    const StepParams& p = dp.p;
+    const uint32_t stage0 = smem_addr(smem + p.off_stages);
+    TileMeta* meta = reinterpret_cast<TileMeta*>(smem + p.off_meta);
+    const int nkb = static_cast<int>(p.D / 64), nvb = static_cast<int>(p.Dv / 64);
+    const uint32_t q_bytes = static_cast<uint32_t>(nkb * kNBlk);
+    const int64_t U = p.B * p.Hk;
+    int64_t issued = 0;
+    Ring ring;
+    bool ok = true;
+    while (ok) {
+        const int64_t q = atomicAdd(p.counter, 1u);
+        if (q >= p.NQ) break;
+        const int64_t idx = chunk_of(q, p.NQ);  // chunk-index-major list
+        const int64_t k = idx / U, u = idx - k * U;
+        const Unit x = load_unit(p, u);
+        // only the tiles below the new length are read (nothing is copied)
+        const int64_t iend = x.n > 0 ? min(p.TPU, (x.N + kDT - 1) / kDT) : 0;
+        const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, iend);
+        if (i0 >= i1) continue;
+        for (int64_t i = i0; i < i1; ++i) {
+            if (issued >= p.NS && !mbar_wait(bars.empty(ring.s), ring.ph ^ 1u, abort)) {
+                ok = false;
+                break;
+            }
+            TileMeta& mt = meta[ring.s];
+            mt.L = x.L;
+            mt.u = u;
+            mt.n = static_cast<int32_t>(x.n);
+            mt.i = static_cast<int32_t>(i);
+            mt.k = static_cast<int32_t>(k);
+            mt.flags = (i == i0 ? kFirst : 0) | (i == i1 - 1 ? kLast : 0);
+            const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
+            const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBlk);
+            const uint32_t sQ = sV + static_cast<uint32_t>(nvb * kBlk);
+            const int64_t j0 = i * kDT;
+            const uint32_t full = bars.full(ring.s);
+            if (!p.block_table) {
+                // one or two boxes of 64 slots per column block: those holding slots below N
+                const int nh = x.N - j0 > kHalf ? 2 : 1;
+                mbar_arrive_expect_tx(full, static_cast<uint32_t>(nh * kHalf * 128 * (nkb + nvb)) +
+                                                q_bytes);  // publishes the metadata too
+                const int z = static_cast<int>(cache_unit(p, u));
+                for (int h = 0; h < nh; ++h) {
+                    const int y = static_cast<int>(j0) + h * kHalf;
+                    const uint32_t o = static_cast<uint32_t>(h * kHalf * 128);
+                    for (int b = 0; b < nkb; ++b)
+                        tma_load_3d(sK + b * kBlk + o, &dp.tm_k, 64 * b, y, z, full);
+                    for (int b = 0; b < nvb; ++b)
+                        tma_load_3d(sV + b * kBlk + o, &dp.tm_v, 64 * b, y, z, full);
+                }
+            } else {
+                // paged: one box of min(64, block_size) slots per block piece of the
+                // tile below the new length (their block ids were checked); the pool
+                // maps are [blocks * Hk][block_size][width]
+                const int64_t hh = min(static_cast<int64_t>(kHalf), p.block_size);
+                const int64_t npc = min((x.N - j0 + hh - 1) / hh, kDT / hh);
+                mbar_arrive_expect_tx(full, static_cast<uint32_t>(npc * hh * 128 * (nkb + nvb)) +
+                                                q_bytes);
+                for (int64_t c = 0; c < npc; ++c) {
+                    const int64_t j = j0 + c * hh;
+                    const int y = static_cast<int>(j % p.block_size);
+                    const int z = static_cast<int>(paged_unit(p, u, j));
+                    const uint32_t o = static_cast<uint32_t>(c * hh * 128);
+                    for (int b = 0; b < nkb; ++b)
+                        tma_load_3d(sK + b * kBlk + o, &dp.tm_k, 64 * b, y, z, full);
+                    for (int b = 0; b < nvb; ++b)
+                        tma_load_3d(sV + b * kBlk + o, &dp.tm_v, 64 * b, y, z, full);
+                }
+            }
+            // the unit's R query rows are rows [u R, u R + 16) of the [U R][D] query view
+            const int qy = static_cast<int>(u * p.R);
+            for (int b = 0; b < nkb; ++b) tma_load_3d(sQ + b * kNBlk, &dp.tm_q, 64 * b, qy, 0, full);
+            ++issued;
+            ring.next(p.NS);
+        }
+    }
+    if (ok) {  // sentinel tile: tells the other roles to stop
+        if (issued < p.NS || mbar_wait(bars.empty(ring.s), ring.ph ^ 1u, abort)) {
+            meta[ring.s].flags = kDone;
+            mbar_arrive_expect_tx(bars.full(ring.s), 0u);
+            return;
+        }
+    }
+    // gave up: do not leave while issued copies may still write shared memory
+    for (int64_t q = issued > p.NS ? issued - p.NS : 0; q < issued; ++q)
+        mbar_drain(bars.full(static_cast<int>(q % p.NS)), static_cast<uint32_t>((q / p.NS) & 1));
+}
+
+// One thread issues every tensor-core instruction of the CTA.
+__device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars bars,
+                               volatile int* abort, uint32_t tmem, bool bf16) {
+    const StepParams& p = dp.p;
+    const uint32_t stage0 = smem_addr(smem + p.off_stages);
+    const uint32_t pt0 = smem_addr(smem + p.dec_off_pt);
+    const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
+    const int nkb = static_cast<int>(p.D / 64), nvb = static_cast<int>(p.Dv / 64);
+    const uint32_t idesc_s = mma_idesc_f16(kDT, kDN, bf16, false, false);
+    const uint32_t idesc_o = mma_idesc_f16(static_cast<int>(p.Dv), kDN, bf16, false, true);
+    Ring ring;
+    int sbuf = 0;
+    int s_uses[2] = {0, 0};
+    int64_t pv_count = 0;  // products O^T += V^T P^T issued; the c-th reads P^T[c % 2]
+    bool attend = false, has_pending = false, pend_first = false;
+    int pend_stage = 0;
+    int64_t N = 0;
+
+    auto issue_pv = [&](int stage, bool first) -> bool {
+        const int pb = static_cast<int>(pv_count & 1);
+        if (!mbar_wait(bars.p_ready(pb), static_cast<uint32_t>((pv_count >> 1) & 1), abort))
+            return false;
+        tc_fence_after();
+        const uint32_t sV = stage0 + static_cast<uint32_t>(stage) * p.stage_bytes +
+                            static_cast<uint32_t>(nkb * kBlk);
+        const uint32_t sP = pt0 + static_cast<uint32_t>(pb * 2 * kNBlk);
+#pragma unroll
+        for (int kk = 0; kk < kDT / 16; ++kk)  // 16 slots per step
+            tc_mma(tmem + kColO, smem_desc_sw128(sV + kk * 16 * 128, kBlk, 1024),
+                   smem_desc_sw128(sP + (kk >> 2) * kNBlk + (kk & 3) * 32, 16, 1024), idesc_o,
+                   !(first && kk == 0));
+        tc_commit(bars.o_done(pb));
+        tc_commit(bars.empty(stage));
+        ++pv_count;
+        return true;
+    };
+
+    for (;;) {
+        const int s = ring.s;
+        const uint32_t ph = ring.ph;
+        ring.next(p.NS);
+        if (!mbar_wait(bars.full(s), ph, abort)) break;
+        const TileMeta mt = meta[s];
+        if (mt.flags & kDone) break;
+        if (mt.flags & kFirst) {
+            N = mt.L + mt.n;
+            attend = mt.n > 0 && static_cast<int64_t>(mt.i) * kDT < N;
+        }
+        const bool comp = attend && static_cast<int64_t>(mt.i) * kDT < N;
+        if (comp) {
+            if (s_uses[sbuf] > 0 &&
+                !mbar_wait(bars.s_free(sbuf), static_cast<uint32_t>((s_uses[sbuf] - 1) & 1), abort))
+                break;
+            tc_fence_after();
+            const uint32_t sK = stage0 + static_cast<uint32_t>(s) * p.stage_bytes;
+            const uint32_t sQ = sK + static_cast<uint32_t>((nkb + nvb) * kBlk);
+            for (int kb = 0; kb < nkb; ++kb) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // 16 elements per step
+                    tc_mma(tmem + sbuf * kDN, smem_desc_sw128(sK + kb * kBlk + kk * 32, 16, 1024),
+                           smem_desc_sw128(sQ + kb * kNBlk + kk * 32, 16, 1024), idesc_s,
+                           (kb | kk) != 0);
+            }
+            tc_commit(bars.s_ready(sbuf));
+            ++s_uses[sbuf];
+            sbuf ^= 1;
+            // the previous tile's product goes after this tile's scores, so the
+            // softmax warps find S^T ready when they finish that tile
+            if (has_pending && !issue_pv(pend_stage, pend_first)) break;
+            has_pending = true;
+            pend_stage = s;
+            pend_first = (mt.flags & kFirst) != 0;
+        } else {
+            if (has_pending) {
+                if (!issue_pv(pend_stage, pend_first)) break;
+                has_pending = false;
+            }
+            mbar_arrive(bars.empty(s), 1u);
+        }
+        if ((mt.flags & kLast) && attend && has_pending) {
+            if (!issue_pv(pend_stage, pend_first)) break;
+            has_pending = false;
+        }
+    }
+    // every issued tensor-core instruction has finished before the CTA frees
+    // tensor memory (also when a wait gave up)
+    tc_commit(bars.drained());
+    volatile int never = 0;
+    mbar_wait(bars.drained(), 0u, &never);
+}
+
+template <typename T, int NR>
+__device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars bars,
+                            volatile int* abort, uint32_t tmem) {
+    using S = Storage<T>;
+    const StepParams& p = dp.p;
+    const int t = threadIdx.x;  // slot of the tile (lane of S^T); value column of O^T
+    const int w = t >> 5, lane = t & 31;
+    const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
+    const int R = static_cast<int>(p.R), Q = static_cast<int>(p.Q);
+    const int nkb = static_cast<int>(p.D / 64), nvb = static_cast<int>(p.Dv / 64);
+    const float qs = p.qscale;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(w * 32) << 16);  // this warp's lanes
+    unsigned char* stages = smem + p.off_stages;
+    unsigned char* pt = smem + p.dec_off_pt;
+    float* xval = reinterpret_cast<float*>(smem + p.dec_off_red);           // [2][kDN][4 warps]
+    int* xflag = reinterpret_cast<int*>(smem + p.dec_off_red + 2 * kDN * 4 * 4);  // [2][4 warps]
+    constexpr int kGroup = 32 / NR;  // lanes that end a reduction with one row
+    Ring ring;
+    int sbuf = 0;
+    int64_t su[2] = {0, 0};   // completions consumed per S^T buffer
+    int64_t comp = 0;         // attending tiles done = products issued for them
+    int64_t pvd[2] = {0, 0};  // completions consumed on o_done[0], o_done[1]
+    uint32_t rv = 0;          // rendezvous of the 4 warps so far
+    bool attend = false, first_tile = false;
+    int64_t L = 0, n = 0, N = 0, u = 0, k = 0, rowoff0 = 0;
+    int lim[NR];
+    float mref[NR], lsum[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        lim[r] = -1;
+        mref[r] = -INFINITY;
+        lsum[r] = 0.f;
+    }
+
+    // Wait until product c (which read P^T[c % 2]) has finished, consuming the
+    // completions of that buffer's barrier strictly in order.
+    auto wait_pv = [&](int64_t c) -> bool {
+        const int b = static_cast<int>(c & 1);
+        for (; pvd[b] <= (c >> 1); ++pvd[b])
+            if (!warp_wait(bars.o_done(b), static_cast<uint32_t>(pvd[b] & 1), abort)) return false;
+        return true;
+    };
+    // The 4 warps meet on an mbarrier (bounded, unlike bar.sync): what each
+    // wrote to buffer rv % 2 before is visible to all after. A warp is at most
+    // one rendezvous ahead of another, so two buffers never collide.
+    auto rendezvous = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.rendezvous(), 1u);
+        const bool ok = warp_wait(bars.rendezvous(), rv & 1u, abort);
+        ++rv;
+        return ok;
+    };
+
+    for (;;) {
+        const int s = ring.s;
+        const uint32_t ph = ring.ph;
+        ring.next(p.NS);
+        if (!warp_wait(bars.full(s), ph, abort)) break;
+        const TileMeta mt = meta[s];
+        if (mt.flags & kDone) break;
+        // the stage is refilled only after this tile's product, which follows
+        // everything this warp writes into it (p_ready)
+        if (lane == 0) mbar_arrive(bars.empty(s), 1u);
+        if (mt.flags & kFirst) {
+            u = mt.u;
+            k = mt.k;
+            L = mt.L;
+            n = mt.n;
+            N = L + n;
+            attend = n > 0 && static_cast<int64_t>(mt.i) * kDT < N;
+            if (attend) {
+                const int64_t b = u / p.Hk, kv = u - b * p.Hk;
+                rowoff0 = (b * p.Hq + kv * p.G) * p.Q * p.M;  // row r's scores at + r M
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    const int tr = r % Q;
+                    lim[r] = (r < R && tr < n) ? static_cast<int>(L + tr) : -1;
+                    mref[r] = -INFINITY;
+                    lsum[r] = 0.f;
+                }
+                first_tile = true;
+            }
+        }
+        const bool is_comp = attend && static_cast<int64_t>(mt.i) * kDT < N;
+        if (is_comp) {
+            if (!warp_wait(bars.s_ready(sbuf), static_cast<uint32_t>(su[sbuf] & 1), abort)) break;
+            ++su[sbuf];
+            tc_fence_after();
+            float sv[NR];
+            tmem_ldn<NR>(trow + static_cast<uint32_t>(sbuf * kDN), sv);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.s_free(sbuf), 1u);
+            sbuf ^= 1;
+            const int j0 = mt.i * kDT, j = j0 + t;
+            bool need = false;
+            float* srow = p.scores + rowoff0 + j;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const bool allowed = j <= lim[r];
+                sv[r] = allowed ? sv[r] * qs : -INFINITY;
+                if (allowed) srow[r * p.M] = sv[r];
+                need |= sv[r] > mref[r] + kRescale;
+            }
+            // raise decisions are taken for the whole tile (every warp the same)
+            const uint32_t bf = rv & 1u;
+            const int wneed = __any_sync(0xffffffffu, need);
+            if (lane == 0) xflag[bf * 4 + w] = wneed;
+            if (!rendezvous()) break;
+            const int4 fl = *reinterpret_cast<const int4*>(xflag + bf * 4);
+            float corr[NR];
+#pragma unroll
+            for (int r = 0; r < NR; ++r) corr[r] = 1.f;
+            bool rescale_o = false;
+            if (fl.x | fl.y | fl.z | fl.w) {
+                const uint32_t bm = rv & 1u;
+                const float mine = warp_reduce_rows<NR, true>(sv);
+                if ((lane & (kGroup - 1)) == 0)
+                    xval[(bm * kDN + (lane >> (5 - RowsLog2<NR>::v))) * 4 + w] = mine;
+                if (!rendezvous()) break;
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    const float4 q4 = *reinterpret_cast<const float4*>(xval + (bm * kDN + r) * 4);
+                    const float tmax = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
+                    if (tmax > mref[r] + kRescale) {
+                        if (mref[r] != -INFINITY) {
+                            corr[r] = fast_exp2(mref[r] - tmax);
+                            rescale_o = true;
+                        }
+                        lsum[r] *= corr[r];
+                        mref[r] = tmax;
+                    }
+                }
+            }
+            // P^T[comp % 2] is free once the product two tiles back has finished
+            if (comp >= 2 && !wait_pv(comp - 2)) break;
+            unsigned char* pbox = pt + (comp & 1) * 2 * kNBlk + (t >> 6) * kNBlk;
+            const int ck = (t & 63) >> 3, e2 = (t & 7) * 2;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const float e = (j <= lim[r]) ? fast_exp2(sv[r] - mref[r]) : 0.f;
+                lsum[r] += e;
+                *reinterpret_cast<T*>(pbox + r * 128 + ((ck ^ (r & 7)) << 4) + e2) = S::from_float(e);
+            }
+            if (j >= N) {  // a value row past the new length: zero in the tile
+                unsigned char* vrow =
+                    stages + static_cast<int64_t>(s) * p.stage_bytes + nkb * kBlk + t * 128;
+                for (int b = 0; b < nvb; ++b)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(vrow + b * kBlk + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (rescale_o && !first_tile) {
+                // O^T must be quiescent: the previous product has finished, this
+                // tile's is not issued before p_ready
+                if (!wait_pv(comp - 1)) break;
+                tc_fence_after();
+                float ov[NR];
+                tmem_ldn<NR>(trow + kColO, ov);
+#pragma unroll
+                for (int r = 0; r < NR; ++r) ov[r] *= corr[r];
+                tmem_stn<NR>(trow + kColO, ov);
+            }
+            fence_async_shared();  // P^T and the zeroed rows, for the tensor cores
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_ready(static_cast<int>(comp & 1)), 1u);
+            ++comp;
+            first_tile = false;
+        }
+        if ((mt.flags & kLast) && attend) {
+            // the chunk's last product: O^T column r is row r's weighted values
+            if (!wait_pv(comp - 1)) break;
+            tc_fence_after();
+            float ov[NR];
+            tmem_ldn<NR>(trow + kColO, ov);
+            tc_fence_before();
+            const int64_t s_k = k * p.CH * kDT;  // the chunk's first slot
+            const int64_t prow0 = (u * p.KP + k) * p.R;
+#pragma unroll
+            for (int r = 0; r < NR; ++r)  // rows with an allowed slot in the chunk
+                if (r < R && lim[r] >= s_k && t < p.Dv) p.part_acc[(prow0 + r) * p.Dv + t] = ov[r];
+            const uint32_t bm = rv & 1u;
+            const float mine = warp_reduce_rows<NR, false>(lsum);
+            if ((lane & (kGroup - 1)) == 0)
+                xval[(bm * kDN + (lane >> (5 - RowsLog2<NR>::v))) * 4 + w] = mine;
+            if (!rendezvous()) break;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                if (t == r && r < R && lim[r] >= s_k) {
+                    const float4 q4 = *reinterpret_cast<const float4*>(xval + (bm * kDN + r) * 4);
+                    p.part_ml[2 * (prow0 + r)] = mref[r];
+                    p.part_ml[2 * (prow0 + r) + 1] = (q4.x + q4.y) + (q4.z + q4.w);
+                }
+            }
+        }
+    }
+}
+
+template <typename T, int NR>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_tc_kernel(const __grid_constant__ DecParams dp) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const StepParams& p = dp.p;
+    const DecBars bars{smem_addr(smem)};
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + p.off_flag);
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.NS; ++s) {
+            mbar_init(bars.full(s), 1u);
+            mbar_init(bars.empty(s), 1u + kSoftWarps);  // MMA issuer, softmax warps
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bars.s_ready(b), 1u);
+            mbar_init(bars.s_free(b), kSoftWarps);
+            mbar_init(bars.p_ready(b), kSoftWarps);
+            mbar_init(bars.o_done(b), 1u);
+        }
+        mbar_init(bars.rendezvous(), kSoftWarps);
+        mbar_init(bars.drained(), 1u);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    // P^T rows past the unit's rows stay zero: clear both buffers once
+    for (int i = threadIdx.x; i < 2 * 2 * kNBlk / 16; i += kDecThreads)
+        reinterpret_cast<uint4*>(smem + p.dec_off_pt)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_async_shared();
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(smem + kTmemSlot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
+
+    if (warp < kSoftWarps) {
+        dec_softmax<T, NR>(dp, smem, bars, abort, tmem);
+    } else if (warp == kMmaWarp) {
+        if ((threadIdx.x & 31) == 0)
+            dec_mma_issuer(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value);
+    } else if (warp == kProdWarp) {
+        if ((threadIdx.x & 31) == 0) dec_producer(dp, smem, bars, abort);
+    }
+    tc_fence_before();
+    __syncthreads();  // every thread reaches this exactly once: all waits are bounded
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (threadIdx.x == 0 && *abort && p.dev_status) atomicOr(p.dev_status, KVC_DEV_TIMEOUT);
+}
+
+template <typename T, int NR>
+cudaError_t launch_t(const DecParams& dp, size_t smem, cudaStream_t stream) {
+    auto kern = decode_tc_kernel<T, NR>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(dp.p.P), kDecThreads, smem, stream>>>(dp);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_rows(const DecParams& dp, int nr, size_t smem, cudaStream_t stream) {
+    switch (nr) {
+        case 4: return launch_t<T, 4>(dp, smem, stream);
+        case 8: return launch_t<T, 8>(dp, smem, stream);
+        default: return launch_t<T, 16>(dp, smem, stream);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const DecParams& dp, int dtype, int nr, size_t smem,
+                             cudaStream_t stream) {
+    return dtype == KVC_BF16 ? launch_rows<__nv_bfloat16>(dp, nr, smem, stream)
+                             : launch_rows<__half>(dp, nr, smem, stream);
+}
+
+}  // namespace kvc

@@ -281,12 +281,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
 }
 
 // Instruction descriptor of a kind::f16 tcgen05.mma with fp32 accumulation.
-// bf16: operands are bf16 (else fp16). b_mn_major: B is stored N-contiguous.
-__host__ __device__ constexpr uint32_t mma_idesc_f16(int M, int N, bool bf16, bool b_mn_major) {
+// bf16: operands are bf16 (else fp16). b_mn_major: B is stored N-contiguous;
+// a_mn_major: A is stored M-contiguous.
+__host__ __device__ constexpr uint32_t mma_idesc_f16(int M, int N, bool bf16, bool b_mn_major,
+                                                     bool a_mn_major = false) {
     return (1u << 4)                                   // D: fp32
            | ((bf16 ? 1u : 0u) << 7)                   // A type
            | ((bf16 ? 1u : 0u) << 10)                  // B type
-           | (0u << 15)                                // A: K-major
+           | ((a_mn_major ? 1u : 0u) << 15)            // A major-ness
            | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
@@ -497,6 +499,9 @@ struct StepParams {
     // tc_off_stg (rows of 128 bytes for TMA stores), tensor-memory columns
     int tc_off_stg, tc_stg_bytes, tc_tmem_cols;
     int64_t tc_nrg;  // row groups of up to 128 query rows per unit (1 or 2)
+    // decode tensor-core kernel layout: the softmax warps' exchange buffers
+    // and the two P^T operand buffers
+    int dec_off_red, dec_off_pt;
     int32_t* dev_status;
     int vec_attention;  // 1: attention rows may be written 8 elements at a time
     // 1: the caches are updated in place (out_key_cache == key_cache): the

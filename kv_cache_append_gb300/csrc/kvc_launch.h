@@ -31,6 +31,23 @@ struct TcParams {
 // Fused copy + scatter + attention partials on the tensor cores (kvc_fused_tc.cu).
 cudaError_t launch_fused_tc(const TcParams& tp, int dtype, size_t smem, cudaStream_t stream);
 
+// Kernel parameters of the decode tensor-core kernel: the caches (or pools)
+// as TMA tensor maps (boxes of 64 elements x min(64, block) slots, 128-byte
+// swizzle), the query as [U * R][D] rows (boxes of 64 elements x 16 rows), and
+// the common parameters.
+struct DecParams {
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
+    CUtensorMap tm_q;
+    StepParams p;
+};
+
+// Attention of the steps that copy no cache (in place, read-only, paged) on
+// the tensor cores, for units of at most 16 query rows (kvc_decode_tc.cu).
+// nr: 4, 8 or 16 rows the kernel is instantiated for (>= R).
+cudaError_t launch_decode_tc(const DecParams& dp, int dtype, int nr, size_t smem,
+                             cudaStream_t stream);
+
 // Merge of the partials: context rows and one RowStat per query row (kvc_finalize.cu).
 cudaError_t launch_finalize_merge(const StepParams& p, int dtype, cudaStream_t stream);
 // Attention rows from the kept scores (or P values) and the RowStats (kvc_finalize.cu).
