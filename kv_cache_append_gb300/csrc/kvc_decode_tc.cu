@@ -66,6 +66,8 @@ constexpr int kDecThreads = 6 * 32;
 constexpr float kRescale = 8.f;      // raise a row's reference maximum when exceeded by 2^8
 constexpr uint32_t kTmemCols = 64;
 constexpr uint32_t kColO = 32;
+constexpr int kMaxPieces = kDT / 8;  // paged: block pieces per tile at most (8-slot blocks)
+constexpr int kIdsOffset = 2 * kDN * 4 * 4 + 2 * 4 * 4 + 32;  // in the exchange region
 
 struct DecBars {
     uint32_t base;
@@ -131,6 +133,26 @@ __device__ void dec_producer(const DecParams& dp, unsigned char* smem, DecBars b
     int64_t issued = 0;
     Ring ring;
     bool ok = true;
+    // paged: block ids of a tile's pieces, two tiles' worth, copied from the
+    // block table without waiting (a piece never straddles two blocks: the
+    // piece height divides the block size)
+    int32_t* pids = reinterpret_cast<int32_t*>(smem + p.dec_off_red + kIdsOffset);
+    auto request_ids = [&](const Unit& x, int64_t i) {
+        const int bs = static_cast<int>(p.block_size), hh = min(kHalf, bs);
+        const int jt = static_cast<int>(i * kDT);
+        const int npc = min((static_cast<int>(x.N) - jt + hh - 1) / hh, kDT / hh);
+        const int32_t* row = p.block_table + x.b * p.max_blocks;
+        int32_t* dst = pids + (i & 1) * kMaxPieces;
+        int blk = jt / bs, y = jt - blk * bs;
+        for (int c = 0; c < npc; ++c) {
+            cp_async4(dst + c, row + blk);
+            y += hh;
+            if (y == bs) {
+                y = 0;
+                ++blk;
+            }
+        }
+    };
     while (ok) {
         const int64_t q = atomicAdd(p.counter, 1u);
         if (q >= p.NQ) break;
@@ -175,21 +197,29 @@ __device__ void dec_producer(const DecParams& dp, unsigned char* smem, DecBars b
             } else {
                 // paged: one box of min(64, block_size) slots per block piece of the
                 // tile below the new length (their block ids were checked); the pool
-                // maps are [blocks * Hk][block_size][width]
-                const int64_t hh = min(static_cast<int64_t>(kHalf), p.block_size);
-                const int64_t npc = min((x.N - j0 + hh - 1) / hh, kDT / hh);
+                // maps are [blocks * Hk][block_size][width]. The pieces' block ids
+                // were requested with the previous tile of the chunk.
+                const int bs = static_cast<int>(p.block_size), hh = min(kHalf, bs);
+                const int jt = static_cast<int>(j0);
+                const int npc = min((static_cast<int>(x.N) - jt + hh - 1) / hh, kDT / hh);
                 mbar_arrive_expect_tx(full, static_cast<uint32_t>(npc * hh * 128 * (nkb + nvb)) +
                                                 q_bytes);
-                for (int64_t c = 0; c < npc; ++c) {
-                    const int64_t j = j0 + c * hh;
-                    const int y = static_cast<int>(j % p.block_size);
-                    const int z = static_cast<int>(paged_unit(p, u, j));
+                if (i == i0) request_ids(x, i);
+                cp_async_wait_all();
+                const int32_t* bid = pids + (i & 1) * kMaxPieces;
+                int y = jt % bs;
+                for (int c = 0; c < npc; ++c) {
+                    const int z = bid[c] * static_cast<int>(p.Hk) + static_cast<int>(x.kv);
                     const uint32_t o = static_cast<uint32_t>(c * hh * 128);
                     for (int b = 0; b < nkb; ++b)
                         tma_load_3d(sK + b * kBlk + o, &dp.tm_k, 64 * b, y, z, full);
                     for (int b = 0; b < nvb; ++b)
                         tma_load_3d(sV + b * kBlk + o, &dp.tm_v, 64 * b, y, z, full);
+                    y += hh;
+                    if (y == bs) y = 0;
                 }
+                // the next tile's ids arrive while the producer waits for a stage
+                if (i + 1 < i1) request_ids(x, i + 1);
             }
             // the unit's R query rows are rows [u R, u R + 16) of the [U R][D] query view
             const int qy = static_cast<int>(u * p.R);
