@@ -337,8 +337,9 @@ bool dec_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
     pl->off_flag = 512;
     pl->off_meta = 1024;  // kMaxStages records of 32 bytes
     int64_t off = 1024 + int64_t(kMaxStages) * 32;
-    pl->dec_off_red = static_cast<int>(off);  // [2][16][4] values, [2][4] flags, [2][16] block ids
-    off = align_up(off + 2 * 16 * 4 * 4 + 2 * 4 * 4 + 32 + 2 * 16 * 4, 1024);
+    // [2][2][16][4] values, [2][2][4] flags, [2][16] block ids
+    pl->dec_off_red = static_cast<int>(off);
+    off = align_up(off + 2 * 2 * 16 * 4 * 4 + 2 * 2 * 4 * 4 + 2 * 16 * 4, 1024);
     pl->dec_off_pt = static_cast<int>(off);
     off += 2 * 2 * 16 * 128;
     pl->off_stages = static_cast<int>(off);

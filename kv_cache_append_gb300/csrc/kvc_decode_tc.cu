@@ -24,7 +24,9 @@
 //                   and the unit's query rows (16 rows, 4 KB from L2) with it.
 //   MMA warp        one thread: S^T into one of two tensor-memory buffers,
 //                   then O^T += V^T P^T into the tensor-memory O^T.
-//   4 softmax warps one slot per thread (= the tensor-memory lane of S^T):
+//   softmax warps  one or two groups of 4 warps (two for 8 or 16 rows, each
+//                   group taking half of them), one slot per thread (= the
+//                   tensor-memory lane of S^T):
 //                   applies scale*log2(e) and the lower-right causal limit
 //                   j <= length + t ("Required behavior", bullet 4), keeps the
 //                   fp32 scores for the attention rows, writes P^T =
@@ -60,14 +62,21 @@ constexpr int kDN = 16;              // query rows of a unit, padded (N of both 
 constexpr int kBlk = kDT * 128;      // one 64-element-wide column block of a K or V tile
 constexpr int kNBlk = kDN * 128;     // one 64-element-wide column block of Q or P^T
 constexpr int kHalf = 64;            // slots per TMA box of a contiguous cache
-constexpr int kSoftWarps = 4;
-constexpr int kMmaWarp = 4, kProdWarp = 5;
-constexpr int kDecThreads = 6 * 32;
+// Warp roles for SG groups of 4 softmax warps (each group takes NR / SG of
+// the unit's rows for all 128 slots), then the MMA warp and the producer.
+template <int SG>
+struct DecRoles {
+    static constexpr int soft = 4 * SG, mma = 4 * SG, prod = 4 * SG + 1;
+    static constexpr int threads = (4 * SG + 2) * 32;
+};
 constexpr float kRescale = 8.f;      // raise a row's reference maximum when exceeded by 2^8
 constexpr uint32_t kTmemCols = 64;
 constexpr uint32_t kColO = 32;
 constexpr int kMaxPieces = kDT / 8;  // paged: block pieces per tile at most (8-slot blocks)
-constexpr int kIdsOffset = 2 * kDN * 4 * 4 + 2 * 4 * 4 + 32;  // in the exchange region
+// exchange region: values [2][2 groups][kDN][4 warps], flags [2][2 groups][4
+// warps], then the paged block ids [2][kMaxPieces]
+constexpr int kFlagOffset = 2 * 2 * kDN * 4 * 4;
+constexpr int kIdsOffset = kFlagOffset + 2 * 2 * 4 * 4;
 
 struct DecBars {
     uint32_t base;
@@ -78,10 +87,11 @@ struct DecBars {
     // one pair per P^T buffer, as in the tensor-core step kernel
     __device__ uint32_t p_ready(int b) const { return base + 288u + 8u * b; }
     __device__ uint32_t o_done(int b) const { return base + 304u + 8u * b; }
-    __device__ uint32_t rendezvous() const { return base + 320u; }  // the 4 softmax warps
-    __device__ uint32_t drained() const { return base + 328u; }
+    // the 4 softmax warps of group g
+    __device__ uint32_t rendezvous(int g) const { return base + 320u + 8u * g; }
+    __device__ uint32_t drained() const { return base + 336u; }
 };
-constexpr int kTmemSlot = 336;  // tensor-memory base address written by tcgen05.alloc
+constexpr int kTmemSlot = 344;  // tensor-memory base address written by tcgen05.alloc
 
 // Reduce v[0..NR) over the 32 lanes of a warp (maximum or sum) by a
 // reduce-scatter butterfly: NR - 1 + 5 - log2(NR) shuffles instead of 5 NR.
@@ -119,8 +129,6 @@ template <>
 struct RowsLog2<4> { static constexpr int v = 2; };
 template <>
 struct RowsLog2<8> { static constexpr int v = 3; };
-template <>
-struct RowsLog2<16> { static constexpr int v = 4; };
 
 __device__ void dec_producer(const DecParams& dp, unsigned char* smem, DecBars bars,
                              volatile int* abort) {
@@ -331,35 +339,38 @@ __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars
     mbar_wait(bars.drained(), 0u, &never);
 }
 
-template <typename T, int NR>
+template <typename T, int NR, int SG>
 __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars bars,
                             volatile int* abort, uint32_t tmem) {
     using S = Storage<T>;
     const StepParams& p = dp.p;
-    const int t = threadIdx.x;  // slot of the tile (lane of S^T); value column of O^T
-    const int w = t >> 5, lane = t & 31;
+    constexpr int NW = NR / SG;  // rows of this thread's group
+    const int t = threadIdx.x & 127;  // slot of the tile (lane of S^T); value column of O^T
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = w >> 2, wq = w & 3;  // group; tensor-memory lane quadrant
+    const int r0 = g * NW;             // the group's first row
     const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
     const int R = static_cast<int>(p.R), Q = static_cast<int>(p.Q);
     const int nkb = static_cast<int>(p.D / 64), nvb = static_cast<int>(p.Dv / 64);
     const float qs = p.qscale;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(w * 32) << 16);  // this warp's lanes
+    const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);  // this warp's lanes
     unsigned char* stages = smem + p.off_stages;
     unsigned char* pt = smem + p.dec_off_pt;
-    float* xval = reinterpret_cast<float*>(smem + p.dec_off_red);           // [2][kDN][4 warps]
-    int* xflag = reinterpret_cast<int*>(smem + p.dec_off_red + 2 * kDN * 4 * 4);  // [2][4 warps]
-    constexpr int kGroup = 32 / NR;  // lanes that end a reduction with one row
+    float* xval = reinterpret_cast<float*>(smem + p.dec_off_red) + g * kDN * 4;
+    int* xflag = reinterpret_cast<int*>(smem + p.dec_off_red + kFlagOffset) + g * 4;
+    constexpr int kGroup = 32 / NW;  // lanes that end a reduction with one row
     Ring ring;
     int sbuf = 0;
     int64_t su[2] = {0, 0};   // completions consumed per S^T buffer
     int64_t comp = 0;         // attending tiles done = products issued for them
     int64_t pvd[2] = {0, 0};  // completions consumed on o_done[0], o_done[1]
-    uint32_t rv = 0;          // rendezvous of the 4 warps so far
+    uint32_t rv = 0;          // rendezvous of the group's 4 warps so far
     bool attend = false, first_tile = false;
     int64_t L = 0, n = 0, N = 0, u = 0, k = 0, rowoff0 = 0;
-    int lim[NR];
-    float mref[NR], lsum[NR];
+    int lim[NW];
+    float mref[NW], lsum[NW];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
+    for (int r = 0; r < NW; ++r) {
         lim[r] = -1;
         mref[r] = -INFINITY;
         lsum[r] = 0.f;
@@ -373,13 +384,13 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
             if (!warp_wait(bars.o_done(b), static_cast<uint32_t>(pvd[b] & 1), abort)) return false;
         return true;
     };
-    // The 4 warps meet on an mbarrier (bounded, unlike bar.sync): what each
-    // wrote to buffer rv % 2 before is visible to all after. A warp is at most
-    // one rendezvous ahead of another, so two buffers never collide.
+    // The group's 4 warps meet on an mbarrier (bounded, unlike bar.sync): what
+    // each wrote to buffer rv % 2 before is visible to all after. A warp is at
+    // most one rendezvous ahead of another, so two buffers never collide.
     auto rendezvous = [&]() -> bool {
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars.rendezvous(), 1u);
-        const bool ok = warp_wait(bars.rendezvous(), rv & 1u, abort);
+        if (lane == 0) mbar_arrive(bars.rendezvous(g), 1u);
+        const bool ok = warp_wait(bars.rendezvous(g), rv & 1u, abort);
         ++rv;
         return ok;
     };
@@ -405,9 +416,9 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
                 const int64_t b = u / p.Hk, kv = u - b * p.Hk;
                 rowoff0 = (b * p.Hq + kv * p.G) * p.Q * p.M;  // row r's scores at + r M
 #pragma unroll
-                for (int r = 0; r < NR; ++r) {
-                    const int tr = r % Q;
-                    lim[r] = (r < R && tr < n) ? static_cast<int>(L + tr) : -1;
+                for (int r = 0; r < NW; ++r) {
+                    const int tr = (r0 + r) % Q;
+                    lim[r] = (r0 + r < R && tr < n) ? static_cast<int>(L + tr) : -1;
                     mref[r] = -INFINITY;
                     lsum[r] = 0.f;
                 }
@@ -419,41 +430,43 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
             if (!warp_wait(bars.s_ready(sbuf), static_cast<uint32_t>(su[sbuf] & 1), abort)) break;
             ++su[sbuf];
             tc_fence_after();
-            float sv[NR];
-            tmem_ldn<NR>(trow + static_cast<uint32_t>(sbuf * kDN), sv);
+            float sv[NW];
+            tmem_ldn<NW>(trow + static_cast<uint32_t>(sbuf * kDN + r0), sv);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.s_free(sbuf), 1u);
             sbuf ^= 1;
             const int j0 = mt.i * kDT, j = j0 + t;
             bool need = false;
-            float* srow = p.scores + rowoff0 + j;
+            float* srow = p.scores + rowoff0 + r0 * p.M + j;
 #pragma unroll
-            for (int r = 0; r < NR; ++r) {
+            for (int r = 0; r < NW; ++r) {
                 const bool allowed = j <= lim[r];
                 sv[r] = allowed ? sv[r] * qs : -INFINITY;
                 if (allowed) srow[r * p.M] = sv[r];
                 need |= sv[r] > mref[r] + kRescale;
             }
-            // raise decisions are taken for the whole tile (every warp the same)
+            // raise decisions are taken for the whole tile (every warp of the
+            // group the same)
             const uint32_t bf = rv & 1u;
             const int wneed = __any_sync(0xffffffffu, need);
-            if (lane == 0) xflag[bf * 4 + w] = wneed;
+            if (lane == 0) xflag[bf * 8 + wq] = wneed;
             if (!rendezvous()) break;
-            const int4 fl = *reinterpret_cast<const int4*>(xflag + bf * 4);
-            float corr[NR];
+            const int4 fl = *reinterpret_cast<const int4*>(xflag + bf * 8);
+            float corr[NW];
 #pragma unroll
-            for (int r = 0; r < NR; ++r) corr[r] = 1.f;
+            for (int r = 0; r < NW; ++r) corr[r] = 1.f;
             bool rescale_o = false;
             if (fl.x | fl.y | fl.z | fl.w) {
                 const uint32_t bm = rv & 1u;
-                const float mine = warp_reduce_rows<NR, true>(sv);
+                const float mine = warp_reduce_rows<NW, true>(sv);
                 if ((lane & (kGroup - 1)) == 0)
-                    xval[(bm * kDN + (lane >> (5 - RowsLog2<NR>::v))) * 4 + w] = mine;
+                    xval[(bm * 2 * kDN + (lane >> (5 - RowsLog2<NW>::v))) * 4 + wq] = mine;
                 if (!rendezvous()) break;
 #pragma unroll
-                for (int r = 0; r < NR; ++r) {
-                    const float4 q4 = *reinterpret_cast<const float4*>(xval + (bm * kDN + r) * 4);
+                for (int r = 0; r < NW; ++r) {
+                    const float4 q4 =
+                        *reinterpret_cast<const float4*>(xval + (bm * 2 * kDN + r) * 4);
                     const float tmax = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
                     if (tmax > mref[r] + kRescale) {
                         if (mref[r] != -INFINITY) {
@@ -470,12 +483,13 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
             unsigned char* pbox = pt + (comp & 1) * 2 * kNBlk + (t >> 6) * kNBlk;
             const int ck = (t & 63) >> 3, e2 = (t & 7) * 2;
 #pragma unroll
-            for (int r = 0; r < NR; ++r) {
+            for (int r = 0; r < NW; ++r) {
                 const float e = (j <= lim[r]) ? fast_exp2(sv[r] - mref[r]) : 0.f;
                 lsum[r] += e;
-                *reinterpret_cast<T*>(pbox + r * 128 + ((ck ^ (r & 7)) << 4) + e2) = S::from_float(e);
+                const int rr = r0 + r;
+                *reinterpret_cast<T*>(pbox + rr * 128 + ((ck ^ (rr & 7)) << 4) + e2) = S::from_float(e);
             }
-            if (j >= N) {  // a value row past the new length: zero in the tile
+            if (g == 0 && j >= N) {  // a value row past the new length: zero in the tile
                 unsigned char* vrow =
                     stages + static_cast<int64_t>(s) * p.stage_bytes + nkb * kBlk + t * 128;
                 for (int b = 0; b < nvb; ++b)
@@ -488,11 +502,11 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
                 // tile's is not issued before p_ready
                 if (!wait_pv(comp - 1)) break;
                 tc_fence_after();
-                float ov[NR];
-                tmem_ldn<NR>(trow + kColO, ov);
+                float ov[NW];
+                tmem_ldn<NW>(trow + kColO + r0, ov);
 #pragma unroll
-                for (int r = 0; r < NR; ++r) ov[r] *= corr[r];
-                tmem_stn<NR>(trow + kColO, ov);
+                for (int r = 0; r < NW; ++r) ov[r] *= corr[r];
+                tmem_stn<NW>(trow + kColO + r0, ov);
             }
             fence_async_shared();  // P^T and the zeroed rows, for the tensor cores
             tc_fence_before();
@@ -505,23 +519,24 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
             // the chunk's last product: O^T column r is row r's weighted values
             if (!wait_pv(comp - 1)) break;
             tc_fence_after();
-            float ov[NR];
-            tmem_ldn<NR>(trow + kColO, ov);
+            float ov[NW];
+            tmem_ldn<NW>(trow + kColO + r0, ov);
             tc_fence_before();
             const int64_t s_k = k * p.CH * kDT;  // the chunk's first slot
-            const int64_t prow0 = (u * p.KP + k) * p.R;
+            const int64_t prow0 = (u * p.KP + k) * p.R + r0;
 #pragma unroll
-            for (int r = 0; r < NR; ++r)  // rows with an allowed slot in the chunk
-                if (r < R && lim[r] >= s_k && t < p.Dv) p.part_acc[(prow0 + r) * p.Dv + t] = ov[r];
+            for (int r = 0; r < NW; ++r)  // rows with an allowed slot in the chunk
+                if (lim[r] >= s_k && t < p.Dv) p.part_acc[(prow0 + r) * p.Dv + t] = ov[r];
             const uint32_t bm = rv & 1u;
-            const float mine = warp_reduce_rows<NR, false>(lsum);
+            const float mine = warp_reduce_rows<NW, false>(lsum);
             if ((lane & (kGroup - 1)) == 0)
-                xval[(bm * kDN + (lane >> (5 - RowsLog2<NR>::v))) * 4 + w] = mine;
+                xval[(bm * 2 * kDN + (lane >> (5 - RowsLog2<NW>::v))) * 4 + wq] = mine;
             if (!rendezvous()) break;
 #pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                if (t == r && r < R && lim[r] >= s_k) {
-                    const float4 q4 = *reinterpret_cast<const float4*>(xval + (bm * kDN + r) * 4);
+            for (int r = 0; r < NW; ++r) {
+                if (t == r && lim[r] >= s_k) {
+                    const float4 q4 =
+                        *reinterpret_cast<const float4*>(xval + (bm * 2 * kDN + r) * 4);
                     p.part_ml[2 * (prow0 + r)] = mref[r];
                     p.part_ml[2 * (prow0 + r) + 1] = (q4.x + q4.y) + (q4.z + q4.w);
                 }
@@ -530,9 +545,10 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
     }
 }
 
-template <typename T, int NR>
-__global__ void __launch_bounds__(kDecThreads, 1)
+template <typename T, int NR, int SG>
+__global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
     decode_tc_kernel(const __grid_constant__ DecParams dp) {
+    using Roles = DecRoles<SG>;
     extern __shared__ __align__(1024) unsigned char smem[];
     const StepParams& p = dp.p;
     const DecBars bars{smem_addr(smem)};
@@ -541,24 +557,24 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.NS; ++s) {
             mbar_init(bars.full(s), 1u);
-            mbar_init(bars.empty(s), 1u + kSoftWarps);  // MMA issuer, softmax warps
+            mbar_init(bars.empty(s), 1u + Roles::soft);  // MMA issuer, softmax warps
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bars.s_ready(b), 1u);
-            mbar_init(bars.s_free(b), kSoftWarps);
-            mbar_init(bars.p_ready(b), kSoftWarps);
+            mbar_init(bars.s_free(b), Roles::soft);
+            mbar_init(bars.p_ready(b), Roles::soft);
             mbar_init(bars.o_done(b), 1u);
         }
-        mbar_init(bars.rendezvous(), kSoftWarps);
+        for (int g = 0; g < 2; ++g) mbar_init(bars.rendezvous(g), 4u);
         mbar_init(bars.drained(), 1u);
         *abort = 0;
         fence_mbar_init();
     }
     // P^T rows past the unit's rows stay zero: clear both buffers once
-    for (int i = threadIdx.x; i < 2 * 2 * kNBlk / 16; i += kDecThreads)
+    for (int i = threadIdx.x; i < 2 * 2 * kNBlk / 16; i += Roles::threads)
         reinterpret_cast<uint4*>(smem + p.dec_off_pt)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_async_shared();
-    if (warp == kMmaWarp) {
+    if (warp == Roles::mma) {
         tmem_alloc(smem_addr(smem + kTmemSlot), kTmemCols);
         tmem_relinquish();
     }
@@ -567,39 +583,43 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
 
-    if (warp < kSoftWarps) {
-        dec_softmax<T, NR>(dp, smem, bars, abort, tmem);
-    } else if (warp == kMmaWarp) {
+    if (warp < Roles::soft) {
+        dec_softmax<T, NR, SG>(dp, smem, bars, abort, tmem);
+    } else if (warp == Roles::mma) {
         if ((threadIdx.x & 31) == 0)
             dec_mma_issuer(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value);
-    } else if (warp == kProdWarp) {
+    } else if (warp == Roles::prod) {
         if ((threadIdx.x & 31) == 0) dec_producer(dp, smem, bars, abort);
     }
     tc_fence_before();
     __syncthreads();  // every thread reaches this exactly once: all waits are bounded
-    if (warp == kMmaWarp) {
+    if (warp == Roles::mma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
     if (threadIdx.x == 0 && *abort && p.dev_status) atomicOr(p.dev_status, KVC_DEV_TIMEOUT);
 }
 
-template <typename T, int NR>
+#ifndef KVC_DEC_GROUPS8
+#define KVC_DEC_GROUPS8 2
+#endif
+
+template <typename T, int NR, int SG>
 cudaError_t launch_t(const DecParams& dp, size_t smem, cudaStream_t stream) {
-    auto kern = decode_tc_kernel<T, NR>;
+    auto kern = decode_tc_kernel<T, NR, SG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(dp.p.P), kDecThreads, smem, stream>>>(dp);
+    kern<<<static_cast<unsigned>(dp.p.P), DecRoles<SG>::threads, smem, stream>>>(dp);
     return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_rows(const DecParams& dp, int nr, size_t smem, cudaStream_t stream) {
     switch (nr) {
-        case 4: return launch_t<T, 4>(dp, smem, stream);
-        case 8: return launch_t<T, 8>(dp, smem, stream);
-        default: return launch_t<T, 16>(dp, smem, stream);
+        case 4: return launch_t<T, 4, 1>(dp, smem, stream);
+        case 8: return launch_t<T, 8, KVC_DEC_GROUPS8>(dp, smem, stream);
+        default: return launch_t<T, 16, 2>(dp, smem, stream);
     }
 }
 
