@@ -328,6 +328,24 @@ KVC_API int kvc_step_static(const kvc_dims *dims, const void *query, const void 
                             void *out_value_cache, int64_t *out_lengths, void *out_attention,
                             void *out_context, int32_t *dev_status, void *stream);
 
+/*
+ * kvc_selftest_wait_timeout -- runs the failure path of the step kernels'
+ * pipeline waits without a fault. Every such wait is an mbarrier wait with a
+ * time limit; when its phase never completes, the waiting role sets the CTA's
+ * abort flag, the other roles return at their next check, and the kernel ORs
+ * KVC_DEV_TIMEOUT into *dev_status. This launches one small kernel whose
+ * barrier is never arrived at: a one-thread wait gives up after limit_ns and
+ * its abort flag ends a whole-warp wait on the same barrier; the kernel then
+ * sets KVC_DEV_TIMEOUT. Nothing faults, traps or waits without a limit, and
+ * the context stays usable.
+ *
+ *   dev_status  device int32, OR-ed with KVC_DEV_TIMEOUT (never cleared here).
+ *   limit_ns    1e3 .. 1e8 (KVC_E_SHAPE otherwise); the kernel takes about
+ *               that long.
+ *   stream      cudaStream_t or NULL; the work is enqueued, not waited for.
+ */
+KVC_API int kvc_selftest_wait_timeout(int32_t *dev_status, int64_t limit_ns, void *stream);
+
 /* Static text for a KVC_OK / KVC_E_* code. */
 KVC_API const char *kvc_status_string(int status);
 

@@ -9,8 +9,8 @@ from .kvc import (DEV_MASK, DEV_OVERFLOW, DEV_TIMEOUT, DTYPES, Dims, KvcError,  
                   attention_over_cache, check_inputs, default_scale, dims_of,
                   kv_cache_attention_step, kv_cache_attention_step_inplace,
                   kv_cache_attention_step_paged, library, paged_workspace_bytes, step_paged_into,
-                  make_dims, plan_info, plan_info_inplace, status_string, step_inplace_into,
-                  step_into, workspace_bytes)
+                  make_dims, plan_info, plan_info_inplace, selftest_wait_timeout, status_string,
+                  step_inplace_into, step_into, workspace_bytes)
 
 __all__ = ["kv_cache_attention_step", "kv_cache_attention_step_inplace",
            "kv_cache_attention_step_paged",

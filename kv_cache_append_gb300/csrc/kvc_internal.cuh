@@ -89,8 +89,11 @@ __device__ __forceinline__ unsigned long long global_ns() {
 
 // Wait for the phase of `bar` with the given parity to complete. Gives up
 // (returns false) when *abort is set by another role of the CTA, or after
-// kWaitLimitNs; in the latter case it sets *abort itself.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// limit_ns (kWaitLimitNs in the kernels); in the latter case it sets *abort
+// itself.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
+                                                volatile int* abort,
+                                                unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = 0;
     for (uint32_t it = 1;; ++it) {
@@ -100,12 +103,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             const unsigned long long now = global_ns();
             if (t0 == 0) {
                 t0 = now;
-            } else if (now - t0 > kWaitLimitNs) {
+            } else if (now - t0 > limit_ns) {
                 *abort = 1;
                 return false;
             }
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+    return mbar_wait_limit(bar, parity, abort, kWaitLimitNs);
 }
 
 // TMA bulk copy global -> shared, completion counted on an mbarrier.

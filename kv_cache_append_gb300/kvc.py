@@ -99,6 +99,8 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kvc_step_paged.argtypes = paged_args
             lib.kvc_step_paged_timed.restype = i32
             lib.kvc_step_paged_timed.argtypes = paged_args + [ctypes.POINTER(vp), i32]
+            lib.kvc_selftest_wait_timeout.restype = i32
+            lib.kvc_selftest_wait_timeout.argtypes = [vp, i64, vp]
             lib.kvc_status_string.restype = ctypes.c_char_p
             lib.kvc_status_string.argtypes = [i32]
             lib.kvc_version.restype = i32
@@ -109,6 +111,19 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
 
 def status_string(status: int) -> str:
     return library().kvc_status_string(status).decode()
+
+
+def selftest_wait_timeout(status, limit_ns: int = 5_000_000, stream=None) -> None:
+    """kvc_selftest_wait_timeout: a kernel whose pipeline wait is never
+    satisfied gives up after limit_ns and ORs DEV_TIMEOUT into `status` (a
+    device int32 tensor of one element)."""
+    if not (status.is_cuda and status.dtype == torch.int32 and status.numel() >= 1):
+        raise ValueError("status must be a device int32 tensor")
+    s = torch.cuda.current_stream(status.device).cuda_stream if stream is None else stream
+    rc = library().kvc_selftest_wait_timeout(ctypes.c_void_p(status.data_ptr()), int(limit_ns),
+                                             ctypes.c_void_p(s))
+    if rc != 0:
+        raise KvcError(rc, status_string(rc))
 
 
 def make_dims(B, Hq, Hk, Q, D, Dv, M, dtype) -> Dims:
