@@ -90,6 +90,9 @@ class Oracle:
         lib.kvo_threads.argtypes = []
         lib.kvo_attend_cache.restype = ctypes.c_int
         lib.kvo_attend_cache.argtypes = [ctypes.c_int] + [i64] * 7 + [vp] * 6 + [dbl] + [vp] * 3
+        lib.kvo_step_backward.restype = ctypes.c_int
+        lib.kvo_step_backward.argtypes = ([ctypes.c_int] + [i64] * 7 + [vp] * 7 + [dbl] +
+                                          [vp] * 11)
         self.lib = lib
 
     def threads(self) -> int:
@@ -178,6 +181,37 @@ class Oracle:
                                   out.ctypes.data, flags.ctypes.data, work.ctypes.data)
         return out, flags
 
+
+    def step_backward(self, query, new_key, new_value, key_cache, value_cache, lengths,
+                      append_mask, d_key_cache=None, d_value_cache=None, d_attention=None,
+                      d_context=None, options: dict | None = None) -> dict:
+        """Gradients of the step's outputs (key_cache, value_cache, attention,
+        context) with respect to query, new_key, new_value, key_cache and
+        value_cache, given the gradients reaching those outputs (tensors in
+        the inputs' dtype, or None for zero). Returns float64 numpy arrays
+        d_query, d_new_key, d_new_value, d_key_cache, d_value_cache and flags."""
+        q, nk, nv, kc, vc = (_host(x) for x in (query, new_key, new_value, key_cache,
+                                                 value_cache))
+        B, Hq, Hk, Q, D, Dv, M = _dims(q, kc, vc)
+        scale = _scale(options, D)
+        ln = _host(lengths).to(torch.int64)
+        mk = _host(append_mask).to(torch.uint8)
+        grads = [None if g is None else _host(g).to(q.dtype)
+                 for g in (d_key_cache, d_value_cache, d_attention, d_context)]
+        out = {"d_query": np.zeros((B, Hq, Q, D)), "d_new_key": np.zeros((B, Hk, Q, D)),
+               "d_new_value": np.zeros((B, Hk, Q, Dv)), "d_key_cache": np.zeros((B, Hk, M, D)),
+               "d_value_cache": np.zeros((B, Hk, M, Dv))}
+        flags = np.zeros(B, dtype=np.int32)
+        work = np.empty(max(1, self.threads()) * 3 * max(1, M), dtype=np.float64)
+        self.lib.kvo_step_backward(
+            DTYPE_CODES[q.dtype], B, Hq, Hk, Q, D, Dv, M, _ptr(q), _ptr(nk), _ptr(nv), _ptr(kc),
+            _ptr(vc), _ptr(ln), _ptr(mk), scale,
+            *(None if g is None else _ptr(g) for g in grads),
+            *(out[k].ctypes.data for k in ("d_query", "d_new_key", "d_new_value", "d_key_cache",
+                                           "d_value_cache")),
+            flags.ctypes.data, work.ctypes.data)
+        out["flags"] = flags
+        return out
 
     def step_paged(self, query, new_key, new_value, key_pool, value_pool, block_table,
                    lengths, append_mask, options: dict | None = None) -> dict:
@@ -279,3 +313,7 @@ def step_paged(*args, **kw):
 
 def rows(*args, **kw):
     return default().rows(*args, **kw)
+
+
+def step_backward(*args, **kw):
+    return default().step_backward(*args, **kw)

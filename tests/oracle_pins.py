@@ -615,6 +615,138 @@ def pin_paged_bad_block_ids_append_nothing(o):
         np.testing.assert_array_equal(got["context"][b], ref["context"][b])
 
 
+# ------------------------------------------------------------------ gradients
+def _grad_case(dtype, seed):
+    """A small ragged case (rows appending 3, 2, 0 and 1 tokens, one full
+    cache, one empty prefix) with random upstream gradients for all four
+    outputs, all stored in `dtype`."""
+    g = torch.Generator().manual_seed(seed)
+    B, Hq, Hk, Q, D, Dv, M = 4, 4, 2, 3, 5, 6, 10
+    q = _rand(g, B, Hq, Q, D, dtype=dtype)
+    nk = _rand(g, B, Hk, Q, D, dtype=dtype)
+    nv = _rand(g, B, Hk, Q, Dv, dtype=dtype)
+    kc = _rand(g, B, Hk, M, D, dtype=dtype)
+    vc = _rand(g, B, Hk, M, Dv, dtype=dtype)
+    lengths = torch.tensor([0, 4, 7, 9])
+    counts = torch.tensor([3, 2, 0, 1])
+    mask = torch.arange(Q)[None, :] < counts[:, None]
+    grads = dict(d_key_cache=_rand(g, B, Hk, M, D, dtype=dtype),
+                 d_value_cache=_rand(g, B, Hk, M, Dv, dtype=dtype),
+                 d_attention=_rand(g, B, Hq, Q, M, dtype=dtype),
+                 d_context=_rand(g, B, Hq, Q, Dv, dtype=dtype))
+    return (q, nk, nv, kc, vc, lengths, mask), counts, grads
+
+
+def _torch_step_fp64(q, nk, nv, kc, vc, lengths, counts, scale):
+    """The step's four outputs as differentiable float64 torch ops, written
+    independently of the oracle: the updated caches by slice assignment into
+    a copy ([contract] bullet 3), query head h on KV head h // G by
+    repeat_interleave (bullet 2), softmax over the allowed slots j <= L + t of
+    the valid rows t < n (bullets 4-5), attention times updated values."""
+    B, Hq, Q, D = q.shape
+    Hk, M = kc.shape[1], kc.shape[2]
+    G = Hq // Hk
+    Kp, Vp = kc.clone(), vc.clone()
+    for b in range(B):
+        L, n = int(lengths[b]), int(counts[b])
+        Kp[b, :, L:L + n] = nk[b, :, :n]
+        Vp[b, :, L:L + n] = nv[b, :, :n]
+    s = scale * q @ Kp.repeat_interleave(G, dim=1).transpose(-1, -2)  # [B,Hq,Q,M]
+    t = torch.arange(Q)[None, :, None]
+    j = torch.arange(M)[None, None, :]
+    allowed = (t < counts[:, None, None]) & (j <= lengths[:, None, None] + t)  # [B,Q,M]
+    allowed = allowed[:, None]
+    a = torch.softmax(torch.where(allowed, s, torch.full_like(s, -1e30)), dim=-1)
+    a = a * allowed.to(a.dtype)
+    c = a @ Vp.repeat_interleave(G, dim=1)
+    return Kp, Vp, a, c
+
+
+def pin_backward_vs_autograd(o):
+    """[contract] Starter code: the suite grades gradients. torch autograd of
+    an independent float64 statement of the step (differentiable slicing,
+    repeat_interleave, masked softmax) gives the same gradients as the
+    oracle's chain rule, for every input, in fp32 and bf16 storage."""
+    for dtype, seed in ((torch.float32, 31), (torch.bfloat16, 32)):
+        args, counts, grads = _grad_case(dtype, seed)
+        q, nk, nv, kc, vc, lengths, mask = args
+        scale = 0.37
+        got = o.step_backward(*args, options={"scale": scale}, **grads)
+        leaves = [o.widen(t) for t in (q, nk, nv, kc, vc)]
+        leaves = [torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in leaves]
+        outs = _torch_step_fp64(*leaves, lengths, counts, scale)
+        gw = [torch.tensor(o.widen(grads[k]), dtype=torch.float64)
+              for k in ("d_key_cache", "d_value_cache", "d_attention", "d_context")]
+        loss = sum((x * w).sum() for x, w in zip(outs, gw))
+        ref = torch.autograd.grad(loss, leaves)
+        for name, r in zip(("d_query", "d_new_key", "d_new_value", "d_key_cache",
+                            "d_value_cache"), ref):
+            np.testing.assert_allclose(got[name], r.numpy(), rtol=1e-9, atol=1e-12, err_msg=name)
+
+
+def pin_backward_finite_differences(o):
+    """The gradient of a scalar of the step's outputs, by central differences
+    of the oracle's own forward (kvo_step) at stored fp32 values, equals the
+    backward's gradient element for elements of every input (query rows of
+    valid and invalid rows, appended and ignored new rows, cache slots below
+    the old length, overwritten and past the new length)."""
+    args, counts, grads = _grad_case(torch.float32, 33)
+    q, nk, nv, kc, vc, lengths, mask = args
+    opts = {"scale": 0.41}
+    back = o.step_backward(*args, options=opts, **grads)
+    gw = {k: o.widen(v) for k, v in grads.items()}
+
+    def loss(xs):
+        r = o.step(*xs, lengths, mask, opts)
+        return float((o.widen(r["key_cache"]) * gw["d_key_cache"]).sum()
+                     + (o.widen(r["value_cache"]) * gw["d_value_cache"]).sum()
+                     + (r["attention"] * gw["d_attention"]).sum()
+                     + (r["context"] * gw["d_context"]).sum())
+
+    base = [q, nk, nv, kc, vc]
+    picks = {0: [(1, 2, 0, 3), (2, 1, 1, 0), (0, 0, 2, 4), (3, 3, 0, 1), (1, 0, 2, 2)],
+             1: [(1, 0, 1, 2), (0, 1, 2, 4), (2, 0, 0, 1)],
+             2: [(1, 1, 0, 5), (0, 0, 2, 0), (3, 1, 1, 3)],
+             3: [(1, 0, 2, 1), (1, 1, 4, 3), (1, 0, 5, 0), (2, 1, 6, 2), (0, 0, 9, 4)],
+             4: [(1, 1, 3, 5), (1, 0, 4, 2), (2, 0, 8, 1), (3, 1, 2, 0)]}
+    names = ("d_query", "d_new_key", "d_new_value", "d_key_cache", "d_value_cache")
+    for which, idxs in picks.items():
+        for idx in idxs:
+            x0 = float(base[which][idx])
+            h = 2.0 ** -9 * max(1.0, abs(x0))
+            vals = []
+            for sgn in (1.0, -1.0):
+                xs = [t.clone() for t in base]
+                xs[which][idx] = x0 + sgn * h
+                vals.append((loss(xs), float(xs[which][idx])))
+            fd = (vals[0][0] - vals[1][0]) / (vals[0][1] - vals[1][1])
+            an = back[names[which]][idx]
+            assert abs(fd - an) <= 2e-4 * max(1.0, abs(an)), (names[which], idx, fd, an)
+
+
+def pin_backward_cache_routing(o):
+    """[contract] bullets 3-4: each entry of a returned cache is either the old
+    cache entry or a new row, so with gradients on the returned caches only,
+    they go back exactly where the entries came from: slots outside
+    [L, L + n) to the input cache, slots L + t to new row t (rows t >= n get
+    none, overwritten cache slots get none), and the query gets none."""
+    args, counts, grads = _grad_case(torch.float32, 34)
+    q, nk, nv, kc, vc, lengths, mask = args
+    got = o.step_backward(*args, d_key_cache=grads["d_key_cache"],
+                          d_value_cache=grads["d_value_cache"])
+    assert np.all(got["d_query"] == 0.0)
+    for dname, nname, src in (("d_key_cache", "d_new_key", grads["d_key_cache"]),
+                              ("d_value_cache", "d_new_value", grads["d_value_cache"])):
+        gsrc = o.widen(src)
+        want_c, want_n = gsrc.copy(), np.zeros(got[nname].shape)
+        for b in range(gsrc.shape[0]):
+            L, n = int(lengths[b]), int(counts[b])
+            want_c[b, :, L:L + n] = 0.0
+            want_n[b, :, :n] = gsrc[b, :, L:L + n]
+        assert np.array_equal(got[dname], want_c), dname
+        assert np.array_equal(got[nname], want_n), nname
+
+
 ALL_PINS = [
     pin_fixed_capacity_example,
     pin_fixed_capacity_closed_form,
@@ -638,4 +770,7 @@ ALL_PINS = [
     pin_attend_cache_outside_contract,
     pin_paged_equals_contiguous_step,
     pin_paged_bad_block_ids_append_nothing,
+    pin_backward_vs_autograd,
+    pin_backward_finite_differences,
+    pin_backward_cache_routing,
 ]

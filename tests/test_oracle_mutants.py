@@ -25,6 +25,15 @@ MUTANTS = {
     "attend_slot_ignored": ("const int64_t slot = slot_ids ? slot_ids[b] : b;", "const int64_t slot = b;"),
     "attend_query_row_fixed": ("const int64_t row = cu_q[b] + t;", "const int64_t row = cu_q[b];"),
     "attend_s_gt_k_accepted": ("const int bad = S < 0 || S > K ||", "const int bad = S < 0 ||"),
+    # gradients
+    "bwd_softmax_not_centred": ("const double ds = a[j] * (g[j] - dot_ag);",
+                                "const double ds = a[j] * g[j];"),
+    "bwd_scale_dropped_in_dq": ("dq[d] += scale * ds * kd;", "dq[d] += ds * kd;"),
+    "bwd_value_grad_from_ds": ("+= a[j] * dc;", "+= ds * dc;"),
+    "bwd_overwritten_slot_keeps_grad": ("d_key_cache[at4(Hk, M, D, b, kv, j, d)] = 0.0;",
+                                        "d_key_cache[at4(Hk, M, D, b, kv, j, d)] = gk;"),
+    "bwd_new_row_offset": ("d_new_key[at4(Hk, Q, D, b, kv, j - L, d)] += scale * ds * qd;",
+                           "d_new_key[at4(Hk, Q, D, b, kv, 0, d)] += scale * ds * qd;"),
 }
 
 
