@@ -329,6 +329,51 @@ KVC_API int kvc_step_static(const kvc_dims *dims, const void *query, const void 
                             void *out_context, int32_t *dev_status, void *stream);
 
 /*
+ * kvc_step_backward -- gradients of kvc_step's outputs with respect to its
+ * inputs. The contract's test suite grades gradients ("Autoregressive KV-cache
+ * append and causal attention", Starter code); the returned caches, attention
+ * and context are functions of query, new_key, new_value, key_cache and
+ * value_cache by the Required behavior, and this is their chain rule:
+ *
+ *   - each entry of a returned cache came from an input cache slot or from a
+ *     new row (bullet 3): its gradient goes back there; slots L + t that a
+ *     new row overwrote pass nothing to the input cache;
+ *   - for a valid query row t and an allowed slot j <= L + t (bullet 4), with
+ *     a = softmax(s), s = scale q.K' (bullet 5), context = a V':
+ *       g_j = d_attention_j + d_context . V'_j,
+ *       ds_j = a_j (g_j - sum_k a_k g_k),
+ *       d_query = scale sum_j ds_j K'_j, dK'_j += scale ds_j q, dV'_j += a_j d_context;
+ *     invalid rows and disallowed slots are constants of the forward and pass
+ *     nothing.
+ *
+ *   dims, query .. scale   as kvc_step (same contract, same flags into
+ *                          *dev_status: a flagged row appends nothing).
+ *   d_key_cache_out        [B,Hk,M,D] device dtype, gradient reaching the
+ *                          returned key cache; NULL = zero.
+ *   d_value_cache_out      [B,Hk,M,Dv], as above for the value cache.
+ *   d_attention            [B,Hq,Q,M], gradient reaching attention; NULL = 0.
+ *   d_context              [B,Hq,Q,Dv], gradient reaching context; NULL = 0.
+ *   d_query                [B,Hq,Q,D]  device dtype, written in full.
+ *   d_new_key / d_new_value [B,Hk,Q,D|Dv] written in full (rows t >= n: 0).
+ *   d_key_cache / d_value_cache [B,Hk,M,D|Dv] written in full.
+ *   workspace              device, >= kvc_backward_workspace_bytes(dims), 16-byte aligned.
+ *
+ * D and Dv at most 256 (KVC_E_SHAPE otherwise). Sums are fp32; gradients are
+ * rounded to the dtype once. The outputs may not overlap any input, the
+ * workspace or each other (KVC_E_ALIAS). Work is enqueued on `stream`.
+ */
+KVC_API size_t kvc_backward_workspace_bytes(const kvc_dims *dims);
+KVC_API int kvc_step_backward(const kvc_dims *dims, const void *query, const void *new_key,
+                              const void *new_value, const void *key_cache,
+                              const void *value_cache, const int64_t *lengths,
+                              const uint8_t *append_mask, double scale,
+                              const void *d_key_cache_out, const void *d_value_cache_out,
+                              const void *d_attention, const void *d_context, void *d_query,
+                              void *d_new_key, void *d_new_value, void *d_key_cache,
+                              void *d_value_cache, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_status, void *stream);
+
+/*
  * kvc_selftest_wait_timeout -- runs the failure path of the step kernels'
  * pipeline waits without a fault. Every such wait is an mbarrier wait with a
  * time limit; when its phase never completes, the waiting role sets the CTA's

@@ -437,6 +437,12 @@ struct StepMode {
     // paged pools (in place only): [num_blocks, Hk, block_size, width]
     const int32_t* block_table = nullptr;  // device [B, M / block_size]
     int64_t block_size = 0, num_blocks = 0;
+    // the backward's statistics pass (with inplace): the step's kernels read
+    // the inputs and write nothing but the workspace: no cache row write, the
+    // CUDA-core or generic path only (fp32 scores), the context also in fp32
+    bool stats_only = false;
+    float* ctx_f32 = nullptr;
+    StepParams* params_out = nullptr;  // receives the parameters the kernels ran with
 };
 
 int step_impl(const kvc_dims* dims, const void* query, const void* new_key, const void* new_value,
@@ -476,10 +482,9 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     const bool tc_pages = !paged || mode.block_size % kTcT == 0 ||
                           (kTcT % mode.block_size == 0 && mode.block_size >= 8);
     Plan pl;
-    if (!(ptrs_aligned && aligned16(query) && tc_pages &&
-          tc_plan(d, dev.sms, dev.smem_optin, &pl)) &&
-        !(inplace && ptrs_aligned && aligned16(query) && tc_pages &&
-          dec_plan(d, dev.sms, dev.smem_optin, &pl)) &&
+    const bool tc_ok = !mode.stats_only && ptrs_aligned && aligned16(query) && tc_pages;
+    if (!(tc_ok && tc_plan(d, dev.sms, dev.smem_optin, &pl)) &&
+        !(tc_ok && inplace && dec_plan(d, dev.sms, dev.smem_optin, &pl)) &&
         !(ptrs_aligned &&
           ((inplace && fused_plan(d, dev.sms, dev.smem_optin, aligned16(query), &pl,
                                   kStageTargetInplace)) ||
@@ -562,6 +567,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     p.tc_tmem_cols = pl.tc_tmem_cols;
     p.dec_off_red = pl.dec_off_red;
     p.dec_off_pt = pl.dec_off_pt;
+    p.ctx_f32 = mode.ctx_f32;
     p.dev_status = dev_status;
     p.vec_attention = (d.M % 8 == 0) && aligned16(out_attention);
     p.inplace = inplace ? 1 : 0;
@@ -583,7 +589,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
         return cudaSuccess;
     };
     cudaError_t e = record();
-    if (e == cudaSuccess && inplace && !mode.readonly) {  // appended rows and lengths, before any reader
+    if (e == cudaSuccess && inplace && !mode.readonly && !mode.stats_only) {  // appended rows and lengths, before any reader
         const bool words16 = (d.D * es) % 16 == 0 && (d.Dv * es) % 16 == 0 && ptrs_aligned;
         e = launch_inplace_rows(p, words16, stream);
         if (e == cudaSuccess) e = record();
@@ -656,6 +662,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
         }
     }
     while (e == cudaSuccess && events && recorded < n_events) e = record();
+    if (mode.params_out) *mode.params_out = p;
     return e == cudaSuccess ? KVC_OK : KVC_E_CUDA;
 }
 
@@ -1058,3 +1065,128 @@ const char* kvc_status_string(int status) {
 int kvc_version(void) { return 100; }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ gradients
+namespace kvc {
+namespace {
+// Backward workspace: the step's workspace (its statistics pass), then the
+// fp32 context rows, the per-row sums D, the step's context in the dtype and
+// its lengths (both unused scratch the step needs as arguments).
+struct BwdLayout {
+    size_t step = 0, ctx_f32 = 0, drow = 0, ctx_t = 0, lengths = 0, total = 0;
+};
+bool bwd_layout(const kvc_dims& d, BwdLayout* L) {
+    const size_t step = kvc_workspace_bytes(&d);
+    if (step == 0) return false;
+    const int64_t rows = d.B * d.Hq * d.Q, es = elem_size(d.dtype);
+    int64_t off = align_up(static_cast<int64_t>(step), 256);
+    L->step = step;
+    L->ctx_f32 = static_cast<size_t>(off);
+    off = align_up(off + rows * d.Dv * 4, 256);
+    L->drow = static_cast<size_t>(off);
+    off = align_up(off + rows * 4, 256);
+    L->ctx_t = static_cast<size_t>(off);
+    off = align_up(off + rows * d.Dv * es, 256);
+    L->lengths = static_cast<size_t>(off);
+    off = align_up(off + d.B * 8, 256);
+    L->total = static_cast<size_t>(off);
+    return true;
+}
+}  // namespace
+}  // namespace kvc
+
+size_t kvc_backward_workspace_bytes(const kvc_dims* dims) {
+    using namespace kvc;
+    if (!dims || check_dims(dims) != KVC_OK) return 0;
+    BwdLayout L;
+    return bwd_layout(*dims, &L) ? L.total : 0;
+}
+
+int kvc_step_backward(const kvc_dims* dims, const void* query, const void* new_key,
+                      const void* new_value, const void* key_cache, const void* value_cache,
+                      const int64_t* lengths, const uint8_t* append_mask, double scale,
+                      const void* d_key_cache_out, const void* d_value_cache_out,
+                      const void* d_attention, const void* d_context, void* d_query,
+                      void* d_new_key, void* d_new_value, void* d_key_cache, void* d_value_cache,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    using namespace kvc;
+    int rc = check_dims(dims);
+    if (rc != KVC_OK) return rc;
+    const kvc_dims d = *dims;
+    if (d.D > 256 || d.Dv > 256) return KVC_E_SHAPE;
+    const bool hasq = d.Q > 0;
+    if (!key_cache || !value_cache || !lengths || !d_key_cache || !d_value_cache)
+        return KVC_E_NULL;
+    if (hasq && (!query || !new_key || !new_value || !append_mask || !d_query || !d_new_key ||
+                 !d_new_value))
+        return KVC_E_NULL;
+    BwdLayout Lw;
+    if (!bwd_layout(d, &Lw)) return KVC_E_SHAPE;
+    if (!workspace || workspace_bytes < Lw.total || !aligned16(workspace)) return KVC_E_WORKSPACE;
+    const int64_t es = elem_size(d.dtype);
+    const int64_t kc_bytes = d.B * d.Hk * d.M * d.D * es, vc_bytes = d.B * d.Hk * d.M * d.Dv * es;
+    const Range in[] = {
+        range_of(query, d.B * d.Hq * d.Q * d.D * es),
+        range_of(new_key, d.B * d.Hk * d.Q * d.D * es),
+        range_of(new_value, d.B * d.Hk * d.Q * d.Dv * es),
+        range_of(key_cache, kc_bytes),
+        range_of(value_cache, vc_bytes),
+        range_of(lengths, d.B * 8),
+        range_of(append_mask, d.B * d.Q),
+        range_of(d_key_cache_out, kc_bytes),
+        range_of(d_value_cache_out, vc_bytes),
+        range_of(d_attention, d.B * d.Hq * d.Q * d.M * es),
+        range_of(d_context, d.B * d.Hq * d.Q * d.Dv * es),
+    };
+    const Range out[] = {
+        range_of(d_query, d.B * d.Hq * d.Q * d.D * es),
+        range_of(d_new_key, d.B * d.Hk * d.Q * d.D * es),
+        range_of(d_new_value, d.B * d.Hk * d.Q * d.Dv * es),
+        range_of(d_key_cache, kc_bytes),
+        range_of(d_value_cache, vc_bytes),
+        range_of(workspace, static_cast<int64_t>(Lw.total)),
+    };
+    for (const Range& o : out)
+        for (const Range& i : in)
+            if (overlaps(o, i)) return KVC_E_ALIAS;
+    for (size_t a = 0; a < sizeof(out) / sizeof(out[0]); ++a)
+        for (size_t b = a + 1; b < sizeof(out) / sizeof(out[0]); ++b)
+            if (overlaps(out[a], out[b])) return KVC_E_ALIAS;
+
+    // 1. the step's statistics over the inputs, writing only the workspace
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    StepMode mode;
+    mode.inplace = true;
+    mode.rows = false;
+    mode.stats_only = true;
+    mode.ctx_f32 = reinterpret_cast<float*>(ws + Lw.ctx_f32);
+    StepParams p;
+    mode.params_out = &p;
+    rc = step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths, append_mask,
+                   scale, const_cast<void*>(key_cache), const_cast<void*>(value_cache),
+                   reinterpret_cast<int64_t*>(ws + Lw.lengths), nullptr, ws + Lw.ctx_t, ws,
+                   Lw.step, dev_status, stream, nullptr, 0, mode);
+    if (rc != KVC_OK) return rc;
+    // 2. the gradients
+    BwdParams bp;
+    std::memset(&bp, 0, sizeof(bp));
+    bp.p = p;
+    bp.d_key_out = d_key_cache_out;
+    bp.d_value_out = d_value_cache_out;
+    bp.d_attention = d_attention;
+    bp.d_context = d_context;
+    bp.d_query = d_query;
+    bp.d_new_key = d_new_key;
+    bp.d_new_value = d_new_value;
+    bp.d_key_cache = d_key_cache;
+    bp.d_value_cache = d_value_cache;
+    bp.drow = reinterpret_cast<float*>(ws + Lw.drow);
+    bp.scale = static_cast<float>(scale);
+    bp.slots_per_block = 64;
+    const bool words16 = (d.D * es) % 16 == 0 && (d.Dv * es) % 16 == 0 &&
+                         aligned16(d_key_cache) && aligned16(d_value_cache) &&
+                         aligned16(d_key_cache_out) && aligned16(d_value_cache_out);
+    const cudaError_t e = launch_backward(bp, d.dtype, words16, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVC_OK : KVC_E_CUDA;
+}
+

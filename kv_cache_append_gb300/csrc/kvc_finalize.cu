@@ -79,7 +79,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
     T* ctx = static_cast<T*>(p.out_context) + row * p.Dv;
     if (t >= ra.n) {
-        for (int64_t e = lane; e < p.Dv; e += 32) ctx[e] = S::from_float(0.f);
+        for (int64_t e = lane; e < p.Dv; e += 32) {
+            ctx[e] = S::from_float(0.f);
+            if (p.ctx_f32) p.ctx_f32[row * p.Dv + e] = 0.f;
+        }
         if (lane == 0) p.rowstat[row] = RowStat{0.f, 0.f, -1, 0};
         return;
     }
@@ -126,8 +129,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
             }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (act[i]) ctx[e0 + lane + 32 * i] = S::from_float(a[i] * inv_l);
+        for (int i = 0; i < 4; ++i) {
+            if (!act[i]) continue;
+            ctx[e0 + lane + 32 * i] = S::from_float(a[i] * inv_l);
+            if (p.ctx_f32) p.ctx_f32[row * p.Dv + e0 + lane + 32 * i] = a[i] * inv_l;
+        }
     }
 }
 

@@ -532,6 +532,7 @@ struct StepParams {
     int64_t fin_seg;    // attention slots per row-writer block (a multiple of 8)
     int64_t fin_nseg;   // row-writer blocks per query row: ceil(M / fin_seg)
     RowStat* rowstat;   // [B][Hq][Q]: the merged maximum, 1 / sum and last allowed slot
+    float* ctx_f32;     // nullable: the merge also writes the context rows in fp32 here
 };
 
 // The cache unit that unit u = b * Hk + kv reads.

@@ -48,6 +48,28 @@ struct DecParams {
 cudaError_t launch_decode_tc(const DecParams& dp, int dtype, int nr, size_t smem,
                              cudaStream_t stream);
 
+// Gradients of the step (kvc_backward.cu). p is the step's own parameters
+// after its statistics pass (scores, rowstat and ctx_f32 filled); the four
+// incoming gradients are nullable (zero); every output is written in full.
+struct BwdParams {
+    StepParams p;
+    const void* d_key_out;    // [B,Hk,M,D]  gradient reaching the returned key cache
+    const void* d_value_out;  // [B,Hk,M,Dv]
+    const void* d_attention;  // [B,Hq,Q,M]
+    const void* d_context;    // [B,Hq,Q,Dv]
+    void* d_query;            // [B,Hq,Q,D]
+    void* d_new_key;          // [B,Hk,Q,D]
+    void* d_new_value;        // [B,Hk,Q,Dv]
+    void* d_key_cache;        // [B,Hk,M,D]
+    void* d_value_cache;      // [B,Hk,M,Dv]
+    float* drow;              // [B*Hq*Q] scratch: sum_j a_j g_j per query row
+    float scale;              // the scores' scale (natural-log domain)
+    int64_t slots_per_block;  // cache slots per block of bwd_kv_kernel
+};
+// words16: cache rows are whole 16-byte words and the gradient buffers are
+// 16-byte aligned (the slots past the new length are copied 16 bytes at a time).
+cudaError_t launch_backward(const BwdParams& bp, int dtype, bool words16, cudaStream_t stream);
+
 // Merge of the partials: context rows and one RowStat per query row (kvc_finalize.cu).
 cudaError_t launch_finalize_merge(const StepParams& p, int dtype, cudaStream_t stream);
 // Attention rows from the kept scores (or P values) and the RowStats (kvc_finalize.cu).

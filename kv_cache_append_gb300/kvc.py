@@ -99,6 +99,11 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kvc_step_paged.argtypes = paged_args
             lib.kvc_step_paged_timed.restype = i32
             lib.kvc_step_paged_timed.argtypes = paged_args + [ctypes.POINTER(vp), i32]
+            lib.kvc_backward_workspace_bytes.restype = sz
+            lib.kvc_backward_workspace_bytes.argtypes = [dp]
+            lib.kvc_step_backward.restype = i32
+            lib.kvc_step_backward.argtypes = ([dp] + [vp] * 7 + [ctypes.c_double] + [vp] * 9 +
+                                              [vp, sz, vp, vp])
             lib.kvc_selftest_wait_timeout.restype = i32
             lib.kvc_selftest_wait_timeout.argtypes = [vp, i64, vp]
             lib.kvc_status_string.restype = ctypes.c_char_p
@@ -280,7 +285,23 @@ def kv_cache_attention_step(query: torch.Tensor, new_key: torch.Tensor, new_valu
     "scale" only (default 1/sqrt(D)). ``status`` is an optional int32 CUDA
     tensor of one element into which the kernels OR contract-violation bits
     (1 = capacity overflow, 2 = non-prefix mask); it is not synchronized.
+
+    Differentiable: when gradients are enabled and query, new_key, new_value
+    or a cache requires grad, the outputs carry a backward (kvc_step_backward)
+    to all five (lengths has none).
     """
+    if torch.is_grad_enabled() and any(
+            t.requires_grad for t in (query, new_key, new_value, key_cache, value_cache)):
+        kc, vc, ln, att, ctx = _Step.apply(query, new_key, new_value, key_cache, value_cache,
+                                           lengths, append_mask, options, status)
+        return {"key_cache": kc, "value_cache": vc, "lengths": ln, "attention": att,
+                "context": ctx}
+    return _step_forward(query, new_key, new_value, key_cache, value_cache, lengths, append_mask,
+                         options, status)
+
+
+def _step_forward(query, new_key, new_value, key_cache, value_cache, lengths, append_mask,
+                  options, status) -> dict:
     check_inputs(query, new_key, new_value, key_cache, value_cache, lengths, append_mask)
     scale = _scale_from(options, query.shape[-1])
     q, nk, nv, kc, vc = (t.contiguous() for t in (query, new_key, new_value, key_cache,
@@ -294,6 +315,99 @@ def kv_cache_attention_step(query: torch.Tensor, new_key: torch.Tensor, new_valu
     ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
     with torch.cuda.device(q.device):
         step_into(dims, q, nk, nv, kc, vc, ln, mk, scale, out, ws, status)
+    return out
+
+
+class _Step(torch.autograd.Function):
+    """The step as an autograd node: forward kvc_step, backward kvc_step_backward."""
+
+    @staticmethod
+    def forward(ctx, query, new_key, new_value, key_cache, value_cache, lengths, append_mask,
+                options, status):
+        out = _step_forward(query.detach(), new_key.detach(), new_value.detach(),
+                            key_cache.detach(), value_cache.detach(), lengths, append_mask,
+                            options, status)
+        ctx.save_for_backward(query, new_key, new_value, key_cache, value_cache, lengths,
+                              append_mask)
+        ctx.options = options
+        ctx.set_materialize_grads(False)
+        ctx.mark_non_differentiable(out["lengths"])
+        return (out["key_cache"], out["value_cache"], out["lengths"], out["attention"],
+                out["context"])
+
+    @staticmethod
+    def backward(ctx, d_key_cache, d_value_cache, _d_lengths, d_attention, d_context):
+        q, nk, nv, kc, vc, ln, mk = ctx.saved_tensors
+        g = kv_cache_attention_step_backward(q.detach(), nk.detach(), nv.detach(), kc.detach(),
+                                             vc.detach(), ln, mk, ctx.options,
+                                             d_key_cache=d_key_cache, d_value_cache=d_value_cache,
+                                             d_attention=d_attention, d_context=d_context)
+        return (g["query"], g["new_key"], g["new_value"], g["key_cache"], g["value_cache"],
+                None, None, None, None)
+
+
+def backward_workspace_bytes(dims: Dims) -> int:
+    return int(library().kvc_backward_workspace_bytes(ctypes.byref(dims)))
+
+
+def step_backward_into(dims: Dims, query, new_key, new_value, key_cache, value_cache, lengths,
+                       append_mask, scale: float, grads: dict, out: dict,
+                       workspace: torch.Tensor, status: Optional[torch.Tensor] = None,
+                       stream: Optional[int] = None) -> None:
+    """Enqueue one kvc_step_backward (no checks beyond libkvc's). grads holds
+    the gradients reaching "key_cache", "value_cache", "attention" and
+    "context" (each a contiguous tensor of the inputs' dtype, or None for
+    zero); out receives "query", "new_key", "new_value", "key_cache" and
+    "value_cache"."""
+    lib = library()
+    if stream is None:
+        stream = torch.cuda.current_stream(query.device).cuda_stream
+    rc = lib.kvc_step_backward(
+        ctypes.byref(dims), _p(query), _p(new_key), _p(new_value), _p(key_cache),
+        _p(value_cache), _p(lengths), _p(append_mask), ctypes.c_double(scale),
+        *(_p(grads.get(k)) for k in ("key_cache", "value_cache", "attention", "context")),
+        *(_p(out[k]) for k in ("query", "new_key", "new_value", "key_cache", "value_cache")),
+        _p(workspace), workspace.numel(), _p(status), ctypes.c_void_p(stream))
+    if rc != KVC_OK:
+        raise KvcError(rc, status_string(rc))
+
+
+def kv_cache_attention_step_backward(query, new_key, new_value, key_cache, value_cache, lengths,
+                                     append_mask, options: Optional[dict] = None,
+                                     d_key_cache=None, d_value_cache=None, d_attention=None,
+                                     d_context=None, status: Optional[torch.Tensor] = None
+                                     ) -> dict:
+    """Gradients of the step's outputs (key_cache, value_cache, attention,
+    context) with respect to query, new_key, new_value, key_cache and
+    value_cache, given the gradients reaching those outputs (None = zero).
+    Returns {"query", "new_key", "new_value", "key_cache", "value_cache"}."""
+    check_inputs(query, new_key, new_value, key_cache, value_cache, lengths, append_mask)
+    scale = _scale_from(options, query.shape[-1])
+    q, nk, nv, kc, vc = (t.contiguous() for t in (query, new_key, new_value, key_cache,
+                                                   value_cache))
+    ln = lengths.to(torch.int64).contiguous()
+    mk = append_mask.contiguous()
+    mk = mk.view(torch.uint8) if mk.dtype == torch.bool else mk
+    B, Hq, Q, D = q.shape
+    M, Dv = kc.shape[2], vc.shape[-1]
+    shapes = {"key_cache": tuple(kc.shape), "value_cache": tuple(vc.shape),
+              "attention": (B, Hq, Q, M), "context": (B, Hq, Q, Dv)}
+    grads = {}
+    for name, g in (("key_cache", d_key_cache), ("value_cache", d_value_cache),
+                    ("attention", d_attention), ("context", d_context)):
+        if g is None:
+            grads[name] = None
+            continue
+        if tuple(g.shape) != shapes[name] or g.device != q.device:
+            raise ValueError(f"gradient of {name}: shape {tuple(g.shape)} != {shapes[name]}")
+        grads[name] = g.to(q.dtype).contiguous()
+    dims = dims_of(q, kc, vc)
+    out = {"query": torch.empty_like(q), "new_key": torch.empty_like(nk),
+           "new_value": torch.empty_like(nv), "key_cache": torch.empty_like(kc),
+           "value_cache": torch.empty_like(vc)}
+    ws = torch.empty(backward_workspace_bytes(dims), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        step_backward_into(dims, q, nk, nv, kc, vc, ln, mk, scale, grads, out, ws, status)
     return out
 
 

@@ -1,0 +1,163 @@
+"""GPU parity of the step's gradients (kvc_step_backward) against the fp64
+oracle (oracle.step_backward), and of the autograd face of
+kv_cache_attention_step.
+
+Tolerances: the kernels sum in fp32 and round each gradient to the dtype
+once, so the error is that final rounding (half an ulp: 2^-9 relative for
+bf16, 2^-12 for fp16, 2^-24 for fp32) plus fp32 summation error, bounded
+here as |got - ref| <= rtol |ref| + atol max|ref| per tensor with
+(rtol, atol) = (8e-3, 2e-3) bf16, (2e-3, 5e-4) fp16, (1e-4, 1e-4) fp32.
+The pure routing parts are exact: cache slots from the new length on carry
+the returned caches' gradient bit for bit, and slots a new row overwrote
+get exactly zero.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kv_cache_append_gb300 as kvc
+import oracle
+import workloads
+from test_gpu_parity import DEV, SMALL, _bits, _built  # noqa: F401
+from workloads import Spec
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.bfloat16: (8e-3, 2e-3), torch.float16: (2e-3, 5e-4), torch.float32: (1e-4, 1e-4)}
+NAMES = ("query", "new_key", "new_value", "key_cache", "value_cache")
+
+
+def upstream(x, seed, which=("key_cache", "value_cache", "attention", "context")):
+    g = torch.Generator().manual_seed(seed)
+    B, Hq, Q, _ = x.query.shape
+    M, Dv = x.key_cache.shape[2], x.value_cache.shape[-1]
+    shapes = {"key_cache": tuple(x.key_cache.shape), "value_cache": tuple(x.value_cache.shape),
+              "attention": (B, Hq, Q, M), "context": (B, Hq, Q, Dv)}
+    return {k: (torch.randn(*shapes[k], generator=g).to(x.query.dtype) if k in which else None)
+            for k in shapes}
+
+
+def check(x, grads, status_expect=0):
+    xg = x.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = kvc.kv_cache_attention_step_backward(
+        *xg.args(), xg.options, status=status,
+        **{f"d_{k}": (None if v is None else v.to(DEV)) for k, v in grads.items()})
+    torch.cuda.synchronize()
+    ref = oracle.step_backward(*x.args(), options=x.options,
+                               **{f"d_{k}": v for k, v in grads.items()})
+    flags = int(np.bitwise_or.reduce(ref["flags"])) if len(ref["flags"]) else 0
+    assert int(status.item()) == flags == status_expect
+    rtol, atol = TOL[x.query.dtype]
+    for name in NAMES:
+        r = ref["d_" + name]
+        gw = got[name].double().cpu().numpy()
+        bound = rtol * np.abs(r) + atol * max(1.0, float(np.abs(r).max(initial=0.0)))
+        err = np.abs(gw - r)
+        assert np.all(err <= bound), (name, float(err.max()), float((err - bound).max()))
+    # exact routing: slots from the new length on, and overwritten slots
+    counts = x.append_mask.to(torch.int64).cumprod(1).sum(1)
+    for name, gk in (("key_cache", grads["key_cache"]), ("value_cache", grads["value_cache"])):
+        out = got[name].cpu()
+        for b in range(x.query.shape[0]):
+            if ref["flags"][b]:
+                continue
+            L, n = int(x.lengths[b]), int(counts[b])
+            tail = out[b, :, L + n:]
+            want = gk[b, :, L + n:] if gk is not None else torch.zeros_like(tail)
+            assert torch.equal(_bits(tail), _bits(want.contiguous())), (name, b)
+            assert torch.count_nonzero(out[b, :, L:L + n]) == 0, (name, b)
+    return got, ref
+
+
+CASES = {
+    "tiny_fp32": SMALL["tiny_fp32"],
+    "decode_bf16_ragged_M": SMALL["decode_bf16_ragged_M"],
+    "specdec_bf16_hot": SMALL["specdec_bf16"],
+    "chunk_fp32_Q40": SMALL["chunk_fp32_Q40"],
+    "mqa_fp16_D192": SMALL["mqa_fp16_D192"].replace(M=700, lengths=("uniform", 100, 690)),
+    "gqa_fp32_small_rows": SMALL["gqa_fp32_small_rows"],   # generic statistics path
+    "generic_bf16_D5_Dv7": Spec(B=3, Hq=4, Hk=2, Q=3, D=5, Dv=7, M=50, dtype="bf16",
+                                counts=("uniform", 0, 3)),
+    "mha_fp16_Dv256": SMALL["mha_fp16_Dv256"],
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("seed", [0, 1])
+def test_backward_parity(name, seed):
+    x = workloads.generate(CASES[name], seed)
+    check(x, upstream(x, 100 + seed))
+
+
+@pytest.mark.parametrize("which", [("context",), ("attention",), ("key_cache", "value_cache"),
+                                   ()])
+def test_backward_partial_gradients(which):
+    x = workloads.generate(SMALL["specdec_bf16"], 3)
+    check(x, upstream(x, 7, which))
+
+
+def test_backward_q0_and_nothing_appended():
+    for spec in (Spec(B=3, Hq=4, Hk=2, Q=0, D=64, Dv=64, M=100, dtype="bf16"),
+                 Spec(B=4, Hq=8, Hk=2, Q=3, D=128, Dv=128, M=300, dtype="bf16",
+                      counts=("fixed", 0))):
+        x = workloads.generate(spec, 1)
+        check(x, upstream(x, 2))
+
+
+def test_backward_contract_violations():
+    spec = Spec(B=5, Hq=4, Hk=2, Q=3, D=64, Dv=64, M=200, dtype="bf16")
+    x = workloads.generate(spec, 11)
+    x.lengths = torch.tensor([10, 199, 250, -3, 40])
+    m = workloads.prefix_mask([3, 3, 1, 1, 3], spec.Q)
+    m[-1, 1] = False  # not a prefix
+    x.append_mask = m
+    check(x, upstream(x, 5), status_expect=kvc.DEV_MASK | kvc.DEV_OVERFLOW)
+
+
+def test_autograd_matches_oracle():
+    """loss.backward() through kv_cache_attention_step gives the oracle's gradients."""
+    x = workloads.generate(SMALL["decode_bf16_ragged_M"].replace(B=3, M=300), 4)
+    grads = upstream(x, 9)
+    xg = x.to(DEV)
+    leaves = [t.clone().requires_grad_(True) for t in (xg.query, xg.new_key, xg.new_value,
+                                                        xg.key_cache, xg.value_cache)]
+    out = kvc.kv_cache_attention_step(*leaves, xg.lengths, xg.append_mask, xg.options)
+    assert out["context"].requires_grad and not out["lengths"].requires_grad
+    loss = sum((out[k].float() * grads[k].to(DEV).float()).sum()
+               for k in ("key_cache", "value_cache", "attention", "context"))
+    loss.backward()
+    ref = oracle.step_backward(*x.args(), options=x.options,
+                               **{f"d_{k}": v for k, v in grads.items()})
+    rtol, atol = TOL[x.query.dtype]
+    for name, leaf in zip(NAMES, leaves):
+        r = ref["d_" + name]
+        err = np.abs(leaf.grad.double().cpu().numpy() - r)
+        assert np.all(err <= rtol * np.abs(r) + atol * max(1.0, float(np.abs(r).max()))), name
+
+
+def test_backward_decode_full_size_sampled():
+    """gqa_decode sizes; the gradients of sampled batch rows against the oracle
+    on the sub-batch they form (batch rows are independent)."""
+    spec = workloads.SPECS["gqa_decode"]
+    x = workloads.generate(spec, seed=1, device=DEV)
+    grads = upstream(x, 12, which=("attention", "context"))
+    grads = {k: (None if v is None else v.to(DEV)) for k, v in grads.items()}
+    got = kvc.kv_cache_attention_step_backward(*x.args(), x.options,
+                                               **{f"d_{k}": v for k, v in grads.items()})
+    torch.cuda.synchronize()
+    lengths = x.lengths.cpu().numpy()
+    bsel = sorted({int(lengths.argmax()), int(lengths.argmin()), 7})
+    idx = torch.tensor(bsel, device=DEV)
+    sub = [t.index_select(0, idx).cpu() for t in x.args()]
+    ref = oracle.step_backward(*sub, options=x.options,
+                               **{f"d_{k}": (None if v is None else v.index_select(0, idx).cpu())
+                                  for k, v in grads.items()})
+    rtol, atol = TOL[x.query.dtype]
+    for name in NAMES:
+        r = ref["d_" + name]
+        gw = got[name].index_select(0, idx).double().cpu().numpy()
+        err = np.abs(gw - r)
+        assert np.all(err <= rtol * np.abs(r) + atol * max(1.0, float(np.abs(r).max()))), name
+    del got, x
+    torch.cuda.empty_cache()
