@@ -56,6 +56,11 @@ PATH_KERNELS_READONLY = {
     path: ["attend_prep_kernel", STEP_KERNEL[path] if path != "generic" else "generic_attend_kernel",
            "finalize_merge_kernel", "attend_unpack_kernel"]
     for path in ("fused", "tensor", "decode_tc", "generic")}
+# the backward: the statistics pass (step kernel and merge, no copy), then its own four
+PATH_KERNELS_BACKWARD = {
+    path: [first, "finalize_merge_kernel", "bwd_rowdot_kernel", "bwd_kv_kernel",
+           "bwd_copy_kernel", "bwd_dq_kernel"]
+    for path, first in (("fused", "fused_step_kernel"), ("generic", "generic_attend_kernel"))}
 PATH_KERNELS = {"fused": ["fused_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "tensor": ["tc_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "generic": ["generic_copy_kernel", "generic_attend_kernel",
@@ -67,6 +72,8 @@ KERNEL_SOURCES = {
                                            "kvc_pipeline.cuh", "kvc_tcgen05.cuh")],
     "decode_tc_kernel": [_CSRC + f for f in ("kvc_decode_tc.cu", "kvc_internal.cuh",
                                              "kvc_pipeline.cuh", "kvc_tcgen05.cuh")],
+    "bwd_kv_kernel": [_CSRC + f for f in ("kvc_backward.cu", "kvc_internal.cuh")],
+    "bwd_copy_kernel": [_CSRC + f for f in ("kvc_backward.cu", "kvc_internal.cuh")],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
 
@@ -123,6 +130,29 @@ def algorithmic_bytes_readonly(spec: workloads.Spec, lengths, counts) -> dict:
             "finalize_kernel": out}
 
 
+def algorithmic_bytes_backward(spec: workloads.Spec, lengths, counts) -> dict:
+    """Bytes the step's backward must move at minimum, all four upstream
+    gradients given: the returned caches' gradient read and the caches'
+    gradient written in full; the valid prefix of both caches (N_b = L_b + n_b
+    slots per KV head) read; the attention gradient on the allowed slots, the
+    context gradient and the query read; the query and new-row gradients
+    written, the new rows read. Per kernel: bwd_kv_kernel covers the slots
+    below the new length (prefix, the two cache gradients there, the
+    attention gradient, query and context gradient rows), bwd_copy_kernel the
+    slots from it on (cache gradients read and written)."""
+    es = 4 if spec.dtype == "f32" else 2
+    B = len(lengths)
+    row = spec.Hk * (spec.D + spec.Dv) * es
+    N = [int(l) + int(c) for l, c in zip(lengths, counts)]
+    allowed = sum(spec.Hq * sum(int(l) + t + 1 for t in range(int(c)))
+                  for l, c in zip(lengths, counts))
+    qrows = B * spec.Hq * spec.Q
+    kv = sum(N) * row * 3 + allowed * es + qrows * (spec.D + spec.Dv) * es
+    copy = sum(spec.M - n for n in N) * row * 2
+    rest = qrows * spec.D * es + 2 * B * spec.Hk * spec.Q * (spec.D + spec.Dv) * es + B * (16 + spec.Q)
+    return {"total": kv + copy + rest, "bwd_kv_kernel": kv, "bwd_copy_kernel": copy}
+
+
 def source_digest(paths) -> str:
     h = hashlib.sha256()
     for p in paths:
@@ -142,8 +172,8 @@ def measured_peak():
 def mode_key(args) -> str:
     """Key of a workload and step face in the traffic record, e.g.
     "gqa_decode", "inplace:gqa_decode", "paged64:gqa_decode"."""
-    mode = ("readonly" if args.readonly else f"paged{args.paged}" if args.paged else
-            "inplace" if args.inplace else "")
+    mode = ("backward" if args.backward else "readonly" if args.readonly else
+            f"paged{args.paged}" if args.paged else "inplace" if args.inplace else "")
     return f"{mode}:{args.workload}" if mode else args.workload
 
 
@@ -261,16 +291,40 @@ def barrier(world: int):
 
 
 # ----------------------------------------------------------------- CPU oracle leg
-def oracle_sample(spec: workloads.Spec, x_cpu: workloads.StepInputs, budget_s: float):
+def backward_grads(spec, x, seed, device):
+    """Seeded upstream gradients of the four outputs, in the inputs' dtype."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    B, Hq, Q, _ = x.query.shape
+    M, Dv = x.key_cache.shape[2], x.value_cache.shape[-1]
+    dt = x.query.dtype
+    return {"key_cache": torch.randn(tuple(x.key_cache.shape), generator=g, device=device).to(dt),
+            "value_cache": torch.randn(tuple(x.value_cache.shape), generator=g,
+                                       device=device).to(dt),
+            "attention": torch.randn(B, Hq, Q, M, generator=g, device=device).to(dt),
+            "context": torch.randn(B, Hq, Q, Dv, generator=g, device=device).to(dt)}
+
+
+def oracle_call(x_cpu, k: int, backward: bool, grads=None):
+    """One oracle step (or its backward) on the first k batch rows."""
+    import oracle
+    sub = [t[:k] for t in x_cpu.args()]
+    if backward:
+        return oracle.step_backward(*sub, options=x_cpu.options,
+                                    **{f"d_{n}": g[:k] for n, g in grads.items()})
+    return oracle.step(*sub, x_cpu.options)
+
+
+def oracle_sample(spec: workloads.Spec, x_cpu: workloads.StepInputs, budget_s: float,
+                  backward: bool = False):
     """Time the fp64 oracle on the first k batch rows, k grown until the run
     takes about budget_s. Returns (seconds, rows, threads)."""
     import oracle
     oracle.build()
+    grads = backward_grads(spec, x_cpu, 5, "cpu") if backward else None
     k = 1
     while True:
-        sub = [t[:k] for t in x_cpu.args()]
         t0 = time.perf_counter()
-        oracle.step(*sub, x_cpu.options)
+        oracle_call(x_cpu, k, backward, grads)
         dt = time.perf_counter() - t0
         if dt >= budget_s or k >= spec.B:
             return dt, k, oracle.threads()
@@ -289,16 +343,19 @@ def run_reference(args, spec, world, rank):
     x = cpu_inputs(spec, seed=1)
     per_step_budget = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     # size the sample once, then time W + K steps of that sample
-    _, rows, threads = oracle_sample(spec, x, per_step_budget)
-    sub = [t[:rows] for t in x.args()]
-    import oracle
+    _, rows, threads = oracle_sample(spec, x, per_step_budget, args.backward)
+    grads = backward_grads(spec, x, 5, "cpu") if args.backward else None
     for _ in range(args.warmup):
-        oracle.step(*sub, x.options)
+        oracle_call(x, rows, args.backward, grads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.step(*sub, x.options)
+        oracle_call(x, rows, args.backward, grads)
     dt = (time.perf_counter() - t0) / args.steps
-    if args.inplace or args.readonly:  # the same attention, counted with that face's bytes
+    if args.backward:
+        nbytes = algorithmic_bytes_backward(spec, x.lengths[:rows].tolist(),
+                                            x.append_mask[:rows].to(torch.int64).sum(1).tolist()
+                                            )["total"]
+    elif args.inplace or args.readonly:  # the same attention, counted with that face's bytes
         f = algorithmic_bytes_readonly if args.readonly else algorithmic_bytes_inplace
         nbytes = f(spec, x.lengths[:rows].tolist(),
                    x.append_mask[:rows].to(torch.int64).sum(1).tolist())["total"]
@@ -399,6 +456,21 @@ def run_ours(args, spec, world, rank, local):
         def step(events=None):
             kvc.attend_cache_into(dims, Bn, q_packed, kc_p, vc_p, cu, kl, False, slots, scale,
                                   out_ro, ws, None, stream.cuda_stream, events)
+    elif args.backward:
+        # the step's gradients for seeded upstream gradients of all four outputs
+        grads = backward_grads(spec, x, 5 + rank, dev)
+        outb = {"query": torch.empty_like(q), "new_key": torch.empty_like(nk),
+                "new_value": torch.empty_like(nv), "key_cache": torch.empty_like(kc),
+                "value_cache": torch.empty_like(vc)}
+        del out
+        torch.cuda.empty_cache()
+        ws = torch.empty(kvc.backward_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+        path = "generic" if kvc.plan_info(dims, kc, vc, nk, nv, kc, vc)[1] == "generic" else "fused"
+        nkern = 6 if spec.Q > 0 else 2
+
+        def step(events=None):
+            kvc.step_backward_into(dims, q, nk, nv, kc, vc, ln, mk, scale, grads, outb, ws, None,
+                                   stream.cuda_stream, events)
     elif args.inplace:
         # donated caches: every step appends the same rows at the same slots,
         # so repeated steps leave the caches as the first one did
@@ -456,23 +528,31 @@ def run_ours(args, spec, world, rank, local):
 
     lengths_h = x.lengths.cpu().tolist()
     counts_h = x.append_mask.to(torch.int64).sum(1).cpu().tolist()
-    nbytes = (algorithmic_bytes_readonly(spec, lengths_h, counts_h) if args.readonly else
+    nbytes = (algorithmic_bytes_backward(spec, lengths_h, counts_h) if args.backward else
+              algorithmic_bytes_readonly(spec, lengths_h, counts_h) if args.readonly else
               algorithmic_bytes_inplace(spec, lengths_h, counts_h) if (args.inplace or args.paged)
               else algorithmic_bytes(spec))
     value = world * nbytes["total"] / (ms_step * 1e-3) / 1e9
     peak, peak_src = measured_peak()
-    ks = (2 if args.paged and nkern > 2 else
-          1 if (args.inplace or args.readonly) and nkern > 1 else 0)  # index of the step kernel
+    if args.backward:  # the longer of the two HBM kernels of the gradients
+        names_b = PATH_KERNELS_BACKWARD[path] if nkern == 6 else ["bwd_kv_kernel", "bwd_copy_kernel"]
+        ks = max((i for i, nm in enumerate(names_b) if nm in ("bwd_kv_kernel", "bwd_copy_kernel")),
+                 key=lambda i: kern_ms[i])
+        kname = names_b[ks]
+        nbytes["fused_kernel"] = nbytes[kname]
+    else:
+        ks = (2 if args.paged and nkern > 2 else
+              1 if (args.inplace or args.readonly) and nkern > 1 else 0)  # index of the step kernel
+        kname = STEP_KERNEL[path]
+        if args.readonly and path == "generic":
+            kname = "generic_attend_kernel"
     fused_ms = kern_ms[ks]
     achieved = nbytes["fused_kernel"] / (fused_ms * 1e-3) / 1e9
-    kname = STEP_KERNEL[path]
-    if args.readonly and path == "generic":
-        kname = "generic_attend_kernel"
     traffic = kernel_traffic(mode_key(args), kname, nbytes["fused_kernel"])
 
     # ---- end to end through the public API: pinned host in, pinned host out
     e2e = None
-    if args.readonly or args.paged:
+    if args.readonly or args.paged or args.backward:
         e2e = None  # these faces have no host-buffer leg here
     elif not args.no_e2e:
         e2e = (measure_e2e_inplace(kvc, x, dev, max(3, min(args.steps, 10)), nbytes["total"],
@@ -483,14 +563,17 @@ def run_ours(args, spec, world, rank, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xc = cpu_inputs(spec, seed=1)
-        dt, rows, threads = oracle_sample(spec, xc, args.cpu_budget)
-        sample_bytes = (algorithmic_bytes_readonly(spec, lengths_h[:rows], counts_h[:rows])
+        dt, rows, threads = oracle_sample(spec, xc, args.cpu_budget, args.backward)
+        sample_bytes = (algorithmic_bytes_backward(spec, lengths_h[:rows], counts_h[:rows])
+                        if args.backward else
+                        algorithmic_bytes_readonly(spec, lengths_h[:rows], counts_h[:rows])
                         if args.readonly else
                         algorithmic_bytes_inplace(spec, lengths_h[:rows], counts_h[:rows])
                         if (args.inplace or args.paged) else algorithmic_bytes(spec, rows))
         cpu = {"value": round(sample_bytes["total"] / dt / 1e9, 4),
                "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"first {rows} of {spec.B} batch rows of {args.workload}, one step"
+               "sample": f"first {rows} of {spec.B} batch rows of {args.workload}, one "
+                         + ("backward" if args.backward else "step")
                          + (" (the oracle's step: the same attention plus the cache copy)"
                             if args.readonly else "")}
 
@@ -518,8 +601,9 @@ def run_ours(args, spec, world, rank, local):
         "gpu_launches": nkern * args.steps,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
-    names = (PATH_KERNELS_READONLY if args.readonly else PATH_KERNELS_PAGED if args.paged else
-             PATH_KERNELS_INPLACE if args.inplace else PATH_KERNELS)[path]
+    names = (names_b if args.backward else
+             (PATH_KERNELS_READONLY if args.readonly else PATH_KERNELS_PAGED if args.paged else
+              PATH_KERNELS_INPLACE if args.inplace else PATH_KERNELS)[path])
     for k in range(nkern):
         if k != ks:
             line["kernels"][names[k]] = {"ms": round(kern_ms[k], 4)}
@@ -533,7 +617,10 @@ def run_ours(args, spec, world, rank, local):
         line["config"]["mode"] = ("read-only re-attention: packed queries (the step's valid "
                                   "rows) over the cached prefix through a slot permutation; "
                                   "context only, no attention rows, cache not written")
-    if nkern > 2:
+    if args.backward:
+        line["config"]["mode"] = ("backward: gradients of all four outputs given (seeded), "
+                                  "the statistics pass over the inputs, then the gradients")
+    if nkern > 2 and not args.backward:
         fin_ms = kern_ms[-1] + kern_ms[-2]
         line["kernels"]["merge + unpack" if args.readonly else "finalize (merge + rows)"] = {
             "ms": round(fin_ms, 4),
@@ -634,6 +721,8 @@ def main():
                     help="time kvc_step_paged on pools of BLOCK_SIZE-slot blocks")
     ap.add_argument("--readonly", action="store_true",
                     help="time kvc_attend_cache (read-only re-attention over the cache)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time kvc_step_backward (gradients of the step's outputs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -363,6 +363,20 @@ KVC_API int kvc_step_static(const kvc_dims *dims, const void *query, const void 
  * workspace or each other (KVC_E_ALIAS). Work is enqueued on `stream`.
  */
 KVC_API size_t kvc_backward_workspace_bytes(const kvc_dims *dims);
+/* kvc_step_backward with events recorded on `stream`: one before the first
+ * kernel and one after each (with query rows: the statistics pass's step
+ * kernel and merge, then bwd_rowdot, bwd_kv, the tail copy and bwd_dq; the
+ * rest, if any, at the end). */
+KVC_API int kvc_step_backward_timed(const kvc_dims *dims, const void *query, const void *new_key,
+                                    const void *new_value, const void *key_cache,
+                                    const void *value_cache, const int64_t *lengths,
+                                    const uint8_t *append_mask, double scale,
+                                    const void *d_key_cache_out, const void *d_value_cache_out,
+                                    const void *d_attention, const void *d_context,
+                                    void *d_query, void *d_new_key, void *d_new_value,
+                                    void *d_key_cache, void *d_value_cache, void *workspace,
+                                    size_t workspace_bytes, int32_t *dev_status, void *stream,
+                                    void *const *events, int n_events);
 KVC_API int kvc_step_backward(const kvc_dims *dims, const void *query, const void *new_key,
                               const void *new_value, const void *key_cache,
                               const void *value_cache, const int64_t *lengths,

@@ -1073,7 +1073,7 @@ namespace {
 // fp32 context rows, the per-row sums D, the step's context in the dtype and
 // its lengths (both unused scratch the step needs as arguments).
 struct BwdLayout {
-    size_t step = 0, ctx_f32 = 0, drow = 0, ctx_t = 0, lengths = 0, total = 0;
+    size_t step = 0, ctx_f32 = 0, drow = 0, dq = 0, ctx_t = 0, lengths = 0, total = 0;
 };
 bool bwd_layout(const kvc_dims& d, BwdLayout* L) {
     const size_t step = kvc_workspace_bytes(&d);
@@ -1085,6 +1085,8 @@ bool bwd_layout(const kvc_dims& d, BwdLayout* L) {
     off = align_up(off + rows * d.Dv * 4, 256);
     L->drow = static_cast<size_t>(off);
     off = align_up(off + rows * 4, 256);
+    L->dq = static_cast<size_t>(off);
+    off = align_up(off + rows * d.D * 4, 256);
     L->ctx_t = static_cast<size_t>(off);
     off = align_up(off + rows * d.Dv * es, 256);
     L->lengths = static_cast<size_t>(off);
@@ -1102,14 +1104,16 @@ size_t kvc_backward_workspace_bytes(const kvc_dims* dims) {
     return bwd_layout(*dims, &L) ? L.total : 0;
 }
 
-int kvc_step_backward(const kvc_dims* dims, const void* query, const void* new_key,
-                      const void* new_value, const void* key_cache, const void* value_cache,
-                      const int64_t* lengths, const uint8_t* append_mask, double scale,
-                      const void* d_key_cache_out, const void* d_value_cache_out,
-                      const void* d_attention, const void* d_context, void* d_query,
-                      void* d_new_key, void* d_new_value, void* d_key_cache, void* d_value_cache,
-                      void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
-    using namespace kvc;
+namespace kvc {
+namespace {
+int backward_impl(const kvc_dims* dims, const void* query, const void* new_key,
+                  const void* new_value, const void* key_cache, const void* value_cache,
+                  const int64_t* lengths, const uint8_t* append_mask, double scale,
+                  const void* d_key_cache_out, const void* d_value_cache_out,
+                  const void* d_attention, const void* d_context, void* d_query, void* d_new_key,
+                  void* d_new_value, void* d_key_cache, void* d_value_cache, void* workspace,
+                  size_t workspace_bytes, int32_t* dev_status, void* stream,
+                  void* const* events, int n_events) {
     int rc = check_dims(dims);
     if (rc != KVC_OK) return rc;
     const kvc_dims d = *dims;
@@ -1162,10 +1166,14 @@ int kvc_step_backward(const kvc_dims* dims, const void* query, const void* new_k
     mode.ctx_f32 = reinterpret_cast<float*>(ws + Lw.ctx_f32);
     StepParams p;
     mode.params_out = &p;
+    // the statistics pass records one event before its kernels and one after
+    // each (the step kernel and the merge, with query rows); the gradient
+    // kernels then record one each
+    const int stats_events = events ? std::min(n_events, hasq ? 3 : 1) : 0;
     rc = step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths, append_mask,
                    scale, const_cast<void*>(key_cache), const_cast<void*>(value_cache),
                    reinterpret_cast<int64_t*>(ws + Lw.lengths), nullptr, ws + Lw.ctx_t, ws,
-                   Lw.step, dev_status, stream, nullptr, 0, mode);
+                   Lw.step, dev_status, stream, events, stats_events, mode);
     if (rc != KVC_OK) return rc;
     // 2. the gradients
     BwdParams bp;
@@ -1181,12 +1189,73 @@ int kvc_step_backward(const kvc_dims* dims, const void* query, const void* new_k
     bp.d_key_cache = d_key_cache;
     bp.d_value_cache = d_value_cache;
     bp.drow = reinterpret_cast<float*>(ws + Lw.drow);
+    bp.dq_acc = reinterpret_cast<float*>(ws + Lw.dq);
+    {  // the unit's rows fit the bwd_kv_kernel's shared memory?
+        DeviceInfo dev;
+        const int64_t R = (d.Hq / d.Hk) * d.Q;
+        const int64_t need = (3 * R + R * (2 * d.D + d.Dv)) * 4;
+        bp.stage_rows = device_info(&dev) == cudaSuccess && need <= dev.smem_optin ? 1 : 0;
+        // the few-rows kernel (D = Dv in {64, 128, 256}, rows 16-byte aligned):
+        // q and dcontext [NR][D], per warp a and dattention [32][NR] and
+        // query-gradient sums [NR][D]
+        const int64_t NR = R <= 4 ? 4 : R <= 8 ? 8 : 16;
+        const int64_t rows_smem = (NR * 2 * d.D + 8 * (2 * 32 * NR + NR * d.D)) * 4;
+        const bool widths = d.D == d.Dv && (d.D == 64 || d.D == 128 || d.D == 256);
+        const bool aligned = aligned16(query) && aligned16(new_key) && aligned16(new_value) &&
+                             aligned16(key_cache) && aligned16(value_cache) &&
+                             aligned16(d_key_cache_out) && aligned16(d_value_cache_out) &&
+                             aligned16(d_key_cache) && aligned16(d_value_cache) &&
+                             aligned16(d_new_key) && aligned16(d_new_value);
+        bp.rows_smem = (R <= 16 && widths && aligned && rows_smem <= dev.smem_optin)
+                           ? static_cast<int>(rows_smem) : 0;
+    }
     bp.scale = static_cast<float>(scale);
-    bp.slots_per_block = 64;
+    bp.slots_per_block = 256;
     const bool words16 = (d.D * es) % 16 == 0 && (d.Dv * es) % 16 == 0 &&
                          aligned16(d_key_cache) && aligned16(d_value_cache) &&
                          aligned16(d_key_cache_out) && aligned16(d_value_cache_out);
-    const cudaError_t e = launch_backward(bp, d.dtype, words16, static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int recorded = stats_events;
+    auto after = [&]() -> cudaError_t {
+        if (events && recorded < n_events)
+            return cudaEventRecord(static_cast<cudaEvent_t>(events[recorded++]), st);
+        return cudaSuccess;
+    };
+    cudaError_t e = launch_backward(bp, d.dtype, words16, st, after);
+    while (e == cudaSuccess && events && recorded < n_events) e = after();
     return e == cudaSuccess ? KVC_OK : KVC_E_CUDA;
+}
+}  // namespace
+}  // namespace kvc
+
+int kvc_step_backward(const kvc_dims* dims, const void* query, const void* new_key,
+                      const void* new_value, const void* key_cache, const void* value_cache,
+                      const int64_t* lengths, const uint8_t* append_mask, double scale,
+                      const void* d_key_cache_out, const void* d_value_cache_out,
+                      const void* d_attention, const void* d_context, void* d_query,
+                      void* d_new_key, void* d_new_value, void* d_key_cache, void* d_value_cache,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    return kvc::backward_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
+                              append_mask, scale, d_key_cache_out, d_value_cache_out, d_attention,
+                              d_context, d_query, d_new_key, d_new_value, d_key_cache,
+                              d_value_cache, workspace, workspace_bytes, dev_status, stream,
+                              nullptr, 0);
+}
+
+int kvc_step_backward_timed(const kvc_dims* dims, const void* query, const void* new_key,
+                            const void* new_value, const void* key_cache,
+                            const void* value_cache, const int64_t* lengths,
+                            const uint8_t* append_mask, double scale,
+                            const void* d_key_cache_out, const void* d_value_cache_out,
+                            const void* d_attention, const void* d_context, void* d_query,
+                            void* d_new_key, void* d_new_value, void* d_key_cache,
+                            void* d_value_cache, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, void* stream, void* const* events,
+                            int n_events) {
+    return kvc::backward_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
+                              append_mask, scale, d_key_cache_out, d_value_cache_out, d_attention,
+                              d_context, d_query, d_new_key, d_new_value, d_key_cache,
+                              d_value_cache, workspace, workspace_bytes, dev_status, stream,
+                              events, n_events);
 }
 

@@ -22,15 +22,19 @@
 //   bwd_rowdot_kernel  one warp per query row: D from the scores, dattention,
 //                      dcontext and the context.
 //   bwd_kv_kernel      one warp per cache slot below the new length of a unit:
-//                      a_j and ds_j for each of the unit's query rows (ds_j
-//                      replaces the score in the workspace), dK'_j and dV'_j,
-//                      plus the returned caches' own gradient, written to the
-//                      cache gradient or the new-row gradient.
+//                      a_j and ds_j for each of the unit's query rows, dK'_j
+//                      and dV'_j plus the returned caches' own gradient,
+//                      written to the cache gradient or the new-row gradient;
+//                      ds_j K'_j summed per row over the block's slots in
+//                      shared memory, then into an fp32 accumulator.
 //   bwd_copy_kernel    the slots from the new length on: their gradient is the
 //                      returned caches' gradient, 16 bytes at a time.
-//   bwd_dq_kernel      one warp per query row: dq = scale sum_j ds_j K'_j.
+//   bwd_dq_kernel      dq = scale * the accumulated sum, in the dtype.
 //
 // All sums are fp32; the gradients are written in the inputs' dtype.
+#include <functional>
+#include <type_traits>
+
 #include "kvc_internal.cuh"
 #include "kvc_launch.h"
 
@@ -79,16 +83,23 @@ __global__ void __launch_bounds__(kBwdWarps * 32) bwd_rowdot_kernel(const BwdPar
     if (lane == 0) bp.drow[row] = acc;
 }
 
-// One warp per slot j < N_b of unit u: the attention gradients of the slot
-// and the returned caches' own gradient, to d_key_cache / d_new_key.
+// One block per slab of slots_per_block slots below N_b of unit u, one warp
+// per slot at a time: the attention gradients of the slot and the returned
+// caches' own gradient, to d_key_cache / d_new_key; each row's query
+// gradient summed over the slab in shared memory and added once to the fp32
+// accumulator. The unit's query and context-gradient rows and the rows'
+// statistics are staged in shared memory (fp32) when they fit
+// (bp.stage_rows), else read from global memory.
 template <typename T>
 __global__ void __launch_bounds__(kBwdWarps * 32) bwd_kv_kernel(const BwdParams bp) {
+    extern __shared__ __align__(16) float sm[];
     const StepParams& p = bp.p;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t u = blockIdx.y, b = u / p.Hk, kv = u - b * p.Hk;
     const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
     const int64_t L = ra.L, n = ra.n, N = L + n;
     const int D = static_cast<int>(p.D), Dv = static_cast<int>(p.Dv);
+    const int R = static_cast<int>(p.R);
     const float scale = bp.scale;
     // new-row gradients of the rows t >= n (nothing reaches them): zero
     if (blockIdx.x == 0) {
@@ -99,47 +110,81 @@ __global__ void __launch_bounds__(kBwdWarps * 32) bwd_kv_kernel(const BwdParams 
     }
     const int64_t jend = ra.flags ? 0 : N;  // slots with attention or a new row
     const int64_t jb = static_cast<int64_t>(blockIdx.x) * bp.slots_per_block;
+    if (jb >= jend) return;  // whole block: uniform
+    const int64_t row0 = (b * p.Hq + kv * p.G) * p.Q;  // the unit's rows are row0 + r
+    // shared memory: per row mx, inv_l, D (3 R floats), then staged q, dcontext
+    // and the slab's query-gradient sums (R (D + Dv + D) floats)
+    float* s_mx = sm;
+    float* s_il = sm + R;
+    float* s_dr = sm + 2 * R;
+    float* s_q = sm + 3 * R;
+    float* s_dc = s_q + R * D;
+    float* s_dq = s_dc + R * Dv;
+    const bool staged = bp.stage_rows;
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+        const RowStat rs = p.rowstat[row0 + r];
+        s_mx[r] = rs.mx;
+        s_il[r] = rs.inv_l;
+        s_dr[r] = bp.drow[row0 + r];
+    }
+    if (staged) {
+        for (int i = threadIdx.x; i < R * D; i += blockDim.x) {
+            s_q[i] = Storage<T>::to_float(static_cast<const T*>(p.query)[row0 * D + i]);
+            s_dq[i] = 0.f;
+        }
+        for (int i = threadIdx.x; i < R * Dv; i += blockDim.x)
+            s_dc[i] = bp.d_context ? ld<T>(bp.d_context, row0 * Dv + i) : 0.f;
+    }
+    __syncthreads();
     for (int64_t j = jb + w; j < min(jb + bp.slots_per_block, jend); j += kBwdWarps) {
         const bool is_new = j >= L;
         const T* krow = is_new ? static_cast<const T*>(p.new_key) + (u * p.Q + (j - L)) * D
                                : static_cast<const T*>(p.key_cache) + (u * p.M + j) * D;
         const T* vrow = is_new ? static_cast<const T*>(p.new_value) + (u * p.Q + (j - L)) * Dv
                                : static_cast<const T*>(p.value_cache) + (u * p.M + j) * Dv;
-        float vj[kMaxLaneElems], dk[kMaxLaneElems], dv[kMaxLaneElems];
+        float kj[kMaxLaneElems], vj[kMaxLaneElems], dk[kMaxLaneElems], dv[kMaxLaneElems];
 #pragma unroll
         for (int i = 0; i < kMaxLaneElems; ++i) {
             const int e = lane + 32 * i;
+            kj[i] = e < D ? Storage<T>::to_float(krow[e]) : 0.f;
             vj[i] = e < Dv ? Storage<T>::to_float(vrow[e]) : 0.f;
             dk[i] = 0.f;
             dv[i] = 0.f;
         }
         // every query row of the unit whose causal limit admits slot j
-        for (int64_t r = 0; r < p.R; ++r) {
+        for (int r = 0; r < R; ++r) {
             const int64_t t = r % p.Q;
             if (t >= n || j > L + t) continue;
-            const int64_t h = kv * p.G + r / p.Q, row = (b * p.Hq + h) * p.Q + t;
-            const RowStat rs = p.rowstat[row];
-            float* sj = p.scores + row * p.M + j;
-            const float a = fast_exp2(*sj - rs.mx) * rs.inv_l;
+            const int64_t row = row0 + r;
+            const float a = fast_exp2(p.scores[row * p.M + j] - s_mx[r]) * s_il[r];
+            const float* qr = staged ? s_q + r * D : nullptr;
+            const float* dcr = staged ? s_dc + r * Dv : nullptr;
+            float dcv[kMaxLaneElems];
             float g = 0.f;
-            if (bp.d_context) {
-#pragma unroll
-                for (int i = 0; i < kMaxLaneElems; ++i) {
-                    const int e = lane + 32 * i;
-                    if (e < Dv) g += ld<T>(bp.d_context, row * Dv + e) * vj[i];
-                }
-                g = bwd_warp_sum(g);
-            }
-            if (bp.d_attention) g += ld<T>(bp.d_attention, row * p.M + j);
-            const float ds = a * (g - bp.drow[row]);
-            __syncwarp();
-            if (lane == 0) *sj = ds;  // kept for the query gradient
-            const T* qrow = static_cast<const T*>(p.query) + row * D;
 #pragma unroll
             for (int i = 0; i < kMaxLaneElems; ++i) {
                 const int e = lane + 32 * i;
-                if (e < D) dk[i] += scale * ds * Storage<T>::to_float(qrow[e]);
-                if (bp.d_context && e < Dv) dv[i] += a * ld<T>(bp.d_context, row * Dv + e);
+                dcv[i] = 0.f;
+                if (e < Dv && bp.d_context)
+                    dcv[i] = staged ? dcr[e] : ld<T>(bp.d_context, row * Dv + e);
+                g += dcv[i] * vj[i];
+            }
+            if (bp.d_context) g = bwd_warp_sum(g);
+            if (bp.d_attention) g += ld<T>(bp.d_attention, row * p.M + j);
+            const float ds = a * (g - s_dr[r]);
+#pragma unroll
+            for (int i = 0; i < kMaxLaneElems; ++i) {
+                const int e = lane + 32 * i;
+                if (e < D) {
+                    const float qe = staged ? qr[e]
+                                            : Storage<T>::to_float(static_cast<const T*>(p.query)[row * D + e]);
+                    dk[i] += scale * ds * qe;
+                    if (staged)
+                        atomicAdd(&s_dq[r * D + e], ds * kj[i]);
+                    else
+                        atomicAdd(&bp.dq_acc[row * D + e], ds * kj[i]);
+                }
+                if (e < Dv) dv[i] += a * dcv[i];
             }
         }
         // plus the returned caches' own gradient at slot j
@@ -165,6 +210,259 @@ __global__ void __launch_bounds__(kBwdWarps * 32) bwd_kv_kernel(const BwdParams 
                         Storage<T>::from_float(0.f);
             }
         }
+    }
+    if (staged) {  // the slab's query-gradient sums into the fp32 accumulator
+        __syncthreads();
+        for (int i = threadIdx.x; i < R * D; i += blockDim.x)
+            if (s_dq[i] != 0.f) atomicAdd(&bp.dq_acc[row0 * D + i], s_dq[i]);
+    }
+}
+
+// Units of at most NR (4, 8, 16) query rows with D = Dv = 32 V: the same work
+// as bwd_kv_kernel, organised for few rows. Lane l owns elements
+// [V l, V l + V) of every row, moved as one vector per row. Each warp takes 32
+// consecutive slots: first one slot per lane, loading the rows' scores and
+// attention gradients of its slot together (coalesced along the slots) into
+// shared memory as a_rj and dattention_rj; then slot by slot (the next slot's
+// rows loading while one is worked), the rows' dcontext . V'_j reduced
+// together by a reduce-scatter butterfly, and ds_rj K'_j summed per row in
+// the warp's own shared-memory buffer (no atomics); at the end the warps'
+// buffers are summed into the fp32 accumulator.
+template <int NR>
+struct Log2Rows;
+template <>
+struct Log2Rows<4> { static constexpr int v = 2; };
+template <>
+struct Log2Rows<8> { static constexpr int v = 3; };
+template <>
+struct Log2Rows<16> { static constexpr int v = 4; };
+
+// V consecutive elements of T (V even), as raw 32-bit words and as floats.
+template <typename T, int V>
+struct LaneVec {
+    static constexpr int kBytes = V * static_cast<int>(sizeof(T));
+    static constexpr int kWords = kBytes / 4;
+    __device__ static void load(const T* p, uint32_t (&w)[kWords]) {
+        if constexpr (kBytes % 16 == 0) {
+#pragma unroll
+            for (int k = 0; k < kBytes / 16; ++k) {
+                const uint4 v = reinterpret_cast<const uint4*>(p)[k];
+                w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+            }
+        } else if constexpr (kBytes % 8 == 0) {
+#pragma unroll
+            for (int k = 0; k < kBytes / 8; ++k) {
+                const uint2 v = reinterpret_cast<const uint2*>(p)[k];
+                w[2 * k] = v.x; w[2 * k + 1] = v.y;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < kWords; ++k) w[k] = reinterpret_cast<const uint32_t*>(p)[k];
+        }
+    }
+    __device__ static void store(T* p, const uint32_t (&w)[kWords]) {
+        if constexpr (kBytes % 16 == 0) {
+#pragma unroll
+            for (int k = 0; k < kBytes / 16; ++k)
+                reinterpret_cast<uint4*>(p)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+        } else if constexpr (kBytes % 8 == 0) {
+#pragma unroll
+            for (int k = 0; k < kBytes / 8; ++k)
+                reinterpret_cast<uint2*>(p)[k] = make_uint2(w[2 * k], w[2 * k + 1]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < kWords; ++k) reinterpret_cast<uint32_t*>(p)[k] = w[k];
+        }
+    }
+    __device__ static void to_f(const uint32_t (&w)[kWords], float (&f)[V]) {
+        if constexpr (sizeof(T) == 4) {
+#pragma unroll
+            for (int i = 0; i < V; ++i) f[i] = __uint_as_float(w[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; i += 2) {
+                const uint32_t x = w[i / 2];
+                const uint16_t lo = static_cast<uint16_t>(x & 0xffffu), hi = static_cast<uint16_t>(x >> 16);
+                f[i] = Storage<T>::to_float(*reinterpret_cast<const T*>(&lo));
+                f[i + 1] = Storage<T>::to_float(*reinterpret_cast<const T*>(&hi));
+            }
+        }
+    }
+    __device__ static void from_f(const float (&f)[V], uint32_t (&w)[kWords]) {
+        if constexpr (sizeof(T) == 4) {
+#pragma unroll
+            for (int i = 0; i < V; ++i) w[i] = __float_as_uint(f[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; i += 2) {
+                const T a = Storage<T>::from_float(f[i]), b = Storage<T>::from_float(f[i + 1]);
+                w[i / 2] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&a)) |
+                           (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&b)) << 16);
+            }
+        }
+    }
+};
+
+template <typename T, int NR, int V>
+__global__ void __launch_bounds__(kBwdWarps * 32) bwd_kv_rows_kernel(const BwdParams bp) {
+    using LV = LaneVec<T, V>;
+    constexpr int W = 32 * V;  // D = Dv
+    constexpr int KW = LV::kWords;
+    extern __shared__ __align__(16) float sm[];
+    const StepParams& p = bp.p;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t u = blockIdx.y, b = u / p.Hk, kv = u - b * p.Hk;
+    const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
+    const int64_t L = ra.L, n = ra.n, N = L + n;
+    const int R = static_cast<int>(p.R);
+    const float scale = bp.scale;
+    if (blockIdx.x == 0) {  // new-row gradients of the rows t >= n: zero
+        for (int64_t i = threadIdx.x; i < (p.Q - n) * W; i += blockDim.x) {
+            static_cast<T*>(bp.d_new_key)[(u * p.Q + n) * W + i] = Storage<T>::from_float(0.f);
+            static_cast<T*>(bp.d_new_value)[(u * p.Q + n) * W + i] = Storage<T>::from_float(0.f);
+        }
+    }
+    const int64_t jend = ra.flags ? 0 : N;
+    const int64_t jb = static_cast<int64_t>(blockIdx.x) * (kBwdWarps * 32);
+    if (jb >= jend) return;  // whole block
+    const int64_t row0 = (b * p.Hq + kv * p.G) * p.Q;
+    // shared memory (floats): q [NR][W], dcontext [NR][W], per warp: a [32][NR],
+    // dattention [32][NR], query-gradient sums [NR][W]
+    constexpr int kWarpFloats = 2 * 32 * NR + NR * W;
+    float* s_q = sm;
+    float* s_dc = s_q + NR * W;
+    float* s_a = s_dc + NR * W + w * kWarpFloats;
+    float* s_da = s_a + 32 * NR;
+    float* s_dq = s_da + 32 * NR;
+    for (int i = threadIdx.x; i < NR * W; i += blockDim.x) {
+        s_q[i] = i < R * W ? Storage<T>::to_float(static_cast<const T*>(p.query)[row0 * W + i]) : 0.f;
+        s_dc[i] = (i < R * W && bp.d_context) ? ld<T>(bp.d_context, row0 * W + i) : 0.f;
+    }
+    for (int i = lane; i < NR * W; i += 32) s_dq[i] = 0.f;
+    int lim[NR];
+    float mx[NR], il[NR], dr[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        const int64_t t = r % p.Q;
+        const bool ok = r < R && t < n;
+        lim[r] = ok ? static_cast<int>(L + t) : -1;
+        const RowStat rs = ok ? p.rowstat[row0 + r] : RowStat{0.f, 0.f, -1, 0};
+        mx[r] = rs.mx;
+        il[r] = rs.inv_l;
+        dr[r] = ok ? bp.drow[row0 + r] : 0.f;
+    }
+    __syncthreads();
+    const int64_t j0 = jb + w * 32;
+    {  // phase 1: one slot per lane
+        const int64_t j = j0 + lane;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const bool ok = j < jend && j <= lim[r];
+            const int64_t idx = (row0 + r) * p.M + j;
+            s_a[lane * NR + r] = ok ? fast_exp2(p.scores[idx] - mx[r]) * il[r] : 0.f;
+            s_da[lane * NR + r] = (ok && bp.d_attention) ? ld<T>(bp.d_attention, idx) : 0.f;
+        }
+    }
+    __syncwarp();
+    // phase 2: slot by slot, lane l on elements [V l, V l + V) of each row
+    const int64_t left = jend - j0;
+    const int nj = left <= 0 ? 0 : left >= 32 ? 32 : static_cast<int>(left);
+    const int e0 = V * lane;
+    const T* nk = static_cast<const T*>(p.new_key);
+    const T* nv = static_cast<const T*>(p.new_value);
+    const T* kc = static_cast<const T*>(p.key_cache);
+    const T* vc = static_cast<const T*>(p.value_cache);
+    const T* gko = static_cast<const T*>(bp.d_key_out);
+    const T* gvo = static_cast<const T*>(bp.d_value_out);
+    // the rows of slot j this lane reads: K'_j, V'_j and the returned caches' gradient
+    auto fetch = [&](int64_t j, uint32_t (&k)[KW], uint32_t (&v)[KW], uint32_t (&gk)[KW],
+                     uint32_t (&gv)[KW]) {
+        const bool nw = j >= L;
+        const int64_t cr = (u * p.M + j) * W + e0;
+        LV::load(nw ? nk + (u * p.Q + (j - L)) * W + e0 : kc + cr, k);
+        LV::load(nw ? nv + (u * p.Q + (j - L)) * W + e0 : vc + cr, v);
+#pragma unroll
+        for (int i = 0; i < KW; ++i) gk[i] = gv[i] = 0u;
+        if (gko) LV::load(gko + cr, gk);
+        if (gvo) LV::load(gvo + cr, gv);
+    };
+    uint32_t nk_w[KW], nv_w[KW], ngk_w[KW], ngv_w[KW];
+    if (nj > 0) fetch(j0, nk_w, nv_w, ngk_w, ngv_w);
+    for (int jj = 0; jj < nj; ++jj) {
+        const int64_t j = j0 + jj;
+        float kj[V], vj[V], gk[V], gv[V];
+        LV::to_f(nk_w, kj);
+        LV::to_f(nv_w, vj);
+        LV::to_f(ngk_w, gk);
+        LV::to_f(ngv_w, gv);
+        if (jj + 1 < nj) fetch(j + 1, nk_w, nv_w, ngk_w, ngv_w);
+        // dcontext_r . V'_j for every row, reduced together, then broadcast
+        float a2[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            float g = 0.f;
+#pragma unroll
+            for (int i = 0; i < V; ++i) g += s_dc[r * W + e0 + i] * vj[i];
+            a2[r] = g;
+        }
+        {
+            int o = 16;
+#pragma unroll
+            for (int h = NR / 2; h >= 1; h /= 2, o /= 2) {
+                const bool up = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < h; ++i) {
+                    const float keep = up ? a2[i + h] : a2[i];
+                    const float send = up ? a2[i] : a2[i + h];
+                    a2[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+#pragma unroll
+            for (; o >= 1; o /= 2) a2[0] += __shfl_xor_sync(0xffffffffu, a2[0], o);
+        }
+        float ds[NR], av[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const float gr = __shfl_sync(0xffffffffu, a2[0], r << (5 - Log2Rows<NR>::v));
+            av[r] = s_a[jj * NR + r];
+            ds[r] = av[r] * (s_da[jj * NR + r] + gr - dr[r]);
+        }
+        float dk[V], dv[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            float sk = 0.f, sv = 0.f;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                sk += ds[r] * s_q[r * W + e0 + i];
+                sv += av[r] * s_dc[r * W + e0 + i];
+                s_dq[r * W + e0 + i] += ds[r] * kj[i];
+            }
+            dk[i] = scale * sk + gk[i];
+            dv[i] = sv + gv[i];
+        }
+        uint32_t ok_w[KW], ov_w[KW];
+        LV::from_f(dk, ok_w);
+        LV::from_f(dv, ov_w);
+        if (j >= L) {  // a new row's slot: its gradient goes to the new row, the cache slot gets none
+            LV::store(static_cast<T*>(bp.d_new_key) + (u * p.Q + (j - L)) * W + e0, ok_w);
+            LV::store(static_cast<T*>(bp.d_new_value) + (u * p.Q + (j - L)) * W + e0, ov_w);
+            uint32_t z[KW];
+#pragma unroll
+            for (int i = 0; i < KW; ++i) z[i] = 0u;
+            LV::store(static_cast<T*>(bp.d_key_cache) + (u * p.M + j) * W + e0, z);
+            LV::store(static_cast<T*>(bp.d_value_cache) + (u * p.M + j) * W + e0, z);
+        } else {
+            LV::store(static_cast<T*>(bp.d_key_cache) + (u * p.M + j) * W + e0, ok_w);
+            LV::store(static_cast<T*>(bp.d_value_cache) + (u * p.M + j) * W + e0, ov_w);
+        }
+    }
+    // the warps' query-gradient sums into the fp32 accumulator
+    __syncthreads();
+    const float* dq0 = s_dc + NR * W + 2 * 32 * NR;  // warp 0's buffer
+    for (int i = threadIdx.x; i < R * W; i += blockDim.x) {
+        float acc = 0.f;
+        for (int ww = 0; ww < kBwdWarps; ++ww) acc += dq0[ww * kWarpFloats + i];
+        if (acc != 0.f) atomicAdd(&bp.dq_acc[row0 * W + i], acc);
     }
 }
 
@@ -209,56 +507,66 @@ __global__ void __launch_bounds__(256) bwd_copy_elems_kernel(const BwdParams bp)
     }
 }
 
-// dq = scale sum_j ds_j K'_j over the row's allowed slots; zero for invalid rows.
+// d_query = scale * the summed ds_j K'_j of the row (zero for invalid rows).
 template <typename T>
-__global__ void __launch_bounds__(kBwdWarps * 32) bwd_dq_kernel(const BwdParams bp) {
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdParams bp) {
     const StepParams& p = bp.p;
-    const int lane = threadIdx.x & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * kBwdWarps + (threadIdx.x >> 5);
-    if (row >= p.B * p.Hq * p.Q) return;
-    const int64_t t = row % p.Q, b = row / (p.Hq * p.Q), h = (row / p.Q) % p.Hq;
-    const int64_t u = b * p.Hk + h / p.G;
-    const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
-    const int D = static_cast<int>(p.D);
-    T* dq = static_cast<T*>(bp.d_query) + row * D;
-    float acc[kMaxLaneElems];
-#pragma unroll
-    for (int i = 0; i < kMaxLaneElems; ++i) acc[i] = 0.f;
-    if (t < ra.n) {
-        const float* ds = p.scores + row * p.M;
-        const int64_t L = ra.L;
-        for (int64_t j = 0; j <= L + t; ++j) {
-            const float w = ds[j];
-            const T* krow = j >= L ? static_cast<const T*>(p.new_key) + (u * p.Q + (j - L)) * D
-                                   : static_cast<const T*>(p.key_cache) + (u * p.M + j) * D;
-#pragma unroll
-            for (int i = 0; i < kMaxLaneElems; ++i) {
-                const int e = lane + 32 * i;
-                if (e < D) acc[i] += w * Storage<T>::to_float(krow[e]);
-            }
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxLaneElems; ++i) {
-        const int e = lane + 32 * i;
-        if (e < D) dq[e] = Storage<T>::from_float(bp.scale * acc[i]);
-    }
+    const int64_t total = p.B * p.Hq * p.Q * p.D;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        static_cast<T*>(bp.d_query)[i] = Storage<T>::from_float(bp.scale * bp.dq_acc[i]);
 }
 
 template <typename T>
-cudaError_t launch_t(const BwdParams& bp, bool words16, cudaStream_t stream) {
+cudaError_t launch_t(const BwdParams& bp, bool words16, cudaStream_t stream,
+                     const std::function<cudaError_t()>& after) {
     const StepParams& p = bp.p;
     const int64_t rows = p.B * p.Hq * p.Q, U = p.B * p.Hk;
     const unsigned row_blocks = static_cast<unsigned>((rows + kBwdWarps - 1) / kBwdWarps);
+    cudaError_t e = cudaSuccess;
     if (rows > 0) {
         bwd_rowdot_kernel<T><<<row_blocks, kBwdWarps * 32, 0, stream>>>(bp);
-        cudaError_t e = cudaGetLastError();
+        e = cudaGetLastError();
+        if (e == cudaSuccess) e = after();
         if (e != cudaSuccess) return e;
     }
-    const dim3 kv_grid(static_cast<unsigned>((p.M + bp.slots_per_block - 1) / bp.slots_per_block),
-                       static_cast<unsigned>(U));
-    bwd_kv_kernel<T><<<kv_grid, kBwdWarps * 32, 0, stream>>>(bp);
-    cudaError_t e = cudaGetLastError();
+    if (rows > 0) {
+        e = cudaMemsetAsync(bp.dq_acc, 0, static_cast<size_t>(rows * p.D) * sizeof(float), stream);
+        if (e != cudaSuccess) return e;
+    }
+    if (p.R <= 16 && bp.rows_smem > 0) {
+        const dim3 grid(static_cast<unsigned>((p.M + kBwdWarps * 32 - 1) / (kBwdWarps * 32)),
+                        static_cast<unsigned>(U));
+        auto launch = [&](auto kern) -> cudaError_t {
+            cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  bp.rows_smem);
+            if (e2 != cudaSuccess) return e2;
+            kern<<<grid, kBwdWarps * 32, bp.rows_smem, stream>>>(bp);
+            return cudaGetLastError();
+        };
+        auto by_rows = [&](auto v_tag) -> cudaError_t {
+            constexpr int V = decltype(v_tag)::value;
+            return p.R <= 4 ? launch(bwd_kv_rows_kernel<T, 4, V>)
+                            : p.R <= 8 ? launch(bwd_kv_rows_kernel<T, 8, V>)
+                                       : launch(bwd_kv_rows_kernel<T, 16, V>);
+        };
+        e = p.D == 64 ? by_rows(std::integral_constant<int, 2>())
+                      : p.D == 128 ? by_rows(std::integral_constant<int, 4>())
+                                   : by_rows(std::integral_constant<int, 8>());
+    } else {
+        const dim3 kv_grid(
+            static_cast<unsigned>((p.M + bp.slots_per_block - 1) / bp.slots_per_block),
+            static_cast<unsigned>(U));
+        const size_t kv_smem =
+            static_cast<size_t>(3 * p.R + (bp.stage_rows ? p.R * (2 * p.D + p.Dv) : 0)) *
+            sizeof(float);
+        e = cudaFuncSetAttribute(bwd_kv_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kv_smem));
+        if (e != cudaSuccess) return e;
+        bwd_kv_kernel<T><<<kv_grid, kBwdWarps * 32, kv_smem, stream>>>(bp);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = after();
     if (e != cudaSuccess) return e;
     const int64_t copy_blocks = (p.M + 255) / 256;
     const dim3 copy_grid(static_cast<unsigned>(copy_blocks < 64 ? copy_blocks : 64),
@@ -268,21 +576,26 @@ cudaError_t launch_t(const BwdParams& bp, bool words16, cudaStream_t stream) {
     else
         bwd_copy_elems_kernel<T><<<copy_grid, 256, 0, stream>>>(bp);
     e = cudaGetLastError();
+    if (e == cudaSuccess) e = after();
     if (e != cudaSuccess) return e;
     if (rows > 0) {
-        bwd_dq_kernel<T><<<row_blocks, kBwdWarps * 32, 0, stream>>>(bp);
+        const int64_t nq = rows * p.D;
+        const unsigned dq_blocks = static_cast<unsigned>(nq / 256 + 1 < 4096 ? nq / 256 + 1 : 4096);
+        bwd_dq_kernel<T><<<dq_blocks, 256, 0, stream>>>(bp);
         e = cudaGetLastError();
+        if (e == cudaSuccess) e = after();
     }
     return e;
 }
 
 }  // namespace
 
-cudaError_t launch_backward(const BwdParams& bp, int dtype, bool words16, cudaStream_t stream) {
+cudaError_t launch_backward(const BwdParams& bp, int dtype, bool words16, cudaStream_t stream,
+                            const std::function<cudaError_t()>& after) {
     switch (dtype) {
-        case KVC_F32: return launch_t<float>(bp, words16, stream);
-        case KVC_BF16: return launch_t<__nv_bfloat16>(bp, words16, stream);
-        default: return launch_t<__half>(bp, words16, stream);
+        case KVC_F32: return launch_t<float>(bp, words16, stream, after);
+        case KVC_BF16: return launch_t<__nv_bfloat16>(bp, words16, stream, after);
+        default: return launch_t<__half>(bp, words16, stream, after);
     }
 }
 

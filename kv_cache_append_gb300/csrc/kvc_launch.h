@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <functional>
+
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -63,12 +65,17 @@ struct BwdParams {
     void* d_key_cache;        // [B,Hk,M,D]
     void* d_value_cache;      // [B,Hk,M,Dv]
     float* drow;              // [B*Hq*Q] scratch: sum_j a_j g_j per query row
+    float* dq_acc;            // [B*Hq*Q*D] scratch: sum_j ds_j K'_j per query row
+    int stage_rows;           // 1: bwd_kv_kernel stages the unit's rows in shared memory
+    int rows_smem;            // > 0: bytes of bwd_kv_rows_kernel's shared memory (units of <= 16 rows)
     float scale;              // the scores' scale (natural-log domain)
     int64_t slots_per_block;  // cache slots per block of bwd_kv_kernel
 };
 // words16: cache rows are whole 16-byte words and the gradient buffers are
 // 16-byte aligned (the slots past the new length are copied 16 bytes at a time).
-cudaError_t launch_backward(const BwdParams& bp, int dtype, bool words16, cudaStream_t stream);
+// after() runs after each kernel launch (event recording for the timed face).
+cudaError_t launch_backward(const BwdParams& bp, int dtype, bool words16, cudaStream_t stream,
+                            const std::function<cudaError_t()>& after);
 
 // Merge of the partials: context rows and one RowStat per query row (kvc_finalize.cu).
 cudaError_t launch_finalize_merge(const StepParams& p, int dtype, cudaStream_t stream);

@@ -104,6 +104,9 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kvc_step_backward.restype = i32
             lib.kvc_step_backward.argtypes = ([dp] + [vp] * 7 + [ctypes.c_double] + [vp] * 9 +
                                               [vp, sz, vp, vp])
+            lib.kvc_step_backward_timed.restype = i32
+            lib.kvc_step_backward_timed.argtypes = (lib.kvc_step_backward.argtypes +
+                                                    [ctypes.POINTER(vp), i32])
             lib.kvc_selftest_wait_timeout.restype = i32
             lib.kvc_selftest_wait_timeout.argtypes = [vp, i64, vp]
             lib.kvc_status_string.restype = ctypes.c_char_p
@@ -353,7 +356,7 @@ def backward_workspace_bytes(dims: Dims) -> int:
 def step_backward_into(dims: Dims, query, new_key, new_value, key_cache, value_cache, lengths,
                        append_mask, scale: float, grads: dict, out: dict,
                        workspace: torch.Tensor, status: Optional[torch.Tensor] = None,
-                       stream: Optional[int] = None) -> None:
+                       stream: Optional[int] = None, events: Optional[Sequence] = None) -> None:
     """Enqueue one kvc_step_backward (no checks beyond libkvc's). grads holds
     the gradients reaching "key_cache", "value_cache", "attention" and
     "context" (each a contiguous tensor of the inputs' dtype, or None for
@@ -362,12 +365,16 @@ def step_backward_into(dims: Dims, query, new_key, new_value, key_cache, value_c
     lib = library()
     if stream is None:
         stream = torch.cuda.current_stream(query.device).cuda_stream
-    rc = lib.kvc_step_backward(
-        ctypes.byref(dims), _p(query), _p(new_key), _p(new_value), _p(key_cache),
-        _p(value_cache), _p(lengths), _p(append_mask), ctypes.c_double(scale),
-        *(_p(grads.get(k)) for k in ("key_cache", "value_cache", "attention", "context")),
-        *(_p(out[k]) for k in ("query", "new_key", "new_value", "key_cache", "value_cache")),
-        _p(workspace), workspace.numel(), _p(status), ctypes.c_void_p(stream))
+    args = [ctypes.byref(dims), _p(query), _p(new_key), _p(new_value), _p(key_cache),
+            _p(value_cache), _p(lengths), _p(append_mask), ctypes.c_double(scale),
+            *(_p(grads.get(k)) for k in ("key_cache", "value_cache", "attention", "context")),
+            *(_p(out[k]) for k in ("query", "new_key", "new_value", "key_cache", "value_cache")),
+            _p(workspace), workspace.numel(), _p(status), ctypes.c_void_p(stream)]
+    if events:
+        handles = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+        rc = lib.kvc_step_backward_timed(*args, handles, len(events))
+    else:
+        rc = lib.kvc_step_backward(*args)
     if rc != KVC_OK:
         raise KvcError(rc, status_string(rc))
 

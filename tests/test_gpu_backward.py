@@ -80,6 +80,13 @@ CASES = {
     "generic_bf16_D5_Dv7": Spec(B=3, Hq=4, Hk=2, Q=3, D=5, Dv=7, M=50, dtype="bf16",
                                 counts=("uniform", 0, 3)),
     "mha_fp16_Dv256": SMALL["mha_fp16_Dv256"],
+    # the few-rows kernel at each width it takes (D = Dv = 64, 128, 256)
+    "rows_f16_D64_R8": Spec(B=3, Hq=8, Hk=2, Q=2, D=64, Dv=64, M=300, dtype="f16",
+                            counts=("uniform", 0, 2)),
+    "rows_f32_D256_R16": Spec(B=2, Hq=8, Hk=2, Q=4, D=256, Dv=256, M=200, dtype="f32",
+                              counts=("uniform", 1, 4)),
+    "rows_bf16_D256_R4_ragged": Spec(B=4, Hq=4, Hk=1, Q=1, D=256, Dv=256, M=700, dtype="bf16",
+                                     lengths=("uniform", 0, 699)),
 }
 
 
