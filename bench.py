@@ -57,10 +57,17 @@ PATH_KERNELS_READONLY = {
            "finalize_merge_kernel", "attend_unpack_kernel"]
     for path in ("fused", "tensor", "decode_tc", "generic")}
 # the backward: the statistics pass (step kernel and merge, no copy), then its own four
+# (the slot kernel is bwd_kv_rows_kernel for units of <= 16 rows with D = Dv in {64, 128, 256})
 PATH_KERNELS_BACKWARD = {
     path: [first, "finalize_merge_kernel", "bwd_rowdot_kernel", "bwd_kv_kernel",
            "bwd_copy_kernel", "bwd_dq_kernel"]
     for path, first in (("fused", "fused_step_kernel"), ("generic", "generic_attend_kernel"))}
+
+
+def backward_slot_kernel(spec) -> str:
+    R = spec.Hq // spec.Hk * spec.Q
+    few = R <= 16 and spec.D == spec.Dv and spec.D in (64, 128, 256)
+    return "bwd_kv_rows_kernel" if few else "bwd_kv_kernel"
 PATH_KERNELS = {"fused": ["fused_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "tensor": ["tc_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "generic": ["generic_copy_kernel", "generic_attend_kernel",
@@ -73,6 +80,7 @@ KERNEL_SOURCES = {
     "decode_tc_kernel": [_CSRC + f for f in ("kvc_decode_tc.cu", "kvc_internal.cuh",
                                              "kvc_pipeline.cuh", "kvc_tcgen05.cuh")],
     "bwd_kv_kernel": [_CSRC + f for f in ("kvc_backward.cu", "kvc_internal.cuh")],
+    "bwd_kv_rows_kernel": [_CSRC + f for f in ("kvc_backward.cu", "kvc_internal.cuh")],
     "bwd_copy_kernel": [_CSRC + f for f in ("kvc_backward.cu", "kvc_internal.cuh")],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
@@ -535,11 +543,13 @@ def run_ours(args, spec, world, rank, local):
     value = world * nbytes["total"] / (ms_step * 1e-3) / 1e9
     peak, peak_src = measured_peak()
     if args.backward:  # the longer of the two HBM kernels of the gradients
-        names_b = PATH_KERNELS_BACKWARD[path] if nkern == 6 else ["bwd_kv_kernel", "bwd_copy_kernel"]
+        names_b = list(PATH_KERNELS_BACKWARD[path] if nkern == 6
+                       else ["bwd_kv_kernel", "bwd_copy_kernel"])
         ks = max((i for i, nm in enumerate(names_b) if nm in ("bwd_kv_kernel", "bwd_copy_kernel")),
                  key=lambda i: kern_ms[i])
+        nbytes["fused_kernel"] = nbytes[names_b[ks]]
+        names_b = [backward_slot_kernel(spec) if nm == "bwd_kv_kernel" else nm for nm in names_b]
         kname = names_b[ks]
-        nbytes["fused_kernel"] = nbytes[kname]
     else:
         ks = (2 if args.paged and nkern > 2 else
               1 if (args.inplace or args.readonly) and nkern > 1 else 0)  # index of the step kernel
