@@ -35,6 +35,10 @@ import workloads  # noqa: E402
 METRIC = "effective HBM GB/s (and % of 8 TB/s) + kv steps/s per config, 1 GB300"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+# CUDA-core fp32 peak: 152 SMs x 128 FP32 lanes x 2 flops per FMA x 2070 MHz
+# (the maximum SM clock); the roofline of the backward's slot kernel when its
+# products, not its bytes, bound it
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 _CSRC = "kv_cache_append_gb300/csrc/"
 # The first kernel of each path and the sources that define it.
 STEP_KERNEL = {"fused": "fused_step_kernel", "tensor": "tc_step_kernel",
@@ -57,7 +61,8 @@ PATH_KERNELS_READONLY = {
            "finalize_merge_kernel", "attend_unpack_kernel"]
     for path in ("fused", "tensor", "decode_tc", "generic")}
 # the backward: the statistics pass (step kernel and merge, no copy), then its own four
-# (the slot kernel is bwd_kv_rows_kernel for units of <= 16 rows with D = Dv in {64, 128, 256})
+# (the slot kernel is bwd_kv_rows_kernel for units of <= 16 rows with D = Dv in {64, 128, 256},
+# bwd_kv_tiled_kernel for other units of more than 4 rows with D and Dv multiples of 64 up to 256)
 PATH_KERNELS_BACKWARD = {
     path: [first, "finalize_merge_kernel", "bwd_rowdot_kernel", "bwd_kv_kernel",
            "bwd_copy_kernel", "bwd_dq_kernel"]
@@ -67,7 +72,9 @@ PATH_KERNELS_BACKWARD = {
 def backward_slot_kernel(spec) -> str:
     R = spec.Hq // spec.Hk * spec.Q
     few = R <= 16 and spec.D == spec.Dv and spec.D in (64, 128, 256)
-    return "bwd_kv_rows_kernel" if few else "bwd_kv_kernel"
+    tiled = (not few and R > 4 and spec.D % 64 == 0 and spec.Dv % 64 == 0 and spec.D <= 256
+             and spec.Dv <= 256)
+    return "bwd_kv_rows_kernel" if few else "bwd_kv_tiled_kernel" if tiled else "bwd_kv_kernel"
 PATH_KERNELS = {"fused": ["fused_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "tensor": ["tc_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "generic": ["generic_copy_kernel", "generic_attend_kernel",
@@ -81,6 +88,7 @@ KERNEL_SOURCES = {
                                              "kvc_pipeline.cuh", "kvc_tcgen05.cuh")],
     "bwd_kv_kernel": [_CSRC + f for f in ("kvc_backward.cu", "kvc_internal.cuh")],
     "bwd_kv_rows_kernel": [_CSRC + f for f in ("kvc_backward.cu", "kvc_internal.cuh")],
+    "bwd_kv_tiled_kernel": [_CSRC + f for f in ("kvc_backward_tiled.cu", "kvc_internal.cuh")],
     "bwd_copy_kernel": [_CSRC + f for f in ("kvc_backward.cu", "kvc_internal.cuh")],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
@@ -159,6 +167,15 @@ def algorithmic_bytes_backward(spec: workloads.Spec, lengths, counts) -> dict:
     copy = sum(spec.M - n for n in N) * row * 2
     rest = qrows * spec.D * es + 2 * B * spec.Hk * spec.Q * (spec.D + spec.Dv) * es + B * (16 + spec.Q)
     return {"total": kv + copy + rest, "bwd_kv_kernel": kv, "bwd_copy_kernel": copy}
+
+
+def flops_backward(spec: workloads.Spec, lengths, counts) -> int:
+    """Arithmetic of the backward's slot kernel: for every allowed (query row,
+    slot) pair, dcontext . V'_j (2 Dv flops), ds q into dK'_j (2 D), a dcontext
+    into dV'_j (2 Dv) and ds K'_j into dq (2 D)."""
+    allowed = sum(spec.Hq * sum(int(l) + t + 1 for t in range(int(c)))
+                  for l, c in zip(lengths, counts))
+    return 4 * (spec.D + spec.Dv) * allowed
 
 
 def source_digest(paths) -> str:
@@ -559,6 +576,20 @@ def run_ours(args, spec, world, rank, local):
     fused_ms = kern_ms[ks]
     achieved = nbytes["fused_kernel"] / (fused_ms * 1e-3) / 1e9
     traffic = kernel_traffic(mode_key(args), kname, nbytes["fused_kernel"])
+    roof = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
+            "traffic": traffic}
+    if args.backward and kname.startswith("bwd_kv"):
+        # the slot kernel: bound by its fp32 products when they take longer at
+        # the CUDA-core peak than its bytes at the HBM peak
+        flops = flops_backward(spec, lengths_h, counts_h)
+        if flops / (FP32_PEAK_TFLOPS * 1e12) > nbytes["fused_kernel"] / (peak * 1e9):
+            tf = flops / (fused_ms * 1e-3) / 1e12
+            roof = {"bound": "alu", "kernel": kname, "achieved": round(tf, 2),
+                    "peak": round(FP32_PEAK_TFLOPS, 2), "unit": "TFLOP/s",
+                    "frac": round(tf / FP32_PEAK_TFLOPS, 4),
+                    "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x 2070 MHz",
+                    "flops": flops, "hbm_frac": round(achieved / peak, 4), "traffic": traffic}
 
     # ---- end to end through the public API: pinned host in, pinned host out
     e2e = None
@@ -602,10 +633,7 @@ def run_ours(args, spec, world, rank, local):
         "kernels": {kname: {"ms": round(kern_ms[ks], 4),
                             "algorithmic_bytes": nbytes["fused_kernel"],
                             "algorithmic_GBps": round(achieved, 1)}},
-        "roofline": {"bound": "hbm", "kernel": kname,
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "traffic": traffic},
+        "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": nkern * args.steps,

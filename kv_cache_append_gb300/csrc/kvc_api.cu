@@ -1072,6 +1072,9 @@ namespace {
 // Backward workspace: the step's workspace (its statistics pass), then the
 // fp32 context rows, the per-row sums D, the step's context in the dtype and
 // its lengths (both unused scratch the step needs as arguments).
+#ifndef KVC_BWD_ROWS_MAX
+#define KVC_BWD_ROWS_MAX 16  // units of up to this many rows (at most 16) take bwd_kv_rows_kernel
+#endif
 struct BwdLayout {
     size_t step = 0, ctx_f32 = 0, drow = 0, dq = 0, ctx_t = 0, lengths = 0, total = 0;
 };
@@ -1206,8 +1209,15 @@ int backward_impl(const kvc_dims* dims, const void* query, const void* new_key,
                              aligned16(d_key_cache_out) && aligned16(d_value_cache_out) &&
                              aligned16(d_key_cache) && aligned16(d_value_cache) &&
                              aligned16(d_new_key) && aligned16(d_new_value);
-        bp.rows_smem = (R <= 16 && widths && aligned && rows_smem <= dev.smem_optin)
+        bp.rows_smem = (R <= KVC_BWD_ROWS_MAX && widths && aligned && rows_smem <= dev.smem_optin)
                            ? static_cast<int>(rows_smem) : 0;
+        // the tiled kernel (more rows; D and Dv multiples of 64 up to 256, the
+        // query, context-gradient and accumulator rows 16-byte aligned too)
+        const int64_t tiled_smem = bwd_tiled_smem_bytes(d.D, d.Dv);
+        const bool tiled_widths = d.D % 64 == 0 && d.Dv % 64 == 0 && d.D <= 256 && d.Dv <= 256;
+        bp.tiled_smem = (bp.rows_smem == 0 && R > 4 && tiled_widths && aligned && aligned16(d_context) &&
+                         aligned16(bp.dq_acc) && tiled_smem <= dev.smem_optin)
+                            ? static_cast<int>(tiled_smem) : 0;
     }
     bp.scale = static_cast<float>(scale);
     bp.slots_per_block = 256;

@@ -19,14 +19,18 @@
 // which leaves each valid row's normaliser (m, 1/l), its fp32 scores on the
 // allowed slots and its fp32 context in the workspace. Then:
 //
-//   bwd_rowdot_kernel  one warp per query row: D from the scores, dattention,
+//   bwd_rowdot_kernel  one block per query row: D from the scores, dattention,
 //                      dcontext and the context.
-//   bwd_kv_kernel      one warp per cache slot below the new length of a unit:
+//   the slot kernel    for every cache slot below the new length of a unit:
 //                      a_j and ds_j for each of the unit's query rows, dK'_j
 //                      and dV'_j plus the returned caches' own gradient,
 //                      written to the cache gradient or the new-row gradient;
-//                      ds_j K'_j summed per row over the block's slots in
-//                      shared memory, then into an fp32 accumulator.
+//                      ds_j K'_j summed per row into an fp32 accumulator.
+//                      bwd_kv_rows_kernel for units of at most 16 rows with
+//                      D = Dv in {64, 128, 256}, bwd_kv_tiled_kernel
+//                      (kvc_backward_tiled.cu) for other units of more than
+//                      4 rows with D and Dv multiples of 64, bwd_kv_kernel
+//                      (one warp per slot) for every other shape.
 //   bwd_copy_kernel    the slots from the new length on: their gradient is the
 //                      returned caches' gradient, 16 bytes at a time.
 //   bwd_dq_kernel      dq = scale * the accumulated sum, in the dtype.
@@ -55,32 +59,40 @@ __device__ __forceinline__ float ld(const void* base, int64_t i) {
     return Storage<T>::to_float(static_cast<const T*>(base)[i]);
 }
 
-// D for every query row; the contract flags once per batch row.
+// D for every query row, one block per row (its slots spread over the
+// block's threads, the warps' sums added in shared memory).
 template <typename T>
 __global__ void __launch_bounds__(kBwdWarps * 32) bwd_rowdot_kernel(const BwdParams bp) {
+    __shared__ float part[kBwdWarps];
     const StepParams& p = bp.p;
-    const int lane = threadIdx.x & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * kBwdWarps + (threadIdx.x >> 5);
-    if (row >= p.B * p.Hq * p.Q) return;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t row = blockIdx.x;
     const int64_t t = row % p.Q, b = row / (p.Hq * p.Q);
     const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
     if (t >= ra.n) {
-        if (lane == 0) bp.drow[row] = 0.f;
+        if (threadIdx.x == 0) bp.drow[row] = 0.f;
         return;
     }
     const RowStat rs = p.rowstat[row];
     float acc = 0.f;
     if (bp.d_attention) {
         const float* s = p.scores + row * p.M;
-        for (int64_t j = lane; j <= rs.lim; j += 32)
+        for (int64_t j = threadIdx.x; j <= rs.lim; j += blockDim.x)
             acc += fast_exp2(s[j] - rs.mx) * rs.inv_l * ld<T>(bp.d_attention, row * p.M + j);
     }
     if (bp.d_context) {
-        for (int64_t e = lane; e < p.Dv; e += 32)
+        for (int64_t e = threadIdx.x; e < p.Dv; e += blockDim.x)
             acc += ld<T>(bp.d_context, row * p.Dv + e) * p.ctx_f32[row * p.Dv + e];
     }
     acc = bwd_warp_sum(acc);
-    if (lane == 0) bp.drow[row] = acc;
+    if (lane == 0) part[w] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float d = 0.f;
+#pragma unroll
+        for (int i = 0; i < kBwdWarps; ++i) d += part[i];
+        bp.drow[row] = d;
+    }
 }
 
 // One block per slab of slots_per_block slots below N_b of unit u, one warp
@@ -518,11 +530,17 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdParams bp) {
 }
 
 template <typename T>
+constexpr int dtype_code() {
+    return std::is_same<T, float>::value ? KVC_F32
+                                         : std::is_same<T, __nv_bfloat16>::value ? KVC_BF16 : KVC_F16;
+}
+
+template <typename T>
 cudaError_t launch_t(const BwdParams& bp, bool words16, cudaStream_t stream,
                      const std::function<cudaError_t()>& after) {
     const StepParams& p = bp.p;
     const int64_t rows = p.B * p.Hq * p.Q, U = p.B * p.Hk;
-    const unsigned row_blocks = static_cast<unsigned>((rows + kBwdWarps - 1) / kBwdWarps);
+    const unsigned row_blocks = static_cast<unsigned>(rows);
     cudaError_t e = cudaSuccess;
     if (rows > 0) {
         bwd_rowdot_kernel<T><<<row_blocks, kBwdWarps * 32, 0, stream>>>(bp);
@@ -534,7 +552,7 @@ cudaError_t launch_t(const BwdParams& bp, bool words16, cudaStream_t stream,
         e = cudaMemsetAsync(bp.dq_acc, 0, static_cast<size_t>(rows * p.D) * sizeof(float), stream);
         if (e != cudaSuccess) return e;
     }
-    if (p.R <= 16 && bp.rows_smem > 0) {
+    if (bp.rows_smem > 0) {
         const dim3 grid(static_cast<unsigned>((p.M + kBwdWarps * 32 - 1) / (kBwdWarps * 32)),
                         static_cast<unsigned>(U));
         auto launch = [&](auto kern) -> cudaError_t {
@@ -553,6 +571,8 @@ cudaError_t launch_t(const BwdParams& bp, bool words16, cudaStream_t stream,
         e = p.D == 64 ? by_rows(std::integral_constant<int, 2>())
                       : p.D == 128 ? by_rows(std::integral_constant<int, 4>())
                                    : by_rows(std::integral_constant<int, 8>());
+    } else if (bp.tiled_smem > 0) {
+        e = launch_bwd_kv_tiled(bp, dtype_code<T>(), stream);
     } else {
         const dim3 kv_grid(
             static_cast<unsigned>((p.M + bp.slots_per_block - 1) / bp.slots_per_block),

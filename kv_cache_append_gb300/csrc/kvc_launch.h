@@ -68,6 +68,7 @@ struct BwdParams {
     float* dq_acc;            // [B*Hq*Q*D] scratch: sum_j ds_j K'_j per query row
     int stage_rows;           // 1: bwd_kv_kernel stages the unit's rows in shared memory
     int rows_smem;            // > 0: bytes of bwd_kv_rows_kernel's shared memory (units of <= 16 rows)
+    int tiled_smem;           // > 0: bytes of bwd_kv_tiled_kernel's shared memory (units of > 16 rows)
     float scale;              // the scores' scale (natural-log domain)
     int64_t slots_per_block;  // cache slots per block of bwd_kv_kernel
 };
@@ -76,6 +77,11 @@ struct BwdParams {
 // after() runs after each kernel launch (event recording for the timed face).
 cudaError_t launch_backward(const BwdParams& bp, int dtype, bool words16, cudaStream_t stream,
                             const std::function<cudaError_t()>& after);
+// The slot gradients as small dense products, for units of many query rows
+// with D and Dv multiples of 64 up to 256 (kvc_backward_tiled.cu); its shared
+// memory in bytes.
+cudaError_t launch_bwd_kv_tiled(const BwdParams& bp, int dtype, cudaStream_t stream);
+int64_t bwd_tiled_smem_bytes(int64_t D, int64_t Dv);
 
 // Merge of the partials: context rows and one RowStat per query row (kvc_finalize.cu).
 cudaError_t launch_finalize_merge(const StepParams& p, int dtype, cudaStream_t stream);

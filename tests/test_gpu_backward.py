@@ -87,6 +87,20 @@ CASES = {
                               counts=("uniform", 1, 4)),
     "rows_bf16_D256_R4_ragged": Spec(B=4, Hq=4, Hk=1, Q=1, D=256, Dv=256, M=700, dtype="bf16",
                                      lengths=("uniform", 0, 699)),
+    # the tiled kernel (more than 4 rows, D and Dv multiples of 64, not taken
+    # by the few-rows kernel): each instance, a last row chunk of 8 rows,
+    # D != Dv, tiles cut by M and N
+    "tiled_bf16_D128_R40_ragged": Spec(B=3, Hq=10, Hk=1, Q=4, D=128, Dv=128, M=500,
+                                       dtype="bf16", lengths=("uniform", 0, 495),
+                                       counts=("uniform", 0, 4)),
+    "tiled_f16_D256_R32": Spec(B=2, Hq=8, Hk=2, Q=8, D=256, Dv=256, M=300, dtype="f16",
+                               counts=("uniform", 1, 8)),
+    "tiled_f32_D128_Dv64_R24": Spec(B=3, Hq=6, Hk=1, Q=4, D=128, Dv=64, M=130, dtype="f32",
+                                    lengths=("uniform", 60, 126)),
+    "tiled_bf16_D64_Dv192_R18": Spec(B=2, Hq=12, Hk=2, Q=3, D=64, Dv=192, M=260, dtype="bf16",
+                                     hot_frac=0.05, hot_scale=20.0),
+    "tiled_f16_D64_Dv128_R8": Spec(B=3, Hq=8, Hk=2, Q=2, D=64, Dv=128, M=400, dtype="f16",
+                                   counts=("uniform", 0, 2)),
 }
 
 
@@ -99,8 +113,9 @@ def test_backward_parity(name, seed):
 
 @pytest.mark.parametrize("which", [("context",), ("attention",), ("key_cache", "value_cache"),
                                    ()])
-def test_backward_partial_gradients(which):
-    x = workloads.generate(SMALL["specdec_bf16"], 3)
+@pytest.mark.parametrize("name", ["specdec_bf16_hot", "tiled_bf16_D128_R40_ragged"])
+def test_backward_partial_gradients(which, name):
+    x = workloads.generate(CASES[name], 3)
     check(x, upstream(x, 7, which))
 
 
@@ -156,6 +171,33 @@ def test_backward_decode_full_size_sampled():
     lengths = x.lengths.cpu().numpy()
     bsel = sorted({int(lengths.argmax()), int(lengths.argmin()), 7})
     idx = torch.tensor(bsel, device=DEV)
+    sub = [t.index_select(0, idx).cpu() for t in x.args()]
+    ref = oracle.step_backward(*sub, options=x.options,
+                               **{f"d_{k}": (None if v is None else v.index_select(0, idx).cpu())
+                                  for k, v in grads.items()})
+    rtol, atol = TOL[x.query.dtype]
+    for name in NAMES:
+        r = ref["d_" + name]
+        gw = got[name].index_select(0, idx).double().cpu().numpy()
+        err = np.abs(gw - r)
+        assert np.all(err <= rtol * np.abs(r) + atol * max(1.0, float(np.abs(r).max()))), name
+    del got, x
+    torch.cuda.empty_cache()
+
+
+def test_backward_long_mqa_heads_sampled():
+    """long_mqa's heads (128 query rows per KV head, D=192, Dv=128, fp16) over
+    8192 slots, B=8: the tiled kernel over 128 tiles per unit; the longest
+    batch row against the oracle (the oracle takes about a minute per batch
+    row at long_mqa's full 65536 slots)."""
+    spec = workloads.SPECS["long_mqa"].replace(M=8192, lengths=("uniform", 7000, 8184))
+    x = workloads.generate(spec, seed=2, device=DEV)
+    grads = upstream(x, 13, which=("attention", "context"))
+    grads = {k: (None if v is None else v.to(DEV)) for k, v in grads.items()}
+    got = kvc.kv_cache_attention_step_backward(*x.args(), x.options,
+                                               **{f"d_{k}": v for k, v in grads.items()})
+    torch.cuda.synchronize()
+    idx = torch.tensor([int(x.lengths.cpu().argmax())], device=DEV)
     sub = [t.index_select(0, idx).cpu() for t in x.args()]
     ref = oracle.step_backward(*sub, options=x.options,
                                **{f"d_{k}": (None if v is None else v.index_select(0, idx).cpu())
