@@ -1198,12 +1198,9 @@ int backward_impl(const kvc_dims* dims, const void* query, const void* new_key,
         const int64_t R = (d.Hq / d.Hk) * d.Q;
         const int64_t need = (3 * R + R * (2 * d.D + d.Dv)) * 4;
         bp.stage_rows = device_info(&dev) == cudaSuccess && need <= dev.smem_optin ? 1 : 0;
-        // the few-rows kernel (D = Dv in {64, 128, 256}, rows 16-byte aligned):
-        // q and dcontext [NR][D], per warp a and dattention [32][NR] and
-        // query-gradient sums [NR][D]
-        const int64_t NR = R <= 4 ? 4 : R <= 8 ? 8 : 16;
-        const int64_t rows_smem = (NR * 2 * d.D + 8 * (2 * 32 * NR + NR * d.D)) * 4;
+        // the few-rows kernel (D = Dv in {64, 128, 256}, rows 16-byte aligned)
         const bool widths = d.D == d.Dv && (d.D == 64 || d.D == 128 || d.D == 256);
+        const int64_t rows_smem = widths ? bwd_rows_smem_bytes(R, d.D) : 0;
         const bool aligned = aligned16(query) && aligned16(new_key) && aligned16(new_value) &&
                              aligned16(key_cache) && aligned16(value_cache) &&
                              aligned16(d_key_cache_out) && aligned16(d_value_cache_out) &&

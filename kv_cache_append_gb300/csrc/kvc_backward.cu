@@ -237,9 +237,12 @@ __global__ void __launch_bounds__(kBwdWarps * 32) bwd_kv_kernel(const BwdParams 
 // attention gradients of its slot together (coalesced along the slots) into
 // shared memory as a_rj and dattention_rj; then slot by slot (the next slot's
 // rows loading while one is worked), the rows' dcontext . V'_j reduced
-// together by a reduce-scatter butterfly, and ds_rj K'_j summed per row in
-// the warp's own shared-memory buffer (no atomics); at the end the warps'
-// buffers are summed into the fp32 accumulator.
+// together by a reduce-scatter butterfly, and ds_rj K'_j summed per row:
+// in registers when NR V <= 64 (the warps' sums merged once per block in
+// shared memory), else in the warp's own shared-memory buffer; at the end
+// the block's sums go to the fp32 accumulator. D_r is folded into the staged
+// attention gradient (dattention_rj - D_r), so that phase 2 holds no per-row
+// state beyond the butterfly's NR partial sums.
 template <int NR>
 struct Log2Rows;
 template <>
@@ -315,9 +318,44 @@ struct LaneVec {
     }
 };
 
+// V consecutive floats of shared memory at p (aligned to 4 V bytes).
+template <int V>
+__device__ __forceinline__ void lds_vec(const float* p, float (&f)[V]) {
+    if constexpr (V % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < V / 4; ++k) {
+            const float4 v = reinterpret_cast<const float4*>(p)[k];
+            f[4 * k] = v.x; f[4 * k + 1] = v.y; f[4 * k + 2] = v.z; f[4 * k + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < V / 2; ++k) {
+            const float2 v = reinterpret_cast<const float2*>(p)[k];
+            f[2 * k] = v.x; f[2 * k + 1] = v.y;
+        }
+    }
+}
+
+// The query-gradient sums stay in registers (NR x V per lane) when they are
+// few enough; else each warp keeps them in its own shared-memory buffer.
+#ifndef KVC_BWD_ROWS_CAP
+#define KVC_BWD_ROWS_CAP 32  // NR x V up to which the registers are capped for two blocks per SM
+#endif
+template <int NR, int V>
+struct RowsLayout {
+    static constexpr bool kRegDq = NR * V <= 64;
+    static constexpr int kBlocks = NR * V <= KVC_BWD_ROWS_CAP ? 2 : 1;
+    static constexpr int kWarpFloats = 2 * 32 * NR + (kRegDq ? 0 : NR * 32 * V);
+    // q, dcontext and (registers case) the block's sums [NR][W]; per warp a,
+    // dattention - D [32][NR] and (else) the warp's sums [NR][W]
+    static constexpr int kFloats = (kRegDq ? 3 : 2) * NR * 32 * V + kBwdWarps * kWarpFloats;
+};
+
 template <typename T, int NR, int V>
-__global__ void __launch_bounds__(kBwdWarps * 32) bwd_kv_rows_kernel(const BwdParams bp) {
+__global__ void __launch_bounds__(kBwdWarps * 32, (RowsLayout<NR, V>::kBlocks))
+    bwd_kv_rows_kernel(const BwdParams bp) {
     using LV = LaneVec<T, V>;
+    using Lay = RowsLayout<NR, V>;
     constexpr int W = 32 * V;  // D = Dv
     constexpr int KW = LV::kWords;
     extern __shared__ __align__(16) float sm[];
@@ -338,44 +376,44 @@ __global__ void __launch_bounds__(kBwdWarps * 32) bwd_kv_rows_kernel(const BwdPa
     const int64_t jb = static_cast<int64_t>(blockIdx.x) * (kBwdWarps * 32);
     if (jb >= jend) return;  // whole block
     const int64_t row0 = (b * p.Hq + kv * p.G) * p.Q;
-    // shared memory (floats): q [NR][W], dcontext [NR][W], per warp: a [32][NR],
-    // dattention [32][NR], query-gradient sums [NR][W]
-    constexpr int kWarpFloats = 2 * 32 * NR + NR * W;
     float* s_q = sm;
     float* s_dc = s_q + NR * W;
-    float* s_a = s_dc + NR * W + w * kWarpFloats;
+    float* s_dqs = s_dc + NR * W;  // the block's sums (registers case)
+    float* s_a = s_dc + NR * W + (Lay::kRegDq ? NR * W : 0) + w * Lay::kWarpFloats;
     float* s_da = s_a + 32 * NR;
-    float* s_dq = s_da + 32 * NR;
+    float* s_dq = s_da + 32 * NR;  // the warp's sums (shared-memory case)
     for (int i = threadIdx.x; i < NR * W; i += blockDim.x) {
         s_q[i] = i < R * W ? Storage<T>::to_float(static_cast<const T*>(p.query)[row0 * W + i]) : 0.f;
         s_dc[i] = (i < R * W && bp.d_context) ? ld<T>(bp.d_context, row0 * W + i) : 0.f;
+        if constexpr (Lay::kRegDq) s_dqs[i] = 0.f;
     }
-    for (int i = lane; i < NR * W; i += 32) s_dq[i] = 0.f;
-    int lim[NR];
-    float mx[NR], il[NR], dr[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-        const int64_t t = r % p.Q;
-        const bool ok = r < R && t < n;
-        lim[r] = ok ? static_cast<int>(L + t) : -1;
-        const RowStat rs = ok ? p.rowstat[row0 + r] : RowStat{0.f, 0.f, -1, 0};
-        mx[r] = rs.mx;
-        il[r] = rs.inv_l;
-        dr[r] = ok ? bp.drow[row0 + r] : 0.f;
-    }
-    __syncthreads();
+    if constexpr (!Lay::kRegDq)
+        for (int i = lane; i < NR * W; i += 32) s_dq[i] = 0.f;
     const int64_t j0 = jb + w * 32;
-    {  // phase 1: one slot per lane
+    {  // phase 1: one slot per lane; a_rj and dattention_rj - D_r
         const int64_t j = j0 + lane;
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
-            const bool ok = j < jend && j <= lim[r];
-            const int64_t idx = (row0 + r) * p.M + j;
-            s_a[lane * NR + r] = ok ? fast_exp2(p.scores[idx] - mx[r]) * il[r] : 0.f;
-            s_da[lane * NR + r] = (ok && bp.d_attention) ? ld<T>(bp.d_attention, idx) : 0.f;
+            const int64_t t = r % p.Q;
+            const bool valid = r < R && t < n;  // uniform over the block
+            RowStat rs{0.f, 0.f, -1, 0};
+            float dr = 0.f;
+            if (valid) {
+                rs = p.rowstat[row0 + r];
+                dr = bp.drow[row0 + r];
+            }
+            const bool ok = valid && j < jend && j <= L + t;
+            float a = 0.f, da = 0.f;
+            if (ok) {
+                const int64_t idx = (row0 + r) * p.M + j;
+                a = fast_exp2(p.scores[idx] - rs.mx) * rs.inv_l;
+                da = (bp.d_attention ? ld<T>(bp.d_attention, idx) : 0.f) - dr;
+            }
+            s_a[lane * NR + r] = a;
+            s_da[lane * NR + r] = da;
         }
     }
-    __syncwarp();
+    __syncthreads();
     // phase 2: slot by slot, lane l on elements [V l, V l + V) of each row
     const int64_t left = jend - j0;
     const int nj = left <= 0 ? 0 : left >= 32 ? 32 : static_cast<int>(left);
@@ -398,6 +436,11 @@ __global__ void __launch_bounds__(kBwdWarps * 32) bwd_kv_rows_kernel(const BwdPa
         if (gko) LV::load(gko + cr, gk);
         if (gvo) LV::load(gvo + cr, gv);
     };
+    float dqr[Lay::kRegDq ? NR : 1][V];
+#pragma unroll
+    for (int r = 0; r < (Lay::kRegDq ? NR : 1); ++r)
+#pragma unroll
+        for (int i = 0; i < V; ++i) dqr[r][i] = 0.f;
     uint32_t nk_w[KW], nv_w[KW], ngk_w[KW], ngv_w[KW];
     if (nj > 0) fetch(j0, nk_w, nv_w, ngk_w, ngv_w);
     for (int jj = 0; jj < nj; ++jj) {
@@ -412,9 +455,11 @@ __global__ void __launch_bounds__(kBwdWarps * 32) bwd_kv_rows_kernel(const BwdPa
         float a2[NR];
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
+            float dcv[V];
+            lds_vec<V>(s_dc + r * W + e0, dcv);
             float g = 0.f;
 #pragma unroll
-            for (int i = 0; i < V; ++i) g += s_dc[r * W + e0 + i] * vj[i];
+            for (int i = 0; i < V; ++i) g = fmaf(dcv[i], vj[i], g);
             a2[r] = g;
         }
         {
@@ -432,25 +477,31 @@ __global__ void __launch_bounds__(kBwdWarps * 32) bwd_kv_rows_kernel(const BwdPa
 #pragma unroll
             for (; o >= 1; o /= 2) a2[0] += __shfl_xor_sync(0xffffffffu, a2[0], o);
         }
-        float ds[NR], av[NR];
+        float dk[V], dv[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) dk[i] = dv[i] = 0.f;
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
             const float gr = __shfl_sync(0xffffffffu, a2[0], r << (5 - Log2Rows<NR>::v));
-            av[r] = s_a[jj * NR + r];
-            ds[r] = av[r] * (s_da[jj * NR + r] + gr - dr[r]);
+            const float av = s_a[jj * NR + r];
+            const float ds = av * (s_da[jj * NR + r] + gr);
+            float qv[V], dcv[V];
+            lds_vec<V>(s_q + r * W + e0, qv);
+            lds_vec<V>(s_dc + r * W + e0, dcv);
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                dk[i] = fmaf(ds, qv[i], dk[i]);
+                dv[i] = fmaf(av, dcv[i], dv[i]);
+                if constexpr (Lay::kRegDq)
+                    dqr[r][i] = fmaf(ds, kj[i], dqr[r][i]);
+                else
+                    s_dq[r * W + e0 + i] += ds * kj[i];
+            }
         }
-        float dk[V], dv[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) {
-            float sk = 0.f, sv = 0.f;
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                sk += ds[r] * s_q[r * W + e0 + i];
-                sv += av[r] * s_dc[r * W + e0 + i];
-                s_dq[r * W + e0 + i] += ds[r] * kj[i];
-            }
-            dk[i] = scale * sk + gk[i];
-            dv[i] = sv + gv[i];
+            dk[i] = scale * dk[i] + gk[i];
+            dv[i] += gv[i];
         }
         uint32_t ok_w[KW], ov_w[KW];
         LV::from_f(dk, ok_w);
@@ -468,13 +519,26 @@ __global__ void __launch_bounds__(kBwdWarps * 32) bwd_kv_rows_kernel(const BwdPa
             LV::store(static_cast<T*>(bp.d_value_cache) + (u * p.M + j) * W + e0, ov_w);
         }
     }
-    // the warps' query-gradient sums into the fp32 accumulator
-    __syncthreads();
-    const float* dq0 = s_dc + NR * W + 2 * 32 * NR;  // warp 0's buffer
-    for (int i = threadIdx.x; i < R * W; i += blockDim.x) {
-        float acc = 0.f;
-        for (int ww = 0; ww < kBwdWarps; ++ww) acc += dq0[ww * kWarpFloats + i];
-        if (acc != 0.f) atomicAdd(&bp.dq_acc[row0 * W + i], acc);
+    // the query-gradient sums into the fp32 accumulator
+    if constexpr (Lay::kRegDq) {
+        if (nj > 0) {
+#pragma unroll
+            for (int r = 0; r < NR; ++r)
+#pragma unroll
+                for (int i = 0; i < V; ++i)
+                    if (r < R) atomicAdd(&s_dqs[r * W + e0 + i], dqr[r][i]);
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < R * W; i += blockDim.x)
+            if (s_dqs[i] != 0.f) atomicAdd(&bp.dq_acc[row0 * W + i], s_dqs[i]);
+    } else {
+        __syncthreads();
+        const float* dq0 = s_dc + NR * W + 2 * 32 * NR;  // warp 0's buffer
+        for (int i = threadIdx.x; i < R * W; i += blockDim.x) {
+            float acc = 0.f;
+            for (int ww = 0; ww < kBwdWarps; ++ww) acc += dq0[ww * Lay::kWarpFloats + i];
+            if (acc != 0.f) atomicAdd(&bp.dq_acc[row0 * W + i], acc);
+        }
     }
 }
 
@@ -609,6 +673,17 @@ cudaError_t launch_t(const BwdParams& bp, bool words16, cudaStream_t stream,
 }
 
 }  // namespace
+
+int64_t bwd_rows_smem_bytes(int64_t R, int64_t D) {
+    auto bytes = [&](auto nr_tag) -> int64_t {
+        constexpr int NR = decltype(nr_tag)::value;
+        return D == 64 ? RowsLayout<NR, 2>::kFloats * 4
+                       : D == 128 ? RowsLayout<NR, 4>::kFloats * 4 : RowsLayout<NR, 8>::kFloats * 4;
+    };
+    return R <= 4 ? bytes(std::integral_constant<int, 4>())
+                  : R <= 8 ? bytes(std::integral_constant<int, 8>())
+                           : bytes(std::integral_constant<int, 16>());
+}
 
 cudaError_t launch_backward(const BwdParams& bp, int dtype, bool words16, cudaStream_t stream,
                             const std::function<cudaError_t()>& after) {

@@ -81,6 +81,9 @@ cudaError_t launch_backward(const BwdParams& bp, int dtype, bool words16, cudaSt
 // with D and Dv multiples of 64 up to 256 (kvc_backward_tiled.cu); its shared
 // memory in bytes.
 cudaError_t launch_bwd_kv_tiled(const BwdParams& bp, int dtype, cudaStream_t stream);
+// Shared memory of bwd_kv_rows_kernel for units of R <= 16 rows and D = Dv in
+// {64, 128, 256} (kvc_backward.cu).
+int64_t bwd_rows_smem_bytes(int64_t R, int64_t D);
 int64_t bwd_tiled_smem_bytes(int64_t D, int64_t Dv);
 
 // Merge of the partials: context rows and one RowStat per query row (kvc_finalize.cu).
