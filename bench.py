@@ -62,6 +62,7 @@ PATH_KERNELS_READONLY = {
     for path in ("fused", "tensor", "decode_tc", "generic")}
 # the backward: the statistics pass (step kernel and merge, no copy), then its own four
 # (the slot kernel is bwd_kv_rows_kernel for units of <= 16 rows with D = Dv in {64, 128, 256},
+# bwd_kv_tc_kernel for 16-bit units of 17-128 rows whose widths fit tensor memory,
 # bwd_kv_tiled_kernel for other units of more than 4 rows with D and Dv multiples of 64 up to 256)
 PATH_KERNELS_BACKWARD = {
     path: [first, "finalize_merge_kernel", "bwd_rowdot_kernel", "bwd_kv_kernel",
@@ -72,9 +73,13 @@ PATH_KERNELS_BACKWARD = {
 def backward_slot_kernel(spec) -> str:
     R = spec.Hq // spec.Hk * spec.Q
     few = R <= 16 and spec.D == spec.Dv and spec.D in (64, 128, 256)
-    tiled = (not few and R > 4 and spec.D % 64 == 0 and spec.Dv % 64 == 0 and spec.D <= 256
-             and spec.Dv <= 256)
-    return "bwd_kv_rows_kernel" if few else "bwd_kv_tiled_kernel" if tiled else "bwd_kv_kernel"
+    first = max(256, spec.D + spec.Dv)  # tensor-memory columns of the first products
+    tc = (not few and spec.dtype != "f32" and 16 < R <= 128 and spec.D % 64 == 0
+          and spec.Dv % 64 == 0 and max(spec.D, spec.Dv) <= 256 and first + spec.D <= 512)
+    tiled = (not few and not tc and R > 4 and spec.D % 64 == 0 and spec.Dv % 64 == 0
+             and spec.D <= 256 and spec.Dv <= 256)
+    return ("bwd_kv_rows_kernel" if few else "bwd_kv_tc_kernel" if tc else
+            "bwd_kv_tiled_kernel" if tiled else "bwd_kv_kernel")
 PATH_KERNELS = {"fused": ["fused_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "tensor": ["tc_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "generic": ["generic_copy_kernel", "generic_attend_kernel",
@@ -89,6 +94,8 @@ KERNEL_SOURCES = {
     "bwd_kv_kernel": [_CSRC + f for f in ("kvc_backward.cu", "kvc_internal.cuh")],
     "bwd_kv_rows_kernel": [_CSRC + f for f in ("kvc_backward.cu", "kvc_internal.cuh")],
     "bwd_kv_tiled_kernel": [_CSRC + f for f in ("kvc_backward_tiled.cu", "kvc_internal.cuh")],
+    "bwd_kv_tc_kernel": [_CSRC + f for f in ("kvc_backward_tc.cu", "kvc_internal.cuh",
+                                             "kvc_tcgen05.cuh")],
     "bwd_copy_kernel": [_CSRC + f for f in ("kvc_backward.cu", "kvc_internal.cuh")],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
@@ -579,9 +586,10 @@ def run_ours(args, spec, world, rank, local):
     roof = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
             "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
             "traffic": traffic}
-    if args.backward and kname.startswith("bwd_kv"):
-        # the slot kernel: bound by its fp32 products when they take longer at
-        # the CUDA-core peak than its bytes at the HBM peak
+    if args.backward and kname.startswith("bwd_kv") and kname != "bwd_kv_tc_kernel":
+        # a CUDA-core slot kernel: bound by its fp32 products when they take
+        # longer at the CUDA-core peak than its bytes at the HBM peak (the
+        # tensor-core one is HBM-bound: its products take ~1/20 of its bytes' time)
         flops = flops_backward(spec, lengths_h, counts_h)
         if flops / (FP32_PEAK_TFLOPS * 1e12) > nbytes["fused_kernel"] / (peak * 1e9):
             tf = flops / (fused_ms * 1e-3) / 1e12

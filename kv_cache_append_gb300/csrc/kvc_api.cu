@@ -1210,9 +1210,20 @@ int backward_impl(const kvc_dims* dims, const void* query, const void* new_key,
                            ? static_cast<int>(rows_smem) : 0;
         // the tiled kernel (more rows; D and Dv multiples of 64 up to 256, the
         // query, context-gradient and accumulator rows 16-byte aligned too)
+        // the tensor-core kernel (16-bit, 17 to 128 rows, widths that fit it)
+        const int64_t tc_smem = bwd_tc_smem_bytes(d.D, d.Dv);
+        bp.tc_smem = (bp.rows_smem == 0 && es == 2 && bwd_tc_fits(R, d.D, d.Dv) && aligned &&
+                      aligned16(d_context) && aligned16(bp.dq_acc) && tc_smem <= dev.smem_optin)
+                         ? static_cast<int>(tc_smem) : 0;
+        if (bp.tc_smem > 0) {  // about two CTAs per SM over all units' tiles
+            const int64_t tiles = (d.M + 127) / 128, units = d.B * d.Hk;
+            const int64_t ctas = 2 * static_cast<int64_t>(dev.sms > 0 ? dev.sms : 1);
+            const int64_t per = (tiles * units + ctas - 1) / ctas;
+            bp.tc_tiles_per_cta = per < 1 ? 1 : per;
+        }
         const int64_t tiled_smem = bwd_tiled_smem_bytes(d.D, d.Dv);
         const bool tiled_widths = d.D % 64 == 0 && d.Dv % 64 == 0 && d.D <= 256 && d.Dv <= 256;
-        bp.tiled_smem = (bp.rows_smem == 0 && R > 4 && tiled_widths && aligned && aligned16(d_context) &&
+        bp.tiled_smem = (bp.rows_smem == 0 && bp.tc_smem == 0 && R > 4 && tiled_widths && aligned && aligned16(d_context) &&
                          aligned16(bp.dq_acc) && tiled_smem <= dev.smem_optin)
                             ? static_cast<int>(tiled_smem) : 0;
     }

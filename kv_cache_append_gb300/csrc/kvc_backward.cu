@@ -27,7 +27,9 @@
 //                      written to the cache gradient or the new-row gradient;
 //                      ds_j K'_j summed per row into an fp32 accumulator.
 //                      bwd_kv_rows_kernel for units of at most 16 rows with
-//                      D = Dv in {64, 128, 256}, bwd_kv_tiled_kernel
+//                      D = Dv in {64, 128, 256}, bwd_kv_tc_kernel
+//                      (kvc_backward_tc.cu, tensor cores) for 16-bit units of
+//                      17 to 128 rows whose widths fit it, bwd_kv_tiled_kernel
 //                      (kvc_backward_tiled.cu) for other units of more than
 //                      4 rows with D and Dv multiples of 64, bwd_kv_kernel
 //                      (one warp per slot) for every other shape.
@@ -635,6 +637,8 @@ cudaError_t launch_t(const BwdParams& bp, bool words16, cudaStream_t stream,
         e = p.D == 64 ? by_rows(std::integral_constant<int, 2>())
                       : p.D == 128 ? by_rows(std::integral_constant<int, 4>())
                                    : by_rows(std::integral_constant<int, 8>());
+    } else if (bp.tc_smem > 0) {
+        e = launch_bwd_kv_tc(bp, dtype_code<T>(), stream);
     } else if (bp.tiled_smem > 0) {
         e = launch_bwd_kv_tiled(bp, dtype_code<T>(), stream);
     } else {

@@ -1,0 +1,420 @@
+// kvc_backward_tc.cu -- the step's slot gradients on the tensor cores, for
+// units of 17 to 128 query rows with 16-bit inputs.
+//
+// For one unit (batch row b, KV head) and its R query rows, the chain rule of
+// the step ("Required behavior", bullets 4-5) gives over the slots j below the
+// new length, with a_rj = exp(s_rj - m_r) / l_r the attention of row r,
+//
+//   G_rj  = dcontext_r . V'_j,   ds_rj = a_rj (dattention_rj + G_rj - D_r),
+//   dK'_j = scale sum_r ds_rj q_r,   dV'_j = sum_r a_rj dcontext_r,
+//   dq_r  = scale sum_j ds_rj K'_j.
+//
+// bwd_kv_tc_kernel computes them per tile of 128 slots as five tcgen05
+// products with fp32 accumulators in tensor memory (TMEM lane = slot for the
+// first four, = query row for the last):
+//
+//   S^T = K' q^T            [128 slots x 128 rows]  (the scores, recomputed)
+//   G^T = V' dcontext^T     [128 x 128]
+//   a^T, ds^T on CUDA cores from S^T, G^T, each row's (m, 1/l, D) and
+//        dattention, written to shared memory in the inputs' dtype
+//   dK' = ds^T q            [128 slots x D]
+//   dV' = a^T dcontext      [128 slots x Dv]
+//   dq += ds K'             [128 rows x D]  (summed over the CTA's tiles)
+//
+// then dK' (times scale) and dV' plus the returned caches' own gradient go to
+// the cache gradient, or to the new row's gradient for a slot a new row
+// filled (whose cache slot gets zero), and after the CTA's last tile its
+// query-gradient sums go to the fp32 accumulator with 16-byte atomics. The
+// unit's rows are padded to 128 with zero rows; ds and a are rounded to the
+// dtype once, as the operands of the last three products.
+//
+// Operands sit in shared memory in the 128-byte-swizzled layout: a 16-bit
+// [128 x W] matrix is W / 64 column blocks of 128 rows x 128 bytes, the
+// 16-byte chunk k of row r stored at chunk k ^ (r & 7). The same bytes serve
+// as a K-major operand (rows = M or N, columns = K) and as an MN-major one
+// (rows = K, columns = M or N): q and dcontext are B of S^T / G^T (K-major)
+// and of dK' / dV' (MN-major); ds^T is A of dK' (K-major) and of dq
+// (MN-major); K' is A of S^T (K-major) and B of dq (MN-major).
+//
+// One thread issues the products; every thread waits on one mbarrier per
+// batch of products (each wait bounded, its outcome made uniform with a
+// barrier so that no thread is left behind), then works on the results.
+#include <type_traits>
+
+#include "kvc_internal.cuh"
+#include "kvc_launch.h"
+#include "kvc_tcgen05.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int kTJ = 128;                // slots per tile (M of the slot-major products)
+constexpr int kTR = 128;                // query rows of a unit, padded (N of S^T, G^T; M of dq)
+constexpr int kTcThreads = 256;         // 8 warps: warp w reads TMEM lanes 32 (w % 4) ..
+constexpr uint32_t kTmemCols = 512;
+constexpr int kBlk = 128 * 128;         // one 64-element column block of a 128-row operand
+constexpr int kMaxChunks = 8;           // 32-element chunks of a K' or V' row (D, Dv <= 256)
+
+struct BtcLayout {
+    uint32_t k, v, q, c, a, ds, stats, bar, slot, flag, total;
+};
+
+__host__ __device__ inline BtcLayout btc_layout(int D, int Dv) {
+    BtcLayout L;
+    uint32_t off = 0;
+    L.k = off;  off += static_cast<uint32_t>(D / 64) * kBlk;   // K' tile
+    L.v = off;  off += static_cast<uint32_t>(Dv / 64) * kBlk;  // V' tile
+    L.q = off;  off += static_cast<uint32_t>(D / 64) * kBlk;   // the unit's query rows
+    L.c = off;  off += static_cast<uint32_t>(Dv / 64) * kBlk;  // the unit's dcontext rows
+    L.a = off;  off += 2 * kBlk;                               // a^T  [slots][rows]
+    L.ds = off; off += 2 * kBlk;                               // ds^T [slots][rows]
+    L.stats = off; off += 4 * kTR * 4;                         // m, 1/l, D, causal limit per row
+    L.bar = off;  off += 8;
+    L.slot = off; off += 4;
+    L.flag = off; off += 4;
+    L.total = off;
+    return L;
+}
+
+// Byte offset of the 16-byte chunk holding elements [c, c + 8) of row r.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+    return static_cast<uint32_t>(c >> 6) * kBlk + static_cast<uint32_t>(r) * 128u +
+           ((static_cast<uint32_t>((c & 63) >> 3) ^ static_cast<uint32_t>(r & 7)) << 4);
+}
+
+// 128 rows x W elements of T into the swizzled layout at dst: row r from
+// row_ptr(r) (16-byte aligned) for r < nvalid when it is not null, else zero.
+// Asynchronous copies: the caller waits for them (cp_async_wait_all).
+template <typename T, typename RowPtr>
+__device__ __forceinline__ void stage_sw128(unsigned char* dst, int W, int nvalid, RowPtr row_ptr) {
+    const int per_row = W / 8;
+    for (int i = threadIdx.x; i < kTJ * per_row; i += kTcThreads) {
+        const int r = i / per_row, c = (i - r * per_row) * 8;
+        unsigned char* d = dst + sw128_off(r, c);
+        const T* s = r < nvalid ? row_ptr(r) : nullptr;
+        if (s)
+            cp_async16(d, s + c);
+        else
+            *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// 32 consecutive elements of T from p (16-byte aligned) as floats.
+template <typename T>
+__device__ __forceinline__ void load32(const T* p, float (&f)[32]) {
+    constexpr int VE = Storage<T>::kVec16;
+#pragma unroll
+    for (int k = 0; k < 32 / VE; ++k)
+        Storage<T>::widen16(reinterpret_cast<const uint4*>(p)[k], f + k * VE);
+}
+
+// 32 floats to p (16-byte aligned) as 16-bit T.
+template <typename T>
+__device__ __forceinline__ void store32(T* p, const float (&f)[32]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        reinterpret_cast<uint4*>(p)[k] =
+            make_uint4(pack2<T>(f[8 * k], f[8 * k + 1]), pack2<T>(f[8 * k + 2], f[8 * k + 3]),
+                       pack2<T>(f[8 * k + 4], f[8 * k + 5]), pack2<T>(f[8 * k + 6], f[8 * k + 7]));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_constant__ BwdParams bp) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const StepParams& p = bp.p;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int D = static_cast<int>(p.D), Dv = static_cast<int>(p.Dv), R = static_cast<int>(p.R);
+    const BtcLayout Ly = btc_layout(D, Dv);
+    const int64_t u = blockIdx.y, b = u / p.Hk, kv = u - b * p.Hk;
+    const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
+    const int64_t L = ra.L, n = ra.n;
+    if (blockIdx.x == 0) {  // new-row gradients of the rows t >= n (nothing reaches them): zero
+        for (int64_t i = tid; i < (p.Q - n) * D; i += kTcThreads)
+            static_cast<T*>(bp.d_new_key)[(u * p.Q + n) * D + i] = Storage<T>::from_float(0.f);
+        for (int64_t i = tid; i < (p.Q - n) * Dv; i += kTcThreads)
+            static_cast<T*>(bp.d_new_value)[(u * p.Q + n) * Dv + i] = Storage<T>::from_float(0.f);
+    }
+    const int64_t jend = ra.flags ? 0 : L + n;
+    const int64_t tiles = (jend + kTJ - 1) / kTJ;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * bp.tc_tiles_per_cta;
+    const int64_t i1 = i0 + bp.tc_tiles_per_cta < tiles ? i0 + bp.tc_tiles_per_cta : tiles;
+    if (i0 >= i1) return;  // whole block, before any barrier or tensor memory
+    const int64_t row0 = (b * p.Hq + kv * p.G) * p.Q;  // the unit's rows are row0 + r
+    const uint32_t bar = smem_addr(smem + Ly.bar);
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + Ly.flag);
+    float* s_mx = reinterpret_cast<float*>(smem + Ly.stats);
+    float* s_il = s_mx + kTR;
+    float* s_dr = s_il + kTR;
+    int* s_lim = reinterpret_cast<int*>(s_dr + kTR);
+    if (tid == 0) {
+        mbar_init(bar, 1u);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    for (int r = tid; r < kTR; r += kTcThreads) {  // padded and invalid rows admit no slot
+        const int64_t t = r % p.Q;
+        const bool valid = r < R && t < n;
+        const RowStat rs = valid ? p.rowstat[row0 + r] : RowStat{0.f, 0.f, -1, 0};
+        s_mx[r] = rs.mx;
+        s_il[r] = rs.inv_l;
+        s_dr[r] = valid ? bp.drow[row0 + r] : 0.f;
+        s_lim[r] = valid ? static_cast<int>(L + t) : -1;
+    }
+    const T* qg = static_cast<const T*>(p.query);
+    const T* dcg = static_cast<const T*>(bp.d_context);
+    const T* dag = static_cast<const T*>(bp.d_attention);
+    // the unit's query and dcontext rows; rows of no valid query stay zero
+    stage_sw128<T>(smem + Ly.q, D, R, [&](int r) {
+        return (r % p.Q) < n ? qg + (row0 + r) * D : static_cast<const T*>(nullptr);
+    });
+    stage_sw128<T>(smem + Ly.c, Dv, R, [&](int r) {
+        return (dcg && (r % p.Q) < n) ? dcg + (row0 + r) * Dv : static_cast<const T*>(nullptr);
+    });
+    if (warp == 0) {
+        tmem_alloc(smem_addr(smem + Ly.slot), kTmemCols);
+        tmem_relinquish();
+    }
+    cp_async_wait_all();
+    fence_async_shared();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + Ly.slot);
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    const uint32_t id_s = mma_idesc_f16(kTJ, kTR, kBf16, false, false);  // S^T, G^T
+    const uint32_t id_k = mma_idesc_f16(kTJ, D, kBf16, true, false);     // dK'
+    const uint32_t id_v = mma_idesc_f16(kTJ, Dv, kBf16, true, false);    // dV'
+    const uint32_t id_q = mma_idesc_f16(kTR, D, kBf16, true, true);      // dq
+    const uint32_t colG = kTR, colV = static_cast<uint32_t>(D), colQ = kTmemCols - D;
+    const uint32_t sK = smem_addr(smem + Ly.k), sV = smem_addr(smem + Ly.v);
+    const uint32_t sQ = smem_addr(smem + Ly.q), sC = smem_addr(smem + Ly.c);
+    const uint32_t sA = smem_addr(smem + Ly.a), sDS = smem_addr(smem + Ly.ds);
+    const uint32_t my_lanes = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const int ts = 32 * (warp & 3) + lane;  // this thread's slot of a tile (TMEM lane)
+    const float qs = p.qscale;
+    const T* kc = static_cast<const T*>(p.key_cache) + u * p.M * D;
+    const T* vc = static_cast<const T*>(p.value_cache) + u * p.M * Dv;
+    const T* nk = static_cast<const T*>(p.new_key) + u * p.Q * D;
+    const T* nv = static_cast<const T*>(p.new_value) + u * p.Q * Dv;
+    uint32_t phase = 0;
+    bool failed = false;
+    // the slot rows of tile i: the input cache below L, the new rows from L on, zero past N
+    auto stage_tile = [&](int64_t i) {
+        const int64_t jb = i * kTJ;
+        const int nj = static_cast<int>(jend - jb < kTJ ? jend - jb : kTJ);
+        stage_sw128<T>(smem + Ly.k, D, nj, [&](int t) {
+            const int64_t j = jb + t;
+            return j >= L ? nk + (j - L) * D : kc + j * D;
+        });
+        stage_sw128<T>(smem + Ly.v, Dv, nj, [&](int t) {
+            const int64_t j = jb + t;
+            return j >= L ? nv + (j - L) * Dv : vc + j * Dv;
+        });
+    };
+    stage_tile(i0);
+    const int rbase = 64 * (warp >> 2);  // rows of this thread in the a / ds pass
+    const bool keys = warp < 4;          // epilogue: dK' (warps 0-3) or dV' (warps 4-7)
+    const int W = keys ? D : Dv;
+    const T* go = static_cast<const T*>(keys ? bp.d_key_out : bp.d_value_out);
+    for (int64_t it = i0; it < i1; ++it) {
+        const int64_t jb = it * kTJ;
+        const int nj = static_cast<int>(jend - jb < kTJ ? jend - jb : kTJ);
+        const int64_t j = jb + ts;  // this thread's slot
+        cp_async_wait_all();
+        fence_async_shared();
+        __syncthreads();
+        if (tid == 0) {  // S^T = K' q^T, G^T = V' dcontext^T (K-major operands, 16 elements a step)
+            tc_fence_after();
+            for (int kb = 0; kb < D / 64; ++kb)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma(tmem, smem_desc_sw128(sK + kb * kBlk + kk * 32, 16, 1024),
+                           smem_desc_sw128(sQ + kb * kBlk + kk * 32, 16, 1024), id_s, (kb | kk) != 0);
+            for (int kb = 0; kb < Dv / 64; ++kb)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma(tmem + colG, smem_desc_sw128(sV + kb * kBlk + kk * 32, 16, 1024),
+                           smem_desc_sw128(sC + kb * kBlk + kk * 32, 16, 1024), id_s, (kb | kk) != 0);
+            tc_commit(bar);
+        }
+        // the attention gradients of this thread's slot and rows, loaded while the products run
+        float dap[64];
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+            const int r = rbase + k;
+            dap[k] = (dag && j <= s_lim[r]) ? Storage<T>::to_float(dag[(row0 + r) * p.M + j]) : 0.f;
+        }
+        bool ok = mbar_wait(bar, phase, abort);
+        phase ^= 1u;
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {  // a^T and ds^T of this thread's slot, 16 rows at a time
+            const int r0 = rbase + 16 * g;
+            float sv[16], gv[16];
+            tmem_ldn<16>(my_lanes + static_cast<uint32_t>(r0), sv);
+            tmem_ldn<16>(my_lanes + colG + static_cast<uint32_t>(r0), gv);
+            uint32_t aw[8], dw[8];
+#pragma unroll
+            for (int k = 0; k < 16; k += 2) {
+                float av[2], dv[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = r0 + k + e;
+                    av[e] = dv[e] = 0.f;
+                    if (j <= s_lim[r]) {  // an allowed slot of a valid row (then j < N)
+                        const float a = fast_exp2(sv[k + e] * qs - s_mx[r]) * s_il[r];
+                        av[e] = a;
+                        dv[e] = a * (dap[16 * g + k + e] + gv[k + e] - s_dr[r]);
+                    }
+                }
+                aw[k / 2] = pack2<T>(av[0], av[1]);
+                dw[k / 2] = pack2<T>(dv[0], dv[1]);
+            }
+            const uint32_t o0 = sw128_off(ts, r0), o1 = sw128_off(ts, r0 + 8);
+            *reinterpret_cast<uint4*>(smem + Ly.a + o0) = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+            *reinterpret_cast<uint4*>(smem + Ly.a + o1) = make_uint4(aw[4], aw[5], aw[6], aw[7]);
+            *reinterpret_cast<uint4*>(smem + Ly.ds + o0) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+            *reinterpret_cast<uint4*>(smem + Ly.ds + o1) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
+        }
+        fence_async_shared();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            // dK' = ds^T q and dV' = a^T dcontext: K = the 128 rows, 16 a step;
+            // A K-major (rows contiguous), B MN-major (q / dcontext rows are K)
+#pragma unroll
+            for (int kk = 0; kk < kTR / 16; ++kk)
+                tc_mma(tmem, smem_desc_sw128(sDS + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024),
+                       smem_desc_sw128(sQ + kk * 16 * 128, kBlk, 1024), id_k, kk != 0);
+#pragma unroll
+            for (int kk = 0; kk < kTR / 16; ++kk)
+                tc_mma(tmem + colV, smem_desc_sw128(sA + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024),
+                       smem_desc_sw128(sC + kk * 16 * 128, kBlk, 1024), id_v, kk != 0);
+            // dq += ds K': K = the 128 slots; A = ds^T read M-contiguous, B = K' N-contiguous
+#pragma unroll
+            for (int kk = 0; kk < kTJ / 16; ++kk)
+                tc_mma(tmem + colQ, smem_desc_sw128(sDS + kk * 16 * 128, kBlk, 1024),
+                       smem_desc_sw128(sK + kk * 16 * 128, kBlk, 1024), id_q,
+                       !(it == i0 && kk == 0));
+            tc_commit(bar);
+        }
+        // the returned caches' gradient at this thread's slot, loaded while the products run
+        const bool live = ts < nj, is_new = j >= L;
+        uint4 gow[kMaxChunks][4];
+#pragma unroll
+        for (int ch = 0; ch < kMaxChunks; ++ch)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) gow[ch][k] = make_uint4(0u, 0u, 0u, 0u);
+        if (live && go) {
+#pragma unroll
+            for (int ch = 0; ch < kMaxChunks; ++ch)
+                if (ch * 32 < W) {
+                    const uint4* src = reinterpret_cast<const uint4*>(go + (u * p.M + j) * W + ch * 32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) gow[ch][k] = src[k];
+                }
+        }
+        ok = mbar_wait(bar, phase, abort);
+        phase ^= 1u;
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        tc_fence_after();
+        if (it + 1 < i1) stage_tile(it + 1);  // the tile buffers are free: the products are done
+        {  // dK' (times scale) or dV' of this thread's slot plus the returned caches' gradient
+            const float sc = keys ? bp.scale : 1.f;
+            T* cache_g = static_cast<T*>(keys ? bp.d_key_cache : bp.d_value_cache) + (u * p.M + j) * W;
+            T* dst = is_new ? static_cast<T*>(keys ? bp.d_new_key : bp.d_new_value) +
+                                  (u * p.Q + (j - L)) * W
+                            : cache_g;
+            const uint32_t base = my_lanes + (keys ? 0u : colV);
+#pragma unroll
+            for (int ch = 0; ch < kMaxChunks; ++ch) {
+                if (ch * 32 >= W) continue;  // uniform over the warp
+                float v[32];
+                tmem_ld32(base + static_cast<uint32_t>(ch * 32), v);  // the whole warp
+                if (live) {
+                    float gf[32];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) Storage<T>::widen16(gow[ch][k], gf + 8 * k);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) v[k] = fmaf(v[k], sc, gf[k]);
+                    store32<T>(dst + ch * 32, v);
+                    if (is_new) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            reinterpret_cast<uint4*>(cache_g + ch * 32)[k] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();  // tensor memory is free for the next tile
+    }
+    cp_async_wait_all();  // nothing in flight past an early exit
+    if (!failed) {  // the CTA's query-gradient sums: TMEM lane = row (warps 0-3)
+        tc_fence_after();
+        if (warp < 4) {
+            const int r = ts;
+            const bool valid = r < R && (r % p.Q) < n;
+            for (int c = 0; c < D; c += 32) {
+                float v[32];
+                tmem_ld32(my_lanes + colQ + static_cast<uint32_t>(c), v);
+                if (valid) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        atomicAdd(reinterpret_cast<float4*>(bp.dq_acc + (row0 + r) * D + c + 4 * k),
+                                  make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();  // every thread reaches this exactly once: all waits are bounded
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (tid == 0 && *abort && p.dev_status) atomicOr(p.dev_status, KVC_DEV_TIMEOUT);
+}
+
+template <typename T>
+cudaError_t launch_tc(const BwdParams& bp, cudaStream_t stream) {
+    const int64_t smem = bwd_tc_smem_bytes(bp.p.D, bp.p.Dv);
+    cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (bp.p.M + kTJ - 1) / kTJ;
+    const dim3 grid(static_cast<unsigned>((tiles + bp.tc_tiles_per_cta - 1) / bp.tc_tiles_per_cta),
+                    static_cast<unsigned>(bp.p.B * bp.p.Hk));
+    bwd_kv_tc_kernel<T><<<grid, kTcThreads, smem, stream>>>(bp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Bytes of shared memory: the layout, at least 116 KB so that one CTA (and
+// one 512-column tensor-memory allocation) runs per SM.
+int64_t bwd_tc_smem_bytes(int64_t D, int64_t Dv) {
+    const int64_t need = btc_layout(static_cast<int>(D), static_cast<int>(Dv)).total;
+    return need > 116 * 1024 ? need : 116 * 1024;
+}
+
+bool bwd_tc_fits(int64_t R, int64_t D, int64_t Dv) {
+    const int64_t kv = D > Dv ? D : Dv;
+    const int64_t first = 2 * kTR > D + Dv ? 2 * kTR : D + Dv;  // S^T, G^T then dK', dV' columns
+    return R > 16 && R <= kTR && D % 64 == 0 && Dv % 64 == 0 && kv <= 256 &&
+           first + D <= static_cast<int64_t>(kTmemCols);
+}
+
+cudaError_t launch_bwd_kv_tc(const BwdParams& bp, int dtype, cudaStream_t stream) {
+    return dtype == KVC_BF16 ? launch_tc<__nv_bfloat16>(bp, stream) : launch_tc<__half>(bp, stream);
+}
+
+}  // namespace kvc

@@ -68,7 +68,9 @@ struct BwdParams {
     float* dq_acc;            // [B*Hq*Q*D] scratch: sum_j ds_j K'_j per query row
     int stage_rows;           // 1: bwd_kv_kernel stages the unit's rows in shared memory
     int rows_smem;            // > 0: bytes of bwd_kv_rows_kernel's shared memory (units of <= 16 rows)
-    int tiled_smem;           // > 0: bytes of bwd_kv_tiled_kernel's shared memory (units of > 16 rows)
+    int tiled_smem;           // > 0: bytes of bwd_kv_tiled_kernel's shared memory (units of > 4 rows)
+    int tc_smem;              // > 0: bytes of bwd_kv_tc_kernel's shared memory (16-bit, 17-128 rows)
+    int64_t tc_tiles_per_cta; // 128-slot tiles of one unit per CTA of bwd_kv_tc_kernel
     float scale;              // the scores' scale (natural-log domain)
     int64_t slots_per_block;  // cache slots per block of bwd_kv_kernel
 };
@@ -81,6 +83,12 @@ cudaError_t launch_backward(const BwdParams& bp, int dtype, bool words16, cudaSt
 // with D and Dv multiples of 64 up to 256 (kvc_backward_tiled.cu); its shared
 // memory in bytes.
 cudaError_t launch_bwd_kv_tiled(const BwdParams& bp, int dtype, cudaStream_t stream);
+// The slot gradients on the tensor cores for 16-bit units of 17 to 128 rows
+// (kvc_backward_tc.cu): whether the shape fits (D, Dv multiples of 64 whose
+// products fit tensor memory), and the kernel's shared memory in bytes.
+cudaError_t launch_bwd_kv_tc(const BwdParams& bp, int dtype, cudaStream_t stream);
+bool bwd_tc_fits(int64_t R, int64_t D, int64_t Dv);
+int64_t bwd_tc_smem_bytes(int64_t D, int64_t Dv);
 // Shared memory of bwd_kv_rows_kernel for units of R <= 16 rows and D = Dv in
 // {64, 128, 256} (kvc_backward.cu).
 int64_t bwd_rows_smem_bytes(int64_t R, int64_t D);

@@ -87,9 +87,11 @@ CASES = {
                               counts=("uniform", 1, 4)),
     "rows_bf16_D256_R4_ragged": Spec(B=4, Hq=4, Hk=1, Q=1, D=256, Dv=256, M=700, dtype="bf16",
                                      lengths=("uniform", 0, 699)),
-    # the tiled kernel (more than 4 rows, D and Dv multiples of 64, not taken
-    # by the few-rows kernel): each instance, a last row chunk of 8 rows,
-    # D != Dv, tiles cut by M and N
+    # units of more than 4 rows with D and Dv multiples of 64 that the
+    # few-rows kernel does not take: the tensor-core kernel for the 16-bit ones
+    # of 17-128 rows whose widths fit it (R40, R18 here), the tiled kernel for
+    # the rest (each of its instances, a last row chunk of 8 rows, D != Dv,
+    # tiles cut by M and N)
     "tiled_bf16_D128_R40_ragged": Spec(B=3, Hq=10, Hk=1, Q=4, D=128, Dv=128, M=500,
                                        dtype="bf16", lengths=("uniform", 0, 495),
                                        counts=("uniform", 0, 4)),
@@ -101,6 +103,14 @@ CASES = {
                                      hot_frac=0.05, hot_scale=20.0),
     "tiled_f16_D64_Dv128_R8": Spec(B=3, Hq=8, Hk=2, Q=2, D=64, Dv=128, M=400, dtype="f16",
                                    counts=("uniform", 0, 2)),
+    # the tensor-core kernel (16-bit, 17-128 rows): 128 rows exactly with tiles
+    # cut by M and N, 17 rows (111 padding rows), hot rows
+    "tc_bf16_D64_R128_ragged": Spec(B=3, Hq=32, Hk=1, Q=4, D=64, Dv=64, M=700, dtype="bf16",
+                                    lengths=("uniform", 0, 690), counts=("uniform", 0, 4)),
+    "tc_f16_D128_R17": Spec(B=2, Hq=17, Hk=1, Q=1, D=128, Dv=128, M=300, dtype="f16",
+                            lengths=("uniform", 100, 299)),
+    "tc_bf16_D128_R32_hot": Spec(B=2, Hq=16, Hk=2, Q=4, D=128, Dv=128, M=500, dtype="bf16",
+                                 hot_frac=0.05, hot_scale=30.0),
 }
 
 
@@ -113,7 +123,8 @@ def test_backward_parity(name, seed):
 
 @pytest.mark.parametrize("which", [("context",), ("attention",), ("key_cache", "value_cache"),
                                    ()])
-@pytest.mark.parametrize("name", ["specdec_bf16_hot", "tiled_bf16_D128_R40_ragged"])
+@pytest.mark.parametrize("name", ["specdec_bf16_hot", "tiled_bf16_D128_R40_ragged",
+                                  "tiled_f16_D256_R32"])
 def test_backward_partial_gradients(which, name):
     x = workloads.generate(CASES[name], 3)
     check(x, upstream(x, 7, which))
@@ -187,7 +198,8 @@ def test_backward_decode_full_size_sampled():
 
 def test_backward_long_mqa_heads_sampled():
     """long_mqa's heads (128 query rows per KV head, D=192, Dv=128, fp16) over
-    8192 slots, B=8: the tiled kernel over 128 tiles per unit; the longest
+    8192 slots, B=8: the tensor-core kernel over 64 tiles per unit, two per
+    CTA (the query-gradient sums kept across a CTA's tiles); the longest
     batch row against the oracle (the oracle takes about a minute per batch
     row at long_mqa's full 65536 slots)."""
     spec = workloads.SPECS["long_mqa"].replace(M=8192, lengths=("uniform", 7000, 8184))
