@@ -60,26 +60,17 @@ PATH_KERNELS_READONLY = {
     path: ["attend_prep_kernel", STEP_KERNEL[path] if path != "generic" else "generic_attend_kernel",
            "finalize_merge_kernel", "attend_unpack_kernel"]
     for path in ("fused", "tensor", "decode_tc", "generic")}
-# the backward: the statistics pass (step kernel and merge, no copy), then its own four
-# (the slot kernel is bwd_kv_rows_kernel for units of <= 16 rows with D = Dv in {64, 128, 256},
-# bwd_kv_tc_kernel for 16-bit units of 17-128 rows whose widths fit tensor memory,
-# bwd_kv_tiled_kernel for other units of more than 4 rows with D and Dv multiples of 64 up to 256)
+# the backward: the statistics pass (step kernel and merge with no copy, or the tensor-core
+# step with its row writer), then its own four; kvc_backward_plan_info names the path and
+# the slot kernel ("bwd_kv_kernel" below stands for it)
 PATH_KERNELS_BACKWARD = {
-    path: [first, "finalize_merge_kernel", "bwd_rowdot_kernel", "bwd_kv_kernel",
-           "bwd_copy_kernel", "bwd_dq_kernel"]
-    for path, first in (("fused", "fused_step_kernel"), ("generic", "generic_attend_kernel"))}
+    path: first + ["bwd_rowdot_kernel", "bwd_kv_kernel", "bwd_copy_kernel", "bwd_dq_kernel"]
+    for path, first in (("fused", ["fused_step_kernel", "finalize_merge_kernel"]),
+                        ("generic", ["generic_attend_kernel", "finalize_merge_kernel"]),
+                        ("tensor", ["tc_step_kernel", "finalize_merge_kernel",
+                                    "finalize_rows_kernel"]))}
 
 
-def backward_slot_kernel(spec) -> str:
-    R = spec.Hq // spec.Hk * spec.Q
-    few = R <= 16 and spec.D == spec.Dv and spec.D in (64, 128, 256)
-    first = max(256, spec.D + spec.Dv)  # tensor-memory columns of the first products
-    tc = (not few and spec.dtype != "f32" and 16 < R <= 128 and spec.D % 64 == 0
-          and spec.Dv % 64 == 0 and max(spec.D, spec.Dv) <= 256 and first + spec.D <= 512)
-    tiled = (not few and not tc and R > 4 and spec.D % 64 == 0 and spec.Dv % 64 == 0
-             and spec.D <= 256 and spec.Dv <= 256)
-    return ("bwd_kv_rows_kernel" if few else "bwd_kv_tc_kernel" if tc else
-            "bwd_kv_tiled_kernel" if tiled else "bwd_kv_kernel")
 PATH_KERNELS = {"fused": ["fused_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "tensor": ["tc_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "generic": ["generic_copy_kernel", "generic_attend_kernel",
@@ -497,8 +488,7 @@ def run_ours(args, spec, world, rank, local):
         del out
         torch.cuda.empty_cache()
         ws = torch.empty(kvc.backward_workspace_bytes(dims), dtype=torch.uint8, device=dev)
-        path = "generic" if kvc.plan_info(dims, kc, vc, nk, nv, kc, vc)[1] == "generic" else "fused"
-        nkern = 6 if spec.Q > 0 else 2
+        nkern, path, slot_kernel = kvc.backward_plan_info(dims)
 
         def step(events=None):
             kvc.step_backward_into(dims, q, nk, nv, kc, vc, ln, mk, scale, grads, outb, ws, None,
@@ -567,12 +557,13 @@ def run_ours(args, spec, world, rank, local):
     value = world * nbytes["total"] / (ms_step * 1e-3) / 1e9
     peak, peak_src = measured_peak()
     if args.backward:  # the longer of the two HBM kernels of the gradients
-        names_b = list(PATH_KERNELS_BACKWARD[path] if nkern == 6
+        names_b = list(PATH_KERNELS_BACKWARD[path] if spec.Q > 0
                        else ["bwd_kv_kernel", "bwd_copy_kernel"])
+        assert len(names_b) == nkern, (names_b, nkern)
         ks = max((i for i, nm in enumerate(names_b) if nm in ("bwd_kv_kernel", "bwd_copy_kernel")),
                  key=lambda i: kern_ms[i])
         nbytes["fused_kernel"] = nbytes[names_b[ks]]
-        names_b = [backward_slot_kernel(spec) if nm == "bwd_kv_kernel" else nm for nm in names_b]
+        names_b = [slot_kernel if nm == "bwd_kv_kernel" else nm for nm in names_b]
         kname = names_b[ks]
     else:
         ks = (2 if args.paged and nkern > 2 else

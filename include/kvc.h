@@ -358,15 +358,28 @@ KVC_API int kvc_step_static(const kvc_dims *dims, const void *query, const void 
  *   d_key_cache / d_value_cache [B,Hk,M,D|Dv] written in full.
  *   workspace              device, >= kvc_backward_workspace_bytes(dims), 16-byte aligned.
  *
- * D and Dv at most 256 (KVC_E_SHAPE otherwise). Sums are fp32; gradients are
- * rounded to the dtype once. The outputs may not overlap any input, the
- * workspace or each other (KVC_E_ALIAS). Work is enqueued on `stream`.
+ * D and Dv at most 256 (KVC_E_SHAPE otherwise). Sums are fp32 and gradients
+ * are rounded to the dtype once, except that with 16-bit inputs and 17 to 128
+ * query rows per KV head (kvc_backward_plan_info: slot kernel
+ * "bwd_kv_tc_kernel") a and ds are also rounded to the dtype, as the
+ * tensor-core operands of dK', dV' and d_query. The outputs may not overlap
+ * any input, the workspace or each other (KVC_E_ALIAS). Work is enqueued on
+ * `stream`.
  */
 KVC_API size_t kvc_backward_workspace_bytes(const kvc_dims *dims);
+/* The kernels kvc_step_backward launches for `dims` on the current device
+ * when every buffer is 16-byte aligned: returns their number (> 0) or a
+ * negative KVC_E_* code. *stats_path (nullable) gets the statistics pass's
+ * step path ("tensor", "fused" or "generic") and *slot_kernel (nullable) the
+ * kernel of the slots below the new length ("bwd_kv_rows_kernel",
+ * "bwd_kv_tc_kernel", "bwd_kv_tiled_kernel" or "bwd_kv_kernel"); the strings
+ * are static. Launches nothing. */
+KVC_API int kvc_backward_plan_info(const kvc_dims *dims, const char **stats_path,
+                                   const char **slot_kernel);
 /* kvc_step_backward with events recorded on `stream`: one before the first
  * kernel and one after each (with query rows: the statistics pass's step
- * kernel and merge, then bwd_rowdot, bwd_kv, the tail copy and bwd_dq; the
- * rest, if any, at the end). */
+ * kernel, merge and, on the "tensor" path, row writer, then bwd_rowdot, the
+ * slot kernel, the tail copy and bwd_dq; the rest, if any, at the end). */
 KVC_API int kvc_step_backward_timed(const kvc_dims *dims, const void *query, const void *new_key,
                                     const void *new_value, const void *key_cache,
                                     const void *value_cache, const int64_t *lengths,

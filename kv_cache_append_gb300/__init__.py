@@ -9,7 +9,8 @@ from .kvc import (DEV_MASK, DEV_OVERFLOW, DEV_TIMEOUT, DTYPES, Dims, KvcError,  
                   attention_over_cache, check_inputs, default_scale, dims_of,
                   kv_cache_attention_step, kv_cache_attention_step_inplace,
                   kv_cache_attention_step_backward, kv_cache_attention_step_paged,
-                  backward_workspace_bytes, library, paged_workspace_bytes, step_backward_into,
+                  backward_plan_info, backward_workspace_bytes, library, paged_workspace_bytes,
+                  step_backward_into,
                   step_paged_into,
                   make_dims, plan_info, plan_info_inplace, selftest_wait_timeout, status_string,
                   step_inplace_into, step_into, workspace_bytes)

@@ -1077,6 +1077,9 @@ namespace {
 #endif
 struct BwdLayout {
     size_t step = 0, ctx_f32 = 0, drow = 0, dq = 0, ctx_t = 0, lengths = 0, total = 0;
+    // the tensor-core statistics pass's outputs (copied caches, attention rows)
+    size_t kscr = 0, vscr = 0, attn = 0;
+    bool tc_room = false;
 };
 bool bwd_layout(const kvc_dims& d, BwdLayout* L) {
     const size_t step = kvc_workspace_bytes(&d);
@@ -1094,11 +1097,98 @@ bool bwd_layout(const kvc_dims& d, BwdLayout* L) {
     off = align_up(off + rows * d.Dv * es, 256);
     L->lengths = static_cast<size_t>(off);
     off = align_up(off + d.B * 8, 256);
+    // shapes whose statistics pass may run the tensor-core step (16-bit, 64 to
+    // 128 rows): room for that step's outputs
+    L->tc_room = tc_shapes(d) && bwd_tc_fits((d.Hq / d.Hk) * d.Q, d.D, d.Dv);
+    if (L->tc_room) {
+        L->kscr = static_cast<size_t>(off);
+        off = align_up(off + d.B * d.Hk * d.M * d.D * es, 256);
+        L->vscr = static_cast<size_t>(off);
+        off = align_up(off + d.B * d.Hk * d.M * d.Dv * es, 256);
+        L->attn = static_cast<size_t>(off);
+        off = align_up(off + rows * d.M * es, 256);
+    }
     L->total = static_cast<size_t>(off);
     return true;
 }
+
+// The backward's kernels for these shapes on this device: the slot kernel (with
+// its shared memory) and whether the statistics pass runs the tensor-core step.
+// aligned: the inputs' and the gradient buffers' rows start on 16 bytes;
+// acc_aligned: the context gradient and the query-gradient accumulator too.
+struct BwdChoice {
+    int stage_rows = 0, rows_smem = 0, tc_smem = 0, tiled_smem = 0;
+    int64_t tc_tiles_per_cta = 1;
+    bool tc_stats = false;
+};
+BwdChoice bwd_choose(const kvc_dims& d, const DeviceInfo& dev, bool aligned, bool acc_aligned) {
+    BwdChoice c;
+    const int64_t R = (d.Hq / d.Hk) * d.Q, es = elem_size(d.dtype);
+    // the unit's rows fit the bwd_kv_kernel's shared memory?
+    const int64_t need = (3 * R + R * (2 * d.D + d.Dv)) * 4;
+    c.stage_rows = need <= dev.smem_optin ? 1 : 0;
+    // the few-rows kernel (D = Dv in {64, 128, 256})
+    const bool widths = d.D == d.Dv && (d.D == 64 || d.D == 128 || d.D == 256);
+    const int64_t rows_smem = widths ? bwd_rows_smem_bytes(R, d.D) : 0;
+    c.rows_smem = (R <= KVC_BWD_ROWS_MAX && widths && aligned && rows_smem <= dev.smem_optin)
+                      ? static_cast<int>(rows_smem) : 0;
+    // the tensor-core kernel (16-bit, 17 to 128 rows, widths that fit it)
+    const int64_t tc_smem = bwd_tc_smem_bytes(d.D, d.Dv);
+    c.tc_smem = (c.rows_smem == 0 && es == 2 && bwd_tc_fits(R, d.D, d.Dv) && aligned &&
+                 acc_aligned && tc_smem <= dev.smem_optin)
+                    ? static_cast<int>(tc_smem) : 0;
+    if (c.tc_smem > 0) {  // about two CTAs per SM over all units' tiles
+        const int64_t tiles = (d.M + 127) / 128, units = d.B * d.Hk;
+        const int64_t ctas = 2 * static_cast<int64_t>(dev.sms > 0 ? dev.sms : 1);
+        const int64_t per = (tiles * units + ctas - 1) / ctas;
+        c.tc_tiles_per_cta = per < 1 ? 1 : per;
+    }
+    // the tiled kernel (more rows; D and Dv multiples of 64 up to 256)
+    const int64_t tiled_smem = bwd_tiled_smem_bytes(d.D, d.Dv);
+    const bool tiled_widths = d.D % 64 == 0 && d.Dv % 64 == 0 && d.D <= 256 && d.Dv <= 256;
+    c.tiled_smem = (c.rows_smem == 0 && c.tc_smem == 0 && R > 4 && tiled_widths && aligned &&
+                    acc_aligned && tiled_smem <= dev.smem_optin)
+                       ? static_cast<int>(tiled_smem) : 0;
+    // with the tensor-core slot kernel (which recomputes the scores) the
+    // statistics come from the tensor-core step where that step runs
+    Plan pl;
+    c.tc_stats = c.tc_smem > 0 && tc_plan(d, dev.sms, dev.smem_optin, &pl);
+    return c;
+}
 }  // namespace
 }  // namespace kvc
+
+int kvc_backward_plan_info(const kvc_dims* dims, const char** stats_path,
+                           const char** slot_kernel) {
+    using namespace kvc;
+    const int rc = check_dims(dims);
+    if (rc != KVC_OK) return rc;
+    const kvc_dims d = *dims;
+    if (d.D > 256 || d.Dv > 256) return KVC_E_SHAPE;
+    DeviceInfo dev;
+    if (device_info(&dev) != cudaSuccess) return KVC_E_CUDA;
+    BwdLayout Lw;
+    if (!bwd_layout(d, &Lw)) return KVC_E_SHAPE;
+    const BwdChoice ch = bwd_choose(d, dev, true, true);
+    const bool hasq = d.Q > 0;
+    const char* stats = "generic";
+    int stats_kernels = hasq ? 2 : 0;  // the step kernel and the merge, with query rows
+    Plan pl;
+    if (ch.tc_stats && Lw.tc_room) {
+        stats = "tensor";
+        stats_kernels = 3;  // plus the row writer
+    } else if (fused_plan(d, dev.sms, dev.smem_optin, true, &pl, kStageTargetInplace) ||
+               fused_plan(d, dev.sms, dev.smem_optin, true, &pl, kStageTargetBytes)) {
+        stats = "fused";
+    }
+    if (stats_path) *stats_path = stats;
+    if (slot_kernel)
+        *slot_kernel = ch.rows_smem > 0 ? "bwd_kv_rows_kernel"
+                       : ch.tc_smem > 0 ? "bwd_kv_tc_kernel"
+                       : ch.tiled_smem > 0 ? "bwd_kv_tiled_kernel" : "bwd_kv_kernel";
+    // then bwd_rowdot and bwd_dq (with query rows), the slot kernel and the tail copy
+    return stats_kernels + (hasq ? 2 : 0) + 2;
+}
 
 size_t kvc_backward_workspace_bytes(const kvc_dims* dims) {
     using namespace kvc;
@@ -1160,23 +1250,49 @@ int backward_impl(const kvc_dims* dims, const void* query, const void* new_key,
         for (size_t b = a + 1; b < sizeof(out) / sizeof(out[0]); ++b)
             if (overlaps(out[a], out[b])) return KVC_E_ALIAS;
 
-    // 1. the step's statistics over the inputs, writing only the workspace
     unsigned char* ws = static_cast<unsigned char*>(workspace);
+    DeviceInfo dev;
+    if (device_info(&dev) != cudaSuccess) return KVC_E_CUDA;
+    float* dq_acc = reinterpret_cast<float*>(ws + Lw.dq);
+    const bool aligned = aligned16(query) && aligned16(new_key) && aligned16(new_value) &&
+                         aligned16(key_cache) && aligned16(value_cache) &&
+                         aligned16(d_key_cache_out) && aligned16(d_value_cache_out) &&
+                         aligned16(d_key_cache) && aligned16(d_value_cache) &&
+                         aligned16(d_new_key) && aligned16(d_new_value);
+    const BwdChoice ch = bwd_choose(d, dev, aligned, aligned16(d_context) && aligned16(dq_acc));
+    const bool tc_stats = ch.tc_stats && Lw.tc_room;
+
+    // 1. the step's statistics over the inputs: each valid row's (m, 1/l) and
+    // its fp32 context, and either its fp32 scores (the step kernels run with
+    // no cache copy and no row write) or, for the tensor-core slot kernel, its
+    // attention rows (the tensor-core step into workspace copies of its outputs)
     StepMode mode;
-    mode.inplace = true;
-    mode.rows = false;
-    mode.stats_only = true;
     mode.ctx_f32 = reinterpret_cast<float*>(ws + Lw.ctx_f32);
     StepParams p;
     mode.params_out = &p;
     // the statistics pass records one event before its kernels and one after
-    // each (the step kernel and the merge, with query rows); the gradient
-    // kernels then record one each
-    const int stats_events = events ? std::min(n_events, hasq ? 3 : 1) : 0;
-    rc = step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths, append_mask,
-                   scale, const_cast<void*>(key_cache), const_cast<void*>(value_cache),
-                   reinterpret_cast<int64_t*>(ws + Lw.lengths), nullptr, ws + Lw.ctx_t, ws,
-                   Lw.step, dev_status, stream, events, stats_events, mode);
+    // each (the step kernel, the merge and, tensor-core, the row writer, with
+    // query rows); the gradient kernels then record one each
+    int stats_events = 0;
+    if (tc_stats) {
+        mode.inplace = false;
+        mode.rows = true;
+        stats_events = events ? std::min(n_events, 4) : 0;
+        rc = step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
+                       append_mask, scale, ws + Lw.kscr, ws + Lw.vscr,
+                       reinterpret_cast<int64_t*>(ws + Lw.lengths), ws + Lw.attn, ws + Lw.ctx_t,
+                       ws, Lw.step, dev_status, stream, events, stats_events, mode);
+    } else {
+        mode.inplace = true;
+        mode.rows = false;
+        mode.stats_only = true;
+        stats_events = events ? std::min(n_events, hasq ? 3 : 1) : 0;
+        rc = step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
+                       append_mask, scale, const_cast<void*>(key_cache),
+                       const_cast<void*>(value_cache), reinterpret_cast<int64_t*>(ws + Lw.lengths),
+                       nullptr, ws + Lw.ctx_t, ws, Lw.step, dev_status, stream, events,
+                       stats_events, mode);
+    }
     if (rc != KVC_OK) return rc;
     // 2. the gradients
     BwdParams bp;
@@ -1192,41 +1308,13 @@ int backward_impl(const kvc_dims* dims, const void* query, const void* new_key,
     bp.d_key_cache = d_key_cache;
     bp.d_value_cache = d_value_cache;
     bp.drow = reinterpret_cast<float*>(ws + Lw.drow);
-    bp.dq_acc = reinterpret_cast<float*>(ws + Lw.dq);
-    {  // the unit's rows fit the bwd_kv_kernel's shared memory?
-        DeviceInfo dev;
-        const int64_t R = (d.Hq / d.Hk) * d.Q;
-        const int64_t need = (3 * R + R * (2 * d.D + d.Dv)) * 4;
-        bp.stage_rows = device_info(&dev) == cudaSuccess && need <= dev.smem_optin ? 1 : 0;
-        // the few-rows kernel (D = Dv in {64, 128, 256}, rows 16-byte aligned)
-        const bool widths = d.D == d.Dv && (d.D == 64 || d.D == 128 || d.D == 256);
-        const int64_t rows_smem = widths ? bwd_rows_smem_bytes(R, d.D) : 0;
-        const bool aligned = aligned16(query) && aligned16(new_key) && aligned16(new_value) &&
-                             aligned16(key_cache) && aligned16(value_cache) &&
-                             aligned16(d_key_cache_out) && aligned16(d_value_cache_out) &&
-                             aligned16(d_key_cache) && aligned16(d_value_cache) &&
-                             aligned16(d_new_key) && aligned16(d_new_value);
-        bp.rows_smem = (R <= KVC_BWD_ROWS_MAX && widths && aligned && rows_smem <= dev.smem_optin)
-                           ? static_cast<int>(rows_smem) : 0;
-        // the tiled kernel (more rows; D and Dv multiples of 64 up to 256, the
-        // query, context-gradient and accumulator rows 16-byte aligned too)
-        // the tensor-core kernel (16-bit, 17 to 128 rows, widths that fit it)
-        const int64_t tc_smem = bwd_tc_smem_bytes(d.D, d.Dv);
-        bp.tc_smem = (bp.rows_smem == 0 && es == 2 && bwd_tc_fits(R, d.D, d.Dv) && aligned &&
-                      aligned16(d_context) && aligned16(bp.dq_acc) && tc_smem <= dev.smem_optin)
-                         ? static_cast<int>(tc_smem) : 0;
-        if (bp.tc_smem > 0) {  // about two CTAs per SM over all units' tiles
-            const int64_t tiles = (d.M + 127) / 128, units = d.B * d.Hk;
-            const int64_t ctas = 2 * static_cast<int64_t>(dev.sms > 0 ? dev.sms : 1);
-            const int64_t per = (tiles * units + ctas - 1) / ctas;
-            bp.tc_tiles_per_cta = per < 1 ? 1 : per;
-        }
-        const int64_t tiled_smem = bwd_tiled_smem_bytes(d.D, d.Dv);
-        const bool tiled_widths = d.D % 64 == 0 && d.Dv % 64 == 0 && d.D <= 256 && d.Dv <= 256;
-        bp.tiled_smem = (bp.rows_smem == 0 && bp.tc_smem == 0 && R > 4 && tiled_widths && aligned && aligned16(d_context) &&
-                         aligned16(bp.dq_acc) && tiled_smem <= dev.smem_optin)
-                            ? static_cast<int>(tiled_smem) : 0;
-    }
+    bp.dq_acc = dq_acc;
+    bp.attn_rows = tc_stats ? ws + Lw.attn : nullptr;
+    bp.stage_rows = ch.stage_rows;
+    bp.rows_smem = ch.rows_smem;
+    bp.tc_smem = ch.tc_smem;
+    bp.tc_tiles_per_cta = ch.tc_tiles_per_cta;
+    bp.tiled_smem = ch.tiled_smem;
     bp.scale = static_cast<float>(scale);
     bp.slots_per_block = 256;
     const bool words16 = (d.D * es) % 16 == 0 && (d.Dv * es) % 16 == 0 &&

@@ -17,10 +17,13 @@
 // The host first runs the step's own kernels on the inputs without writing
 // anything (the caches are not copied, the new rows are read where they are),
 // which leaves each valid row's normaliser (m, 1/l), its fp32 scores on the
-// allowed slots and its fp32 context in the workspace. Then:
+// allowed slots and its fp32 context in the workspace. When the slot kernel is
+// the tensor-core one (which recomputes the scores) and the tensor-core step
+// takes the shape, that step runs instead, into workspace copies of its
+// outputs, leaving the attention rows in place of the scores. Then:
 //
-//   bwd_rowdot_kernel  one block per query row: D from the scores, dattention,
-//                      dcontext and the context.
+//   bwd_rowdot_kernel  one block per query row: D from the scores (or the
+//                      attention rows), dattention, dcontext and the context.
 //   the slot kernel    for every cache slot below the new length of a unit:
 //                      a_j and ds_j for each of the unit's query rows, dK'_j
 //                      and dV'_j plus the returned caches' own gradient,
@@ -62,7 +65,8 @@ __device__ __forceinline__ float ld(const void* base, int64_t i) {
 }
 
 // D for every query row, one block per row (its slots spread over the
-// block's threads, the warps' sums added in shared memory).
+// block's threads, the warps' sums added in shared memory); a_j from the fp32
+// scores, or from the attention rows when the statistics pass wrote them.
 template <typename T>
 __global__ void __launch_bounds__(kBwdWarps * 32) bwd_rowdot_kernel(const BwdParams bp) {
     __shared__ float part[kBwdWarps];
@@ -77,7 +81,10 @@ __global__ void __launch_bounds__(kBwdWarps * 32) bwd_rowdot_kernel(const BwdPar
     }
     const RowStat rs = p.rowstat[row];
     float acc = 0.f;
-    if (bp.d_attention) {
+    if (bp.d_attention && bp.attn_rows) {  // the statistics pass wrote the attention rows
+        for (int64_t j = threadIdx.x; j <= rs.lim; j += blockDim.x)
+            acc += ld<T>(bp.attn_rows, row * p.M + j) * ld<T>(bp.d_attention, row * p.M + j);
+    } else if (bp.d_attention) {
         const float* s = p.scores + row * p.M;
         for (int64_t j = threadIdx.x; j <= rs.lim; j += blockDim.x)
             acc += fast_exp2(s[j] - rs.mx) * rs.inv_l * ld<T>(bp.d_attention, row * p.M + j);

@@ -64,6 +64,8 @@ struct BwdParams {
     void* d_new_value;        // [B,Hk,Q,Dv]
     void* d_key_cache;        // [B,Hk,M,D]
     void* d_value_cache;      // [B,Hk,M,Dv]
+    const void* attn_rows;    // [B,Hq,Q,M] attention rows of the statistics pass, or null
+                              // (then a = 2^(s - m) / l from the fp32 scores)
     float* drow;              // [B*Hq*Q] scratch: sum_j a_j g_j per query row
     float* dq_acc;            // [B*Hq*Q*D] scratch: sum_j ds_j K'_j per query row
     int stage_rows;           // 1: bwd_kv_kernel stages the unit's rows in shared memory

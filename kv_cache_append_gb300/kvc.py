@@ -82,6 +82,8 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.kvc_step_inplace_timed.argtypes = inplace_args + [ctypes.POINTER(vp), i32]
             lib.kvc_plan_info_inplace.restype = i32
             lib.kvc_plan_info_inplace.argtypes = [dp] + [vp] * 4 + [ctypes.POINTER(ctypes.c_char_p)]
+            lib.kvc_backward_plan_info.restype = i32
+            lib.kvc_backward_plan_info.argtypes = [dp] + [ctypes.POINTER(ctypes.c_char_p)] * 2
             i64 = ctypes.c_int64
             attend_args = ([dp, i64, i64] + [vp] * 5 + [i32, vp, ctypes.c_double, vp, vp, sz, vp,
                                                          vp])
@@ -169,6 +171,17 @@ def plan_info_inplace(dims: Dims, key_cache, value_cache, new_key, new_value):
     if n < 0:
         raise KvcError(n, status_string(n))
     return n, name.value.decode()
+
+
+def backward_plan_info(dims: Dims):
+    """(kernel count, statistics path, slot kernel) kvc_step_backward takes
+    for these shapes with 16-byte aligned buffers."""
+    stats, slot = ctypes.c_char_p(), ctypes.c_char_p()
+    n = library().kvc_backward_plan_info(ctypes.byref(dims), ctypes.byref(stats),
+                                         ctypes.byref(slot))
+    if n < 0:
+        raise KvcError(n, status_string(n))
+    return n, stats.value.decode(), slot.value.decode()
 
 
 def _p(t: Optional[torch.Tensor]):

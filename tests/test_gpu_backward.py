@@ -114,6 +114,43 @@ CASES = {
 }
 
 
+# the slot kernel each case runs (kvc_backward_plan_info), so that every
+# kernel stays covered
+SLOT = {"tiny_fp32": "bwd_kv_kernel", "decode_bf16_ragged_M": "bwd_kv_rows_kernel",
+        "specdec_bf16_hot": "bwd_kv_rows_kernel", "chunk_fp32_Q40": "bwd_kv_tiled_kernel",
+        "mqa_fp16_D192": "bwd_kv_tc_kernel", "gqa_fp32_small_rows": "bwd_kv_kernel",
+        "generic_bf16_D5_Dv7": "bwd_kv_kernel", "mha_fp16_Dv256": "bwd_kv_kernel",
+        "rows_f16_D64_R8": "bwd_kv_rows_kernel", "rows_f32_D256_R16": "bwd_kv_rows_kernel",
+        "rows_bf16_D256_R4_ragged": "bwd_kv_rows_kernel",
+        "tiled_bf16_D128_R40_ragged": "bwd_kv_tc_kernel",
+        "tiled_f16_D256_R32": "bwd_kv_tiled_kernel",
+        "tiled_f32_D128_Dv64_R24": "bwd_kv_tiled_kernel",
+        "tiled_bf16_D64_Dv192_R18": "bwd_kv_tc_kernel",
+        "tiled_f16_D64_Dv128_R8": "bwd_kv_tiled_kernel",
+        "tc_bf16_D64_R128_ragged": "bwd_kv_tc_kernel", "tc_f16_D128_R17": "bwd_kv_tc_kernel",
+        "tc_bf16_D128_R32_hot": "bwd_kv_tc_kernel"}
+
+
+def plan_of(spec):
+    dims = kvc.make_dims(spec.B, spec.Hq, spec.Hk, spec.Q, spec.D, spec.Dv, spec.M,
+                         workloads.DTYPES[spec.dtype])
+    return kvc.backward_plan_info(dims)
+
+
+def test_backward_plan():
+    assert sorted(SLOT) == sorted(CASES)
+    for name, spec in CASES.items():
+        assert plan_of(spec)[2] == SLOT[name], name
+    # the statistics pass: the tensor-core step where the tensor-core slot
+    # kernel and the tensor-core step both take the shape (64-128 rows)
+    assert plan_of(workloads.SPECS["long_mqa"]) == (7, "tensor", "bwd_kv_tc_kernel")
+    assert plan_of(CASES["tc_bf16_D64_R128_ragged"])[:2] == (7, "tensor")
+    assert plan_of(CASES["tiled_bf16_D128_R40_ragged"])[:2] == (6, "fused")
+    assert plan_of(workloads.SPECS["chunked_append"]) == (6, "fused", "bwd_kv_tiled_kernel")
+    assert plan_of(workloads.SPECS["gqa_decode"]) == (6, "fused", "bwd_kv_rows_kernel")
+    assert plan_of(workloads.SPECS["gqa_decode"].replace(Q=0))[0] == 2
+
+
 @pytest.mark.parametrize("name", sorted(CASES))
 @pytest.mark.parametrize("seed", [0, 1])
 def test_backward_parity(name, seed):
