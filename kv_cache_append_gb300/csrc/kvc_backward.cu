@@ -350,10 +350,13 @@ __device__ __forceinline__ void lds_vec(const float* p, float (&f)[V]) {
 #ifndef KVC_BWD_ROWS_CAP
 #define KVC_BWD_ROWS_CAP 32  // NR x V up to which the registers are capped for two blocks per SM
 #endif
+#ifndef KVC_BWD_ROWS_CAP3
+#define KVC_BWD_ROWS_CAP3 16  // NR x V up to which they are capped for three blocks per SM
+#endif
 template <int NR, int V>
 struct RowsLayout {
     static constexpr bool kRegDq = NR * V <= 64;
-    static constexpr int kBlocks = NR * V <= KVC_BWD_ROWS_CAP ? 2 : 1;
+    static constexpr int kBlocks = NR * V <= KVC_BWD_ROWS_CAP3 ? 3 : NR * V <= KVC_BWD_ROWS_CAP ? 2 : 1;
     static constexpr int kWarpFloats = 2 * 32 * NR + (kRegDq ? 0 : NR * 32 * V);
     // q, dcontext and (registers case) the block's sums [NR][W]; per warp a,
     // dattention - D [32][NR] and (else) the warp's sums [NR][W]
