@@ -158,6 +158,20 @@ def test_backward_parity(name, seed):
     check(x, upstream(x, 100 + seed))
 
 
+@pytest.mark.parametrize("name", ["tc_f16_D128_R17", "tc_bf16_D64_R128_ragged", "rows_f16_D64_R8",
+                                  "tiled_f16_D256_R32", "mha_fp16_Dv256"])
+def test_backward_poisoned_tail(name):
+    """Inf keys and NaN values from each row's new length on reach no gradient
+    (every slot kernel reads only the slots below the new length)."""
+    x = workloads.generate(CASES[name], 6)
+    counts = x.append_mask.to(torch.int64).cumprod(1).sum(1)
+    for b in range(x.key_cache.shape[0]):
+        n_b = int(x.lengths[b]) + int(counts[b])
+        x.key_cache[b, :, n_b:] = float("inf")
+        x.value_cache[b, :, n_b:] = float("nan")
+    check(x, upstream(x, 8))
+
+
 @pytest.mark.parametrize("which", [("context",), ("attention",), ("key_cache", "value_cache"),
                                    ()])
 @pytest.mark.parametrize("name", ["specdec_bf16_hot", "tiled_bf16_D128_R40_ragged",
