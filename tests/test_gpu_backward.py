@@ -3,8 +3,10 @@ oracle (oracle.step_backward), and of the autograd face of
 kv_cache_attention_step.
 
 Tolerances: the kernels sum in fp32 and round each gradient to the dtype
-once, so the error is that final rounding (half an ulp: 2^-9 relative for
-bf16, 2^-12 for fp16, 2^-24 for fp32) plus fp32 summation error, bounded
+once (the tensor-core slot kernel also rounds a and ds to the dtype as its
+operands; those independent roundings keep the relative error of one), so
+the error is that rounding (half an ulp: 2^-9 relative for bf16, 2^-12 for
+fp16, 2^-24 for fp32) plus fp32 summation error, bounded
 here as |got - ref| <= rtol |ref| + atol max|ref| per tensor with
 (rtol, atol) = (8e-3, 2e-3) bf16, (2e-3, 5e-4) fp16, (1e-4, 1e-4) fp32.
 The pure routing parts are exact: cache slots from the new length on carry
