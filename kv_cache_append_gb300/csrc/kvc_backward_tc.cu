@@ -50,10 +50,16 @@ namespace {
 
 constexpr int kTJ = 128;                // slots per tile (M of the slot-major products)
 constexpr int kTR = 128;                // query rows of a unit, padded (N of S^T, G^T; M of dq)
-constexpr int kTcThreads = 256;         // 8 warps: warp w reads TMEM lanes 32 (w % 4) ..
+#ifndef KVC_BWD_TC_WARPS
+#define KVC_BWD_TC_WARPS 16  // 8 or 16
+#endif
+constexpr int kTcWarps = KVC_BWD_TC_WARPS;
+constexpr int kTcThreads = 32 * kTcWarps;  // warp w reads TMEM lanes 32 (w % 4) ..
+constexpr int kParts = kTcWarps / 4;        // warps sharing one quarter of the TMEM lanes
+constexpr int kRowsPer = kTR / kParts;      // rows of a thread in the a / ds pass
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBlk = 128 * 128;         // one 64-element column block of a 128-row operand
-constexpr int kMaxChunks = 8;           // 32-element chunks of a K' or V' row (D, Dv <= 256)
+constexpr int kMaxChunks = 16 / kParts;  // 32-column chunks of an epilogue thread (D, Dv <= 256)
 
 struct BtcLayout {
     uint32_t k, v, q, c, a, ds, stats, bar, slot, flag, total;
@@ -212,9 +218,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
         });
     };
     stage_tile(i0);
-    const int rbase = 64 * (warp >> 2);  // rows of this thread in the a / ds pass
-    const bool keys = warp < 4;          // epilogue: dK' (warps 0-3) or dV' (warps 4-7)
+    const int part = warp >> 2;               // which of the warps on these TMEM lanes
+    const int rbase = kRowsPer * part;         // rows of this thread in the a / ds pass
+    const bool keys = part < kParts / 2;       // epilogue: dK' or dV' ...
     const int W = keys ? D : Dv;
+    const int nch = W / 32 / (kParts / 2);     // ... its 32-column chunks c0 .. c0 + nch - 1
+    const int c0 = (part % (kParts / 2)) * nch;
     const T* go = static_cast<const T*>(keys ? bp.d_key_out : bp.d_value_out);
     for (int64_t it = i0; it < i1; ++it) {
         const int64_t jb = it * kTJ;
@@ -238,9 +247,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
             tc_commit(bar);
         }
         // the attention gradients of this thread's slot and rows, loaded while the products run
-        float dap[64];
+        float dap[kRowsPer];
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
+        for (int k = 0; k < kRowsPer; ++k) {
             const int r = rbase + k;
             dap[k] = (dag && j <= s_lim[r]) ? Storage<T>::to_float(dag[(row0 + r) * p.M + j]) : 0.f;
         }
@@ -252,7 +261,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
         }
         tc_fence_after();
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {  // a^T and ds^T of this thread's slot, 16 rows at a time
+        for (int g = 0; g < kRowsPer / 16; ++g) {  // a^T and ds^T of this thread's slot, 16 rows a time
             const int r0 = rbase + 16 * g;
             float sv[16], gv[16];
             tmem_ldn<16>(my_lanes + static_cast<uint32_t>(r0), sv);
@@ -313,8 +322,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
         if (live && go) {
 #pragma unroll
             for (int ch = 0; ch < kMaxChunks; ++ch)
-                if (ch * 32 < W) {
-                    const uint4* src = reinterpret_cast<const uint4*>(go + (u * p.M + j) * W + ch * 32);
+                if (ch < nch) {
+                    const uint4* src =
+                        reinterpret_cast<const uint4*>(go + (u * p.M + j) * W + (c0 + ch) * 32);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) gow[ch][k] = src[k];
                 }
@@ -336,20 +346,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
             const uint32_t base = my_lanes + (keys ? 0u : colV);
 #pragma unroll
             for (int ch = 0; ch < kMaxChunks; ++ch) {
-                if (ch * 32 >= W) continue;  // uniform over the warp
+                if (ch >= nch) continue;  // uniform over the warp
+                const int col = (c0 + ch) * 32;
                 float v[32];
-                tmem_ld32(base + static_cast<uint32_t>(ch * 32), v);  // the whole warp
+                tmem_ld32(base + static_cast<uint32_t>(col), v);  // the whole warp
                 if (live) {
                     float gf[32];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) Storage<T>::widen16(gow[ch][k], gf + 8 * k);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) v[k] = fmaf(v[k], sc, gf[k]);
-                    store32<T>(dst + ch * 32, v);
+                    store32<T>(dst + col, v);
                     if (is_new) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            reinterpret_cast<uint4*>(cache_g + ch * 32)[k] = make_uint4(0u, 0u, 0u, 0u);
+                            reinterpret_cast<uint4*>(cache_g + col)[k] = make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
             }
@@ -358,12 +369,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
         __syncthreads();  // tensor memory is free for the next tile
     }
     cp_async_wait_all();  // nothing in flight past an early exit
-    if (!failed) {  // the CTA's query-gradient sums: TMEM lane = row (warps 0-3)
+    if (!failed) {  // the CTA's query-gradient sums: TMEM lane = row, chunks split over the parts
         tc_fence_after();
-        if (warp < 4) {
+        {
             const int r = ts;
             const bool valid = r < R && (r % p.Q) < n;
-            for (int c = 0; c < D; c += 32) {
+            for (int c = 32 * part; c < D; c += 32 * kParts) {
                 float v[32];
                 tmem_ld32(my_lanes + colQ + static_cast<uint32_t>(c), v);
                 if (valid) {
