@@ -357,6 +357,10 @@ KVC_API int kvc_step_static(const kvc_dims *dims, const void *query, const void 
  *   d_new_key / d_new_value [B,Hk,Q,D|Dv] written in full (rows t >= n: 0).
  *   d_key_cache / d_value_cache [B,Hk,M,D|Dv] written in full.
  *   workspace              device, >= kvc_backward_workspace_bytes(dims), 16-byte aligned.
+ *                          For 16-bit shapes of 64 to 128 query rows per KV head whose
+ *                          widths fit the tensor-core kernels it includes room for a
+ *                          copy of both caches and the attention rows: the statistics
+ *                          pass then runs the tensor-core step into it.
  *
  * D and Dv at most 256 (KVC_E_SHAPE otherwise). Sums are fp32 and gradients
  * are rounded to the dtype once, except that with 16-bit inputs and 17 to 128
