@@ -204,10 +204,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
     const T* nv = static_cast<const T*>(p.new_value) + u * p.Q * Dv;
     uint32_t phase = 0;
     bool failed = false;
-    // the slot rows of tile i: the input cache below L, the new rows from L on, zero past N
+    // the attention gradients of a tile go through the a^T buffer (free from the
+    // previous tile's products to this tile's a / ds pass) when their rows are
+    // whole 16-byte words: [row][slot], 256 bytes a row
+    const bool stage_da =
+        dag && p.M % 8 == 0 && (reinterpret_cast<uintptr_t>(dag) & 15u) == 0;
+    const T* s_da = reinterpret_cast<const T*>(smem + Ly.a);
+    // the slot rows of tile i: the input cache below L, the new rows from L on,
+    // zero past N; with stage_da its valid rows' attention gradients too
     auto stage_tile = [&](int64_t i) {
         const int64_t jb = i * kTJ;
         const int nj = static_cast<int>(jend - jb < kTJ ? jend - jb : kTJ);
+        if (stage_da) {
+            for (int idx = tid; idx < kTR * (kTJ / 8); idx += kTcThreads) {
+                const int r = idx / (kTJ / 8), c = idx - r * (kTJ / 8);
+                if (r < R && (r % p.Q) < n && 8 * c < nj)
+                    cp_async16(smem + Ly.a + r * (kTJ * 2) + c * 16,
+                               dag + (row0 + r) * p.M + jb + 8 * c);
+            }
+        }
         stage_sw128<T>(smem + Ly.k, D, nj, [&](int t) {
             const int64_t j = jb + t;
             return j >= L ? nk + (j - L) * D : kc + j * D;
@@ -246,12 +261,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
                            smem_desc_sw128(sC + kb * kBlk + kk * 32, 16, 1024), id_s, (kb | kk) != 0);
             tc_commit(bar);
         }
-        // the attention gradients of this thread's slot and rows, loaded while the products run
+        // the attention gradients of this thread's slot and rows, read while the
+        // products run (before the barrier after which the a^T buffer is rewritten)
         float dap[kRowsPer];
 #pragma unroll
         for (int k = 0; k < kRowsPer; ++k) {
             const int r = rbase + k;
-            dap[k] = (dag && j <= s_lim[r]) ? Storage<T>::to_float(dag[(row0 + r) * p.M + j]) : 0.f;
+            dap[k] = 0.f;
+            if (dag && j <= s_lim[r])
+                dap[k] = Storage<T>::to_float(stage_da ? s_da[r * kTJ + ts] : dag[(row0 + r) * p.M + j]);
         }
         bool ok = mbar_wait(bar, phase, abort);
         phase ^= 1u;
