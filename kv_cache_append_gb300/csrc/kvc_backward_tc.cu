@@ -105,15 +105,6 @@ __device__ __forceinline__ void stage_sw128(unsigned char* dst, int W, int nvali
     }
 }
 
-// 32 consecutive elements of T from p (16-byte aligned) as floats.
-template <typename T>
-__device__ __forceinline__ void load32(const T* p, float (&f)[32]) {
-    constexpr int VE = Storage<T>::kVec16;
-#pragma unroll
-    for (int k = 0; k < 32 / VE; ++k)
-        Storage<T>::widen16(reinterpret_cast<const uint4*>(p)[k], f + k * VE);
-}
-
 // 32 floats to p (16-byte aligned) as 16-bit T.
 template <typename T>
 __device__ __forceinline__ void store32(T* p, const float (&f)[32]) {
