@@ -113,6 +113,11 @@ CASES = {
                             lengths=("uniform", 100, 299)),
     "tc_bf16_D128_R32_hot": Spec(B=2, Hq=16, Hk=2, Q=4, D=128, Dv=128, M=500, dtype="bf16",
                                  hot_frac=0.05, hot_scale=30.0),
+    # M a multiple of 8: the attention gradients staged through shared memory
+    "tc_bf16_D64_R64_staged": Spec(B=3, Hq=16, Hk=1, Q=4, D=64, Dv=64, M=520, dtype="bf16",
+                                   lengths=("uniform", 0, 515), counts=("uniform", 0, 4)),
+    "tc_f16_D128_R32_staged": Spec(B=2, Hq=8, Hk=1, Q=4, D=128, Dv=128, M=384, dtype="f16",
+                                   lengths=("uniform", 120, 379)),
 }
 
 
@@ -130,7 +135,8 @@ SLOT = {"tiny_fp32": "bwd_kv_kernel", "decode_bf16_ragged_M": "bwd_kv_rows_kerne
         "tiled_bf16_D64_Dv192_R18": "bwd_kv_tc_kernel",
         "tiled_f16_D64_Dv128_R8": "bwd_kv_tiled_kernel",
         "tc_bf16_D64_R128_ragged": "bwd_kv_tc_kernel", "tc_f16_D128_R17": "bwd_kv_tc_kernel",
-        "tc_bf16_D128_R32_hot": "bwd_kv_tc_kernel"}
+        "tc_bf16_D128_R32_hot": "bwd_kv_tc_kernel", "tc_bf16_D64_R64_staged": "bwd_kv_tc_kernel",
+        "tc_f16_D128_R32_staged": "bwd_kv_tc_kernel"}
 
 
 def plan_of(spec):
@@ -161,7 +167,7 @@ def test_backward_parity(name, seed):
 
 
 @pytest.mark.parametrize("name", ["tc_f16_D128_R17", "tc_bf16_D64_R128_ragged", "rows_f16_D64_R8",
-                                  "tiled_f16_D256_R32", "mha_fp16_Dv256"])
+                                  "tiled_f16_D256_R32", "mha_fp16_Dv256", "tc_f16_D128_R32_staged"])
 def test_backward_poisoned_tail(name):
     """Inf keys and NaN values from each row's new length on reach no gradient
     (every slot kernel reads only the slots below the new length)."""
