@@ -1,8 +1,6 @@
 """Plant plausible mistakes in a copy of the oracle's C source, build each
 mutant on the CPU, and check that at least one pin fails for every mutant.
 This shows the pins constrain the oracle, not just exercise it."""
-import os
-
 import pytest
 
 import oracle
