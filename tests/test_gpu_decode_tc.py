@@ -95,8 +95,8 @@ def test_decode_tc_paged(name, bs):
     spec = spec.replace(M=M)
     assert path_of(spec) == "decode_tc"
     x = workloads.generate(spec, 9)
-    out, status, ref, _ = run_paged(x, bs, seed=bs)
-    compare_paged(x, out, status, ref)
+    out, status, ref, table = run_paged(x, bs, seed=bs)
+    compare_paged(x, out, status, ref, table=table)
 
 
 def test_decode_tc_multi_tile_chunks_hot_rows():

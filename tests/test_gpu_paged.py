@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+import bounds
 import kv_cache_append_gb300 as kvc
 import oracle
 import workloads
@@ -49,7 +50,9 @@ def run_paged(x, bs, seed=0, table_edit=None):
     return out, int(status.item()), ref, table
 
 
-def compare_paged(x, out, status, ref, expect_flags=0):
+def compare_paged(x, out, status, ref, expect_flags=0, table=None):
+    """Pools bit for bit, lengths, flags, the absolute bars and, given the
+    block table, the per-row bounds on the logical caches read back through it."""
     assert torch.equal(_bits(out["key_cache"].cpu()), _bits(ref["key_cache"]))
     assert torch.equal(_bits(out["value_cache"].cpu()), _bits(ref["value_cache"]))
     assert torch.equal(out["lengths"].cpu(), ref["lengths"])
@@ -60,6 +63,22 @@ def compare_paged(x, out, status, ref, expect_flags=0):
                                rtol=0, atol=atol_a)
     np.testing.assert_allclose(out["context"].double().cpu().numpy(), ref["context"],
                                rtol=0, atol=atol_c)
+    if table is not None:
+        B, mb = table.shape
+        kp, vp = ref["key_cache"], ref["value_cache"]
+        _, Hk, bs, D = kp.shape
+        t = table.long().clamp(0, kp.shape[0] - 1)
+        lk = kp[t].permute(0, 2, 1, 3, 4).reshape(B, Hk, mb * bs, D)
+        lv = vp[t].permute(0, 2, 1, 3, 4).reshape(B, Hk, mb * bs, vp.shape[-1])
+        xs = workloads.StepInputs(x.query, x.new_key, x.new_value, x.key_cache, x.value_cache,
+                                  x.lengths, x.append_mask.clone(), x.options)
+        for b in range(B):   # rows the block check rejected append nothing
+            if ref["flags"][b]:
+                xs.append_mask[b] = False
+        bounds.check_step(xs, lk, lv, out["attention"].double().cpu().numpy(),
+                          out["context"].double().cpu().numpy(), ref["attention"],
+                          ref["context"], float(x.options.get("scale", kvc.default_scale(D))),
+                          "paged")
 
 
 CASES = {
@@ -81,8 +100,8 @@ def test_paged_parity(name):
     for i, bs in enumerate(sizes):
         assert spec.M % bs == 0
         x = workloads.generate(spec, 20 + i)
-        out, status, ref, _ = run_paged(x, bs, seed=i)
-        compare_paged(x, out, status, ref)
+        out, status, ref, table = run_paged(x, bs, seed=i)
+        compare_paged(x, out, status, ref, table=table)
 
 
 @pytest.mark.parametrize("name,bs", [("specdec_bf16", 16), ("tc_r128_fp16_D192", 16),
@@ -119,8 +138,8 @@ def test_paged_bad_block_ids(name, bs):
     def edit(table):
         table[1, 0] = 10 ** 6      # row 1 always needs block 0
         table[-1, -1] = -5         # the last row needs its last block only if it reaches it
-    out, status, ref, _ = run_paged(x, bs, seed=3, table_edit=edit)
-    compare_paged(x, out, status, ref, expect_flags=kvc.DEV_OVERFLOW)
+    out, status, ref, table = run_paged(x, bs, seed=3, table_edit=edit)
+    compare_paged(x, out, status, ref, expect_flags=kvc.DEV_OVERFLOW, table=table)
     assert ref["flags"][1] == 1
 
 

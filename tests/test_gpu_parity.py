@@ -4,8 +4,12 @@ seeded inputs.
 Bars: caches and lengths bit-exact; fp32 attention within 1e-5 and context
 within 1e-4 (absolute); bf16/fp16 attention within 4e-3 and context within
 2e-2 (absolute), the oracle's exact double result being the reference.
-Small cases compare every element; the full-size workloads, run in the same
-launch configuration as bench.py, compare every cache element through the
+Every comparison also applies the per-row error bounds of tests/bounds.py
+(derived from the kernels' arithmetic, relative to each row's own magnitude),
+which can fail on long rows where the absolute bars cannot, and asserts that
+wrong variants of the oracle's own output (scaled by 0.9, all zero) exceed
+them. Small cases compare every element; the full-size workloads, run in the
+same launch configuration as bench.py, compare every cache element through the
 append property and sampled batch rows against the oracle.
 """
 import hashlib
@@ -14,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import bounds
 import kv_cache_append_gb300 as kvc
 import oracle
 import workloads
@@ -63,7 +68,14 @@ def compare_full(xc: workloads.StepInputs, out, status, expect_flags=0):
     # masked / invalid entries are exactly +0
     zero = ref["attention"] == 0.0
     assert np.all(att[zero] == 0.0) and not np.any(np.signbit(att[zero]))
+    # per-row bounds relative to each row's magnitude
+    bounds.check_step(xc, ref["key_cache"], ref["value_cache"], att, ctx, ref["attention"],
+                      ref["context"], scale_of(xc))
     return ref
+
+
+def scale_of(x):
+    return float(x.options.get("scale", kvc.default_scale(x.query.shape[-1])))
 
 
 def check_append_property(x, out):
@@ -100,6 +112,15 @@ def compare_batch_rows(x, out, bsel):
     np.testing.assert_allclose(att, att_ref, rtol=0, atol=atol_a)
     np.testing.assert_allclose(ctx, ctx_ref, rtol=0, atol=atol_c)
     assert np.all(att[att_ref == 0.0] == 0.0)
+    # per-row bounds on the updated caches the step returned (already checked
+    # bit for bit against the append property)
+    xs = workloads.StepInputs(*sub, x.options)
+    upd_k = out["key_cache"].index_select(0, idx).cpu()
+    upd_v = out["value_cache"].index_select(0, idx).cpu()
+    M, Dv = att.shape[-1], ctx.shape[-1]
+    return bounds.check_step(xs, upd_k, upd_v, att.reshape(B, Hq, Q, M),
+                             ctx.reshape(B, Hq, Q, Dv), att_ref.reshape(B, Hq, Q, M),
+                             ctx_ref.reshape(B, Hq, Q, Dv), scale_of(x), "sampled")
 
 
 # ------------------------------------------------------------------ small cases
@@ -264,7 +285,26 @@ def test_full_size_workload(name):
     bsel = {int(lengths.argmax()), int(lengths.argmin()), int(counts.argmax())}
     bsel |= set(rng.choice(spec.B, size=min(3, spec.B), replace=False).tolist())
     if name == "long_mqa":
-        bsel = set(list(bsel)[:2])
+        bsel = set(sorted(bsel)[:4])
+    compare_batch_rows(x, out, bsel)
+    del out, x
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["gqa_decode", "ragged_specdec"])
+def test_full_size_workload_fp32(name):
+    """The decode shapes at full size in fp32 (the CUDA-core kernel), checked at
+    the fp32 bars (1e-5 / 1e-4) and the per-row bounds on sampled batch rows."""
+    spec = workloads.SPECS[name].replace(dtype="f32")
+    x = workloads.generate(spec, seed=3, device=DEV)
+    out, status = run_gpu(x)
+    assert status == 0
+    check_append_property(x, out)
+    lengths = x.lengths.cpu().numpy()
+    counts = x.append_mask.sum(1).cpu().numpy()
+    rng = np.random.default_rng(7)
+    bsel = {int(lengths.argmax()), int(lengths.argmin()), int(counts.argmax())}
+    bsel |= set(rng.choice(spec.B, size=3, replace=False).tolist())
     compare_batch_rows(x, out, bsel)
     del out, x
     torch.cuda.empty_cache()
