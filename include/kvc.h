@@ -313,12 +313,22 @@ KVC_API int kvc_attend_cache_timed(const kvc_dims *dims, int64_t num_slots, int6
  * workspace_bytes. Sizes whose kvc_workspace_bytes() exceeds
  * KVC_STATIC_SCRATCH_BYTES are rejected with KVC_E_STATIC_LIMIT before any
  * launch (the gqa_decode shape, B=64 Hq=32 Hk=8 Q=1 M=8192, needs about
- * 70 MB). The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture. Every call shares the one array: calls whose
- * kernels may overlap on the GPU (unordered streams) race and must not be
- * issued; calls ordered on one stream are fine. Nothing in the array needs
- * clearing between calls. Never allocates device memory.
+ * 70 MB).
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress; the lookup is repeated
+ * only when the device's context changes (e.g. after cudaDeviceReset). Under
+ * CUDA's default lazy module loading that first lookup is also when the
+ * driver commits the array, so the first call on each device needs
+ * KVC_STATIC_SCRATCH_BYTES of free device memory: make it at start-up,
+ * before the caller reserves its device memory and before any stream
+ * capture. Later calls allocate nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *
+ * Every call shares the one array, which keeps the last call's contents:
+ * calls whose kernels may overlap on the GPU (unordered streams) race and
+ * must not be issued; calls ordered on one stream are fine. The step clears
+ * what must start at zero (its work counter) on the stream at each call.
  */
 #define KVC_STATIC_SCRATCH_BYTES (96ull << 20)
 KVC_API int kvc_step_static(const kvc_dims *dims, const void *query, const void *new_key,

@@ -14,14 +14,22 @@
 //
 // Host code must not pass `g_kvc_scratch` itself to a kernel: on the host that
 // name is only a stand-in for the device array. The device address is looked
-// up once per device, with that device current, by cudaGetSymbolAddress; the
-// first kvc_step_static call on a device does this, so that first call should
-// come before any stream capture.
+// up by cudaGetSymbolAddress, with the device current, once per device
+// context: the first kvc_step_static call on a device does this set-up, so
+// that first call should come before any stream capture. Under CUDA's default
+// lazy module loading that first lookup is also when the driver commits the
+// array's memory, so the first call needs KVC_STATIC_SCRATCH_BYTES free on
+// the device; later calls allocate nothing. The set-up is keyed by the
+// context's id (cuCtxGetId, unique for the life of the process), so a context
+// rebuilt after cudaDeviceReset gets a fresh lookup instead of a stale
+// address.
 //
 // All calls share the one array and it keeps whatever the last call left in
-// it. The step writes every scratch entry it reads before reading it, so
-// nothing needs clearing. Calls whose kernels overlap on the GPU (different
-// streams, no ordering between them) race on the array.
+// it. The step writes every scratch entry it reads before reading it, except
+// its work counter, which kvc_step clears on the stream at the start of every
+// call; so nothing needs clearing here. Calls whose kernels overlap on the GPU
+// (different streams, no ordering between them) race on the array.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -34,21 +42,62 @@ constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_kvc_scratch[KVC_STATIC_SCRATCH_BYTES];
 
-std::mutex g_scratch_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchSetup {
+    unsigned long long ctx_id = 0;  // 0: not set up
+    void* addr = nullptr;
+};
 
-// Device address of g_kvc_scratch on the current device (looked up once).
+std::mutex g_scratch_mutex;
+ScratchSetup g_setup[kMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// The current context's id, through the runtime's driver entry points (no
+// libcuda link). Returns false if the driver cannot say.
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+}
+
+// Device address of g_kvc_scratch in the current device's context, looked up
+// once per context (on every call if the driver cannot name the context).
 int scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVC_E_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return KVC_E_DEVICE;
+    // binds the device's primary context to this thread (CUDA 12 and later
+    // initialise it here); allocates nothing
+    if (cudaSetDevice(dev) != cudaSuccess) return KVC_E_CUDA;
+    unsigned long long id = 0;
+    const bool known = current_context_id(&id);
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    ScratchSetup& s = g_setup[dev];
+    if (!known || s.ctx_id != id) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_kvc_scratch) != cudaSuccess || !p) return KVC_E_CUDA;
-        g_scratch_addr[dev] = p;
+        s.addr = p;
+        s.ctx_id = known ? id : 0;
     }
-    *out = g_scratch_addr[dev];
+    *out = s.addr;
     return KVC_OK;
 }
 
