@@ -662,39 +662,266 @@ def run_ours(args, spec, world, rank, local):
         line["kernels"]["merge + unpack" if args.readonly else "finalize (merge + rows)"] = {
             "ms": round(fin_ms, 4),
             "algorithmic_GBps": round(nbytes["finalize_kernel"] / (fin_ms * 1e-3) / 1e9, 1)}
+    default_face = not (args.inplace or args.paged or args.readonly or args.backward)
+    if (world == 1 and default_face and not args.no_per_config and args.batch is None
+            and args.q is None and args.dtype is None):
+        x = out = ws = q = nk = nv = kc = vc = ln = mk = step = None
+        torch.cuda.empty_cache()
+        line["per_config"] = run_per_config(args, kvc, dev, stream)
     print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- the other configs
+# Every configuration the metric is quoted per, measured in the same run as the
+# headline: (name, workload, dtype override).
+PER_CONFIG = [("tiny_fp32", "tiny_fp32", None), ("chunked_append_bf16", "chunked_append", "bf16"),
+              ("chunked_append_f32", "chunked_append", "f32"),
+              ("ragged_specdec", "ragged_specdec", None), ("long_mqa", "long_mqa", None)]
+L2_FLUSH_BYTES = 512 << 20   # written between timed steps of the L2-sized configs
+
+
+def _roofline_entry(kname, kern_ms, kbytes, key, peak, peak_src):
+    achieved = kbytes / (kern_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
+            "traffic": kernel_traffic(key, kname, kbytes)}
+
+
+def _split_kernels(step, nkern, reps, stream, dev, flush=None):
+    """Mean time of each kernel of a step: events recorded between them."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nkern + 1)] for _ in range(reps)]
+    for i in range(reps):
+        if flush is not None:
+            flush()
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    return [statistics.mean(e[k].elapsed_time(e[k + 1]) for e in evs) for k in range(nkern)]
+
+
+def _cpu_entry(spec, x_cpu, budget, what):
+    dt, rows, threads = oracle_sample(spec, x_cpu, budget)
+    sample_bytes = algorithmic_bytes(spec, rows)["total"]
+    return {"value": round(sample_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "sample": f"first {rows} of {spec.B} batch rows of {what}, one step"}
+
+
+def measure_config(kvc, name, spec, steps, warmup, dev, stream, cpu_budget, peak, peak_src):
+    """ms/step, GB/s, steps/s, the step kernel's roofline and the oracle's
+    GB/s for one configuration. Inputs larger than L2 are timed back to back;
+    smaller ones with an L2 flush (a write larger than L2) before each step,
+    events around the step only."""
+    x = workloads.generate(spec, seed=1, device=dev)
+    q, nk, nv, kc, vc, ln, mk = x.args()
+    mk = mk.view(torch.uint8)
+    scale = x.options.get("scale", kvc.default_scale(spec.D))
+    dims = kvc.dims_of(q, kc, vc)
+    out = kvc.allocate_outputs(q, kc, vc)
+    ws = torch.empty(max(1, kvc.workspace_bytes(dims)), dtype=torch.uint8, device=dev)
+    nkern, path = kvc.plan_info(dims, kc, vc, nk, nv, out["key_cache"], out["value_cache"])
+    nbytes = algorithmic_bytes(spec)
+    small = 2 * nbytes["fused_kernel"] < (128 << 20)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if small else None
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def step(events=None):
+        kvc.step_into(dims, q, nk, nv, kc, vc, ln, mk, scale, out, ws, None, stream.cuda_stream,
+                      events)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if small:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            flush()
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    else:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = a.elapsed_time(b) / steps
+    kern_ms = _split_kernels(step, nkern, min(steps, 20), stream, dev, flush if small else None)
+    kname = STEP_KERNEL[path]
+    entry = {"workload": name, "path": path, "ms_per_step": round(ms, 4),
+             "GBps": round(nbytes["total"] / (ms * 1e-3) / 1e9, 2),
+             "pct_of_8TBs": round(100.0 * nbytes["total"] / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 2),
+             "steps_per_s": round(1e3 / ms, 2), "bytes_per_step": nbytes["total"],
+             "kernels_ms": {nm: round(t, 4) for nm, t in zip(PATH_KERNELS[path], kern_ms)},
+             "roofline": _roofline_entry(kname, kern_ms[0], nbytes["fused_kernel"], name, peak,
+                                         peak_src),
+             "timed_steps": steps,
+             "l2": ("inputs smaller than L2: a 512 MB write flushes it before each timed step"
+                    if small else "inputs larger than the 129 MB L2; no flush")}
+    del x, out, ws, flush_buf
+    torch.cuda.empty_cache()
+    if cpu_budget > 0:
+        entry["cpu_baseline"] = _cpu_entry(spec, cpu_inputs(spec, seed=1), cpu_budget, name)
+    return entry
+
+
+def measure_chain(kvc, name, spec, steps, warmup, dev, stream, cpu_budget, peak, peak_src):
+    """The chunked append as the configuration defines it: three chained steps
+    (Q = 40, 32, 24), each consuming the previous step's returned caches and
+    lengths. L2 is flushed before each chain; each step is timed with events."""
+    first, rest = workloads.chain_chunks(spec, seed=1, device=dev)
+    qs = [first.query] + [r[0] for r in rest]
+    nks = [first.new_key] + [r[1] for r in rest]
+    nvs = [first.new_value] + [r[2] for r in rest]
+    mks = [first.append_mask.view(torch.uint8)] + [r[3].view(torch.uint8) for r in rest]
+    scale = first.options.get("scale", kvc.default_scale(spec.D))
+    outs, dims, plans = [], [], []
+    kc, vc, ln = first.key_cache, first.value_cache, first.lengths
+    for k in range(len(qs)):
+        d = kvc.dims_of(qs[k], kc, vc)
+        o = kvc.allocate_outputs(qs[k], kc, vc)
+        plans.append(kvc.plan_info(d, kc, vc, nks[k], nvs[k], o["key_cache"], o["value_cache"]))
+        outs.append(o)
+        dims.append(d)
+        kc, vc, ln = o["key_cache"], o["value_cache"], o["lengths"]
+    ws = torch.empty(max(kvc.workspace_bytes(d) for d in dims), dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def one(k, events=None):
+        src = {"key_cache": first.key_cache, "value_cache": first.value_cache,
+               "lengths": first.lengths} if k == 0 else outs[k - 1]
+        kvc.step_into(dims[k], qs[k], nks[k], nvs[k], src["key_cache"], src["value_cache"],
+                      src["lengths"], mks[k], scale, outs[k], ws, None, stream.cuda_stream, events)
+
+    for _ in range(warmup):
+        for k in range(len(qs)):
+            one(k)
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(qs) + 1)] for _ in range(steps)]
+    for e in ev:
+        flush_buf.fill_(1)
+        e[0].record(stream)
+        for k in range(len(qs)):
+            one(k)
+            e[k + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    per_q = {}
+    for k, Q in enumerate(workloads.CHUNKS):
+        ms = statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev)
+        nkern, path = plans[k]
+        sk = spec.replace(Q=Q)
+        nbytes = algorithmic_bytes(sk)
+
+        def step_k(events=None, k=k):
+            one(k, events)
+
+        def prep(k=k):   # the chain up to step k, after a flush
+            flush_buf.fill_(1)
+            for j in range(k):
+                one(j)
+        kern_ms = _split_kernels(step_k, nkern, min(steps, 20), stream, dev, prep)
+        kname = STEP_KERNEL[path]
+        per_q[f"Q{Q}"] = {
+            "path": path, "ms_per_step": round(ms, 4),
+            "GBps": round(nbytes["total"] / (ms * 1e-3) / 1e9, 2),
+            "steps_per_s": round(1e3 / ms, 2), "bytes_per_step": nbytes["total"],
+            "kernels_ms": {nm: round(t, 4) for nm, t in zip(PATH_KERNELS[path], kern_ms)},
+            "roofline": _roofline_entry(kname, kern_ms[0], nbytes["fused_kernel"],
+                                        f"{name}:Q{Q}", peak, peak_src)}
+    chain_ms = sum(v["ms_per_step"] for v in per_q.values())
+    entry = {"workload": "chunked_append", "dtype": spec.dtype, "chain": list(workloads.CHUNKS),
+             "per_step": per_q, "chain_ms": round(chain_ms, 4),
+             "chains_per_s": round(1e3 / chain_ms, 2), "timed_chains": steps,
+             "l2": "inputs smaller than L2: a 512 MB write flushes it before each chain",
+             "note": "L2-sized and launch-bound by design; GB/s is reported, steps/s is the figure"}
+    del outs, ws, flush_buf, first, rest
+    torch.cuda.empty_cache()
+    if cpu_budget > 0:
+        s40 = spec.replace(Q=workloads.CHUNKS[0])
+        entry["cpu_baseline"] = _cpu_entry(s40, cpu_inputs(s40, seed=1), cpu_budget,
+                                           f"{name} (the Q=40 step)")
+    return entry
+
+
+def run_per_config(args, kvc, dev, stream):
+    """Every other configuration, measured after the headline one."""
+    peak, peak_src = measured_peak()
+    budget = 0.0 if args.no_cpu_baseline else min(args.cpu_budget, 4.0)
+    res = {}
+    for name, wl, dt in PER_CONFIG:
+        if wl == args.workload and dt is None:
+            continue
+        spec = workloads.SPECS[wl] if dt is None else workloads.SPECS[wl].replace(dtype=dt)
+        slow = wl == "ragged_specdec"
+        steps = max(5, min(args.steps, 40 if slow else 200))
+        warm = max(3, min(args.warmup, 5))
+        if wl == "chunked_append":
+            res[name] = measure_chain(kvc, name, spec, steps, warm, dev, stream, budget, peak,
+                                      peak_src)
+        else:
+            res[name] = measure_config(kvc, name, spec, steps, warm, dev, stream, budget, peak,
+                                       peak_src)
+    return res
 
 
 def measure_e2e(kvc, x, dev, spec, steps, nbytes, world):
     """The public call with host buffers: every step copies the inputs from
-    pinned host memory, runs kv_cache_attention_step, copies every output back."""
+    pinned host memory, runs kv_cache_attention_step and copies every output
+    back. Two input and two output buffers alternate, the host-to-device
+    copies run on one copy stream and the device-to-host copies on another, so
+    step i+1's inputs stream in while step i's outputs stream out; every copy
+    of every step is inside the timed region."""
     host_in = [t.to("cpu").pin_memory() for t in x.args()]
     out0 = kvc.kv_cache_attention_step(*x.args(), x.options)
-    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out0.items()}
+    host_out = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out0.items()}
+                for _ in range(2)]
     del out0
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
     stream = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    dev_in = [[torch.empty_like(t, device=dev) for t in host_in] for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]     # dev_in[s] consumed by its step
+    drained = [torch.cuda.Event() for _ in range(2)]   # host_out[s] written back
+    for e in freed + drained:
+        e.record(stream)
 
-    def one():
-        args = [t.to(dev, non_blocking=True) for t in host_in]
-        out = kvc.kv_cache_attention_step(*args, x.options)
-        for k, v in out.items():
-            host_out[k].copy_(v, non_blocking=True)
+    def one(i):
+        s_ = i % 2
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(freed[s_])
+            for d, h in zip(dev_in[s_], host_in):
+                d.copy_(h, non_blocking=True)
+        stream.wait_stream(s_in)
+        out = kvc.kv_cache_attention_step(*dev_in[s_], x.options)
+        freed[s_].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_stream(stream)
+            s_out.wait_event(drained[s_])
+            for k, v in out.items():
+                host_out[s_][k].copy_(v, non_blocking=True)
+                v.record_stream(s_out)
+            drained[s_].record(s_out)
 
-    one()
+    for i in range(2):
+        one(i)
     torch.cuda.synchronize(dev)
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
     s.record(stream)
-    for _ in range(steps):
-        one()
+    for i in range(steps):
+        one(i)
+    stream.wait_stream(s_out)
     e.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(s.elapsed_time(e) / steps, world)
     return {"value": round(world * nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
-            "steps": steps}
+            "steps": steps, "copies": "double-buffered; H2D and D2H on two copy streams"}
 
 
 def measure_e2e_inplace(kvc, x, dev, steps, nbytes, world):
@@ -746,6 +973,8 @@ def main():
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure only --workload (no per_config block for the other configs)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size B (profiling captures)")
     ap.add_argument("--q", type=int, default=None,
