@@ -690,6 +690,9 @@ def _roofline_entry(kname, kern_ms, kbytes, key, peak, peak_src):
 def _split_kernels(step, nkern, reps, stream, dev, flush=None):
     """Mean time of each kernel of a step: events recorded between them."""
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nkern + 1)] for _ in range(reps)]
+    for e in [ev for row in evs for ev in row]:
+        e.record(stream)  # torch creates the CUDA event on its first record
+    torch.cuda.synchronize(dev)
     for i in range(reps):
         if flush is not None:
             flush()

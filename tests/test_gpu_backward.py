@@ -7,8 +7,9 @@ gradient to the dtype once (the tensor-core slot kernel also rounds a and ds
 to the dtype as its operands), so the error is that rounding plus sums of
 independently rounded terms: |got - ref| <= rtol |ref| + atol RMS(ref) per
 tensor (RMS over its nonzero reference entries) plus one fp16 subnormal
-spacing, with (rtol, atol) = (2^-7, 2^-6) bf16, (2^-9, 2^-9) fp16,
-(1e-4, 1e-4) fp32. Every case runs twice: with all four upstream gradients,
+spacing, with (rtol, atol) = (2^-7, 2^-5) bf16, (2^-9, 2^-8) fp16,
+(1e-4, 1e-4) fp32 (atol = 8u: the Hoeffding bound on sums of independently
+rounded 16-bit operands, lambda = 8). Every case runs twice: with all four upstream gradients,
 and with gradients reaching only attention and context, so that the
 attention-derived part of the cache gradients (about a_j * dcontext, 1e-4 on
 long rows) is bounded by its own RMS rather than hidden under the routed part

@@ -12,13 +12,15 @@ tensor with one and two row groups, generic, fp32), in place (decode
 tensor-core, fused, tensor), paged (decode tensor-core, fused, tensor),
 read-only re-attention, the gradients (each slot kernel) and the
 no-allocation entry. The guarded run's results must equal an unguarded run's
-bit for bit, so the guarded call did the real work.
+(bit for bit; the gradients, whose query sums use atomics, within their
+bound), so the guarded call did the real work.
 """
 import ctypes
 
 import pytest
 import torch
 
+import bounds
 import kv_cache_append_gb300 as kvc
 import workloads
 from test_gpu_parity import DEV, SMALL, TC, _built  # noqa: F401
@@ -245,8 +247,12 @@ def test_backward_writes_stay_in_bounds(name):
     torch.cuda.synchronize()
     assert_intact({**gi, **{"grad_" + k: v for k, v in gg.items()},
                    **{"out_" + k: v for k, v in go.items()}, "workspace": ws, "status": st})
+    # the query gradient's fp32 sums are added with atomics, so its last bit
+    # may differ between runs: compared within the gradient bound
     for k in want:
-        assert torch.equal(_bits(go[k].t), _bits(want[k])), k
+        r = bounds.grad_ratio(go[k].t.double().cpu().numpy(), want[k].double().cpu().numpy(),
+                              x.query.dtype)
+        assert r <= 1.0, (k, r)
 
 
 def test_static_entry_writes_stay_in_bounds():
