@@ -42,6 +42,7 @@ FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 _CSRC = "kv_cache_append_gb300/csrc/"
 # The first kernel of each path and the sources that define it.
 STEP_KERNEL = {"fused": "fused_step_kernel", "tensor": "tc_step_kernel",
+               "tensor_2pass": "tc_step_kernel",
                "decode_tc": "decode_tc_kernel", "generic": "generic_copy_kernel"}
 # Every kernel of a step with query rows, in launch order (in place: the
 # cache write comes first and the generic path has no copy kernel).
@@ -73,6 +74,8 @@ PATH_KERNELS_BACKWARD = {
 
 PATH_KERNELS = {"fused": ["fused_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
                 "tensor": ["tc_step_kernel", "finalize_merge_kernel", "finalize_rows_kernel"],
+                # two passes: the step kernel writes the attention rows itself
+                "tensor_2pass": ["tc_step_kernel", "finalize_merge_kernel"],
                 "generic": ["generic_copy_kernel", "generic_attend_kernel",
                             "finalize_merge_kernel", "finalize_rows_kernel"]}
 KERNEL_SOURCES = {
@@ -105,7 +108,14 @@ def algorithmic_bytes(spec: workloads.Spec, batch_rows: int | None = None) -> di
     att = B * spec.Hq * spec.Q * spec.M * es
     ctx = B * spec.Hq * spec.Q * spec.Dv * es
     fused = 2 * cache + qkv + small
-    return {"total": fused + att + ctx, "fused_kernel": fused, "finalize_kernel": att + ctx}
+    return {"total": fused + att + ctx, "fused_kernel": fused, "finalize_kernel": att + ctx,
+            "attention": att}
+
+
+def step_kernel_bytes(nbytes: dict, path: str) -> int:
+    """Algorithmic bytes of the step kernel: the copy and its inputs, plus the
+    attention rows where the step kernel writes them (the two-pass form)."""
+    return nbytes["fused_kernel"] + (nbytes.get("attention", 0) if path == "tensor_2pass" else 0)
 
 
 def algorithmic_bytes_inplace(spec: workloads.Spec, lengths, counts) -> dict:
@@ -571,6 +581,7 @@ def run_ours(args, spec, world, rank, local):
         kname = STEP_KERNEL[path]
         if args.readonly and path == "generic":
             kname = "generic_attend_kernel"
+        nbytes["fused_kernel"] = step_kernel_bytes(nbytes, path)
     fused_ms = kern_ms[ks]
     achieved = nbytes["fused_kernel"] / (fused_ms * 1e-3) / 1e9
     traffic = kernel_traffic(mode_key(args), kname, nbytes["fused_kernel"])
@@ -760,8 +771,8 @@ def measure_config(kvc, name, spec, steps, warmup, dev, stream, cpu_budget, peak
              "pct_of_8TBs": round(100.0 * nbytes["total"] / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 2),
              "steps_per_s": round(1e3 / ms, 2), "bytes_per_step": nbytes["total"],
              "kernels_ms": {nm: round(t, 4) for nm, t in zip(PATH_KERNELS[path], kern_ms)},
-             "roofline": _roofline_entry(kname, kern_ms[0], nbytes["fused_kernel"], name, peak,
-                                         peak_src),
+             "roofline": _roofline_entry(kname, kern_ms[0], step_kernel_bytes(nbytes, path), name,
+                                         peak, peak_src),
              "timed_steps": steps,
              "l2": ("inputs smaller than L2: a 512 MB write flushes it before each timed step"
                     if small else "inputs larger than the 129 MB L2; no flush")}
@@ -833,7 +844,7 @@ def measure_chain(kvc, name, spec, steps, warmup, dev, stream, cpu_budget, peak,
             "GBps": round(nbytes["total"] / (ms * 1e-3) / 1e9, 2),
             "steps_per_s": round(1e3 / ms, 2), "bytes_per_step": nbytes["total"],
             "kernels_ms": {nm: round(t, 4) for nm, t in zip(PATH_KERNELS[path], kern_ms)},
-            "roofline": _roofline_entry(kname, kern_ms[0], nbytes["fused_kernel"],
+            "roofline": _roofline_entry(kname, kern_ms[0], step_kernel_bytes(nbytes, path),
                                         f"{name}:Q{Q}", peak, peak_src)}
     chain_ms = sum(v["ms_per_step"] for v in per_q.values())
     entry = {"workload": "chunked_append", "dtype": spec.dtype, "chain": list(workloads.CHUNKS),

@@ -72,5 +72,35 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, defines, force: bool = False) -> str:
+    """libkvc_<name>.so next to libkvc.so, compiled with extra -D defines
+    (compile-time alternatives of the kernels, for tests and measurements)."""
+    lib = os.path.join(HERE, f"libkvc_{name}.so")
+    if not force and os.path.exists(lib) and all(
+            os.path.getmtime(f) <= os.path.getmtime(lib) for f in _inputs() + [__file__]):
+        return lib
+    odir = os.path.join(OBJDIR, name)
+    os.makedirs(odir, exist_ok=True)
+    nvcc = _nvcc()
+    procs, objs = [], []
+    for src in sorted(glob.glob(os.path.join(CSRC, "*.cu"))):
+        obj = os.path.join(odir, os.path.basename(src)[:-3] + ".o")
+        objs.append(obj)
+        cmd = [nvcc] + NVCC_FLAGS + [f"-D{d}" for d in defines] + ["-c", src, "-o", obj]
+        procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+    failed = []
+    for cmd, pr in procs:
+        out, _ = pr.communicate()
+        if pr.returncode:
+            sys.stdout.write(out.decode(errors="replace"))
+            failed.append(" ".join(cmd))
+    if failed:
+        raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
+    tmp = lib + f".tmp{os.getpid()}"
+    subprocess.run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs, check=True)
+    os.replace(tmp, lib)
+    return lib
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -90,6 +90,10 @@ struct Plan {
     int q_stage_bytes = 0, off_stage_q = 0;
     size_t smem = 0;
     size_t off_counter = 0, off_ml = 0, off_acc = 0, off_rowstat = 0, off_scores = 0, ws_bytes = 0;
+    // two-pass tensor-core step: per-unit first-pass counters (after the chunk
+    // counter, cleared with it) and the first pass's (max, sum) per chunk
+    bool tc_two = false;
+    size_t off_unit_done = 0, off_p1ml = 0;
 };
 
 #ifndef KVC_CHUNKS_PER_CTA
@@ -108,15 +112,22 @@ bool fused_shapes(const kvc_dims& d) {
     return (d.D * es) % 16 == 0 && (d.Dv * es) % 16 == 0 && d.D * es <= 512 && d.Dv <= 256;
 }
 
-// Workspace: chunk counter | partial (max, sum) | partial weighted values |
-// attention-row inputs, either fp32 scores or fp16 2^(score - tile max) plus
-// one fp32 tile maximum per (row, 64 slots); the region fits both.
+bool two_pass_shapes(const kvc_dims& d);
+
+// Workspace: chunk counter | (two-pass shapes: one counter per unit) |
+// partial (max, sum) | partial weighted values | attention-row inputs, either
+// fp32 scores or fp16 2^(score - tile max) plus one fp32 tile maximum per
+// (row, 64 slots); the region fits both | (two-pass shapes: the first pass's
+// (max, sum) per chunk).
 void workspace_layout(const kvc_dims& d, int64_t KP, Plan* pl) {
     const int64_t U = d.B * d.Hk, R = (d.Hq / d.Hk) * d.Q;
     const int64_t rows = d.B * d.Hq * d.Q;
+    const bool two = two_pass_shapes(d);
     int64_t off = 0;
     pl->off_counter = static_cast<size_t>(off);
     off = 256;
+    pl->off_unit_done = static_cast<size_t>(off);
+    if (two) off = align_up(off + U * 4, 256);
     pl->off_ml = static_cast<size_t>(off);
     off = align_up(off + U * KP * R * 2 * 4, 256);
     pl->off_acc = static_cast<size_t>(off);
@@ -128,6 +139,8 @@ void workspace_layout(const kvc_dims& d, int64_t KP, Plan* pl) {
     pl->off_tile_max = static_cast<size_t>(off + fp16_part);
     const int64_t fmt1 = fp16_part + rows * ((d.M + 63) / 64) * 4;
     off = align_up(off + std::max<int64_t>(rows * d.M * 4, fmt1), 256);
+    pl->off_p1ml = static_cast<size_t>(off);
+    if (two) off = align_up(off + U * KP * R * 2 * 4, 256);
     pl->ws_bytes = static_cast<size_t>(off);
 }
 
@@ -269,6 +282,27 @@ bool tc_shapes(const kvc_dims& d) {
     return d.dtype != KVC_F32 && d.D % 64 == 0 && d.D <= 256 && d.Dv % 64 == 0 && d.Dv <= 256 &&
            d.Dv + d.D / 2 <= 320 && d.Q >= 1 && R >= KVC_TC_MIN_ROWS && R <= 256 &&
            d.B * d.Hk < (int64_t(1) << 31);
+}
+
+// The two-pass tensor-core step (kvc_fused_tc.cu) is built only with
+// -DKVC_TC_TWO_PASS=1: on one GB300 it measured slower than the one-pass step
+// with stored P rows (long_mqa: 0.235 ms per step against 0.208 ms), because
+// the tensor-core pipeline is bound per tile, not by DRAM bytes, and the key
+// pass adds a tile for every 64 allowed slots. KVC_TC_DIST: units between a
+// unit's first and second pass in the hand-out order (8 measured best).
+#ifndef KVC_TC_TWO_PASS
+#define KVC_TC_TWO_PASS 0
+#endif
+#ifndef KVC_TC_DIST
+#define KVC_TC_DIST 8
+#endif
+// Shapes the two-pass tensor-core step takes (out of place, with attention
+// rows, 16-byte aligned attention): one row group (at most 128 query rows per
+// unit), and attention rows whose pitch is a whole number of 16-byte words
+// (the kernel stores them by TMA).
+bool two_pass_shapes(const kvc_dims& d) {
+    const int64_t R = (d.Hq / d.Hk) * d.Q;
+    return KVC_TC_TWO_PASS && tc_shapes(d) && R <= 128 && d.M % 8 == 0;
 }
 
 void tc_tiling(const kvc_dims& d, Plan* pl) {
@@ -441,6 +475,9 @@ struct StepMode {
     // the inputs and write nothing but the workspace: no cache row write, the
     // CUDA-core or generic path only (fp32 scores), the context also in fp32
     bool stats_only = false;
+    // the two-pass tensor-core step may be taken (the backward's statistics
+    // pass keeps the one-pass form, whose kernels its event list names)
+    bool two_pass = true;
     float* ctx_f32 = nullptr;
     StepParams* params_out = nullptr;  // receives the parameters the kernels ran with
 };
@@ -491,6 +528,12 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
            fused_plan(d, dev.sms, dev.smem_optin, aligned16(query), &pl, kStageTargetBytes))))
         generic_plan(d, &pl);
 
+    if (pl.tensor && mode.two_pass && two_pass_shapes(d) && !inplace && !paged && !mode.readonly &&
+        mode.rows && hasq && aligned16(out_attention)) {
+        pl.tc_two = true;
+        pl.NQ = 2 * d.B * d.Hk * pl.KP;  // every chunk once per pass
+        pl.P = std::min<int64_t>(dev.sms, pl.NQ);
+    }
     if (pl.ws_bytes > 0) {
         if (!workspace || workspace_bytes < pl.ws_bytes || !aligned16(workspace))
             return KVC_E_WORKSPACE;
@@ -565,6 +608,12 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     p.tc_nrg = pl.tc_nrg;
     p.tc_stg_bytes = pl.tc_stg_bytes;
     p.tc_tmem_cols = pl.tc_tmem_cols;
+    p.tc_two_pass = pl.tc_two ? 1 : 0;
+    p.tc_dist = std::min<int64_t>(KVC_TC_DIST, d.B * d.Hk);
+    if (pl.tc_two) {
+        p.unit_done = reinterpret_cast<unsigned int*>(ws + pl.off_unit_done);
+        p.part1_ml = reinterpret_cast<float*>(ws + pl.off_p1ml);
+    }
     p.dec_off_red = pl.dec_off_red;
     p.dec_off_pt = pl.dec_off_pt;
     p.ctx_f32 = mode.ctx_f32;
@@ -614,7 +663,17 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
                 !rows_map(&tp.tm_acc, p.part_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d.Dv, d.Dv,
                           p.R, d.B * d.Hk * p.KP, 32, static_cast<int>(std::min<int64_t>(p.R, 128))))
                 return KVC_E_CUDA;
-            e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream);
+            if (pl.tc_two &&
+                !rows_map(&tp.tm_att, out_attention,
+                          d.dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          2, d.M, d.M, p.R, d.B * d.Hk, 64, static_cast<int>(p.R)))
+                return KVC_E_CUDA;
+            // the chunk counter (and, two-pass, the units' first-pass counters)
+            e = cudaMemsetAsync(p.counter, 0,
+                                pl.tc_two ? pl.off_unit_done + static_cast<size_t>(d.B * d.Hk) * 4
+                                          : sizeof(unsigned int),
+                                stream);
             if (e == cudaSuccess) e = launch_fused_tc(tp, d.dtype, pl.smem, stream);
             if (e == cudaSuccess) e = record();
         } else if (pl.dec) {
@@ -655,7 +714,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
         if (e == cudaSuccess && hasq) {
             e = launch_finalize_merge(p, d.dtype, stream);
             if (e == cudaSuccess) e = record();
-            if (e == cudaSuccess && mode.rows) {
+            if (e == cudaSuccess && mode.rows && !pl.tc_two) {  // (two-pass: written already)
                 e = launch_finalize_rows(p, d.dtype, stream);
                 if (e == cudaSuccess) e = record();
             }
@@ -962,9 +1021,11 @@ int kvc_plan_info(const kvc_dims* dims, const void* key_cache, const void* value
                               (!hasq || (aligned16(new_key) && aligned16(new_value)));
     Plan pl;
     // the step kernel(s), then (with query rows) the merge and the row writer
+    // (the two-pass tensor-core step writes the attention rows itself)
     if (ptrs_aligned && tc_plan(*dims, dev.sms, dev.smem_optin, &pl)) {
-        if (path_name) *path_name = "tensor";
-        return 3;
+        const bool two = two_pass_shapes(*dims) && out_key_cache != key_cache;
+        if (path_name) *path_name = two ? "tensor_2pass" : "tensor";
+        return two ? 2 : 3;
     }
     const bool fused = ptrs_aligned && fused_plan(*dims, dev.sms, dev.smem_optin, true, &pl);
     if (path_name) *path_name = fused ? "fused" : "generic";
@@ -1277,6 +1338,7 @@ int backward_impl(const kvc_dims* dims, const void* query, const void* new_key,
     if (tc_stats) {
         mode.inplace = false;
         mode.rows = true;
+        mode.two_pass = false;
         stats_events = events ? std::min(n_events, 4) : 0;
         rc = step_impl(dims, query, new_key, new_value, key_cache, value_cache, lengths,
                        append_mask, scale, ws + Lw.kscr, ws + Lw.vscr,

@@ -43,6 +43,21 @@
 // Tensor memory (512 columns x 128 lanes, fp32 words): S0 [0, 64), S1 [64,
 // 128), O [128, 128 + Dv), Q [128 + Dv, + D/2) as packed 16-bit pairs, P0 and
 // P1 32 columns each after Q.
+//
+// Two-pass form (one row group, out of place, TWO = true). Writing the P rows
+// and reading them back to normalise them costs twice the attention rows'
+// bytes; instead every unit is worked twice. The first pass reads only the
+// unit's key prefix (the tiles below its new length), computes S = Q K^T and
+// keeps each row's running maximum and sum per chunk. The second pass is the
+// copy + attention above, but with each row's final maximum and sum known: it
+// writes the normalised attention rows 2^(s - m) / l straight to the output
+// (zero rows for the tiles past the new length) and the context partials,
+// and no row is rescaled. Units are handed out in waves (the first pass of
+// unit u + dist, then the second pass of unit u), so the second pass finds
+// the unit's keys, loaded a little earlier with the evict_last L2 policy,
+// still in L2, while the streamed copy uses evict_first. A second-pass chunk
+// waits (bounded) until every first-pass chunk of its unit has finished;
+// those were handed out earlier to CTAs that are running, so the wait ends.
 #include <cuda.h>
 
 #include <type_traits>
@@ -64,6 +79,13 @@ constexpr int kTcThreads = 7 * 32;
 constexpr float kRescale = 8.f;           // raise the reference max when exceeded by 2^8
 constexpr int kRgShift = 8;               // TileMeta flags bits 8..: the tile's row group
 constexpr int kRgRows = 128;              // query rows per row group (one product row each)
+#ifndef KVC_TC_PREFETCH
+#define KVC_TC_PREFETCH 0
+#endif
+// The producer asks L2 for the tile this many tiles ahead of the one it
+// loads (within the chunk), so that the loads into the few shared-memory
+// stages find their data in L2 instead of waiting the full DRAM latency.
+constexpr int kPrefetchTiles = KVC_TC_PREFETCH;
 
 struct TcBars {
     uint32_t base;
@@ -110,16 +132,55 @@ __device__ __forceinline__ PatchRange patch_range(const TileMeta& mt, const Step
         r.a = max(mt.L, j0);
         r.c = min(N, j1);
     }
-    if (mt.n > 0 && j0 < N && N < j1) {
+    if (mt.n > 0 && j0 < N && N < j1 && !(mt.flags & kPass1)) {
         r.za = N;
         r.zc = j1;
     }
     return r;
 }
 
+// Two-pass hand-out order: group g of KP chunks is (pass, unit): the first
+// pass of units [0, dist), then alternately the first pass of unit dist + i
+// and the second pass of unit i, then the second passes of the last dist units.
+__device__ __forceinline__ void two_pass_group(int64_t g, int64_t U, int64_t dist, bool* pass1,
+                                               int64_t* u) {
+    if (g < dist) {
+        *pass1 = true;
+        *u = g;
+        return;
+    }
+    const int64_t m = g - dist;
+    if (m < 2 * (U - dist)) {
+        *pass1 = (m & 1) == 0;
+        *u = *pass1 ? dist + (m >> 1) : (m >> 1);
+        return;
+    }
+    *pass1 = false;
+    *u = g - U;
+}
+
+// First-pass chunks of a unit of new length N (tiles below N, CH per chunk).
+__device__ __forceinline__ int64_t pass1_chunks(const StepParams& p, int64_t n, int64_t N) {
+    if (n <= 0) return 0;
+    const int64_t tiles = min(p.TPU, (N + kTcT - 1) / kTcT);
+    return (tiles + p.CH - 1) / p.CH;
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* a) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add_u32(unsigned int* a, unsigned int v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+template <bool TWO>
 __device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars,
                             volatile int* abort) {
     const StepParams& p = tp.p;
+    const uint64_t pol_first = TWO ? l2_policy_evict_first() : 0;
+    const uint64_t pol_last = TWO ? l2_policy_evict_last() : 0;
     const uint32_t stage0 = smem_addr(smem + p.off_stages);
     TileMeta* meta = reinterpret_cast<TileMeta*>(smem + p.off_meta);
     const int nkb = static_cast<int>(p.D / 64), nvb = static_cast<int>(p.Dv / 64);
@@ -131,15 +192,36 @@ __device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars
     while (ok) {
         const int64_t q = atomicAdd(p.counter, 1u);
         if (q >= p.NQ) break;
-        const int64_t idx = chunk_of(q, p.NQ);  // chunk k of (unit u, row group rg)
-        const int64_t UG = U * p.tc_nrg;
-        const int64_t k = idx / UG, ug = idx - k * UG;
-        const int64_t u = ug / p.tc_nrg, rg = ug - u * p.tc_nrg;
+        int64_t u, rg = 0, k;
+        bool pass1 = false;
+        if (TWO) {
+            const int64_t g = q / p.KP;
+            k = q - g * p.KP;
+            two_pass_group(g, U, p.tc_dist, &pass1, &u);
+        } else {
+            const int64_t idx = chunk_of(q, p.NQ);  // chunk k of (unit u, row group rg)
+            const int64_t UG = U * p.tc_nrg;
+            k = idx / UG;
+            const int64_t ug = idx - k * UG;
+            u = ug / p.tc_nrg;
+            rg = ug - u * p.tc_nrg;
+        }
         const Unit x = load_unit(p, u);
-        // in place, tiles from the new length on are neither read nor written
-        const int64_t iend = !p.inplace ? p.TPU : x.n > 0 ? min(p.TPU, (x.N + kTcT - 1) / kTcT) : 0;
+        // in place, tiles from the new length on are neither read nor written;
+        // a first pass reads only the tiles below the new length
+        const int64_t below = x.n > 0 ? min(p.TPU, (x.N + kTcT - 1) / kTcT) : 0;
+        const int64_t iend = (!p.inplace && !pass1) ? p.TPU : below;
         const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, iend);
         if (i0 >= i1) continue;
+        const int zc = static_cast<int>(cache_unit(p, u));
+        auto prefetch = [&](int64_t i) {  // the tile's boxes into L2 (not paged)
+            const int y = static_cast<int>(i * kTcT);
+            for (int b = 0; b < nkb; ++b) tma_prefetch_3d(&tp.tm_k, 64 * b, y, zc);
+            if (!pass1)
+                for (int b = 0; b < nvb; ++b) tma_prefetch_3d(&tp.tm_v, 64 * b, y, zc);
+        };
+        if (kPrefetchTiles > 0 && !p.block_table)
+            for (int64_t i = i0; i < min(i1, i0 + kPrefetchTiles); ++i) prefetch(i);
         if (x.n > 0 && i0 * kTcT < x.L + x.n) {  // the softmax warps load these rows at the chunk start
             const int64_t r0 = rg * kRgRows, nr = min(static_cast<int64_t>(kRgRows), p.R - r0);
             bulk_prefetch_l2(static_cast<const unsigned char*>(p.query) + (u * p.R + r0) * p.D * p.es,
@@ -157,10 +239,23 @@ __device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars
             mt.i = static_cast<int32_t>(i);
             mt.k = static_cast<int32_t>(k);
             mt.flags = (i == i0 ? kFirst : 0) | (i == i1 - 1 ? kLast : 0) |
-                       static_cast<int32_t>(rg << kRgShift);
+                       (pass1 ? kPass1 : 0) | static_cast<int32_t>(rg << kRgShift);
             const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
             const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBox);
-            if (!p.block_table) {
+            if (TWO) {
+                // first pass: the keys, kept in L2 for the second pass; second
+                // pass: keys (their last use) and values, streamed
+                const int y = static_cast<int>(i * kTcT), z = static_cast<int>(u);
+                mbar_arrive_expect_tx(bars.full(ring.s),
+                                      pass1 ? static_cast<uint32_t>(nkb * kBox) : tile_bytes);
+                for (int b = 0; b < nkb; ++b)
+                    tma_load_3d_hint(sK + b * kBox, &tp.tm_k, 64 * b, y, z, bars.full(ring.s),
+                                     pass1 ? pol_last : pol_first);
+                if (!pass1)
+                    for (int b = 0; b < nvb; ++b)
+                        tma_load_3d_hint(sV + b * kBox, &tp.tm_v, 64 * b, y, z, bars.full(ring.s),
+                                         pol_first);
+            } else if (!p.block_table) {
                 mbar_arrive_expect_tx(bars.full(ring.s), tile_bytes);  // publishes the metadata too
                 const int y = static_cast<int>(i * kTcT), z = static_cast<int>(cache_unit(p, u));
                 for (int b = 0; b < nkb; ++b)
@@ -187,6 +282,8 @@ __device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars
                         tma_load_3d(sV + b * kBox + o, &tp.tm_v, 64 * b, y, z, bars.full(ring.s));
                 }
             }
+            if (kPrefetchTiles > 0 && !p.block_table && i + kPrefetchTiles < i1)
+                prefetch(i + kPrefetchTiles);
             ++issued;
             ring.next(p.NS);
         }
@@ -203,9 +300,11 @@ __device__ void tc_producer(const TcParams& tp, unsigned char* smem, TcBars bars
 }
 
 // Whole warp: patch the new rows into the swizzled tile, then (lane 0) store it.
+template <bool TWO>
 __device__ void tc_storer(const TcParams& tp, unsigned char* smem, TcBars bars,
                           volatile int* abort) {
     const StepParams& p = tp.p;
+    const uint64_t pol_first = TWO ? l2_policy_evict_first() : 0;
     const int lane = threadIdx.x & 31;
     const uint32_t stage0 = smem_addr(smem + p.off_stages);
     const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
@@ -228,7 +327,9 @@ __device__ void tc_storer(const TcParams& tp, unsigned char* smem, TcBars bars,
         unsigned char* tV = tK + nkb * kBox;
         const int64_t j0 = static_cast<int64_t>(mt.i) * kTcT;
         const PatchRange pr = patch_range(mt, p);
-        const bool store = (mt.flags >> kRgShift) == 0 && !p.inplace;  // other row groups read it too
+        // other row groups read it too; a first-pass tile holds only keys
+        const bool pass1 = (mt.flags & kPass1) != 0;
+        const bool store = (mt.flags >> kRgShift) == 0 && !p.inplace && !pass1;
         bool committed = false;
         if (pr.c > pr.a) {
             const int rows = static_cast<int>(pr.c - pr.a);
@@ -240,7 +341,7 @@ __device__ void tc_storer(const TcParams& tp, unsigned char* smem, TcBars bars,
                 *reinterpret_cast<uint4*>(tK + (ch >> 3) * kBox + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
                     *reinterpret_cast<const uint4*>(nku + rr * rowK + ch * 16);
             }
-            for (int e = lane; e < rows * ckV; e += 32) {
+            for (int e = lane; e < (pass1 ? 0 : rows * ckV); e += 32) {
                 const int rr = e / ckV, ch = e - rr * ckV;
                 const int r = static_cast<int>(pr.a - j0) + rr;
                 *reinterpret_cast<uint4*>(tV + (ch >> 3) * kBox + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
@@ -252,8 +353,15 @@ __device__ void tc_storer(const TcParams& tp, unsigned char* smem, TcBars bars,
         auto store_tile = [&]() {  // lane 0: the tile to the output caches, one bulk group
             if (store) {
                 const int y = static_cast<int>(j0), z = static_cast<int>(mt.u);
-                for (int b = 0; b < nkb; ++b) tma_store_3d(&tp.tm_ok, 64 * b, y, z, sK + b * kBox);
-                for (int b = 0; b < nvb; ++b) tma_store_3d(&tp.tm_ov, 64 * b, y, z, sV + b * kBox);
+                if (TWO) {
+                    for (int b = 0; b < nkb; ++b)
+                        tma_store_3d_hint(&tp.tm_ok, 64 * b, y, z, sK + b * kBox, pol_first);
+                    for (int b = 0; b < nvb; ++b)
+                        tma_store_3d_hint(&tp.tm_ov, 64 * b, y, z, sV + b * kBox, pol_first);
+                } else {
+                    for (int b = 0; b < nkb; ++b) tma_store_3d(&tp.tm_ok, 64 * b, y, z, sK + b * kBox);
+                    for (int b = 0; b < nvb; ++b) tma_store_3d(&tp.tm_ov, 64 * b, y, z, sV + b * kBox);
+                }
             }
             bulk_commit();  // (an empty group for a tile it does not store)
         };
@@ -368,6 +476,7 @@ __device__ void tc_mma_issuer(const TcParams& tp, unsigned char* smem, TcBars ba
                 if (!mbar_wait(bars.q_ready(), q_ph, abort)) break;
                 q_ph ^= 1u;
             }
+            const bool pass1 = (mt.flags & kPass1) != 0;
             if (s_uses[sbuf] > 0 &&
                 !mbar_wait(bars.s_free(sbuf), static_cast<uint32_t>((s_uses[sbuf] - 1) & 1), abort))
                 break;
@@ -384,6 +493,10 @@ __device__ void tc_mma_issuer(const TcParams& tp, unsigned char* smem, TcBars ba
             tc_commit(bars.s_ready(sbuf));
             ++s_uses[sbuf];
             sbuf ^= 1;
+            if (pass1) {  // keys only: the stage is free once S is
+                tc_commit(bars.empty(s));
+                continue;
+            }
             if (has_pending && !issue_pv(pend_stage, pend_first)) break;
             has_pending = true;
             pend_stage = s;
@@ -409,7 +522,7 @@ __device__ void tc_mma_issuer(const TcParams& tp, unsigned char* smem, TcBars ba
     mbar_wait(bars.drained(), 0u, &never);
 }
 
-template <typename T>
+template <typename T, bool TWO>
 __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
                            volatile int* abort, uint32_t tmem) {
     const StepParams& p = tp.p;
@@ -436,6 +549,9 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
     int lim = -1;
     bool valid = false;
     float m_ref = -INFINITY, l = 0.f;
+    float inv_l = 0.f;  // two-pass, second pass: 1 / the row's final sum
+    bool pass1 = false;
+    const uint64_t pol_first = TWO ? l2_policy_evict_first() : 0;
 
     // Wait until product c (which read P[c % 2]) has finished, consuming the
     // completions of that buffer's barrier strictly in order.
@@ -472,7 +588,11 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
         if (r == 0) {
             ok = mbar_wait(bars.stg_full(b), static_cast<uint32_t>((use >> 1) & 1), abort);
             if (ok) {
-                tma_store_3d(map, x, rbase, z, stg_addr + static_cast<uint32_t>(b * p.tc_stg_bytes));
+                if (TWO)
+                    tma_store_3d_hint(map, x, rbase, z,
+                                      stg_addr + static_cast<uint32_t>(b * p.tc_stg_bytes), pol_first);
+                else
+                    tma_store_3d(map, x, rbase, z, stg_addr + static_cast<uint32_t>(b * p.tc_stg_bytes));
                 bulk_commit();
                 if (use >= 1) {  // the previous round's store has read its buffer
                     bulk_wait_read(1);
@@ -482,6 +602,36 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
         }
         ++use;
         return w != 0 || __shfl_sync(0xffffffffu, ok, 0);
+    };
+    // Two-pass: lane 0 waits until unit uu's first pass has finished (every
+    // softmax warp of each of its first-pass chunks counted), bounded like
+    // every other wait; then each lane takes its own acquire of the count.
+    auto wait_unit = [&](int64_t uu, unsigned int target) -> bool {
+        int okw = 1;
+        if (lane == 0) {
+            unsigned long long t0 = 0;
+            for (uint32_t it = 0; ld_acquire_u32(p.unit_done + uu) < target; ++it) {
+                if ((it & 15u) == 15u) {
+                    if (*abort) {
+                        okw = 0;
+                        break;
+                    }
+                    const unsigned long long now = global_ns();
+                    if (t0 == 0) {
+                        t0 = now;
+                    } else if (now - t0 > kWaitLimitNs) {
+                        *abort = 1;
+                        okw = 0;
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+            }
+        }
+        __syncwarp();
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (okw) (void)ld_acquire_u32(p.unit_done + uu);
+        return okw != 0;
     };
 
     bool ok = true;
@@ -499,12 +649,13 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
             L = mt.L;
             n = mt.n;
             N = L + n;
+            pass1 = TWO && (mt.flags & kPass1) != 0;
             attend = n > 0 && static_cast<int64_t>(mt.i) * kTcT < N;
             const int rg = mt.flags >> kRgShift;
             rbase = rg * kRgRows;
             Rg = min(kRgRows, R - rbase);
             const int64_t b = u / p.Hk, kv = u - b * p.Hk;
-            if (k == 0 && kv == 0 && rg == 0 && r == 0 && !p.inplace) {
+            if (k == 0 && kv == 0 && rg == 0 && r == 0 && !p.inplace && !pass1) {
                 const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
                 p.out_lengths[b] = ra.L + ra.n;
                 if (ra.flags && p.dev_status) atomicOr(p.dev_status, ra.flags);
@@ -537,10 +688,85 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
                 m_ref = -INFINITY;
                 l = 0.f;
                 first_tile = true;
+                if (TWO && !pass1) {
+                    // the row's final maximum and sum from its unit's first pass
+                    const unsigned int target =
+                        static_cast<unsigned int>(kSoftWarps * pass1_chunks(p, n, N));
+                    if (!wait_unit(u, target)) break;
+                    m_ref = 0.f;
+                    inv_l = 0.f;
+                    if (valid) {
+                        const int64_t kmax = min(p.KP, lim / (p.CH * kTcT) + 1);
+                        const float* ml = p.part1_ml + 2 * (u * p.KP * p.R + r);
+                        float mx = -INFINITY;
+                        for (int64_t kk = 0; kk < kmax; ++kk)
+                            mx = fmaxf(mx, __ldcg(ml + 2 * kk * p.R));
+                        float ls = 0.f;
+                        for (int64_t kk = 0; kk < kmax; ++kk)
+                            ls = fmaf(__ldcg(ml + 2 * kk * p.R + 1),
+                                      fast_exp2(__ldcg(ml + 2 * kk * p.R) - mx), ls);
+                        m_ref = mx;
+                        inv_l = 1.f / ls;
+                    }
+                }
             }
         }
         const bool is_comp = attend && static_cast<int64_t>(mt.i) * kTcT < N;
-        if (is_comp) {
+        if (TWO && pass1) {
+            // first pass: the row's running maximum and sum over the tile
+            if (is_comp) {
+                if (!warp_wait(bars.s_ready(sbuf), static_cast<uint32_t>((sbuf ? su1 : su0) & 1),
+                               abort))
+                    break;
+                if (sbuf) ++su1; else ++su0;
+                tc_fence_after();
+                float sv[kTcT];
+                tmem_ld32(trow + sbuf * kTcT, sv);
+                tmem_ld32(trow + sbuf * kTcT + 32, sv + 32);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.s_free(sbuf), 1u);
+                sbuf ^= 1;
+                const int j0 = mt.i * kTcT;
+                const bool none = j0 > lim;
+                if (!none) {
+                    if (j0 + kTcT - 1 > lim) {
+#pragma unroll
+                        for (int c = 0; c < kTcT; ++c)
+                            if (j0 + c > lim) sv[c] = -INFINITY;
+                    }
+                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int c = 0; c < kTcT; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+                    const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * qs;
+                    if (tmax > m_ref + kRescale) {
+                        if (m_ref != -INFINITY) l *= fast_exp2(m_ref - tmax);
+                        m_ref = tmax;
+                    }
+                    const float negm = -m_ref;
+                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int c = 0; c < kTcT; ++c) ls[c & 3] += fast_exp2(fmaf(sv[c], qs, negm));
+                    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                }
+            }
+            if ((mt.flags & kLast) && attend) {
+                // this chunk's (max, sum) per row, then count the warp's part done
+                if (valid) {
+                    float* ml = p.part1_ml + 2 * ((u * p.KP + k) * p.R + rbase + r);
+                    ml[0] = m_ref;
+                    ml[1] = l;
+                }
+                __syncwarp();
+                if (lane == 0) red_release_add_u32(p.unit_done + u, 1u);
+            }
+            continue;
+        }
+        if (TWO && !is_comp) {
+            // second pass, no allowed slot in the tile for any row: zero attention rows
+            const uint32_t zw[32] = {};
+            if (!stage(zw, &tp.tm_att, mt.i * kTcT, static_cast<int>(u))) break;
+        } else if (is_comp) {
             if (!warp_wait(bars.s_ready(sbuf), static_cast<uint32_t>((sbuf ? su1 : su0) & 1), abort))
                 break;
             if (sbuf) ++su1; else ++su0;
@@ -555,7 +781,10 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
             // causal limit: slots j <= lim count; the scale is applied through qs > 0
             const int j0 = mt.i * kTcT;
             const bool none = j0 > lim;
-            if (!__all_sync(0xffffffffu, j0 + kTcT - 1 <= lim || none)) {
+            // (the two-pass kernel writes every row's attention from here: rows
+            // with no allowed slot are masked too, so a non-finite score past
+            // the new length cannot reach them)
+            if (!__all_sync(0xffffffffu, j0 + kTcT - 1 <= lim || (none && !TWO))) {
 #pragma unroll
                 for (int c = 0; c < kTcT; ++c)
                     if (j0 + c > lim) sv[c] = -INFINITY;
@@ -566,9 +795,11 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
             const float tmax = none ? -INFINITY : fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * qs;
             // P[comp % 2] is free once the product two tiles back has finished
             if (comp >= 2 && !wait_pv(comp - 2)) break;
-            const bool raise = tmax > m_ref + kRescale;
+            // (the second pass of the two-pass kernel knows the row's maximum:
+            // its reference never moves)
+            const bool raise = !TWO && tmax > m_ref + kRescale;
             const float corr = (raise && m_ref != -INFINITY) ? fast_exp2(m_ref - tmax) : 1.f;
-            if (__any_sync(0xffffffffu, raise && m_ref != -INFINITY && !first_tile)) {
+            if (!TWO && __any_sync(0xffffffffu, raise && m_ref != -INFINITY && !first_tile)) {
                 // O must be quiescent: the previous product has finished, this
                 // tile's is not issued before p_ready
                 if (!wait_pv(comp - 1)) break;
@@ -589,23 +820,28 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
             const float negm = (none || m_ref == -INFINITY) ? -INFINITY : -m_ref;
             float ls0 = 0.f, ls1 = 0.f;
             uint32_t pk[kTcT / 2];  // operand type, two per word
-            uint32_t ph[kTcT / 2];  // fp16, two per word (the attention rows' inputs)
+            uint32_t ph[kTcT / 2];  // fp16 P (one pass) or the attention values (two passes)
 #pragma unroll
             for (int c = 0; c < kTcT; c += 2) {
                 const float e0 = fast_exp2(fmaf(sv[c], qs, negm));
                 const float e1 = fast_exp2(fmaf(sv[c + 1], qs, negm));
                 if (c & 2) ls1 += e0 + e1; else ls0 += e0 + e1;
                 pk[c / 2] = pack2<T>(e0, e1);
-                if constexpr (!std::is_same<T, __half>::value) ph[c / 2] = pack2<__half>(e0, e1);
+                if constexpr (TWO) ph[c / 2] = pack2<T>(e0 * inv_l, e1 * inv_l);
+                else if constexpr (!std::is_same<T, __half>::value) ph[c / 2] = pack2<__half>(e0, e1);
             }
             l += ls0 + ls1;
             tmem_st32u(trow + cols.p0 + 32 * static_cast<uint32_t>(comp & 1), pk);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.p_ready(static_cast<int>(comp & 1)), 1u);
-            if (valid && !none) p.tile_max[rowg * p.tiles64 + mt.i] = m_ref;
-            if (!stage(std::is_same<T, __half>::value ? pk : ph, &tp.tm_pv, j0, static_cast<int>(u)))
-                break;
+            if (TWO) {
+                if (!stage(ph, &tp.tm_att, j0, static_cast<int>(u))) break;
+            } else {
+                if (valid && !none) p.tile_max[rowg * p.tiles64 + mt.i] = m_ref;
+                if (!stage(std::is_same<T, __half>::value ? pk : ph, &tp.tm_pv, j0, static_cast<int>(u)))
+                    break;
+            }
             ++comp;
             first_tile = false;
         }
@@ -631,7 +867,7 @@ __device__ void tc_softmax(const TcParams& tp, unsigned char* smem, TcBars bars,
     if (r == 0) bulk_wait_all();  // the staged stores have finished
 }
 
-template <typename T>
+template <typename T, bool TWO>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_step_kernel(const __grid_constant__ TcParams tp) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const StepParams& p = tp.p;
@@ -669,14 +905,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_step_kernel(const __grid_con
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
 
     if (warp < kSoftWarps) {
-        tc_softmax<T>(tp, smem, bars, abort, tmem);
+        tc_softmax<T, TWO>(tp, smem, bars, abort, tmem);
     } else if (warp == kMmaWarp) {
         if ((threadIdx.x & 31) == 0)
             tc_mma_issuer(tp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value);
     } else if (warp == kProdWarp) {
-        if ((threadIdx.x & 31) == 0) tc_producer(tp, smem, bars, abort);
+        if ((threadIdx.x & 31) == 0) tc_producer<TWO>(tp, smem, bars, abort);
     } else if (warp == kStoreWarp) {
-        tc_storer(tp, smem, bars, abort);
+        tc_storer<TWO>(tp, smem, bars, abort);
     }
     tc_fence_before();
     __syncthreads();  // every thread reaches this exactly once: all waits are bounded
@@ -690,7 +926,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_step_kernel(const __grid_con
 }  // namespace
 
 cudaError_t launch_fused_tc(const TcParams& tp, int dtype, size_t smem, cudaStream_t stream) {
-    auto kern = dtype == KVC_BF16 ? tc_step_kernel<__nv_bfloat16> : tc_step_kernel<__half>;
+    auto kern = tp.p.tc_two_pass
+                    ? (dtype == KVC_BF16 ? tc_step_kernel<__nv_bfloat16, true>
+                                         : tc_step_kernel<__half, true>)
+                    : (dtype == KVC_BF16 ? tc_step_kernel<__nv_bfloat16, false>
+                                         : tc_step_kernel<__half, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;

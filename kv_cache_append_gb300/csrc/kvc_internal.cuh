@@ -172,6 +172,47 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, int x, int y, int
                  : "memory");
 }
 
+// L2 eviction-priority policies for the cache_hint forms below: lines loaded
+// or stored with evict_first go first when L2 needs room, lines with
+// evict_last stay longest (data that is read again soon).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_3d / tma_store_3d with an L2 eviction policy.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tmap, int x, int y, int z,
+                                                 uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_3d_hint(const void* tmap, int x, int y, int z,
+                                                  uint32_t src, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+        " [%0, {%1, %2, %3}], [%4], %5;" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+        "r"(x), "r"(y), "r"(z), "r"(src), "l"(pol)
+        : "memory");
+}
+
+// Prefetch of one box of a tiled tensor into L2 (no shared memory, no
+// completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared (no registers in between).
 __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src)
@@ -509,6 +550,17 @@ struct StepParams {
     // tc_off_stg (rows of 128 bytes for TMA stores), tensor-memory columns
     int tc_off_stg, tc_stg_bytes, tc_tmem_cols;
     int64_t tc_nrg;  // row groups of up to 128 query rows per unit (1 or 2)
+    // Two-pass tensor-core step (tc_two_pass = 1; one row group, out of place):
+    // a first pass over each unit's key prefix leaves every row's softmax
+    // maximum and sum per chunk in part1_ml ([U][KP][R][2], base 2) and counts
+    // its finished chunk passes in unit_done[u] (one per softmax warp); the
+    // second pass copies the caches, writes the normalised attention rows
+    // straight to out_attention and the context partials. tc_dist: units
+    // between a unit's first and second pass in the hand-out order.
+    int tc_two_pass;
+    int64_t tc_dist;
+    float* part1_ml;
+    unsigned int* unit_done;
     // decode tensor-core kernel layout: the softmax warps' exchange buffers
     // and the two P^T operand buffers
     int dec_off_red, dec_off_pt;

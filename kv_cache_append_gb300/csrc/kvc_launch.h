@@ -27,6 +27,7 @@ struct TcParams {
     CUtensorMap tm_ov;   // out_value_cache
     CUtensorMap tm_pv;   // pvals as [U][R][pv_ld] fp16, boxes of 64 slots x R rows
     CUtensorMap tm_acc;  // part_acc as [U * KP][R][Dv] fp32, boxes of 32 values x R rows
+    CUtensorMap tm_att;  // two-pass step: out_attention as [U][R][M], boxes of 64 slots x R rows
     StepParams p;
 };
 

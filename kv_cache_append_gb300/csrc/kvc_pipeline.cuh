@@ -38,6 +38,7 @@ constexpr int kFirst = 1;    // first tile of its chunk
 constexpr int kLast = 2;     // last tile of its chunk
 constexpr int kDone = 4;     // no more tiles: the roles stop
 constexpr int kQStaged = 8;  // the stage also holds the unit's query rows
+constexpr int kPass1 = 16;   // two-pass tensor-core step: a first-pass (key-only) tile
 
 // Position in the stage ring: stage index and the parity of its current lap.
 struct Ring {

@@ -23,7 +23,9 @@ from typing import Optional, Sequence
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libkvc.so")
+# KVC_LIBRARY names another build of the same library (e.g. one compiled with
+# other compile-time options by build.build_variant); default: the in-tree build.
+LIB_PATH = os.environ.get("KVC_LIBRARY") or os.path.join(_HERE, "libkvc.so")
 
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 

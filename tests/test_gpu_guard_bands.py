@@ -8,7 +8,7 @@ allocation whose 4 KB bands on both sides hold a known byte pattern; after
 the call the bands must be unchanged ("inputs are never modified", Required
 behavior, bullet 4, and no write outside the buffers the caller passed). Every
 face and path is covered on small odd shapes: the out-of-place step (fused,
-tensor with one and two row groups, generic, fp32), in place (decode
+tensor with one and two row groups, the two-pass tensor form, generic, fp32), in place (decode
 tensor-core, fused, tensor), paged (decode tensor-core, fused, tensor),
 read-only re-attention, the gradients (each slot kernel) and the
 no-allocation entry. The guarded run's results must equal an unguarded run's
@@ -81,6 +81,9 @@ STEP = {
     "fused_specdec_bf16": SMALL["specdec_bf16"],
     "fused_fp32_Q40": SMALL["chunk_fp32_Q40"],
     "tensor_f16_D192": TC["r128_fp16_D192_Dv128"].replace(M=1001, lengths=("uniform", 500, 993)),
+    # one row group, M a multiple of 8: the two-pass form, which writes the
+    # attention rows from the step kernel
+    "tensor2_f16_D192": TC["r128_fp16_D192_Dv128"].replace(M=1000, lengths=("uniform", 500, 992)),
     "tensor_bf16_rg2": TC["r160_bf16_chunk40"],
     "generic_D5_Dv7": Spec(B=3, Hq=4, Hk=2, Q=3, D=5, Dv=7, M=51, dtype="bf16",
                            counts=("uniform", 0, 3)),

@@ -13,6 +13,7 @@ same launch configuration as bench.py, compare every cache element through the
 append property and sampled batch rows against the oracle.
 """
 import hashlib
+import os
 
 import numpy as np
 import pytest
@@ -337,9 +338,35 @@ TC = {
 }
 
 
+# the tensor-core step: one pass with stored P rows and the row writer, or
+# (one row group, out of place, M a multiple of 8) two passes writing the
+# attention rows directly
+TENSOR_PATHS = ("tensor", "tensor_2pass")
+
+
 def _path(x):
+    """The path kvc_step takes for x (out of place: output caches of their own)."""
+    ok, ov = torch.empty_like(x.key_cache), torch.empty_like(x.value_cache)
     return kvc.plan_info(kvc.dims_of(x.query, x.key_cache, x.value_cache), x.key_cache,
-                         x.value_cache, x.new_key, x.new_value, x.key_cache, x.value_cache)[1]
+                         x.value_cache, x.new_key, x.new_value, ok, ov)[1]
+
+
+@pytest.mark.skipif(os.environ.get("KVC_EXPECT_TWO_PASS") != "1",
+                    reason="the two-pass form is built only with KVC_TC_TWO_PASS=1")
+def test_two_pass_taken_where_it_applies():
+    """The two-pass form for one row group with M a multiple of 8 (out of
+    place), the one-pass form otherwise (two row groups, M = 700 or 9005, in
+    place)."""
+    want = {"r128_fp16_D192_Dv128": "tensor_2pass", "r64_fp16_D256_Dv64": "tensor_2pass",
+            "r96_bf16_hot": "tensor_2pass", "r64_fp16_segments": "tensor_2pass",
+            "r64_bf16_ragged": "tensor", "r64_bf16_segments_M9005": "tensor",
+            "r160_bf16_chunk40": "tensor", "r200_fp16_ragged": "tensor"}
+    for name, path in want.items():
+        xg = workloads.generate(TC[name], 0).to(DEV)
+        assert _path(xg) == path, name
+        dims = kvc.dims_of(xg.query, xg.key_cache, xg.value_cache)
+        assert kvc.plan_info_inplace(dims, xg.key_cache, xg.value_cache, xg.new_key,
+                                     xg.new_value)[1] == "tensor"
 
 
 @pytest.mark.parametrize("name", sorted(TC))
@@ -347,7 +374,7 @@ def _path(x):
 def test_tensor_core_path(name, seed):
     x = workloads.generate(TC[name], seed)
     xg = x.to(DEV)
-    assert _path(xg) == "tensor"
+    assert _path(xg) in TENSOR_PATHS
     out, status = run_gpu(xg)
     compare_full(x, out, status)
 
@@ -362,7 +389,7 @@ def test_tensor_core_path_growing_scores():
     x.key_cache = (x.key_cache.float() * ramp).to(torch.bfloat16)
     x.query = (x.query.float() * 4.0).to(torch.bfloat16)
     xg = x.to(DEV)
-    assert _path(xg) == "tensor"
+    assert _path(xg) in TENSOR_PATHS
     out, status = run_gpu(xg)
     compare_full(x, out, status)
 
@@ -376,7 +403,7 @@ def test_tensor_core_path_contract_violations():
     m[3, 7] = True   # not a prefix
     x.append_mask = m
     xg = x.to(DEV)
-    assert _path(xg) == "tensor"
+    assert _path(xg) in TENSOR_PATHS
     out, status = run_gpu(xg)
     compare_full(x, out, status, expect_flags=kvc.DEV_MASK | kvc.DEV_OVERFLOW)
 
