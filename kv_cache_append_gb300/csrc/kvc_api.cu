@@ -84,6 +84,8 @@ struct Plan {
     int T = 0;
     int64_t TPU = 0, CH = 1, KP = 1, NQ = 0, P = 0;
     int RPW = 4, WR = 1, WS = 8, NRG = 1, SW = 0, NS = 0, LAG = 0, DVC = 1, NCHL = 0;
+    int RB = 0;        // rows per work item of the fused kernel (0: all of the unit's)
+    int64_t NRB = 1;   // row blocks per unit
     int stage_bytes = 0, off_stages = 0, off_q = 0, off_p = 0, off_state = 0, off_state_acc = 0,
         off_row_lim = 0, off_row_off = 0, off_flag = 0, off_meta = 0;
     bool q_staged = false;
@@ -151,8 +153,25 @@ void workspace_layout(const kvc_dims& d, int64_t KP, Plan* pl) {
 // overhead per slot (decode in place: 0.536 -> 0.466 ms per step).
 constexpr int64_t kStageTargetInplace = 2 * kStageTargetBytes;
 
-// Tiling of the fused kernel that depends only on the sizes.
-void fused_tiling(const kvc_dims& d, Plan* pl, int64_t stage_target = kStageTargetBytes) {
+// Rows per work item of the fused kernel. Units of more than kRowBlock rows
+// whose caches stay in L2 (both caches at most kRowBlockCache bytes) are
+// split into row blocks of kRowBlock rows, each its own work item, so that
+// their query rows stay in registers (the decode form) and their tiles spread
+// over more SMs; every block reads the tile (from L2 after the first), block
+// 0 stores it. The chunked 40-token fp32 append went from one CTA per chunk
+// doing 160 rows from shared memory to five register-row items.
+constexpr int64_t kRowBlock = 32;
+constexpr int64_t kRowBlockCache = int64_t(64) << 20;
+int64_t fused_block_rows(const kvc_dims& d, bool query_aligned) {
+    const int64_t R = (d.Hq / d.Hk) * d.Q;
+    const int64_t cache = 2 * d.B * d.Hk * d.M * (d.D + d.Dv) * elem_size(d.dtype);
+    return (R > kRowBlock && query_aligned && cache <= kRowBlockCache) ? kRowBlock : R;
+}
+
+// Tiling of the fused kernel that depends only on the sizes (and the rows
+// per work item, rb; 0: every row of the unit).
+void fused_tiling(const kvc_dims& d, Plan* pl, int64_t stage_target = kStageTargetBytes,
+                  int64_t rb = 0) {
     const int64_t es = elem_size(d.dtype);
     const int64_t row = (d.D + d.Dv) * es;
     int64_t T = stage_target / row / 32 * 32;
@@ -160,7 +179,7 @@ void fused_tiling(const kvc_dims& d, Plan* pl, int64_t stage_target = kStageTarg
     if (d.M < T) T = align_up(d.M, 32);
     pl->T = static_cast<int>(T);
     pl->TPU = (d.M + T - 1) / T;
-    const int64_t R = (d.Hq / d.Hk) * d.Q;
+    const int64_t R = rb > 0 ? rb : (d.Hq / d.Hk) * d.Q;
     // Up to 32 rows per unit: 4 rows per warp, one row group each, query rows
     // in registers. More rows: 8 rows per warp from shared memory.
     pl->RPW = R <= 32 ? 4 : 8;
@@ -215,9 +234,12 @@ int64_t sizing_kp(const kvc_dims& d, int64_t T, int64_t TPU) {
 bool fused_plan(const kvc_dims& d, int sms, int smem_cap, bool query_aligned, Plan* pl,
                 int64_t stage_target = kStageTargetBytes) {
     if (!fused_shapes(d)) return false;
-    fused_tiling(d, pl, stage_target);
+    const int64_t RU = (d.Hq / d.Hk) * d.Q;       // rows of a unit
+    const int64_t R = fused_block_rows(d, query_aligned);  // rows of a work item
+    fused_tiling(d, pl, stage_target, R);
+    pl->RB = static_cast<int>(R);
+    pl->NRB = RU > 0 ? (RU + R - 1) / R : 1;
     const int64_t es = elem_size(d.dtype);
-    const int64_t R = (d.Hq / d.Hk) * d.Q;
     const int64_t qbytes = R * d.D * es;
     pl->q_staged = d.Q > 0 && query_aligned && qbytes <= kMaxStagedQuery;
     if (pl->RPW == 4 && d.Q > 0 && !pl->q_staged) return false;  // register path reads staged rows
@@ -248,6 +270,7 @@ bool fused_plan(const kvc_dims& d, int sms, int smem_cap, bool query_aligned, Pl
     pl->LAG = std::min(std::min(kStoreLag, 7), pl->NS - 1);
     pl->smem = static_cast<size_t>(off + int64_t(pl->NS) * stage);
     chunking(d, sms, pl);
+    pl->NQ *= pl->NRB;  // every chunk once per row block
     pl->P = std::min<int64_t>(sms, pl->NQ);
     pl->fused = true;
     workspace_layout(d, pl->KP, pl);
@@ -579,6 +602,8 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     p.qscale = static_cast<float>(scale * 1.4426950408889634);
     p.T = pl.T; p.TPU = pl.TPU; p.CH = pl.CH; p.KP = pl.KP; p.NQ = pl.NQ; p.P = pl.P;
     p.RPW = pl.RPW; p.WR = pl.WR; p.WS = pl.WS; p.NRG = pl.NRG; p.SW = pl.SW;
+    p.RB = pl.RB > 0 ? pl.RB : static_cast<int>(p.R);
+    p.NRB = pl.NRB;
     p.NS = pl.NS; p.LAG = pl.LAG;
     p.stage_bytes = pl.stage_bytes; p.off_stages = pl.off_stages; p.off_q = pl.off_q;
     p.off_p = pl.off_p; p.off_state = pl.off_state; p.off_state_acc = pl.off_state_acc;

@@ -30,12 +30,21 @@
 //
 // So the valid prefix of the cache is read from HBM once and serves both the
 // copy and the attention. kvc_finalize.cu merges the partials.
+//
+// Units of more than 32 query rows on caches small enough to stay in L2 (the
+// chunked multi-token appends) are split into row blocks of 32 rows, each a
+// work item of its own: the rows of a block stay in registers (the decode
+// form below) instead of being read from shared memory for every product,
+// and the unit's tiles are spread over more SMs. Every block reads the tile
+// (from L2 after the first); only block 0 stores it.
 #include "kvc_internal.cuh"
 #include "kvc_launch.h"
 #include "kvc_pipeline.cuh"
 
 namespace kvc {
 namespace {
+
+constexpr int kRbShift = 8;  // TileMeta flags bits 8..: the tile's row block
 
 struct Bars {
     uint32_t base;
@@ -63,7 +72,10 @@ __device__ void run_producer(const StepParams& p, unsigned char* smem, Bars bars
         const int64_t q = atomicAdd(p.counter, 1u);
         if (q >= p.NQ) break;
         const int64_t idx = chunk_of(q, p.NQ);
-        const int64_t k = idx / U, u = idx - k * U;  // chunk-index-major list
+        // chunk-index-major list of (unit, row block) work items
+        const int64_t k = idx / (U * p.NRB), ub = idx - k * U * p.NRB;
+        const int64_t u = ub / p.NRB, rb = ub - u * p.NRB;
+        const int64_t rows_b = min(static_cast<int64_t>(p.RB), p.R - rb * p.RB);
         const Unit x = load_unit(p, u);
         // in place, tiles from the new length on are neither read nor written
         const int64_t iend = !p.inplace ? p.TPU : x.n > 0 ? min(p.TPU, (x.N + p.T - 1) / p.T) : 0;
@@ -93,10 +105,11 @@ __device__ void run_producer(const StepParams& p, unsigned char* smem, Bars bars
             mt.n = static_cast<int32_t>(x.n);
             mt.i = static_cast<int32_t>(i);
             mt.k = static_cast<int32_t>(k);
-            mt.flags = (i == i0 ? kFirst : 0) | (i == i1 - 1 ? kLast : 0) | (stage_q ? kQStaged : 0);
+            mt.flags = (i == i0 ? kFirst : 0) | (i == i1 - 1 ? kLast : 0) | (stage_q ? kQStaged : 0) |
+                       static_cast<int32_t>(rb << kRbShift);
             const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
             uint32_t bytes = static_cast<uint32_t>((j1 - j0) * (rowK + rowV));
-            if (stage_q) bytes += static_cast<uint32_t>(p.q_stage_bytes);
+            if (stage_q) bytes += static_cast<uint32_t>(rows_b * rowK);
             mbar_arrive_expect_tx(bars.full(ring.s), bytes);  // publishes the metadata too
             if (p.block_table) {
                 load_rows_paged(sK, sK + vofs, p, ids, u, nku, nvu, rowK, rowV, j0, j1, Ls, x.N,
@@ -109,8 +122,8 @@ __device__ void run_producer(const StepParams& p, unsigned char* smem, Bars bars
             }
             if (stage_q)  // the G*Q query rows of the unit are contiguous in query
                 bulk_g2s(sK + static_cast<uint32_t>(p.off_stage_q),
-                         qry + (x.b * p.Hq + x.kv * p.G) * p.Q * rowK,
-                         static_cast<uint32_t>(p.q_stage_bytes), bars.full(ring.s));
+                         qry + ((x.b * p.Hq + x.kv * p.G) * p.Q + rb * p.RB) * rowK,
+                         static_cast<uint32_t>(rows_b * rowK), bars.full(ring.s));
             ++issued;
             ring.next(p.NS);
         }
@@ -147,7 +160,7 @@ __device__ void run_storer(const StepParams& p, unsigned char* smem, Bars bars,
         if (mt.flags & kDone) break;
         const int64_t j0 = static_cast<int64_t>(mt.i) * p.T, j1 = min(j0 + p.T, p.M);
         const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
-        if (!p.inplace) {
+        if (!p.inplace && (mt.flags >> kRbShift) == 0) {  // row block 0 stores the tile
             bulk_s2g(okc + (mt.u * p.M + j0) * rowK, sK, static_cast<uint32_t>((j1 - j0) * rowK));
             bulk_s2g(ovc + (mt.u * p.M + j0) * rowV, sK + vofs,
                      static_cast<uint32_t>((j1 - j0) * rowV));
@@ -486,12 +499,14 @@ __device__ __forceinline__ void load_state(const StepParams& p, const float* st_
     }
 }
 
+// rows r0.. of a state buffer of R rows (fewer in the last row block)
 template <typename T, int RPW, int DVC>
-__device__ __forceinline__ void store_state(const StepParams& p, float* st_ml, float* st_acc,
-                                            int r0, const float (&m)[RPW], const float (&l)[RPW],
+__device__ __forceinline__ void store_state(const StepParams& p, int R, float* st_ml,
+                                            float* st_acc, int r0, const float (&m)[RPW],
+                                            const float (&l)[RPW],
                                             const float (&acc)[RPW][DVC][4]) {
     const int lane = threadIdx.x & 31;
-    const int R = static_cast<int>(p.R), Dv = static_cast<int>(p.Dv);
+    const int Dv = static_cast<int>(p.Dv);
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
         const int r = r0 + i;
@@ -535,9 +550,12 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
     Ring ring;
     uint32_t cphase = 0;
 
-    // current chunk
+    // current chunk; its row block: rows [rbase, rbase + Rl) of the unit (the
+    // register path); the shared-memory path always takes every row
     bool attend = false;
     int64_t L = 0, n = 0, N = 0, u = 0, k = 0, b = 0, kv = 0;
+    int rbase = 0, Rl = R;
+    const int RS = p.RB;  // row stride of the per-warp state slots
     // register path (NCHL > 0): 4 rows per warp, whole chunk
     constexpr int V2 = VEC / 2;
     constexpr int NQR = NCHL > 0 ? NCHL : 1;
@@ -568,7 +586,9 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
             b = u / p.Hk;
             kv = u - b * p.Hk;
             attend = n > 0 && static_cast<int64_t>(mt.i) * p.T < N;
-            if (k == 0 && kv == 0 && w == 0 && lane == 0 && !p.inplace) {
+            rbase = (mt.flags >> kRbShift) * p.RB;
+            Rl = min(p.RB, R - rbase);
+            if (k == 0 && kv == 0 && rbase == 0 && w == 0 && lane == 0 && !p.inplace) {
                 // returned length and contract flags: once per batch row
                 const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
                 p.out_lengths[b] = ra.L + ra.n;
@@ -581,13 +601,13 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
                     const int r0 = wr * 4;
 #pragma unroll
                     for (int ii = 0; ii < 4; ++ii) {
-                        const int r = r0 + ii;
-                        const int t = r % Q;
-                        lim4[ii] = (r < R && t < n) ? static_cast<int>(L + t) : -1;
+                        const int r = r0 + ii;  // row of the block (staged at r)
+                        const int t = (rbase + r) % Q;
+                        lim4[ii] = (r < Rl && t < n) ? static_cast<int>(L + t) : -1;
 #pragma unroll
                         for (int cc = 0; cc < NCHL; ++cc) {
                             const int ck = sub + 8 * cc;
-                            if (r < R && ck < nck) {
+                            if (r < Rl && ck < nck) {
                                 const uint4 raw =
                                     *reinterpret_cast<const uint4*>(qst + (r * nck + ck) * 16);
                                 S::widen16_2(raw, qr[ii][cc]);
@@ -613,7 +633,7 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
 #pragma unroll
                     for (int ii = 0; ii < 4; ++ii) {
                         if ((sub >> 1) == ii) {  // the row this lane's scores end in
-                            const int r = r0 + ii;
+                            const int r = rbase + r0 + ii;
                             mylim = lim4[ii];
                             myoff = ((b * p.Hq + kv * p.G + r / Q) * p.Q + r % Q) * p.M;
                         }
@@ -659,7 +679,7 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
         if (attend && static_cast<int64_t>(mt.i) * p.T < N) {
             const int j0 = mt.i * p.T;
             if constexpr (NCHL > 0) {
-                if (wr * 4 < R)
+                if (wr * 4 < Rl)
                     tile_rows_qr<T, NCHL, DVC>(p, ws, j0, sK, sK + vofs, qr, pb, maxlim, mylim,
                                                myoff, m4, lp, acc2);
             } else {
@@ -670,7 +690,7 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
                     tile_rows<T, RPW, DVC>(p, rg, ws, j0, sK, sK + vofs, qs, pb, row_lim,
                                            row_off, m, l, acc);
                     if (p.NRG > 1)
-                        store_state<T, RPW, DVC>(p, st_ml, st_acc, rg * RPW, m, l, acc);
+                        store_state<T, RPW, DVC>(p, R, st_ml, st_acc, rg * RPW, m, l, acc);
                 }
             }
         }
@@ -681,7 +701,7 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
         // ---- end of an attending chunk: merge the WS slot-split warps per row
         if constexpr (NCHL > 0) {
             const int r0 = wr * 4;
-            if (r0 < R) {
+            if (r0 < Rl) {
                 float mm[4], ll[4], aa[4][DVC][4];
 #pragma unroll
                 for (int ii = 0; ii < 4; ++ii) {
@@ -698,26 +718,27 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
                         aa[ii][cc][3] = acc2[ii][cc][1].y;
                     }
                 }
-                store_state<T, 4, DVC>(p, st_ml + 2 * ws * R, st_acc + ws * R * Dv, r0, mm, ll, aa);
+                store_state<T, 4, DVC>(p, Rl, st_ml + 2 * ws * RS, st_acc + ws * RS * Dv, r0, mm,
+                                       ll, aa);
             }
         } else {
             if (p.NRG == 1 && wr * RPW < R)
-                store_state<T, RPW, DVC>(p, st_ml + 2 * ws * R, st_acc + ws * R * Dv, wr * RPW, m,
-                                         l, acc);
+                store_state<T, RPW, DVC>(p, R, st_ml + 2 * ws * RS, st_acc + ws * RS * Dv, wr * RPW,
+                                         m, l, acc);
         }
         if (!consumer_rendezvous(bars, cphase, abort)) break;
         const int64_t s_k = k * p.CH * p.T;  // the chunk's first slot
-        for (int r = w; r < R; r += kConsumerWarps) {
-            const int t = r % Q;
+        for (int r = w; r < Rl; r += kConsumerWarps) {  // r: row of the block
+            const int t = (rbase + r) % Q;
             if (t >= n || s_k > L + t) continue;  // no allowed slot of this row here
             float mx = -INFINITY;
-            for (int q = 0; q < p.WS; ++q) mx = fmaxf(mx, st_ml[2 * (q * R + r)]);
+            for (int q = 0; q < p.WS; ++q) mx = fmaxf(mx, st_ml[2 * (q * RS + r)]);
             float lsum = 0.f;
             for (int q = 0; q < p.WS; ++q) {
-                const float mq = st_ml[2 * (q * R + r)];
-                if (mq != -INFINITY) lsum += st_ml[2 * (q * R + r) + 1] * fast_exp2(mq - mx);
+                const float mq = st_ml[2 * (q * RS + r)];
+                if (mq != -INFINITY) lsum += st_ml[2 * (q * RS + r) + 1] * fast_exp2(mq - mx);
             }
-            const int64_t prow = (u * p.KP + k) * p.R + r;
+            const int64_t prow = (u * p.KP + k) * p.R + rbase + r;
             if (lane == 0) {
                 p.part_ml[2 * prow] = mx;
                 p.part_ml[2 * prow + 1] = lsum;
@@ -725,11 +746,11 @@ __device__ void run_consumers(const StepParams& p, unsigned char* smem, Bars bar
             for (int e0 = lane * 4; e0 < Dv; e0 += 128) {
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int q = 0; q < p.WS; ++q) {
-                    const float mq = st_ml[2 * (q * R + r)];
+                    const float mq = st_ml[2 * (q * RS + r)];
                     if (mq == -INFINITY) continue;
                     const float wq = fast_exp2(mq - mx);
                     const float4 bq =
-                        *reinterpret_cast<const float4*>(st_acc + (q * R + r) * Dv + e0);
+                        *reinterpret_cast<const float4*>(st_acc + (q * RS + r) * Dv + e0);
                     a.x = fmaf(bq.x, wq, a.x);
                     a.y = fmaf(bq.y, wq, a.y);
                     a.z = fmaf(bq.z, wq, a.z);

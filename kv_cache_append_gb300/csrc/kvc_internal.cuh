@@ -550,6 +550,12 @@ struct StepParams {
     // tc_off_stg (rows of 128 bytes for TMA stores), tensor-memory columns
     int tc_off_stg, tc_stg_bytes, tc_tmem_cols;
     int64_t tc_nrg;  // row groups of up to 128 query rows per unit (1 or 2)
+    // CUDA-core fused kernel, units of many rows on small caches: a unit's R
+    // query rows are worked as NRB row blocks of RB rows, each its own work
+    // item (chunk k of unit u, row block rb), all reading the tile and the
+    // first one storing it (RB = R, NRB = 1 otherwise).
+    int RB;
+    int64_t NRB;
     // Two-pass tensor-core step (tc_two_pass = 1; one row group, out of place):
     // a first pass over each unit's key prefix leaves every row's softmax
     // maximum and sum per chunk in part1_ml ([U][KP][R][2], base 2) and counts

@@ -145,6 +145,12 @@ SMALL = {
     # rows longer than one finalize segment (8192 slots), M not a multiple of 8
     "fp32_three_segments": Spec(B=1, Hq=2, Hk=1, Q=2, D=16, Dv=16, M=2 * 8192 + 13,
                                 dtype="f32", lengths=("uniform", 9000, 16395)),
+    # more than 32 rows per unit on small caches: row blocks of 32 rows, the
+    # last one partial (42 = 32 + 10 rows; 48 = 32 + 16 rows, 16-bit D = 96)
+    "rowblocks_fp32_R42": Spec(B=3, Hq=6, Hk=1, Q=7, D=64, Dv=64, M=300, dtype="f32",
+                               counts=("uniform", 0, 7)),
+    "rowblocks_bf16_D96_R48": Spec(B=2, Hq=12, Hk=2, Q=8, D=96, Dv=64, M=257, dtype="bf16",
+                                   lengths=("uniform", 0, 249), counts=("uniform", 1, 8)),
 }
 
 
