@@ -662,7 +662,16 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
             return cudaEventRecord(static_cast<cudaEvent_t>(events[recorded++]), stream);
         return cudaSuccess;
     };
-    cudaError_t e = record();
+    // The step kernels hand out chunks from a counter that starts at zero (and
+    // the two-pass tensor-core step counts each unit's first pass): cleared
+    // first, so that the events of the timed faces bracket only the kernels.
+    cudaError_t e = cudaSuccess;
+    if ((hasq || !inplace) && p.counter && (pl.tensor || pl.dec || pl.fused))
+        e = cudaMemsetAsync(p.counter, 0,
+                            pl.tc_two ? pl.off_unit_done + static_cast<size_t>(d.B * d.Hk) * 4
+                                      : sizeof(unsigned int),
+                            stream);
+    if (e == cudaSuccess) e = record();
     if (e == cudaSuccess && inplace && !mode.readonly && !mode.stats_only) {  // appended rows and lengths, before any reader
         const bool words16 = (d.D * es) % 16 == 0 && (d.Dv * es) % 16 == 0 && ptrs_aligned;
         e = launch_inplace_rows(p, words16, stream);
@@ -694,12 +703,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                           2, d.M, d.M, p.R, d.B * d.Hk, 64, static_cast<int>(p.R)))
                 return KVC_E_CUDA;
-            // the chunk counter (and, two-pass, the units' first-pass counters)
-            e = cudaMemsetAsync(p.counter, 0,
-                                pl.tc_two ? pl.off_unit_done + static_cast<size_t>(d.B * d.Hk) * 4
-                                          : sizeof(unsigned int),
-                                stream);
-            if (e == cudaSuccess) e = launch_fused_tc(tp, d.dtype, pl.smem, stream);
+            e = launch_fused_tc(tp, d.dtype, pl.smem, stream);
             if (e == cudaSuccess) e = record();
         } else if (pl.dec) {
             DecParams dp;
@@ -718,13 +722,10 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                          2, d.D, d.D, d.B * d.Hk * p.R, 1, 64, 16);
             if (!ok_maps) return KVC_E_CUDA;
-            e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream);
-            if (e == cudaSuccess) e = launch_decode_tc(dp, d.dtype, pl.dec_nr, pl.smem, stream);
+            e = launch_decode_tc(dp, d.dtype, pl.dec_nr, pl.smem, stream);
             if (e == cudaSuccess) e = record();
         } else if (pl.fused) {
-            // chunks are handed out from a counter that starts at zero
-            if (p.counter) e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), stream);
-            if (e == cudaSuccess) e = launch_fused(p, d.dtype, pl.DVC, pl.NCHL, pl.smem, stream);
+            e = launch_fused(p, d.dtype, pl.DVC, pl.NCHL, pl.smem, stream);
             if (e == cudaSuccess) e = record();
         } else {
             if (!inplace) {
