@@ -41,6 +41,7 @@
 //   bwd_dq_kernel      dq = scale * the accumulated sum, in the dtype.
 //
 // All sums are fp32; the gradients are written in the inputs' dtype.
+#include <algorithm>
 #include <functional>
 #include <type_traits>
 
@@ -353,6 +354,11 @@ __device__ __forceinline__ void lds_vec(const float* p, float (&f)[V]) {
 #ifndef KVC_BWD_ROWS_CAP3
 #define KVC_BWD_ROWS_CAP3 16  // NR x V up to which they are capped for three blocks per SM
 #endif
+#ifndef KVC_BWD_ROWS_GRID_X
+#define KVC_BWD_ROWS_GRID_X 8
+#endif
+constexpr int64_t kRowsGridX = KVC_BWD_ROWS_GRID_X;  // blocks per unit of bwd_kv_rows_kernel
+
 template <int NR, int V>
 struct RowsLayout {
     static constexpr bool kRegDq = NR * V <= 64;
@@ -385,8 +391,10 @@ __global__ void __launch_bounds__(kBwdWarps * 32, (RowsLayout<NR, V>::kBlocks))
         }
     }
     const int64_t jend = ra.flags ? 0 : N;
-    const int64_t jb = static_cast<int64_t>(blockIdx.x) * (kBwdWarps * 32);
-    if (jb >= jend) return;  // whole block
+    // the block works slot blocks blockIdx.x, blockIdx.x + gridDim.x, ... of
+    // its unit (a bounded grid: most units of a ragged batch are short)
+    constexpr int64_t SB = kBwdWarps * 32;  // slots per slot block
+    if (static_cast<int64_t>(blockIdx.x) * SB >= jend) return;  // whole block
     const int64_t row0 = (b * p.Hq + kv * p.G) * p.Q;
     float* s_q = sm;
     float* s_dc = s_q + NR * W;
@@ -401,7 +409,22 @@ __global__ void __launch_bounds__(kBwdWarps * 32, (RowsLayout<NR, V>::kBlocks))
     }
     if constexpr (!Lay::kRegDq)
         for (int i = lane; i < NR * W; i += 32) s_dq[i] = 0.f;
+    const T* nk = static_cast<const T*>(p.new_key);
+    const T* nv = static_cast<const T*>(p.new_value);
+    const T* kc = static_cast<const T*>(p.key_cache);
+    const T* vc = static_cast<const T*>(p.value_cache);
+    const T* gko = static_cast<const T*>(bp.d_key_out);
+    const T* gvo = static_cast<const T*>(bp.d_value_out);
+    const int e0 = V * lane;
+    float dqr[Lay::kRegDq ? NR : 1][V];
+#pragma unroll
+    for (int r = 0; r < (Lay::kRegDq ? NR : 1); ++r)
+#pragma unroll
+        for (int i = 0; i < V; ++i) dqr[r][i] = 0.f;
+    for (int64_t jb = static_cast<int64_t>(blockIdx.x) * SB; jb < jend;
+         jb += static_cast<int64_t>(gridDim.x) * SB) {
     const int64_t j0 = jb + w * 32;
+    __syncthreads();  // the previous slot block's phase 2 is done with s_a / s_da
     {  // phase 1: one slot per lane; a_rj and dattention_rj - D_r
         const int64_t j = j0 + lane;
 #pragma unroll
@@ -429,13 +452,6 @@ __global__ void __launch_bounds__(kBwdWarps * 32, (RowsLayout<NR, V>::kBlocks))
     // phase 2: slot by slot, lane l on elements [V l, V l + V) of each row
     const int64_t left = jend - j0;
     const int nj = left <= 0 ? 0 : left >= 32 ? 32 : static_cast<int>(left);
-    const int e0 = V * lane;
-    const T* nk = static_cast<const T*>(p.new_key);
-    const T* nv = static_cast<const T*>(p.new_value);
-    const T* kc = static_cast<const T*>(p.key_cache);
-    const T* vc = static_cast<const T*>(p.value_cache);
-    const T* gko = static_cast<const T*>(bp.d_key_out);
-    const T* gvo = static_cast<const T*>(bp.d_value_out);
     // the rows of slot j this lane reads: K'_j, V'_j and the returned caches' gradient
     auto fetch = [&](int64_t j, uint32_t (&k)[KW], uint32_t (&v)[KW], uint32_t (&gk)[KW],
                      uint32_t (&gv)[KW]) {
@@ -448,11 +464,6 @@ __global__ void __launch_bounds__(kBwdWarps * 32, (RowsLayout<NR, V>::kBlocks))
         if (gko) LV::load(gko + cr, gk);
         if (gvo) LV::load(gvo + cr, gv);
     };
-    float dqr[Lay::kRegDq ? NR : 1][V];
-#pragma unroll
-    for (int r = 0; r < (Lay::kRegDq ? NR : 1); ++r)
-#pragma unroll
-        for (int i = 0; i < V; ++i) dqr[r][i] = 0.f;
     uint32_t nk_w[KW], nv_w[KW], ngk_w[KW], ngv_w[KW];
     if (nj > 0) fetch(j0, nk_w, nv_w, ngk_w, ngv_w);
     for (int jj = 0; jj < nj; ++jj) {
@@ -531,9 +542,10 @@ __global__ void __launch_bounds__(kBwdWarps * 32, (RowsLayout<NR, V>::kBlocks))
             LV::store(static_cast<T*>(bp.d_value_cache) + (u * p.M + j) * W + e0, ov_w);
         }
     }
+    }  // slot blocks
     // the query-gradient sums into the fp32 accumulator
     if constexpr (Lay::kRegDq) {
-        if (nj > 0) {
+        {
 #pragma unroll
             for (int r = 0; r < NR; ++r)
 #pragma unroll
@@ -629,7 +641,10 @@ cudaError_t launch_t(const BwdParams& bp, bool words16, cudaStream_t stream,
         if (e != cudaSuccess) return e;
     }
     if (bp.rows_smem > 0) {
-        const dim3 grid(static_cast<unsigned>((p.M + kBwdWarps * 32 - 1) / (kBwdWarps * 32)),
+        // at most kRowsGridX blocks per unit, each striding over the unit's
+        // slot blocks below its new length
+        const int64_t sblocks = (p.M + kBwdWarps * 32 - 1) / (kBwdWarps * 32);
+        const dim3 grid(static_cast<unsigned>(std::min<int64_t>(sblocks, kRowsGridX)),
                         static_cast<unsigned>(U));
         auto launch = [&](auto kern) -> cudaError_t {
             cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
