@@ -67,6 +67,7 @@ PATH_KERNELS_READONLY = {
 PATH_KERNELS_BACKWARD = {
     path: first + ["bwd_rowdot_kernel", "bwd_kv_kernel", "bwd_copy_kernel", "bwd_dq_kernel"]
     for path, first in (("fused", ["fused_step_kernel", "finalize_merge_kernel"]),
+                        ("decode", ["decode_tc_kernel", "finalize_merge_kernel"]),
                         ("generic", ["generic_attend_kernel", "finalize_merge_kernel"]),
                         ("tensor", ["tc_step_kernel", "finalize_merge_kernel",
                                     "finalize_rows_kernel"]))}

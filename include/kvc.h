@@ -384,7 +384,7 @@ KVC_API size_t kvc_backward_workspace_bytes(const kvc_dims *dims);
 /* The kernels kvc_step_backward launches for `dims` on the current device
  * when every buffer is 16-byte aligned: returns their number (> 0) or a
  * negative KVC_E_* code. *stats_path (nullable) gets the statistics pass's
- * step path ("tensor", "fused" or "generic") and *slot_kernel (nullable) the
+ * step path ("tensor", "decode", "fused" or "generic") and *slot_kernel (nullable) the
  * kernel of the slots below the new length ("bwd_kv_rows_kernel",
  * "bwd_kv_tc_kernel", "bwd_kv_tiled_kernel" or "bwd_kv_kernel"); the strings
  * are static. Launches nothing. */

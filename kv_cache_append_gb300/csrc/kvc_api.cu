@@ -383,9 +383,11 @@ void dec_tiling(const kvc_dims& d, Plan* pl) {
 }
 
 // Shared memory: barriers | abort flag | tile metadata | exchange buffers |
-// two P^T buffers (16 rows x 128 slots) | stages of K (128 x D), V (128 x Dv)
+// two P^T buffers (16 rows x 128 slots; four with src) | stages of K (128 x D), V (128 x Dv)
 // and the unit's 16 query rows, all in 64-element column blocks.
-bool dec_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
+// src: the statistics-pass instance, which also keeps the low parts of P^T
+// (two more buffers) for an fp32-accurate context.
+bool dec_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl, bool src = false) {
     if (!dec_shapes(d)) return false;
     *pl = Plan();
     dec_tiling(d, pl);
@@ -398,7 +400,7 @@ bool dec_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
     pl->dec_off_red = static_cast<int>(off);
     off = align_up(off + 2 * 2 * 16 * 4 * 4 + 2 * 2 * 4 * 4 + 2 * 16 * 4, 1024);
     pl->dec_off_pt = static_cast<int>(off);
-    off += 2 * 2 * 16 * 128;
+    off += (src ? 2 : 1) * 2 * 2 * 16 * 128;
     pl->off_stages = static_cast<int>(off);
     const int64_t stage = (nkb + nvb) * kDecT * 128 + nkb * 16 * 128;
     pl->stage_bytes = static_cast<int>(stage);
@@ -496,7 +498,8 @@ struct StepMode {
     int64_t block_size = 0, num_blocks = 0;
     // the backward's statistics pass (with inplace): the step's kernels read
     // the inputs and write nothing but the workspace: no cache row write, the
-    // CUDA-core or generic path only (fp32 scores), the context also in fp32
+    // decode tensor-core, CUDA-core or generic path only (fp32 scores), the
+    // context also in fp32
     bool stats_only = false;
     // the two-pass tensor-core step may be taken (the backward's statistics
     // pass keeps the one-pass form, whose kernels its event list names)
@@ -542,9 +545,12 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     const bool tc_pages = !paged || mode.block_size % kTcT == 0 ||
                           (kTcT % mode.block_size == 0 && mode.block_size >= 8);
     Plan pl;
-    const bool tc_ok = !mode.stats_only && ptrs_aligned && aligned16(query) && tc_pages;
+    // the statistics pass may take the decode kernel (which then sources the
+    // appended rows itself), not the tensor-core step (fp16 P values, no fp32 scores)
+    const bool dec_ok = ptrs_aligned && aligned16(query) && tc_pages;
+    const bool tc_ok = !mode.stats_only && dec_ok;
     if (!(tc_ok && tc_plan(d, dev.sms, dev.smem_optin, &pl)) &&
-        !(tc_ok && inplace && dec_plan(d, dev.sms, dev.smem_optin, &pl)) &&
+        !(dec_ok && inplace && dec_plan(d, dev.sms, dev.smem_optin, &pl, mode.stats_only)) &&
         !(ptrs_aligned &&
           ((inplace && fused_plan(d, dev.sms, dev.smem_optin, aligned16(query), &pl,
                                   kStageTargetInplace)) ||
@@ -709,6 +715,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
             DecParams dp;
             std::memset(&dp, 0, sizeof(dp));
             dp.p = p;
+            dp.src_new = mode.stats_only ? 1 : 0;
             const int64_t bh = paged ? std::min<int64_t>(kDecT / 2, mode.block_size) : kDecT / 2;
             const bool ok_maps =
                 (paged ? cache_map(&dp.tm_k, key_cache, d.dtype, d.D, mode.block_size,
@@ -1264,6 +1271,8 @@ int kvc_backward_plan_info(const kvc_dims* dims, const char** stats_path,
     if (ch.tc_stats && Lw.tc_room) {
         stats = "tensor";
         stats_kernels = 3;  // plus the row writer
+    } else if (dec_plan(d, dev.sms, dev.smem_optin, &pl, true)) {
+        stats = "decode";
     } else if (fused_plan(d, dev.sms, dev.smem_optin, true, &pl, kStageTargetInplace) ||
                fused_plan(d, dev.sms, dev.smem_optin, true, &pl, kStageTargetBytes)) {
         stats = "fused";
@@ -1351,8 +1360,10 @@ int backward_impl(const kvc_dims* dims, const void* query, const void* new_key,
 
     // 1. the step's statistics over the inputs: each valid row's (m, 1/l) and
     // its fp32 context, and either its fp32 scores (the step kernels run with
-    // no cache copy and no row write) or, for the tensor-core slot kernel, its
-    // attention rows (the tensor-core step into workspace copies of its outputs)
+    // no cache copy and no row write; the decode kernel, where it takes the
+    // shape, sources the appended rows from new_key / new_value) or, for the
+    // tensor-core slot kernel, its attention rows (the tensor-core step into
+    // workspace copies of its outputs)
     StepMode mode;
     mode.ctx_f32 = reinterpret_cast<float*>(ws + Lw.ctx_f32);
     StepParams p;
@@ -1398,6 +1409,8 @@ int backward_impl(const kvc_dims* dims, const void* query, const void* new_key,
     bp.drow = reinterpret_cast<float*>(ws + Lw.drow);
     bp.dq_acc = dq_acc;
     bp.attn_rows = tc_stats ? ws + Lw.attn : nullptr;
+    // (the scores, the attention rows and the workspace start on 256 bytes)
+    bp.rowdot_vec = d.M % 8 == 0 && aligned16(d_attention) ? 1 : 0;
     bp.stage_rows = ch.stage_rows;
     bp.rows_smem = ch.rows_smem;
     bp.tc_smem = ch.tc_smem;

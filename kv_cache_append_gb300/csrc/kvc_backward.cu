@@ -65,9 +65,23 @@ __device__ __forceinline__ float ld(const void* base, int64_t i) {
     return Storage<T>::to_float(static_cast<const T*>(base)[i]);
 }
 
+// Eight consecutive elements at p (16-byte aligned), widened to fp32.
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float* f) {
+    if constexpr (std::is_same<T, float>::value) {
+        const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    } else {
+        Storage<T>::widen16(*reinterpret_cast<const uint4*>(p), f);
+    }
+}
+
 // D for every query row, one block per row (its slots spread over the
 // block's threads, the warps' sums added in shared memory); a_j from the fp32
 // scores, or from the attention rows when the statistics pass wrote them.
+// bp.rowdot_vec: eight slots per thread and load (M a multiple of 8, the rows
+// 16-byte aligned); the slots past the row's last allowed one are masked.
 template <typename T>
 __global__ void __launch_bounds__(kBwdWarps * 32) bwd_rowdot_kernel(const BwdParams bp) {
     __shared__ float part[kBwdWarps];
@@ -82,7 +96,26 @@ __global__ void __launch_bounds__(kBwdWarps * 32) bwd_rowdot_kernel(const BwdPar
     }
     const RowStat rs = p.rowstat[row];
     float acc = 0.f;
-    if (bp.d_attention && bp.attn_rows) {  // the statistics pass wrote the attention rows
+    if (bp.d_attention && bp.rowdot_vec) {
+        const int64_t nj = static_cast<int64_t>(rs.lim) + 1;
+        const T* da = static_cast<const T*>(bp.d_attention) + row * p.M;
+        const T* ar = bp.attn_rows ? static_cast<const T*>(bp.attn_rows) + row * p.M : nullptr;
+        const float* sc = p.scores + row * p.M;
+        for (int64_t j0 = 8 * static_cast<int64_t>(threadIdx.x); j0 < nj; j0 += 8 * blockDim.x) {
+            float g[8], a[8];
+            load8<T>(da + j0, g);
+            if (ar) {
+                load8<T>(ar + j0, a);
+            } else {
+                load8<float>(sc + j0, a);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a[e] = fast_exp2(a[e] - rs.mx) * rs.inv_l;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (j0 + e < nj) acc = fmaf(a[e], g[e], acc);
+        }
+    } else if (bp.d_attention && bp.attn_rows) {  // the statistics pass wrote the attention rows
         for (int64_t j = threadIdx.x; j <= rs.lim; j += blockDim.x)
             acc += ld<T>(bp.attn_rows, row * p.M + j) * ld<T>(bp.d_attention, row * p.M + j);
     } else if (bp.d_attention) {

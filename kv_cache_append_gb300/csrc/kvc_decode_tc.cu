@@ -43,6 +43,16 @@
 // and row writer (kvc_finalize.cu) finish the step ("stable softmax on
 // allowed keys", bullet 5).
 //
+// The gradients' statistics pass runs this kernel over the inputs, whose
+// caches do not hold the appended rows (src_new): for the at most Q slots
+// [length, new length) of a unit the softmax thread of the slot replaces the
+// tile's scores by the new key's dot products with the query rows (CUDA
+// cores, fp32) and writes the new value row into the tile before the second
+// product reads it. The gradients need the context to fp32's order (their
+// per-row sum D = dcontext . context sits under differences a (g - D)), so
+// that instance also writes P^T's low parts (P - hi, rounded) into two more
+// buffers and adds a second product V^T lo^T.
+//
 // Tensor memory (64 columns x 128 lanes, fp32): S^T buffers at columns 0 and
 // 16, O^T at 32 (lane = value column, column = query row).
 #include <cuda.h>
@@ -250,7 +260,7 @@ __device__ void dec_producer(const DecParams& dp, unsigned char* smem, DecBars b
 
 // One thread issues every tensor-core instruction of the CTA.
 __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars bars,
-                               volatile int* abort, uint32_t tmem, bool bf16) {
+                               volatile int* abort, uint32_t tmem, bool bf16, bool lo) {
     const StepParams& p = dp.p;
     const uint32_t stage0 = smem_addr(smem + p.off_stages);
     const uint32_t pt0 = smem_addr(smem + p.dec_off_pt);
@@ -279,6 +289,13 @@ __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars
             tc_mma(tmem + kColO, smem_desc_sw128(sV + kk * 16 * 128, kBlk, 1024),
                    smem_desc_sw128(sP + (kk >> 2) * kNBlk + (kk & 3) * 32, 16, 1024), idesc_o,
                    !(first && kk == 0));
+        if (lo) {  // the low parts of P^T, two buffers on
+#pragma unroll
+            for (int kk = 0; kk < kDT / 16; ++kk)
+                tc_mma(tmem + kColO, smem_desc_sw128(sV + kk * 16 * 128, kBlk, 1024),
+                       smem_desc_sw128(sP + 4 * kNBlk + (kk >> 2) * kNBlk + (kk & 3) * 32, 16, 1024),
+                       idesc_o, true);
+        }
         tc_commit(bars.o_done(pb));
         tc_commit(bars.empty(stage));
         ++pv_count;
@@ -339,7 +356,7 @@ __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars
     mbar_wait(bars.drained(), 0u, &never);
 }
 
-template <typename T, int NR, int SG>
+template <typename T, int NR, int SG, bool SRC>
 __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars bars,
                             volatile int* abort, uint32_t tmem) {
     using S = Storage<T>;
@@ -437,6 +454,35 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
             if (lane == 0) mbar_arrive(bars.s_free(sbuf), 1u);
             sbuf ^= 1;
             const int j0 = mt.i * kDT, j = j0 + t;
+            unsigned char* stage = stages + static_cast<int64_t>(s) * p.stage_bytes;
+            if (SRC && j >= L && j < N) {
+                // an appended row the cache does not hold: its dot products
+                // with the group's query rows (the stage's Q tile), on the
+                // CUDA cores in fp32, replace the tile's column
+                const unsigned char* krow = static_cast<const unsigned char*>(p.new_key) +
+                                            (u * p.Q + (j - L)) * p.D * sizeof(T);
+                const unsigned char* qt = stage + (nkb + nvb) * kBlk;
+                float acc[NW];
+#pragma unroll
+                for (int r = 0; r < NW; ++r) acc[r] = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < nkb * 8; ++c) {  // 16-byte chunks of the key row
+                    float kf[8];
+                    S::widen16(*reinterpret_cast<const uint4*>(krow + c * 16), kf);
+#pragma unroll
+                    for (int r = 0; r < NW; ++r) {
+                        const int rr = r0 + r;
+                        float qf[8];
+                        S::widen16(*reinterpret_cast<const uint4*>(
+                                       qt + (c >> 3) * kNBlk + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)),
+                                   qf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[r] = fmaf(qf[e], kf[e], acc[r]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < NW; ++r) sv[r] = acc[r];
+            }
             bool need = false;
             float* srow = p.scores + rowoff0 + r0 * p.M + j;
 #pragma unroll
@@ -487,15 +533,28 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
                 const float e = (j <= lim[r]) ? fast_exp2(sv[r] - mref[r]) : 0.f;
                 lsum[r] += e;
                 const int rr = r0 + r;
-                *reinterpret_cast<T*>(pbox + rr * 128 + ((ck ^ (rr & 7)) << 4) + e2) = S::from_float(e);
+                const T hi = S::from_float(e);
+                *reinterpret_cast<T*>(pbox + rr * 128 + ((ck ^ (rr & 7)) << 4) + e2) = hi;
+                if (SRC)  // the statistics pass: P = hi + lo, its context accurate to fp32's order
+                    *reinterpret_cast<T*>(pbox + 4 * kNBlk + rr * 128 + ((ck ^ (rr & 7)) << 4) + e2) =
+                        S::from_float(e - S::to_float(hi));
             }
             if (g == 0 && j >= N) {  // a value row past the new length: zero in the tile
-                unsigned char* vrow =
-                    stages + static_cast<int64_t>(s) * p.stage_bytes + nkb * kBlk + t * 128;
+                unsigned char* vrow = stage + nkb * kBlk + t * 128;
                 for (int b = 0; b < nvb; ++b)
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         *reinterpret_cast<uint4*>(vrow + b * kBlk + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+            } else if (SRC && g == 0 && j >= L) {  // an appended value row, into the tile
+                unsigned char* vrow = stage + nkb * kBlk + t * 128;
+                const unsigned char* src = static_cast<const unsigned char*>(p.new_value) +
+                                           (u * p.Q + (j - L)) * p.Dv * sizeof(T);
+#pragma unroll 1
+                for (int b = 0; b < nvb; ++b)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(vrow + b * kBlk + ((c ^ (t & 7)) << 4)) =
+                            *reinterpret_cast<const uint4*>(src + (b * 8 + c) * 16);
             }
             if (rescale_o && !first_tile) {
                 // O^T must be quiescent: the previous product has finished, this
@@ -545,7 +604,7 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
     }
 }
 
-template <typename T, int NR, int SG>
+template <typename T, int NR, int SG, bool SRC>
 __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
     decode_tc_kernel(const __grid_constant__ DecParams dp) {
     using Roles = DecRoles<SG>;
@@ -571,7 +630,7 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
         fence_mbar_init();
     }
     // P^T rows past the unit's rows stay zero: clear both buffers once
-    for (int i = threadIdx.x; i < 2 * 2 * kNBlk / 16; i += Roles::threads)
+    for (int i = threadIdx.x; i < (SRC ? 2 : 1) * 2 * 2 * kNBlk / 16; i += Roles::threads)
         reinterpret_cast<uint4*>(smem + p.dec_off_pt)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_async_shared();
     if (warp == Roles::mma) {
@@ -584,10 +643,10 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
 
     if (warp < Roles::soft) {
-        dec_softmax<T, NR, SG>(dp, smem, bars, abort, tmem);
+        dec_softmax<T, NR, SG, SRC>(dp, smem, bars, abort, tmem);
     } else if (warp == Roles::mma) {
         if ((threadIdx.x & 31) == 0)
-            dec_mma_issuer(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value);
+            dec_mma_issuer(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value, SRC);
     } else if (warp == Roles::prod) {
         if ((threadIdx.x & 31) == 0) dec_producer(dp, smem, bars, abort);
     }
@@ -604,9 +663,9 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
 #define KVC_DEC_GROUPS8 2
 #endif
 
-template <typename T, int NR, int SG>
+template <typename T, int NR, int SG, bool SRC>
 cudaError_t launch_t(const DecParams& dp, size_t smem, cudaStream_t stream) {
-    auto kern = decode_tc_kernel<T, NR, SG>;
+    auto kern = decode_tc_kernel<T, NR, SG, SRC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -616,10 +675,18 @@ cudaError_t launch_t(const DecParams& dp, size_t smem, cudaStream_t stream) {
 
 template <typename T>
 cudaError_t launch_rows(const DecParams& dp, int nr, size_t smem, cudaStream_t stream) {
+    // SRC: the appended rows come from new_key / new_value (the statistics pass)
+    if (dp.src_new) {
+        switch (nr) {
+            case 4: return launch_t<T, 4, 1, true>(dp, smem, stream);
+            case 8: return launch_t<T, 8, KVC_DEC_GROUPS8, true>(dp, smem, stream);
+            default: return launch_t<T, 16, 2, true>(dp, smem, stream);
+        }
+    }
     switch (nr) {
-        case 4: return launch_t<T, 4, 1>(dp, smem, stream);
-        case 8: return launch_t<T, 8, KVC_DEC_GROUPS8>(dp, smem, stream);
-        default: return launch_t<T, 16, 2>(dp, smem, stream);
+        case 4: return launch_t<T, 4, 1, false>(dp, smem, stream);
+        case 8: return launch_t<T, 8, KVC_DEC_GROUPS8, false>(dp, smem, stream);
+        default: return launch_t<T, 16, 2, false>(dp, smem, stream);
     }
 }
 

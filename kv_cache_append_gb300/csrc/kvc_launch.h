@@ -43,6 +43,11 @@ struct DecParams {
     CUtensorMap tm_v;
     CUtensorMap tm_q;
     StepParams p;
+    // 1 (in place): the caches do not hold the appended rows (nothing wrote
+    // them: the gradients' statistics pass over the inputs), so the slots
+    // [length, new length) take their keys and values from new_key /
+    // new_value; selects the kernel instance that does so.
+    int src_new;
 };
 
 // Attention of the steps that copy no cache (in place, read-only, paged) on
@@ -74,6 +79,8 @@ struct BwdParams {
     int tiled_smem;           // > 0: bytes of bwd_kv_tiled_kernel's shared memory (units of > 4 rows)
     int tc_smem;              // > 0: bytes of bwd_kv_tc_kernel's shared memory (16-bit, 17-128 rows)
     int64_t tc_tiles_per_cta; // 128-slot tiles of one unit per CTA of bwd_kv_tc_kernel
+    int rowdot_vec;           // 1: M % 8 == 0 and the attention-gradient (and attention) rows
+                              // 16-byte aligned: bwd_rowdot_kernel loads 8 slots at a time
     float scale;              // the scores' scale (natural-log domain)
     int64_t slots_per_block;  // cache slots per block of bwd_kv_kernel
 };

@@ -129,7 +129,11 @@ def test_gradient_bound(dtype):
     cut = ref.copy()
     cut[:, :, :100] = 0.0
     assert bounds.grad_ratio(cut, ref, dtype) > 1.0
-    # an entry whose reference is exactly zero must come back exactly zero
+    # an entry the structure makes zero must come back exactly zero; one that
+    # is zero by cancellation keeps the absolute term
     bad = got.copy()
     bad[0, 0, 350, 0] = 1e-30
-    assert bounds.grad_ratio(bad, ref, dtype) > 1.0
+    structural = np.zeros(ref.shape, dtype=bool)
+    structural[:, :, 300:] = True
+    assert bounds.grad_ratio(bad, ref, dtype, exact_zero=structural) > 1.0
+    assert bounds.grad_ratio(bad, ref, dtype) <= 1.0

@@ -45,17 +45,32 @@ def upstream(x, seed, which=("key_cache", "value_cache", "attention", "context")
             for k in shapes}
 
 
+def structural_zeros(x, ref):
+    """The row gradients the step's structure makes zero: query rows t >= n_b
+    (invalid rows) and new rows t >= n_b (nothing appended), n_b = 0 for a
+    row outside the contract."""
+    counts = x.append_mask.to(torch.int64).cumprod(1).sum(1).numpy()
+    n = np.where(np.asarray(ref["flags"]) != 0, 0, counts)
+    Q = x.query.shape[2]
+    invalid = np.arange(Q)[None, :] >= n[:, None]          # [B, Q]
+    return {"query": invalid[:, None, :, None], "new_key": invalid[:, None, :, None],
+            "new_value": invalid[:, None, :, None]}
+
+
 def check_grads(got, ref, x, where=""):
-    """Every gradient within bounds.grad_ratio. With no gradient reaching the
-    returned caches (grads of attention/context only), the cache gradients
-    below the old length are the attention-derived dK', dV' alone: zeroing
-    them, or scaling the query gradient by 0.9, must exceed the bound."""
+    """Every gradient within bounds.grad_ratio, the structurally zero row
+    gradients exactly zero. With no gradient reaching the returned caches
+    (grads of attention/context only), the cache gradients below the old
+    length are the attention-derived dK', dV' alone: zeroing them, or scaling
+    the query gradient by 0.9, must exceed the bound."""
     dt = x.query.dtype
+    zeros = structural_zeros(x, ref)
     for name in NAMES:
         r = ref["d_" + name]
         gw = got[name]
         gw = gw.double().cpu().numpy() if torch.is_tensor(gw) else gw
-        ratio = bounds.grad_ratio(gw, r, dt)
+        ez = np.broadcast_to(zeros[name], r.shape) if name in zeros else None
+        ratio = bounds.grad_ratio(gw, r, dt, exact_zero=ez)
         assert ratio <= 1.0, (where, name, ratio)
 
 
@@ -149,6 +164,16 @@ CASES = {
                                    lengths=("uniform", 0, 515), counts=("uniform", 0, 4)),
     "tc_f16_D128_R32_staged": Spec(B=2, Hq=8, Hk=1, Q=4, D=128, Dv=128, M=384, dtype="f16",
                                    lengths=("uniform", 120, 379)),
+    # statistics on the decode tensor-core kernel (16-bit, Dv = 128, at most 16
+    # rows), which takes the appended rows from new_key / new_value: 16 rows
+    # whose new rows straddle the first 128-slot tile's end, D = 256 (8 rows)
+    # (the tiled slot kernel) and D = 64 (4 rows, the generic slot kernel)
+    "dec_bf16_R16_tile_edge": Spec(B=6, Hq=16, Hk=4, Q=4, D=128, Dv=128, M=400, dtype="bf16",
+                                   lengths=("uniform", 123, 129), counts=("uniform", 0, 4)),
+    "dec_f16_D256_R8": Spec(B=3, Hq=8, Hk=2, Q=2, D=256, Dv=128, M=300, dtype="f16",
+                            lengths=("uniform", 0, 297), counts=("uniform", 0, 2)),
+    "dec_bf16_D64_R4": Spec(B=4, Hq=4, Hk=1, Q=1, D=64, Dv=128, M=260, dtype="bf16",
+                            lengths=("uniform", 0, 259)),
 }
 
 
@@ -167,7 +192,13 @@ SLOT = {"tiny_fp32": "bwd_kv_kernel", "decode_bf16_ragged_M": "bwd_kv_rows_kerne
         "tiled_f16_D64_Dv128_R8": "bwd_kv_tiled_kernel",
         "tc_bf16_D64_R128_ragged": "bwd_kv_tc_kernel", "tc_f16_D128_R17": "bwd_kv_tc_kernel",
         "tc_bf16_D128_R32_hot": "bwd_kv_tc_kernel", "tc_bf16_D64_R64_staged": "bwd_kv_tc_kernel",
-        "tc_f16_D128_R32_staged": "bwd_kv_tc_kernel"}
+        "tc_f16_D128_R32_staged": "bwd_kv_tc_kernel",
+        "dec_bf16_R16_tile_edge": "bwd_kv_rows_kernel", "dec_f16_D256_R8": "bwd_kv_tiled_kernel",
+        "dec_bf16_D64_R4": "bwd_kv_kernel"}
+
+# the cases whose statistics pass runs the decode tensor-core kernel
+DECODE_STATS = ("decode_bf16_ragged_M", "specdec_bf16_hot", "tiled_f16_D64_Dv128_R8",
+                "dec_bf16_R16_tile_edge", "dec_f16_D256_R8", "dec_bf16_D64_R4")
 
 
 def plan_of(spec):
@@ -186,7 +217,13 @@ def test_backward_plan():
     assert plan_of(CASES["tc_bf16_D64_R128_ragged"])[:2] == (7, "tensor")
     assert plan_of(CASES["tiled_bf16_D128_R40_ragged"])[:2] == (6, "fused")
     assert plan_of(workloads.SPECS["chunked_append"]) == (6, "fused", "bwd_kv_tiled_kernel")
-    assert plan_of(workloads.SPECS["gqa_decode"]) == (6, "fused", "bwd_kv_rows_kernel")
+    # 16-bit, Dv = 128, at most 16 rows: the decode tensor-core kernel
+    assert plan_of(workloads.SPECS["gqa_decode"]) == (6, "decode", "bwd_kv_rows_kernel")
+    assert plan_of(workloads.SPECS["ragged_specdec"]) == (6, "decode", "bwd_kv_rows_kernel")
+    for name in DECODE_STATS:
+        assert plan_of(CASES[name])[1] == "decode", name
+    assert plan_of(CASES["rows_f32_D256_R16"])[1] != "decode"   # fp32
+    assert plan_of(CASES["rows_f16_D64_R8"])[1] != "decode"     # Dv = 64
     assert plan_of(workloads.SPECS["gqa_decode"].replace(Q=0))[0] == 2
 
 
@@ -210,6 +247,21 @@ def test_backward_poisoned_tail(name):
         x.key_cache[b, :, n_b:] = float("inf")
         x.value_cache[b, :, n_b:] = float("nan")
     check(x, upstream(x, 8))
+
+
+@pytest.mark.parametrize("name", DECODE_STATS)
+def test_backward_overwritten_slots_poisoned(name):
+    """The statistics pass reads the inputs, whose caches still hold the old
+    contents at the slots the new rows overwrite: Inf keys and NaN values
+    there, and from the new length on, reach no gradient (the decode kernel
+    replaces those slots' scores and value rows by the new rows')."""
+    x = workloads.generate(CASES[name], 9)
+    for b in range(x.key_cache.shape[0]):
+        L = max(0, int(x.lengths[b]))
+        x.key_cache[b, :, L:] = float("inf")
+        x.value_cache[b, :, L:] = float("nan")
+    check(x, upstream(x, 10))
+    check(x, upstream(x, 11, which=("attention", "context")))
 
 
 @pytest.mark.parametrize("which", [("context",), ("attention",), ("key_cache", "value_cache"),
