@@ -1212,7 +1212,7 @@ bool bwd_layout(const kvc_dims& d, BwdLayout* L) {
 // acc_aligned: the context gradient and the query-gradient accumulator too.
 struct BwdChoice {
     int stage_rows = 0, rows_smem = 0, tc_smem = 0, tiled_smem = 0;
-    int64_t tc_tiles_per_cta = 1;
+    int64_t tc_ctas = 1;
     bool tc_stats = false;
 };
 BwdChoice bwd_choose(const kvc_dims& d, const DeviceInfo& dev, bool aligned, bool acc_aligned) {
@@ -1223,20 +1223,16 @@ BwdChoice bwd_choose(const kvc_dims& d, const DeviceInfo& dev, bool aligned, boo
     c.stage_rows = need <= dev.smem_optin ? 1 : 0;
     // the few-rows kernel (D = Dv in {64, 128, 256})
     const bool widths = d.D == d.Dv && (d.D == 64 || d.D == 128 || d.D == 256);
-    const int64_t rows_smem = widths ? bwd_rows_smem_bytes(R, d.D) : 0;
-    c.rows_smem = (R <= KVC_BWD_ROWS_MAX && widths && aligned && rows_smem <= dev.smem_optin)
-                      ? static_cast<int>(rows_smem) : 0;
     // the tensor-core kernel (16-bit, 17 to 128 rows, widths that fit it)
     const int64_t tc_smem = bwd_tc_smem_bytes(d.D, d.Dv);
-    c.tc_smem = (c.rows_smem == 0 && es == 2 && bwd_tc_fits(R, d.D, d.Dv) && aligned &&
-                 acc_aligned && tc_smem <= dev.smem_optin)
-                    ? static_cast<int>(tc_smem) : 0;
-    if (c.tc_smem > 0) {  // about two CTAs per SM over all units' tiles
-        const int64_t tiles = (d.M + 127) / 128, units = d.B * d.Hk;
-        const int64_t ctas = 2 * static_cast<int64_t>(dev.sms > 0 ? dev.sms : 1);
-        const int64_t per = (tiles * units + ctas - 1) / ctas;
-        c.tc_tiles_per_cta = per < 1 ? 1 : per;
-    }
+    const bool tc_fit = es == 2 && bwd_tc_fits(R, d.D, d.Dv) && aligned && acc_aligned &&
+                        tc_smem <= dev.smem_optin;
+    const int64_t rows_smem = widths ? bwd_rows_smem_bytes(R, d.D) : 0;
+    c.rows_smem = (!tc_fit && R <= KVC_BWD_ROWS_MAX && widths && aligned &&
+                   rows_smem <= dev.smem_optin)
+                      ? static_cast<int>(rows_smem) : 0;
+    c.tc_smem = tc_fit ? static_cast<int>(tc_smem) : 0;
+    c.tc_ctas = dev.sms > 0 ? dev.sms : 1;  // one CTA per SM, the tiles split evenly
     // the tiled kernel (more rows; D and Dv multiples of 64 up to 256)
     const int64_t tiled_smem = bwd_tiled_smem_bytes(d.D, d.Dv);
     const bool tiled_widths = d.D % 64 == 0 && d.Dv % 64 == 0 && d.D <= 256 && d.Dv <= 256;
@@ -1414,7 +1410,7 @@ int backward_impl(const kvc_dims* dims, const void* query, const void* new_key,
     bp.stage_rows = ch.stage_rows;
     bp.rows_smem = ch.rows_smem;
     bp.tc_smem = ch.tc_smem;
-    bp.tc_tiles_per_cta = ch.tc_tiles_per_cta;
+    bp.tc_ctas = ch.tc_ctas;
     bp.tiled_smem = ch.tiled_smem;
     bp.scale = static_cast<float>(scale);
     bp.slots_per_block = 256;

@@ -62,7 +62,7 @@ constexpr int kBlk = 128 * 128;         // one 64-element column block of a 128-
 constexpr int kMaxChunks = 16 / kParts;  // 32-column chunks of an epilogue thread (D, Dv <= 256)
 
 struct BtcLayout {
-    uint32_t k, v, q, c, a, ds, stats, bar, slot, flag, total;
+    uint32_t k, v, q, c, a, ds, stats, scan, bar, slot, flag, total;
 };
 
 __host__ __device__ inline BtcLayout btc_layout(int D, int Dv) {
@@ -75,6 +75,7 @@ __host__ __device__ inline BtcLayout btc_layout(int D, int Dv) {
     L.a = off;  off += 2 * kBlk;                               // a^T  [slots][rows]
     L.ds = off; off += 2 * kBlk;                               // ds^T [slots][rows]
     L.stats = off; off += 4 * kTR * 4;                         // m, 1/l, D, causal limit per row
+    L.scan = off; off += (kTcWarps + 3) * 8;                   // block scan, located tile
     L.bar = off;  off += 8;
     L.slot = off; off += 4;
     L.flag = off; off += 4;
@@ -115,6 +116,57 @@ __device__ __forceinline__ void store32(T* p, const float (&f)[32]) {
                        pack2<T>(f[8 * k + 4], f[8 * k + 5]), pack2<T>(f[8 * k + 6], f[8 * k + 7]));
 }
 
+// Inclusive block-wide sum scan of v (every thread of the block calls it);
+// *total gets the block's sum. sh: kTcWarps + 1 int64 of shared memory.
+__device__ __forceinline__ int64_t block_scan(int64_t v, int64_t* sh, int64_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[warp] = x;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int64_t run = 0;
+        for (int w = 0; w < kTcWarps; ++w) {
+            const int64_t t = sh[w];
+            sh[w] = run;
+            run += t;
+        }
+        sh[kTcWarps] = run;
+    }
+    __syncthreads();
+    const int64_t r = x + sh[warp];
+    *total = sh[kTcWarps];
+    __syncthreads();  // sh is reused by the next call
+    return r;
+}
+
+// One unit of the walk: its batch row's append and its 128-slot tiles.
+struct BtcUnit {
+    int64_t u, row0, L, n, jend, tiles;
+};
+__device__ __forceinline__ BtcUnit btc_unit(const StepParams& p, int64_t u) {
+    BtcUnit x;
+    x.u = u;
+    const int64_t b = u / p.Hk, kv = u - b * p.Hk;
+    const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
+    x.L = ra.L;
+    x.n = ra.n;
+    x.jend = ra.flags ? 0 : ra.L + ra.n;
+    x.row0 = (b * p.Hq + kv * p.G) * p.Q;  // the unit's rows are row0 + r
+    x.tiles = (x.jend + kTJ - 1) / kTJ;
+    return x;
+}
+
+// The CTAs split the tiles of all units (unit-major order, each unit's tiles
+// below its new length) into gridDim.x equal contiguous ranges; a CTA walks its
+// range tile by tile, staging a unit's query and dcontext rows when it enters
+// the unit and adding the unit's query-gradient sums to the accumulator when it
+// leaves it. The tile counts come from the lengths and masks, read by every
+// CTA (a block-wide scan over the batch rows), so no host round trip is needed.
 template <typename T>
 __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_constant__ BwdParams bp) {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -122,21 +174,55 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int D = static_cast<int>(p.D), Dv = static_cast<int>(p.Dv), R = static_cast<int>(p.R);
     const BtcLayout Ly = btc_layout(D, Dv);
-    const int64_t u = blockIdx.y, b = u / p.Hk, kv = u - b * p.Hk;
-    const RowAppend ra = row_append(p.lengths, p.mask, b, p.Q, p.M);
-    const int64_t L = ra.L, n = ra.n;
-    if (blockIdx.x == 0) {  // new-row gradients of the rows t >= n (nothing reaches them): zero
+    const int64_t U = p.B * p.Hk;
+    // new-row gradients of the rows t >= n (nothing reaches them): zero, for the
+    // units u = blockIdx.x (mod gridDim.x)
+    for (int64_t uz = blockIdx.x; uz < U; uz += gridDim.x) {
+        const int64_t n = row_append(p.lengths, p.mask, uz / p.Hk, p.Q, p.M).n;
         for (int64_t i = tid; i < (p.Q - n) * D; i += kTcThreads)
-            static_cast<T*>(bp.d_new_key)[(u * p.Q + n) * D + i] = Storage<T>::from_float(0.f);
+            static_cast<T*>(bp.d_new_key)[(uz * p.Q + n) * D + i] = Storage<T>::from_float(0.f);
         for (int64_t i = tid; i < (p.Q - n) * Dv; i += kTcThreads)
-            static_cast<T*>(bp.d_new_value)[(u * p.Q + n) * Dv + i] = Storage<T>::from_float(0.f);
+            static_cast<T*>(bp.d_new_value)[(uz * p.Q + n) * Dv + i] = Storage<T>::from_float(0.f);
     }
-    const int64_t jend = ra.flags ? 0 : L + n;
-    const int64_t tiles = (jend + kTJ - 1) / kTJ;
-    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * bp.tc_tiles_per_cta;
-    const int64_t i1 = i0 + bp.tc_tiles_per_cta < tiles ? i0 + bp.tc_tiles_per_cta : tiles;
-    if (i0 >= i1) return;  // whole block, before any barrier or tensor memory
-    const int64_t row0 = (b * p.Hq + kv * p.G) * p.Q;  // the unit's rows are row0 + r
+    // this CTA's range [g0, g1) of the tiles of all units
+    int64_t* sh = reinterpret_cast<int64_t*>(smem + Ly.scan);
+    int64_t total = 0;
+    {
+        int64_t mine = 0;
+        for (int64_t b = tid; b < p.B; b += kTcThreads)
+            mine += p.Hk * btc_unit(p, b * p.Hk).tiles;
+        int64_t all = 0;
+        block_scan(mine, sh, &all);
+        total = all;
+    }
+    const int64_t g0 = total * blockIdx.x / gridDim.x, g1 = total * (blockIdx.x + 1) / gridDim.x;
+    if (g0 >= g1) return;  // whole block, before any barrier wait or tensor memory
+    // the batch row holding tile g0, and g0's place in it
+    int64_t* found = sh + kTcWarps + 1;  // [batch row, tiles before it]
+    if (tid == 0) found[0] = -1;
+    __syncthreads();
+    for (int64_t base = 0, run = 0; base < p.B; base += kTcThreads) {
+        const int64_t b = base + tid;
+        const int64_t v = b < p.B ? p.Hk * btc_unit(p, b * p.Hk).tiles : 0;
+        int64_t chunk = 0;
+        const int64_t incl = block_scan(v, sh, &chunk);
+        if (v > 0 && run + incl - v <= g0 && g0 < run + incl) {
+            found[0] = b;
+            found[1] = run + incl - v;
+        }
+        __syncthreads();
+        if (found[0] >= 0) break;  // uniform
+        run += chunk;
+    }
+    if (found[0] < 0) return;  // (not reached: tile g0 < total lies in some batch row)
+    BtcUnit X;
+    int64_t it;  // tile of unit X
+    {
+        const int64_t b = found[0], off = g0 - found[1];
+        const int64_t tb = btc_unit(p, b * p.Hk).tiles;
+        X = btc_unit(p, b * p.Hk + off / tb);
+        it = off % tb;
+    }
     const uint32_t bar = smem_addr(smem + Ly.bar);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + Ly.flag);
     float* s_mx = reinterpret_cast<float*>(smem + Ly.stats);
@@ -148,31 +234,92 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
         *abort = 0;
         fence_mbar_init();
     }
-    for (int r = tid; r < kTR; r += kTcThreads) {  // padded and invalid rows admit no slot
-        const int64_t t = r % p.Q;
-        const bool valid = r < R && t < n;
-        const RowStat rs = valid ? p.rowstat[row0 + r] : RowStat{0.f, 0.f, -1, 0};
-        s_mx[r] = rs.mx;
-        s_il[r] = rs.inv_l;
-        s_dr[r] = valid ? bp.drow[row0 + r] : 0.f;
-        s_lim[r] = valid ? static_cast<int>(L + t) : -1;
-    }
     const T* qg = static_cast<const T*>(p.query);
     const T* dcg = static_cast<const T*>(bp.d_context);
     const T* dag = static_cast<const T*>(bp.d_attention);
-    // the unit's query and dcontext rows; rows of no valid query stay zero
-    stage_sw128<T>(smem + Ly.q, D, R, [&](int r) {
-        return (r % p.Q) < n ? qg + (row0 + r) * D : static_cast<const T*>(nullptr);
-    });
-    stage_sw128<T>(smem + Ly.c, Dv, R, [&](int r) {
-        return (dcg && (r % p.Q) < n) ? dcg + (row0 + r) * Dv : static_cast<const T*>(nullptr);
-    });
+    // padded rows (r >= R) admit no slot and their operand rows stay zero
+    for (int r = R + tid; r < kTR; r += kTcThreads) {
+        s_mx[r] = 0.f;
+        s_il[r] = 0.f;
+        s_dr[r] = 0.f;
+        s_lim[r] = -1;
+    }
+    auto zero_rows = [&](unsigned char* dst, int W) {
+        const int per_row = W / 8;
+        for (int i = tid; i < (kTR - R) * per_row; i += kTcThreads) {
+            const int r = R + i / per_row, c = (i % per_row) * 8;
+            *reinterpret_cast<uint4*>(dst + sw128_off(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    zero_rows(smem + Ly.q, D);
+    zero_rows(smem + Ly.c, Dv);
+    // a unit's rows: statistics, query and dcontext rows (zero for invalid rows)
+    auto stage_unit = [&](const BtcUnit& Y) {
+        for (int r = tid; r < R; r += kTcThreads) {
+            const int64_t t = r % p.Q;
+            const bool valid = t < Y.n;
+            const RowStat rs = valid ? p.rowstat[Y.row0 + r] : RowStat{0.f, 0.f, -1, 0};
+            s_mx[r] = rs.mx;
+            s_il[r] = rs.inv_l;
+            s_dr[r] = valid ? bp.drow[Y.row0 + r] : 0.f;
+            s_lim[r] = valid ? static_cast<int>(Y.L + t) : -1;
+        }
+        const int pq = D / 8, pc = Dv / 8;
+        for (int i = tid; i < R * pq; i += kTcThreads) {
+            const int r = i / pq, c = (i - r * pq) * 8;
+            unsigned char* d = smem + Ly.q + sw128_off(r, c);
+            if ((r % p.Q) < Y.n)
+                cp_async16(d, qg + (Y.row0 + r) * D + c);
+            else
+                *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        for (int i = tid; i < R * pc; i += kTcThreads) {
+            const int r = i / pc, c = (i - r * pc) * 8;
+            unsigned char* d = smem + Ly.c + sw128_off(r, c);
+            if (dcg && (r % p.Q) < Y.n)
+                cp_async16(d, dcg + (Y.row0 + r) * Dv + c);
+            else
+                *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    // the attention gradients of a tile go through the a^T buffer (free from the
+    // previous tile's products to this tile's a / ds pass) when their rows are
+    // whole 16-byte words: [row][slot], 256 bytes a row
+    const bool stage_da =
+        dag && p.M % 8 == 0 && (reinterpret_cast<uintptr_t>(dag) & 15u) == 0;
+    const T* s_da = reinterpret_cast<const T*>(smem + Ly.a);
+    // the slot rows of tile i of unit Y: the input cache below L, the new rows
+    // from L on, zero past N; with stage_da its valid rows' attention gradients too
+    auto stage_tile = [&](const BtcUnit& Y, int64_t i) {
+        const int64_t jb = i * kTJ;
+        const int nj = static_cast<int>(Y.jend - jb < kTJ ? Y.jend - jb : kTJ);
+        const T* kc = static_cast<const T*>(p.key_cache) + Y.u * p.M * D;
+        const T* vc = static_cast<const T*>(p.value_cache) + Y.u * p.M * Dv;
+        const T* nk = static_cast<const T*>(p.new_key) + Y.u * p.Q * D;
+        const T* nv = static_cast<const T*>(p.new_value) + Y.u * p.Q * Dv;
+        if (stage_da) {
+            for (int idx = tid; idx < kTR * (kTJ / 8); idx += kTcThreads) {
+                const int r = idx / (kTJ / 8), c = idx - r * (kTJ / 8);
+                if (r < R && (r % p.Q) < Y.n && 8 * c < nj)
+                    cp_async16(smem + Ly.a + r * (kTJ * 2) + c * 16,
+                               dag + (Y.row0 + r) * p.M + jb + 8 * c);
+            }
+        }
+        stage_sw128<T>(smem + Ly.k, D, nj, [&](int t) {
+            const int64_t j = jb + t;
+            return j >= Y.L ? nk + (j - Y.L) * D : kc + j * D;
+        });
+        stage_sw128<T>(smem + Ly.v, Dv, nj, [&](int t) {
+            const int64_t j = jb + t;
+            return j >= Y.L ? nv + (j - Y.L) * Dv : vc + j * Dv;
+        });
+    };
+    stage_unit(X);
+    stage_tile(X, it);
     if (warp == 0) {
         tmem_alloc(smem_addr(smem + Ly.slot), kTmemCols);
         tmem_relinquish();
     }
-    cp_async_wait_all();
-    fence_async_shared();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -189,41 +336,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
     const uint32_t my_lanes = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     const int ts = 32 * (warp & 3) + lane;  // this thread's slot of a tile (TMEM lane)
     const float qs = p.qscale;
-    const T* kc = static_cast<const T*>(p.key_cache) + u * p.M * D;
-    const T* vc = static_cast<const T*>(p.value_cache) + u * p.M * Dv;
-    const T* nk = static_cast<const T*>(p.new_key) + u * p.Q * D;
-    const T* nv = static_cast<const T*>(p.new_value) + u * p.Q * Dv;
     uint32_t phase = 0;
     bool failed = false;
-    // the attention gradients of a tile go through the a^T buffer (free from the
-    // previous tile's products to this tile's a / ds pass) when their rows are
-    // whole 16-byte words: [row][slot], 256 bytes a row
-    const bool stage_da =
-        dag && p.M % 8 == 0 && (reinterpret_cast<uintptr_t>(dag) & 15u) == 0;
-    const T* s_da = reinterpret_cast<const T*>(smem + Ly.a);
-    // the slot rows of tile i: the input cache below L, the new rows from L on,
-    // zero past N; with stage_da its valid rows' attention gradients too
-    auto stage_tile = [&](int64_t i) {
-        const int64_t jb = i * kTJ;
-        const int nj = static_cast<int>(jend - jb < kTJ ? jend - jb : kTJ);
-        if (stage_da) {
-            for (int idx = tid; idx < kTR * (kTJ / 8); idx += kTcThreads) {
-                const int r = idx / (kTJ / 8), c = idx - r * (kTJ / 8);
-                if (r < R && (r % p.Q) < n && 8 * c < nj)
-                    cp_async16(smem + Ly.a + r * (kTJ * 2) + c * 16,
-                               dag + (row0 + r) * p.M + jb + 8 * c);
-            }
-        }
-        stage_sw128<T>(smem + Ly.k, D, nj, [&](int t) {
-            const int64_t j = jb + t;
-            return j >= L ? nk + (j - L) * D : kc + j * D;
-        });
-        stage_sw128<T>(smem + Ly.v, Dv, nj, [&](int t) {
-            const int64_t j = jb + t;
-            return j >= L ? nv + (j - L) * Dv : vc + j * Dv;
-        });
-    };
-    stage_tile(i0);
     const int part = warp >> 2;               // which of the warps on these TMEM lanes
     const int rbase = kRowsPer * part;         // rows of this thread in the a / ds pass
     const bool keys = part < kParts / 2;       // epilogue: dK' or dV' ...
@@ -231,9 +345,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
     const int nch = W / 32 / (kParts / 2);     // ... its 32-column chunks c0 .. c0 + nch - 1
     const int c0 = (part % (kParts / 2)) * nch;
     const T* go = static_cast<const T*>(keys ? bp.d_key_out : bp.d_value_out);
-    for (int64_t it = i0; it < i1; ++it) {
+    bool first = true;  // the first tile of this CTA in unit X: dq starts from zero
+    for (int64_t g = g0; g < g1; ++g) {
         const int64_t jb = it * kTJ;
-        const int nj = static_cast<int>(jend - jb < kTJ ? jend - jb : kTJ);
+        const int nj = static_cast<int>(X.jend - jb < kTJ ? X.jend - jb : kTJ);
         const int64_t j = jb + ts;  // this thread's slot
         cp_async_wait_all();
         fence_async_shared();
@@ -260,7 +375,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
             const int r = rbase + k;
             dap[k] = 0.f;
             if (dag && j <= s_lim[r])
-                dap[k] = Storage<T>::to_float(stage_da ? s_da[r * kTJ + ts] : dag[(row0 + r) * p.M + j]);
+                dap[k] = Storage<T>::to_float(stage_da ? s_da[r * kTJ + ts] : dag[(X.row0 + r) * p.M + j]);
         }
         bool ok = mbar_wait(bar, phase, abort);
         phase ^= 1u;
@@ -270,8 +385,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
         }
         tc_fence_after();
 #pragma unroll
-        for (int g = 0; g < kRowsPer / 16; ++g) {  // a^T and ds^T of this thread's slot, 16 rows a time
-            const int r0 = rbase + 16 * g;
+        for (int gr = 0; gr < kRowsPer / 16; ++gr) {  // a^T and ds^T of this thread's slot, 16 rows a time
+            const int r0 = rbase + 16 * gr;
             float sv[16], gv[16];
             tmem_ldn<16>(my_lanes + static_cast<uint32_t>(r0), sv);
             tmem_ldn<16>(my_lanes + colG + static_cast<uint32_t>(r0), gv);
@@ -286,7 +401,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
                     if (j <= s_lim[r]) {  // an allowed slot of a valid row (then j < N)
                         const float a = fast_exp2(sv[k + e] * qs - s_mx[r]) * s_il[r];
                         av[e] = a;
-                        dv[e] = a * (dap[16 * g + k + e] + gv[k + e] - s_dr[r]);
+                        dv[e] = a * (dap[16 * gr + k + e] + gv[k + e] - s_dr[r]);
                     }
                 }
                 aw[k / 2] = pack2<T>(av[0], av[1]);
@@ -318,11 +433,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
             for (int kk = 0; kk < kTJ / 16; ++kk)
                 tc_mma(tmem + colQ, smem_desc_sw128(sDS + kk * 16 * 128, kBlk, 1024),
                        smem_desc_sw128(sK + kk * 16 * 128, kBlk, 1024), id_q,
-                       !(it == i0 && kk == 0));
+                       !(first && kk == 0));
             tc_commit(bar);
         }
         // the returned caches' gradient at this thread's slot, loaded while the products run
-        const bool live = ts < nj, is_new = j >= L;
+        const bool live = ts < nj, is_new = j >= X.L;
         uint4 gow[kMaxChunks][4];
 #pragma unroll
         for (int ch = 0; ch < kMaxChunks; ++ch)
@@ -333,7 +448,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
             for (int ch = 0; ch < kMaxChunks; ++ch)
                 if (ch < nch) {
                     const uint4* src =
-                        reinterpret_cast<const uint4*>(go + (u * p.M + j) * W + (c0 + ch) * 32);
+                        reinterpret_cast<const uint4*>(go + (X.u * p.M + j) * W + (c0 + ch) * 32);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) gow[ch][k] = src[k];
                 }
@@ -345,12 +460,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
             break;
         }
         tc_fence_after();
-        if (it + 1 < i1) stage_tile(it + 1);  // the tile buffers are free: the products are done
+        // the next tile: of this unit, or the first of the next unit with tiles
+        // (the tile and row buffers are free: the products are done)
+        BtcUnit Y = X;
+        int64_t inext = it + 1;
+        const bool more = g + 1 < g1;
+        if (more && inext == X.tiles) {  // a later unit holds tile g + 1
+            Y = btc_unit(p, X.u + 1);
+            while (Y.tiles == 0 && Y.u + 1 < U) Y = btc_unit(p, Y.u + 1);
+            inext = 0;
+        }
+        const bool leave = !more || Y.u != X.u;  // the unit's last tile of this CTA
+        if (more) {
+            if (Y.u != X.u) stage_unit(Y);
+            stage_tile(Y, inext);
+        }
         {  // dK' (times scale) or dV' of this thread's slot plus the returned caches' gradient
             const float sc = keys ? bp.scale : 1.f;
-            T* cache_g = static_cast<T*>(keys ? bp.d_key_cache : bp.d_value_cache) + (u * p.M + j) * W;
+            T* cache_g = static_cast<T*>(keys ? bp.d_key_cache : bp.d_value_cache) + (X.u * p.M + j) * W;
             T* dst = is_new ? static_cast<T*>(keys ? bp.d_new_key : bp.d_new_value) +
-                                  (u * p.Q + (j - L)) * W
+                                  (X.u * p.Q + (j - X.L)) * W
                             : cache_g;
             const uint32_t base = my_lanes + (keys ? 0u : colV);
 #pragma unroll
@@ -374,27 +503,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
                 }
             }
         }
-        tc_fence_before();
-        __syncthreads();  // tensor memory is free for the next tile
-    }
-    cp_async_wait_all();  // nothing in flight past an early exit
-    if (!failed) {  // the CTA's query-gradient sums: TMEM lane = row, chunks split over the parts
-        tc_fence_after();
-        {
+        if (leave) {  // the unit's query-gradient sums: TMEM lane = row, chunks split over the parts
             const int r = ts;
-            const bool valid = r < R && (r % p.Q) < n;
+            const bool valid = r < R && (r % p.Q) < X.n;
             for (int c = 32 * part; c < D; c += 32 * kParts) {
                 float v[32];
                 tmem_ld32(my_lanes + colQ + static_cast<uint32_t>(c), v);
                 if (valid) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        atomicAdd(reinterpret_cast<float4*>(bp.dq_acc + (row0 + r) * D + c + 4 * k),
+                        atomicAdd(reinterpret_cast<float4*>(bp.dq_acc + (X.row0 + r) * D + c + 4 * k),
                                   make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
                 }
             }
         }
+        first = leave;
+        X = Y;
+        it = inext;
+        tc_fence_before();
+        __syncthreads();  // tensor memory is free for the next tile
     }
+    cp_async_wait_all();  // nothing in flight past an early exit
     tc_fence_before();
     __syncthreads();  // every thread reaches this exactly once: all waits are bounded
     if (warp == 0) {
@@ -402,6 +531,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
         tmem_dealloc(tmem, kTmemCols);
     }
     if (tid == 0 && *abort && p.dev_status) atomicOr(p.dev_status, KVC_DEV_TIMEOUT);
+    (void)failed;
 }
 
 template <typename T>
@@ -410,10 +540,7 @@ cudaError_t launch_tc(const BwdParams& bp, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int64_t tiles = (bp.p.M + kTJ - 1) / kTJ;
-    const dim3 grid(static_cast<unsigned>((tiles + bp.tc_tiles_per_cta - 1) / bp.tc_tiles_per_cta),
-                    static_cast<unsigned>(bp.p.B * bp.p.Hk));
-    bwd_kv_tc_kernel<T><<<grid, kTcThreads, smem, stream>>>(bp);
+    bwd_kv_tc_kernel<T><<<static_cast<unsigned>(bp.tc_ctas), kTcThreads, smem, stream>>>(bp);
     return cudaGetLastError();
 }
 
@@ -426,10 +553,14 @@ int64_t bwd_tc_smem_bytes(int64_t D, int64_t Dv) {
     return need > 116 * 1024 ? need : 116 * 1024;
 }
 
+#ifndef KVC_BWD_TC_MIN_ROWS
+#define KVC_BWD_TC_MIN_ROWS 17  // fewer rows per unit: the few-rows CUDA-core kernel
+#endif
+
 bool bwd_tc_fits(int64_t R, int64_t D, int64_t Dv) {
     const int64_t kv = D > Dv ? D : Dv;
     const int64_t first = 2 * kTR > D + Dv ? 2 * kTR : D + Dv;  // S^T, G^T then dK', dV' columns
-    return R > 16 && R <= kTR && D % 64 == 0 && Dv % 64 == 0 && kv <= 256 &&
+    return R >= KVC_BWD_TC_MIN_ROWS && R <= kTR && D % 64 == 0 && Dv % 64 == 0 && kv <= 256 &&
            first + D <= static_cast<int64_t>(kTmemCols);
 }
 

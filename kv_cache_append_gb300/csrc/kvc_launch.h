@@ -78,7 +78,7 @@ struct BwdParams {
     int rows_smem;            // > 0: bytes of bwd_kv_rows_kernel's shared memory (units of <= 16 rows)
     int tiled_smem;           // > 0: bytes of bwd_kv_tiled_kernel's shared memory (units of > 4 rows)
     int tc_smem;              // > 0: bytes of bwd_kv_tc_kernel's shared memory (16-bit, 17-128 rows)
-    int64_t tc_tiles_per_cta; // 128-slot tiles of one unit per CTA of bwd_kv_tc_kernel
+    int64_t tc_ctas;          // CTAs of bwd_kv_tc_kernel (one per SM), splitting all units' tiles
     int rowdot_vec;           // 1: M % 8 == 0 and the attention-gradient (and attention) rows
                               // 16-byte aligned: bwd_rowdot_kernel loads 8 slots at a time
     float scale;              // the scores' scale (natural-log domain)

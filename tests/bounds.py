@@ -180,37 +180,110 @@ def check_step(inputs, upd_key, upd_value, att, ctx, att_ref, ctx_ref, scale, wh
 
 
 # ---------------------------------------------------------------- gradients
-# |got - ref| <= rtol |ref| + atol RMS(ref) + floor, RMS over the tensor's
-# nonzero reference entries; the entries the step's structure makes zero
-# (exact_zero: invalid query rows, new rows nothing appended) must be exactly
-# zero. Any other entry may be zero by cancellation (a row with two allowed
-# slots has ds_0 = -ds_1, so its query gradient vanishes wherever the two keys
-# agree) and keeps the atol term: the fp32 sums leave a residue there. rtol covers the final rounding of a gradient and, on the
-# tensor-core slot kernel, the rounding of a and ds to 16-bit operands (2u for
-# bf16, 4u for fp16). atol covers the sums of independently rounded terms,
-# whose error is relative to the terms' magnitude rather than to the
-# (possibly cancelled) entry: by Hoeffding's inequality at most lambda u
-# sqrt(sum of squared terms), with lambda = 8 as for the forward bounds, so
-# atol = 8u (2^-5 bf16, 2^-8 fp16); fp32 keeps 1e-4 for its fp32 sums over up
-# to 1e5 slots. The floor is one fp16 subnormal spacing (long-row cache
-# gradients are fp16 subnormals) or fp32's flush-to-zero threshold.
+# |got - ref| <= rtol |ref| + atol (RMS(ref) + T) + floor per entry, with RMS
+# over the tensor's nonzero reference entries and T the root of the sum of
+# squares of the entry's own terms (grad_terms).
+#
+# rtol covers the final rounding of a gradient and, on the tensor-core slot
+# kernel, the rounding of a and ds to 16-bit operands (2u for bf16, 4u for
+# fp16). atol covers the sums of independently rounded terms, whose error is
+# relative to the terms' magnitude rather than to the (possibly cancelled)
+# entry: by Hoeffding's inequality at most lambda u T, with lambda = 8 as for
+# the forward bounds, so atol = 8u (2^-5 bf16, 2^-8 fp16); fp32 keeps 1e-4 for
+# its fp32 sums over up to 1e5 slots. The RMS term is the tensor-wide share of
+# the errors of the rows' shared fp32 statistics (normaliser, maximum, D).
+# The floor is one fp16 subnormal spacing (long-row cache gradients are fp16
+# subnormals) or fp32's flush-to-zero threshold.
+#
+# The entries the step's structure makes zero (exact_zero: invalid query
+# rows, new rows nothing appended) must be exactly zero. Any other entry may
+# be zero by cancellation (a row with two allowed slots has ds_0 = -ds_1, so
+# its query gradient vanishes wherever the two keys agree) and keeps the atol
+# term: the fp32 sums leave a residue there.
 GRAD_TOL = {torch.bfloat16: (2.0 ** -7, 2.0 ** -5), torch.float16: (2.0 ** -9, 2.0 ** -8),
             torch.float32: (1e-4, 1e-4)}
 GRAD_FLOOR = {torch.bfloat16: TINY, torch.float16: 2.0 ** -24, torch.float32: TINY}
 
 
-def grad_ratio(got, ref, dtype, exact_zero=None) -> float:
-    """max |got - ref| / (rtol |ref| + atol RMS(ref) + floor); <= 1 passes.
-    exact_zero (boolean, ref's shape, or None): entries that must be zero."""
+def grad_ratio(got, ref, dtype, exact_zero=None, terms=None) -> float:
+    """max |got - ref| / (rtol |ref| + atol (RMS(ref) + T) + floor); <= 1 passes.
+    exact_zero (boolean, ref's shape, or None): entries that must be zero.
+    terms (ref's shape, or None for zero): T, the root of the sum of squares of
+    the terms each entry sums (grad_terms)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     rtol, atol = GRAD_TOL[dtype]
     nz = ref[ref != 0.0]
     rms = float(np.sqrt(np.mean(nz ** 2))) if nz.size else 0.0
     err = np.abs(got - ref)
-    tol = rtol * np.abs(ref) + atol * rms + GRAD_FLOOR[dtype]
+    spread = rms if terms is None else rms + np.asarray(terms, dtype=np.float64)
+    tol = rtol * np.abs(ref) + atol * spread + GRAD_FLOOR[dtype]
     if exact_zero is not None:
         tol = np.where(exact_zero, 0.0, tol)
     with np.errstate(divide="ignore", invalid="ignore"):
         r = np.where(err == 0.0, 0.0, err / tol)
     return float(r.max(initial=0.0))
+
+
+def grad_terms(query, lengths, append_mask, fwd, d_attention, d_context, scale, sums=False):
+    """T per gradient entry: the root of the sum of squares of the terms it
+    sums, from the oracle's forward pass fwd (oracle.step: attention rows a
+    and updated caches K', V') and the incoming gradients (None: zero). For a
+    valid row r of a unit and an allowed slot j, with g_rj = dattention_rj +
+    dcontext_r . V'_j, D_r = sum_j a_rj g_rj and ds_rj = a_rj (g_rj - D_r):
+
+      dK'_j: scale sqrt(sum_r (ds_rj q_r)^2)     dV'_j: sqrt(sum_r (a_rj dcontext_r)^2)
+      dq_r:  scale sqrt(sum_j (ds_rj K'_j)^2)
+
+    elementwise over the width; a new row's gradient takes its slot's. The
+    16-bit rounding of a and ds (independent per term) moves an entry by at
+    most lambda u T (Hoeffding), which on a row of few slots, whose terms are
+    large next to the tensor's RMS, is the larger part of the error.
+    Returns a dict keyed like the gradients (query, new_key, new_value,
+    key_cache, value_cache); with sums, also the terms' plain sums (the
+    attention-derived part of each gradient) under "sum_" + key."""
+    q = np.asarray(query.double().numpy() if torch.is_tensor(query) else query, dtype=np.float64)
+    K = fwd["key_cache"].double().numpy()
+    V = fwd["value_cache"].double().numpy()
+    att = np.asarray(fwd["attention"], dtype=np.float64)
+    B, Hq, Q, D = q.shape
+    Hk, M, Dv = V.shape[1], V.shape[2], V.shape[3]
+    G = Hq // Hk
+    da = (np.zeros((B, Hq, Q, M)) if d_attention is None else d_attention.double().numpy())
+    dc = (np.zeros((B, Hq, Q, Dv)) if d_context is None else d_context.double().numpy())
+    counts = append_mask.to(torch.int64).cumprod(1).sum(1).numpy()
+    ln = lengths.numpy()
+    shapes = {"query": (B, Hq, Q, D), "new_key": (B, Hk, Q, D), "new_value": (B, Hk, Q, Dv),
+              "key_cache": (B, Hk, M, D), "value_cache": (B, Hk, M, Dv)}
+    out = {k: np.zeros(v) for k, v in shapes.items()}
+    if sums:
+        out.update({"sum_" + k: np.zeros(v) for k, v in shapes.items()})
+    for b in range(B):
+        L, n = int(ln[b]), int(counts[b])
+        if fwd["flags"][b] or n == 0:
+            continue
+        N = L + n
+        for kv in range(Hk):
+            hs = slice(kv * G, (kv + 1) * G)
+            a = att[b, hs, :n, :N].reshape(G * n, N)
+            Kp, Vp = K[b, kv, :N], V[b, kv, :N]
+            qr = q[b, hs, :n].reshape(G * n, D)
+            dcr = dc[b, hs, :n].reshape(G * n, Dv)
+            g = da[b, hs, :n, :N].reshape(G * n, N) + dcr @ Vp.T
+            ds = a * (g - (a * g).sum(1, keepdims=True))
+            Tk = scale * np.sqrt((ds ** 2).T @ (qr ** 2))
+            Tv = np.sqrt((a ** 2).T @ (dcr ** 2))
+            Tq = scale * np.sqrt((ds ** 2) @ (Kp ** 2))
+            out["key_cache"][b, kv, :L] = Tk[:L]
+            out["new_key"][b, kv, :n] = Tk[L:N]
+            out["value_cache"][b, kv, :L] = Tv[:L]
+            out["new_value"][b, kv, :n] = Tv[L:N]
+            out["query"][b, hs, :n] = Tq.reshape(G, n, D)
+            if sums:
+                Sk, Sv, Sq = scale * (ds.T @ qr), a.T @ dcr, scale * (ds @ Kp)
+                out["sum_key_cache"][b, kv, :L] = Sk[:L]
+                out["sum_new_key"][b, kv, :n] = Sk[L:N]
+                out["sum_value_cache"][b, kv, :L] = Sv[:L]
+                out["sum_new_value"][b, kv, :n] = Sv[L:N]
+                out["sum_query"][b, hs, :n] = Sq.reshape(G, n, D)
+    return out

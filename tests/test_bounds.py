@@ -137,3 +137,41 @@ def test_gradient_bound(dtype):
     structural[:, :, 300:] = True
     assert bounds.grad_ratio(bad, ref, dtype, exact_zero=structural) > 1.0
     assert bounds.grad_ratio(bad, ref, dtype) <= 1.0
+
+
+def test_grad_terms_sum_to_the_oracle_gradients():
+    """grad_terms' per-term decomposition (a, g, D, ds from the oracle's
+    forward pass) sums to the oracle's own backward (an independent C
+    statement of the chain rule): with gradients reaching only attention and
+    context, the cache gradients below the old length, the new rows' and the
+    query's are exactly those sums. T bounds each sum: |sum| <= sqrt(terms) T."""
+    spec = Spec(B=4, Hq=6, Hk=2, Q=3, D=16, Dv=8, M=40, dtype="f32",
+                lengths=("uniform", 0, 36), counts=("uniform", 0, 3))
+    x = workloads.generate(spec, 21)
+    x.lengths[2] = 39   # 39 + n > M for n >= 2: a flagged row
+    x.append_mask[2] = True
+    g = torch.Generator().manual_seed(22)
+    da = torch.randn(4, 6, 3, 40, generator=g)
+    dc = torch.randn(4, 6, 3, 8, generator=g)
+    ref = oracle.step_backward(*x.args(), d_attention=da, d_context=dc, options=x.options)
+    assert ref["flags"][2] != 0
+    fwd = oracle.step(*x.args(), options=x.options)
+    scale = oracle.default_scale(16)
+    t = bounds.grad_terms(x.query, x.lengths, x.append_mask, fwd, da, dc, scale, sums=True)
+    counts = x.append_mask.to(torch.int64).cumprod(1).sum(1)
+    for b in range(4):
+        L, n = int(x.lengths[b]), (0 if ref["flags"][b] else int(counts[b]))
+        np.testing.assert_allclose(t["sum_key_cache"][b, :, :L], ref["d_key_cache"][b, :, :L],
+                                   rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(t["sum_value_cache"][b, :, :L],
+                                   ref["d_value_cache"][b, :, :L], rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(t["sum_new_key"][b, :, :n], ref["d_new_key"][b, :, :n],
+                                   rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(t["sum_new_value"][b, :, :n], ref["d_new_value"][b, :, :n],
+                                   rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(t["sum_query"], ref["d_query"], rtol=1e-9, atol=1e-12)
+    # the root of the sum of squares bounds the sum over at most M (slots) or
+    # Hq / Hk * Q (rows) terms
+    assert np.all(np.abs(t["sum_query"]) <= np.sqrt(40) * t["query"] + 1e-12)
+    assert np.all(np.abs(t["sum_key_cache"]) <= np.sqrt(9) * t["key_cache"] + 1e-12)
+    assert np.any(t["key_cache"] > 0) and np.any(t["query"] > 0)

@@ -57,25 +57,36 @@ def structural_zeros(x, ref):
             "new_value": invalid[:, None, :, None]}
 
 
-def check_grads(got, ref, x, where=""):
-    """Every gradient within bounds.grad_ratio, the structurally zero row
-    gradients exactly zero. With no gradient reaching the returned caches
-    (grads of attention/context only), the cache gradients below the old
-    length are the attention-derived dK', dV' alone: zeroing them, or scaling
-    the query gradient by 0.9, must exceed the bound."""
+def terms_of(x, grads):
+    """bounds.grad_terms for the inputs x and the incoming gradients."""
+    fwd = oracle.step(*x.args(), options=x.options)
+    scale = x.options.get("scale", oracle.default_scale(x.query.shape[-1]))
+    cpu = {k: (None if v is None else v.cpu()) for k, v in grads.items()}
+    return bounds.grad_terms(x.query, x.lengths, x.append_mask, fwd, cpu["attention"],
+                             cpu["context"], scale)
+
+
+def check_grads(got, ref, x, grads, where=""):
+    """Every gradient within bounds.grad_ratio (with each entry's own terms),
+    the structurally zero row gradients exactly zero."""
     dt = x.query.dtype
     zeros = structural_zeros(x, ref)
+    terms = terms_of(x, grads)
     for name in NAMES:
         r = ref["d_" + name]
         gw = got[name]
         gw = gw.double().cpu().numpy() if torch.is_tensor(gw) else gw
         ez = np.broadcast_to(zeros[name], r.shape) if name in zeros else None
-        ratio = bounds.grad_ratio(gw, r, dt, exact_zero=ez)
+        ratio = bounds.grad_ratio(gw, r, dt, exact_zero=ez, terms=terms[name])
         assert ratio <= 1.0, (where, name, ratio)
+    return terms
 
 
-def check_mutants(ref, x, lengths, where=""):
-    """Wrong variants of the oracle's attention-only gradients fail the bound."""
+def check_mutants(ref, x, lengths, terms, where=""):
+    """With no gradient reaching the returned caches (grads of attention and
+    context only), the cache gradients below the old length are the
+    attention-derived dK', dV' alone: zeroing them, or scaling the query
+    gradient by 0.9, made from the oracle's own output, must exceed the bound."""
     dt = x.query.dtype
     for name in ("key_cache", "value_cache"):
         r = ref["d_" + name]
@@ -83,10 +94,10 @@ def check_mutants(ref, x, lengths, where=""):
         for b in range(r.shape[0]):
             cut[b, :, :max(0, int(lengths[b]))] = 0.0
         if np.any(cut != r):
-            assert bounds.grad_ratio(cut, r, dt) > 1.0, (where, name, "zeroed dK'")
+            assert bounds.grad_ratio(cut, r, dt, terms=terms[name]) > 1.0, (where, name, "zeroed dK'")
     r = ref["d_query"]
     if np.any(r != 0.0):
-        assert bounds.grad_ratio(0.9 * r, r, dt) > 1.0, (where, "0.9 dq")
+        assert bounds.grad_ratio(0.9 * r, r, dt, terms=terms["query"]) > 1.0, (where, "0.9 dq")
 
 
 def check(x, grads, status_expect=0):
@@ -100,9 +111,9 @@ def check(x, grads, status_expect=0):
                                **{f"d_{k}": v for k, v in grads.items()})
     flags = int(np.bitwise_or.reduce(ref["flags"])) if len(ref["flags"]) else 0
     assert int(status.item()) == flags == status_expect
-    check_grads(got, ref, x)
+    terms = check_grads(got, ref, x, grads)
     if grads["key_cache"] is None and grads["value_cache"] is None:
-        check_mutants(ref, x, x.lengths)
+        check_mutants(ref, x, x.lengths, terms)
     # exact routing: slots from the new length on, and overwritten slots
     counts = x.append_mask.to(torch.int64).cumprod(1).sum(1)
     for name, gk in (("key_cache", grads["key_cache"]), ("value_cache", grads["value_cache"])):
@@ -164,6 +175,12 @@ CASES = {
                                    lengths=("uniform", 0, 515), counts=("uniform", 0, 4)),
     "tc_f16_D128_R32_staged": Spec(B=2, Hq=8, Hk=1, Q=4, D=128, Dv=128, M=384, dtype="f16",
                                    lengths=("uniform", 120, 379)),
+    # more tiles than the tensor-core kernel has CTAs (one per SM), so that a
+    # CTA's range of tiles starts, ends and crosses units mid-way
+    "tc_walk_bf16_R32_units": Spec(B=40, Hq=16, Hk=2, Q=4, D=64, Dv=64, M=700, dtype="bf16",
+                                   lengths=("uniform", 0, 690), counts=("uniform", 0, 4)),
+    "tc_walk_f16_R64_D128": Spec(B=40, Hq=16, Hk=1, Q=4, D=128, Dv=128, M=1100, dtype="f16",
+                                 lengths=("uniform", 300, 1090)),
     # statistics on the decode tensor-core kernel (16-bit, Dv = 128, at most 16
     # rows), which takes the appended rows from new_key / new_value: 16 rows
     # whose new rows straddle the first 128-slot tile's end, D = 256 (8 rows)
@@ -194,7 +211,8 @@ SLOT = {"tiny_fp32": "bwd_kv_kernel", "decode_bf16_ragged_M": "bwd_kv_rows_kerne
         "tc_bf16_D128_R32_hot": "bwd_kv_tc_kernel", "tc_bf16_D64_R64_staged": "bwd_kv_tc_kernel",
         "tc_f16_D128_R32_staged": "bwd_kv_tc_kernel",
         "dec_bf16_R16_tile_edge": "bwd_kv_rows_kernel", "dec_f16_D256_R8": "bwd_kv_tiled_kernel",
-        "dec_bf16_D64_R4": "bwd_kv_kernel"}
+        "dec_bf16_D64_R4": "bwd_kv_kernel", "tc_walk_bf16_R32_units": "bwd_kv_tc_kernel",
+        "tc_walk_f16_R64_D128": "bwd_kv_tc_kernel"}
 
 # the cases whose statistics pass runs the decode tensor-core kernel
 DECODE_STATS = ("decode_bf16_ragged_M", "specdec_bf16_hot", "tiled_f16_D64_Dv128_R8",
@@ -291,6 +309,25 @@ def test_backward_contract_violations():
     check(x, upstream(x, 5), status_expect=kvc.DEV_MASK | kvc.DEV_OVERFLOW)
 
 
+def test_backward_tc_walk_skips_flagged_rows():
+    """Rows outside the contract (a non-prefix mask, a length past the
+    capacity) hold no tile: the tensor-core kernel's walk over all units'
+    tiles steps over them, and their caches pass the gradient straight through."""
+    spec = CASES["tc_walk_bf16_R32_units"]
+    x = workloads.generate(spec, 12)
+    lengths = x.lengths.clone()
+    lengths[3], lengths[17], lengths[18] = 699, -1, 0
+    x.lengths = lengths
+    m = x.append_mask.clone()
+    m[3] = True                                        # 699 + 4 > M = 700
+    m[5] = torch.tensor([True, False, True, False])   # not a prefix
+    m[18] = False                                      # L = 0, nothing appended: no tile
+    x.append_mask = m
+    check(x, upstream(x, 13), status_expect=kvc.DEV_MASK | kvc.DEV_OVERFLOW)
+    check(x, upstream(x, 14, which=("attention", "context")),
+          status_expect=kvc.DEV_MASK | kvc.DEV_OVERFLOW)
+
+
 def test_autograd_matches_oracle():
     """loss.backward() through kv_cache_attention_step gives the oracle's gradients."""
     x = workloads.generate(SMALL["decode_bf16_ragged_M"].replace(B=3, M=300), 4)
@@ -305,7 +342,7 @@ def test_autograd_matches_oracle():
     loss.backward()
     ref = oracle.step_backward(*x.args(), options=x.options,
                                **{f"d_{k}": v for k, v in grads.items()})
-    check_grads({name: leaf.grad for name, leaf in zip(NAMES, leaves)}, ref, x, "autograd")
+    check_grads({name: leaf.grad for name, leaf in zip(NAMES, leaves)}, ref, x, grads, "autograd")
 
 
 def test_backward_decode_full_size_sampled():
@@ -326,8 +363,9 @@ def test_backward_decode_full_size_sampled():
                                **{f"d_{k}": (None if v is None else v.index_select(0, idx).cpu())
                                   for k, v in grads.items()})
     xs = workloads.StepInputs(*sub, x.options)
-    check_grads({k: v.index_select(0, idx) for k, v in got.items()}, ref, xs, "sampled")
-    check_mutants(ref, xs, xs.lengths, "sampled")
+    gs = {k: (None if v is None else v.index_select(0, idx).cpu()) for k, v in grads.items()}
+    terms = check_grads({k: v.index_select(0, idx) for k, v in got.items()}, ref, xs, gs, "sampled")
+    check_mutants(ref, xs, xs.lengths, terms, "sampled")
     del got, x
     torch.cuda.empty_cache()
 
@@ -351,7 +389,8 @@ def test_backward_long_mqa_heads_sampled():
                                **{f"d_{k}": (None if v is None else v.index_select(0, idx).cpu())
                                   for k, v in grads.items()})
     xs = workloads.StepInputs(*sub, x.options)
-    check_grads({k: v.index_select(0, idx) for k, v in got.items()}, ref, xs, "sampled")
-    check_mutants(ref, xs, xs.lengths, "sampled")
+    gs = {k: (None if v is None else v.index_select(0, idx).cpu()) for k, v in grads.items()}
+    terms = check_grads({k: v.index_select(0, idx) for k, v in got.items()}, ref, xs, gs, "sampled")
+    check_mutants(ref, xs, xs.lengths, terms, "sampled")
     del got, x
     torch.cuda.empty_cache()
