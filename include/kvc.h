@@ -373,7 +373,7 @@ KVC_API int kvc_step_static(const kvc_dims *dims, const void *query, const void 
  *                          pass then runs the tensor-core step into it.
  *
  * D and Dv at most 256 (KVC_E_SHAPE otherwise). Sums are fp32 and gradients
- * are rounded to the dtype once, except that with 16-bit inputs and 17 to 128
+ * are rounded to the dtype once, except that with 16-bit inputs and 9 to 128
  * query rows per KV head (kvc_backward_plan_info: slot kernel
  * "bwd_kv_tc_kernel") a and ds are also rounded to the dtype, as the
  * tensor-core operands of dK', dV' and d_query. The outputs may not overlap

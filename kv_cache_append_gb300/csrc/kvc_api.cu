@@ -457,7 +457,8 @@ bool cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t width,
 // [planes][rows][ld] array of `es`-byte elements (only the first `width` of
 // each row in the map) as boxes of box_x elements x box_y rows, 128-byte swizzle.
 bool rows_map(CUtensorMap* map, void* base, CUtensorMapDataType type, int64_t es, int64_t width,
-              int64_t ld, int64_t rows, int64_t planes, int box_x, int box_y) {
+              int64_t ld, int64_t rows, int64_t planes, int box_x, int box_y,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows),
@@ -467,7 +468,7 @@ bool rows_map(CUtensorMap* map, void* base, CUtensorMapDataType type, int64_t es
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_x), static_cast<cuuint32_t>(box_y), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, type, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1223,7 +1224,7 @@ BwdChoice bwd_choose(const kvc_dims& d, const DeviceInfo& dev, bool aligned, boo
     c.stage_rows = need <= dev.smem_optin ? 1 : 0;
     // the few-rows kernel (D = Dv in {64, 128, 256})
     const bool widths = d.D == d.Dv && (d.D == 64 || d.D == 128 || d.D == 256);
-    // the tensor-core kernel (16-bit, 17 to 128 rows, widths that fit it)
+    // the tensor-core kernel (16-bit, 9 to 128 rows, widths that fit it)
     const int64_t tc_smem = bwd_tc_smem_bytes(d.D, d.Dv);
     const bool tc_fit = es == 2 && bwd_tc_fits(R, d.D, d.Dv) && aligned && acc_aligned &&
                         tc_smem <= dev.smem_optin;
@@ -1411,6 +1412,19 @@ int backward_impl(const kvc_dims* dims, const void* query, const void* new_key,
     bp.rows_smem = ch.rows_smem;
     bp.tc_smem = ch.tc_smem;
     bp.tc_ctas = ch.tc_ctas;
+    if (ch.tc_smem > 0) {  // the tensor-core slot kernel's TMA maps
+        const CUtensorMapDataType t16 = d.dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        if (!cache_map(&bp.tm_kc, key_cache, d.dtype, d.D, d.M, d.B * d.Hk) ||
+            !cache_map(&bp.tm_vc, value_cache, d.dtype, d.Dv, d.M, d.B * d.Hk))
+            return KVC_E_CUDA;
+        bp.tc_tma_da = d_attention && d.M % 8 == 0 && aligned16(d_attention) ? 1 : 0;
+        if (bp.tc_tma_da &&
+            !rows_map(&bp.tm_da, const_cast<void*>(d_attention), t16, 2, d.M, d.M,
+                      d.B * d.Hq * d.Q, 1, 128, static_cast<int>((d.Hq / d.Hk) * d.Q),
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+            return KVC_E_CUDA;
+    }
     bp.tiled_smem = ch.tiled_smem;
     bp.scale = static_cast<float>(scale);
     bp.slots_per_block = 256;

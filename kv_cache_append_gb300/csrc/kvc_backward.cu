@@ -29,10 +29,10 @@
 //                      and dV'_j plus the returned caches' own gradient,
 //                      written to the cache gradient or the new-row gradient;
 //                      ds_j K'_j summed per row into an fp32 accumulator.
-//                      bwd_kv_rows_kernel for units of at most 16 rows with
-//                      D = Dv in {64, 128, 256}, bwd_kv_tc_kernel
-//                      (kvc_backward_tc.cu, tensor cores) for 16-bit units of
-//                      17 to 128 rows whose widths fit it, bwd_kv_tiled_kernel
+//                      bwd_kv_tc_kernel (kvc_backward_tc.cu, tensor cores)
+//                      for 16-bit units of 9 to 128 rows whose widths fit
+//                      it, bwd_kv_rows_kernel for other units of at most 16
+//                      rows with D = Dv in {64, 128, 256}, bwd_kv_tiled_kernel
 //                      (kvc_backward_tiled.cu) for other units of more than
 //                      4 rows with D and Dv multiples of 64, bwd_kv_kernel
 //                      (one warp per slot) for every other shape.

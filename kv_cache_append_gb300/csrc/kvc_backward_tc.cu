@@ -1,5 +1,5 @@
 // kvc_backward_tc.cu -- the step's slot gradients on the tensor cores, for
-// units of 17 to 128 query rows with 16-bit inputs.
+// units of 9 to 128 query rows with 16-bit inputs.
 //
 // For one unit (batch row b, KV head) and its R query rows, the chain rule of
 // the step ("Required behavior", bullets 4-5) gives over the slots j below the
@@ -23,10 +23,17 @@
 //
 // then dK' (times scale) and dV' plus the returned caches' own gradient go to
 // the cache gradient, or to the new row's gradient for a slot a new row
-// filled (whose cache slot gets zero), and after the CTA's last tile its
+// filled (whose cache slot gets zero), and when the CTA leaves a unit its
 // query-gradient sums go to the fp32 accumulator with 16-byte atomics. The
 // unit's rows are padded to 128 with zero rows; ds and a are rounded to the
 // dtype once, as the operands of the last three products.
+//
+// A tile's K' and V' rows come from the input caches by TMA (64-slot boxes in
+// the operand layout below), with the tile's attention-gradient rows when
+// they are whole 16-byte words; once they land, the threads copy the new rows
+// into the slots [L, N) and zero the rows from N on. The next tile's copies
+// are issued as soon as a tile's products have finished, so they land while
+// the epilogue stores.
 //
 // Operands sit in shared memory in the 128-byte-swizzled layout: a 16-bit
 // [128 x W] matrix is W / 64 column blocks of 128 rows x 128 bytes, the
@@ -62,7 +69,7 @@ constexpr int kBlk = 128 * 128;         // one 64-element column block of a 128-
 constexpr int kMaxChunks = 16 / kParts;  // 32-column chunks of an epilogue thread (D, Dv <= 256)
 
 struct BtcLayout {
-    uint32_t k, v, q, c, a, ds, stats, scan, bar, slot, flag, total;
+    uint32_t k, v, q, c, a, ds, stats, scan, bar, tbar, slot, flag, total;
 };
 
 __host__ __device__ inline BtcLayout btc_layout(int D, int Dv) {
@@ -77,6 +84,7 @@ __host__ __device__ inline BtcLayout btc_layout(int D, int Dv) {
     L.stats = off; off += 4 * kTR * 4;                         // m, 1/l, D, causal limit per row
     L.scan = off; off += (kTcWarps + 3) * 8;                   // block scan, located tile
     L.bar = off;  off += 8;
+    L.tbar = off; off += 8;                                    // the tile copies' barrier
     L.slot = off; off += 4;
     L.flag = off; off += 4;
     L.total = off;
@@ -223,7 +231,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
         X = btc_unit(p, b * p.Hk + off / tb);
         it = off % tb;
     }
-    const uint32_t bar = smem_addr(smem + Ly.bar);
+    const uint32_t bar = smem_addr(smem + Ly.bar), tbar = smem_addr(smem + Ly.tbar);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + Ly.flag);
     float* s_mx = reinterpret_cast<float*>(smem + Ly.stats);
     float* s_il = s_mx + kTR;
@@ -231,6 +239,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
     int* s_lim = reinterpret_cast<int*>(s_dr + kTR);
     if (tid == 0) {
         mbar_init(bar, 1u);
+        mbar_init(tbar, 1u);
         *abort = 0;
         fence_mbar_init();
     }
@@ -283,39 +292,63 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
         }
     };
     // the attention gradients of a tile go through the a^T buffer (free from the
-    // previous tile's products to this tile's a / ds pass) when their rows are
-    // whole 16-byte words: [row][slot], 256 bytes a row
-    const bool stage_da =
-        dag && p.M % 8 == 0 && (reinterpret_cast<uintptr_t>(dag) & 15u) == 0;
+    // previous tile's products to this tile's a / ds pass): the unit's R rows of
+    // the tile's 128 slots, [row][slot], 256 bytes a row, copied by TMA
+    const bool stage_da = dag && bp.tc_tma_da;
     const T* s_da = reinterpret_cast<const T*>(smem + Ly.a);
-    // the slot rows of tile i of unit Y: the input cache below L, the new rows
-    // from L on, zero past N; with stage_da its valid rows' attention gradients too
-    auto stage_tile = [&](const BtcUnit& Y, int64_t i) {
+    const uint32_t sK0 = smem_addr(smem + Ly.k), sV0 = smem_addr(smem + Ly.v);
+    const uint32_t sA0 = smem_addr(smem + Ly.a);
+    // one thread: the tile's K' and V' rows from the input caches (boxes of 64
+    // slots x 64 elements, the 128-byte-swizzled operand layout; the second
+    // half only when the tile holds slots past 64) and, with stage_da, its
+    // attention-gradient rows, all counted on tbar
+    auto issue_tile = [&](const BtcUnit& Y, int64_t i) {
+        const int64_t jb = i * kTJ;
+        const int halves = Y.jend - jb > kTJ / 2 ? 2 : 1;
+        const uint32_t bytes = static_cast<uint32_t>(halves * 64 * 128 * (D / 64 + Dv / 64)) +
+                               (stage_da ? static_cast<uint32_t>(R * kTJ * 2) : 0u);
+        mbar_arrive_expect_tx(tbar, bytes);
+        const int z = static_cast<int>(Y.u);
+        for (int h = 0; h < halves; ++h) {
+            const int y = static_cast<int>(jb) + 64 * h;
+            const uint32_t o = static_cast<uint32_t>(h * 64 * 128);
+            for (int kb = 0; kb < D / 64; ++kb)
+                tma_load_3d(sK0 + kb * kBlk + o, &bp.tm_kc, 64 * kb, y, z, tbar);
+            for (int kb = 0; kb < Dv / 64; ++kb)
+                tma_load_3d(sV0 + kb * kBlk + o, &bp.tm_vc, 64 * kb, y, z, tbar);
+        }
+        if (stage_da) tma_load_3d(sA0, &bp.tm_da, static_cast<int>(jb), static_cast<int>(Y.row0), 0, tbar);
+    };
+    // every thread, once the copies landed: the new rows into slots [L, N) of
+    // the tile and zero rows from N on (the cache holds anything there, and
+    // dq = ds K' reads every row of the tile)
+    auto patch_tile = [&](const BtcUnit& Y, int64_t i) {
         const int64_t jb = i * kTJ;
         const int nj = static_cast<int>(Y.jend - jb < kTJ ? Y.jend - jb : kTJ);
-        const T* kc = static_cast<const T*>(p.key_cache) + Y.u * p.M * D;
-        const T* vc = static_cast<const T*>(p.value_cache) + Y.u * p.M * Dv;
-        const T* nk = static_cast<const T*>(p.new_key) + Y.u * p.Q * D;
-        const T* nv = static_cast<const T*>(p.new_value) + Y.u * p.Q * Dv;
-        if (stage_da) {
-            for (int idx = tid; idx < kTR * (kTJ / 8); idx += kTcThreads) {
-                const int r = idx / (kTJ / 8), c = idx - r * (kTJ / 8);
-                if (r < R && (r % p.Q) < Y.n && 8 * c < nj)
-                    cp_async16(smem + Ly.a + r * (kTJ * 2) + c * 16,
-                               dag + (Y.row0 + r) * p.M + jb + 8 * c);
-            }
+        const int64_t a = Y.L > jb ? Y.L : jb;
+        const int pa = static_cast<int>(a - jb), pc = a < Y.jend ? nj : pa;  // rows [pa, pc) are new
+        const T* nk = static_cast<const T*>(p.new_key) + (Y.u * p.Q + (a - Y.L)) * D;
+        const T* nv = static_cast<const T*>(p.new_value) + (Y.u * p.Q + (a - Y.L)) * Dv;
+        const int ck = D / 8, cv = Dv / 8;
+        for (int e = tid; e < (pc - pa) * (ck + cv); e += kTcThreads) {
+            const int rr = e / (ck + cv), c = e - rr * (ck + cv), t = pa + rr;
+            if (c < ck)
+                *reinterpret_cast<uint4*>(smem + Ly.k + sw128_off(t, 8 * c)) =
+                    *reinterpret_cast<const uint4*>(nk + rr * D + 8 * c);
+            else
+                *reinterpret_cast<uint4*>(smem + Ly.v + sw128_off(t, 8 * (c - ck))) =
+                    *reinterpret_cast<const uint4*>(nv + rr * Dv + 8 * (c - ck));
         }
-        stage_sw128<T>(smem + Ly.k, D, nj, [&](int t) {
-            const int64_t j = jb + t;
-            return j >= Y.L ? nk + (j - Y.L) * D : kc + j * D;
-        });
-        stage_sw128<T>(smem + Ly.v, Dv, nj, [&](int t) {
-            const int64_t j = jb + t;
-            return j >= Y.L ? nv + (j - Y.L) * Dv : vc + j * Dv;
-        });
+        for (int e = tid; e < (kTJ - nj) * (ck + cv); e += kTcThreads) {
+            const int rr = e / (ck + cv), c = e - rr * (ck + cv), t = nj + rr;
+            unsigned char* d = c < ck ? smem + Ly.k + sw128_off(t, 8 * c)
+                                      : smem + Ly.v + sw128_off(t, 8 * (c - ck));
+            *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+        }
     };
     stage_unit(X);
-    stage_tile(X, it);
+    if (tid == 0) issue_tile(X, it);
+    uint32_t tphase = 0;
     if (warp == 0) {
         tmem_alloc(smem_addr(smem + Ly.slot), kTmemCols);
         tmem_relinquish();
@@ -337,7 +370,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
     const int ts = 32 * (warp & 3) + lane;  // this thread's slot of a tile (TMEM lane)
     const float qs = p.qscale;
     uint32_t phase = 0;
-    bool failed = false;
+    bool failed = false, copy_pending = false;
     const int part = warp >> 2;               // which of the warps on these TMEM lanes
     const int rbase = kRowsPer * part;         // rows of this thread in the a / ds pass
     const bool keys = part < kParts / 2;       // epilogue: dK' or dV' ...
@@ -350,7 +383,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
         const int64_t jb = it * kTJ;
         const int nj = static_cast<int>(X.jend - jb < kTJ ? X.jend - jb : kTJ);
         const int64_t j = jb + ts;  // this thread's slot
-        cp_async_wait_all();
+        {
+            const bool okt = mbar_wait(tbar, tphase, abort);
+            if (__syncthreads_or(!okt)) {
+                failed = true;
+                copy_pending = true;
+                break;
+            }
+            tphase ^= 1u;
+        }
+        patch_tile(X, it);
+        cp_async_wait_all();  // the unit's rows
         fence_async_shared();
         __syncthreads();
         if (tid == 0) {  // S^T = K' q^T, G^T = V' dcontext^T (K-major operands, 16 elements a step)
@@ -473,7 +516,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
         const bool leave = !more || Y.u != X.u;  // the unit's last tile of this CTA
         if (more) {
             if (Y.u != X.u) stage_unit(Y);
-            stage_tile(Y, inext);
+            if (tid == 0) issue_tile(Y, inext);
         }
         {  // dK' (times scale) or dV' of this thread's slot plus the returned caches' gradient
             const float sc = keys ? bp.scale : 1.f;
@@ -524,6 +567,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
         __syncthreads();  // tensor memory is free for the next tile
     }
     cp_async_wait_all();  // nothing in flight past an early exit
+    if (copy_pending && tid == 0) {
+        // the tile copy whose wait gave up may still be landing: wait for it
+        // (bounded) before the shared memory is released
+        volatile int never = 0;
+        mbar_wait(tbar, tphase, &never);
+    }
     tc_fence_before();
     __syncthreads();  // every thread reaches this exactly once: all waits are bounded
     if (warp == 0) {
@@ -554,7 +603,9 @@ int64_t bwd_tc_smem_bytes(int64_t D, int64_t Dv) {
 }
 
 #ifndef KVC_BWD_TC_MIN_ROWS
-#define KVC_BWD_TC_MIN_ROWS 17  // fewer rows per unit: the few-rows CUDA-core kernel
+// fewer rows per unit: the few-rows CUDA-core kernel (on gqa_decode's
+// shapes it is faster at 4 and 8 rows, slower from 12 on)
+#define KVC_BWD_TC_MIN_ROWS 9
 #endif
 
 bool bwd_tc_fits(int64_t R, int64_t D, int64_t Dv) {

@@ -77,8 +77,15 @@ struct BwdParams {
     int stage_rows;           // 1: bwd_kv_kernel stages the unit's rows in shared memory
     int rows_smem;            // > 0: bytes of bwd_kv_rows_kernel's shared memory (units of <= 16 rows)
     int tiled_smem;           // > 0: bytes of bwd_kv_tiled_kernel's shared memory (units of > 4 rows)
-    int tc_smem;              // > 0: bytes of bwd_kv_tc_kernel's shared memory (16-bit, 17-128 rows)
+    int tc_smem;              // > 0: bytes of bwd_kv_tc_kernel's shared memory (16-bit, 9-128 rows)
     int64_t tc_ctas;          // CTAs of bwd_kv_tc_kernel (one per SM), splitting all units' tiles
+    // bwd_kv_tc_kernel's TMA copies: the input caches as [U][M][width] (boxes
+    // of 64 elements x 64 slots, 128-byte swizzle) and, with tc_tma_da, the
+    // attention gradient as [B*Hq*Q][M] rows (boxes of 128 slots x R rows)
+    CUtensorMap tm_kc;
+    CUtensorMap tm_vc;
+    CUtensorMap tm_da;
+    int tc_tma_da;
     int rowdot_vec;           // 1: M % 8 == 0 and the attention-gradient (and attention) rows
                               // 16-byte aligned: bwd_rowdot_kernel loads 8 slots at a time
     float scale;              // the scores' scale (natural-log domain)
@@ -93,7 +100,7 @@ cudaError_t launch_backward(const BwdParams& bp, int dtype, bool words16, cudaSt
 // with D and Dv multiples of 64 up to 256 (kvc_backward_tiled.cu); its shared
 // memory in bytes.
 cudaError_t launch_bwd_kv_tiled(const BwdParams& bp, int dtype, cudaStream_t stream);
-// The slot gradients on the tensor cores for 16-bit units of 17 to 128 rows
+// The slot gradients on the tensor cores for 16-bit units of 9 to 128 rows
 // (kvc_backward_tc.cu): whether the shape fits (D, Dv multiples of 64 whose
 // products fit tensor memory), and the kernel's shared memory in bytes.
 cudaError_t launch_bwd_kv_tc(const BwdParams& bp, int dtype, cudaStream_t stream);

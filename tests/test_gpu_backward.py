@@ -148,7 +148,7 @@ CASES = {
                                      lengths=("uniform", 0, 699)),
     # units of more than 4 rows with D and Dv multiples of 64 that the
     # few-rows kernel does not take: the tensor-core kernel for the 16-bit ones
-    # of 17-128 rows whose widths fit it (R40, R18 here), the tiled kernel for
+    # of 9-128 rows whose widths fit it (R40, R18 here), the tiled kernel for
     # the rest (each of its instances, a last row chunk of 8 rows, D != Dv,
     # tiles cut by M and N)
     "tiled_bf16_D128_R40_ragged": Spec(B=3, Hq=10, Hk=1, Q=4, D=128, Dv=128, M=500,
@@ -162,7 +162,7 @@ CASES = {
                                      hot_frac=0.05, hot_scale=20.0),
     "tiled_f16_D64_Dv128_R8": Spec(B=3, Hq=8, Hk=2, Q=2, D=64, Dv=128, M=400, dtype="f16",
                                    counts=("uniform", 0, 2)),
-    # the tensor-core kernel (16-bit, 17-128 rows): 128 rows exactly with tiles
+    # the tensor-core kernel (16-bit, 9-128 rows): 128 rows exactly with tiles
     # cut by M and N, 17 rows (111 padding rows), hot rows
     "tc_bf16_D64_R128_ragged": Spec(B=3, Hq=32, Hk=1, Q=4, D=64, Dv=64, M=700, dtype="bf16",
                                     lengths=("uniform", 0, 690), counts=("uniform", 0, 4)),
@@ -197,7 +197,7 @@ CASES = {
 # the slot kernel each case runs (kvc_backward_plan_info), so that every
 # kernel stays covered
 SLOT = {"tiny_fp32": "bwd_kv_kernel", "decode_bf16_ragged_M": "bwd_kv_rows_kernel",
-        "specdec_bf16_hot": "bwd_kv_rows_kernel", "chunk_fp32_Q40": "bwd_kv_tiled_kernel",
+        "specdec_bf16_hot": "bwd_kv_tc_kernel", "chunk_fp32_Q40": "bwd_kv_tiled_kernel",
         "mqa_fp16_D192": "bwd_kv_tc_kernel", "gqa_fp32_small_rows": "bwd_kv_kernel",
         "generic_bf16_D5_Dv7": "bwd_kv_kernel", "mha_fp16_Dv256": "bwd_kv_kernel",
         "rows_f16_D64_R8": "bwd_kv_rows_kernel", "rows_f32_D256_R16": "bwd_kv_rows_kernel",
@@ -210,7 +210,7 @@ SLOT = {"tiny_fp32": "bwd_kv_kernel", "decode_bf16_ragged_M": "bwd_kv_rows_kerne
         "tc_bf16_D64_R128_ragged": "bwd_kv_tc_kernel", "tc_f16_D128_R17": "bwd_kv_tc_kernel",
         "tc_bf16_D128_R32_hot": "bwd_kv_tc_kernel", "tc_bf16_D64_R64_staged": "bwd_kv_tc_kernel",
         "tc_f16_D128_R32_staged": "bwd_kv_tc_kernel",
-        "dec_bf16_R16_tile_edge": "bwd_kv_rows_kernel", "dec_f16_D256_R8": "bwd_kv_tiled_kernel",
+        "dec_bf16_R16_tile_edge": "bwd_kv_tc_kernel", "dec_f16_D256_R8": "bwd_kv_tiled_kernel",
         "dec_bf16_D64_R4": "bwd_kv_kernel", "tc_walk_bf16_R32_units": "bwd_kv_tc_kernel",
         "tc_walk_f16_R64_D128": "bwd_kv_tc_kernel"}
 
@@ -237,7 +237,7 @@ def test_backward_plan():
     assert plan_of(workloads.SPECS["chunked_append"]) == (6, "fused", "bwd_kv_tiled_kernel")
     # 16-bit, Dv = 128, at most 16 rows: the decode tensor-core kernel
     assert plan_of(workloads.SPECS["gqa_decode"]) == (6, "decode", "bwd_kv_rows_kernel")
-    assert plan_of(workloads.SPECS["ragged_specdec"]) == (6, "decode", "bwd_kv_rows_kernel")
+    assert plan_of(workloads.SPECS["ragged_specdec"]) == (6, "decode", "bwd_kv_tc_kernel")
     for name in DECODE_STATS:
         assert plan_of(CASES[name])[1] == "decode", name
     assert plan_of(CASES["rows_f32_D256_R16"])[1] != "decode"   # fp32
