@@ -22,8 +22,11 @@
 //                   each tile's K and V rows below the new length (64-element
 //                   boxes, 128-byte swizzle, the layout the tensor cores read)
 //                   and the unit's query rows (16 rows, 4 KB from L2) with it.
-//   MMA warp        one thread: S^T into one of two tensor-memory buffers,
-//                   then O^T += V^T P^T into the tensor-memory O^T.
+//   MMA warp        one thread: S^T into one of two tensor-memory buffers.
+//   P.V warp        one thread: O^T += V^T P^T into the tensor-memory O^T as
+//                   soon as a tile's P^T is ready, then releases the stage
+//                   (issued from the MMA thread after the next tile's S^T, the
+//                   stage would be held until the next tile lands).
 //   softmax warps  one or two groups of 4 warps (two for 8 or 16 rows, each
 //                   group taking half of them), one slot per thread (= the
 //                   tensor-memory lane of S^T):
@@ -72,12 +75,21 @@ constexpr int kDN = 16;              // query rows of a unit, padded (N of both 
 constexpr int kBlk = kDT * 128;      // one 64-element-wide column block of a K or V tile
 constexpr int kNBlk = kDN * 128;     // one 64-element-wide column block of Q or P^T
 constexpr int kHalf = 64;            // slots per TMA box of a contiguous cache
+// KVC_DEC_PV_WARP: the P.V products get an issuer thread (and warp) of their
+// own, so that a tile's product goes out, and its stage is released, as soon
+// as its P^T is ready instead of after the next tile's scores (which wait for
+// the next tile to land). 0: one thread issues both products.
+#ifndef KVC_DEC_PV_WARP
+#define KVC_DEC_PV_WARP 1
+#endif
+constexpr bool kPvWarp = KVC_DEC_PV_WARP != 0;
 // Warp roles for SG groups of 4 softmax warps (each group takes NR / SG of
-// the unit's rows for all 128 slots), then the MMA warp and the producer.
+// the unit's rows for all 128 slots), then the MMA warp, the producer and,
+// with kPvWarp, the P.V issuer.
 template <int SG>
 struct DecRoles {
-    static constexpr int soft = 4 * SG, mma = 4 * SG, prod = 4 * SG + 1;
-    static constexpr int threads = (4 * SG + 2) * 32;
+    static constexpr int soft = 4 * SG, mma = 4 * SG, prod = 4 * SG + 1, pv = 4 * SG + 2;
+    static constexpr int threads = (4 * SG + (kPvWarp ? 3 : 2)) * 32;
 };
 constexpr float kRescale = 8.f;      // raise a row's reference maximum when exceeded by 2^8
 constexpr uint32_t kTmemCols = 64;
@@ -331,6 +343,7 @@ __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars
             tc_commit(bars.s_ready(sbuf));
             ++s_uses[sbuf];
             sbuf ^= 1;
+            if (kPvWarp) continue;  // the P.V issuer releases the stage
             // the previous tile's product goes after this tile's scores, so the
             // softmax warps find S^T ready when they finish that tile
             if (has_pending && !issue_pv(pend_stage, pend_first)) break;
@@ -351,6 +364,60 @@ __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars
     }
     // every issued tensor-core instruction has finished before the CTA frees
     // tensor memory (also when a wait gave up)
+    tc_commit(bars.drained());
+    volatile int never = 0;
+    mbar_wait(bars.drained(), 0u, &never);
+}
+
+// With kPvWarp: one thread issues every O^T += V^T P^T product, walking the
+// same ring, and releases each attended stage after its product.
+__device__ void dec_pv_issuer(const DecParams& dp, unsigned char* smem, DecBars bars,
+                              volatile int* abort, uint32_t tmem, bool bf16, bool lo) {
+    const StepParams& p = dp.p;
+    const uint32_t stage0 = smem_addr(smem + p.off_stages);
+    const uint32_t pt0 = smem_addr(smem + p.dec_off_pt);
+    const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
+    const int nkb = static_cast<int>(p.D / 64);
+    const uint32_t idesc_o = mma_idesc_f16(static_cast<int>(p.Dv), kDN, bf16, false, true);
+    Ring ring;
+    int64_t pv_count = 0;
+    bool attend = false;
+    int64_t N = 0;
+    for (;;) {
+        const int s = ring.s;
+        const uint32_t ph = ring.ph;
+        ring.next(p.NS);
+        if (!mbar_wait(bars.full(s), ph, abort)) break;
+        const TileMeta mt = meta[s];
+        if (mt.flags & kDone) break;
+        if (mt.flags & kFirst) {
+            N = mt.L + mt.n;
+            attend = mt.n > 0 && static_cast<int64_t>(mt.i) * kDT < N;
+        }
+        if (!(attend && static_cast<int64_t>(mt.i) * kDT < N)) continue;  // the S issuer releases it
+        const int pb = static_cast<int>(pv_count & 1);
+        if (!mbar_wait(bars.p_ready(pb), static_cast<uint32_t>((pv_count >> 1) & 1), abort)) break;
+        tc_fence_after();
+        const uint32_t sV = stage0 + static_cast<uint32_t>(s) * p.stage_bytes +
+                            static_cast<uint32_t>(nkb * kBlk);
+        const uint32_t sP = pt0 + static_cast<uint32_t>(pb * 2 * kNBlk);
+        const bool first = (mt.flags & kFirst) != 0;
+#pragma unroll
+        for (int kk = 0; kk < kDT / 16; ++kk)
+            tc_mma(tmem + kColO, smem_desc_sw128(sV + kk * 16 * 128, kBlk, 1024),
+                   smem_desc_sw128(sP + (kk >> 2) * kNBlk + (kk & 3) * 32, 16, 1024), idesc_o,
+                   !(first && kk == 0));
+        if (lo) {
+#pragma unroll
+            for (int kk = 0; kk < kDT / 16; ++kk)
+                tc_mma(tmem + kColO, smem_desc_sw128(sV + kk * 16 * 128, kBlk, 1024),
+                       smem_desc_sw128(sP + 4 * kNBlk + (kk >> 2) * kNBlk + (kk & 3) * 32, 16, 1024),
+                       idesc_o, true);
+        }
+        tc_commit(bars.o_done(pb));
+        tc_commit(bars.empty(s));
+        ++pv_count;
+    }
     tc_commit(bars.drained());
     volatile int never = 0;
     mbar_wait(bars.drained(), 0u, &never);
@@ -625,7 +692,7 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
             mbar_init(bars.o_done(b), 1u);
         }
         for (int g = 0; g < 2; ++g) mbar_init(bars.rendezvous(g), 4u);
-        mbar_init(bars.drained(), 1u);
+        mbar_init(bars.drained(), kPvWarp ? 2u : 1u);  // every issuing thread commits once
         *abort = 0;
         fence_mbar_init();
     }
@@ -649,6 +716,9 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
             dec_mma_issuer(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value, SRC);
     } else if (warp == Roles::prod) {
         if ((threadIdx.x & 31) == 0) dec_producer(dp, smem, bars, abort);
+    } else if (kPvWarp && warp == Roles::pv) {
+        if ((threadIdx.x & 31) == 0)
+            dec_pv_issuer(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value, SRC);
     }
     tc_fence_before();
     __syncthreads();  // every thread reaches this exactly once: all waits are bounded
