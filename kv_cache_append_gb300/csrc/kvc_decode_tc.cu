@@ -83,6 +83,7 @@ constexpr int kHalf = 64;            // slots per TMA box of a contiguous cache
 #define KVC_DEC_PV_WARP 1
 #endif
 constexpr bool kPvWarp = KVC_DEC_PV_WARP != 0;
+
 // Warp roles for SG groups of 4 softmax warps (each group takes NR / SG of
 // the unit's rows for all 128 slots), then the MMA warp, the producer and,
 // with kPvWarp, the P.V issuer.
@@ -258,6 +259,130 @@ __device__ void dec_producer(const DecParams& dp, unsigned char* smem, DecBars b
             ring.next(p.NS);
         }
     }
+    if (ok) {  // sentinel tile: tells the other roles to stop
+        if (issued < p.NS || mbar_wait(bars.empty(ring.s), ring.ph ^ 1u, abort)) {
+            meta[ring.s].flags = kDone;
+            mbar_arrive_expect_tx(bars.full(ring.s), 0u);
+            return;
+        }
+    }
+    // gave up: do not leave while issued copies may still write shared memory
+    for (int64_t q = issued > p.NS ? issued - p.NS : 0; q < issued; ++q)
+        mbar_drain(bars.full(static_cast<int>(q % p.NS)), static_cast<uint32_t>((q / p.NS) & 1));
+}
+
+// The whole producer warp (paged pools of small blocks): lane 0 takes the
+// chunks, waits for free stages and writes the tile metadata; the tile's TMA
+// copies (one per block piece and 64-element column block) are spread over
+// the lanes, so a tile of 16-slot blocks (8 pieces x 4 copies) is issued in
+// parallel.
+__device__ void dec_producer_warp(const DecParams& dp, unsigned char* smem, DecBars bars,
+                                  volatile int* abort) {
+    const StepParams& p = dp.p;
+    const int lane = threadIdx.x & 31;
+    const uint32_t stage0 = smem_addr(smem + p.off_stages);
+    TileMeta* meta = reinterpret_cast<TileMeta*>(smem + p.off_meta);
+    const int nkb = static_cast<int>(p.D / 64), nvb = static_cast<int>(p.Dv / 64);
+    const int nb = nkb + nvb;
+    const uint32_t q_bytes = static_cast<uint32_t>(nkb * kNBlk);
+    const int64_t U = p.B * p.Hk;
+    int64_t issued = 0;
+    Ring ring;
+    bool ok = true;
+    int32_t* pids = reinterpret_cast<int32_t*>(smem + p.dec_off_red + kIdsOffset);
+    auto request_ids = [&](const Unit& x, int64_t i) {  // lane 0
+        const int bs = static_cast<int>(p.block_size), hh = min(kHalf, bs);
+        const int jt = static_cast<int>(i * kDT);
+        const int npc = min((static_cast<int>(x.N) - jt + hh - 1) / hh, kDT / hh);
+        const int32_t* row = p.block_table + x.b * p.max_blocks;
+        int32_t* dst = pids + (i & 1) * kMaxPieces;
+        int blk = jt / bs, y = jt - blk * bs;
+        for (int c = 0; c < npc; ++c) {
+            cp_async4(dst + c, row + blk);
+            y += hh;
+            if (y == bs) {
+                y = 0;
+                ++blk;
+            }
+        }
+    };
+    while (ok) {
+        unsigned int qv = 0;
+        if (lane == 0) qv = atomicAdd(p.counter, 1u);
+        const int64_t q = __shfl_sync(0xffffffffu, qv, 0);
+        if (q >= p.NQ) break;
+        const int64_t idx = chunk_of(q, p.NQ);  // chunk-index-major list
+        const int64_t k = idx / U, u = idx - k * U;
+        const Unit x = load_unit(p, u);
+        const int64_t iend = x.n > 0 ? min(p.TPU, (x.N + kDT - 1) / kDT) : 0;
+        const int64_t i0 = k * p.CH, i1 = min(i0 + p.CH, iend);
+        if (i0 >= i1) continue;
+        for (int64_t i = i0; i < i1; ++i) {
+            int got = 1;
+            if (lane == 0 && issued >= p.NS)
+                got = mbar_wait(bars.empty(ring.s), ring.ph ^ 1u, abort) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, got, 0)) {
+                ok = false;
+                break;
+            }
+            const uint32_t sK = stage0 + static_cast<uint32_t>(ring.s) * p.stage_bytes;
+            const uint32_t sV = sK + static_cast<uint32_t>(nkb * kBlk);
+            const uint32_t sQ = sV + static_cast<uint32_t>(nvb * kBlk);
+            const int64_t j0 = i * kDT;
+            const uint32_t full = bars.full(ring.s);
+            const bool paged = p.block_table != nullptr;
+            const int bs = paged ? static_cast<int>(p.block_size) : 0;
+            const int hh = paged ? min(kHalf, bs) : kHalf;
+            const int jt = static_cast<int>(j0);
+            // pieces of hh slots below the new length: one or two halves, or block pieces
+            const int npc = paged ? min((static_cast<int>(x.N) - jt + hh - 1) / hh, kDT / hh)
+                                  : (x.N - j0 > kHalf ? 2 : 1);
+            if (lane == 0) {
+                TileMeta& mt = meta[ring.s];
+                mt.L = x.L;
+                mt.u = u;
+                mt.n = static_cast<int32_t>(x.n);
+                mt.i = static_cast<int32_t>(i);
+                mt.k = static_cast<int32_t>(k);
+                mt.flags = (i == i0 ? kFirst : 0) | (i == i1 - 1 ? kLast : 0);
+                mbar_arrive_expect_tx(full, static_cast<uint32_t>(npc * hh * 128 * nb) + q_bytes);
+                if (paged) {
+                    if (i == i0) request_ids(x, i);
+                    cp_async_wait_all();
+                }
+            }
+            __syncwarp();  // the expectation is set and the block ids are in shared memory
+            const int32_t* bid = pids + (i & 1) * kMaxPieces;
+            const int z0 = static_cast<int>(cache_unit(p, u));
+            for (int l = lane; l < npc * nb; l += 32) {
+                const int c = l / nb, b = l - c * nb;
+                const uint32_t o = static_cast<uint32_t>(c * hh * 128);
+                int y, z;
+                if (paged) {
+                    y = (jt % bs + c * hh) % bs;
+                    z = bid[c] * static_cast<int>(p.Hk) + static_cast<int>(x.kv);
+                } else {
+                    y = jt + c * kHalf;
+                    z = z0;
+                }
+                if (b < nkb)
+                    tma_load_3d(sK + b * kBlk + o, &dp.tm_k, 64 * b, y, z, full);
+                else
+                    tma_load_3d(sV + (b - nkb) * kBlk + o, &dp.tm_v, 64 * (b - nkb), y, z, full);
+            }
+            if (lane == 0) {
+                // the next tile's ids arrive while the producer waits for a stage
+                if (paged && i + 1 < i1) request_ids(x, i + 1);
+                const int qy = static_cast<int>(u * p.R);
+                for (int b = 0; b < nkb; ++b)
+                    tma_load_3d(sQ + b * kNBlk, &dp.tm_q, 64 * b, qy, 0, full);
+            }
+            __syncwarp();  // the ids of this tile are read before lane 0 refills them
+            ++issued;
+            ring.next(p.NS);
+        }
+    }
+    if (lane != 0) return;
     if (ok) {  // sentinel tile: tells the other roles to stop
         if (issued < p.NS || mbar_wait(bars.empty(ring.s), ring.ph ^ 1u, abort)) {
             meta[ring.s].flags = kDone;
@@ -715,7 +840,14 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
         if ((threadIdx.x & 31) == 0)
             dec_mma_issuer(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value, SRC);
     } else if (warp == Roles::prod) {
-        if ((threadIdx.x & 31) == 0) dec_producer(dp, smem, bars, abort);
+        // paged pools of blocks under 64 slots: 8 to 16 pieces of 4 copies per
+        // tile, issued by the warp's lanes (in-place gqa_decode 16-slot blocks:
+        // 0.42 -> 0.55 of the copy ceiling); one thread issues the few large
+        // copies of the other tiles faster (in place 0.84 against 0.73)
+        if (p.block_table && p.block_size < kHalf)
+            dec_producer_warp(dp, smem, bars, abort);
+        else if ((threadIdx.x & 31) == 0)
+            dec_producer(dp, smem, bars, abort);
     } else if (kPvWarp && warp == Roles::pv) {
         if ((threadIdx.x & 31) == 0)
             dec_pv_issuer(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value, SRC);
