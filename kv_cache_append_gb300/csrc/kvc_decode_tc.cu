@@ -796,7 +796,9 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
     }
 }
 
-template <typename T, int NR, int SG, bool SRC>
+// SRC: the statistics instance (appended rows from new_key / new_value); WP:
+// the paged instance for pools of blocks under 64 slots (the warp producer).
+template <typename T, int NR, int SG, bool SRC, bool WP>
 __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
     decode_tc_kernel(const __grid_constant__ DecParams dp) {
     using Roles = DecRoles<SG>;
@@ -843,8 +845,10 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
         // paged pools of blocks under 64 slots: 8 to 16 pieces of 4 copies per
         // tile, issued by the warp's lanes (in-place gqa_decode 16-slot blocks:
         // 0.42 -> 0.55 of the copy ceiling); one thread issues the few large
-        // copies of the other tiles faster (in place 0.84 against 0.73)
-        if (p.block_table && p.block_size < kHalf)
+        // copies of the other tiles faster (in place 0.84 against 0.73). A
+        // separate instance: with both producers compiled in, the 16-row
+        // instance ran ragged_specdec in place 7% slower.
+        if (WP)
             dec_producer_warp(dp, smem, bars, abort);
         else if ((threadIdx.x & 31) == 0)
             dec_producer(dp, smem, bars, abort);
@@ -865,9 +869,9 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
 #define KVC_DEC_GROUPS8 2
 #endif
 
-template <typename T, int NR, int SG, bool SRC>
+template <typename T, int NR, int SG, bool SRC, bool WP = false>
 cudaError_t launch_t(const DecParams& dp, size_t smem, cudaStream_t stream) {
-    auto kern = decode_tc_kernel<T, NR, SG, SRC>;
+    auto kern = decode_tc_kernel<T, NR, SG, SRC, WP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -883,6 +887,13 @@ cudaError_t launch_rows(const DecParams& dp, int nr, size_t smem, cudaStream_t s
             case 4: return launch_t<T, 4, 1, true>(dp, smem, stream);
             case 8: return launch_t<T, 8, KVC_DEC_GROUPS8, true>(dp, smem, stream);
             default: return launch_t<T, 16, 2, true>(dp, smem, stream);
+        }
+    }
+    if (dp.p.block_table && dp.p.block_size < kHalf) {  // the warp producer
+        switch (nr) {
+            case 4: return launch_t<T, 4, 1, false, true>(dp, smem, stream);
+            case 8: return launch_t<T, 8, KVC_DEC_GROUPS8, false, true>(dp, smem, stream);
+            default: return launch_t<T, 16, 2, false, true>(dp, smem, stream);
         }
     }
     switch (nr) {
