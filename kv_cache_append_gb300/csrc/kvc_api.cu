@@ -289,9 +289,18 @@ void generic_plan(const kvc_dims& d, Plan* pl) {
     workspace_layout(d, 1, pl);
 }
 
+// From 9 query rows per unit the tensor-core step beats the CUDA-core kernel,
+// whose per-slot work grows with the rows (gqa_decode's shapes with Q = 2, 4,
+// 8, 12, i.e. 8, 16, 32, 48 rows: CUDA-core kernel 0.79 / 0.49 / 0.28 / 0.088 of
+// the measured copy ceiling, tensor-core step 0.74-0.75 at every row count;
+// ragged_specdec, 16 rows on mostly short rows: 1.015 -> 1.039).
 #ifndef KVC_TC_MIN_ROWS
-#define KVC_TC_MIN_ROWS 64
+#define KVC_TC_MIN_ROWS 9
 #endif
+// The gradients' statistics pass runs the tensor-core step (into workspace
+// copies of its outputs, a full cache copy) only for units this wide; below,
+// the decode kernel or the CUDA-core kernel leave the statistics without a copy.
+constexpr int64_t kTcStatsMinRows = 64;
 constexpr int kTcT = 64;        // slots per tile of the tensor-core kernel
 constexpr int kTcBox = 64 * 128;  // one 64-element-wide box of a tile
 
@@ -550,8 +559,10 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
     // appended rows itself), not the tensor-core step (fp16 P values, no fp32 scores)
     const bool dec_ok = ptrs_aligned && aligned16(query) && tc_pages;
     const bool tc_ok = !mode.stats_only && dec_ok;
-    if (!(tc_ok && tc_plan(d, dev.sms, dev.smem_optin, &pl)) &&
-        !(dec_ok && inplace && dec_plan(d, dev.sms, dev.smem_optin, &pl, mode.stats_only)) &&
+    // (the steps that copy no cache take the decode kernel first: on its shapes
+    // it reads the prefix faster than the tensor-core step)
+    if (!(dec_ok && inplace && dec_plan(d, dev.sms, dev.smem_optin, &pl, mode.stats_only)) &&
+        !(tc_ok && tc_plan(d, dev.sms, dev.smem_optin, &pl)) &&
         !(ptrs_aligned &&
           ((inplace && fused_plan(d, dev.sms, dev.smem_optin, aligned16(query), &pl,
                                   kStageTargetInplace)) ||
@@ -1074,9 +1085,9 @@ int kvc_plan_info_inplace(const kvc_dims* dims, const void* key_cache, const voi
     if (rc < 0) return rc;
     DeviceInfo dev;
     Plan pl;
-    if (path_name && std::strcmp(*path_name, "tensor") != 0 && device_info(&dev) == cudaSuccess &&
-        aligned16(key_cache) && aligned16(value_cache) &&
-        (dims->Q == 0 || (aligned16(new_key) && aligned16(new_value))) &&
+    // the decode kernel comes first for the steps that copy no cache
+    if (path_name && device_info(&dev) == cudaSuccess && aligned16(key_cache) &&
+        aligned16(value_cache) && (dims->Q == 0 || (aligned16(new_key) && aligned16(new_value))) &&
         dec_plan(*dims, dev.sms, dev.smem_optin, &pl))
         *path_name = "decode_tc";
     // the cache write, then with query rows the step kernel, the merge and the row writer
@@ -1194,7 +1205,8 @@ bool bwd_layout(const kvc_dims& d, BwdLayout* L) {
     off = align_up(off + d.B * 8, 256);
     // shapes whose statistics pass may run the tensor-core step (16-bit, 64 to
     // 128 rows): room for that step's outputs
-    L->tc_room = tc_shapes(d) && bwd_tc_fits((d.Hq / d.Hk) * d.Q, d.D, d.Dv);
+    L->tc_room = tc_shapes(d) && (d.Hq / d.Hk) * d.Q >= kTcStatsMinRows &&
+                 bwd_tc_fits((d.Hq / d.Hk) * d.Q, d.D, d.Dv);
     if (L->tc_room) {
         L->kscr = static_cast<size_t>(off);
         off = align_up(off + d.B * d.Hk * d.M * d.D * es, 256);
@@ -1243,7 +1255,7 @@ BwdChoice bwd_choose(const kvc_dims& d, const DeviceInfo& dev, bool aligned, boo
     // with the tensor-core slot kernel (which recomputes the scores) the
     // statistics come from the tensor-core step where that step runs
     Plan pl;
-    c.tc_stats = c.tc_smem > 0 && tc_plan(d, dev.sms, dev.smem_optin, &pl);
+    c.tc_stats = c.tc_smem > 0 && R >= kTcStatsMinRows && tc_plan(d, dev.sms, dev.smem_optin, &pl);
     return c;
 }
 }  // namespace

@@ -62,7 +62,8 @@ def test_decode_tc_path_taken(name):
 def test_decode_tc_not_taken_outside_its_shapes():
     assert path_of(Spec(B=2, Hq=8, Hk=2, Q=1, D=128, Dv=128, M=100, dtype="f32")) == "fused"
     assert path_of(Spec(B=2, Hq=8, Hk=2, Q=1, D=128, Dv=64, M=100, dtype="bf16")) == "fused"
-    assert path_of(Spec(B=2, Hq=8, Hk=1, Q=5, D=128, Dv=128, M=100, dtype="bf16")) == "fused"
+    # 40 rows: the tensor-core step (from 9 rows), 16-bit with widths it takes
+    assert path_of(Spec(B=2, Hq=8, Hk=1, Q=5, D=128, Dv=128, M=100, dtype="bf16")) == "tensor"
     assert path_of(Spec(B=2, Hq=8, Hk=2, Q=1, D=96, Dv=128, M=100, dtype="bf16")) == "fused"
 
 

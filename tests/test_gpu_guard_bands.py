@@ -78,7 +78,8 @@ def scale_of(x):
 
 
 STEP = {
-    "fused_specdec_bf16": SMALL["specdec_bf16"],
+    "fused_specdec_bf16": SMALL["specdec_bf16"].replace(Q=2, counts=("uniform", 0, 2)),
+    "tensor_specdec_bf16_r16": SMALL["specdec_bf16"],
     "fused_fp32_Q40": SMALL["chunk_fp32_Q40"],
     "tensor_f16_D192": TC["r128_fp16_D192_Dv128"].replace(M=1001, lengths=("uniform", 500, 993)),
     # one row group, M a multiple of 8: the two-pass form, which writes the

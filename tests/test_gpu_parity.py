@@ -341,6 +341,17 @@ TC = {
                              lengths=("uniform", 0, 752), counts=("uniform", 0, 25)),
     "r256_bf16_D192": Spec(B=1, Hq=16, Hk=1, Q=16, D=192, Dv=128, M=1000, dtype="bf16",
                            lengths=("uniform", 500, 984), counts=("uniform", 1, 16)),
+    # 9 to 63 rows per unit (the rest of the 128 tensor-memory lanes are padding):
+    # the least, a decode-like GQA spec step, D = 256 with Dv = 64, a ragged 48
+    "r9_f16_min": Spec(B=3, Hq=9, Hk=1, Q=1, D=128, Dv=128, M=500, dtype="f16",
+                       lengths=("uniform", 0, 498)),
+    "r16_bf16_specdec": Spec(B=4, Hq=8, Hk=2, Q=4, D=128, Dv=128, M=700, dtype="bf16",
+                             lengths=("uniform", 10, 690), counts=("uniform", 0, 4),
+                             hot_frac=0.05, hot_scale=50.0),
+    "r12_bf16_D256_Dv64": Spec(B=2, Hq=12, Hk=4, Q=4, D=256, Dv=64, M=400, dtype="bf16",
+                               lengths=("uniform", 100, 390)),
+    "r48_fp16_ragged": Spec(B=3, Hq=16, Hk=1, Q=3, D=64, Dv=64, M=650, dtype="f16",
+                            lengths=("uniform", 0, 640), counts=("uniform", 0, 3)),
 }
 
 
