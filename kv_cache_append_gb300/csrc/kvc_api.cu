@@ -297,6 +297,15 @@ void generic_plan(const kvc_dims& d, Plan* pl) {
 #ifndef KVC_TC_MIN_ROWS
 #define KVC_TC_MIN_ROWS 9
 #endif
+// Wide rows (D + Dv of 320 elements and more) take it at any row count: per
+// 64-slot tile the products are cheap and the tile's bytes large, while the
+// CUDA-core kernel's per-lane query registers grow with D (gqa_decode's shapes
+// with 4 rows: D = 192 / Dv = 128 0.72 -> 0.89 of the copy ceiling, D = 256 /
+// Dv = 128 0.53 -> 1.00, D = 256 / Dv = 64 0.44 -> 0.98; D = Dv = 128 stays on
+// the CUDA-core kernel, 0.99 against 0.74).
+#ifndef KVC_TC_MIN_WIDTH
+#define KVC_TC_MIN_WIDTH 320
+#endif
 // The gradients' statistics pass runs the tensor-core step (into workspace
 // copies of its outputs, a full cache copy) only for units this wide; below,
 // the decode kernel or the CUDA-core kernel leave the statistics without a copy.
@@ -305,14 +314,16 @@ constexpr int kTcT = 64;        // slots per tile of the tensor-core kernel
 constexpr int kTcBox = 64 * 128;  // one 64-element-wide box of a tile
 
 // Shapes the tensor-core kernel takes: 16-bit caches, key and value widths
-// multiples of 64 (at most 256), KVC_TC_MIN_ROWS..256 query rows per unit
-// (more than 128: two row groups).
+// multiples of 64 (at most 256), KVC_TC_MIN_ROWS..256 query rows per unit, or
+// any row count for rows of KVC_TC_MIN_WIDTH elements (more than 128 rows:
+// two row groups).
 // Tensor memory holds S twice (2 x 64 columns), O (Dv), Q (D/2) and P twice
 // (2 x 32): Dv + D/2 <= 320.
 bool tc_shapes(const kvc_dims& d) {
     const int64_t R = (d.Hq / d.Hk) * d.Q;
     return d.dtype != KVC_F32 && d.D % 64 == 0 && d.D <= 256 && d.Dv % 64 == 0 && d.Dv <= 256 &&
-           d.Dv + d.D / 2 <= 320 && d.Q >= 1 && R >= KVC_TC_MIN_ROWS && R <= 256 &&
+           d.Dv + d.D / 2 <= 320 && d.Q >= 1 &&
+           (R >= KVC_TC_MIN_ROWS || d.D + d.Dv >= KVC_TC_MIN_WIDTH) && R <= 256 &&
            d.B * d.Hk < (int64_t(1) << 31);
 }
 

@@ -352,6 +352,13 @@ TC = {
                                lengths=("uniform", 100, 390)),
     "r48_fp16_ragged": Spec(B=3, Hq=16, Hk=1, Q=3, D=64, Dv=64, M=650, dtype="f16",
                             lengths=("uniform", 0, 640), counts=("uniform", 0, 3)),
+    # rows of 320 elements and more at any row count (decode shapes of wide heads)
+    "r4_bf16_D256_Dv128": Spec(B=3, Hq=8, Hk=2, Q=1, D=256, Dv=128, M=450, dtype="bf16",
+                               lengths=("uniform", 0, 449)),
+    "r1_f16_D192_Dv128": Spec(B=4, Hq=2, Hk=2, Q=1, D=192, Dv=128, M=300, dtype="f16",
+                              lengths=("uniform", 50, 299)),
+    "r6_bf16_D64_Dv256_ragged": Spec(B=3, Hq=2, Hk=1, Q=3, D=64, Dv=256, M=200, dtype="bf16",
+                                     lengths=("uniform", 0, 197), counts=("uniform", 0, 3)),
 }
 
 
