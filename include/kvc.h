@@ -191,7 +191,8 @@ KVC_API int kvc_step_inplace_timed(const kvc_dims *dims, const void *query, cons
  * Kernel count and path name of kvc_step_inplace for these sizes and
  * pointers: as kvc_plan_info, or "decode_tc" where the step that copies no
  * cache runs its attention on the decode tensor-core kernel (16-bit caches,
- * D a multiple of 64 up to 256, Dv = 128, at most 16 query rows per KV head).
+ * D a multiple of 64 up to 256, Dv = 128, at most 32 query rows per KV head;
+ * 17 to 32 rows with D up to 192, where two stages fit shared memory).
  * The read-only re-attention and the paged step (block sizes that are a
  * multiple of 64, or 8, 16 or 32) take the same path.
  */

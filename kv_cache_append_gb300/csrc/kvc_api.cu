@@ -385,15 +385,18 @@ bool tc_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
 #ifndef KVC_DECODE_TC
 #define KVC_DECODE_TC 1
 #endif
+#ifndef KVC_DEC_MAX_ROWS
+#define KVC_DEC_MAX_ROWS 32  // units of up to this many rows (16 or 32) take the decode kernel
+#endif
 constexpr int kDecT = 128;  // slots per tile of the decode tensor-core kernel
 
 // Shapes the decode tensor-core kernel takes (steps that copy no cache):
 // 16-bit caches, key width a multiple of 64 (at most 256), value width 128,
-// 1..16 query rows per unit.
+// 1..32 query rows per unit.
 bool dec_shapes(const kvc_dims& d) {
     const int64_t R = (d.Hq / d.Hk) * d.Q;
     return KVC_DECODE_TC && d.dtype != KVC_F32 && d.D % 64 == 0 && d.D <= 256 && d.Dv == 128 &&
-           d.Q >= 1 && R <= 16 && d.B * d.Hk * R < (int64_t(1) << 31) &&
+           d.Q >= 1 && R <= KVC_DEC_MAX_ROWS && d.B * d.Hk * R < (int64_t(1) << 31) &&
            d.M < (int64_t(1) << 30);
 }
 
@@ -403,8 +406,8 @@ void dec_tiling(const kvc_dims& d, Plan* pl) {
 }
 
 // Shared memory: barriers | abort flag | tile metadata | exchange buffers |
-// two P^T buffers (16 rows x 128 slots; four with src) | stages of K (128 x D), V (128 x Dv)
-// and the unit's 16 query rows, all in 64-element column blocks.
+// two P^T buffers (DN rows x 128 slots; four with src) | stages of K (128 x D), V (128 x Dv)
+// and the unit's DN query rows (16, or 32 for 17 to 32 rows), all in 64-element column blocks.
 // src: the statistics-pass instance, which also keeps the low parts of P^T
 // (two more buffers) for an fp32-accurate context.
 bool dec_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl, bool src = false) {
@@ -413,21 +416,22 @@ bool dec_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl, bool src = fal
     dec_tiling(d, pl);
     const int64_t nkb = d.D / 64, nvb = d.Dv / 64;
     const int64_t R = (d.Hq / d.Hk) * d.Q;
+    const int64_t DN = R <= 16 ? 16 : 32;  // the unit's rows padded (N of the products)
     pl->off_flag = 512;
     pl->off_meta = 1024;  // kMaxStages records of 32 bytes
     int64_t off = 1024 + int64_t(kMaxStages) * 32;
-    // [2][2][16][4] values, [2][2][4] flags, [2][16] block ids
+    // [2][2][DN][4] values, [2][2][4] flags, [2][16] block ids
     pl->dec_off_red = static_cast<int>(off);
-    off = align_up(off + 2 * 2 * 16 * 4 * 4 + 2 * 2 * 4 * 4 + 2 * 16 * 4, 1024);
+    off = align_up(off + 2 * 2 * DN * 4 * 4 + 2 * 2 * 4 * 4 + 2 * 16 * 4, 1024);
     pl->dec_off_pt = static_cast<int>(off);
-    off += (src ? 2 : 1) * 2 * 2 * 16 * 128;
+    off += (src ? 2 : 1) * 2 * 2 * DN * 128;
     pl->off_stages = static_cast<int>(off);
-    const int64_t stage = (nkb + nvb) * kDecT * 128 + nkb * 16 * 128;
+    const int64_t stage = (nkb + nvb) * kDecT * 128 + nkb * DN * 128;
     pl->stage_bytes = static_cast<int>(stage);
     if (off + 2 * stage > smem_cap) return false;
     pl->NS = static_cast<int>(std::min<int64_t>(kMaxStages, (smem_cap - off) / stage));
     pl->smem = static_cast<size_t>(off + int64_t(pl->NS) * stage);
-    pl->dec_nr = R <= 4 ? 4 : R <= 8 ? 8 : 16;
+    pl->dec_nr = R <= 4 ? 4 : R <= 8 ? 8 : R <= 16 ? 16 : 32;
     chunking(d, sms, pl);
     pl->P = std::min<int64_t>(sms, pl->NQ);
     pl->dec = true;
@@ -750,7 +754,7 @@ int step_impl(const kvc_dims* dims, const void* query, const void* new_key, cons
                 rows_map(&dp.tm_q, const_cast<void*>(query),
                          d.dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                         2, d.D, d.D, d.B * d.Hk * p.R, 1, 64, 16);
+                         2, d.D, d.D, d.B * d.Hk * p.R, 1, 64, pl.dec_nr <= 16 ? 16 : 32);
             if (!ok_maps) return KVC_E_CUDA;
             e = launch_decode_tc(dp, d.dtype, pl.dec_nr, pl.smem, stream);
             if (e == cudaSuccess) e = record();

@@ -1,5 +1,5 @@
 // kvc_decode_tc.cu -- attention of the steps that copy no cache (in place,
-// read-only re-attention, paged) on the tensor cores, for units of at most 16
+// read-only re-attention, paged) on the tensor cores, for units of at most 32
 // query rows (G = Hq/Hk heads x Q new tokens): decode and short speculative
 // steps.
 //
@@ -7,11 +7,11 @@
 // does 2 * R * (D + Dv) flops on it; on the CUDA cores the few rows per unit
 // cost tens of instructions per slot and warp, and the instruction issue, not
 // HBM, bounds the step. Here the cache slots are the M dimension of both
-// tcgen05 products of a 128-slot tile, with the unit's query rows as N = 16
-// (padded):
+// tcgen05 products of a 128-slot tile, with the unit's query rows as N = DN
+// (padded to 16, or to 32 for units of 17 to 32 rows):
 //
-//   S^T  = K Q^T      M = 128 slots, N = 16 rows, K = D    (A = K tile, B = Q)
-//   O^T += V^T P^T    M = Dv = 128,  N = 16 rows, K = 128 slots
+//   S^T  = K Q^T      M = 128 slots, N = DN rows, K = D    (A = K tile, B = Q)
+//   O^T += V^T P^T    M = Dv = 128,  N = DN rows, K = 128 slots
 //                                               (A = V tile read M-major, B = P^T)
 //
 // so per tile the tensor cores take the dot products and the weighted sum,
@@ -21,14 +21,15 @@
 //                   (the fused kernel's chunking and hand-out order), TMA-loads
 //                   each tile's K and V rows below the new length (64-element
 //                   boxes, 128-byte swizzle, the layout the tensor cores read)
-//                   and the unit's query rows (16 rows, 4 KB from L2) with it.
+//                   and the unit's query rows (DN rows, 4 or 8 KB from L2)
+//                   with it.
 //   MMA warp        one thread: S^T into one of two tensor-memory buffers.
 //   P.V warp        one thread: O^T += V^T P^T into the tensor-memory O^T as
 //                   soon as a tile's P^T is ready, then releases the stage
 //                   (issued from the MMA thread after the next tile's S^T, the
 //                   stage would be held until the next tile lands).
-//   softmax warps  one or two groups of 4 warps (two for 8 or 16 rows, each
-//                   group taking half of them), one slot per thread (= the
+//   softmax warps  one or two groups of 4 warps (two for 8, 16 or 32 rows,
+//                   each group taking half of them), one slot per thread (= the
 //                   tensor-memory lane of S^T):
 //                   applies scale*log2(e) and the lower-right causal limit
 //                   j <= length + t ("Required behavior", bullet 4), keeps the
@@ -71,10 +72,21 @@ namespace kvc {
 namespace {
 
 constexpr int kDT = 128;             // slots per tile (M of S^T = K Q^T)
-constexpr int kDN = 16;              // query rows of a unit, padded (N of both products)
 constexpr int kBlk = kDT * 128;      // one 64-element-wide column block of a K or V tile
-constexpr int kNBlk = kDN * 128;     // one 64-element-wide column block of Q or P^T
 constexpr int kHalf = 64;            // slots per TMA box of a contiguous cache
+// A unit's query rows padded to DN = 16 (units of up to 16 rows) or 32 (17 to
+// 32): the N of both products. Per DN: a 64-element column block of Q or P^T,
+// the tensor-memory columns (S^T twice, then O^T) and the exchange region's
+// layout (values [2][2 groups][DN][4 warps], flags [2][2 groups][4 warps],
+// then the paged block ids [2][kMaxPieces]).
+template <int DN>
+struct DecShape {
+    static constexpr int nblk = DN * 128;
+    static constexpr uint32_t col_o = 2 * DN;
+    static constexpr uint32_t tmem_cols = DN <= 16 ? 64 : 128;
+    static constexpr int flag_offset = 2 * 2 * DN * 4 * 4;
+    static constexpr int ids_offset = flag_offset + 2 * 2 * 4 * 4;
+};
 // KVC_DEC_PV_WARP: the P.V products get an issuer thread (and warp) of their
 // own, so that a tile's product goes out, and its stage is released, as soon
 // as its P^T is ready instead of after the next tile's scores (which wait for
@@ -93,13 +105,7 @@ struct DecRoles {
     static constexpr int threads = (4 * SG + (kPvWarp ? 3 : 2)) * 32;
 };
 constexpr float kRescale = 8.f;      // raise a row's reference maximum when exceeded by 2^8
-constexpr uint32_t kTmemCols = 64;
-constexpr uint32_t kColO = 32;
 constexpr int kMaxPieces = kDT / 8;  // paged: block pieces per tile at most (8-slot blocks)
-// exchange region: values [2][2 groups][kDN][4 warps], flags [2][2 groups][4
-// warps], then the paged block ids [2][kMaxPieces]
-constexpr int kFlagOffset = 2 * 2 * kDN * 4 * 4;
-constexpr int kIdsOffset = kFlagOffset + 2 * 2 * 4 * 4;
 
 struct DecBars {
     uint32_t base;
@@ -152,9 +158,13 @@ template <>
 struct RowsLog2<4> { static constexpr int v = 2; };
 template <>
 struct RowsLog2<8> { static constexpr int v = 3; };
+template <>
+struct RowsLog2<16> { static constexpr int v = 4; };
 
+template <int DN>
 __device__ void dec_producer(const DecParams& dp, unsigned char* smem, DecBars bars,
                              volatile int* abort) {
+    constexpr int kNBlk = DecShape<DN>::nblk;
     const StepParams& p = dp.p;
     const uint32_t stage0 = smem_addr(smem + p.off_stages);
     TileMeta* meta = reinterpret_cast<TileMeta*>(smem + p.off_meta);
@@ -167,7 +177,7 @@ __device__ void dec_producer(const DecParams& dp, unsigned char* smem, DecBars b
     // paged: block ids of a tile's pieces, two tiles' worth, copied from the
     // block table without waiting (a piece never straddles two blocks: the
     // piece height divides the block size)
-    int32_t* pids = reinterpret_cast<int32_t*>(smem + p.dec_off_red + kIdsOffset);
+    int32_t* pids = reinterpret_cast<int32_t*>(smem + p.dec_off_red + DecShape<DN>::ids_offset);
     auto request_ids = [&](const Unit& x, int64_t i) {
         const int bs = static_cast<int>(p.block_size), hh = min(kHalf, bs);
         const int jt = static_cast<int>(i * kDT);
@@ -276,8 +286,10 @@ __device__ void dec_producer(const DecParams& dp, unsigned char* smem, DecBars b
 // copies (one per block piece and 64-element column block) are spread over
 // the lanes, so a tile of 16-slot blocks (8 pieces x 4 copies) is issued in
 // parallel.
+template <int DN>
 __device__ void dec_producer_warp(const DecParams& dp, unsigned char* smem, DecBars bars,
                                   volatile int* abort) {
+    constexpr int kNBlk = DecShape<DN>::nblk;
     const StepParams& p = dp.p;
     const int lane = threadIdx.x & 31;
     const uint32_t stage0 = smem_addr(smem + p.off_stages);
@@ -289,7 +301,7 @@ __device__ void dec_producer_warp(const DecParams& dp, unsigned char* smem, DecB
     int64_t issued = 0;
     Ring ring;
     bool ok = true;
-    int32_t* pids = reinterpret_cast<int32_t*>(smem + p.dec_off_red + kIdsOffset);
+    int32_t* pids = reinterpret_cast<int32_t*>(smem + p.dec_off_red + DecShape<DN>::ids_offset);
     auto request_ids = [&](const Unit& x, int64_t i) {  // lane 0
         const int bs = static_cast<int>(p.block_size), hh = min(kHalf, bs);
         const int jt = static_cast<int>(i * kDT);
@@ -396,15 +408,18 @@ __device__ void dec_producer_warp(const DecParams& dp, unsigned char* smem, DecB
 }
 
 // One thread issues every tensor-core instruction of the CTA.
+template <int DN>
 __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars bars,
                                volatile int* abort, uint32_t tmem, bool bf16, bool lo) {
+    constexpr int kNBlk = DecShape<DN>::nblk;
+    constexpr uint32_t kColO = DecShape<DN>::col_o;
     const StepParams& p = dp.p;
     const uint32_t stage0 = smem_addr(smem + p.off_stages);
     const uint32_t pt0 = smem_addr(smem + p.dec_off_pt);
     const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
     const int nkb = static_cast<int>(p.D / 64), nvb = static_cast<int>(p.Dv / 64);
-    const uint32_t idesc_s = mma_idesc_f16(kDT, kDN, bf16, false, false);
-    const uint32_t idesc_o = mma_idesc_f16(static_cast<int>(p.Dv), kDN, bf16, false, true);
+    const uint32_t idesc_s = mma_idesc_f16(kDT, DN, bf16, false, false);
+    const uint32_t idesc_o = mma_idesc_f16(static_cast<int>(p.Dv), DN, bf16, false, true);
     Ring ring;
     int sbuf = 0;
     int s_uses[2] = {0, 0};
@@ -461,7 +476,7 @@ __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars
             for (int kb = 0; kb < nkb; ++kb) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // 16 elements per step
-                    tc_mma(tmem + sbuf * kDN, smem_desc_sw128(sK + kb * kBlk + kk * 32, 16, 1024),
+                    tc_mma(tmem + sbuf * DN, smem_desc_sw128(sK + kb * kBlk + kk * 32, 16, 1024),
                            smem_desc_sw128(sQ + kb * kNBlk + kk * 32, 16, 1024), idesc_s,
                            (kb | kk) != 0);
             }
@@ -496,14 +511,17 @@ __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars
 
 // With kPvWarp: one thread issues every O^T += V^T P^T product, walking the
 // same ring, and releases each attended stage after its product.
+template <int DN>
 __device__ void dec_pv_issuer(const DecParams& dp, unsigned char* smem, DecBars bars,
                               volatile int* abort, uint32_t tmem, bool bf16, bool lo) {
+    constexpr int kNBlk = DecShape<DN>::nblk;
+    constexpr uint32_t kColO = DecShape<DN>::col_o;
     const StepParams& p = dp.p;
     const uint32_t stage0 = smem_addr(smem + p.off_stages);
     const uint32_t pt0 = smem_addr(smem + p.dec_off_pt);
     const TileMeta* meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
     const int nkb = static_cast<int>(p.D / 64);
-    const uint32_t idesc_o = mma_idesc_f16(static_cast<int>(p.Dv), kDN, bf16, false, true);
+    const uint32_t idesc_o = mma_idesc_f16(static_cast<int>(p.Dv), DN, bf16, false, true);
     Ring ring;
     int64_t pv_count = 0;
     bool attend = false;
@@ -553,6 +571,10 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
                             volatile int* abort, uint32_t tmem) {
     using S = Storage<T>;
     const StepParams& p = dp.p;
+    constexpr int DN = NR <= 16 ? 16 : 32;  // rows padded (N of the products)
+    constexpr int kDN = DN;
+    constexpr int kNBlk = DecShape<DN>::nblk;
+    constexpr uint32_t kColO = DecShape<DN>::col_o;
     constexpr int NW = NR / SG;  // rows of this thread's group
     const int t = threadIdx.x & 127;  // slot of the tile (lane of S^T); value column of O^T
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -566,7 +588,7 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
     unsigned char* stages = smem + p.off_stages;
     unsigned char* pt = smem + p.dec_off_pt;
     float* xval = reinterpret_cast<float*>(smem + p.dec_off_red) + g * kDN * 4;
-    int* xflag = reinterpret_cast<int*>(smem + p.dec_off_red + kFlagOffset) + g * 4;
+    int* xflag = reinterpret_cast<int*>(smem + p.dec_off_red + DecShape<DN>::flag_offset) + g * 4;
     constexpr int kGroup = 32 / NW;  // lanes that end a reduction with one row
     Ring ring;
     int sbuf = 0;
@@ -802,6 +824,9 @@ template <typename T, int NR, int SG, bool SRC, bool WP>
 __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
     decode_tc_kernel(const __grid_constant__ DecParams dp) {
     using Roles = DecRoles<SG>;
+    constexpr int DN = NR <= 16 ? 16 : 32;
+    constexpr int kNBlk = DecShape<DN>::nblk;
+    constexpr uint32_t kTmemCols = DecShape<DN>::tmem_cols;
     extern __shared__ __align__(1024) unsigned char smem[];
     const StepParams& p = dp.p;
     const DecBars bars{smem_addr(smem)};
@@ -840,7 +865,7 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
         dec_softmax<T, NR, SG, SRC>(dp, smem, bars, abort, tmem);
     } else if (warp == Roles::mma) {
         if ((threadIdx.x & 31) == 0)
-            dec_mma_issuer(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value, SRC);
+            dec_mma_issuer<DN>(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value, SRC);
     } else if (warp == Roles::prod) {
         // paged pools of blocks under 64 slots: 8 to 16 pieces of 4 copies per
         // tile, issued by the warp's lanes (in-place gqa_decode 16-slot blocks:
@@ -849,12 +874,12 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
         // separate instance: with both producers compiled in, the 16-row
         // instance ran ragged_specdec in place 7% slower.
         if (WP)
-            dec_producer_warp(dp, smem, bars, abort);
+            dec_producer_warp<DN>(dp, smem, bars, abort);
         else if ((threadIdx.x & 31) == 0)
-            dec_producer(dp, smem, bars, abort);
+            dec_producer<DN>(dp, smem, bars, abort);
     } else if (kPvWarp && warp == Roles::pv) {
         if ((threadIdx.x & 31) == 0)
-            dec_pv_issuer(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value, SRC);
+            dec_pv_issuer<DN>(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value, SRC);
     }
     tc_fence_before();
     __syncthreads();  // every thread reaches this exactly once: all waits are bounded
@@ -886,20 +911,23 @@ cudaError_t launch_rows(const DecParams& dp, int nr, size_t smem, cudaStream_t s
         switch (nr) {
             case 4: return launch_t<T, 4, 1, true>(dp, smem, stream);
             case 8: return launch_t<T, 8, KVC_DEC_GROUPS8, true>(dp, smem, stream);
-            default: return launch_t<T, 16, 2, true>(dp, smem, stream);
+            case 16: return launch_t<T, 16, 2, true>(dp, smem, stream);
+            default: return launch_t<T, 32, 2, true>(dp, smem, stream);
         }
     }
     if (dp.p.block_table && dp.p.block_size < kHalf) {  // the warp producer
         switch (nr) {
             case 4: return launch_t<T, 4, 1, false, true>(dp, smem, stream);
             case 8: return launch_t<T, 8, KVC_DEC_GROUPS8, false, true>(dp, smem, stream);
-            default: return launch_t<T, 16, 2, false, true>(dp, smem, stream);
+            case 16: return launch_t<T, 16, 2, false, true>(dp, smem, stream);
+            default: return launch_t<T, 32, 2, false, true>(dp, smem, stream);
         }
     }
     switch (nr) {
         case 4: return launch_t<T, 4, 1, false>(dp, smem, stream);
         case 8: return launch_t<T, 8, KVC_DEC_GROUPS8, false>(dp, smem, stream);
-        default: return launch_t<T, 16, 2, false>(dp, smem, stream);
+        case 16: return launch_t<T, 16, 2, false>(dp, smem, stream);
+        default: return launch_t<T, 32, 2, false>(dp, smem, stream);
     }
 }
 

@@ -51,8 +51,8 @@ struct DecParams {
 };
 
 // Attention of the steps that copy no cache (in place, read-only, paged) on
-// the tensor cores, for units of at most 16 query rows (kvc_decode_tc.cu).
-// nr: 4, 8 or 16 rows the kernel is instantiated for (>= R).
+// the tensor cores, for units of at most 32 query rows (kvc_decode_tc.cu).
+// nr: 4, 8, 16 or 32 rows the kernel is instantiated for (>= R).
 cudaError_t launch_decode_tc(const DecParams& dp, int dtype, int nr, size_t smem,
                              cudaStream_t stream);
 

@@ -181,7 +181,7 @@ CASES = {
                                    lengths=("uniform", 0, 690), counts=("uniform", 0, 4)),
     "tc_walk_f16_R64_D128": Spec(B=40, Hq=16, Hk=1, Q=4, D=128, Dv=128, M=1100, dtype="f16",
                                  lengths=("uniform", 300, 1090)),
-    # statistics on the decode tensor-core kernel (16-bit, Dv = 128, at most 16
+    # statistics on the decode tensor-core kernel (16-bit, Dv = 128, at most 32
     # rows), which takes the appended rows from new_key / new_value: 16 rows
     # whose new rows straddle the first 128-slot tile's end, D = 256 (8 rows)
     # (the tiled slot kernel) and D = 64 (4 rows, the generic slot kernel)
@@ -216,7 +216,8 @@ SLOT = {"tiny_fp32": "bwd_kv_kernel", "decode_bf16_ragged_M": "bwd_kv_rows_kerne
 
 # the cases whose statistics pass runs the decode tensor-core kernel
 DECODE_STATS = ("decode_bf16_ragged_M", "specdec_bf16_hot", "tiled_f16_D64_Dv128_R8",
-                "dec_bf16_R16_tile_edge", "dec_f16_D256_R8", "dec_bf16_D64_R4")
+                "dec_bf16_R16_tile_edge", "dec_f16_D256_R8", "dec_bf16_D64_R4",
+                "tc_f16_D128_R17", "tc_bf16_D128_R32_hot", "tc_f16_D128_R32_staged")
 
 
 def plan_of(spec):
@@ -235,7 +236,7 @@ def test_backward_plan():
     assert plan_of(CASES["tc_bf16_D64_R128_ragged"])[:2] == (7, "tensor")
     assert plan_of(CASES["tiled_bf16_D128_R40_ragged"])[:2] == (6, "fused")
     assert plan_of(workloads.SPECS["chunked_append"]) == (6, "fused", "bwd_kv_tiled_kernel")
-    # 16-bit, Dv = 128, at most 16 rows: the decode tensor-core kernel
+    # 16-bit, Dv = 128, at most 32 rows: the decode tensor-core kernel
     assert plan_of(workloads.SPECS["gqa_decode"]) == (6, "decode", "bwd_kv_rows_kernel")
     assert plan_of(workloads.SPECS["ragged_specdec"]) == (6, "decode", "bwd_kv_tc_kernel")
     for name in DECODE_STATS:

@@ -1,6 +1,6 @@
 """GPU parity of the decode tensor-core kernel (kvc_decode_tc.cu) against the
 fp64 oracle: steps that copy no cache (in place, paged, read-only) with 16-bit
-caches, D a multiple of 64 up to 256, Dv = 128 and at most 16 query rows per
+caches, D a multiple of 64 up to 256, Dv = 128 and at most 32 query rows per
 KV head. The caches after the step bit for bit, lengths exact, attention and
 context within the step's tolerances. Shapes cover every row count the kernel
 is instantiated for, tiles cut by M and by the new length, many chunks per
@@ -45,6 +45,15 @@ CASES = {
                             lengths=("uniform", 200, 1490), hot_frac=0.05, hot_scale=50.0),
     "r16_f16_Q16_mqa": Spec(B=2, Hq=1, Hk=1, Q=16, D=128, Dv=128, M=600, dtype="f16",
                             counts=("uniform", 1, 16)),
+    # 17 to 32 rows: two groups of 16 padded rows, the second one partly empty
+    "r24_bf16_Q3": Spec(B=3, Hq=8, Hk=1, Q=3, D=128, Dv=128, M=700, dtype="bf16",
+                        counts=("uniform", 0, 3)),
+    "r20_f16_Q5_D64": Spec(B=2, Hq=4, Hk=1, Q=5, D=64, Dv=128, M=333, dtype="f16",
+                           lengths=("uniform", 0, 300)),
+    "r32_bf16_Q4_hot": Spec(B=3, Hq=32, Hk=4, Q=4, D=128, Dv=128, M=1300, dtype="bf16",
+                            lengths=("uniform", 100, 1290), hot_frac=0.05, hot_scale=50.0),
+    "r32_f16_Q8_D192": Spec(B=2, Hq=4, Hk=1, Q=8, D=192, Dv=128, M=500, dtype="f16",
+                            counts=("uniform", 1, 8)),
     # one unit, many chunks (one tile each at 152 CTAs), a hot slot late in the row
     "r4_bf16_long_row": Spec(B=1, Hq=4, Hk=1, Q=1, D=128, Dv=128, M=20000, dtype="bf16",
                              lengths=("uniform", 19000, 19990), hot_frac=0.5, hot_scale=40.0),
@@ -65,6 +74,8 @@ def test_decode_tc_not_taken_outside_its_shapes():
     # 40 rows: the tensor-core step (from 9 rows), 16-bit with widths it takes
     assert path_of(Spec(B=2, Hq=8, Hk=1, Q=5, D=128, Dv=128, M=100, dtype="bf16")) == "tensor"
     assert path_of(Spec(B=2, Hq=8, Hk=2, Q=1, D=96, Dv=128, M=100, dtype="bf16")) == "fused"
+    # 17 to 32 rows with D = 256: two stages of 32 padded rows overflow shared memory
+    assert path_of(Spec(B=2, Hq=4, Hk=1, Q=8, D=256, Dv=128, M=100, dtype="f16")) == "tensor"
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
@@ -75,7 +86,8 @@ def test_decode_tc_inplace_parity(name, seed):
     compare_full(x, out, status)
 
 
-@pytest.mark.parametrize("name", ["r4_bf16_D256", "r16_bf16_Q4_hot", "r5_f16_ragged"])
+@pytest.mark.parametrize("name", ["r4_bf16_D256", "r16_bf16_Q4_hot", "r5_f16_ragged",
+                                  "r32_bf16_Q4_hot"])
 def test_decode_tc_poisoned_tail(name):
     """Inf keys and NaN values from each row's new length on reach nothing."""
     x = workloads.generate(CASES[name], 3)
@@ -89,7 +101,7 @@ def test_decode_tc_poisoned_tail(name):
 
 
 @pytest.mark.parametrize("bs", [8, 16, 32, 64, 128, 256])
-@pytest.mark.parametrize("name", ["r4_bf16_D256", "r16_bf16_Q4_hot"])
+@pytest.mark.parametrize("name", ["r4_bf16_D256", "r16_bf16_Q4_hot", "r24_bf16_Q3"])
 def test_decode_tc_paged(name, bs):
     spec = CASES[name]
     M = (spec.M + bs - 1) // bs * bs
