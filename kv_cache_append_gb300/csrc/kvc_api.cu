@@ -385,6 +385,9 @@ bool tc_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl) {
 #ifndef KVC_DECODE_TC
 #define KVC_DECODE_TC 1
 #endif
+#ifndef KVC_DEC_PT32
+#define KVC_DEC_PT32 1  // P^T buffers of the decode kernel's 32-row forward instances
+#endif
 #ifndef KVC_DEC_MAX_ROWS
 #define KVC_DEC_MAX_ROWS 32  // units of up to this many rows (16 or 32) take the decode kernel
 #endif
@@ -406,10 +409,11 @@ void dec_tiling(const kvc_dims& d, Plan* pl) {
 }
 
 // Shared memory: barriers | abort flag | tile metadata | exchange buffers |
-// two P^T buffers (DN rows x 128 slots; four with src) | stages of K (128 x D), V (128 x Dv)
-// and the unit's DN query rows (16, or 32 for 17 to 32 rows), all in 64-element column blocks.
+// P^T buffers (DN rows x 128 slots; two, one for 32 rows outside src; twice as
+// many with src) | stages of K (128 x D), V (128 x Dv) and the unit's DN query
+// rows (16, or 32 for 17 to 32 rows), all in 64-element column blocks.
 // src: the statistics-pass instance, which also keeps the low parts of P^T
-// (two more buffers) for an fp32-accurate context.
+// for an fp32-accurate context.
 bool dec_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl, bool src = false) {
     if (!dec_shapes(d)) return false;
     *pl = Plan();
@@ -420,11 +424,12 @@ bool dec_plan(const kvc_dims& d, int sms, int smem_cap, Plan* pl, bool src = fal
     pl->off_flag = 512;
     pl->off_meta = 1024;  // kMaxStages records of 32 bytes
     int64_t off = 1024 + int64_t(kMaxStages) * 32;
-    // [2][2][DN][4] values, [2][2][4] flags, [2][16] block ids
+    // [2][2][DN/2][4] values, [2][2][4] flags, [2][16] block ids
     pl->dec_off_red = static_cast<int>(off);
-    off = align_up(off + 2 * 2 * DN * 4 * 4 + 2 * 2 * 4 * 4 + 2 * 16 * 4, 1024);
+    off = align_up(off + 2 * 2 * (DN / 2) * 4 * 4 + 2 * 2 * 4 * 4 + 2 * 16 * 4, 1024);
     pl->dec_off_pt = static_cast<int>(off);
-    off += (src ? 2 : 1) * 2 * 2 * DN * 128;
+    const int64_t npt = (DN == 32 && !src) ? KVC_DEC_PT32 : 2;  // P^T buffers
+    off += (src ? 2 : 1) * npt * 2 * DN * 128;
     pl->off_stages = static_cast<int>(off);
     const int64_t stage = (nkb + nvb) * kDecT * 128 + nkb * DN * 128;
     pl->stage_bytes = static_cast<int>(stage);

@@ -77,16 +77,26 @@ constexpr int kHalf = 64;            // slots per TMA box of a contiguous cache
 // A unit's query rows padded to DN = 16 (units of up to 16 rows) or 32 (17 to
 // 32): the N of both products. Per DN: a 64-element column block of Q or P^T,
 // the tensor-memory columns (S^T twice, then O^T) and the exchange region's
-// layout (values [2][2 groups][DN][4 warps], flags [2][2 groups][4 warps],
-// then the paged block ids [2][kMaxPieces]).
+// layout (values [2][2 groups][DN/2 rows][4 warps], flags [2][2 groups][4
+// warps], then the paged block ids [2][kMaxPieces]).
 template <int DN>
 struct DecShape {
     static constexpr int nblk = DN * 128;
     static constexpr uint32_t col_o = 2 * DN;
     static constexpr uint32_t tmem_cols = DN <= 16 ? 64 : 128;
-    static constexpr int flag_offset = 2 * 2 * DN * 4 * 4;
+    static constexpr int xrows = DN / 2;  // rows of a softmax group at most
+    static constexpr int flag_offset = 2 * 2 * xrows * 4 * 4;
     static constexpr int ids_offset = flag_offset + 2 * 2 * 4 * 4;
 };
+// P^T buffers: two, so that a tile's P^T is written while the previous
+// tile's product reads the other; one for the 32-row forward instances, whose
+// 8 KB P^T would otherwise cost the third ring stage at D = 128 (the softmax
+// then computes a tile's P before it waits for the previous product).
+#ifndef KVC_DEC_PT32
+#define KVC_DEC_PT32 1  // P^T buffers of the 32-row forward instances (1 or 2)
+#endif
+template <int DN, bool SRC>
+struct DecPt { static constexpr int n = (DN == 32 && !SRC) ? KVC_DEC_PT32 : 2; };
 // KVC_DEC_PV_WARP: the P.V products get an issuer thread (and warp) of their
 // own, so that a tile's product goes out, and its stage is released, as soon
 // as its P^T is ready instead of after the next tile's scores (which wait for
@@ -408,7 +418,7 @@ __device__ void dec_producer_warp(const DecParams& dp, unsigned char* smem, DecB
 }
 
 // One thread issues every tensor-core instruction of the CTA.
-template <int DN>
+template <int DN, int NPT>
 __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars bars,
                                volatile int* abort, uint32_t tmem, bool bf16, bool lo) {
     constexpr int kNBlk = DecShape<DN>::nblk;
@@ -423,14 +433,14 @@ __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars
     Ring ring;
     int sbuf = 0;
     int s_uses[2] = {0, 0};
-    int64_t pv_count = 0;  // products O^T += V^T P^T issued; the c-th reads P^T[c % 2]
+    int64_t pv_count = 0;  // products O^T += V^T P^T issued; the c-th reads P^T[c % NPT]
     bool attend = false, has_pending = false, pend_first = false;
     int pend_stage = 0;
     int64_t N = 0;
 
     auto issue_pv = [&](int stage, bool first) -> bool {
-        const int pb = static_cast<int>(pv_count & 1);
-        if (!mbar_wait(bars.p_ready(pb), static_cast<uint32_t>((pv_count >> 1) & 1), abort))
+        const int pb = static_cast<int>(pv_count % NPT);
+        if (!mbar_wait(bars.p_ready(pb), static_cast<uint32_t>((pv_count / NPT) & 1), abort))
             return false;
         tc_fence_after();
         const uint32_t sV = stage0 + static_cast<uint32_t>(stage) * p.stage_bytes +
@@ -441,11 +451,11 @@ __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars
             tc_mma(tmem + kColO, smem_desc_sw128(sV + kk * 16 * 128, kBlk, 1024),
                    smem_desc_sw128(sP + (kk >> 2) * kNBlk + (kk & 3) * 32, 16, 1024), idesc_o,
                    !(first && kk == 0));
-        if (lo) {  // the low parts of P^T, two buffers on
+        if (lo) {  // the low parts of P^T, NPT buffers on
 #pragma unroll
             for (int kk = 0; kk < kDT / 16; ++kk)
                 tc_mma(tmem + kColO, smem_desc_sw128(sV + kk * 16 * 128, kBlk, 1024),
-                       smem_desc_sw128(sP + 4 * kNBlk + (kk >> 2) * kNBlk + (kk & 3) * 32, 16, 1024),
+                       smem_desc_sw128(sP + NPT * 2 * kNBlk + (kk >> 2) * kNBlk + (kk & 3) * 32, 16, 1024),
                        idesc_o, true);
         }
         tc_commit(bars.o_done(pb));
@@ -511,7 +521,7 @@ __device__ void dec_mma_issuer(const DecParams& dp, unsigned char* smem, DecBars
 
 // With kPvWarp: one thread issues every O^T += V^T P^T product, walking the
 // same ring, and releases each attended stage after its product.
-template <int DN>
+template <int DN, int NPT>
 __device__ void dec_pv_issuer(const DecParams& dp, unsigned char* smem, DecBars bars,
                               volatile int* abort, uint32_t tmem, bool bf16, bool lo) {
     constexpr int kNBlk = DecShape<DN>::nblk;
@@ -538,8 +548,8 @@ __device__ void dec_pv_issuer(const DecParams& dp, unsigned char* smem, DecBars 
             attend = mt.n > 0 && static_cast<int64_t>(mt.i) * kDT < N;
         }
         if (!(attend && static_cast<int64_t>(mt.i) * kDT < N)) continue;  // the S issuer releases it
-        const int pb = static_cast<int>(pv_count & 1);
-        if (!mbar_wait(bars.p_ready(pb), static_cast<uint32_t>((pv_count >> 1) & 1), abort)) break;
+        const int pb = static_cast<int>(pv_count % NPT);
+        if (!mbar_wait(bars.p_ready(pb), static_cast<uint32_t>((pv_count / NPT) & 1), abort)) break;
         tc_fence_after();
         const uint32_t sV = stage0 + static_cast<uint32_t>(s) * p.stage_bytes +
                             static_cast<uint32_t>(nkb * kBlk);
@@ -554,7 +564,7 @@ __device__ void dec_pv_issuer(const DecParams& dp, unsigned char* smem, DecBars 
 #pragma unroll
             for (int kk = 0; kk < kDT / 16; ++kk)
                 tc_mma(tmem + kColO, smem_desc_sw128(sV + kk * 16 * 128, kBlk, 1024),
-                       smem_desc_sw128(sP + 4 * kNBlk + (kk >> 2) * kNBlk + (kk & 3) * 32, 16, 1024),
+                       smem_desc_sw128(sP + NPT * 2 * kNBlk + (kk >> 2) * kNBlk + (kk & 3) * 32, 16, 1024),
                        idesc_o, true);
         }
         tc_commit(bars.o_done(pb));
@@ -575,6 +585,8 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
     constexpr int kDN = DN;
     constexpr int kNBlk = DecShape<DN>::nblk;
     constexpr uint32_t kColO = DecShape<DN>::col_o;
+    constexpr int kX = DecShape<DN>::xrows;
+    constexpr int NPT = DecPt<DN, SRC>::n;
     constexpr int NW = NR / SG;  // rows of this thread's group
     const int t = threadIdx.x & 127;  // slot of the tile (lane of S^T); value column of O^T
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -587,14 +599,14 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
     const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);  // this warp's lanes
     unsigned char* stages = smem + p.off_stages;
     unsigned char* pt = smem + p.dec_off_pt;
-    float* xval = reinterpret_cast<float*>(smem + p.dec_off_red) + g * kDN * 4;
+    float* xval = reinterpret_cast<float*>(smem + p.dec_off_red) + g * kX * 4;
     int* xflag = reinterpret_cast<int*>(smem + p.dec_off_red + DecShape<DN>::flag_offset) + g * 4;
     constexpr int kGroup = 32 / NW;  // lanes that end a reduction with one row
     Ring ring;
     int sbuf = 0;
     int64_t su[2] = {0, 0};   // completions consumed per S^T buffer
     int64_t comp = 0;         // attending tiles done = products issued for them
-    int64_t pvd[2] = {0, 0};  // completions consumed on o_done[0], o_done[1]
+    int64_t pvd[2] = {0, 0};  // completions consumed on o_done[0], o_done[NPT - 1]
     uint32_t rv = 0;          // rendezvous of the group's 4 warps so far
     bool attend = false, first_tile = false;
     int64_t L = 0, n = 0, N = 0, u = 0, k = 0, rowoff0 = 0;
@@ -607,11 +619,11 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
         lsum[r] = 0.f;
     }
 
-    // Wait until product c (which read P^T[c % 2]) has finished, consuming the
-    // completions of that buffer's barrier strictly in order.
+    // Wait until product c (which read P^T[c % NPT]) has finished, consuming
+    // the completions of that buffer's barrier strictly in order.
     auto wait_pv = [&](int64_t c) -> bool {
-        const int b = static_cast<int>(c & 1);
-        for (; pvd[b] <= (c >> 1); ++pvd[b])
+        const int b = static_cast<int>(c % NPT);
+        for (; pvd[b] <= c / NPT; ++pvd[b])
             if (!warp_wait(bars.o_done(b), static_cast<uint32_t>(pvd[b] & 1), abort)) return false;
         return true;
     };
@@ -721,12 +733,12 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
                 const uint32_t bm = rv & 1u;
                 const float mine = warp_reduce_rows<NW, true>(sv);
                 if ((lane & (kGroup - 1)) == 0)
-                    xval[(bm * 2 * kDN + (lane >> (5 - RowsLog2<NW>::v))) * 4 + wq] = mine;
+                    xval[(bm * 2 * kX + (lane >> (5 - RowsLog2<NW>::v))) * 4 + wq] = mine;
                 if (!rendezvous()) break;
 #pragma unroll
                 for (int r = 0; r < NW; ++r) {
                     const float4 q4 =
-                        *reinterpret_cast<const float4*>(xval + (bm * 2 * kDN + r) * 4);
+                        *reinterpret_cast<const float4*>(xval + (bm * 2 * kX + r) * 4);
                     const float tmax = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
                     if (tmax > mref[r] + kRescale) {
                         if (mref[r] != -INFINITY) {
@@ -738,20 +750,23 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
                     }
                 }
             }
-            // P^T[comp % 2] is free once the product two tiles back has finished
-            if (comp >= 2 && !wait_pv(comp - 2)) break;
-            unsigned char* pbox = pt + (comp & 1) * 2 * kNBlk + (t >> 6) * kNBlk;
+#pragma unroll
+            for (int r = 0; r < NW; ++r) {  // sv[r] becomes P of row r
+                sv[r] = (j <= lim[r]) ? fast_exp2(sv[r] - mref[r]) : 0.f;
+                lsum[r] += sv[r];
+            }
+            // P^T[comp % NPT] is free once the product NPT tiles back has finished
+            if (comp >= NPT && !wait_pv(comp - NPT)) break;
+            unsigned char* pbox = pt + (comp % NPT) * 2 * kNBlk + (t >> 6) * kNBlk;
             const int ck = (t & 63) >> 3, e2 = (t & 7) * 2;
 #pragma unroll
             for (int r = 0; r < NW; ++r) {
-                const float e = (j <= lim[r]) ? fast_exp2(sv[r] - mref[r]) : 0.f;
-                lsum[r] += e;
                 const int rr = r0 + r;
-                const T hi = S::from_float(e);
+                const T hi = S::from_float(sv[r]);
                 *reinterpret_cast<T*>(pbox + rr * 128 + ((ck ^ (rr & 7)) << 4) + e2) = hi;
                 if (SRC)  // the statistics pass: P = hi + lo, its context accurate to fp32's order
-                    *reinterpret_cast<T*>(pbox + 4 * kNBlk + rr * 128 + ((ck ^ (rr & 7)) << 4) + e2) =
-                        S::from_float(e - S::to_float(hi));
+                    *reinterpret_cast<T*>(pbox + NPT * 2 * kNBlk + rr * 128 + ((ck ^ (rr & 7)) << 4) +
+                                          e2) = S::from_float(sv[r] - S::to_float(hi));
             }
             if (g == 0 && j >= N) {  // a value row past the new length: zero in the tile
                 unsigned char* vrow = stage + nkb * kBlk + t * 128;
@@ -784,7 +799,7 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
             fence_async_shared();  // P^T and the zeroed rows, for the tensor cores
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.p_ready(static_cast<int>(comp & 1)), 1u);
+            if (lane == 0) mbar_arrive(bars.p_ready(static_cast<int>(comp % NPT)), 1u);
             ++comp;
             first_tile = false;
         }
@@ -803,13 +818,13 @@ __device__ void dec_softmax(const DecParams& dp, unsigned char* smem, DecBars ba
             const uint32_t bm = rv & 1u;
             const float mine = warp_reduce_rows<NW, false>(lsum);
             if ((lane & (kGroup - 1)) == 0)
-                xval[(bm * 2 * kDN + (lane >> (5 - RowsLog2<NW>::v))) * 4 + wq] = mine;
+                xval[(bm * 2 * kX + (lane >> (5 - RowsLog2<NW>::v))) * 4 + wq] = mine;
             if (!rendezvous()) break;
 #pragma unroll
             for (int r = 0; r < NW; ++r) {
                 if (t == r && lim[r] >= s_k) {
                     const float4 q4 =
-                        *reinterpret_cast<const float4*>(xval + (bm * 2 * kDN + r) * 4);
+                        *reinterpret_cast<const float4*>(xval + (bm * 2 * kX + r) * 4);
                     p.part_ml[2 * (prow0 + r)] = mref[r];
                     p.part_ml[2 * (prow0 + r) + 1] = (q4.x + q4.y) + (q4.z + q4.w);
                 }
@@ -848,8 +863,9 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
         *abort = 0;
         fence_mbar_init();
     }
-    // P^T rows past the unit's rows stay zero: clear both buffers once
-    for (int i = threadIdx.x; i < (SRC ? 2 : 1) * 2 * 2 * kNBlk / 16; i += Roles::threads)
+    // P^T rows past the unit's rows stay zero: clear every buffer once
+    for (int i = threadIdx.x; i < (SRC ? 2 : 1) * DecPt<DN, SRC>::n * 2 * kNBlk / 16;
+         i += Roles::threads)
         reinterpret_cast<uint4*>(smem + p.dec_off_pt)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_async_shared();
     if (warp == Roles::mma) {
@@ -865,7 +881,8 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
         dec_softmax<T, NR, SG, SRC>(dp, smem, bars, abort, tmem);
     } else if (warp == Roles::mma) {
         if ((threadIdx.x & 31) == 0)
-            dec_mma_issuer<DN>(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value, SRC);
+            dec_mma_issuer<DN, DecPt<DN, SRC>::n>(dp, smem, bars, abort, tmem,
+                                                  std::is_same<T, __nv_bfloat16>::value, SRC);
     } else if (warp == Roles::prod) {
         // paged pools of blocks under 64 slots: 8 to 16 pieces of 4 copies per
         // tile, issued by the warp's lanes (in-place gqa_decode 16-slot blocks:
@@ -879,7 +896,8 @@ __global__ void __launch_bounds__(DecRoles<SG>::threads, 1)
             dec_producer<DN>(dp, smem, bars, abort);
     } else if (kPvWarp && warp == Roles::pv) {
         if ((threadIdx.x & 31) == 0)
-            dec_pv_issuer<DN>(dp, smem, bars, abort, tmem, std::is_same<T, __nv_bfloat16>::value, SRC);
+            dec_pv_issuer<DN, DecPt<DN, SRC>::n>(dp, smem, bars, abort, tmem,
+                                                 std::is_same<T, __nv_bfloat16>::value, SRC);
     }
     tc_fence_before();
     __syncthreads();  // every thread reaches this exactly once: all waits are bounded
