@@ -205,10 +205,17 @@ def measured_peak():
 
 def mode_key(args) -> str:
     """Key of a workload and step face in the traffic record, e.g.
-    "gqa_decode", "inplace:gqa_decode", "paged64:gqa_decode"."""
+    "gqa_decode", "inplace:gqa_decode", "paged64:gqa_decode", and with a
+    token or dtype override "inplace:gqa_decode:Q8" (the attention rows a
+    step writes grow with Q, so a capture holds for its own Q only)."""
     mode = ("backward" if args.backward else "readonly" if args.readonly else
             f"paged{args.paged}" if args.paged else "inplace" if args.inplace else "")
-    return f"{mode}:{args.workload}" if mode else args.workload
+    key = f"{mode}:{args.workload}" if mode else args.workload
+    if args.q is not None:
+        key += f":Q{args.q}"
+    if args.dtype is not None:
+        key += f":{args.dtype}"
+    return key
 
 
 def kernel_traffic(key: str, kernel: str, algorithmic: int):

@@ -55,6 +55,9 @@
 namespace kvc {
 namespace {
 
+#ifndef KVC_BWD_TC_STAGED_STORE
+#define KVC_BWD_TC_STAGED_STORE 1  // the epilogue's stores go through shared memory, row-contiguous
+#endif
 constexpr int kTJ = 128;                // slots per tile (M of the slot-major products)
 constexpr int kTR = 128;                // query rows of a unit, padded (N of S^T, G^T; M of dq)
 #ifndef KVC_BWD_TC_WARPS
@@ -518,7 +521,55 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_kv_tc_kernel(const __grid_c
             if (Y.u != X.u) stage_unit(Y);
             if (tid == 0) issue_tile(Y, inext);
         }
-        {  // dK' (times scale) or dV' of this thread's slot plus the returned caches' gradient
+        // dK' (times scale) or dV' of this thread's slot plus the returned caches'
+        // gradient, rounded to the dtype: through shared memory for whole tiles,
+        // one slot per thread for a unit's last, partial tile
+        if (KVC_BWD_TC_STAGED_STORE && nj == kTJ) {
+            // stored row-contiguous through the ds^T buffer (free once the products
+            // finished; the next tile's a / ds pass rewrites it after the barrier
+            // that ends this tile): a warp's store covers 8 slots x 64 bytes
+            // instead of 32 slots x 16 bytes
+            const float sc = keys ? bp.scale : 1.f;
+            T* const cache_b = static_cast<T*>(keys ? bp.d_key_cache : bp.d_value_cache);
+            T* const new_b = static_cast<T*>(keys ? bp.d_new_key : bp.d_new_value);
+            unsigned char* const sb = smem + Ly.ds + warp * 2048;  // [32 slots][64 bytes], swizzled
+            const uint32_t base = my_lanes + (keys ? 0u : colV);
+            const int wslot0 = 32 * (warp & 3) + (lane >> 2);  // this lane's first slot of pass two
+#pragma unroll
+            for (int ch = 0; ch < kMaxChunks; ++ch) {
+                if (ch >= nch) continue;  // uniform over the warp
+                const int col = (c0 + ch) * 32;
+                float v[32];
+                tmem_ld32(base + static_cast<uint32_t>(col), v);  // the whole warp
+#pragma unroll
+                for (int pc = 0; pc < 4; ++pc) {  // 16-byte piece pc of slot `lane` (every slot live)
+                    float gf[8];
+                    Storage<T>::widen16(gow[ch][pc], gf);
+                    const float* vv = v + 8 * pc;
+                    *reinterpret_cast<uint4*>(sb + lane * 64 + ((pc ^ ((lane >> 1) & 3)) << 4)) =
+                        make_uint4(pack2<T>(fmaf(vv[0], sc, gf[0]), fmaf(vv[1], sc, gf[1])),
+                                   pack2<T>(fmaf(vv[2], sc, gf[2]), fmaf(vv[3], sc, gf[3])),
+                                   pack2<T>(fmaf(vv[4], sc, gf[4]), fmaf(vv[5], sc, gf[5])),
+                                   pack2<T>(fmaf(vv[6], sc, gf[6]), fmaf(vv[7], sc, gf[7])));
+                }
+                __syncwarp();
+#pragma unroll 1
+                for (int i8 = 0; i8 < 4; ++i8) {  // slots rr = lane / 4 + 8 i8, piece lane % 4
+                    const int rr = (lane >> 2) + 8 * i8, pc = lane & 3;
+                    const int64_t jr = jb + wslot0 + 8 * i8;
+                    const uint4 val =
+                        *reinterpret_cast<const uint4*>(sb + rr * 64 + ((pc ^ ((rr >> 1) & 3)) << 4));
+                    uint4* crow = reinterpret_cast<uint4*>(cache_b + (X.u * p.M + jr) * W + col + 8 * pc);
+                    if (jr >= X.L) {  // a new row's slot: its gradient to the new row, zero here
+                        *reinterpret_cast<uint4*>(new_b + (X.u * p.Q + (jr - X.L)) * W + col + 8 * pc) = val;
+                        *crow = make_uint4(0u, 0u, 0u, 0u);
+                    } else {
+                        *crow = val;
+                    }
+                }
+                __syncwarp();  // the staging rows are rewritten by the next chunk
+            }
+        } else {
             const float sc = keys ? bp.scale : 1.f;
             T* cache_g = static_cast<T*>(keys ? bp.d_key_cache : bp.d_value_cache) + (X.u * p.M + j) * W;
             T* dst = is_new ? static_cast<T*>(keys ? bp.d_new_key : bp.d_new_value) +
