@@ -60,9 +60,11 @@ def check(q, kc, vc, cu, K, slot, k_cumulative=False, expect_flags=0, scale=None
 
 
 CASES = {
-    # (B, Hq, Hk, D, Dv, M, dtype, smax): fused path (few rows per KV head)
+    # (B, Hq, Hk, D, Dv, M, dtype, smax): few rows per KV head (the decode
+    # tensor-core kernel for 16-bit Dv = 128, the fused one otherwise)
     "decode_bf16": (12, 32, 8, 128, 128, 700, "bf16", 1),
     "specdec_bf16": (10, 32, 8, 128, 128, 900, "bf16", 4),
+    "specdec32_bf16": (5, 32, 4, 128, 128, 800, "bf16", 4),  # up to 32 rows
     "fp32_gqa": (6, 8, 2, 64, 64, 300, "f32", 5),
     # tensor-core path (G * Qmax >= 64)
     "mqa_f16_D192": (4, 16, 1, 192, 128, 1500, "f16", 8),
@@ -107,12 +109,17 @@ def test_sequences_outside_the_contract():
         assert torch.count_nonzero(out[int(cu[b]):int(cu[b + 1])]) == 0
 
 
-@pytest.mark.parametrize("spec_name", ["specdec", "mqa"])
+REATTEND = {
+    "specdec": Spec(B=6, Hq=32, Hk=8, Q=4, D=128, Dv=128, M=640, dtype="bf16", counts=("all",)),
+    "specdec24": Spec(B=4, Hq=8, Hk=1, Q=3, D=128, Dv=128, M=500, dtype="bf16", counts=("all",)),
+    "mqa": Spec(B=3, Hq=16, Hk=1, Q=8, D=192, Dv=128, M=1000, dtype="f16", counts=("all",),
+                lengths=("uniform", 300, 990)),
+}
+
+
+@pytest.mark.parametrize("spec_name", sorted(REATTEND))
 def test_reattending_the_appended_cache_reproduces_the_step(spec_name):
-    spec = (Spec(B=6, Hq=32, Hk=8, Q=4, D=128, Dv=128, M=640, dtype="bf16", counts=("all",))
-            if spec_name == "specdec" else
-            Spec(B=3, Hq=16, Hk=1, Q=8, D=192, Dv=128, M=1000, dtype="f16", counts=("all",),
-                 lengths=("uniform", 300, 990)))
+    spec = REATTEND[spec_name]
     x = workloads.generate(spec, 4).to(DEV)
     kc, vc = x.key_cache.clone(), x.value_cache.clone()
     ref = kvc.kv_cache_attention_step_inplace(x.query, x.new_key, x.new_value, kc, vc,

@@ -115,6 +115,9 @@ INPLACE = {
                                lengths=("uniform", 100, 511), hot_frac=0.05, hot_scale=50.0),
     "fused_fp32": SMALL["chunk_fp32_Q40"],
     "tensor_f16_D192": STEP["tensor_f16_D192"],
+    # 24 rows per KV head: the decode kernel's 32-row instance
+    "decode_tc32_f16": Spec(B=3, Hq=8, Hk=1, Q=3, D=128, Dv=128, M=333, dtype="f16",
+                            counts=("uniform", 0, 3)),
 }
 
 
@@ -142,6 +145,7 @@ def test_inplace_writes_stay_in_bounds(name):
 
 PAGED = {
     "decode_tc_bs16": (INPLACE["decode_tc_bf16_hot"].replace(M=512), 16),
+    "decode_tc32_bs16": (INPLACE["decode_tc32_f16"].replace(M=336), 16),
     "fused_fp32_bs8": (SMALL["chunk_fp32_Q40"], 8),
     "tensor_f16_bs64": (STEP["tensor_f16_D192"].replace(M=1024), 64),
     "fused_bs40": (TC["r160_bf16_chunk40"], 40),
@@ -190,6 +194,7 @@ def test_paged_writes_stay_in_bounds(name):
 READONLY = {
     # (B, Hq, Hk, D, Dv, M, dtype, smax)
     "decode_tc": (6, 16, 4, 128, 128, 700, "bf16", 4),
+    "decode_tc32": (4, 32, 4, 128, 128, 500, "bf16", 4),
     "fused_fp32": (5, 8, 2, 64, 64, 300, "f32", 5),
     "tensor": (3, 16, 1, 192, 128, 900, "f16", 8),
 }
@@ -221,6 +226,9 @@ BACKWARD = {
     "tiled_fp32": SMALL["chunk_fp32_Q40"],
     "tc_f16_D192": SMALL["mqa_fp16_D192"].replace(M=700, lengths=("uniform", 100, 690)),
     "generic_bf16": STEP["generic_D5_Dv7"],
+    # statistics on the decode kernel's 32-row instance, slots on the tensor-core kernel
+    "dec32_tc_bf16": Spec(B=3, Hq=8, Hk=1, Q=3, D=128, Dv=128, M=300, dtype="bf16",
+                          lengths=("uniform", 20, 290)),
 }
 
 
