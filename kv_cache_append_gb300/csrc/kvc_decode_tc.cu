@@ -54,11 +54,12 @@
 // cores, fp32) and writes the new value row into the tile before the second
 // product reads it. The gradients need the context to fp32's order (their
 // per-row sum D = dcontext . context sits under differences a (g - D)), so
-// that instance also writes P^T's low parts (P - hi, rounded) into two more
-// buffers and adds a second product V^T lo^T.
+// that instance also writes P^T's low parts (P - hi, rounded) into as many
+// more buffers and adds a second product V^T lo^T.
 //
-// Tensor memory (64 columns x 128 lanes, fp32): S^T buffers at columns 0 and
-// 16, O^T at 32 (lane = value column, column = query row).
+// Tensor memory (128 lanes, fp32; 64 columns for DN = 16, 128 for DN = 32):
+// S^T buffers at columns 0 and DN, O^T at 2 DN (lane = value column, column =
+// query row).
 #include <cuda.h>
 
 #include <type_traits>
@@ -272,7 +273,7 @@ __device__ void dec_producer(const DecParams& dp, unsigned char* smem, DecBars b
                 // the next tile's ids arrive while the producer waits for a stage
                 if (i + 1 < i1) request_ids(x, i + 1);
             }
-            // the unit's R query rows are rows [u R, u R + 16) of the [U R][D] query view
+            // the unit's R query rows are rows [u R, u R + DN) of the [U R][D] query view
             const int qy = static_cast<int>(u * p.R);
             for (int b = 0; b < nkb; ++b) tma_load_3d(sQ + b * kNBlk, &dp.tm_q, 64 * b, qy, 0, full);
             ++issued;

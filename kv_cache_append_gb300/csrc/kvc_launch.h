@@ -36,7 +36,7 @@ cudaError_t launch_fused_tc(const TcParams& tp, int dtype, size_t smem, cudaStre
 
 // Kernel parameters of the decode tensor-core kernel: the caches (or pools)
 // as TMA tensor maps (boxes of 64 elements x min(64, block) slots, 128-byte
-// swizzle), the query as [U * R][D] rows (boxes of 64 elements x 16 rows), and
+// swizzle), the query as [U * R][D] rows (boxes of 64 elements x 16 or 32 rows), and
 // the common parameters.
 struct DecParams {
     CUtensorMap tm_k;
