@@ -181,6 +181,10 @@ CASES = {
                                    lengths=("uniform", 0, 690), counts=("uniform", 0, 4)),
     "tc_walk_f16_R64_D128": Spec(B=40, Hq=16, Hk=1, Q=4, D=128, Dv=128, M=1100, dtype="f16",
                                  lengths=("uniform", 300, 1090)),
+    # new rows at slots 126-129: two in the first, whole tile (whose cache
+    # gradient goes out through shared memory), two in the second, partial one
+    "tc_bf16_R32_new_rows_in_whole_tile": Spec(B=2, Hq=16, Hk=2, Q=4, D=128, Dv=128, M=300,
+                                               dtype="bf16", lengths=("uniform", 126, 126)),
     # statistics on the decode tensor-core kernel (16-bit, Dv = 128, at most 32
     # rows), which takes the appended rows from new_key / new_value: 16 rows
     # whose new rows straddle the first 128-slot tile's end, D = 256 (8 rows)
@@ -212,12 +216,14 @@ SLOT = {"tiny_fp32": "bwd_kv_kernel", "decode_bf16_ragged_M": "bwd_kv_rows_kerne
         "tc_f16_D128_R32_staged": "bwd_kv_tc_kernel",
         "dec_bf16_R16_tile_edge": "bwd_kv_tc_kernel", "dec_f16_D256_R8": "bwd_kv_tiled_kernel",
         "dec_bf16_D64_R4": "bwd_kv_kernel", "tc_walk_bf16_R32_units": "bwd_kv_tc_kernel",
-        "tc_walk_f16_R64_D128": "bwd_kv_tc_kernel"}
+        "tc_walk_f16_R64_D128": "bwd_kv_tc_kernel",
+        "tc_bf16_R32_new_rows_in_whole_tile": "bwd_kv_tc_kernel"}
 
 # the cases whose statistics pass runs the decode tensor-core kernel
 DECODE_STATS = ("decode_bf16_ragged_M", "specdec_bf16_hot", "tiled_f16_D64_Dv128_R8",
                 "dec_bf16_R16_tile_edge", "dec_f16_D256_R8", "dec_bf16_D64_R4",
-                "tc_f16_D128_R17", "tc_bf16_D128_R32_hot", "tc_f16_D128_R32_staged")
+                "tc_f16_D128_R17", "tc_bf16_D128_R32_hot", "tc_f16_D128_R32_staged",
+                "tc_bf16_R32_new_rows_in_whole_tile")
 
 
 def plan_of(spec):
