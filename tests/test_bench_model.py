@@ -108,3 +108,26 @@ def test_backward_bytes_split_at_the_new_length(i):
     model = bench.algorithmic_bytes_backward(spec, x.lengths.tolist(), n)
     assert model["bwd_copy_kernel"] == tail
     assert model["bwd_kv_kernel"] == below + allowed * es + qrows * (spec.D + spec.Dv) * es
+
+
+def test_traffic_keys_separate_token_and_dtype_overrides():
+    """A kernel's DRAM traffic is recorded per workload face; the attention rows
+    a step writes grow with Q, so a capture taken at the workload's own Q must
+    not be scaled onto a run with another Q (or dtype)."""
+    import argparse
+
+    def args(**kw):
+        base = dict(backward=False, readonly=False, paged=None, inplace=False,
+                    workload="gqa_decode", q=None, dtype=None)
+        base.update(kw)
+        return argparse.Namespace(**base)
+
+    assert bench.mode_key(args()) == "gqa_decode"
+    assert bench.mode_key(args(inplace=True)) == "inplace:gqa_decode"
+    assert bench.mode_key(args(paged=16)) == "paged16:gqa_decode"
+    assert bench.mode_key(args(inplace=True, q=8)) == "inplace:gqa_decode:Q8"
+    assert bench.mode_key(args(workload="chunked_append", dtype="f32")) == "chunked_append:f32"
+    keys = {bench.mode_key(args(**kw)) for kw in
+            ({}, {"q": 8}, {"dtype": "f16"}, {"inplace": True}, {"inplace": True, "q": 8},
+             {"readonly": True}, {"backward": True}, {"paged": 64})}
+    assert len(keys) == 8
